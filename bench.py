@@ -1,0 +1,488 @@
+"""Benchmark of the GB300 gated delta-rule block (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload batched_decode_64|single_seq_decode_1000|
+                                serving_pool_256_of_512|prefill_scan_4x4096]
+
+Default workload: batched decode, 64 independent sequences, one token each per
+step (Hk=16, H=32, S=128, conv 4), through the fused gdn_block_decode kernel.
+A step is one fused launch over the 64 sequences; the state (128 MiB) is carried
+from step to step. L2 is flushed (a 256 MiB write) before every timed step, and
+each step is timed with CUDA events on the launching stream.
+
+With N > 1 (torchrun, one process per GPU) every rank serves its own 64
+sequences (weak scaling, no collective on the data path); rank 0 prints the
+line, timed as the max over ranks.
+
+--impl reference times the CPU oracle (the plain C reference, float build,
+single-threaded) on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_deltanet_linear_scan_gb300 import inputs as I  # noqa: E402
+
+METRIC = "GDN decode tokens/s and state HBM GB/s (fraction of GB300 peak), 1 GPU"
+WORKLOADS = {"batched_decode_64": 3, "single_seq_decode_1000": 1,
+             "serving_pool_256_of_512": 4, "prefill_scan_4x4096": 2}
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ small helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for rel in files:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "block_decode_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_block.cu",
+                            "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh"],
+    "recurrence_scan_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_recurrence.cu",
+                               "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh"],
+}
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if the kernel's source is unchanged since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_s = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    if not (m_b and m_s) or m_s.group(1) != source_sha(KERNEL_SOURCES[kernel]):
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ the workload
+
+def algorithmic_bytes_block(cfg, n):
+    """Bytes a fused block decode launch over n sequences must move at minimum."""
+    H, S, C, K = cfg.n_v_heads, cfg.state_size, cfg.conv_dim, cfg.conv_kernel
+    state = 2 * n * H * S * S * 4
+    other = (2 * n * C * (K - 1) * 4      # conv_state read + write
+             + n * C * 4                  # qkv
+             + 2 * n * H * S * 4          # z in, out
+             + 2 * n * H * 4              # alpha, b
+             + C * K * 4 + S * 4 + 2 * H * 4)  # conv weight, norm weight, dt, a
+    return state, state + other
+
+
+def cpu_sample_block(cfg, seqs, max_steps, budget_s):
+    """Time the oracle (float build) on `seqs` sequences of the workload for up to
+    max_steps steps or budget_s seconds. Returns (tokens/s, steps, seconds)."""
+    import oracle
+    st = I.block_static(cfg)
+    state = I.state_pool(cfg, which=[int(s) for s in seqs]).astype(np.float32)
+    conv = I.conv_state_pool(cfg, which=[int(s) for s in seqs]).astype(np.float32)
+    steps_in = [I.block_step(cfg, s, seqs=seqs) for s in range(min(max_steps, 8))]
+    oracle.sigmoid(np.zeros(1, np.float32), "f32")  # load the library outside the timing
+    t0 = time.perf_counter()
+    done = 0
+    while done < max_steps:
+        a = steps_in[done % len(steps_in)]
+        oracle.block_decode(a["qkv"], st["conv_w"], conv, a["alpha"], a["b"], st["dt"], st["a"],
+                            a["z"], st["norm_w"], state, cfg.n_k_heads, cfg.scale, cfg.eps,
+                            cfg.eps, prec="f32")
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return len(seqs) * done / dt, done, dt
+
+
+def cpu_sample_scan(cfg, tokens, budget_s):
+    """Time the oracle scan on one (sequence, v-head) unit for `tokens` tokens and
+    scale to all units: returns tokens/s of the whole workload on one core."""
+    import oracle
+    x = I.recurrence_seq(cfg, 0, n_tokens=tokens)
+    st = I.state_slot(cfg, 0)[:1][None].astype(np.float32)
+    unit = {"q": x["q"][None, :, :1], "k": x["k"][None, :, :1], "v": x["v"][None, :, :1],
+            "g": x["g"][None, :, :1], "beta": x["beta"][None, :, :1]}
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.recurrence(st, scale=cfg.scale, prec="f32", **unit)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    units = cfg.n_seqs * cfg.n_v_heads
+    # tokens of the full workload per second = tokens per unit-second / units
+    return reps * tokens / dt / units, reps, dt
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return 0
+    if cfg.cid == 2:
+        tokens = 256
+        vals = []
+        t_all = time.perf_counter()
+        for _ in range(args.warmup):
+            cpu_sample_scan(cfg, tokens, 0.0)
+        for _ in range(args.steps):
+            v, _, _ = cpu_sample_scan(cfg, tokens, 0.0)
+            vals.append(v)
+        value = statistics.mean(vals)
+        sample = (f"one (sequence, v-head) unit of the 4x4096 scan, {tokens} tokens per step, "
+                  "scaled to the 128 units")
+        ms = 1e3 * cfg.n_seqs * cfg.n_tokens / value
+        unit = "tokens/s"
+    else:
+        seqs = list(range(min(4, cfg.n_seqs)))
+        cpu_sample_block(cfg, seqs, args.warmup, 1e9)
+        t0 = time.perf_counter()
+        value, done, dt = cpu_sample_block(cfg, seqs, args.steps, 1e9)
+        sample = (f"{len(seqs)} of {cfg.n_seqs} sequences per step, {done} chained steps of the "
+                  "fused block")
+        ms = 1e3 * dt / done
+        unit = "tokens/s"
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "impl": "reference", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "oracle": "plain C, float build, 1 thread"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+    import gated_deltanet_linear_scan_gb300 as gdn
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    gdn.build_if_needed()
+    torch.cuda.set_device(local_rank)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    pk, pk_kind = peaks()
+    N = cfg.n_seqs
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    if cfg.cid == 2:
+        return run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
+
+    # This rank's sequences (its own seeded streams) and pool slots.
+    base = rank * N
+    seqs = list(range(base, base + N))
+    slots = I.slots(cfg)
+    pool = cfg.pool_size
+    st = I.block_static(cfg)
+    d_st = {k: dev(v) for k, v in st.items()}
+    state = dev(I.state_pool(cfg, which=range(rank * pool, (rank + 1) * pool)))
+    conv = dev(I.conv_state_pool(cfg, which=range(rank * pool, (rank + 1) * pool)))
+    d_slots = dev(slots) if slots is not None else None
+    n_distinct = 8
+    steps_in = [I.block_step(cfg, s, seqs=seqs) for s in range(n_distinct)]
+    d_steps = [{k: dev(v) for k, v in a.items()} for a in steps_in]
+    H, S = cfg.n_v_heads, cfg.state_size
+    out = torch.empty(N, H, S, device="cuda")
+
+    def launch(a, o):
+        gdn.gdn_block_decode(a["qkv"], d_st["conv_w"], conv, a["alpha"], a["b"], d_st["dt"],
+                             d_st["a"], a["z"], d_st["norm_w"], state, o, N, cfg.n_k_heads, H, S,
+                             cfg.conv_kernel, cfg.scale, cfg.eps, cfg.eps, slots=d_slots,
+                             pool=pool)
+
+    for w in range(args.warmup):
+        flush()
+        launch(d_steps[w % n_distinct], out)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_wall = time.perf_counter()
+    with ClockSampler(local_rank) as clocks:
+        for i in range(args.steps):
+            flush()
+            ev[i][0].record(stream)
+            launch(d_steps[i % n_distinct], out)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    gdn.gdn_device_error()
+    kernel_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    total_s = sum(kernel_ms) / 1e3
+    if dist:
+        t = torch.tensor([total_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    tokens = world * N * args.steps
+    value = tokens / total_s
+    per_launch_s = total_s / args.steps
+    state_b, alg_b = algorithmic_bytes_block(cfg, N)
+    achieved = alg_b / per_launch_s / 1e9
+
+    # ---- end to end: pinned host inputs -> device, the C-ABI call, output -> host
+    h_steps = [{k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in a.items()}
+               for a in steps_in]
+    h_out = torch.empty(N, H, S).pin_memory()
+    d_in = {k: torch.empty_like(v, device="cuda") for k, v in d_steps[0].items()}
+    h2d = sum(v.numel() * 4 for v in h_steps[0].values())
+    d2h = h_out.numel() * 4
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush()
+        e2e_ev[i][0].record(stream)
+        for k, v in h_steps[i % n_distinct].items():
+            d_in[k].copy_(v, non_blocking=True)
+        launch(d_in, out)
+        h_out.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_s = sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1:
+        sample_seqs = list(range(min(4, N)))
+        v_cpu, done, dt = cpu_sample_block(cfg, sample_seqs, 10 ** 6, args.cpu_budget)
+        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(sample_seqs)} of {N} sequences, {done} chained steps of the block "
+                         f"({dt:.1f} s), plain C float build, 1 thread"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded PCG64; N(0,1) qkv/z, state N(0,0.1^2), g~U(-2,-0.01))",
+        "config": {"workload": args.workload, "n_seqs_per_gpu": N, "n_k_heads": cfg.n_k_heads,
+                   "n_v_heads": H, "state_size": S, "conv_kernel": cfg.conv_kernel,
+                   "pool_slots": pool, "kernel": "gdn_block_decode (fused, 1 launch/step)",
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "state_gbs": state_b / per_launch_s / 1e9,
+                   "state_frac_of_peak": state_b / per_launch_s / 1e9 / pk["hbm_gbs"],
+                   "wall_s_timed_loop": t_wall},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"],
+                     "traffic": ncu_traffic("block_decode_kernel", args.workload),
+                     "algorithmic_bytes_per_launch": alg_b,
+                     "peak_source": f"hbm_gbs ({pk_kind})"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
+    import torch
+    import gated_deltanet_linear_scan_gb300 as gdn
+    stream = torch.cuda.current_stream()
+    N, T, H, Hk, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.n_k_heads, cfg.state_size
+    seqs = list(range(rank * N, (rank + 1) * N))
+    x = I.recurrence_batch(cfg, seqs=seqs)
+    d = {k: dev(v) for k, v in x.items()}
+    state0 = dev(I.state_pool(cfg, which=seqs))
+    state = state0.clone()
+    y = torch.empty(N, T, H, S, device="cuda")
+
+    def launch():
+        gdn.gdn_recurrence_scan(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y, N, T, Hk, H,
+                                S, cfg.scale)
+
+    for _ in range(args.warmup):
+        state.copy_(state0)
+        flush()
+        launch()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        for i in range(args.steps):
+            state.copy_(state0)
+            flush()
+            ev[i][0].record(stream)
+            launch()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    gdn.gdn_device_error()
+    total_s = sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
+    if dist:
+        t = torch.tensor([total_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    per = total_s / args.steps
+    tokens = world * N * T * args.steps
+    flops = 7.0 * N * T * H * S * S
+    props = torch.cuda.get_device_properties(0)
+    clk = clocks.summary()
+    mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
+    fp32_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+    achieved = flops / per / 1e12
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1:
+        v_cpu, reps, dt = cpu_sample_scan(cfg, 256, args.cpu_budget)
+        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"one (sequence, v-head) unit, 256 tokens x {reps} reps ({dt:.1f} s), "
+                         "scaled to the 128 units; plain C float build, 1 thread"}
+    line = {
+        "metric": METRIC, "value": tokens / total_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded PCG64; unit q/k, g~U(-0.5,-0.001))",
+        "config": {"workload": args.workload, "n_seqs": N, "n_tokens": T, "n_k_heads": Hk,
+                   "n_v_heads": H, "state_size": S, "kernel": "gdn_recurrence_scan",
+                   "l2": "flushed (256 MiB write) before every timed step"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp32_peak,
+                     "traffic": ncu_traffic("recurrence_scan_kernel", args.workload),
+                     "peak_source": "FP32 FMA pipes: SMs x 128 lanes x 2 flop x median SM clock"},
+        "cpu_baseline": cpu,
+        "e2e": None,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="batched_decode_64")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for the cpu_baseline sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = I.get_config(WORKLOADS[args.workload])
+    if args.impl == "reference":
+        return run_reference(args, cfg, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        return run_ours(args, cfg, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,214 @@
+"""Python binding of the GB300 gated delta-rule SSM library (libgdn.so).
+
+Argument marshalling only: every function passes tensor data pointers, sizes and
+the current CUDA stream to the C ABI of include/gdn.h, checks the returned
+status and raises GdnError on failure. All arithmetic runs in the library's
+sm_103a kernels; there is no fallback. If libgdn.so has not been built, the
+first call raises (``build_if_needed()`` builds it with nvcc).
+
+Tensors are torch CUDA tensors (float32, or int32 for slot ids), contiguous,
+with the layouts documented in include/gdn.h.
+"""
+import ctypes
+import os
+
+from . import _build
+
+__all__ = [
+    "GdnError", "build_if_needed", "library", "lib_path",
+    "gdn_status_str", "gdn_version", "gdn_device_error",
+    "gdn_decay_gate", "gdn_beta_sigmoid", "gdn_conv1d_silu", "gdn_conv1d_silu_seq",
+    "gdn_qkv_split_norm", "gdn_recurrence_decode", "gdn_recurrence_scan", "gdn_gated_norm",
+    "gdn_block_decode",
+]
+
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
+          4: "GDN_ERR_ALIGN", 5: "GDN_ERR_LAUNCH", 6: "GDN_ERR_DEVICE"}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+_LIB = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+_SIGS = {
+    "gdn_status_str": ([_I], ctypes.c_char_p),
+    "gdn_version": ([], _I),
+    "gdn_device_error": ([_P], _I),
+    "gdn_decay_gate": ([_P, _P, _P, _P, _I, _I, _P], _I),
+    "gdn_beta_sigmoid": ([_P, _P, _I, _P], _I),
+    "gdn_conv1d_silu": ([_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P], _I),
+    "gdn_conv1d_silu_seq": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P], _I),
+    "gdn_qkv_split_norm": ([_P, _P, _P, _P, _I, _I, _I, _I, _F, _P], _I),
+    "gdn_recurrence_decode": ([_P] * 7 + [_I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
+    "gdn_recurrence_scan": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
+    "gdn_gated_norm": ([_P, _P, _P, _P, _I, _I, _F, _P], _I),
+    "gdn_block_decode": ([_P] * 11 + [_I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P, _P], _I),
+}
+
+
+def lib_path():
+    return _build.LIB
+
+
+def build_if_needed(force=False):
+    """Compile libgdn.so for sm_103a if it is missing or older than its sources."""
+    return _build.build(force=force)
+
+
+def library():
+    """The loaded libgdn.so (ctypes.CDLL). Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"libgdn.so is not built ({_build.LIB}); run "
+                               "gated_deltanet_linear_scan_gb300.build_if_needed()")
+        lib = ctypes.CDLL(_build.LIB)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = lib
+    return _LIB
+
+
+# ------------------------------------------------------------------ marshalling helpers
+
+def _stream(stream):
+    if stream is not None:
+        return int(stream)
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t, name, dtype=None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    want = dtype or torch.float32
+    if t.dtype != want:
+        raise TypeError(f"{name} must be {want}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _slots(slots):
+    import torch
+    return _ptr(slots, "slots", torch.int32, optional=True)
+
+
+def _errc(err_count):
+    import torch
+    return _ptr(err_count, "err_count", torch.int32, optional=True)
+
+
+def _pool(pool, n_seqs, slots):
+    if pool is not None:
+        return int(pool)
+    if slots is not None:
+        raise ValueError("pool (the number of slots the state buffers hold) is required with slots")
+    return max(1, int(n_seqs))
+
+
+def _check(fn, status):
+    if status != 0:
+        raise GdnError(fn, status)
+
+
+# ------------------------------------------------------------------ the C ABI
+
+def gdn_status_str(status):
+    return library().gdn_status_str(int(status)).decode()
+
+
+def gdn_version():
+    return library().gdn_version()
+
+
+def gdn_device_error(stream=None):
+    """Synchronise the stream; raise GdnError if a kernel's bounded wait gave up."""
+    _check("gdn_device_error", library().gdn_device_error(_stream(stream)))
+
+
+def gdn_decay_gate(alpha, dt, a, g, n_heads, rows, stream=None):
+    _check("gdn_decay_gate", library().gdn_decay_gate(
+        _ptr(alpha, "alpha"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(g, "g"), n_heads, rows,
+        _stream(stream)))
+
+
+def gdn_beta_sigmoid(b, beta, n, stream=None):
+    _check("gdn_beta_sigmoid", library().gdn_beta_sigmoid(_ptr(b, "b"), _ptr(beta, "beta"), n,
+                                                         _stream(stream)))
+
+
+def gdn_conv1d_silu(qkv, w, conv_state, out, n_seqs, conv_dim, conv_kernel, slots=None,
+                    pool=None, err_count=None, stream=None):
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_conv1d_silu", library().gdn_conv1d_silu(
+        _ptr(qkv, "qkv"), _ptr(w, "w"), _ptr(conv_state, "conv_state"), _ptr(out, "out"),
+        n_seqs, conv_dim, conv_kernel, _slots(slots), pool, _errc(err_count), _stream(stream)))
+
+
+def gdn_conv1d_silu_seq(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, conv_kernel,
+                        slots=None, pool=None, err_count=None, stream=None):
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_conv1d_silu_seq", library().gdn_conv1d_silu_seq(
+        _ptr(qkv, "qkv"), _ptr(w, "w"), _ptr(conv_state, "conv_state"), _ptr(out, "out"),
+        n_seqs, n_tokens, conv_dim, conv_kernel, _slots(slots), pool, _errc(err_count),
+        _stream(stream)))
+
+
+def gdn_qkv_split_norm(conv_out, q, k, v, rows, n_k_heads, n_v_heads, state_size, eps,
+                       stream=None):
+    _check("gdn_qkv_split_norm", library().gdn_qkv_split_norm(
+        _ptr(conv_out, "conv_out"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), rows, n_k_heads,
+        n_v_heads, state_size, eps, _stream(stream)))
+
+
+def gdn_recurrence_decode(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, state_size,
+                          scale, slots=None, pool=None, err_count=None, stream=None):
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_recurrence_decode", library().gdn_recurrence_decode(
+        _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
+        _ptr(beta, "beta"), _ptr(y, "y"), n_seqs, n_k_heads, n_v_heads, state_size, scale,
+        _slots(slots), pool, _errc(err_count), _stream(stream)))
+
+
+def gdn_recurrence_scan(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
+                        state_size, scale, slots=None, pool=None, err_count=None, stream=None):
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_recurrence_scan", library().gdn_recurrence_scan(
+        _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
+        _ptr(beta, "beta"), _ptr(y, "y"), n_seqs, n_tokens, n_k_heads, n_v_heads, state_size,
+        scale, _slots(slots), pool, _errc(err_count), _stream(stream)))
+
+
+def gdn_gated_norm(y, w, z, out, rows, head_dim, eps, stream=None):
+    _check("gdn_gated_norm", library().gdn_gated_norm(
+        _ptr(y, "y"), _ptr(w, "w"), _ptr(z, "z"), _ptr(out, "out"), rows, head_dim, eps,
+        _stream(stream)))
+
+
+def gdn_block_decode(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                     n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps, norm_eps,
+                     slots=None, pool=None, err_count=None, stream=None):
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_block_decode", library().gdn_block_decode(
+        _ptr(qkv, "qkv"), _ptr(conv_w, "conv_w"), _ptr(conv_state, "conv_state"),
+        _ptr(alpha, "alpha"), _ptr(b, "b"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(z, "z"),
+        _ptr(norm_w, "norm_w"), _ptr(state, "state"), _ptr(out, "out"), n_seqs, n_k_heads,
+        n_v_heads, state_size, conv_kernel, scale, l2_eps, norm_eps, _slots(slots), pool,
+        _errc(err_count), _stream(stream)))

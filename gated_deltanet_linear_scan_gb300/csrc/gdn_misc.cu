@@ -1,0 +1,273 @@
+// gdn_misc.cu -- the small per-token steps of the block as standalone kernels:
+// decay gate, beta sigmoid, causal conv1d + SiLU (single token and scan), q/k
+// split + L2-norm, gated RMSNorm; plus the status helpers of the C ABI.
+//
+// These steps move a few bytes per channel and are HBM/latency bound; they use
+// one thread per element (conv: per channel, history in registers across tokens)
+// or one warp per head vector with a shuffle reduction.
+#include <cstdio>
+
+#include "gdn_device.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+
+// fm_kernel_ssm.m, "Decay gate"; ssm_gated_delta.cu, fc_ssm_decay_gate_nx: one
+// thread per (row, head).
+__global__ void __launch_bounds__(kThreads) decay_gate_kernel(const float *__restrict__ alpha,
+                                                               const float *__restrict__ dt,
+                                                               const float *__restrict__ a,
+                                                               float *g, int n_heads,
+                                                               long long total) {
+    const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (idx >= total) return;
+    const int h = static_cast<int>(idx % n_heads);
+    g[idx] = a[h] * softplus_guarded(alpha[idx] + dt[h]);
+}
+
+// ssm_gated_delta.cu, fc_sigmoid.
+__global__ void __launch_bounds__(kThreads) sigmoid_kernel(const float *__restrict__ b,
+                                                            float *beta, long long n) {
+    const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (i < n) beta[i] = 1.0f / (1.0f + expf(-b[i]));
+}
+
+// Causal depthwise conv1d + SiLU over n_tokens positions, fm_kernel_ssm.m "Causal
+// depthwise conv1d + SiLU" and its scan form. One thread per (sequence, channel);
+// the K-1 taps of history live in registers for the whole scan and are written
+// back once. The accumulation is the current tap first, then the history
+// oldest-first; a single-token call is the n_tokens == 1 case of the same code, so
+// a scan and n single-token calls agree bit for bit.
+template <int K>
+__global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
+    const float *__restrict__ qkv, const float *__restrict__ w, float *conv_state,
+    float *__restrict__ out, int n_tokens, int conv_dim, const int32_t *__restrict__ slots,
+    int pool, int32_t *err_count) {
+    constexpr int TAPS = K - 1;
+    const int n = blockIdx.y;
+    const int c = blockIdx.x * kThreads + threadIdx.x;
+    const int slot = slots ? slots[n] : n;
+    if (slot < 0 || slot >= pool) {
+        if (err_count && blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(err_count, 1);
+        return;
+    }
+    if (c >= conv_dim) return;
+    float wc[K];
+#pragma unroll
+    for (int t = 0; t < K; ++t) wc[t] = w[static_cast<size_t>(c) * K + t];
+    float *hs = conv_state + (static_cast<size_t>(slot) * conv_dim + c) * TAPS;
+    float hist[TAPS];
+#pragma unroll
+    for (int t = 0; t < TAPS; ++t) hist[t] = hs[t];
+    const float *x_ptr = qkv + static_cast<size_t>(n) * n_tokens * conv_dim + c;
+    float *o_ptr = out + static_cast<size_t>(n) * n_tokens * conv_dim + c;
+    for (int p = 0; p < n_tokens; ++p) {
+        const float x = x_ptr[static_cast<size_t>(p) * conv_dim];
+        float pre = __fmul_rn(x, wc[K - 1]);
+#pragma unroll
+        for (int t = 0; t < TAPS; ++t) pre = __fmaf_rn(hist[t], wc[t], pre);
+        o_ptr[static_cast<size_t>(p) * conv_dim] = silu(pre);
+#pragma unroll
+        for (int t = 0; t + 1 < TAPS; ++t) hist[t] = hist[t + 1];
+        hist[TAPS - 1] = x;
+    }
+#pragma unroll
+    for (int t = 0; t < TAPS; ++t) hs[t] = hist[t];
+}
+
+// q/k split + L2-norm (ssm_gated_delta.cu, fc_ssm_qknorm_gqa_nx, without the GQA
+// copies): one CTA per row, one warp per head vector, lane L holding elements
+// [E*L, E*L+E); v is copied through.
+template <int E>
+__global__ void __launch_bounds__(kThreads) qkv_split_norm_kernel(
+    const float *__restrict__ conv_out, float *__restrict__ q, float *__restrict__ k,
+    float *__restrict__ v, int n_k_heads, int n_v_heads, float eps) {
+    constexpr int S = 32 * E;
+    const int row = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int key_dim = n_k_heads * S;
+    const size_t conv_dim = static_cast<size_t>(2 * key_dim + n_v_heads * S);
+    const float *src = conv_out + row * conv_dim;
+    for (int hv = warp; hv < 2 * n_k_heads; hv += kThreads / 32) {
+        float x[E];
+        load_vec<E>(x, src + static_cast<size_t>(hv) * S + lane * E);
+        float ss = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) ss = __fmaf_rn(x[e], x[e], ss);
+        ss = warp_allsum(ss);
+        const float inv = 1.0f / fmaxf(sqrtf(ss), eps);
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[e] *= inv;
+        float *dst = (hv < n_k_heads ? q : k) +
+                     (static_cast<size_t>(row) * n_k_heads + (hv % n_k_heads)) * S + lane * E;
+        store_vec<E>(dst, x);
+    }
+    const float4 *vs = reinterpret_cast<const float4 *>(src + 2 * key_dim);
+    float4 *vd = reinterpret_cast<float4 *>(v + static_cast<size_t>(row) * n_v_heads * S);
+    for (int i = threadIdx.x; i < n_v_heads * S / 4; i += kThreads) vd[i] = vs[i];
+}
+
+// Gated RMSNorm, fm_kernel_ssm.m "Gated RMSNorm" and ssm_gated_delta.cu Kernel 3:
+// one warp per head row, one shuffle reduction, weight shared across heads.
+template <int E>
+__global__ void __launch_bounds__(kThreads) gated_norm_kernel(const float *y,
+                                                               const float *__restrict__ w,
+                                                               const float *__restrict__ z,
+                                                               float *out, long long rows,
+                                                               float eps) {
+    constexpr int D = 32 * E;
+    const long long row = blockIdx.x * static_cast<long long>(kThreads / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    float yv[E], zv[E], wv[E];
+    load_vec<E>(yv, y + row * D + lane * E);
+    load_vec<E>(zv, z + row * D + lane * E);
+    load_vec<E>(wv, w + lane * E);
+    float ss = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = __fmaf_rn(yv[e], yv[e], ss);
+    ss = warp_allsum(ss);
+    const float inv_rms = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
+    float o[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = yv[e] * inv_rms * wv[e] * silu(zv[e]);
+    store_vec<E>(out + row * D + lane * E, o);
+}
+
+template <int K>
+gdn_status launch_conv(const float *qkv, const float *w, float *conv_state, float *out,
+                       int n_seqs, int n_tokens, int conv_dim, const int32_t *slots, int pool,
+                       int32_t *err_count, cudaStream_t s) {
+    const dim3 grid((conv_dim + kThreads - 1) / kThreads, n_seqs);
+    conv1d_silu_kernel<K><<<grid, kThreads, 0, s>>>(qkv, w, conv_state, out, n_tokens, conv_dim,
+                                                    slots, pool, err_count);
+    return launch_status();
+}
+
+gdn_status conv_common(const float *qkv, const float *w, float *conv_state, float *out,
+                       int n_seqs, int n_tokens, int conv_dim, int conv_kernel,
+                       const int32_t *slots, int pool, int32_t *err_count, gdn_stream_t stream) {
+    if (!qkv || !w || !conv_state || !out) return GDN_ERR_NULL;
+    if (n_seqs < 0 || n_tokens < 0 || conv_dim < 1) return GDN_ERR_SHAPE;
+    if (conv_kernel < 2 || conv_kernel > 8) return GDN_ERR_SHAPE;
+    GDN_TRY(check_pool(n_seqs, slots, pool));
+    if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
+    if (n_seqs > 65535) return GDN_ERR_UNSUPPORTED;
+    const cudaStream_t s = as_cuda(stream);
+    switch (conv_kernel) {
+        case 2: return launch_conv<2>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
+        case 3: return launch_conv<3>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
+        case 4: return launch_conv<4>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
+        case 5: return launch_conv<5>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
+        case 6: return launch_conv<6>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
+        case 7: return launch_conv<7>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
+        default: return launch_conv<8>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
+    }
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+const char *gdn_status_str(gdn_status status) {
+    switch (status) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_NULL: return "GDN_ERR_NULL";
+        case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+        case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN";
+        case GDN_ERR_LAUNCH: return "GDN_ERR_LAUNCH";
+        case GDN_ERR_DEVICE: return "GDN_ERR_DEVICE";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+int gdn_version(void) { return (1 << 16) | 0; }
+
+gdn_status gdn_device_error(gdn_stream_t stream) {
+    const cudaStream_t s = as_cuda(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_LAUNCH;
+    unsigned flags = read_and_clear_watchdog_recurrence(s) | read_and_clear_watchdog_block(s);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_LAUNCH;
+    return flags ? GDN_ERR_DEVICE : GDN_OK;
+}
+
+gdn_status gdn_decay_gate(const float *alpha, const float *dt, const float *a, float *g,
+                          int n_heads, int rows, gdn_stream_t stream) {
+    if (!alpha || !dt || !a || !g) return GDN_ERR_NULL;
+    if (n_heads < 1 || rows < 0) return GDN_ERR_SHAPE;
+    if (rows == 0) return GDN_OK;
+    const long long total = static_cast<long long>(rows) * n_heads;
+    const unsigned blocks = static_cast<unsigned>((total + kThreads - 1) / kThreads);
+    decay_gate_kernel<<<blocks, kThreads, 0, as_cuda(stream)>>>(alpha, dt, a, g, n_heads, total);
+    return launch_status();
+}
+
+gdn_status gdn_beta_sigmoid(const float *b, float *beta, int n, gdn_stream_t stream) {
+    if (!b || !beta) return GDN_ERR_NULL;
+    if (n < 0) return GDN_ERR_SHAPE;
+    if (n == 0) return GDN_OK;
+    sigmoid_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, as_cuda(stream)>>>(b, beta, n);
+    return launch_status();
+}
+
+gdn_status gdn_conv1d_silu(const float *qkv, const float *w, float *conv_state, float *out,
+                           int n_seqs, int conv_dim, int conv_kernel, const int32_t *slots,
+                           int pool, int32_t *err_count, gdn_stream_t stream) {
+    return conv_common(qkv, w, conv_state, out, n_seqs, 1, conv_dim, conv_kernel, slots, pool,
+                       err_count, stream);
+}
+
+gdn_status gdn_conv1d_silu_seq(const float *qkv, const float *w, float *conv_state, float *out,
+                               int n_seqs, int n_tokens, int conv_dim, int conv_kernel,
+                               const int32_t *slots, int pool, int32_t *err_count,
+                               gdn_stream_t stream) {
+    return conv_common(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, conv_kernel, slots,
+                       pool, err_count, stream);
+}
+
+gdn_status gdn_qkv_split_norm(const float *conv_out, float *q, float *k, float *v, int rows,
+                              int n_k_heads, int n_v_heads, int state_size, float eps,
+                              gdn_stream_t stream) {
+    if (!conv_out || !q || !k || !v) return GDN_ERR_NULL;
+    if (rows < 0) return GDN_ERR_SHAPE;
+    GDN_TRY(check_heads(n_k_heads, n_v_heads, state_size));
+    if (!aligned16(conv_out) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_ERR_ALIGN;
+    if (rows == 0) return GDN_OK;
+    const cudaStream_t s = as_cuda(stream);
+    switch (state_size) {
+        case 32: qkv_split_norm_kernel<1><<<rows, kThreads, 0, s>>>(conv_out, q, k, v, n_k_heads, n_v_heads, eps); break;
+        case 64: qkv_split_norm_kernel<2><<<rows, kThreads, 0, s>>>(conv_out, q, k, v, n_k_heads, n_v_heads, eps); break;
+        case 128: qkv_split_norm_kernel<4><<<rows, kThreads, 0, s>>>(conv_out, q, k, v, n_k_heads, n_v_heads, eps); break;
+        default: qkv_split_norm_kernel<8><<<rows, kThreads, 0, s>>>(conv_out, q, k, v, n_k_heads, n_v_heads, eps); break;
+    }
+    return launch_status();
+}
+
+gdn_status gdn_gated_norm(const float *y, const float *w, const float *z, float *out, int rows,
+                          int head_dim, float eps, gdn_stream_t stream) {
+    if (!y || !w || !z || !out) return GDN_ERR_NULL;
+    if (rows < 0 || head_dim < 1) return GDN_ERR_SHAPE;
+    if (!supported_state_size(head_dim)) {
+        return (head_dim % 32 == 0 && head_dim <= 256) ? GDN_ERR_UNSUPPORTED : GDN_ERR_SHAPE;
+    }
+    if (!aligned16(y) || !aligned16(w) || !aligned16(z) || !aligned16(out)) return GDN_ERR_ALIGN;
+    if (rows == 0) return GDN_OK;
+    const cudaStream_t s = as_cuda(stream);
+    const unsigned blocks = static_cast<unsigned>((rows + kThreads / 32 - 1) / (kThreads / 32));
+    switch (head_dim) {
+        case 32: gated_norm_kernel<1><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps); break;
+        case 64: gated_norm_kernel<2><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps); break;
+        case 128: gated_norm_kernel<4><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps); break;
+        default: gated_norm_kernel<8><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps); break;
+    }
+    return launch_status();
+}
+
+}  // extern "C"

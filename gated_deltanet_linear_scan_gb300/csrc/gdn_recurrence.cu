@@ -1,0 +1,349 @@
+// gdn_recurrence.cu -- the delta-rule recurrence on sm_103a: single-token decode
+// over many sequences (HBM bound) and the multi-token sequential scan (latency /
+// issue bound).
+//
+// Work split, both kernels: a warp owns R = 4 rows (v-index j) of one head's
+// transposed state; lane L holds the contiguous cells [E*L, E*L+E) of each row
+// (E = S/32), so a row moves as one 128-bit access per lane. The two dots per
+// row and token are a 4-term in-lane chain plus a packed shuffle butterfly that
+// serves R rows per shuffle: no shared-memory reduction tree, no barrier inside
+// the token loop. Decode and scan call the same row step, so a scan over T tokens
+// and T decode calls agree bit for bit (fm_kernel_ssm.m states the same property
+// of its scan).
+#include "gdn_device.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+__device__ unsigned g_watchdog;
+
+constexpr int kWarps = 8;           // consumer warps per CTA
+constexpr int kRowsPerWarp = 4;     // R
+constexpr int kRowsPerCta = kWarps * kRowsPerWarp;  // 32 state rows
+constexpr int kScanTokens = 16;     // tokens per staged chunk in the scan
+constexpr int kScanStages = 2;
+
+// Lanes that hold a finished readout for one of the R rows, and which row.
+template <int R>
+__device__ __forceinline__ bool y_writer(int lane, int &r) {
+    constexpr int low = (R == 1) ? 31 : (R == 2) ? 15 : (R == 4) ? 7 : 3;
+    r = ((lane >> 4) & 1) | (((lane >> 3) & 1) << 1) | (((lane >> 2) & 1) << 2);
+    r &= (R - 1);
+    return (lane & low) == 0;
+}
+
+// ---------------------------------------------------------------------------- decode
+// Grid: one CTA per (sequence, v-head, block of 32 rows). Each warp pulls its 4
+// contiguous state rows (4*S*4 bytes) with one bulk copy into shared memory while
+// the lanes fetch k, q, v, g and beta; the update goes back to HBM with 128-bit
+// stores. The state of a (slot, head) is S*S*4 contiguous bytes, so a CTA's tile is
+// one contiguous run and every access is fully coalesced.
+template <int E>
+__global__ void __launch_bounds__(kWarps * 32) recurrence_decode_kernel(
+    float *state, const float *__restrict__ q, const float *__restrict__ k,
+    const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
+    float *__restrict__ y, int n_k_heads, int n_v_heads, float scale,
+    const int32_t *__restrict__ slots, int pool, int32_t *err_count) {
+    constexpr int S = 32 * E, R = kRowsPerWarp;
+    constexpr int kBlocksPerHead = S / kRowsPerCta;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *tile = reinterpret_cast<float *>(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + kRowsPerCta * S * sizeof(float));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int part = blockIdx.x % kBlocksPerHead;
+    const int vh = (blockIdx.x / kBlocksPerHead) % n_v_heads;
+    const int n = blockIdx.x / (kBlocksPerHead * n_v_heads);
+    const int kh = vh % n_k_heads;
+    const int slot = slots ? slots[n] : n;
+    if (slot < 0 || slot >= pool) {
+        if (err_count && vh == 0 && part == 0 && threadIdx.x == 0) atomicAdd(err_count, 1);
+        return;
+    }
+    const int row0 = part * kRowsPerCta + warp * R;  // first row of this warp
+    float *gstate = state + ((static_cast<size_t>(slot) * n_v_heads + vh) * S + row0) * S;
+    float *wtile = tile + warp * R * S;
+    uint64_t *bar = bars + warp;
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, R * S * sizeof(float));
+        bulk_g2s(wtile, gstate, R * S * sizeof(float), bar);
+    }
+    float kk[E], qq[E], vv[R];
+    load_vec<E>(kk, k + (static_cast<size_t>(n) * n_k_heads + kh) * S + lane * E);
+    load_vec<E>(qq, q + (static_cast<size_t>(n) * n_k_heads + kh) * S + lane * E);
+    const size_t hv = static_cast<size_t>(n) * n_v_heads + vh;
+#pragma unroll
+    for (int r = 0; r < R; ++r) vv[r] = v[hv * S + row0 + r];
+    const float decay = expf(g[hv]);
+    const float bt = beta[hv];
+    __syncwarp();
+    if (!mbar_wait(bar, 0)) {
+        if (lane == 0) atomicOr(&g_watchdog, WD_STATE_COPY);
+        mbar_wait(bar, 0);  // never leave with a copy still landing in shared memory
+        return;
+    }
+    float row[R][E];
+#pragma unroll
+    for (int r = 0; r < R; ++r) load_vec<E>(row[r], wtile + r * S + lane * E);
+    const float ysum = row_step<E, R>(row, kk, qq, vv, decay, bt, lane);
+#pragma unroll
+    for (int r = 0; r < R; ++r) store_vec<E>(gstate + r * S + lane * E, row[r]);
+    int r;
+    if (y_writer<R>(lane, r)) y[hv * S + row0 + r] = __fmul_rn(scale, ysum);
+}
+
+// ---------------------------------------------------------------------------- scan
+// Grid: one CTA per (sequence, v-head, block of 32 rows); 8 consumer warps hold
+// their 4 rows in registers for all tokens, plus one producer warp that stages the
+// per-token k, q (S floats each) and this block's 32 v values through a 2-deep ring
+// of shared-memory chunks with bulk copies, each chunk tracked by a "full" and an
+// "empty" mbarrier. g and beta (one float per token and head) are read by the lanes
+// a chunk ahead and broadcast with shuffles. The state reaches HBM once per call.
+template <int E>
+struct ScanSmem {
+    static constexpr int S = 32 * E;
+    static constexpr int kFloats = kScanTokens * S;             // per array per stage
+    static constexpr int vFloats = kScanTokens * kRowsPerCta;
+    static constexpr size_t stage_bytes = (2 * kFloats + vFloats) * sizeof(float);
+    static constexpr size_t bytes = kScanStages * stage_bytes + 2 * kScanStages * sizeof(uint64_t);
+};
+
+template <int E>
+__global__ void __launch_bounds__((kWarps + 1) * 32) recurrence_scan_kernel(
+    float *state, const float *__restrict__ q, const float *__restrict__ k,
+    const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
+    float *__restrict__ y, int n_tokens, int n_k_heads, int n_v_heads, float scale,
+    const int32_t *__restrict__ slots, int pool, int32_t *err_count) {
+    constexpr int S = 32 * E, R = kRowsPerWarp, TC = kScanTokens;
+    constexpr int kBlocksPerHead = S / kRowsPerCta;
+    using L = ScanSmem<E>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + kScanStages * L::stage_bytes);
+    uint64_t *empty = full + kScanStages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int part = blockIdx.x % kBlocksPerHead;
+    const int vh = (blockIdx.x / kBlocksPerHead) % n_v_heads;
+    const int n = blockIdx.x / (kBlocksPerHead * n_v_heads);
+    const int kh = vh % n_k_heads;
+    const int slot = slots ? slots[n] : n;
+    if (slot < 0 || slot >= pool) {
+        if (err_count && vh == 0 && part == 0 && threadIdx.x == 0) atomicAdd(err_count, 1);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kScanStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, kWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int n_chunks = (n_tokens + TC - 1) / TC;
+    const size_t kq_tok = static_cast<size_t>(n_k_heads) * S;   // q/k stride per token
+    const size_t v_tok = static_cast<size_t>(n_v_heads) * S;    // v/y stride per token
+    const float *kbase = k + (static_cast<size_t>(n) * n_tokens * n_k_heads + kh) * S;
+    const float *qbase = q + (static_cast<size_t>(n) * n_tokens * n_k_heads + kh) * S;
+    const float *vbase = v + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S +
+                         part * kRowsPerCta;
+
+    if (warp == kWarps) {
+        // ---- producer warp: lane t copies token t of each chunk.
+        bool ok = true;
+        for (int c = 0; c < n_chunks && ok; ++c) {
+            const int s = c % kScanStages, use = c / kScanStages;
+            if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1)) {
+                if (lane == 0) atomicOr(&g_watchdog, WD_STAGE_FREE);
+                ok = false;
+                break;
+            }
+            const int tc = min(TC, n_tokens - c * TC);
+            unsigned char *st = smem_raw + s * L::stage_bytes;
+            float *ks = reinterpret_cast<float *>(st);
+            float *qs = ks + L::kFloats;
+            float *vs = qs + L::kFloats;
+            if (lane == 0)
+                mbar_arrive_expect_tx(full + s, tc * (2 * S + kRowsPerCta) * sizeof(float));
+            __syncwarp();
+            if (lane < tc) {
+                const size_t t = static_cast<size_t>(c) * TC + lane;
+                bulk_g2s(ks + lane * S, kbase + t * kq_tok, S * sizeof(float), full + s);
+                bulk_g2s(qs + lane * S, qbase + t * kq_tok, S * sizeof(float), full + s);
+                bulk_g2s(vs + lane * kRowsPerCta, vbase + t * v_tok, kRowsPerCta * sizeof(float),
+                         full + s);
+            }
+        }
+        // Do not leave while copies may still be landing in this CTA's shared memory.
+        if (ok && n_chunks > 0) {
+            for (int c = max(0, n_chunks - kScanStages); c < n_chunks; ++c)
+                mbar_wait(full + c % kScanStages, (c / kScanStages) & 1);
+        }
+        return;
+    }
+
+    // ---- consumer warps
+    const int row0 = part * kRowsPerCta + warp * R;
+    float *gstate = state + ((static_cast<size_t>(slot) * n_v_heads + vh) * S + row0) * S;
+    float row[R][E];
+#pragma unroll
+    for (int r = 0; r < R; ++r) load_vec<E>(row[r], gstate + r * S + lane * E);
+    const size_t gb_base = static_cast<size_t>(n) * n_tokens * n_v_heads + vh;
+    int yr;
+    const bool writer = y_writer<R>(lane, yr);
+    float *ybase = y + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S + row0 + yr;
+
+    // g and beta of token (chunk*TC + lane), one chunk ahead.
+    auto fetch_gb = [&](int c, float &dec, float &bt) {
+        const int t = c * TC + lane;
+        if (lane < TC && c < n_chunks && t < n_tokens) {
+            dec = expf(g[gb_base + static_cast<size_t>(t) * n_v_heads]);
+            bt = beta[gb_base + static_cast<size_t>(t) * n_v_heads];
+        } else {
+            dec = 1.0f;
+            bt = 0.0f;
+        }
+    };
+    float dec_cur, bt_cur, dec_nxt, bt_nxt;
+    fetch_gb(0, dec_cur, bt_cur);
+    bool ok = true;
+    for (int c = 0; c < n_chunks; ++c) {
+        const int s = c % kScanStages;
+        fetch_gb(c + 1, dec_nxt, bt_nxt);
+        if (!mbar_wait(full + s, (c / kScanStages) & 1)) {
+            if (lane == 0) atomicOr(&g_watchdog, WD_STAGE_COPY);
+            ok = false;
+            break;
+        }
+        const unsigned char *st = smem_raw + s * L::stage_bytes;
+        const float *ks = reinterpret_cast<const float *>(st);
+        const float *qs = ks + L::kFloats;
+        const float *vs = qs + L::kFloats;
+        const int tc = min(TC, n_tokens - c * TC);
+        for (int t = 0; t < tc; ++t) {
+            float kk[E], qq[E], vv[R];
+            load_vec<E>(kk, ks + t * S + lane * E);
+            load_vec<E>(qq, qs + t * S + lane * E);
+            load_vec<R>(vv, vs + t * kRowsPerCta + warp * R);
+            const float decay = __shfl_sync(FULL_MASK, dec_cur, t);
+            const float bt = __shfl_sync(FULL_MASK, bt_cur, t);
+            const float ysum = row_step<E, R>(row, kk, qq, vv, decay, bt, lane);
+            if (writer) ybase[(static_cast<size_t>(c) * TC + t) * v_tok] = __fmul_rn(scale, ysum);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + s);
+        dec_cur = dec_nxt;
+        bt_cur = bt_nxt;
+    }
+    if (!ok) return;  // leave the state untouched rather than write a partial scan
+#pragma unroll
+    for (int r = 0; r < R; ++r) store_vec<E>(gstate + r * S + lane * E, row[r]);
+}
+
+// Opts a kernel in to more than 48 KiB of dynamic shared memory.
+template <typename Kern>
+gdn_status set_smem(Kern kern, size_t bytes) {
+    if (bytes <= 48 * 1024) return GDN_OK;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(bytes)) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_LAUNCH;
+}
+
+template <int E>
+gdn_status launch_decode(float *state, const float *q, const float *k, const float *v,
+                         const float *g, const float *beta, float *y, int n_seqs, int n_k_heads,
+                         int n_v_heads, float scale, const int32_t *slots, int pool,
+                         int32_t *err_count, cudaStream_t s) {
+    constexpr int S = 32 * E;
+    const size_t smem = kRowsPerCta * S * sizeof(float) + kWarps * sizeof(uint64_t);
+    GDN_TRY(set_smem(recurrence_decode_kernel<E>, smem));
+    const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / kRowsPerCta);
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    recurrence_decode_kernel<E><<<static_cast<unsigned>(blocks), kWarps * 32, smem, s>>>(
+        state, q, k, v, g, beta, y, n_k_heads, n_v_heads, scale, slots, pool, err_count);
+    return launch_status();
+}
+
+template <int E>
+gdn_status launch_scan(float *state, const float *q, const float *k, const float *v,
+                       const float *g, const float *beta, float *y, int n_seqs, int n_tokens,
+                       int n_k_heads, int n_v_heads, float scale, const int32_t *slots, int pool,
+                       int32_t *err_count, cudaStream_t s) {
+    constexpr int S = 32 * E;
+    const size_t smem = ScanSmem<E>::bytes;
+    GDN_TRY(set_smem(recurrence_scan_kernel<E>, smem));
+    const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / kRowsPerCta);
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    recurrence_scan_kernel<E><<<static_cast<unsigned>(blocks), (kWarps + 1) * 32, smem, s>>>(
+        state, q, k, v, g, beta, y, n_tokens, n_k_heads, n_v_heads, scale, slots, pool,
+        err_count);
+    return launch_status();
+}
+
+gdn_status check_recurrence_args(const float *state, const float *q, const float *k,
+                                 const float *v, const float *g, const float *beta,
+                                 const float *y, int n_seqs, int n_tokens, int n_k_heads,
+                                 int n_v_heads, int state_size, const int32_t *slots, int pool) {
+    if (!state || !q || !k || !v || !g || !beta || !y) return GDN_ERR_NULL;
+    if (n_seqs < 0 || n_tokens < 0) return GDN_ERR_SHAPE;
+    GDN_TRY(check_heads(n_k_heads, n_v_heads, state_size));
+    GDN_TRY(check_pool(n_seqs, slots, pool));
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_ERR_ALIGN;
+    return GDN_OK;
+}
+
+}  // namespace
+
+unsigned read_and_clear_watchdog_recurrence(cudaStream_t s) {
+    unsigned flags = 0;
+    const unsigned zero = 0;
+    cudaMemcpyFromSymbolAsync(&flags, g_watchdog, sizeof(flags), 0, cudaMemcpyDeviceToHost, s);
+    cudaMemcpyToSymbolAsync(g_watchdog, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+    cudaStreamSynchronize(s);
+    return flags;
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+gdn_status gdn_recurrence_decode(float *state, const float *q, const float *k, const float *v,
+                                 const float *g, const float *beta, float *y, int n_seqs,
+                                 int n_k_heads, int n_v_heads, int state_size, float scale,
+                                 const int32_t *slots, int pool, int32_t *err_count,
+                                 gdn_stream_t stream) {
+    GDN_TRY(check_recurrence_args(state, q, k, v, g, beta, y, n_seqs, 1, n_k_heads, n_v_heads,
+                                  state_size, slots, pool));
+    if (n_seqs == 0) return GDN_OK;
+    const cudaStream_t s = as_cuda(stream);
+    switch (state_size) {
+        case 32: return launch_decode<1>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+        case 64: return launch_decode<2>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+        case 128: return launch_decode<4>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+        default: return launch_decode<8>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+    }
+}
+
+gdn_status gdn_recurrence_scan(float *state, const float *q, const float *k, const float *v,
+                               const float *g, const float *beta, float *y, int n_seqs,
+                               int n_tokens, int n_k_heads, int n_v_heads, int state_size,
+                               float scale, const int32_t *slots, int pool, int32_t *err_count,
+                               gdn_stream_t stream) {
+    GDN_TRY(check_recurrence_args(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads,
+                                  n_v_heads, state_size, slots, pool));
+    if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
+    const cudaStream_t s = as_cuda(stream);
+    switch (state_size) {
+        case 32: return launch_scan<1>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+        case 64: return launch_scan<2>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+        case 128: return launch_scan<4>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+        default: return launch_scan<8>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+    }
+}
+
+}  // extern "C"

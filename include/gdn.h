@@ -1,0 +1,172 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated delta-rule SSM library.
+ *
+ * The Gated-DeltaNet SSM block of a hybrid LLM, per (sequence, v-head h):
+ *   decay gate      g = a[h] * softplus(alpha + dt[h])
+ *   conv1d + SiLU   causal depthwise, kernel K, rolling conv_state
+ *   q/k L2-norm     x / max(||x||, eps), then GQA: v-head vh reads k-head vh % Hk
+ *   recurrence      S <- exp(g) S; pred = S k; delta = (v - pred) beta;
+ *                   S <- S + k delta^T; y = scale S^T q  (read after the write)
+ *   gated RMSNorm   out = y / sqrt(mean(y^2) + eps) * w * silu(z)
+ * Sources: "fm_kernel_ssm.m" (Foundry: Metal host dispatch + shader source),
+ * "ssm_gated_delta.cu" (Foundry: CUDA kernels), "gated_delta_net_decode.metal"
+ * (mlx-native 0.21.1). Each entry point below names the section it follows.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All array arguments are DEVICE pointers to fp32 (int32 for slot ids),
+ *   allocated and owned by the caller. The library allocates and frees nothing.
+ * - Every call is asynchronous on `stream` (NULL = legacy default stream). A
+ *   return of GDN_OK means the work was validated and enqueued.
+ * - Arguments are validated on the host before anything is enqueued; on any
+ *   error nothing is enqueued and no memory is touched. (The pages' launchers
+ *   return silently on bad arguments; here the failure is a status code.)
+ * - Pointers used with 128-bit or bulk (TMA) copies must be 16-byte aligned;
+ *   a misaligned one gives GDN_ERR_ALIGN. Buffers from cudaMalloc are.
+ * - Shapes: n_v_heads % n_k_heads == 0; state_size (= D_k = D_v = S) in
+ *   {32, 64, 128, 256}; conv_kernel K in [2, 8] (the fused block: K = 4).
+ *   n_seqs == 0 or n_tokens == 0 is a valid no-op.
+ * - Layouts (row-major, innermost last):
+ *     state       [pool][H][S][S]  state[((slot*H + h)*S + j)*S + i] == S_h[i][j]
+ *                                  (transposed: row j, a v-index, is contiguous over i)
+ *     conv_state  [pool][C][K-1]   oldest tap first, holding RAW (pre-conv) inputs
+ *     conv_w      [C][K]           conv_w[c][K-1] multiplies the current input
+ *     qkv         [N][T][C]        C = 2*Hk*S + H*S packed as [q | k | v]
+ *     q, k        [N][T][Hk][S]    k-head space (post-L2-norm for the recurrence)
+ *     v, y, z     [N][T][H][S]
+ *     g, beta     [N][T][H]        g is the log-decay (<= 0), beta in (0, 1)
+ * - Serving pool: sequence n uses state (and conv_state) slot slots[n], or n
+ *   when `slots` is NULL. `pool` is the number of slots the buffers hold. Slot
+ *   ids within one call must be distinct (duplicates race: undefined result).
+ *   A sequence whose id lies outside [0, pool) is skipped -- nothing of it is
+ *   read or written -- and, if `err_count` (device int32) is non-NULL, 1 is
+ *   added to *err_count per skipped sequence. Untouched slots keep their bits.
+ * - Kernels that wait on their own asynchronous copies bound every wait (about
+ *   two seconds). A wait that gives up skips the work it guarded and raises a
+ *   device-side flag; gdn_device_error() reads and clears it.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; spelled here so the header needs no CUDA include. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,        /* a required pointer is NULL */
+    GDN_ERR_SHAPE = 2,       /* a dimension is negative/zero where it may not be, or inconsistent */
+    GDN_ERR_UNSUPPORTED = 3, /* valid for the method, but no kernel is built for it */
+    GDN_ERR_ALIGN = 4,       /* a pointer that needs 16-byte alignment is not aligned */
+    GDN_ERR_LAUNCH = 5,      /* the CUDA launch itself failed (see cudaGetLastError) */
+    GDN_ERR_DEVICE = 6       /* a kernel's bounded wait gave up (from gdn_device_error) */
+} gdn_status;
+
+/* Name of a status code ("GDN_OK", ...); never NULL. */
+const char *gdn_status_str(gdn_status status);
+
+/* ABI version of this library, (major << 16) | minor. */
+int gdn_version(void);
+
+/* Synchronises `stream`, then reads and clears the device-side flag raised by
+ * bounded waits that gave up. GDN_OK if none did, GDN_ERR_DEVICE otherwise, or
+ * GDN_ERR_LAUNCH if the synchronisation itself reported a CUDA error. */
+gdn_status gdn_device_error(gdn_stream_t stream);
+
+/* Decay gate. fm_kernel_ssm.m, "Decay gate: g[r][h] = a[h] * softplus(alpha[r][h] +
+ * dt[h])"; ssm_gated_delta.cu, glue kernels (fc_ssm_decay_gate, _nx).
+ *   g[r][h] = a[h] * softplus(alpha[r][h] + dt[h]),  softplus(v) = v > 20 ? v : log1p(exp(v))
+ * alpha, g: [rows][n_heads]; dt, a: [n_heads] (a = -exp(A_log), baked by the caller).
+ * g may alias alpha. rows == 0 is a no-op. */
+gdn_status gdn_decay_gate(const float *alpha, const float *dt, const float *a, float *g,
+                          int n_heads, int rows, gdn_stream_t stream);
+
+/* beta = 1 / (1 + exp(-b)) over n elements. ssm_gated_delta.cu, glue kernels
+ * (fc_sigmoid). beta may alias b. */
+gdn_status gdn_beta_sigmoid(const float *b, float *beta, int n, gdn_stream_t stream);
+
+/* Causal depthwise conv1d + SiLU, one token per sequence. fm_kernel_ssm.m, "Causal
+ * depthwise conv1d + SiLU"; ssm_gated_delta.cu, Kernel 2 and the slot variant.
+ *   pre = qkv[c] * w[c][K-1] + sum_{t<K-1} hist[c][t] * w[c][t];  out[c] = silu(pre)
+ * then hist[c] drops its oldest tap and appends the raw qkv[c].
+ * qkv, out: [n_seqs][conv_dim]; w: [conv_dim][K]; conv_state: [pool][conv_dim][K-1]
+ * (in place). out must not alias qkv. */
+gdn_status gdn_conv1d_silu(const float *qkv, const float *w, float *conv_state, float *out,
+                           int n_seqs, int conv_dim, int conv_kernel, const int32_t *slots,
+                           int pool, int32_t *err_count, gdn_stream_t stream);
+
+/* The same over n_tokens positions per sequence, history carried in registers;
+ * bit-identical to n_tokens single-token calls. fm_kernel_ssm.m, the conv scan
+ * (fmssm_conv1d_silu_seq); ssm_gated_delta.cu, "BATCHED (prefill) variants".
+ * qkv, out: [n_seqs][n_tokens][conv_dim]. */
+gdn_status gdn_conv1d_silu_seq(const float *qkv, const float *w, float *conv_state, float *out,
+                               int n_seqs, int n_tokens, int conv_dim, int conv_kernel,
+                               const int32_t *slots, int pool, int32_t *err_count,
+                               gdn_stream_t stream);
+
+/* Split a conv output row [q | k | v] and L2-normalise q and k per k-head.
+ * ssm_gated_delta.cu, glue kernels (fc_ssm_qknorm_gqa_nx: "x / max(sqrt(sum x^2),
+ * eps)", v a plain copy). No GQA copy is made: the recurrence maps v-head vh to
+ * k-head vh % n_k_heads itself.
+ * conv_out: [rows][C]; q, k: [rows][Hk][S]; v: [rows][H][S]. No aliasing. */
+gdn_status gdn_qkv_split_norm(const float *conv_out, float *q, float *k, float *v, int rows,
+                              int n_k_heads, int n_v_heads, int state_size, float eps,
+                              gdn_stream_t stream);
+
+/* Delta-rule recurrence, one token per sequence (decode). fm_kernel_ssm.m,
+ * "Delta-rule recurrence -- register-resident"; ssm_gated_delta.cu, Kernel 1 and
+ * the slot variant; gated_delta_net_decode.metal, "Mathematical recurrence".
+ * state: [pool][H][S][S], updated in place (16-byte aligned); q, k: [n_seqs][Hk][S]
+ * (post-norm, 16-byte aligned); v, y: [n_seqs][H][S]; g, beta: [n_seqs][H].
+ * scale multiplies the readout: 1/sqrt(S), or 1.0f when q is pre-scaled. */
+gdn_status gdn_recurrence_decode(float *state, const float *q, const float *k, const float *v,
+                                 const float *g, const float *beta, float *y, int n_seqs,
+                                 int n_k_heads, int n_v_heads, int state_size, float scale,
+                                 const int32_t *slots, int pool, int32_t *err_count,
+                                 gdn_stream_t stream);
+
+/* Sequential scan over n_tokens positions per sequence, the state kept in
+ * registers and written back once. fm_kernel_ssm.m, "The sequential scan";
+ * ssm_gated_delta.cu, fc_ssm_recurrence_seq and its warp form; gated_delta_net_decode.metal
+ * (per-token pointer advance). Bit-identical to n_tokens decode calls.
+ * q, k: [n_seqs][n_tokens][Hk][S]; v, y: [n_seqs][n_tokens][H][S];
+ * g, beta: [n_seqs][n_tokens][H]; state as for decode. */
+gdn_status gdn_recurrence_scan(float *state, const float *q, const float *k, const float *v,
+                               const float *g, const float *beta, float *y, int n_seqs,
+                               int n_tokens, int n_k_heads, int n_v_heads, int state_size,
+                               float scale, const int32_t *slots, int pool, int32_t *err_count,
+                               gdn_stream_t stream);
+
+/* Gated RMSNorm. fm_kernel_ssm.m, "Gated RMSNorm"; ssm_gated_delta.cu, Kernel 3.
+ *   out[r][d] = y[r][d] / sqrt(mean_d(y[r]^2) + eps) * w[d] * silu(z[r][d])
+ * y, z, out: [rows][head_dim]; w: [head_dim], the one weight shared by all heads.
+ * head_dim in {32, 64, 128, 256}. out may alias y. */
+gdn_status gdn_gated_norm(const float *y, const float *w, const float *z, float *out, int rows,
+                          int head_dim, float eps, gdn_stream_t stream);
+
+/* The whole block for one decode token per sequence, in one kernel: conv1d+SiLU
+ * of the raw qkv row (rolling conv_state), q/k L2-norm, GQA, decay gate, beta =
+ * sigmoid(b), recurrence, gated RMSNorm. Each state byte is read and written
+ * once. Follows the single-token glue order of ssm_gated_delta.cu ("SSM glue
+ * kernels" and Kernels 1-3).
+ * qkv: [n_seqs][C] raw; conv_w: [C][4]; conv_state: [pool][C][3] in place;
+ * alpha, b: [n_seqs][H] raw gate and beta logits; dt, a: [H]; z: [n_seqs][H][S];
+ * norm_w: [S]; state: [pool][H][S][S] in place; out: [n_seqs][H][S].
+ * conv_kernel must be 4; n_v_heads / n_k_heads <= 8. All pointers 16-byte aligned. */
+gdn_status gdn_block_decode(const float *qkv, const float *conv_w, float *conv_state,
+                            const float *alpha, const float *b, const float *dt, const float *a,
+                            const float *z, const float *norm_w, float *state, float *out,
+                            int n_seqs, int n_k_heads, int n_v_heads, int state_size,
+                            int conv_kernel, float scale, float l2_eps, float norm_eps,
+                            const int32_t *slots, int pool, int32_t *err_count,
+                            gdn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H */

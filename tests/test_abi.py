@@ -1,0 +1,144 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+libgdn.so must load, export every function include/gdn.h declares, and reject
+bad arguments on the host with the documented status before anything is
+enqueued. Only argument combinations that fail validation (or are documented
+no-ops) are passed here, so no CUDA call is made.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_linear_scan_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+OK, NULL, SHAPE, UNSUP, ALIGN = 0, 1, 2, 3, 4
+P = 0x10000      # a 16-byte aligned fake device address (never dereferenced here)
+MIS = 0x10004    # a misaligned one
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gdn.build_if_needed()
+    return gdn.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for want in ("gdn_decay_gate", "gdn_beta_sigmoid", "gdn_conv1d_silu", "gdn_conv1d_silu_seq",
+                 "gdn_qkv_split_norm", "gdn_recurrence_decode", "gdn_recurrence_scan",
+                 "gdn_gated_norm", "gdn_block_decode", "gdn_status_str", "gdn_version",
+                 "gdn_device_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libgdn.so does not export {name}"
+    # and the binding wraps each of them under the same name
+    for name in declared_functions():
+        assert hasattr(gdn, name), f"binding lacks {name}"
+
+
+def test_status_strings_and_version(lib):
+    for code, name in gdn.STATUS.items():
+        assert lib.gdn_status_str(code).decode() == name
+    assert lib.gdn_status_str(99).decode() == "GDN_ERR_UNKNOWN"
+    assert lib.gdn_version() >> 16 == 1
+
+
+def rec(lib, name, state=P, q=P, k=P, v=P, g=P, beta=P, y=P, n_seqs=1, n_tokens=1, hk=2, hv=4,
+        s=32, scale=0.1, slots=None, pool=None, err=None):
+    pool = max(1, n_seqs) if pool is None else pool
+    if name == "gdn_recurrence_decode":
+        return lib.gdn_recurrence_decode(state, q, k, v, g, beta, y, n_seqs, hk, hv, s, scale,
+                                         slots, pool, err, None)
+    return lib.gdn_recurrence_scan(state, q, k, v, g, beta, y, n_seqs, n_tokens, hk, hv, s, scale,
+                                   slots, pool, err, None)
+
+
+@pytest.mark.parametrize("name", ["gdn_recurrence_decode", "gdn_recurrence_scan"])
+def test_recurrence_validation(lib, name):
+    assert rec(lib, name, state=None) == NULL
+    assert rec(lib, name, y=None) == NULL
+    assert rec(lib, name, n_seqs=-1) == SHAPE
+    assert rec(lib, name, hk=3, hv=4) == SHAPE          # H % Hk != 0
+    assert rec(lib, name, hk=0) == SHAPE
+    assert rec(lib, name, s=48) == SHAPE                # not a multiple of 32... 48 % 32 != 0
+    assert rec(lib, name, s=512) == SHAPE               # beyond 8 cells per lane
+    assert rec(lib, name, s=96) == UNSUP                # valid for the method, no kernel built
+    assert rec(lib, name, n_seqs=3, pool=2) == SHAPE    # no slots and pool < n_seqs
+    assert rec(lib, name, pool=0) == SHAPE
+    assert rec(lib, name, state=MIS) == ALIGN
+    assert rec(lib, name, q=MIS) == ALIGN
+    assert rec(lib, name, n_seqs=0) == OK               # documented no-op
+    if name == "gdn_recurrence_scan":
+        assert rec(lib, name, n_tokens=-1) == SHAPE
+        assert rec(lib, name, n_tokens=0) == OK
+
+
+def test_conv_validation(lib):
+    f = lib.gdn_conv1d_silu
+    assert f(None, P, P, P, 1, 256, 4, None, 1, None, None) == NULL
+    assert f(P, P, P, P, 1, 256, 1, None, 1, None, None) == SHAPE
+    assert f(P, P, P, P, 1, 256, 9, None, 1, None, None) == SHAPE
+    assert f(P, P, P, P, 1, 0, 4, None, 1, None, None) == SHAPE
+    assert f(P, P, P, P, 2, 256, 4, None, 1, None, None) == SHAPE
+    assert f(P, P, P, P, 0, 256, 4, None, 1, None, None) == OK
+    fs = lib.gdn_conv1d_silu_seq
+    assert fs(P, P, P, P, 1, -2, 256, 4, None, 1, None, None) == SHAPE
+    assert fs(P, P, P, P, 1, 0, 256, 4, None, 1, None, None) == OK
+
+
+def test_elementwise_validation(lib):
+    assert lib.gdn_decay_gate(P, P, None, P, 4, 2, None) == NULL
+    assert lib.gdn_decay_gate(P, P, P, P, 0, 2, None) == SHAPE
+    assert lib.gdn_decay_gate(P, P, P, P, 4, 0, None) == OK
+    assert lib.gdn_beta_sigmoid(P, None, 4, None) == NULL
+    assert lib.gdn_beta_sigmoid(P, P, -1, None) == SHAPE
+    assert lib.gdn_beta_sigmoid(P, P, 0, None) == OK
+    assert lib.gdn_gated_norm(P, P, P, None, 4, 128, 1e-6, None) == NULL
+    assert lib.gdn_gated_norm(P, P, P, P, 4, 100, 1e-6, None) == SHAPE
+    assert lib.gdn_gated_norm(P, P, P, P, 4, 96, 1e-6, None) == UNSUP
+    assert lib.gdn_gated_norm(MIS, P, P, P, 4, 128, 1e-6, None) == ALIGN
+    assert lib.gdn_gated_norm(P, P, P, P, 0, 128, 1e-6, None) == OK
+    assert lib.gdn_qkv_split_norm(P, P, P, None, 1, 2, 4, 32, 1e-6, None) == NULL
+    assert lib.gdn_qkv_split_norm(P, P, P, P, 1, 3, 4, 32, 1e-6, None) == SHAPE
+    assert lib.gdn_qkv_split_norm(P, P, MIS, P, 1, 2, 4, 32, 1e-6, None) == ALIGN
+    assert lib.gdn_qkv_split_norm(P, P, P, P, 0, 2, 4, 32, 1e-6, None) == OK
+
+
+def block(lib, qkv=P, state=P, out=P, n_seqs=1, hk=2, hv=4, s=32, K=4, slots=None, pool=None):
+    pool = max(1, n_seqs) if pool is None else pool
+    return lib.gdn_block_decode(qkv, P, P, P, P, P, P, P, P, state, out, n_seqs, hk, hv, s, K,
+                                0.1, 1e-6, 1e-6, slots, pool, None, None)
+
+
+def test_block_validation(lib):
+    assert block(lib, qkv=None) == NULL
+    assert block(lib, out=None) == NULL
+    assert block(lib, K=1) == SHAPE
+    assert block(lib, K=3) == UNSUP        # valid conv kernel, the fused block is built for 4
+    assert block(lib, hk=1, hv=16) == UNSUP  # GQA ratio beyond a portable cluster
+    assert block(lib, hk=3, hv=4) == SHAPE
+    assert block(lib, s=96) == UNSUP
+    assert block(lib, state=MIS) == ALIGN
+    assert block(lib, n_seqs=4, pool=2) == SHAPE
+    assert block(lib, n_seqs=0) == OK
+
+
+def test_binding_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(4)
+    with pytest.raises(ValueError):
+        gdn.gdn_beta_sigmoid(x, x, 4, stream=0)

@@ -1,0 +1,453 @@
+"""GPU parity: every entry point of libgdn.so against the CPU oracle.
+
+All inputs come from the seeded generators; the oracle (double build) and the
+GPU see the same float32 arrays. Tolerances are the ones stated for the method:
+  - one step (single token, or the first of a chain): elementwise
+    |gpu - ref| <= 1e-4 + 1e-4 * |ref| for y/out and the state;
+  - after a long chain or scan: max |gpu - ref| <= 2e-3 * RMS(ref), per tensor.
+Within the GPU library, the scan and repeated decode calls (and the scan split in
+two) must agree bit for bit; the fused block with a whole head per CTA must
+equal the unfused pipeline bit for bit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gated_deltanet_linear_scan_gb300 import inputs as I
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ helpers
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.detach().cpu().numpy()
+
+
+def f64(x):
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def assert_step(gpu, ref, name):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert gpu.shape == ref.shape, name
+    assert np.all(np.isfinite(gpu)), f"{name}: non-finite values"
+    err = np.abs(gpu - ref)
+    bound = 1e-4 + 1e-4 * np.abs(ref)
+    worst = np.max(err - bound)
+    assert worst <= 0, f"{name}: elementwise bound exceeded by {worst:.3e} (max err {err.max():.3e})"
+
+
+def assert_rms(gpu, ref, name, rel=2e-3):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(gpu)), f"{name}: non-finite values"
+    rms = np.sqrt(np.mean(ref * ref))
+    err = np.max(np.abs(gpu - ref))
+    assert err <= rel * rms, f"{name}: max err {err:.3e} > {rel} * RMS {rms:.3e}"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib(cuda_lib):
+    yield cuda_lib
+    cuda_lib.gdn_device_error()  # no bounded wait gave up during the module
+
+
+# ------------------------------------------------------------------ small steps
+
+def test_decay_gate_and_beta(lib):
+    r = np.random.default_rng(100)
+    rows, H = 37, 32
+    alpha = r.normal(0, 6, (rows, H)).astype(np.float32)
+    alpha[0, :4] = [25.0, 20.0, 19.99, -40.0]  # both sides of the guard at 20
+    dt = r.normal(0, 0.5, H).astype(np.float32)
+    a = (-np.exp(r.uniform(-1, 1, H))).astype(np.float32)
+    g = torch.empty(rows, H, device="cuda")
+    lib.gdn_decay_gate(dev(alpha), dev(dt), dev(a), g, H, rows)
+    assert_step(host(g), oracle.decay_gate(alpha, dt, a), "g")
+    b = r.normal(0, 3, 1001).astype(np.float32)
+    beta = dev(b)
+    lib.gdn_beta_sigmoid(beta, beta, b.size)  # in place
+    assert_step(host(beta), oracle.sigmoid(b), "beta")
+
+
+@pytest.mark.parametrize("K", [2, 3, 4, 5, 8])
+@pytest.mark.parametrize("C,T", [(256, 1), (256, 21), (8192, 3)])
+def test_conv1d_silu(lib, K, C, T):
+    r = np.random.default_rng(101 + K)
+    N, P = 3, 5
+    slots = np.array([4, 0, 2], dtype=np.int32)
+    qkv = r.normal(0, 1, (N, T, C)).astype(np.float32)
+    w = r.normal(0, 0.5, (C, K)).astype(np.float32)
+    cs0 = r.normal(0, 1, (P, C, K - 1)).astype(np.float32)
+    cs = dev(cs0)
+    out = torch.zeros(N, T, C, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.gdn_conv1d_silu_seq(dev(qkv), dev(w), cs, out, N, T, C, K, slots=dev(slots), pool=P,
+                            err_count=err)
+    cs_ref = f64(cs0)
+    out_ref, skipped = oracle.conv1d_silu_seq(qkv, w, cs_ref, slots=slots, pool=P)
+    assert skipped == 0 and host(err)[0] == 0
+    assert_step(host(out), out_ref, "conv out")
+    assert_step(host(cs), cs_ref, "conv_state")
+    for s in (1, 3):
+        np.testing.assert_array_equal(host(cs)[s], cs0[s])
+    # the scan equals T single-token calls, bit for bit
+    cs2 = dev(cs0)
+    for t in range(T):
+        o1 = torch.zeros(N, C, device="cuda")
+        lib.gdn_conv1d_silu(dev(qkv[:, t]), dev(w), cs2, o1, N, C, K, slots=dev(slots), pool=P)
+        np.testing.assert_array_equal(host(o1), host(out)[:, t])
+    np.testing.assert_array_equal(host(cs2), host(cs))
+
+
+def test_conv1d_silu_invalid_slot(lib):
+    r = np.random.default_rng(102)
+    N, C, K, P = 3, 256, 4, 4
+    slots = np.array([1, 7, -2], dtype=np.int32)
+    qkv = r.normal(0, 1, (N, C)).astype(np.float32)
+    w = r.normal(0, 0.5, (C, K)).astype(np.float32)
+    cs0 = r.normal(0, 1, (P, C, K - 1)).astype(np.float32)
+    cs = dev(cs0)
+    out = torch.full((N, C), 7.0, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.gdn_conv1d_silu(dev(qkv), dev(w), cs, out, N, C, K, slots=dev(slots), pool=P,
+                        err_count=err)
+    assert host(err)[0] == 2
+    o = host(out)
+    assert np.all(o[1:] == 7.0)
+    np.testing.assert_array_equal(host(cs)[[0, 2, 3]], cs0[[0, 2, 3]])
+
+
+@pytest.mark.parametrize("Hk,H,S", [(2, 4, 32), (16, 32, 128), (1, 2, 64), (2, 4, 256)])
+def test_qkv_split_norm(lib, Hk, H, S):
+    r = np.random.default_rng(103)
+    rows = 5
+    C = 2 * Hk * S + H * S
+    x = r.normal(0, 1, (rows, C)).astype(np.float32)
+    x[2, :S] = 0.0  # a zero q head: maps to zeros
+    q = torch.empty(rows, Hk, S, device="cuda")
+    k = torch.empty_like(q)
+    v = torch.empty(rows, H, S, device="cuda")
+    lib.gdn_qkv_split_norm(dev(x), q, k, v, rows, Hk, H, S, 1e-6)
+    key = Hk * S
+    assert_step(host(q), oracle.l2norm(x[:, :key].reshape(rows, Hk, S), 1e-6), "q")
+    assert_step(host(k), oracle.l2norm(x[:, key:2 * key].reshape(rows, Hk, S), 1e-6), "k")
+    np.testing.assert_array_equal(host(v), x[:, 2 * key:].reshape(rows, H, S))
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+def test_gated_norm(lib, D):
+    r = np.random.default_rng(104)
+    rows = 67
+    y = r.normal(0, 1, (rows, D)).astype(np.float32)
+    z = r.normal(0, 1, (rows, D)).astype(np.float32)
+    w = r.normal(1, 0.1, D).astype(np.float32)
+    out = torch.empty(rows, D, device="cuda")
+    lib.gdn_gated_norm(dev(y), dev(w), dev(z), out, rows, D, 1e-6)
+    assert_step(host(out), oracle.gated_norm(y, w, z, 1e-6), "gated norm")
+    yt = dev(y)
+    lib.gdn_gated_norm(yt, dev(w), dev(z), yt, rows, D, 1e-6)  # in place
+    np.testing.assert_array_equal(host(yt), host(out))
+
+
+# ------------------------------------------------------------------ recurrence
+
+def rec_case(Hk, H, S, N, T, seed, pool=None):
+    cfg = I.get_config(0, n_k_heads=Hk, n_v_heads=H, state_size=S, n_seqs=N, n_tokens=T,
+                       pool=pool, cid=200 + seed)
+    x = I.recurrence_batch(cfg)
+    st0 = I.state_pool(cfg)
+    return cfg, x, st0
+
+
+def run_decode(lib, cfg, x, st, t, slots=None, pool=None, err=None):
+    N, H, S = cfg.n_seqs, cfg.n_v_heads, cfg.state_size
+    y = torch.zeros(N, H, S, device="cuda")
+    lib.gdn_recurrence_decode(st, dev(x["q"][:, t]), dev(x["k"][:, t]), dev(x["v"][:, t]),
+                              dev(x["g"][:, t]), dev(x["beta"][:, t]), y, N, cfg.n_k_heads, H, S,
+                              cfg.scale, slots=slots, pool=pool, err_count=err)
+    return y
+
+
+@pytest.mark.parametrize("Hk,H,S", [(2, 4, 32), (16, 32, 128), (1, 1, 64), (4, 16, 256),
+                                    (8, 8, 128)])
+def test_recurrence_decode(lib, Hk, H, S):
+    cfg, x, st0 = rec_case(Hk, H, S, N=3, T=1, seed=S + H)
+    st = dev(st0)
+    y = run_decode(lib, cfg, x, st, 0)
+    st_ref = f64(st0)
+    y_ref, _ = oracle.recurrence(st_ref, x["q"][:, :1], x["k"][:, :1], x["v"][:, :1],
+                                 x["g"][:, :1], x["beta"][:, :1], cfg.scale)
+    assert_step(host(y), y_ref[:, 0], "y")
+    assert_step(host(st), st_ref, "state")
+
+
+def test_recurrence_decode_slots(lib):
+    cfg, x, _ = rec_case(2, 4, 128, N=4, T=1, seed=7, pool=9)
+    pool0 = I.state_pool(cfg)
+    slots = np.array([5, 0, 11, 3], dtype=np.int32)  # 11 is out of range
+    st = dev(pool0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = run_decode(lib, cfg, x, st, 0, slots=dev(slots), pool=9, err=err)
+    assert host(err)[0] == 1
+    st_ref = f64(pool0)
+    y_ref, skipped = oracle.recurrence(st_ref, x["q"][:, :1], x["k"][:, :1], x["v"][:, :1],
+                                       x["g"][:, :1], x["beta"][:, :1], cfg.scale, slots=slots,
+                                       pool=9)
+    assert skipped == 1
+    got = host(st)
+    for s in (1, 2, 4, 6, 7, 8):
+        np.testing.assert_array_equal(got[s], pool0[s])  # untouched slots keep their bits
+    assert_step(got, st_ref, "state pool")
+    yy = host(y)
+    assert np.all(yy[2] == 0.0)
+    assert_step(yy[[0, 1, 3]], y_ref[[0, 1, 3], 0], "y")
+
+
+def run_scan(lib, cfg, x, st, lo, hi, slots=None, pool=None, err=None):
+    N, H, S = cfg.n_seqs, cfg.n_v_heads, cfg.state_size
+    T = hi - lo
+    y = torch.zeros(N, T, H, S, device="cuda")
+    sl = lambda a: dev(a[:, lo:hi])  # noqa: E731
+    lib.gdn_recurrence_scan(st, sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["g"]), sl(x["beta"]), y,
+                            N, T, cfg.n_k_heads, H, S, cfg.scale, slots=slots, pool=pool,
+                            err_count=err)
+    return y
+
+
+@pytest.mark.parametrize("Hk,H,S,T", [(2, 4, 32, 16), (2, 4, 128, 37), (1, 2, 64, 5),
+                                      (2, 4, 256, 33)])
+def test_recurrence_scan(lib, Hk, H, S, T):
+    cfg, x, st0 = rec_case(Hk, H, S, N=2, T=T, seed=T + S)
+    st = dev(st0)
+    y = run_scan(lib, cfg, x, st, 0, T)
+    st_ref = f64(st0)
+    y_ref, _ = oracle.recurrence(st_ref, x["q"], x["k"], x["v"], x["g"], x["beta"], cfg.scale)
+    assert_step(host(y), y_ref, "y")
+    assert_step(host(st), st_ref, "final state")
+    # T decode calls agree with the scan bit for bit, and so does a split scan.
+    st_d = dev(st0)
+    for t in range(T):
+        yd = run_decode(lib, cfg, x, st_d, t)
+        np.testing.assert_array_equal(host(yd), host(y)[:, t])
+    np.testing.assert_array_equal(host(st_d), host(st))
+    st_s = dev(st0)
+    cut = T // 2
+    y1 = run_scan(lib, cfg, x, st_s, 0, cut)
+    y2 = run_scan(lib, cfg, x, st_s, cut, T)
+    np.testing.assert_array_equal(np.concatenate([host(y1), host(y2)], axis=1), host(y))
+    np.testing.assert_array_equal(host(st_s), host(st))
+
+
+def test_recurrence_scan_slots(lib):
+    cfg, x, _ = rec_case(2, 4, 128, N=3, T=20, seed=3, pool=5)
+    pool0 = I.state_pool(cfg)
+    slots = np.array([4, -1, 1], dtype=np.int32)
+    st = dev(pool0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = run_scan(lib, cfg, x, st, 0, 20, slots=dev(slots), pool=5, err=err)
+    assert host(err)[0] == 1
+    st_ref = f64(pool0)
+    y_ref, _ = oracle.recurrence(st_ref, x["q"], x["k"], x["v"], x["g"], x["beta"], cfg.scale,
+                                 slots=slots, pool=5)
+    got = host(st)
+    for s in (0, 2, 3):
+        np.testing.assert_array_equal(got[s], pool0[s])
+    assert_step(got, st_ref, "state pool")
+    assert_step(host(y)[[0, 2]], y_ref[[0, 2]], "y")
+
+
+@pytest.mark.slow
+def test_recurrence_scan_prefill_4x4096(lib):
+    """The long-scan workload at full size (N=4, T=4096, H=32, Hk=16, S=128),
+    checked on sampled (sequence, v-head) units against the oracle."""
+    cfg = I.get_config(2)
+    x = I.recurrence_batch(cfg)
+    st0 = I.state_pool(cfg)
+    st = dev(st0)
+    y = run_scan(lib, cfg, x, st, 0, cfg.n_tokens)
+    yh, sth = host(y), host(st)
+    assert np.all(np.isfinite(yh)) and np.all(np.isfinite(sth))
+    for n, vh in ((0, 0), (1, 17), (3, 31), (2, 8)):
+        kh = vh % cfg.n_k_heads
+        unit = {key: x[key][n:n + 1] for key in x}
+        unit["q"] = unit["q"][:, :, kh:kh + 1]
+        unit["k"] = unit["k"][:, :, kh:kh + 1]
+        unit["v"] = unit["v"][:, :, vh:vh + 1]
+        unit["g"] = unit["g"][:, :, vh:vh + 1]
+        unit["beta"] = unit["beta"][:, :, vh:vh + 1]
+        s_ref = f64(st0[n:n + 1, vh:vh + 1])
+        y_ref, _ = oracle.recurrence(s_ref, scale=cfg.scale, **unit)
+        assert_step(yh[n, :1, vh], y_ref[0, :1, 0], f"y token 0 ({n},{vh})")
+        assert_rms(yh[n, :, vh], y_ref[0, :, 0], f"y ({n},{vh})")
+        assert_rms(sth[n, vh], s_ref[0, 0], f"final state ({n},{vh})")
+
+
+# ------------------------------------------------------------------ fused block
+
+class BlockRun:
+    """Chained decode steps of the fused block on the GPU, with the oracle
+    following a subset of sequences in lockstep."""
+
+    def __init__(self, lib, cfg, sample):
+        self.lib, self.cfg, self.sample = lib, cfg, list(sample)
+        st = I.block_static(cfg)
+        self.static = st
+        self.slots = I.slots(cfg)
+        P = cfg.pool_size
+        self.state0 = I.state_pool(cfg)
+        self.conv0 = I.conv_state_pool(cfg)
+        self.state = dev(self.state0)
+        self.conv = dev(self.conv0)
+        self.d_static = {k: dev(v) for k, v in st.items()}
+        self.d_slots = dev(self.slots) if self.slots is not None else None
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ids = [self.slot_of(n) for n in self.sample]
+        self.ref_state = f64(self.state0[ids])
+        self.ref_conv = f64(self.conv0[ids])
+        self.P = P
+
+    def slot_of(self, n):
+        return int(self.slots[n]) if self.slots is not None else n
+
+    def step(self, step):
+        cfg = self.cfg
+        a = I.block_step(cfg, step)
+        out = torch.zeros(cfg.n_seqs, cfg.n_v_heads, cfg.state_size, device="cuda")
+        self.lib.gdn_block_decode(
+            dev(a["qkv"]), self.d_static["conv_w"], self.conv, dev(a["alpha"]), dev(a["b"]),
+            self.d_static["dt"], self.d_static["a"], dev(a["z"]), self.d_static["norm_w"],
+            self.state, out, cfg.n_seqs, cfg.n_k_heads, cfg.n_v_heads, cfg.state_size,
+            cfg.conv_kernel, cfg.scale, cfg.eps, cfg.eps, slots=self.d_slots, pool=self.P,
+            err_count=self.err)
+        s = self.sample
+        ref, skipped = oracle.block_decode(
+            a["qkv"][s], self.static["conv_w"], self.ref_conv, a["alpha"][s], a["b"][s],
+            self.static["dt"], self.static["a"], a["z"][s], self.static["norm_w"],
+            self.ref_state, cfg.n_k_heads, cfg.scale, cfg.eps, cfg.eps)
+        assert skipped == 0
+        return host(out), ref
+
+
+def check_block_chain(lib, cfg, sample, steps):
+    run = BlockRun(lib, cfg, sample)
+    for step in range(steps):
+        out, ref = run.step(step)
+        if step == 0:
+            assert_step(out[sample], ref, "out, first step")
+    assert_rms(out[sample], ref, f"out after {steps} steps")
+    ids = [run.slot_of(n) for n in sample]
+    assert_rms(host(run.state)[ids], run.ref_state, f"state after {steps} steps")
+    assert_rms(host(run.conv)[ids], run.ref_conv, f"conv_state after {steps} steps")
+    assert host(run.err)[0] == 0
+    return run
+
+
+def test_block_decode_tiny_chain(lib):
+    """The tiny workload (N=1, Hk=2, H=4, S=32), 16 chained steps, every step checked."""
+    cfg = I.get_config(0)
+    run = BlockRun(lib, cfg, [0])
+    for step in range(cfg.steps):
+        out, ref = run.step(step)
+        assert_step(out, ref, f"out step {step}")
+    assert_step(host(run.state), run.ref_state, "state")
+    assert_step(host(run.conv), run.ref_conv, "conv_state")
+
+
+@pytest.mark.parametrize("Hk,H,S,N", [(1, 1, 64, 2), (2, 8, 128, 3), (4, 4, 256, 2),
+                                      (1, 2, 32, 5)])
+def test_block_decode_shapes(lib, Hk, H, S, N):
+    cfg = I.get_config(0, n_k_heads=Hk, n_v_heads=H, state_size=S, n_seqs=N, cid=300 + S + H)
+    check_block_chain(lib, cfg, list(range(N)), steps=3)
+
+
+@pytest.mark.slow
+def test_block_decode_single_seq_1000(lib):
+    """Single-sequence decode at the verified shape, 1000 chained steps."""
+    cfg = I.get_config(1)
+    check_block_chain(lib, cfg, [0], steps=cfg.steps)
+
+
+@pytest.mark.slow
+def test_block_decode_batched_64(lib):
+    """Batched decode, 64 sequences, 200 chained steps; sampled sequences checked."""
+    cfg = I.get_config(3)
+    check_block_chain(lib, cfg, [0, 37, 63], steps=cfg.steps)
+
+
+@pytest.mark.slow
+def test_block_decode_serving_pool(lib):
+    """256 active slots of a 512-slot pool, 50 steps: sampled active slots match the
+    oracle and every untouched slot keeps its bits."""
+    cfg = I.get_config(4)
+    run = check_block_chain(lib, cfg, [0, 101, 255], steps=cfg.steps)
+    active = set(int(s) for s in run.slots)
+    untouched = torch.tensor(sorted(set(range(cfg.pool_size)) - active), device="cuda")
+    init_state = dev(run.state0)
+    init_conv = dev(run.conv0)
+    assert torch.equal(run.state.index_select(0, untouched), init_state.index_select(0, untouched))
+    assert torch.equal(run.conv.index_select(0, untouched), init_conv.index_select(0, untouched))
+
+
+def test_block_decode_invalid_slot(lib):
+    cfg = I.get_config(0, n_seqs=3, pool=4, cid=400)
+    run = BlockRun(lib, cfg, [0])
+    run.slots = np.array([2, 9, 0], dtype=np.int32)
+    run.d_slots = dev(run.slots)
+    a = I.block_step(cfg, 0)
+    out = torch.full((3, cfg.n_v_heads, cfg.state_size), 5.0, device="cuda")
+    lib.gdn_block_decode(dev(a["qkv"]), run.d_static["conv_w"], run.conv, dev(a["alpha"]),
+                         dev(a["b"]), run.d_static["dt"], run.d_static["a"], dev(a["z"]),
+                         run.d_static["norm_w"], run.state, out, 3, cfg.n_k_heads, cfg.n_v_heads,
+                         cfg.state_size, 4, cfg.scale, cfg.eps, cfg.eps, slots=run.d_slots,
+                         pool=4, err_count=run.err)
+    assert host(run.err)[0] == 1
+    assert np.all(host(out)[1] == 5.0)
+    np.testing.assert_array_equal(host(run.state)[[1, 3]], run.state0[[1, 3]])
+    np.testing.assert_array_equal(host(run.conv)[[1, 3]], run.conv0[[1, 3]])
+
+
+def test_block_equals_unfused_pipeline(lib):
+    """With a whole head per CTA (64 sequences), the fused block and the chain of
+    standalone kernels give the same bits."""
+    cfg = I.get_config(3)
+    N, Hk, H, S, C = cfg.n_seqs, cfg.n_k_heads, cfg.n_v_heads, cfg.state_size, cfg.conv_dim
+    st = I.block_static(cfg)
+    a = I.block_step(cfg, 0)
+    state0 = dev(np.random.default_rng(5).normal(0, 0.1, (N, H, S, S)).astype(np.float32))
+    conv0 = dev(np.random.default_rng(6).normal(0, 1, (N, C, 3)).astype(np.float32))
+    d = {k: dev(v) for k, v in {**st, **a}.items()}
+    # fused
+    st_f, cv_f = state0.clone(), conv0.clone()
+    out_f = torch.empty(N, H, S, device="cuda")
+    lib.gdn_block_decode(d["qkv"], d["conv_w"], cv_f, d["alpha"], d["b"], d["dt"], d["a"], d["z"],
+                         d["norm_w"], st_f, out_f, N, Hk, H, S, 4, cfg.scale, cfg.eps, cfg.eps)
+    # unfused
+    st_u, cv_u = state0.clone(), conv0.clone()
+    conv_out = torch.empty(N, C, device="cuda")
+    lib.gdn_conv1d_silu(d["qkv"], d["conv_w"], cv_u, conv_out, N, C, 4)
+    q = torch.empty(N, Hk, S, device="cuda")
+    k = torch.empty_like(q)
+    v = torch.empty(N, H, S, device="cuda")
+    lib.gdn_qkv_split_norm(conv_out, q, k, v, N, Hk, H, S, cfg.eps)
+    g = torch.empty(N, H, device="cuda")
+    lib.gdn_decay_gate(d["alpha"], d["dt"], d["a"], g, H, N)
+    beta = torch.empty(N, H, device="cuda")
+    lib.gdn_beta_sigmoid(d["b"], beta, N * H)
+    y = torch.empty(N, H, S, device="cuda")
+    lib.gdn_recurrence_decode(st_u, q, k, v, g, beta, y, N, Hk, H, S, cfg.scale)
+    out_u = torch.empty_like(y)
+    lib.gdn_gated_norm(y, d["norm_w"], d["z"], out_u, N * H, S, cfg.eps)
+    torch.cuda.synchronize()
+    assert torch.equal(cv_f, cv_u)
+    assert torch.equal(st_f, st_u)
+    assert torch.equal(out_f, out_u)
