@@ -229,6 +229,7 @@ __global__ void __launch_bounds__(kThreads) block_decode_kernel(const BlockParam
         ss = warp_allsum(ss);
         if (lane == 0) scal[4] = ss;
     }
+    __syncthreads();         // the partial is visible to every warp of this CTA
     cluster_wait_acquire();  // phase 1 complete: every CTA has read the old q/k history
     float ss_total;
     if (p.split > 1) {

@@ -76,8 +76,10 @@ CONFIGS = {
 }
 
 
-def get_config(cid, **overrides):
-    cfg = CONFIGS[cid]
+def get_config(which, **overrides):
+    """One of the five workloads, optionally with fields replaced (a new `cid`
+    gives the variant its own seeds)."""
+    cfg = CONFIGS[which]
     return replace(cfg, **overrides) if overrides else cfg
 
 
