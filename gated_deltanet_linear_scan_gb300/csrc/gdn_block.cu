@@ -266,6 +266,312 @@ __global__ void __launch_bounds__(kThreads) block_decode_kernel(const BlockParam
     if (p.split > 1) cluster_wait_acquire();  // keep shared memory alive for remote readers
 }
 
+// ============================================================================ persistent form
+// For many sequences the cluster-per-group kernel leaves HBM idle between a CTA's
+// load, compute and store phases. The persistent form keeps one CTA per SM alive
+// for the whole step: each CTA owns whole (sequence, k-head) groups (so it alone
+// reads and rolls the group's q/k history, no cluster needed), a producer warp
+// streams the group's state in units of 64 rows through a ring of shared-memory
+// stages with bulk copies (full/empty mbarriers) and prefetches the next group's
+// qkv, conv history, conv weights and z, and 16 consumer warps run the prologue,
+// the row steps and the gated RMSNorm. The state stream never waits on the
+// per-group prologue or epilogue.
+constexpr int kPWarps = 16;                  // consumer warps
+constexpr int kPThreads = (kPWarps + 1) * 32;
+constexpr int kPUnitRows = kPWarps * kR;     // 64 state rows per ring stage
+constexpr int kPMaxStages = 8;
+constexpr int kPSmemBudget = 227 * 1024;
+
+struct PLayout {
+    int S, r, stages;
+    size_t unit_bytes, gbuf_bytes, ring, gbuf0, gbuf1, carea, bars, total;
+    __host__ __device__ PLayout(int S_, int r_, int stages_) : S(S_), r(r_), stages(stages_) {
+        unit_bytes = static_cast<size_t>(kPUnitRows) * S * sizeof(float);
+        // per group: qkv slices, conv history, conv weights of the 2 + r channel
+        // slices (q, k, one v per head), and z of the r heads
+        gbuf_bytes = static_cast<size_t>((2 + r) * S * 8 + r * S) * sizeof(float);
+        ring = 0;
+        gbuf0 = ring + stages * unit_bytes;
+        gbuf1 = gbuf0 + gbuf_bytes;
+        carea = gbuf1 + gbuf_bytes;
+        // consumer area: raw q and k, v, y, scalars
+        bars = carea + static_cast<size_t>(2 * S + 2 * r * S + 64) * sizeof(float);
+        // sfull[stages], sempty[stages], gfull[2], gempty[2]; then per-stage and
+        // per-buffer issue counts and the abort flag
+        total = bars + (2 * stages + 4) * sizeof(uint64_t) + (stages + 3) * sizeof(int);
+    }
+};
+
+// First conv channel of slice 0 = q of kh, 1 = k of kh, 2 + rr = v of v-head rr*Hk + kh.
+__host__ __device__ inline size_t p_channel0(int slice, int kh, int S, int Hk) {
+    const size_t key_dim = static_cast<size_t>(Hk) * S;
+    if (slice == 0) return static_cast<size_t>(kh) * S;
+    if (slice == 1) return key_dim + static_cast<size_t>(kh) * S;
+    return 2 * key_dim + (static_cast<size_t>(slice - 2) * Hk + kh) * S;
+}
+
+template <int E>
+__global__ void __launch_bounds__(kPThreads, 1) block_decode_persistent_kernel(const BlockParams p,
+                                                                               int n_groups,
+                                                                               int stages) {
+    constexpr int S = 32 * E;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int r = p.ratio;
+    const PLayout L(S, r, stages);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int Hk = p.n_k_heads, H = p.n_v_heads;
+    const size_t conv_dim = static_cast<size_t>(2 * Hk * S + H * S);
+    const int n_slices = 2 + r;
+    const int units_per_head = S / kPUnitRows;
+    const int units_per_group = r * units_per_head;
+
+    uint64_t *sfull = reinterpret_cast<uint64_t *>(smem_raw + L.bars);
+    uint64_t *sempty = sfull + stages;
+    uint64_t *gfull = sempty + stages;
+    uint64_t *gempty = gfull + 2;
+    int *s_issued = reinterpret_cast<int *>(gempty + 2);  // [stages] uses issued per stage
+    int *g_issued = s_issued + stages;                     // [2], then the abort flag
+    float *QH = reinterpret_cast<float *>(smem_raw + L.carea);
+    float *KH = QH + S;
+    float *V = KH + S;
+    float *Y = V + r * S;
+    float *SC = Y + r * S;  // [0,r) decay, [r,2r) beta, 2r inv_q, 2r+1 inv_k, [2r+2, 3r+2) inv_rms
+
+    if (tid == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(sfull + i, 1);
+            mbar_init(sempty + i, kPWarps);
+            s_issued[i] = 0;
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(gfull + i, 1);
+            mbar_init(gempty + i, kPWarps);
+            g_issued[i] = 0;
+        }
+        g_issued[2] = 0;  // abort flag
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto slot_of = [&](int n) { return p.slots ? p.slots[n] : n; };
+    auto valid_slot = [&](int slot) { return slot >= 0 && slot < p.pool; };
+    // A wait that gives up raises the watchdog flag and sets `abort`; from then on
+    // every thread skips its remaining waits and work but still passes every
+    // barrier, so the CTA always runs to its end.
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(g_issued + 2);
+    auto give_up = [&](unsigned bit) {
+        if (lane == 0) atomicOr(&g_watchdog, bit);
+        *abort_flag = 1;
+    };
+
+    if (warp == kPWarps) {
+        // ------------------------------------------------------------ producer warp
+        int unit = 0, gi = 0;
+        for (int g = blockIdx.x; g < n_groups && !*abort_flag; g += gridDim.x) {
+            const int n = g / Hk, kh = g % Hk;
+            const int slot = slot_of(n);
+            if (!valid_slot(slot)) continue;
+            const int gb = gi & 1, guse = gi >> 1;
+            ++gi;
+            if (guse > 0 && !mbar_wait(gempty + gb, (guse - 1) & 1)) {
+                give_up(WD_STAGE_FREE);
+                break;
+            }
+            float *gbuf = reinterpret_cast<float *>(smem_raw + (gb ? L.gbuf1 : L.gbuf0));
+            float *X = gbuf, *Hh = X + n_slices * S, *W = Hh + 3 * n_slices * S;
+            float *Z = W + 4 * n_slices * S;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(gfull + gb, static_cast<uint32_t>(L.gbuf_bytes));
+                g_issued[gb] = guse + 1;
+            }
+            __syncwarp();
+            const int n_copies = 3 * n_slices + r;
+            for (int c = lane; c < n_copies; c += 32) {
+                if (c < n_slices) {
+                    bulk_g2s(X + c * S, p.qkv + n * conv_dim + p_channel0(c, kh, S, Hk),
+                             S * sizeof(float), gfull + gb);
+                } else if (c < 2 * n_slices) {
+                    const int sl = c - n_slices;
+                    bulk_g2s(Hh + sl * 3 * S,
+                             p.conv_state + (slot * conv_dim + p_channel0(sl, kh, S, Hk)) * kTaps,
+                             3 * S * sizeof(float), gfull + gb);
+                } else if (c < 3 * n_slices) {
+                    const int sl = c - 2 * n_slices;
+                    bulk_g2s(W + sl * 4 * S, p.conv_w + p_channel0(sl, kh, S, Hk) * 4,
+                             4 * S * sizeof(float), gfull + gb);
+                } else {
+                    const int rr = c - 3 * n_slices;
+                    bulk_g2s(Z + rr * S, p.z + (static_cast<size_t>(n) * H + rr * Hk + kh) * S,
+                             S * sizeof(float), gfull + gb);
+                }
+            }
+            for (int u = 0; u < units_per_group; ++u, ++unit) {
+                const int st = unit % stages, use = unit / stages;
+                if (use > 0 && (*abort_flag || !mbar_wait(sempty + st, (use - 1) & 1))) {
+                    give_up(WD_STAGE_FREE);
+                    break;
+                }
+                if (lane == 0) {
+                    const int rr = u / units_per_head, row0 = (u % units_per_head) * kPUnitRows;
+                    const float *src =
+                        p.state + ((static_cast<size_t>(slot) * H + rr * Hk + kh) * S + row0) * S;
+                    mbar_arrive_expect_tx(sfull + st, static_cast<uint32_t>(L.unit_bytes));
+                    bulk_g2s(smem_raw + L.ring + st * L.unit_bytes, src,
+                             static_cast<uint32_t>(L.unit_bytes), sfull + st);
+                    s_issued[st] = use + 1;
+                }
+                __syncwarp();
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumer warps
+        const int ctid = tid;  // 0 .. 16*32-1
+        int unit = 0, gi = 0;
+        // gate inputs of the next group, prefetched into registers by threads < r
+        float nx_alpha = 0.f, nx_b = 0.f, nx_dt = 0.f, nx_a = 0.f;
+        auto fetch_gate = [&](int g) {
+            if (ctid < r && g < n_groups) {
+                const int n = g / Hk, kh = g % Hk, vh = ctid * Hk + kh;
+                nx_alpha = p.alpha[static_cast<size_t>(n) * H + vh];
+                nx_b = p.b[static_cast<size_t>(n) * H + vh];
+                nx_dt = p.dt[vh];
+                nx_a = p.a[vh];
+            }
+        };
+        fetch_gate(blockIdx.x);
+        int yr;
+        const bool writer = [&] {
+            yr = ((lane >> 4) & 1) | (((lane >> 3) & 1) << 1);
+            return (lane & 7) == 0;
+        }();
+        for (int g = blockIdx.x; g < n_groups; g += gridDim.x) {
+            const int n = g / Hk, kh = g % Hk;
+            const int slot = slot_of(n);
+            const float cur_alpha = nx_alpha, cur_b = nx_b, cur_dt = nx_dt, cur_a = nx_a;
+            fetch_gate(g + gridDim.x);  // the next group this CTA processes
+            if (!valid_slot(slot)) {
+                if (ctid == 0 && kh == 0 && p.err_count) atomicAdd(p.err_count, 1);
+                continue;  // uniform over all consumer warps
+            }
+            const int gb = gi & 1, guse = gi >> 1;
+            ++gi;
+            bool live = !*abort_flag;
+            if (live && !mbar_wait(gfull + gb, guse & 1)) {
+                give_up(WD_STAGE_COPY);
+                live = false;
+            }
+            const float *gbuf = reinterpret_cast<const float *>(smem_raw + (gb ? L.gbuf1 : L.gbuf0));
+            const float *X = gbuf, *Hh = X + n_slices * S, *W = Hh + 3 * n_slices * S;
+            const float *Z = W + 4 * n_slices * S;
+
+            // prologue: conv1d+SiLU of the group's channels, rolling their history
+            if (live) {
+                for (int c = ctid; c < n_slices * S; c += kPWarps * 32) {
+                    const float x = X[c];
+                    const float h0 = Hh[3 * c], h1 = Hh[3 * c + 1], h2 = Hh[3 * c + 2];
+                    const float4 w = *reinterpret_cast<const float4 *>(W + 4 * c);
+                    const float val = conv_channel(x, w, h0, h1, h2);
+                    if (c < 2 * S) QH[c] = val;  // QH and KH are adjacent
+                    else V[c - 2 * S] = val;
+                    float *hs = p.conv_state +
+                                (slot * conv_dim + p_channel0(c / S, kh, S, Hk) + (c % S)) * kTaps;
+                    hs[0] = h1; hs[1] = h2; hs[2] = x;
+                }
+                if (ctid < r) {
+                    SC[ctid] = expf(cur_a * softplus_guarded(cur_alpha + cur_dt));
+                    SC[r + ctid] = 1.0f / (1.0f + expf(-cur_b));
+                }
+            }
+            named_barrier_sync(1, kPWarps * 32);
+            if (live && warp < 2) {  // x / max(||x||, eps) for q (warp 0) and k (warp 1)
+                float xv[E];
+                load_vec<E>(xv, QH + warp * S + lane * E);
+                float ss = 0.0f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) ss = __fmaf_rn(xv[e], xv[e], ss);
+                ss = warp_allsum(ss);
+                if (lane == 0) SC[2 * r + warp] = 1.0f / fmaxf(sqrtf(ss), p.l2_eps);
+            }
+            named_barrier_sync(1, kPWarps * 32);
+            float kk[E], qq[E];
+            load_vec<E>(qq, QH + lane * E);
+            load_vec<E>(kk, KH + lane * E);
+            {
+                const float inv_q = SC[2 * r], inv_k = SC[2 * r + 1];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    qq[e] *= inv_q;
+                    kk[e] *= inv_k;
+                }
+            }
+
+            // the state stream: 64 rows per stage, 4 per warp
+            for (int u = 0; u < units_per_group; ++u, ++unit) {
+                const int st = unit % stages, use = unit / stages;
+                if (live && (*abort_flag || !mbar_wait(sfull + st, use & 1))) {
+                    give_up(WD_STATE_COPY);
+                    live = false;
+                }
+                if (live) {
+                    const int rr = u / units_per_head;
+                    const int j0 = (u % units_per_head) * kPUnitRows + warp * kR;
+                    const int vh = rr * Hk + kh;
+                    const float *tile =
+                        reinterpret_cast<const float *>(smem_raw + L.ring + st * L.unit_bytes) +
+                        warp * kR * S;
+                    float row[kR][E], vv[kR];
+#pragma unroll
+                    for (int q = 0; q < kR; ++q) {
+                        load_vec<E>(row[q], tile + q * S + lane * E);
+                        vv[q] = V[rr * S + j0 + q];
+                    }
+                    const float ysum = row_step<E, kR>(row, kk, qq, vv, SC[rr], SC[r + rr], lane);
+                    float *gst = p.state + ((static_cast<size_t>(slot) * H + vh) * S + j0) * S;
+#pragma unroll
+                    for (int q = 0; q < kR; ++q) store_vec<E>(gst + q * S + lane * E, row[q]);
+                    if (writer) Y[rr * S + j0 + yr] = __fmul_rn(p.scale, ysum);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sempty + st);
+            }
+
+            // gated RMSNorm of the group's r heads
+            named_barrier_sync(1, kPWarps * 32);
+            if (live && warp < r) {
+                float yv[E];
+                load_vec<E>(yv, Y + warp * S + lane * E);
+                float ss = 0.0f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) ss = __fmaf_rn(yv[e], yv[e], ss);
+                ss = warp_allsum(ss);
+                if (lane == 0) SC[2 * r + 2 + warp] = 1.0f / sqrtf(ss / static_cast<float>(S) + p.norm_eps);
+            }
+            named_barrier_sync(1, kPWarps * 32);
+            if (live && !*abort_flag) {
+                for (int idx = ctid; idx < r * S; idx += kPWarps * 32) {
+                    const int rr = idx / S, j = idx % S;
+                    const float zv = Z[idx];
+                    p.out[(static_cast<size_t>(n) * H + rr * Hk + kh) * S + j] =
+                        Y[idx] * SC[2 * r + 2 + rr] * p.norm_w[j] * silu(zv);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(gempty + gb);
+            // the next prologue rewrites the consumer area: every warp first finishes
+            // reading this group's values
+            named_barrier_sync(1, kPWarps * 32);
+        }
+    }
+    // Never leave while a bulk copy may still be landing in shared memory.
+    __syncthreads();
+    if (tid == 0) {
+        for (int i = 0; i < stages; ++i)
+            if (s_issued[i] > 0) mbar_wait(sfull + i, (s_issued[i] - 1) & 1);
+        for (int i = 0; i < 2; ++i)
+            if (g_issued[i] > 0) mbar_wait(gfull + i, (g_issued[i] - 1) & 1);
+    }
+}
+
 int sm_count() {
     static std::atomic<int> cached{0};
     int v = cached.load();
@@ -279,9 +585,40 @@ int sm_count() {
     return v;
 }
 
+// Persistent form: one CTA per SM when there are at least two (sequence, k-head)
+// groups per SM and the ring of 64-row stages fits in shared memory.
+template <int E>
+gdn_status launch_block_persistent(BlockParams p, int n_seqs, cudaStream_t s, bool &used) {
+    constexpr int S = 32 * E;
+    static_assert(S == 64 || S == 128, "the persistent form streams 64-row stages");
+    used = false;
+    const int ratio = p.n_v_heads / p.n_k_heads;
+    const long long groups = static_cast<long long>(n_seqs) * p.n_k_heads;
+    const int sms = sm_count();
+    if (groups < 2LL * sms || groups > 0x7fffffffLL) return GDN_OK;
+    int stages = kPMaxStages;
+    while (stages >= 2 && PLayout(S, ratio, stages).total > static_cast<size_t>(kPSmemBudget)) --stages;
+    if (stages < 2) return GDN_OK;
+    p.ratio = ratio;
+    p.split = 1;
+    const size_t smem = PLayout(S, ratio, stages).total;
+    if (cudaFuncSetAttribute(block_decode_persistent_kernel<E>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    used = true;
+    block_decode_persistent_kernel<E><<<sms, kPThreads, smem, s>>>(p, static_cast<int>(groups), stages);
+    return launch_status();
+}
+
 template <int E>
 gdn_status launch_block(BlockParams p, int n_seqs, cudaStream_t s) {
     constexpr int S = 32 * E;
+    if constexpr (E == 2 || E == 4) {
+        bool used = false;
+        const gdn_status pst = launch_block_persistent<E>(p, n_seqs, s, used);
+        if (used || pst != GDN_OK) return pst;
+    }
     const int ratio = p.n_v_heads / p.n_k_heads;
     // Smallest split that keeps the tile within shared memory, doubled while the
     // grid is short of two CTAs per SM; a CTA keeps at least 32 rows and a

@@ -88,6 +88,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Barrier `id` over `count` threads (a multiple of 32), leaving the other warps
+// of the CTA free to run.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---- thread-block clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

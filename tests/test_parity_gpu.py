@@ -370,6 +370,45 @@ def test_block_decode_shapes(lib, Hk, H, S, N):
     check_block_chain(lib, cfg, list(range(N)), steps=3)
 
 
+@pytest.mark.parametrize("Hk,H,S,N", [(16, 32, 128, 20), (8, 16, 64, 40), (16, 16, 128, 20),
+                                      (4, 16, 128, 80)])
+def test_block_decode_persistent_shapes(lib, Hk, H, S, N):
+    """At least two (sequence, k-head) groups per SM: the persistent form runs."""
+    cfg = I.get_config(0, n_k_heads=Hk, n_v_heads=H, state_size=S, n_seqs=N, cid=500 + S + H + N)
+    check_block_chain(lib, cfg, [0, N // 2, N - 1], steps=3)
+
+
+def test_block_decode_persistent_invalid_slot(lib):
+    cfg = I.get_config(3, n_seqs=20, pool=24, cid=600)
+    run = BlockRun(lib, cfg, [0])
+    slots = np.arange(20, dtype=np.int32) + 2
+    slots[7] = 99  # out of range: skipped, counted, untouched
+    run.slots, run.d_slots = slots, dev(slots)
+    a = I.block_step(cfg, 0)
+    out = torch.full((20, cfg.n_v_heads, cfg.state_size), 5.0, device="cuda")
+    lib.gdn_block_decode(dev(a["qkv"]), run.d_static["conv_w"], run.conv, dev(a["alpha"]),
+                         dev(a["b"]), run.d_static["dt"], run.d_static["a"], dev(a["z"]),
+                         run.d_static["norm_w"], run.state, out, 20, cfg.n_k_heads, cfg.n_v_heads,
+                         cfg.state_size, 4, cfg.scale, cfg.eps, cfg.eps, slots=run.d_slots,
+                         pool=24, err_count=run.err)
+    assert host(run.err)[0] == 1
+    o = host(out)
+    assert np.all(o[7] == 5.0) and np.all(np.isfinite(o))
+    st, cv = host(run.state), host(run.conv)
+    for sl in (0, 1, 9):  # slot 9 belonged to the skipped sequence
+        np.testing.assert_array_equal(st[sl], run.state0[sl])
+        np.testing.assert_array_equal(cv[sl], run.conv0[sl])
+    # a valid sequence matches the oracle
+    ref_st = f64(run.state0[slots[3]:slots[3] + 1])
+    ref_cv = f64(run.conv0[slots[3]:slots[3] + 1])
+    ref, _ = oracle.block_decode(a["qkv"][3:4], run.static["conv_w"], ref_cv, a["alpha"][3:4],
+                                 a["b"][3:4], run.static["dt"], run.static["a"], a["z"][3:4],
+                                 run.static["norm_w"], ref_st, cfg.n_k_heads, cfg.scale, cfg.eps,
+                                 cfg.eps)
+    assert_step(o[3:4], ref, "out")
+    assert_step(st[slots[3]:slots[3] + 1], ref_st, "state")
+
+
 @pytest.mark.slow
 def test_block_decode_single_seq_1000(lib):
     """Single-sequence decode at the verified shape, 1000 chained steps."""
