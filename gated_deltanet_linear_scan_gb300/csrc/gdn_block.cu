@@ -269,36 +269,52 @@ __global__ void __launch_bounds__(kThreads) block_decode_kernel(const BlockParam
 // ============================================================================ persistent form
 // For many sequences the cluster-per-group kernel leaves HBM idle between a CTA's
 // load, compute and store phases. The persistent form keeps one CTA per SM alive
-// for the whole step: each CTA owns whole (sequence, k-head) groups (so it alone
-// reads and rolls the group's q/k history, no cluster needed), a producer warp
-// streams the group's state in units of 64 rows through a ring of shared-memory
-// stages with bulk copies (full/empty mbarriers) and prefetches the next group's
-// qkv, conv history, conv weights and z, and 16 consumer warps run the prologue,
-// the row steps and the gated RMSNorm. The state stream never waits on the
-// per-group prologue or epilogue.
-constexpr int kPWarps = 16;                  // consumer warps
-constexpr int kPThreads = (kPWarps + 1) * 32;
-constexpr int kPUnitRows = kPWarps * kR;     // 64 state rows per ring stage
+// for the whole step. Each CTA owns whole (sequence, k-head) groups, so it alone
+// reads and rolls a group's q/k history (no cluster needed). Its warps have fixed
+// roles and talk only through mbarriers, so no role ever waits at a CTA-wide
+// barrier for another:
+//   producer  (1 warp)  streams each group's state in units of 64 rows through a
+//             ring of shared-memory stages (bulk copies, full/empty barriers) and
+//             fetches the next group's qkv, conv history, conv weights and z into
+//             a double buffer;
+//   prologue  (4 warps) conv1d+SiLU of the group's channel slices (q and k, each
+//             with its L2 norm, and one v slice per head) plus the gate and
+//             beta, rolling the conv history, ahead of the row steps;
+//   rows      (16 warps) the row steps, 4 rows per warp per unit;
+//   epilogue  (2 warps) the gated RMSNorm of the finished group, a head each.
+// Per-group operands and values rotate through three buffers: the producer refills
+// buffer i%3 for group i once the epilogue of group i-3 has released it, so unit
+// loads never wait on a recent group's prologue or epilogue.
+constexpr int kPRowWarps = 16;
+constexpr int kPProWarps = 4;
+constexpr int kPEpiWarps = 2;
+constexpr int kPProducer = kPRowWarps;      // warp index of the first warp of each role
+constexpr int kPPro0 = kPRowWarps + 1;
+constexpr int kPEpi0 = kPPro0 + kPProWarps;
+constexpr int kPThreads = (kPRowWarps + 1 + kPProWarps + kPEpiWarps) * 32;
+constexpr int kPUnitRows = kPRowWarps * kR;  // 64 state rows per ring stage
 constexpr int kPMaxStages = 8;
+constexpr int kPBufs = 3;  // depth of the per-group operand buffers and slots
 constexpr int kPSmemBudget = 227 * 1024;
 
 struct PLayout {
     int S, r, stages;
-    size_t unit_bytes, gbuf_bytes, ring, gbuf0, gbuf1, carea, bars, total;
+    size_t unit_bytes, gbuf_bytes, slot_floats, ring, gbuf, slot, bars, total;
     __host__ __device__ PLayout(int S_, int r_, int stages_) : S(S_), r(r_), stages(stages_) {
         unit_bytes = static_cast<size_t>(kPUnitRows) * S * sizeof(float);
         // per group: qkv slices, conv history, conv weights of the 2 + r channel
         // slices (q, k, one v per head), and z of the r heads
         gbuf_bytes = static_cast<size_t>((2 + r) * S * 8 + r * S) * sizeof(float);
+        // per group slot: q^, k^ (normalised), v, y, decay, beta (padded to 16 B)
+        slot_floats = (static_cast<size_t>(2 * S + 2 * r * S + 2 * r) + 3) / 4 * 4;
         ring = 0;
-        gbuf0 = ring + stages * unit_bytes;
-        gbuf1 = gbuf0 + gbuf_bytes;
-        carea = gbuf1 + gbuf_bytes;
-        // consumer area: raw q and k, v, y, scalars
-        bars = carea + static_cast<size_t>(2 * S + 2 * r * S + 64) * sizeof(float);
-        // sfull[stages], sempty[stages], gfull[2], gempty[2]; then per-stage and
-        // per-buffer issue counts and the abort flag
-        total = bars + (2 * stages + 4) * sizeof(uint64_t) + (stages + 3) * sizeof(int);
+        gbuf = ring + stages * unit_bytes;
+        slot = gbuf + kPBufs * gbuf_bytes;
+        bars = slot + kPBufs * slot_floats * sizeof(float);
+        // sfull/sempty[stages], gfull/gempty/cfull/yfull/cfree[kPBufs]; then the
+        // per-stage and per-buffer issue counts and the abort flag
+        total = bars + (2 * stages + 5 * kPBufs) * sizeof(uint64_t) +
+                (stages + kPBufs + 1) * sizeof(int);
     }
 };
 
@@ -308,6 +324,26 @@ __host__ __device__ inline size_t p_channel0(int slice, int kh, int S, int Hk) {
     if (slice == 0) return static_cast<size_t>(kh) * S;
     if (slice == 1) return key_dim + static_cast<size_t>(kh) * S;
     return 2 * key_dim + (static_cast<size_t>(slice - 2) * Hk + kh) * S;
+}
+
+// Conv1d+SiLU of E consecutive channels held by one lane (buffers in shared memory:
+// x [E], history [3E], weights [4E]); writes the rolled history of those channels
+// (3E consecutive floats) to global memory.
+template <int E>
+__device__ __forceinline__ void p_conv_lane(const float *X, const float *Hh, const float *W,
+                                            float *hist_out, float (&val)[E]) {
+    float x[E], h[3 * E];
+    load_vec<E>(x, X);
+    load_vec<3 * E>(h, Hh);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float4 w = *reinterpret_cast<const float4 *>(W + 4 * e);
+        val[e] = conv_channel(x[e], w, h[3 * e], h[3 * e + 1], h[3 * e + 2]);
+        h[3 * e] = h[3 * e + 1];
+        h[3 * e + 1] = h[3 * e + 2];
+        h[3 * e + 2] = x[e];
+    }
+    store_vec<3 * E>(hist_out, h);
 }
 
 template <int E>
@@ -328,89 +364,105 @@ __global__ void __launch_bounds__(kPThreads, 1) block_decode_persistent_kernel(c
     uint64_t *sfull = reinterpret_cast<uint64_t *>(smem_raw + L.bars);
     uint64_t *sempty = sfull + stages;
     uint64_t *gfull = sempty + stages;
-    uint64_t *gempty = gfull + 2;
-    int *s_issued = reinterpret_cast<int *>(gempty + 2);  // [stages] uses issued per stage
-    int *g_issued = s_issued + stages;                     // [2], then the abort flag
-    float *QH = reinterpret_cast<float *>(smem_raw + L.carea);
-    float *KH = QH + S;
-    float *V = KH + S;
-    float *Y = V + r * S;
-    float *SC = Y + r * S;  // [0,r) decay, [r,2r) beta, 2r inv_q, 2r+1 inv_k, [2r+2, 3r+2) inv_rms
+    uint64_t *gempty = gfull + kPBufs;
+    uint64_t *cfull = gempty + kPBufs;   // prologue -> row warps
+    uint64_t *yfull = cfull + kPBufs;    // row warps -> epilogue
+    uint64_t *cfree = yfull + kPBufs;    // epilogue -> prologue
+    int *s_issued = reinterpret_cast<int *>(cfree + kPBufs);  // [stages] uses issued per stage
+    int *g_issued = s_issued + stages;                         // [kPBufs], then the abort flag
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(g_issued + kPBufs);
 
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) {
             mbar_init(sfull + i, 1);
-            mbar_init(sempty + i, kPWarps);
+            mbar_init(sempty + i, kPRowWarps);
             s_issued[i] = 0;
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kPBufs; ++i) {
             mbar_init(gfull + i, 1);
-            mbar_init(gempty + i, kPWarps);
+            mbar_init(gempty + i, kPProWarps + kPEpiWarps);
+            mbar_init(cfull + i, kPProWarps);
+            mbar_init(yfull + i, kPRowWarps);
+            mbar_init(cfree + i, kPEpiWarps);
             g_issued[i] = 0;
         }
-        g_issued[2] = 0;  // abort flag
+        *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
-    auto slot_of = [&](int n) { return p.slots ? p.slots[n] : n; };
-    auto valid_slot = [&](int slot) { return slot >= 0 && slot < p.pool; };
-    // A wait that gives up raises the watchdog flag and sets `abort`; from then on
-    // every thread skips its remaining waits and work but still passes every
-    // barrier, so the CTA always runs to its end.
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(g_issued + 2);
-    auto give_up = [&](unsigned bit) {
+    // A wait that gives up raises the watchdog flag and sets `abort`; every role
+    // then leaves its loop, and all threads meet at the final barrier.
+    auto wait = [&](uint64_t *bar, int parity, unsigned bit) {
+        if (*abort_flag) return false;
+        if (mbar_wait(bar, parity & 1)) return true;
         if (lane == 0) atomicOr(&g_watchdog, bit);
         *abort_flag = 1;
+        return false;
     };
+    auto slot_of = [&](int n) { return p.slots ? p.slots[n] : n; };
+    auto valid_slot = [&](int slot) { return slot >= 0 && slot < p.pool; };
+    auto gbuf_at = [&](int gb) { return reinterpret_cast<float *>(smem_raw + L.gbuf + gb * L.gbuf_bytes); };
+    auto slot_at = [&](int cs) {
+        return reinterpret_cast<float *>(smem_raw + L.slot + cs * L.slot_floats * sizeof(float));
+    };
+    // slot layout
+    auto QH = [&](float *c) { return c; };
+    auto KH = [&](float *c) { return c + S; };
+    auto VV = [&](float *c) { return c + 2 * S; };
+    auto YY = [&](float *c) { return c + 2 * S + r * S; };
+    auto DEC = [&](float *c) { return c + 2 * S + 2 * r * S; };
+    auto BET = [&](float *c) { return c + 2 * S + 2 * r * S + r; };
 
-    if (warp == kPWarps) {
-        // ------------------------------------------------------------ producer warp
-        int unit = 0, gi = 0;
-        for (int g = blockIdx.x; g < n_groups && !*abort_flag; g += gridDim.x) {
-            const int n = g / Hk, kh = g % Hk;
-            const int slot = slot_of(n);
-            if (!valid_slot(slot)) continue;
-            const int gb = gi & 1, guse = gi >> 1;
-            ++gi;
-            if (guse > 0 && !mbar_wait(gempty + gb, (guse - 1) & 1)) {
-                give_up(WD_STAGE_FREE);
-                break;
-            }
-            float *gbuf = reinterpret_cast<float *>(smem_raw + (gb ? L.gbuf1 : L.gbuf0));
-            float *X = gbuf, *Hh = X + n_slices * S, *W = Hh + 3 * n_slices * S;
-            float *Z = W + 4 * n_slices * S;
+    int gi = 0;  // index of the valid group, shared by all roles
+    for (int g = blockIdx.x; g < n_groups; g += gridDim.x) {
+        const int n = g / Hk, kh = g % Hk;
+        const int slot = slot_of(n);
+        if (!valid_slot(slot)) {
+            if (warp == kPPro0 && lane == 0 && kh == 0 && p.err_count) atomicAdd(p.err_count, 1);
+            continue;
+        }
+        const int use = gi / kPBufs, b = gi % kPBufs;  // gbuf and group slot rotate together
+        ++gi;
+        if (*abort_flag) break;
+        float *gbuf = gbuf_at(b);
+        float *X = gbuf, *Hh = X + n_slices * S, *W = Hh + 3 * n_slices * S;
+        float *Z = W + 4 * n_slices * S;
+        float *cslot = slot_at(b);
+
+        if (warp == kPProducer) {
+            // -------------------------------------------------------- producer
+            if (use > 0 && !wait(gempty + b, use - 1, WD_STAGE_FREE)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(gfull + gb, static_cast<uint32_t>(L.gbuf_bytes));
-                g_issued[gb] = guse + 1;
+                mbar_arrive_expect_tx(gfull + b, static_cast<uint32_t>(L.gbuf_bytes));
+                g_issued[b] = use + 1;
             }
             __syncwarp();
             const int n_copies = 3 * n_slices + r;
             for (int c = lane; c < n_copies; c += 32) {
                 if (c < n_slices) {
                     bulk_g2s(X + c * S, p.qkv + n * conv_dim + p_channel0(c, kh, S, Hk),
-                             S * sizeof(float), gfull + gb);
+                             S * sizeof(float), gfull + b);
                 } else if (c < 2 * n_slices) {
                     const int sl = c - n_slices;
                     bulk_g2s(Hh + sl * 3 * S,
                              p.conv_state + (slot * conv_dim + p_channel0(sl, kh, S, Hk)) * kTaps,
-                             3 * S * sizeof(float), gfull + gb);
+                             3 * S * sizeof(float), gfull + b);
                 } else if (c < 3 * n_slices) {
                     const int sl = c - 2 * n_slices;
                     bulk_g2s(W + sl * 4 * S, p.conv_w + p_channel0(sl, kh, S, Hk) * 4,
-                             4 * S * sizeof(float), gfull + gb);
+                             4 * S * sizeof(float), gfull + b);
                 } else {
                     const int rr = c - 3 * n_slices;
                     bulk_g2s(Z + rr * S, p.z + (static_cast<size_t>(n) * H + rr * Hk + kh) * S,
-                             S * sizeof(float), gfull + gb);
+                             S * sizeof(float), gfull + b);
                 }
             }
-            for (int u = 0; u < units_per_group; ++u, ++unit) {
-                const int st = unit % stages, use = unit / stages;
-                if (use > 0 && (*abort_flag || !mbar_wait(sempty + st, (use - 1) & 1))) {
-                    give_up(WD_STAGE_FREE);
-                    break;
-                }
+            bool ok = true;
+            for (int u = 0; u < units_per_group; ++u) {
+                const int unit = (gi - 1) * units_per_group + u;
+                const int st = unit % stages, su = unit / stages;
+                if (su > 0 && !wait(sempty + st, su - 1, WD_STAGE_FREE)) { ok = false; break; }
                 if (lane == 0) {
                     const int rr = u / units_per_head, row0 = (u % units_per_head) * kPUnitRows;
                     const float *src =
@@ -418,148 +470,118 @@ __global__ void __launch_bounds__(kPThreads, 1) block_decode_persistent_kernel(c
                     mbar_arrive_expect_tx(sfull + st, static_cast<uint32_t>(L.unit_bytes));
                     bulk_g2s(smem_raw + L.ring + st * L.unit_bytes, src,
                              static_cast<uint32_t>(L.unit_bytes), sfull + st);
-                    s_issued[st] = use + 1;
+                    s_issued[st] = su + 1;
                 }
                 __syncwarp();
             }
-        }
-    } else {
-        // ------------------------------------------------------------ consumer warps
-        const int ctid = tid;  // 0 .. 16*32-1
-        int unit = 0, gi = 0;
-        // gate inputs of the next group, prefetched into registers by threads < r
-        float nx_alpha = 0.f, nx_b = 0.f, nx_dt = 0.f, nx_a = 0.f;
-        auto fetch_gate = [&](int g) {
-            if (ctid < r && g < n_groups) {
-                const int n = g / Hk, kh = g % Hk, vh = ctid * Hk + kh;
-                nx_alpha = p.alpha[static_cast<size_t>(n) * H + vh];
-                nx_b = p.b[static_cast<size_t>(n) * H + vh];
-                nx_dt = p.dt[vh];
-                nx_a = p.a[vh];
+            if (!ok) break;
+        } else if (warp >= kPPro0 && warp < kPEpi0) {
+            // -------------------------------------------------------- prologue
+            const int pw = warp - kPPro0;
+            // the gate inputs first, so their latency overlaps the convolutions
+            const bool gate_lane = (pw == kPProWarps - 1) && lane < r;
+            float g_alpha = 0.f, g_b = 0.f, g_dt = 0.f, g_a = 0.f;
+            if (gate_lane) {
+                const int vh = lane * Hk + kh;
+                const size_t nh = static_cast<size_t>(n) * H + vh;
+                g_alpha = p.alpha[nh];
+                g_b = p.b[nh];
+                g_dt = p.dt[vh];
+                g_a = p.a[vh];
             }
-        };
-        fetch_gate(blockIdx.x);
-        int yr;
-        const bool writer = [&] {
-            yr = ((lane >> 4) & 1) | (((lane >> 3) & 1) << 1);
-            return (lane & 7) == 0;
-        }();
-        for (int g = blockIdx.x; g < n_groups; g += gridDim.x) {
-            const int n = g / Hk, kh = g % Hk;
-            const int slot = slot_of(n);
-            const float cur_alpha = nx_alpha, cur_b = nx_b, cur_dt = nx_dt, cur_a = nx_a;
-            fetch_gate(g + gridDim.x);  // the next group this CTA processes
-            if (!valid_slot(slot)) {
-                if (ctid == 0 && kh == 0 && p.err_count) atomicAdd(p.err_count, 1);
-                continue;  // uniform over all consumer warps
-            }
-            const int gb = gi & 1, guse = gi >> 1;
-            ++gi;
-            bool live = !*abort_flag;
-            if (live && !mbar_wait(gfull + gb, guse & 1)) {
-                give_up(WD_STAGE_COPY);
-                live = false;
-            }
-            const float *gbuf = reinterpret_cast<const float *>(smem_raw + (gb ? L.gbuf1 : L.gbuf0));
-            const float *X = gbuf, *Hh = X + n_slices * S, *W = Hh + 3 * n_slices * S;
-            const float *Z = W + 4 * n_slices * S;
-
-            // prologue: conv1d+SiLU of the group's channels, rolling their history
-            if (live) {
-                for (int c = ctid; c < n_slices * S; c += kPWarps * 32) {
-                    const float x = X[c];
-                    const float h0 = Hh[3 * c], h1 = Hh[3 * c + 1], h2 = Hh[3 * c + 2];
-                    const float4 w = *reinterpret_cast<const float4 *>(W + 4 * c);
-                    const float val = conv_channel(x, w, h0, h1, h2);
-                    if (c < 2 * S) QH[c] = val;  // QH and KH are adjacent
-                    else V[c - 2 * S] = val;
-                    float *hs = p.conv_state +
-                                (slot * conv_dim + p_channel0(c / S, kh, S, Hk) + (c % S)) * kTaps;
-                    hs[0] = h1; hs[1] = h2; hs[2] = x;
-                }
-                if (ctid < r) {
-                    SC[ctid] = expf(cur_a * softplus_guarded(cur_alpha + cur_dt));
-                    SC[r + ctid] = 1.0f / (1.0f + expf(-cur_b));
-                }
-            }
-            named_barrier_sync(1, kPWarps * 32);
-            if (live && warp < 2) {  // x / max(||x||, eps) for q (warp 0) and k (warp 1)
-                float xv[E];
-                load_vec<E>(xv, QH + warp * S + lane * E);
-                float ss = 0.0f;
+            if (!wait(gfull + b, use, WD_STAGE_COPY)) break;
+            if (use > 0 && !wait(cfree + b, use - 1, WD_STAGE_FREE)) break;
+            // slice 0 = q, 1 = k (each L2-normalised), 2 + rr = v of head rr; lane L
+            // takes channels [E*L, E*L+E) of the slice
+            for (int sl = pw; sl < n_slices; sl += kPProWarps) {
+                float val[E];
+                const int c0 = sl * S + lane * E;
+                p_conv_lane<E>(X + c0, Hh + 3 * c0, W + 4 * c0,
+                               p.conv_state +
+                                   (slot * conv_dim + p_channel0(sl, kh, S, Hk) + lane * E) * kTaps,
+                               val);
+                if (sl < 2) {  // x / max(||x||, eps)
+                    float ss = 0.0f;
 #pragma unroll
-                for (int e = 0; e < E; ++e) ss = __fmaf_rn(xv[e], xv[e], ss);
-                ss = warp_allsum(ss);
-                if (lane == 0) SC[2 * r + warp] = 1.0f / fmaxf(sqrtf(ss), p.l2_eps);
-            }
-            named_barrier_sync(1, kPWarps * 32);
-            float kk[E], qq[E];
-            load_vec<E>(qq, QH + lane * E);
-            load_vec<E>(kk, KH + lane * E);
-            {
-                const float inv_q = SC[2 * r], inv_k = SC[2 * r + 1];
+                    for (int e = 0; e < E; ++e) ss = __fmaf_rn(val[e], val[e], ss);
+                    ss = warp_allsum(ss);
+                    const float inv = 1.0f / fmaxf(sqrtf(ss), p.l2_eps);
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    qq[e] *= inv_q;
-                    kk[e] *= inv_k;
+                    for (int e = 0; e < E; ++e) val[e] *= inv;
+                    store_vec<E>((sl ? KH(cslot) : QH(cslot)) + lane * E, val);
+                } else {
+                    store_vec<E>(VV(cslot) + (sl - 2) * S + lane * E, val);
                 }
             }
-
-            // the state stream: 64 rows per stage, 4 per warp
-            for (int u = 0; u < units_per_group; ++u, ++unit) {
-                const int st = unit % stages, use = unit / stages;
-                if (live && (*abort_flag || !mbar_wait(sfull + st, use & 1))) {
-                    give_up(WD_STATE_COPY);
-                    live = false;
-                }
-                if (live) {
-                    const int rr = u / units_per_head;
-                    const int j0 = (u % units_per_head) * kPUnitRows + warp * kR;
-                    const int vh = rr * Hk + kh;
-                    const float *tile =
-                        reinterpret_cast<const float *>(smem_raw + L.ring + st * L.unit_bytes) +
-                        warp * kR * S;
-                    float row[kR][E], vv[kR];
-#pragma unroll
-                    for (int q = 0; q < kR; ++q) {
-                        load_vec<E>(row[q], tile + q * S + lane * E);
-                        vv[q] = V[rr * S + j0 + q];
-                    }
-                    const float ysum = row_step<E, kR>(row, kk, qq, vv, SC[rr], SC[r + rr], lane);
-                    float *gst = p.state + ((static_cast<size_t>(slot) * H + vh) * S + j0) * S;
-#pragma unroll
-                    for (int q = 0; q < kR; ++q) store_vec<E>(gst + q * S + lane * E, row[q]);
-                    if (writer) Y[rr * S + j0 + yr] = __fmul_rn(p.scale, ysum);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sempty + st);
+            if (gate_lane) {
+                DEC(cslot)[lane] = expf(g_a * softplus_guarded(g_alpha + g_dt));
+                BET(cslot)[lane] = 1.0f / (1.0f + expf(-g_b));
             }
-
-            // gated RMSNorm of the group's r heads
-            named_barrier_sync(1, kPWarps * 32);
-            if (live && warp < r) {
-                float yv[E];
-                load_vec<E>(yv, Y + warp * S + lane * E);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(gempty + b);  // done with X, H, W of this buffer
+                mbar_arrive(cfull + b);
+            }
+        } else if (warp >= kPEpi0) {
+            // -------------------------------------------------------- epilogue
+            if (!wait(yfull + b, use, WD_STAGE_COPY)) break;
+            if (!wait(gfull + b, use, WD_STAGE_COPY)) break;  // z of this group
+            for (int rr = warp - kPEpi0; rr < r; rr += kPEpiWarps) {
+                float yv[E], zv[E], wv[E], o[E];
+                load_vec<E>(yv, YY(cslot) + rr * S + lane * E);
+                load_vec<E>(zv, Z + rr * S + lane * E);
+                load_vec<E>(wv, p.norm_w + lane * E);
                 float ss = 0.0f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) ss = __fmaf_rn(yv[e], yv[e], ss);
                 ss = warp_allsum(ss);
-                if (lane == 0) SC[2 * r + 2 + warp] = 1.0f / sqrtf(ss / static_cast<float>(S) + p.norm_eps);
-            }
-            named_barrier_sync(1, kPWarps * 32);
-            if (live && !*abort_flag) {
-                for (int idx = ctid; idx < r * S; idx += kPWarps * 32) {
-                    const int rr = idx / S, j = idx % S;
-                    const float zv = Z[idx];
-                    p.out[(static_cast<size_t>(n) * H + rr * Hk + kh) * S + j] =
-                        Y[idx] * SC[2 * r + 2 + rr] * p.norm_w[j] * silu(zv);
-                }
+                const float inv_rms = 1.0f / sqrtf(ss / static_cast<float>(S) + p.norm_eps);
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[e] = yv[e] * inv_rms * wv[e] * silu(zv[e]);
+                store_vec<E>(p.out + (static_cast<size_t>(n) * H + rr * Hk + kh) * S + lane * E, o);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(gempty + gb);
-            // the next prologue rewrites the consumer area: every warp first finishes
-            // reading this group's values
-            named_barrier_sync(1, kPWarps * 32);
+            if (lane == 0) {
+                mbar_arrive(gempty + b);  // done with z
+                mbar_arrive(cfree + b);   // slot reusable
+            }
+        } else {
+            // -------------------------------------------------------- row warps
+            if (!wait(cfull + b, use, WD_STAGE_COPY)) break;
+            float kk[E], qq[E];
+            load_vec<E>(qq, QH(cslot) + lane * E);
+            load_vec<E>(kk, KH(cslot) + lane * E);
+            int yr;
+            const bool writer = [&] {
+                yr = ((lane >> 4) & 1) | (((lane >> 3) & 1) << 1);
+                return (lane & 7) == 0;
+            }();
+            bool ok = true;
+            for (int u = 0; u < units_per_group; ++u) {
+                const int unit = (gi - 1) * units_per_group + u;
+                const int st = unit % stages, su = unit / stages;
+                if (!wait(sfull + st, su, WD_STATE_COPY)) { ok = false; break; }
+                const int rr = u / units_per_head;
+                const int j0 = (u % units_per_head) * kPUnitRows + warp * kR;
+                const int vh = rr * Hk + kh;
+                const float *tile =
+                    reinterpret_cast<const float *>(smem_raw + L.ring + st * L.unit_bytes) + warp * kR * S;
+                float row[kR][E], vv[kR];
+#pragma unroll
+                for (int q = 0; q < kR; ++q) load_vec<E>(row[q], tile + q * S + lane * E);
+                load_vec<kR>(vv, VV(cslot) + rr * S + j0);
+                const float ysum =
+                    row_step<E, kR>(row, kk, qq, vv, DEC(cslot)[rr], BET(cslot)[rr], lane);
+                float *gst = p.state + ((static_cast<size_t>(slot) * H + vh) * S + j0) * S;
+#pragma unroll
+                for (int q = 0; q < kR; ++q) store_vec<E>(gst + q * S + lane * E, row[q]);
+                if (writer) YY(cslot)[rr * S + j0 + yr] = __fmul_rn(p.scale, ysum);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sempty + st);
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(yfull + b);
         }
     }
     // Never leave while a bulk copy may still be landing in shared memory.
@@ -567,7 +589,7 @@ __global__ void __launch_bounds__(kPThreads, 1) block_decode_persistent_kernel(c
     if (tid == 0) {
         for (int i = 0; i < stages; ++i)
             if (s_issued[i] > 0) mbar_wait(sfull + i, (s_issued[i] - 1) & 1);
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < kPBufs; ++i)
             if (g_issued[i] > 0) mbar_wait(gfull + i, (g_issued[i] - 1) & 1);
     }
 }
@@ -687,8 +709,8 @@ extern "C" gdn_status gdn_block_decode(const float *qkv, const float *conv_w, fl
     GDN_TRY(check_pool(n_seqs, slots, pool));
     if (conv_kernel != 4) return GDN_ERR_UNSUPPORTED;
     if (n_v_heads / n_k_heads > 8) return GDN_ERR_UNSUPPORTED;
-    if (!aligned16(qkv) || !aligned16(conv_w) || !aligned16(state) || !aligned16(z) ||
-        !aligned16(out) || !aligned16(norm_w))
+    if (!aligned16(qkv) || !aligned16(conv_w) || !aligned16(conv_state) || !aligned16(state) ||
+        !aligned16(z) || !aligned16(out) || !aligned16(norm_w))
         return GDN_ERR_ALIGN;
     if (n_seqs == 0) return GDN_OK;
     BlockParams p{qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, slots, err_count,

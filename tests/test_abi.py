@@ -118,9 +118,10 @@ def test_elementwise_validation(lib):
     assert lib.gdn_qkv_split_norm(P, P, P, P, 0, 2, 4, 32, 1e-6, None) == OK
 
 
-def block(lib, qkv=P, state=P, out=P, n_seqs=1, hk=2, hv=4, s=32, K=4, slots=None, pool=None):
+def block(lib, qkv=P, state=P, out=P, conv_state=P, n_seqs=1, hk=2, hv=4, s=32, K=4, slots=None,
+          pool=None):
     pool = max(1, n_seqs) if pool is None else pool
-    return lib.gdn_block_decode(qkv, P, P, P, P, P, P, P, P, state, out, n_seqs, hk, hv, s, K,
+    return lib.gdn_block_decode(qkv, P, conv_state, P, P, P, P, P, P, state, out, n_seqs, hk, hv, s, K,
                                 0.1, 1e-6, 1e-6, slots, pool, None, None)
 
 
@@ -133,6 +134,7 @@ def test_block_validation(lib):
     assert block(lib, hk=3, hv=4) == SHAPE
     assert block(lib, s=96) == UNSUP
     assert block(lib, state=MIS) == ALIGN
+    assert block(lib, conv_state=MIS) == ALIGN
     assert block(lib, n_seqs=4, pool=2) == SHAPE
     assert block(lib, n_seqs=0) == OK
 
