@@ -141,6 +141,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ ranks (weak scaling)
+
+def rank_work(cfg, rank):
+    """The sequences and pool slots rank `rank` serves: every rank its own n_seqs
+    sequences (own seeded streams) and its own pool; nothing is shared."""
+    n, pool = cfg.n_seqs, cfg.pool_size
+    return {"seqs": list(range(rank * n, (rank + 1) * n)),
+            "pool_ids": list(range(rank * pool, (rank + 1) * pool))}
+
+
+def reduce_max(value, dist, device):
+    """Max of a float over all ranks (the timing rule); the value itself at one rank."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ the workload
 
 def algorithmic_bytes_block(cfg, n):
@@ -269,14 +289,14 @@ def run_ours(args, cfg, rank, world, local_rank):
         return run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
 
     # This rank's sequences (its own seeded streams) and pool slots.
-    base = rank * N
-    seqs = list(range(base, base + N))
+    work = rank_work(cfg, rank)
+    seqs = work["seqs"]
     slots = I.slots(cfg)
     pool = cfg.pool_size
     st = I.block_static(cfg)
     d_st = {k: dev(v) for k, v in st.items()}
-    state = dev(I.state_pool(cfg, which=range(rank * pool, (rank + 1) * pool)))
-    conv = dev(I.conv_state_pool(cfg, which=range(rank * pool, (rank + 1) * pool)))
+    state = dev(I.state_pool(cfg, which=work["pool_ids"]))
+    conv = dev(I.conv_state_pool(cfg, which=work["pool_ids"]))
     d_slots = dev(slots) if slots is not None else None
     n_distinct = 8
     steps_in = [I.block_step(cfg, s, seqs=seqs) for s in range(n_distinct)]
@@ -313,11 +333,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     gdn.gdn_device_error()
     kernel_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-    total_s = sum(kernel_ms) / 1e3
-    if dist:
-        t = torch.tensor([total_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = reduce_max(sum(kernel_ms) / 1e3, dist, "cuda")
     tokens = world * N * args.steps
     value = tokens / total_s
     per_launch_s = total_s / args.steps
@@ -342,11 +358,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         h_out.copy_(out, non_blocking=True)
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_s = sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
 
     if rank != 0:
         return 0
@@ -389,7 +401,7 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     import gated_deltanet_linear_scan_gb300 as gdn
     stream = torch.cuda.current_stream()
     N, T, H, Hk, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.n_k_heads, cfg.state_size
-    seqs = list(range(rank * N, (rank + 1) * N))
+    seqs = rank_work(cfg, rank)["seqs"]
     x = I.recurrence_batch(cfg, seqs=seqs)
     d = {k: dev(v) for k, v in x.items()}
     state0 = dev(I.state_pool(cfg, which=seqs))
@@ -418,11 +430,7 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
     gdn.gdn_device_error()
-    total_s = sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
-    if dist:
-        t = torch.tensor([total_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, dist, "cuda")
     per = total_s / args.steps
     tokens = world * N * T * args.steps
     flops = 7.0 * N * T * H * S * S
