@@ -112,7 +112,7 @@ struct ScanSmem {
 };
 
 template <int E>
-__global__ void __launch_bounds__((kWarps + 1) * 32) recurrence_scan_kernel(
+__global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrence_scan_kernel(
     float *state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
     float *__restrict__ y, int n_tokens, int n_k_heads, int n_v_heads, float scale,
