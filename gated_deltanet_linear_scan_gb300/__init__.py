@@ -19,7 +19,8 @@ __all__ = [
     "gdn_status_str", "gdn_version", "gdn_device_error",
     "gdn_decay_gate", "gdn_beta_sigmoid", "gdn_conv1d_silu", "gdn_conv1d_silu_seq",
     "gdn_qkv_split_norm", "gdn_recurrence_decode", "gdn_recurrence_scan", "gdn_gated_norm",
-    "gdn_block_decode",
+    "gdn_block_decode", "gdn_recurrence_decode_2pass", "gdn_recurrence_scan_snapshots",
+    "gdn_conv1d_silu_seq_snapshots",
 ]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
@@ -50,6 +51,9 @@ _SIGS = {
     "gdn_recurrence_scan": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
     "gdn_gated_norm": ([_P, _P, _P, _P, _I, _I, _F, _P], _I),
     "gdn_block_decode": ([_P] * 11 + [_I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P, _P], _I),
+    "gdn_recurrence_decode_2pass": ([_P] * 7 + [_I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
+    "gdn_recurrence_scan_snapshots": ([_P] * 8 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
+    "gdn_conv1d_silu_seq_snapshots": ([_P] * 5 + [_I, _I, _I, _I, _P, _I, _P, _P], _I),
 }
 
 
@@ -211,4 +215,34 @@ def gdn_block_decode(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state,
         _ptr(alpha, "alpha"), _ptr(b, "b"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(z, "z"),
         _ptr(norm_w, "norm_w"), _ptr(state, "state"), _ptr(out, "out"), n_seqs, n_k_heads,
         n_v_heads, state_size, conv_kernel, scale, l2_eps, norm_eps, _slots(slots), pool,
+        _errc(err_count), _stream(stream)))
+
+
+def gdn_recurrence_decode_2pass(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads,
+                                state_size, scale, slots=None, pool=None, err_count=None,
+                                stream=None):
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_recurrence_decode_2pass", library().gdn_recurrence_decode_2pass(
+        _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
+        _ptr(beta, "beta"), _ptr(y, "y"), n_seqs, n_k_heads, n_v_heads, state_size, scale,
+        _slots(slots), pool, _errc(err_count), _stream(stream)))
+
+
+def gdn_recurrence_scan_snapshots(state, q, k, v, g, beta, y, snaps, n_seqs, n_tokens,
+                                  n_k_heads, n_v_heads, state_size, scale, slots=None, pool=None,
+                                  err_count=None, stream=None):
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_recurrence_scan_snapshots", library().gdn_recurrence_scan_snapshots(
+        _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
+        _ptr(beta, "beta"), _ptr(y, "y"), _ptr(snaps, "snaps"), n_seqs, n_tokens, n_k_heads,
+        n_v_heads, state_size, scale, _slots(slots), pool, _errc(err_count), _stream(stream)))
+
+
+def gdn_conv1d_silu_seq_snapshots(qkv, w, conv_state, out, snaps, n_seqs, n_tokens, conv_dim,
+                                  conv_kernel, slots=None, pool=None, err_count=None,
+                                  stream=None):
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_conv1d_silu_seq_snapshots", library().gdn_conv1d_silu_seq_snapshots(
+        _ptr(qkv, "qkv"), _ptr(w, "w"), _ptr(conv_state, "conv_state"), _ptr(out, "out"),
+        _ptr(snaps, "snaps"), n_seqs, n_tokens, conv_dim, conv_kernel, _slots(slots), pool,
         _errc(err_count), _stream(stream)))

@@ -241,6 +241,40 @@ __device__ __forceinline__ float row_step(float (&row)[R][E], const float (&k)[E
     return warp_sum_packed<R>(part, lane);
 }
 
+// The same token with the readout factorised (ssm_gated_delta.cu, "T4: 3-pass ->
+// 2-pass state-access factorization"): with r the decayed row,
+//   y = scale * (r_new . q) = scale * (r . q + delta * (k . q)),
+// so both dots reduce off the same decayed row and the second no longer waits for
+// the update. `kq` is k . q of the token (the same for every row). The state update
+// is the row step's, bit for bit; y differs from it by rounding only. Returns
+// scale * y in lane row_home_lane<R>(r) for row r.
+template <int E, int R>
+__device__ __forceinline__ float row_step_factored(float (&row)[R][E], const float (&k)[E],
+                                                   const float (&q)[E], const float (&v)[R],
+                                                   float decay, float beta, float kq, float scale,
+                                                   int lane) {
+    float pk[R], pq[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) row[r][e] = __fmul_rn(row[r][e], decay);
+        pk[r] = lane_dot<E>(row[r], k);
+        pq[r] = lane_dot<E>(row[r], q);
+    }
+    warp_allsum_rows<R>(pk, lane);
+    const float oq = warp_sum_packed<R>(pq, lane);
+    float my_delta = 0.0f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float delta = __fmul_rn(__fsub_rn(v[r], pk[r]), beta);
+#pragma unroll
+        for (int e = 0; e < E; ++e) row[r][e] = __fmaf_rn(k[e], delta, row[r][e]);
+        if (row_home_lane<R>(r) == (lane & (R == 1 ? 0 : R == 2 ? 16 : R == 4 ? 24 : 28)))
+            my_delta = delta;
+    }
+    return __fmul_rn(scale, __fmaf_rn(my_delta, kq, oq));
+}
+
 // ------------------------------------------------------------------ vector memory
 
 template <int E>

@@ -41,11 +41,11 @@ __global__ void __launch_bounds__(kThreads) sigmoid_kernel(const float *__restri
 // back once. The accumulation is the current tap first, then the history
 // oldest-first; a single-token call is the n_tokens == 1 case of the same code, so
 // a scan and n single-token calls agree bit for bit.
-template <int K>
+template <int K, bool SNAP>
 __global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
     const float *__restrict__ qkv, const float *__restrict__ w, float *conv_state,
     float *__restrict__ out, int n_tokens, int conv_dim, const int32_t *__restrict__ slots,
-    int pool, int32_t *err_count) {
+    int pool, int32_t *err_count, float *__restrict__ snaps) {
     constexpr int TAPS = K - 1;
     const int n = blockIdx.y;
     const int c = blockIdx.x * kThreads + threadIdx.x;
@@ -73,6 +73,11 @@ __global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
 #pragma unroll
         for (int t = 0; t + 1 < TAPS; ++t) hist[t] = hist[t + 1];
         hist[TAPS - 1] = x;
+        if constexpr (SNAP) {  // the history after token p: snaps[n][p][C][K-1]
+            float *sn = snaps + ((static_cast<size_t>(n) * n_tokens + p) * conv_dim + c) * TAPS;
+#pragma unroll
+            for (int t = 0; t < TAPS; ++t) sn[t] = hist[t];
+        }
     }
 #pragma unroll
     for (int t = 0; t < TAPS; ++t) hs[t] = hist[t];
@@ -140,16 +145,21 @@ __global__ void __launch_bounds__(kThreads) gated_norm_kernel(const float *y,
 template <int K>
 gdn_status launch_conv(const float *qkv, const float *w, float *conv_state, float *out,
                        int n_seqs, int n_tokens, int conv_dim, const int32_t *slots, int pool,
-                       int32_t *err_count, cudaStream_t s) {
+                       int32_t *err_count, float *snaps, cudaStream_t s) {
     const dim3 grid((conv_dim + kThreads - 1) / kThreads, n_seqs);
-    conv1d_silu_kernel<K><<<grid, kThreads, 0, s>>>(qkv, w, conv_state, out, n_tokens, conv_dim,
-                                                    slots, pool, err_count);
+    if (snaps)
+        conv1d_silu_kernel<K, true><<<grid, kThreads, 0, s>>>(qkv, w, conv_state, out, n_tokens,
+                                                              conv_dim, slots, pool, err_count, snaps);
+    else
+        conv1d_silu_kernel<K, false><<<grid, kThreads, 0, s>>>(qkv, w, conv_state, out, n_tokens,
+                                                               conv_dim, slots, pool, err_count, nullptr);
     return launch_status();
 }
 
 gdn_status conv_common(const float *qkv, const float *w, float *conv_state, float *out,
                        int n_seqs, int n_tokens, int conv_dim, int conv_kernel,
-                       const int32_t *slots, int pool, int32_t *err_count, gdn_stream_t stream) {
+                       const int32_t *slots, int pool, int32_t *err_count, float *snaps,
+                       gdn_stream_t stream) {
     if (!qkv || !w || !conv_state || !out) return GDN_ERR_NULL;
     if (n_seqs < 0 || n_tokens < 0 || conv_dim < 1) return GDN_ERR_SHAPE;
     if (conv_kernel < 2 || conv_kernel > 8) return GDN_ERR_SHAPE;
@@ -158,13 +168,13 @@ gdn_status conv_common(const float *qkv, const float *w, float *conv_state, floa
     if (n_seqs > 65535) return GDN_ERR_UNSUPPORTED;
     const cudaStream_t s = as_cuda(stream);
     switch (conv_kernel) {
-        case 2: return launch_conv<2>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
-        case 3: return launch_conv<3>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
-        case 4: return launch_conv<4>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
-        case 5: return launch_conv<5>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
-        case 6: return launch_conv<6>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
-        case 7: return launch_conv<7>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
-        default: return launch_conv<8>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, s);
+        case 2: return launch_conv<2>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, snaps, s);
+        case 3: return launch_conv<3>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, snaps, s);
+        case 4: return launch_conv<4>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, snaps, s);
+        case 5: return launch_conv<5>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, snaps, s);
+        case 6: return launch_conv<6>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, snaps, s);
+        case 7: return launch_conv<7>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, snaps, s);
+        default: return launch_conv<8>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, snaps, s);
     }
 }
 
@@ -221,7 +231,7 @@ gdn_status gdn_conv1d_silu(const float *qkv, const float *w, float *conv_state, 
                            int n_seqs, int conv_dim, int conv_kernel, const int32_t *slots,
                            int pool, int32_t *err_count, gdn_stream_t stream) {
     return conv_common(qkv, w, conv_state, out, n_seqs, 1, conv_dim, conv_kernel, slots, pool,
-                       err_count, stream);
+                       err_count, nullptr, stream);
 }
 
 gdn_status gdn_conv1d_silu_seq(const float *qkv, const float *w, float *conv_state, float *out,
@@ -229,7 +239,16 @@ gdn_status gdn_conv1d_silu_seq(const float *qkv, const float *w, float *conv_sta
                                const int32_t *slots, int pool, int32_t *err_count,
                                gdn_stream_t stream) {
     return conv_common(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, conv_kernel, slots,
-                       pool, err_count, stream);
+                       pool, err_count, nullptr, stream);
+}
+
+gdn_status gdn_conv1d_silu_seq_snapshots(const float *qkv, const float *w, float *conv_state,
+                                         float *out, float *snaps, int n_seqs, int n_tokens,
+                                         int conv_dim, int conv_kernel, const int32_t *slots,
+                                         int pool, int32_t *err_count, gdn_stream_t stream) {
+    if (!snaps) return GDN_ERR_NULL;
+    return conv_common(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, conv_kernel, slots,
+                       pool, err_count, snaps, stream);
 }
 
 gdn_status gdn_qkv_split_norm(const float *conv_out, float *q, float *k, float *v, int rows,

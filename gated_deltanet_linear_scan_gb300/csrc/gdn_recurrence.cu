@@ -39,7 +39,7 @@ __device__ __forceinline__ bool y_writer(int lane, int &r) {
 // the lanes fetch k, q, v, g and beta; the update goes back to HBM with 128-bit
 // stores. The state of a (slot, head) is S*S*4 contiguous bytes, so a CTA's tile is
 // one contiguous run and every access is fully coalesced.
-template <int E>
+template <int E, bool FACTORED>
 __global__ void __launch_bounds__(kWarps * 32) recurrence_decode_kernel(
     float *state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
@@ -88,11 +88,17 @@ __global__ void __launch_bounds__(kWarps * 32) recurrence_decode_kernel(
     float row[R][E];
 #pragma unroll
     for (int r = 0; r < R; ++r) load_vec<E>(row[r], wtile + r * S + lane * E);
-    const float ysum = row_step<E, R>(row, kk, qq, vv, decay, bt, lane);
+    float yout;
+    if constexpr (FACTORED) {
+        const float kq = warp_allsum(lane_dot<E>(kk, qq));
+        yout = row_step_factored<E, R>(row, kk, qq, vv, decay, bt, kq, scale, lane);
+    } else {
+        yout = __fmul_rn(scale, row_step<E, R>(row, kk, qq, vv, decay, bt, lane));
+    }
 #pragma unroll
     for (int r = 0; r < R; ++r) store_vec<E>(gstate + r * S + lane * E, row[r]);
     int r;
-    if (y_writer<R>(lane, r)) y[hv * S + row0 + r] = __fmul_rn(scale, ysum);
+    if (y_writer<R>(lane, r)) y[hv * S + row0 + r] = yout;
 }
 
 // ---------------------------------------------------------------------------- scan
@@ -111,12 +117,12 @@ struct ScanSmem {
     static constexpr size_t bytes = kScanStages * stage_bytes + 2 * kScanStages * sizeof(uint64_t);
 };
 
-template <int E>
+template <int E, bool SNAP>
 __global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrence_scan_kernel(
     float *state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
     float *__restrict__ y, int n_tokens, int n_k_heads, int n_v_heads, float scale,
-    const int32_t *__restrict__ slots, int pool, int32_t *err_count) {
+    const int32_t *__restrict__ slots, int pool, int32_t *err_count, float *__restrict__ snaps) {
     constexpr int S = 32 * E, R = kRowsPerWarp, TC = kScanTokens;
     constexpr int kBlocksPerHead = S / kRowsPerCta;
     using L = ScanSmem<E>;
@@ -194,6 +200,11 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrenc
     int yr;
     const bool writer = y_writer<R>(lane, yr);
     float *ybase = y + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S + row0 + yr;
+    // snapshot of token t: snaps[n][t][H][S][S], the state layout of one slot
+    const size_t snap_tok = static_cast<size_t>(n_v_heads) * S * S;
+    float *sbase = SNAP ? snaps + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S * S +
+                              static_cast<size_t>(row0) * S + lane * E
+                        : nullptr;
 
     // g and beta of token (chunk*TC + lane), one chunk ahead.
     auto fetch_gb = [&](int c, float &dec, float &bt) {
@@ -231,6 +242,11 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrenc
             const float bt = __shfl_sync(FULL_MASK, bt_cur, t);
             const float ysum = row_step<E, R>(row, kk, qq, vv, decay, bt, lane);
             if (writer) ybase[(static_cast<size_t>(c) * TC + t) * v_tok] = __fmul_rn(scale, ysum);
+            if constexpr (SNAP) {
+                float *sn = sbase + (static_cast<size_t>(c) * TC + t) * snap_tok;
+#pragma unroll
+                for (int r = 0; r < R; ++r) store_vec<E>(sn + r * S, row[r]);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + s);
@@ -252,34 +268,34 @@ gdn_status set_smem(Kern kern, size_t bytes) {
                : GDN_ERR_LAUNCH;
 }
 
-template <int E>
+template <int E, bool FACTORED>
 gdn_status launch_decode(float *state, const float *q, const float *k, const float *v,
                          const float *g, const float *beta, float *y, int n_seqs, int n_k_heads,
                          int n_v_heads, float scale, const int32_t *slots, int pool,
                          int32_t *err_count, cudaStream_t s) {
     constexpr int S = 32 * E;
     const size_t smem = kRowsPerCta * S * sizeof(float) + kWarps * sizeof(uint64_t);
-    GDN_TRY(set_smem(recurrence_decode_kernel<E>, smem));
+    GDN_TRY(set_smem(recurrence_decode_kernel<E, FACTORED>, smem));
     const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / kRowsPerCta);
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-    recurrence_decode_kernel<E><<<static_cast<unsigned>(blocks), kWarps * 32, smem, s>>>(
+    recurrence_decode_kernel<E, FACTORED><<<static_cast<unsigned>(blocks), kWarps * 32, smem, s>>>(
         state, q, k, v, g, beta, y, n_k_heads, n_v_heads, scale, slots, pool, err_count);
     return launch_status();
 }
 
-template <int E>
+template <int E, bool SNAP>
 gdn_status launch_scan(float *state, const float *q, const float *k, const float *v,
                        const float *g, const float *beta, float *y, int n_seqs, int n_tokens,
                        int n_k_heads, int n_v_heads, float scale, const int32_t *slots, int pool,
-                       int32_t *err_count, cudaStream_t s) {
+                       int32_t *err_count, float *snaps, cudaStream_t s) {
     constexpr int S = 32 * E;
     const size_t smem = ScanSmem<E>::bytes;
-    GDN_TRY(set_smem(recurrence_scan_kernel<E>, smem));
+    GDN_TRY(set_smem(recurrence_scan_kernel<E, SNAP>, smem));
     const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / kRowsPerCta);
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-    recurrence_scan_kernel<E><<<static_cast<unsigned>(blocks), (kWarps + 1) * 32, smem, s>>>(
+    recurrence_scan_kernel<E, SNAP><<<static_cast<unsigned>(blocks), (kWarps + 1) * 32, smem, s>>>(
         state, q, k, v, g, beta, y, n_tokens, n_k_heads, n_v_heads, scale, slots, pool,
-        err_count);
+        err_count, snaps);
     return launch_status();
 }
 
@@ -306,6 +322,46 @@ unsigned read_and_clear_watchdog_recurrence(cudaStream_t s) {
     return flags;
 }
 
+namespace {
+
+template <bool FACTORED>
+gdn_status decode_entry(float *state, const float *q, const float *k, const float *v,
+                        const float *g, const float *beta, float *y, int n_seqs, int n_k_heads,
+                        int n_v_heads, int state_size, float scale, const int32_t *slots, int pool,
+                        int32_t *err_count, gdn_stream_t stream) {
+    GDN_TRY(check_recurrence_args(state, q, k, v, g, beta, y, n_seqs, 1, n_k_heads, n_v_heads,
+                                  state_size, slots, pool));
+    if (n_seqs == 0) return GDN_OK;
+    const cudaStream_t s = as_cuda(stream);
+    switch (state_size) {
+        case 32: return launch_decode<1, FACTORED>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+        case 64: return launch_decode<2, FACTORED>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+        case 128: return launch_decode<4, FACTORED>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+        default: return launch_decode<8, FACTORED>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
+    }
+}
+
+template <bool SNAP>
+gdn_status scan_entry(float *state, const float *q, const float *k, const float *v,
+                      const float *g, const float *beta, float *y, int n_seqs, int n_tokens,
+                      int n_k_heads, int n_v_heads, int state_size, float scale,
+                      const int32_t *slots, int pool, int32_t *err_count, float *snaps,
+                      gdn_stream_t stream) {
+    GDN_TRY(check_recurrence_args(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads,
+                                  n_v_heads, state_size, slots, pool));
+    if (SNAP && snaps == nullptr) return GDN_ERR_NULL;
+    if (SNAP && !aligned16(snaps)) return GDN_ERR_ALIGN;
+    if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
+    const cudaStream_t s = as_cuda(stream);
+    switch (state_size) {
+        case 32: return launch_scan<1, SNAP>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
+        case 64: return launch_scan<2, SNAP>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
+        case 128: return launch_scan<4, SNAP>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
+        default: return launch_scan<8, SNAP>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
+    }
+}
+
+}  // namespace
 }  // namespace gdn
 
 using namespace gdn;
@@ -317,16 +373,17 @@ gdn_status gdn_recurrence_decode(float *state, const float *q, const float *k, c
                                  int n_k_heads, int n_v_heads, int state_size, float scale,
                                  const int32_t *slots, int pool, int32_t *err_count,
                                  gdn_stream_t stream) {
-    GDN_TRY(check_recurrence_args(state, q, k, v, g, beta, y, n_seqs, 1, n_k_heads, n_v_heads,
-                                  state_size, slots, pool));
-    if (n_seqs == 0) return GDN_OK;
-    const cudaStream_t s = as_cuda(stream);
-    switch (state_size) {
-        case 32: return launch_decode<1>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
-        case 64: return launch_decode<2>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
-        case 128: return launch_decode<4>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
-        default: return launch_decode<8>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
-    }
+    return decode_entry<false>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads,
+                               state_size, scale, slots, pool, err_count, stream);
+}
+
+gdn_status gdn_recurrence_decode_2pass(float *state, const float *q, const float *k,
+                                       const float *v, const float *g, const float *beta,
+                                       float *y, int n_seqs, int n_k_heads, int n_v_heads,
+                                       int state_size, float scale, const int32_t *slots,
+                                       int pool, int32_t *err_count, gdn_stream_t stream) {
+    return decode_entry<true>(state, q, k, v, g, beta, y, n_seqs, n_k_heads, n_v_heads,
+                              state_size, scale, slots, pool, err_count, stream);
 }
 
 gdn_status gdn_recurrence_scan(float *state, const float *q, const float *k, const float *v,
@@ -334,16 +391,18 @@ gdn_status gdn_recurrence_scan(float *state, const float *q, const float *k, con
                                int n_tokens, int n_k_heads, int n_v_heads, int state_size,
                                float scale, const int32_t *slots, int pool, int32_t *err_count,
                                gdn_stream_t stream) {
-    GDN_TRY(check_recurrence_args(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads,
-                                  n_v_heads, state_size, slots, pool));
-    if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
-    const cudaStream_t s = as_cuda(stream);
-    switch (state_size) {
-        case 32: return launch_scan<1>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
-        case 64: return launch_scan<2>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
-        case 128: return launch_scan<4>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
-        default: return launch_scan<8>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, s);
-    }
+    return scan_entry<false>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
+                             state_size, scale, slots, pool, err_count, nullptr, stream);
+}
+
+gdn_status gdn_recurrence_scan_snapshots(float *state, const float *q, const float *k,
+                                         const float *v, const float *g, const float *beta,
+                                         float *y, float *snaps, int n_seqs, int n_tokens,
+                                         int n_k_heads, int n_v_heads, int state_size,
+                                         float scale, const int32_t *slots, int pool,
+                                         int32_t *err_count, gdn_stream_t stream) {
+    return scan_entry<true>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
+                            state_size, scale, slots, pool, err_count, snaps, stream);
 }
 
 }  // extern "C"

@@ -130,6 +130,17 @@ gdn_status gdn_recurrence_decode(float *state, const float *q, const float *k, c
                                  const int32_t *slots, int pool, int32_t *err_count,
                                  gdn_stream_t stream);
 
+/* Decode with the readout factorised. ssm_gated_delta.cu, "T4: 3-pass -> 2-pass
+ * state-access factorization" (fc_ssm_recurrence_slots_2pass): with r the decayed
+ * row, y = scale * (r . q + delta * (k . q)), so the readout no longer waits for the
+ * rank-1 write. Same arguments and layouts as gdn_recurrence_decode; the state is
+ * updated bit for bit as there, y agrees with it up to rounding. */
+gdn_status gdn_recurrence_decode_2pass(float *state, const float *q, const float *k,
+                                       const float *v, const float *g, const float *beta,
+                                       float *y, int n_seqs, int n_k_heads, int n_v_heads,
+                                       int state_size, float scale, const int32_t *slots,
+                                       int pool, int32_t *err_count, gdn_stream_t stream);
+
 /* Sequential scan over n_tokens positions per sequence, the state kept in
  * registers and written back once. fm_kernel_ssm.m, "The sequential scan";
  * ssm_gated_delta.cu, fc_ssm_recurrence_seq and its warp form; gated_delta_net_decode.metal
@@ -141,6 +152,29 @@ gdn_status gdn_recurrence_scan(float *state, const float *q, const float *k, con
                                int n_tokens, int n_k_heads, int n_v_heads, int state_size,
                                float scale, const int32_t *slots, int pool, int32_t *err_count,
                                gdn_stream_t stream);
+
+/* The scan, also writing the state after every position, for speculative
+ * decoding: ssm_gated_delta.cu, fc_ssm_recurrence_seq's `snaps` ("snaps[t] = the
+ * full recurrent state AFTER position t's update ... a partial accept of M
+ * positions restores state-after-M with one contiguous copy of snaps[M-1]").
+ * snaps: [n_seqs][n_tokens][H][S][S] (the state layout of one slot per position,
+ * sequence n in call order), 16-byte aligned, NULL is an error. Otherwise as
+ * gdn_recurrence_scan, whose results it reproduces bit for bit. */
+gdn_status gdn_recurrence_scan_snapshots(float *state, const float *q, const float *k,
+                                         const float *v, const float *g, const float *beta,
+                                         float *y, float *snaps, int n_seqs, int n_tokens,
+                                         int n_k_heads, int n_v_heads, int state_size,
+                                         float scale, const int32_t *slots, int pool,
+                                         int32_t *err_count, gdn_stream_t stream);
+
+/* The conv scan, also writing the conv history after every position (ssm_gated_delta.cu,
+ * fc_ssm_conv1d_silu_seq's `snaps`): snaps [n_seqs][n_tokens][conv_dim][K-1], the
+ * conv_state layout of one slot per position. NULL is an error. Otherwise as
+ * gdn_conv1d_silu_seq. */
+gdn_status gdn_conv1d_silu_seq_snapshots(const float *qkv, const float *w, float *conv_state,
+                                         float *out, float *snaps, int n_seqs, int n_tokens,
+                                         int conv_dim, int conv_kernel, const int32_t *slots,
+                                         int pool, int32_t *err_count, gdn_stream_t stream);
 
 /* Gated RMSNorm. fm_kernel_ssm.m, "Gated RMSNorm"; ssm_gated_delta.cu, Kernel 3.
  *   out[r][d] = y[r][d] / sqrt(mean_d(y[r]^2) + eps) * w[d] * silu(z[r][d])

@@ -125,6 +125,21 @@ def block(lib, qkv=P, state=P, out=P, conv_state=P, n_seqs=1, hk=2, hv=4, s=32, 
                                 0.1, 1e-6, 1e-6, slots, pool, None, None)
 
 
+def test_variant_validation(lib):
+    f = lib.gdn_recurrence_decode_2pass
+    assert f(P, P, P, P, P, P, None, 1, 2, 4, 32, 0.1, None, 1, None, None) == NULL
+    assert f(P, P, P, P, P, P, P, 1, 2, 4, 96, 0.1, None, 1, None, None) == UNSUP
+    assert f(P, P, P, P, P, P, P, 0, 2, 4, 32, 0.1, None, 1, None, None) == OK
+    fs = lib.gdn_recurrence_scan_snapshots
+    assert fs(P, P, P, P, P, P, P, None, 1, 4, 2, 4, 32, 0.1, None, 1, None, None) == NULL
+    assert fs(P, P, P, P, P, P, P, MIS, 1, 4, 2, 4, 32, 0.1, None, 1, None, None) == ALIGN
+    assert fs(P, P, P, P, P, P, P, P, 1, 0, 2, 4, 32, 0.1, None, 1, None, None) == OK
+    fc = lib.gdn_conv1d_silu_seq_snapshots
+    assert fc(P, P, P, P, None, 1, 4, 256, 4, None, 1, None, None) == NULL
+    assert fc(P, P, P, P, P, 1, 4, 256, 1, None, 1, None, None) == SHAPE
+    assert fc(P, P, P, P, P, 1, 0, 256, 4, None, 1, None, None) == OK
+
+
 def test_block_validation(lib):
     assert block(lib, qkv=None) == NULL
     assert block(lib, out=None) == NULL

@@ -292,6 +292,79 @@ def test_recurrence_scan_prefill_4x4096(lib):
         assert_rms(sth[n, vh], s_ref[0, 0], f"final state ({n},{vh})")
 
 
+@pytest.mark.parametrize("Hk,H,S", [(2, 4, 32), (16, 32, 128), (4, 16, 256), (1, 2, 64)])
+def test_recurrence_decode_2pass(lib, Hk, H, S):
+    """Factorised readout: the state is the plain decode's bit for bit, y matches the
+    oracle within the one-step bound."""
+    cfg, x, st0 = rec_case(Hk, H, S, N=3, T=1, seed=S + H + 7)
+    N = cfg.n_seqs
+    st_a, st_b = dev(st0), dev(st0)
+    y_a = run_decode(lib, cfg, x, st_a, 0)
+    y_b = torch.zeros(N, H, S, device="cuda")
+    lib.gdn_recurrence_decode_2pass(st_b, dev(x["q"][:, 0]), dev(x["k"][:, 0]), dev(x["v"][:, 0]),
+                                    dev(x["g"][:, 0]), dev(x["beta"][:, 0]), y_b, N, Hk, H, S,
+                                    cfg.scale)
+    assert torch.equal(st_a, st_b)
+    st_ref = f64(st0)
+    y_ref, _ = oracle.recurrence(st_ref, x["q"][:, :1], x["k"][:, :1], x["v"][:, :1],
+                                 x["g"][:, :1], x["beta"][:, :1], cfg.scale)
+    assert_step(host(y_b), y_ref[:, 0], "y (2-pass)")
+    assert_step(host(y_a), host(y_b), "y plain vs 2-pass")
+
+
+@pytest.mark.parametrize("S,T", [(128, 37), (32, 16)])
+def test_recurrence_scan_snapshots(lib, S, T):
+    """snaps[t] is the state after token t: equal bit for bit to t+1 decode calls,
+    and restoring snaps[M-1] then scanning the rest reproduces the full scan."""
+    cfg, x, st0 = rec_case(2, 4, S, N=2, T=T, seed=S + T + 11)
+    N, H = cfg.n_seqs, cfg.n_v_heads
+    st_full = dev(st0)
+    y_full = run_scan(lib, cfg, x, st_full, 0, T)
+    st = dev(st0)
+    y = torch.zeros(N, T, H, S, device="cuda")
+    snaps = torch.zeros(N, T, H, S, S, device="cuda")
+    lib.gdn_recurrence_scan_snapshots(st, dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["g"]),
+                                      dev(x["beta"]), y, snaps, N, T, cfg.n_k_heads, H, S,
+                                      cfg.scale)
+    assert torch.equal(y, y_full) and torch.equal(st, st_full)
+    assert torch.equal(snaps[:, T - 1], st)
+    st_d = dev(st0)
+    for t in range(T):
+        run_decode(lib, cfg, x, st_d, t)
+        assert torch.equal(snaps[:, t], st_d), f"snapshot {t}"
+    st_ref = f64(st0)
+    oracle.recurrence(st_ref, scale=cfg.scale, **{k_: v_[:, :5] for k_, v_ in x.items()})
+    assert_step(host(snaps[:, 4]), st_ref, "snapshot 4 vs oracle")
+    M = T // 3  # accept M tokens, roll back the rest, resume
+    st_r = snaps[:, M - 1].contiguous().clone()
+    y_r = run_scan(lib, cfg, x, st_r, M, T)
+    assert torch.equal(y_r, y_full[:, M:]) and torch.equal(st_r, st_full)
+
+
+def test_conv1d_silu_seq_snapshots(lib):
+    r = np.random.default_rng(105)
+    N, T, C, K = 2, 9, 256, 4
+    qkv = r.normal(0, 1, (N, T, C)).astype(np.float32)
+    w = r.normal(0, 0.5, (C, K)).astype(np.float32)
+    cs0 = r.normal(0, 1, (N, C, K - 1)).astype(np.float32)
+    cs = dev(cs0)
+    out = torch.zeros(N, T, C, device="cuda")
+    snaps = torch.zeros(N, T, C, K - 1, device="cuda")
+    lib.gdn_conv1d_silu_seq_snapshots(dev(qkv), dev(w), cs, out, snaps, N, T, C, K)
+    cs2 = dev(cs0)
+    out2 = torch.zeros(N, T, C, device="cuda")
+    lib.gdn_conv1d_silu_seq(dev(qkv), dev(w), cs2, out2, N, T, C, K)
+    assert torch.equal(out, out2) and torch.equal(cs, cs2)
+    cs3 = dev(cs0)
+    for t in range(T):
+        o1 = torch.zeros(N, C, device="cuda")
+        lib.gdn_conv1d_silu(dev(qkv[:, t]), dev(w), cs3, o1, N, C, K)
+        assert torch.equal(snaps[:, t], cs3), f"conv snapshot {t}"
+    ref = f64(cs0)
+    oracle.conv1d_silu_seq(qkv[:, :3], w, ref)
+    assert_step(host(snaps[:, 2]), ref, "conv snapshot 2 vs oracle")
+
+
 # ------------------------------------------------------------------ fused block
 
 class BlockRun:
