@@ -21,8 +21,6 @@ __device__ unsigned g_watchdog;
 constexpr int kWarps = 8;           // consumer warps per CTA
 constexpr int kRowsPerWarp = 4;     // R
 constexpr int kRowsPerCta = kWarps * kRowsPerWarp;  // 32 state rows
-constexpr int kScanTokens = 16;     // tokens per staged chunk in the scan
-constexpr int kScanStages = 2;
 
 // Lanes that hold a finished readout for one of the R rows, and which row.
 template <int R>
@@ -102,33 +100,87 @@ __global__ void __launch_bounds__(kWarps * 32) recurrence_decode_kernel(
 }
 
 // ---------------------------------------------------------------------------- scan
-// Grid: one CTA per (sequence, v-head, block of 32 rows); 8 consumer warps hold
-// their 4 rows in registers for all tokens, plus one producer warp that stages the
+// The scan is bound by instruction issue, not memory: every state element is
+// touched by 4 FP operations per token and the two dots per row and token must be
+// reduced. Here a state row is held by a group of 4 lanes instead of a whole warp,
+// so a warp carries 8 rows and each reduction needs only 2 shuffle levels.
+//
+// Lane g (0..3) of a row group holds the 8 chunks of E cells that lanes g, g+4, ...,
+// g+28 hold in the decode kernels' layout (chunk m = cells [4E*m + E*g, ... + E)).
+// The first three butterfly levels of the decode kernels (partners L^16, L^8,
+// L^4) then pair chunks inside one lane, in the same order, and the last two
+// (L^2, L^1) are shuffles inside the group: every sum, hence every state bit and
+// output, is the decode kernels'. A scan over T tokens still equals T decode calls
+// bit for bit.
+constexpr int kScanWarps = 4;       // consumer warps per CTA
+constexpr int kScanRowsPerWarp = 8; // 8 groups of 4 lanes
+constexpr int kScanRows = kScanWarps * kScanRowsPerWarp;  // 32 state rows per CTA
+constexpr int kScanTok = 16;        // tokens per staged chunk
+constexpr int kScanDepth = 2;       // chunks in flight
+
+template <int E>
+struct ScanSmem {
+    static constexpr int S = 32 * E;
+    static constexpr int kFloats = kScanTok * S;             // per array per stage
+    static constexpr int vFloats = kScanTok * kScanRows;
+    static constexpr size_t stage_bytes = (2 * kFloats + vFloats) * sizeof(float);
+    static constexpr size_t bytes = kScanDepth * stage_bytes + 2 * kScanDepth * sizeof(uint64_t);
+};
+
+// The 8 chunks of lane g of a row: chunk m starts at cell 4E*m + E*g.
+template <int E>
+__device__ __forceinline__ void load_group(float (&dst)[8][E], const float *row, int g) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) load_vec<E>(dst[m], row + 4 * E * m + E * g);
+}
+
+template <int E>
+__device__ __forceinline__ void store_group(float *row, const float (&src)[8][E], int g) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) store_vec<E>(row + 4 * E * m + E * g, src[m]);
+}
+
+// Dot of a row with x (lane g's chunks read from shared memory at xs) over the
+// whole row, in the decode kernels' exact order: per-chunk FMA chains, then chunks
+// m and m+4, m and m+2, 0 and 1 (the partners L^16, L^8, L^4), then the group
+// shuffles L^2 and L^1. Every lane of the group returns the same bits.
+template <int E>
+__device__ __forceinline__ float group_dot(const float (&r)[8][E], const float *xs, int g) {
+    float p[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        float x[E];
+        load_vec<E>(x, xs + 4 * E * m + E * g);
+        p[m] = lane_dot<E>(r[m], x);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) p[m] = __fadd_rn(p[m], p[m + 4]);
+#pragma unroll
+    for (int m = 0; m < 2; ++m) p[m] = __fadd_rn(p[m], p[m + 2]);
+    float acc = __fadd_rn(p[0], p[1]);
+    acc = __fadd_rn(acc, __shfl_xor_sync(FULL_MASK, acc, 2));
+    acc = __fadd_rn(acc, __shfl_xor_sync(FULL_MASK, acc, 1));
+    return acc;
+}
+
+// Grid: one CTA per (sequence, v-head, block of 32 rows); 4 consumer warps hold 8
+// rows each in registers for all tokens, plus one producer warp that stages the
 // per-token k, q (S floats each) and this block's 32 v values through a 2-deep ring
 // of shared-memory chunks with bulk copies, each chunk tracked by a "full" and an
 // "empty" mbarrier. g and beta (one float per token and head) are read by the lanes
 // a chunk ahead and broadcast with shuffles. The state reaches HBM once per call.
-template <int E>
-struct ScanSmem {
-    static constexpr int S = 32 * E;
-    static constexpr int kFloats = kScanTokens * S;             // per array per stage
-    static constexpr int vFloats = kScanTokens * kRowsPerCta;
-    static constexpr size_t stage_bytes = (2 * kFloats + vFloats) * sizeof(float);
-    static constexpr size_t bytes = kScanStages * stage_bytes + 2 * kScanStages * sizeof(uint64_t);
-};
-
 template <int E, bool SNAP>
-__global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrence_scan_kernel(
+__global__ void __launch_bounds__((kScanWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrence_scan_kernel(
     float *state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
     float *__restrict__ y, int n_tokens, int n_k_heads, int n_v_heads, float scale,
     const int32_t *__restrict__ slots, int pool, int32_t *err_count, float *__restrict__ snaps) {
-    constexpr int S = 32 * E, R = kRowsPerWarp, TC = kScanTokens;
-    constexpr int kBlocksPerHead = S / kRowsPerCta;
+    constexpr int S = 32 * E, TC = kScanTok;
+    constexpr int kBlocksPerHead = S / kScanRows;
     using L = ScanSmem<E>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + kScanStages * L::stage_bytes);
-    uint64_t *empty = full + kScanStages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + kScanDepth * L::stage_bytes);
+    uint64_t *empty = full + kScanDepth;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int part = blockIdx.x % kBlocksPerHead;
@@ -141,9 +193,9 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrenc
         return;
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kScanStages; ++s) {
+        for (int s = 0; s < kScanDepth; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, kWarps);
+            mbar_init(empty + s, kScanWarps);
         }
         fence_mbar_init();
     }
@@ -154,13 +206,13 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrenc
     const float *kbase = k + (static_cast<size_t>(n) * n_tokens * n_k_heads + kh) * S;
     const float *qbase = q + (static_cast<size_t>(n) * n_tokens * n_k_heads + kh) * S;
     const float *vbase = v + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S +
-                         part * kRowsPerCta;
+                         part * kScanRows;
 
-    if (warp == kWarps) {
+    if (warp == kScanWarps) {
         // ---- producer warp: lane t copies token t of each chunk.
         bool ok = true;
         for (int c = 0; c < n_chunks && ok; ++c) {
-            const int s = c % kScanStages, use = c / kScanStages;
+            const int s = c % kScanDepth, use = c / kScanDepth;
             if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1)) {
                 if (lane == 0) atomicOr(&g_watchdog, WD_STAGE_FREE);
                 ok = false;
@@ -172,39 +224,37 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrenc
             float *qs = ks + L::kFloats;
             float *vs = qs + L::kFloats;
             if (lane == 0)
-                mbar_arrive_expect_tx(full + s, tc * (2 * S + kRowsPerCta) * sizeof(float));
+                mbar_arrive_expect_tx(full + s, tc * (2 * S + kScanRows) * sizeof(float));
             __syncwarp();
             if (lane < tc) {
                 const size_t t = static_cast<size_t>(c) * TC + lane;
                 bulk_g2s(ks + lane * S, kbase + t * kq_tok, S * sizeof(float), full + s);
                 bulk_g2s(qs + lane * S, qbase + t * kq_tok, S * sizeof(float), full + s);
-                bulk_g2s(vs + lane * kRowsPerCta, vbase + t * v_tok, kRowsPerCta * sizeof(float),
+                bulk_g2s(vs + lane * kScanRows, vbase + t * v_tok, kScanRows * sizeof(float),
                          full + s);
             }
         }
         // Do not leave while copies may still be landing in this CTA's shared memory.
         if (ok && n_chunks > 0) {
-            for (int c = max(0, n_chunks - kScanStages); c < n_chunks; ++c)
-                mbar_wait(full + c % kScanStages, (c / kScanStages) & 1);
+            for (int c = max(0, n_chunks - kScanDepth); c < n_chunks; ++c)
+                mbar_wait(full + c % kScanDepth, (c / kScanDepth) & 1);
         }
         return;
     }
 
-    // ---- consumer warps
-    const int row0 = part * kRowsPerCta + warp * R;
-    float *gstate = state + ((static_cast<size_t>(slot) * n_v_heads + vh) * S + row0) * S;
-    float row[R][E];
-#pragma unroll
-    for (int r = 0; r < R; ++r) load_vec<E>(row[r], gstate + r * S + lane * E);
+    // ---- consumer warps: lane = 4 * (row of the warp) + g
+    const int rho = lane >> 2, gq = lane & 3;
+    const int rl = warp * kScanRowsPerWarp + rho;  // row within the CTA's 32
+    const int j = part * kScanRows + rl;         // state row (v index)
+    float *grow = state + ((static_cast<size_t>(slot) * n_v_heads + vh) * S + j) * S;
+    float row[8][E];
+    load_group<E>(row, grow, gq);
     const size_t gb_base = static_cast<size_t>(n) * n_tokens * n_v_heads + vh;
-    int yr;
-    const bool writer = y_writer<R>(lane, yr);
-    float *ybase = y + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S + row0 + yr;
+    float *yrow = y + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S + j;
     // snapshot of token t: snaps[n][t][H][S][S], the state layout of one slot
     const size_t snap_tok = static_cast<size_t>(n_v_heads) * S * S;
-    float *sbase = SNAP ? snaps + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S * S +
-                              static_cast<size_t>(row0) * S + lane * E
-                        : nullptr;
+    float *srow = SNAP ? snaps + ((static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S + j) * S
+                       : nullptr;
 
     // g and beta of token (chunk*TC + lane), one chunk ahead.
     auto fetch_gb = [&](int c, float &dec, float &bt) {
@@ -221,9 +271,9 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrenc
     fetch_gb(0, dec_cur, bt_cur);
     bool ok = true;
     for (int c = 0; c < n_chunks; ++c) {
-        const int s = c % kScanStages;
+        const int s = c % kScanDepth;
         fetch_gb(c + 1, dec_nxt, bt_nxt);
-        if (!mbar_wait(full + s, (c / kScanStages) & 1)) {
+        if (!mbar_wait(full + s, (c / kScanDepth) & 1)) {
             if (lane == 0) atomicOr(&g_watchdog, WD_STAGE_COPY);
             ok = false;
             break;
@@ -234,19 +284,30 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrenc
         const float *vs = qs + L::kFloats;
         const int tc = min(TC, n_tokens - c * TC);
         for (int t = 0; t < tc; ++t) {
-            float kk[E], qq[E], vv[R];
-            load_vec<E>(kk, ks + t * S + lane * E);
-            load_vec<E>(qq, qs + t * S + lane * E);
-            load_vec<R>(vv, vs + t * kRowsPerCta + warp * R);
+            // the row step of the decode kernels, in the group layout
             const float decay = __shfl_sync(FULL_MASK, dec_cur, t);
             const float bt = __shfl_sync(FULL_MASK, bt_cur, t);
-            const float ysum = row_step<E, R>(row, kk, qq, vv, decay, bt, lane);
-            if (writer) ybase[(static_cast<size_t>(c) * TC + t) * v_tok] = __fmul_rn(scale, ysum);
-            if constexpr (SNAP) {
-                float *sn = sbase + (static_cast<size_t>(c) * TC + t) * snap_tok;
+            // k and q chunks are read from shared memory where they are used, so the
+            // warp keeps only its state rows live across the token
+            const float *kt = ks + t * S;
+            const float vj = vs[t * kScanRows + rl];
 #pragma unroll
-                for (int r = 0; r < R; ++r) store_vec<E>(sn + r * S, row[r]);
+            for (int m = 0; m < 8; ++m)
+#pragma unroll
+                for (int e = 0; e < E; ++e) row[m][e] = __fmul_rn(row[m][e], decay);
+            const float pred = group_dot<E>(row, kt, gq);
+            const float delta = __fmul_rn(__fsub_rn(vj, pred), bt);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                float kc[E];
+                load_vec<E>(kc, kt + 4 * E * m + E * gq);
+#pragma unroll
+                for (int e = 0; e < E; ++e) row[m][e] = __fmaf_rn(kc[e], delta, row[m][e]);
             }
+            const float ysum = group_dot<E>(row, qs + t * S, gq);
+            const size_t tok = static_cast<size_t>(c) * TC + t;
+            if (gq == 0) yrow[tok * v_tok] = __fmul_rn(scale, ysum);
+            if constexpr (SNAP) store_group<E>(srow + tok * snap_tok, row, gq);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + s);
@@ -254,8 +315,7 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrenc
         bt_cur = bt_nxt;
     }
     if (!ok) return;  // leave the state untouched rather than write a partial scan
-#pragma unroll
-    for (int r = 0; r < R; ++r) store_vec<E>(gstate + r * S + lane * E, row[r]);
+    store_group<E>(grow, row, gq);
 }
 
 // Opts a kernel in to more than 48 KiB of dynamic shared memory.
@@ -291,9 +351,9 @@ gdn_status launch_scan(float *state, const float *q, const float *k, const float
     constexpr int S = 32 * E;
     const size_t smem = ScanSmem<E>::bytes;
     GDN_TRY(set_smem(recurrence_scan_kernel<E, SNAP>, smem));
-    const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / kRowsPerCta);
+    const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / kScanRows);
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-    recurrence_scan_kernel<E, SNAP><<<static_cast<unsigned>(blocks), (kWarps + 1) * 32, smem, s>>>(
+    recurrence_scan_kernel<E, SNAP><<<static_cast<unsigned>(blocks), (kScanWarps + 1) * 32, smem, s>>>(
         state, q, k, v, g, beta, y, n_tokens, n_k_heads, n_v_heads, scale, slots, pool,
         err_count, snaps);
     return launch_status();
