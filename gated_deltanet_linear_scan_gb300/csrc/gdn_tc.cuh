@@ -1,0 +1,121 @@
+// gdn_tc.cuh -- 5th-generation tensor core (tcgen05) building blocks for sm_103a:
+// tensor-memory allocation, shared-memory matrix descriptors, the TF32 MMA issued
+// by one thread with its accumulator in tensor memory, completion through an
+// mbarrier, and tensor memory -> register loads.
+//
+// Operand layout used throughout: K-major, no swizzle. A tile of R rows by K
+// 32-bit elements is stored as 8-row x 16-byte core matrices; element (r, k) sits
+// at byte  (r / 8) * sbo + (k / 4) * lbo + (r % 8) * 16 + (k % 4) * 4,
+// so a core matrix is 128 contiguous bytes, lbo steps to the next 4 elements of K
+// and sbo to the next 8 rows.
+#pragma once
+
+#include <cstdint>
+
+#include "gdn_device.cuh"
+
+namespace gdn {
+namespace tc {
+
+// Byte offset of element (r, k) in the K-major core-matrix layout.
+__host__ __device__ __forceinline__ uint32_t kmajor_offset(int r, int k, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint32_t>(r >> 3) * sbo + static_cast<uint32_t>(k >> 2) * lbo +
+           static_cast<uint32_t>(r & 7) * 16u + static_cast<uint32_t>(k & 3) * 4u;
+}
+
+// Shared-memory matrix descriptor: start address, leading (K) and stride (row
+// group) byte offsets, descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(const void *start, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr(start) & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// Instruction descriptor of a dense kind::tf32 MMA: f32 accumulator, tf32 A and
+// B, both K-major, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ---- tensor memory (allocation is warp-wide; the same warp frees it)
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---- MMA (one thread issues; D lives in tensor memory)
+
+// D[M x N] (+)= A[M x K=8] * B[N x K=8]^T, tf32 inputs, f32 accumulate.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
+// Arrive once on `bar` when every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+// ---- tensor memory -> registers: lane i of the warp reads 16 consecutive 32-bit
+// columns of tensor-memory lane (taddr's lane + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Round-to-nearest tf32 (10 explicit mantissa bits) of an fp32 value, kept in a
+// 32-bit container, and the split x = hi + lo used for 3-pass tf32 products.
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
+    hi = to_tf32(x);
+    lo = to_tf32(x - hi);
+}
+
+}  // namespace tc
+}  // namespace gdn

@@ -1,0 +1,70 @@
+"""GPU unit test of the tcgen05 building blocks (gdn_tc.cuh) on a single tile.
+
+D[128 x 64] = A[128 x 32] B[64 x 32]^T on the tensor cores: one tf32 pass must
+equal the product of tf32-rounded inputs (up to accumulation order), and the
+three-pass hi/lo split must match the fp64 product to fp32 accuracy.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "gated_deltanet_linear_scan_gb300", "csrc")
+
+
+@pytest.fixture(scope="module")
+def tclib(tmp_path_factory):
+    out = str(tmp_path_factory.mktemp("tc") / "libtc_gemm_test.so")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                    "-shared", "-Xcompiler", "-fPIC", "-I", CSRC, "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "cuda", "tc_gemm_test.cu"), "-o", out], check=True)
+    lib = ctypes.CDLL(out)
+    lib.tc_gemm_test.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_void_p]
+    lib.tc_gemm_test.restype = ctypes.c_int
+    return lib
+
+
+def tf32_round(x):
+    b = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x1000) & 0xFFFFE000  # nearest, ties away from zero (magnitude bits)
+    return b.astype(np.uint32).view(np.float32)
+
+
+def run(tclib, A, B, split):
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dD = torch.full((128, 64), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = tclib.tc_gemm_test(dA.data_ptr(), dB.data_ptr(), dD.data_ptr(), split, st.data_ptr(),
+                            torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0, "the MMA completion wait gave up"
+    return dD.cpu().numpy()
+
+
+def test_single_pass_tf32(tclib):
+    r = np.random.default_rng(1)
+    A = r.normal(0, 1, (128, 32)).astype(np.float32)
+    B = r.normal(0, 1, (64, 32)).astype(np.float32)
+    D = run(tclib, A, B, 0)
+    want = tf32_round(A).astype(np.float64) @ tf32_round(B).astype(np.float64).T
+    np.testing.assert_allclose(D, want, rtol=0, atol=1e-4)
+
+
+def test_three_pass_split_tf32(tclib):
+    r = np.random.default_rng(2)
+    A = r.normal(0, 1, (128, 32)).astype(np.float32)
+    B = r.normal(0, 1, (64, 32)).astype(np.float32)
+    D = run(tclib, A, B, 1)
+    want = A.astype(np.float64) @ B.astype(np.float64).T
+    np.testing.assert_allclose(D, want, rtol=0, atol=2e-5)
+    single = run(tclib, A, B, 0)
+    assert np.abs(single - want).max() > 10 * np.abs(D - want).max()
