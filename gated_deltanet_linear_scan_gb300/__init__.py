@@ -20,7 +20,7 @@ __all__ = [
     "gdn_decay_gate", "gdn_beta_sigmoid", "gdn_conv1d_silu", "gdn_conv1d_silu_seq",
     "gdn_qkv_split_norm", "gdn_recurrence_decode", "gdn_recurrence_scan", "gdn_gated_norm",
     "gdn_block_decode", "gdn_recurrence_decode_2pass", "gdn_recurrence_scan_snapshots",
-    "gdn_conv1d_silu_seq_snapshots",
+    "gdn_conv1d_silu_seq_snapshots", "gdn_block_prefill_workspace_size", "gdn_block_prefill",
 ]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
@@ -54,6 +54,9 @@ _SIGS = {
     "gdn_recurrence_decode_2pass": ([_P] * 7 + [_I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
     "gdn_recurrence_scan_snapshots": ([_P] * 8 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
     "gdn_conv1d_silu_seq_snapshots": ([_P] * 5 + [_I, _I, _I, _I, _P, _I, _P, _P], _I),
+    "gdn_block_prefill_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
+    "gdn_block_prefill": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P, _P,
+                                       ctypes.c_size_t, _P], _I),
 }
 
 
@@ -246,3 +249,25 @@ def gdn_conv1d_silu_seq_snapshots(qkv, w, conv_state, out, snaps, n_seqs, n_toke
         _ptr(qkv, "qkv"), _ptr(w, "w"), _ptr(conv_state, "conv_state"), _ptr(out, "out"),
         _ptr(snaps, "snaps"), n_seqs, n_tokens, conv_dim, conv_kernel, _slots(slots), pool,
         _errc(err_count), _stream(stream)))
+
+
+def gdn_block_prefill_workspace_size(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size):
+    return library().gdn_block_prefill_workspace_size(n_seqs, n_tokens, n_k_heads, n_v_heads,
+                                                      state_size)
+
+
+def gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                      n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                      norm_eps, workspace, slots=None, pool=None, err_count=None, stream=None):
+    """`workspace`: a CUDA tensor of at least gdn_block_prefill_workspace_size() bytes."""
+    pool = _pool(pool, n_seqs, slots)
+    import torch
+    if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    _check("gdn_block_prefill", library().gdn_block_prefill(
+        _ptr(qkv, "qkv"), _ptr(conv_w, "conv_w"), _ptr(conv_state, "conv_state"),
+        _ptr(alpha, "alpha"), _ptr(b, "b"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(z, "z"),
+        _ptr(norm_w, "norm_w"), _ptr(state, "state"), _ptr(out, "out"), n_seqs, n_tokens,
+        n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps, norm_eps, _slots(slots),
+        pool, _errc(err_count), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(stream)))

@@ -33,6 +33,12 @@ inline gdn_status check_heads(int n_k_heads, int n_v_heads, int state_size) {
     return GDN_OK;
 }
 
+// Gated RMSNorm over `rows` rows of head_dim; with `slots` non-NULL the rows of
+// sequence r / rows_per_seq are skipped when its slot is outside [0, pool).
+gdn_status launch_gated_norm(const float *y, const float *w, const float *z, float *out,
+                             long long rows, int head_dim, float eps, long long rows_per_seq,
+                             const int32_t *slots, int pool, cudaStream_t s);
+
 // Per-translation-unit watchdog flags (a bounded wait that gave up sets a bit).
 unsigned read_and_clear_watchdog_recurrence(cudaStream_t s);
 unsigned read_and_clear_watchdog_block(cudaStream_t s);

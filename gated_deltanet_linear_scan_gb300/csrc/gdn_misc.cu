@@ -117,15 +117,23 @@ __global__ void __launch_bounds__(kThreads) qkv_split_norm_kernel(
 
 // Gated RMSNorm, fm_kernel_ssm.m "Gated RMSNorm" and ssm_gated_delta.cu Kernel 3:
 // one warp per head row, one shuffle reduction, weight shared across heads.
+// With `slots` non-NULL, row r belongs to sequence r / rows_per_seq, and the rows
+// of a sequence whose slot is outside [0, pool) are left untouched.
 template <int E>
 __global__ void __launch_bounds__(kThreads) gated_norm_kernel(const float *y,
                                                                const float *__restrict__ w,
                                                                const float *__restrict__ z,
                                                                float *out, long long rows,
-                                                               float eps) {
+                                                               float eps, long long rows_per_seq,
+                                                               const int32_t *__restrict__ slots,
+                                                               int pool) {
     constexpr int D = 32 * E;
     const long long row = blockIdx.x * static_cast<long long>(kThreads / 32) + (threadIdx.x >> 5);
     if (row >= rows) return;
+    if (slots) {
+        const int slot = slots[row / rows_per_seq];
+        if (slot < 0 || slot >= pool) return;
+    }
     const int lane = threadIdx.x & 31;
     float yv[E], zv[E], wv[E];
     load_vec<E>(yv, y + row * D + lane * E);
@@ -179,6 +187,21 @@ gdn_status conv_common(const float *qkv, const float *w, float *conv_state, floa
 }
 
 }  // namespace
+
+gdn_status launch_gated_norm(const float *y, const float *w, const float *z, float *out,
+                             long long rows, int head_dim, float eps, long long rows_per_seq,
+                             const int32_t *slots, int pool, cudaStream_t s) {
+    if (rows == 0) return GDN_OK;
+    const unsigned blocks = static_cast<unsigned>((rows + kThreads / 32 - 1) / (kThreads / 32));
+    switch (head_dim) {
+        case 32: gated_norm_kernel<1><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, rows_per_seq, slots, pool); break;
+        case 64: gated_norm_kernel<2><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, rows_per_seq, slots, pool); break;
+        case 128: gated_norm_kernel<4><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, rows_per_seq, slots, pool); break;
+        default: gated_norm_kernel<8><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, rows_per_seq, slots, pool); break;
+    }
+    return launch_status();
+}
+
 }  // namespace gdn
 
 using namespace gdn;
@@ -277,16 +300,7 @@ gdn_status gdn_gated_norm(const float *y, const float *w, const float *z, float 
         return (head_dim % 32 == 0 && head_dim <= 256) ? GDN_ERR_UNSUPPORTED : GDN_ERR_SHAPE;
     }
     if (!aligned16(y) || !aligned16(w) || !aligned16(z) || !aligned16(out)) return GDN_ERR_ALIGN;
-    if (rows == 0) return GDN_OK;
-    const cudaStream_t s = as_cuda(stream);
-    const unsigned blocks = static_cast<unsigned>((rows + kThreads / 32 - 1) / (kThreads / 32));
-    switch (head_dim) {
-        case 32: gated_norm_kernel<1><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps); break;
-        case 64: gated_norm_kernel<2><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps); break;
-        case 128: gated_norm_kernel<4><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps); break;
-        default: gated_norm_kernel<8><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps); break;
-    }
-    return launch_status();
+    return launch_gated_norm(y, w, z, out, rows, head_dim, eps, 1, nullptr, 0, as_cuda(stream));
 }
 
 }  // extern "C"

@@ -48,6 +48,7 @@
 #ifndef GDN_H
 #define GDN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -199,6 +200,30 @@ gdn_status gdn_block_decode(const float *qkv, const float *conv_w, float *conv_s
                             int conv_kernel, float scale, float l2_eps, float norm_eps,
                             const int32_t *slots, int pool, int32_t *err_count,
                             gdn_stream_t stream);
+
+/* Bytes of workspace gdn_block_prefill needs for these sizes (0 for invalid ones). */
+size_t gdn_block_prefill_workspace_size(int n_seqs, int n_tokens, int n_k_heads, int n_v_heads,
+                                        int state_size);
+
+/* The whole block over n_tokens positions per sequence (prefill), following the
+ * batched variants of ssm_gated_delta.cu ("BATCHED (prefill) variants": decay gate,
+ * conv scan, q/k norm with the v passthrough, recurrence scan) and the gated
+ * RMSNorm: conv1d+SiLU scan (rolling conv_state), q/k L2-norm, decay gate, beta =
+ * sigmoid(b), the sequential scan (state in place), gated RMSNorm.
+ * qkv: [n_seqs][n_tokens][C] raw; alpha, b: [n_seqs][n_tokens][H]; z, out:
+ * [n_seqs][n_tokens][H][S]; the other arguments as for gdn_block_decode (any K in
+ * [2, 8]). The result equals n_tokens gdn_block_decode calls up to rounding.
+ * workspace: device memory of at least gdn_block_prefill_workspace_size() bytes,
+ * 16-byte aligned, owned by the caller; its contents on entry do not matter and
+ * are garbage afterwards. Too small: GDN_ERR_SHAPE. Several kernels are enqueued
+ * on `stream`; calls that share a workspace must not overlap. */
+gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_state,
+                             const float *alpha, const float *b, const float *dt, const float *a,
+                             const float *z, const float *norm_w, float *state, float *out,
+                             int n_seqs, int n_tokens, int n_k_heads, int n_v_heads,
+                             int state_size, int conv_kernel, float scale, float l2_eps,
+                             float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
+                             void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 #ifdef __cplusplus
 }

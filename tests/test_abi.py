@@ -140,6 +140,31 @@ def test_variant_validation(lib):
     assert fc(P, P, P, P, P, 1, 0, 256, 4, None, 1, None, None) == OK
 
 
+def test_prefill_validation(lib):
+    ws = lib.gdn_block_prefill_workspace_size
+    ws.restype = ctypes.c_size_t
+    need = ws(2, 16, 2, 4, 32)
+    # conv_out + q + k + v + g + beta, each rounded up to 64 floats
+    C = (2 * 2 + 4) * 32
+    parts = [2 * 16 * C, 2 * 16 * 2 * 32, 2 * 16 * 2 * 32, 2 * 16 * 4 * 32, 2 * 16 * 4, 2 * 16 * 4]
+    assert need == 4 * sum((p + 63) // 64 * 64 for p in parts)
+    assert ws(-1, 16, 2, 4, 32) == 0
+    f = lib.gdn_block_prefill
+    f.argtypes = [ctypes.c_void_p] * 11 + [ctypes.c_int] * 6 + [ctypes.c_float] * 3 + [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+        ctypes.c_void_p]
+
+    def call(workspace=P, nbytes=need, n_tokens=16, K=4, qkv=P):
+        return f(qkv, P, P, P, P, P, P, P, P, P, P, 2, n_tokens, 2, 4, 32, K, 0.1, 1e-6, 1e-6,
+                 None, 2, None, workspace, nbytes, None)
+    assert call(qkv=None) == NULL
+    assert call(workspace=None) == NULL
+    assert call(nbytes=need - 4) == SHAPE
+    assert call(workspace=MIS) == ALIGN
+    assert call(K=9) == SHAPE
+    assert call(n_tokens=0, workspace=None) == OK
+
+
 def test_block_validation(lib):
     assert block(lib, qkv=None) == NULL
     assert block(lib, out=None) == NULL

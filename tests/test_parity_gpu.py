@@ -563,3 +563,99 @@ def test_block_equals_unfused_pipeline(lib):
     assert torch.equal(cv_f, cv_u)
     assert torch.equal(st_f, st_u)
     assert torch.equal(out_f, out_u)
+
+
+# ------------------------------------------------------------------ prefill block
+
+def run_prefill(lib, cfg, T, seqs_in, state, conv, slots=None, pool=None, err=None, out=None):
+    N, H, S = len(seqs_in[0]["qkv"]), cfg.n_v_heads, cfg.state_size
+    st = I.block_static(cfg)
+    stack = {key: np.stack([a[key] for a in seqs_in], axis=1) for key in ("qkv", "alpha", "b", "z")}
+    out = torch.zeros(N, T, H, S, device="cuda") if out is None else out
+    nbytes = lib.gdn_block_prefill_workspace_size(N, T, cfg.n_k_heads, H, S)
+    ws = torch.empty(nbytes // 4, device="cuda")
+    lib.gdn_block_prefill(dev(stack["qkv"]), dev(st["conv_w"]), conv, dev(stack["alpha"]),
+                          dev(stack["b"]), dev(st["dt"]), dev(st["a"]), dev(stack["z"]),
+                          dev(st["norm_w"]), state, out, N, T, cfg.n_k_heads, H, S,
+                          cfg.conv_kernel, cfg.scale, cfg.eps, cfg.eps, ws, slots=slots,
+                          pool=pool, err_count=err)
+    return out, stack
+
+
+@pytest.mark.parametrize("Hk,H,S,N,T", [(2, 4, 32, 1, 16), (2, 4, 128, 2, 37), (16, 32, 128, 3, 20)])
+def test_block_prefill(lib, Hk, H, S, N, T):
+    """The prefill block equals T single-token steps of the block (oracle), and the
+    GPU's own T decode calls, within the stated bounds."""
+    cfg = I.get_config(0, n_k_heads=Hk, n_v_heads=H, state_size=S, n_seqs=N, cid=700 + S + T)
+    steps = [I.block_step(cfg, t) for t in range(T)]
+    st0, cs0 = I.state_pool(cfg), I.conv_state_pool(cfg)
+    state, conv = dev(st0), dev(cs0)
+    out, stack = run_prefill(lib, cfg, T, steps, state, conv)
+    got = host(out)
+    stat = I.block_static(cfg)
+    ref_st, ref_cs = f64(st0), f64(cs0)
+    ref = np.zeros(got.shape)
+    for t in range(T):
+        a = steps[t]
+        ref[:, t], _ = oracle.block_decode(a["qkv"], stat["conv_w"], ref_cs, a["alpha"], a["b"],
+                                           stat["dt"], stat["a"], a["z"], stat["norm_w"], ref_st,
+                                           cfg.n_k_heads, cfg.scale, cfg.eps, cfg.eps)
+    assert_step(got[:, 0], ref[:, 0], "out token 0")
+    assert_rms(got, ref, "out")
+    assert_rms(host(state), ref_st, "state")
+    assert_rms(host(conv), ref_cs, "conv_state")
+    # against T calls of the GPU's fused decode
+    st_d, cs_d = dev(st0), dev(cs0)
+    dd = {k_: dev(v_) for k_, v_ in stat.items()}
+    for t in range(T):
+        a = steps[t]
+        o = torch.empty(N, H, S, device="cuda")
+        lib.gdn_block_decode(dev(a["qkv"]), dd["conv_w"], cs_d, dev(a["alpha"]), dev(a["b"]),
+                             dd["dt"], dd["a"], dev(a["z"]), dd["norm_w"], st_d, o, N, Hk, H, S,
+                             4, cfg.scale, cfg.eps, cfg.eps)
+        assert_step(got[:, t], host(o), f"prefill vs decode, token {t}")
+
+
+def test_block_prefill_invalid_slot(lib):
+    cfg = I.get_config(0, n_seqs=3, pool=4, cid=800)
+    T = 12
+    steps = [I.block_step(cfg, t) for t in range(T)]
+    st0, cs0 = I.state_pool(cfg), I.conv_state_pool(cfg)
+    state, conv = dev(st0), dev(cs0)
+    slots = np.array([3, 6, 0], dtype=np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((3, T, cfg.n_v_heads, cfg.state_size), 9.0, device="cuda")
+    run_prefill(lib, cfg, T, steps, state, conv, slots=dev(slots), pool=4, err=err, out=out)
+    assert host(err)[0] == 1
+    o = host(out)
+    assert np.all(o[1] == 9.0) and np.all(np.isfinite(o))
+    for sl in (1, 2):
+        np.testing.assert_array_equal(host(state)[sl], st0[sl])
+        np.testing.assert_array_equal(host(conv)[sl], cs0[sl])
+
+
+@pytest.mark.slow
+def test_block_prefill_4_sequences_512_tokens(lib):
+    """Full-width heads (Hk=16, H=32, S=128), 4 sequences x 512 tokens; one sampled
+    sequence checked against the oracle."""
+    cfg = I.get_config(2)
+    T = 512
+    steps = [I.block_step(cfg, t) for t in range(T)]
+    st0, cs0 = I.state_pool(cfg), I.conv_state_pool(cfg)
+    state, conv = dev(st0), dev(cs0)
+    out, _ = run_prefill(lib, cfg, T, steps, state, conv)
+    got = host(out)
+    stat = I.block_static(cfg)
+    n = 2
+    ref_st, ref_cs = f64(st0[n:n + 1]), f64(cs0[n:n + 1])
+    ref = np.zeros((T,) + got.shape[2:])
+    for t in range(T):
+        a = steps[t]
+        r, _ = oracle.block_decode(a["qkv"][n:n + 1], stat["conv_w"], ref_cs, a["alpha"][n:n + 1],
+                                   a["b"][n:n + 1], stat["dt"], stat["a"], a["z"][n:n + 1],
+                                   stat["norm_w"], ref_st, cfg.n_k_heads, cfg.scale, cfg.eps,
+                                   cfg.eps)
+        ref[t] = r[0]
+    assert_step(got[n, 0], ref[0], "out token 0")
+    assert_rms(got[n], ref, "out")
+    assert_rms(host(state)[n], ref_st[0], "state")
