@@ -38,7 +38,7 @@ from gated_deltanet_linear_scan_gb300 import inputs as I  # noqa: E402
 
 METRIC = "GDN decode tokens/s and state HBM GB/s (fraction of GB300 peak), 1 GPU"
 WORKLOADS = {"batched_decode_64": 3, "single_seq_decode_1000": 1,
-             "serving_pool_256_of_512": 4, "prefill_scan_4x4096": 2}
+             "serving_pool_256_of_512": 4, "prefill_scan_4x4096": 2, "prefill_block_4x4096": 2}
 FLUSH_BYTES = 256 << 20
 L2_NOTE = "flushed before every timed step (256 MiB write, then 256 MiB read: cold, clean L2)"
 FALLBACK_HBM_GBS = 6800.0
@@ -285,6 +285,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         flush_w.fill_(1.0)
         flush_r.sum()
 
+    if args.workload == "prefill_block_4x4096":
+        return run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
     if cfg.cid == 2:
         return run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
 
@@ -471,6 +473,76 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         "e2e": None,
         "gpu_launches": args.steps,
         "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
+    """The whole block over 4 sequences x 4096 tokens (gdn_block_prefill)."""
+    import torch
+    import gated_deltanet_linear_scan_gb300 as gdn
+    stream = torch.cuda.current_stream()
+    N, T, H, Hk, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.n_k_heads, cfg.state_size
+    seqs = rank_work(cfg, rank)["seqs"]
+    per = [I.prefill_seq(cfg, n) for n in seqs]
+    d = {key: dev(np.stack([p_[key] for p_ in per])) for key in per[0]}
+    st = {k_: dev(v_) for k_, v_ in I.block_static(cfg).items()}
+    state0 = dev(I.state_pool(cfg, which=seqs))
+    conv0 = dev(I.conv_state_pool(cfg, which=seqs))
+    state, conv = state0.clone(), conv0.clone()
+    out = torch.empty(N, T, H, S, device="cuda")
+    ws = torch.empty(gdn.gdn_block_prefill_workspace_size(N, T, Hk, H, S) // 4 + 64, device="cuda")
+
+    def launch():
+        gdn.gdn_block_prefill(d["qkv"], st["conv_w"], conv, d["alpha"], d["b"], st["dt"], st["a"],
+                              d["z"], st["norm_w"], state, out, N, T, Hk, H, S, cfg.conv_kernel,
+                              cfg.scale, cfg.eps, cfg.eps, ws)
+
+    def reset():
+        state.copy_(state0)
+        conv.copy_(conv0)
+
+    for _ in range(args.warmup):
+        reset()
+        flush()
+        launch()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        for i in range(args.steps):
+            reset()
+            flush()
+            ev[i][0].record(stream)
+            launch()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    gdn.gdn_device_error()
+    total_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, dist, "cuda")
+    per_s = total_s / args.steps
+    flops = 7.0 * N * T * H * S * S
+    props = torch.cuda.get_device_properties(0)
+    clk = clocks.summary()
+    mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
+    fp32_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": world * N * T * args.steps / total_s, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_s,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded PCG64; N(0,1) qkv/z, g~U(-0.5,-0.001))",
+        "config": {"workload": args.workload, "n_seqs": N, "n_tokens": T, "n_k_heads": Hk,
+                   "n_v_heads": H, "state_size": S, "conv_kernel": cfg.conv_kernel,
+                   "kernel": "gdn_block_prefill (6 launches: conv scan, split norm, gate, beta, "
+                             "scan, gated norm)", "l2": L2_NOTE},
+        "roofline": {"bound": "alu", "achieved": flops / per_s / 1e12, "peak": fp32_peak,
+                     "unit": "TFLOP/s", "frac": flops / per_s / 1e12 / fp32_peak, "traffic": None,
+                     "peak_source": "FP32 FMA pipes (the recurrence scan dominates)"},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": 6 * args.steps, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
     return 0

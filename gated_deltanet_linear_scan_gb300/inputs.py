@@ -84,7 +84,8 @@ def get_config(which, **overrides):
 
 
 _TAGS = {"state": 1, "conv_state": 2, "conv_w": 3, "norm_w": 4, "gate_params": 5, "slots": 6,
-         "qkv": 11, "gate": 12, "b": 13, "z": 14, "q": 21, "k": 22, "v": 23, "g": 24, "beta": 25}
+         "qkv": 11, "gate": 12, "b": 13, "z": 14, "q": 21, "k": 22, "v": 23, "g": 24, "beta": 25,
+         "pqkv": 31, "pgate": 32, "pb": 33, "pz": 34}
 
 
 def _rng(cfg, tag, idx=0, step=0):
@@ -173,6 +174,20 @@ def block_step(cfg, step, seqs=None):
         z.append(_normal(_rng(cfg, "z", n, step), (H, S)))
     return {"qkv": np.stack(qkv), "alpha": np.stack(alpha), "b": np.stack(b),
             "z": np.stack(z)}
+
+
+def prefill_seq(cfg, n, n_tokens=None):
+    """Raw block inputs of sequence n over n_tokens positions, each array drawn from
+    its own stream (distributions as block_step): qkv [T][C], alpha, b [T][H],
+    z [T][H][S]."""
+    T = cfg.n_tokens if n_tokens is None else n_tokens
+    dt, a = gate_params(cfg)
+    H, S, C = cfg.n_v_heads, cfg.state_size, cfg.conv_dim
+    lo, hi = cfg.g_range
+    g = _uniform(_rng(cfg, "pgate", n), lo, hi, (T, H)).astype(np.float64)
+    alpha = (np.log(np.expm1(g / a.astype(np.float64))) - dt).astype(np.float32)
+    return {"qkv": _normal(_rng(cfg, "pqkv", n), (T, C)), "alpha": alpha,
+            "b": _normal(_rng(cfg, "pb", n), (T, H)), "z": _normal(_rng(cfg, "pz", n), (T, H, S))}
 
 
 def block_static(cfg):
