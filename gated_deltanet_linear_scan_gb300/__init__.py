@@ -21,6 +21,7 @@ __all__ = [
     "gdn_qkv_split_norm", "gdn_recurrence_decode", "gdn_recurrence_scan", "gdn_gated_norm",
     "gdn_block_decode", "gdn_recurrence_decode_2pass", "gdn_recurrence_scan_snapshots",
     "gdn_conv1d_silu_seq_snapshots", "gdn_block_prefill_workspace_size", "gdn_block_prefill",
+    "gdn_block_prefill_noalloc", "PREFILL_NOALLOC_SCRATCH_BYTES",
 ]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
@@ -57,7 +58,12 @@ _SIGS = {
     "gdn_block_prefill_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
     "gdn_block_prefill": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P, _P,
                                        ctypes.c_size_t, _P], _I),
+    "gdn_block_prefill_noalloc": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P,
+                                               _P], _I),
 }
+
+# Size of the fixed device scratch of gdn_block_prefill_noalloc (include/gdn.h).
+PREFILL_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def lib_path():
@@ -271,3 +277,18 @@ def gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state
         n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps, norm_eps, _slots(slots),
         pool, _errc(err_count), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def gdn_block_prefill_noalloc(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,
+                              n_seqs, n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel,
+                              scale, l2_eps, norm_eps, slots=None, pool=None, err_count=None,
+                              stream=None):
+    """gdn_block_prefill working in the library's fixed device scratch instead of a
+    caller workspace, for callers that cannot allocate device memory."""
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_block_prefill_noalloc", library().gdn_block_prefill_noalloc(
+        _ptr(qkv, "qkv"), _ptr(conv_w, "conv_w"), _ptr(conv_state, "conv_state"),
+        _ptr(alpha, "alpha"), _ptr(b, "b"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(z, "z"),
+        _ptr(norm_w, "norm_w"), _ptr(state, "state"), _ptr(out, "out"), n_seqs, n_tokens,
+        n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps, norm_eps, _slots(slots),
+        pool, _errc(err_count), _stream(stream)))

@@ -90,3 +90,62 @@ gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_
 }
 
 }  // extern "C"
+
+// ============================================================================ no allocation
+// An allocation-free form of gdn_block_prefill for callers that cannot allocate
+// device memory: a plugin that only ever receives the input and output buffers of
+// the engine hosting it, or a serving loop that must not allocate in the middle
+// of a step (a device allocation can synchronise the whole device). Its workspace
+// is a fixed array in device memory that every GPU loading this library holds
+// until the process exits.
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = GDN_PREFILL_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+// In host code this name is only a stand-in for the array, not its device address.
+static __device__ __align__(256) unsigned char g_prefill_scratch[kNoAllocScratchBytes];
+
+// Device address of g_prefill_scratch on the current device, looked up on the
+// first call per device (with that device current) and remembered.
+gdn_status scratch_on_current_device(void **out) {
+    static std::mutex lock;
+    static void *addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_LAUNCH;
+    std::lock_guard<std::mutex> guard(lock);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess || p == nullptr)
+            return GDN_ERR_LAUNCH;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" gdn_status gdn_block_prefill_noalloc(
+    const float *qkv, const float *conv_w, float *conv_state, const float *alpha, const float *b,
+    const float *dt, const float *a, const float *z, const float *norm_w, float *state, float *out,
+    int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int state_size, int conv_kernel,
+    float scale, float l2_eps, float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
+    gdn_stream_t stream) {
+    if (n_seqs < 0 || n_tokens < 0 || n_k_heads < 1 || n_v_heads < 1 || state_size < 1)
+        return GDN_ERR_SHAPE;
+    const size_t need =
+        PrefillLayout(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size).total_floats *
+        sizeof(float);
+    if (need > kNoAllocScratchBytes) return GDN_ERR_UNSUPPORTED;  // beyond the fixed scratch
+    void *scratch = nullptr;
+    GDN_TRY(scratch_on_current_device(&scratch));
+    // Nothing needs clearing: every scratch value that can reach an output is written
+    // earlier in the same call (rows of a skipped sequence are read but never used).
+    return gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,
+                             n_seqs, n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel,
+                             scale, l2_eps, norm_eps, slots, pool, err_count, scratch,
+                             kNoAllocScratchBytes, stream);
+}

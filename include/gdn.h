@@ -225,6 +225,32 @@ gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_
                              float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
                              void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/* Bytes of the fixed device scratch gdn_block_prefill_noalloc works in. */
+#define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* gdn_block_prefill without a caller workspace, for callers that cannot allocate
+ * device memory: e.g. a plugin that only receives an engine's input and output
+ * buffers, or a serving loop that must not allocate mid-step (an allocation can
+ * synchronise the whole device). The pages have no counterpart; this is a
+ * library convenience.
+ * The workspace is a fixed GDN_PREFILL_NOALLOC_SCRATCH_BYTES array in device
+ * memory that every GPU loading this library holds until the process exits.
+ * Sizes whose gdn_block_prefill_workspace_size() exceeds it return
+ * GDN_ERR_UNSUPPORTED before anything is enqueued. The first call on a device
+ * looks up the array's device address on the current device (the stream must
+ * belong to it); make that first call before any stream capture. All calls share
+ * the array, which keeps the last call's contents (nothing in it needs to start
+ * at zero): calls that overlap on the GPU, on any stream, race. Allocates
+ * nothing. Arguments and results otherwise as gdn_block_prefill. */
+gdn_status gdn_block_prefill_noalloc(const float *qkv, const float *conv_w, float *conv_state,
+                                     const float *alpha, const float *b, const float *dt,
+                                     const float *a, const float *z, const float *norm_w,
+                                     float *state, float *out, int n_seqs, int n_tokens,
+                                     int n_k_heads, int n_v_heads, int state_size,
+                                     int conv_kernel, float scale, float l2_eps, float norm_eps,
+                                     const int32_t *slots, int pool, int32_t *err_count,
+                                     gdn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
