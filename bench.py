@@ -2,7 +2,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload batched_decode_64|single_seq_decode_1000|
-                                serving_pool_256_of_512|prefill_scan_4x4096]
+                                serving_pool_256_of_512|prefill_scan_4x4096|
+                                prefill_block_4x4096]
 
 Default workload: batched decode, 64 independent sequences, one token each per
 step (Hk=16, H=32, S=128, conv 4), through the fused gdn_block_decode kernel.
@@ -224,7 +225,7 @@ def cpu_sample_scan(cfg, tokens, budget_s):
 def run_reference(args, cfg, rank, world):
     if rank != 0:
         return 0
-    if cfg.cid == 2:
+    if args.workload == "prefill_scan_4x4096":
         tokens = 256
         vals = []
         t_all = time.perf_counter()
@@ -244,7 +245,7 @@ def run_reference(args, cfg, rank, world):
         t0 = time.perf_counter()
         value, done, dt = cpu_sample_block(cfg, seqs, args.steps, 1e9)
         sample = (f"{len(seqs)} of {cfg.n_seqs} sequences per step, {done} chained steps of the "
-                  "fused block")
+                  "fused block" + (" (one token of each sequence per step)" if cfg.cid == 2 else ""))
         ms = 1e3 * dt / done
         unit = "tokens/s"
     line = {
@@ -443,6 +444,26 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     total_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, dist, "cuda")
     per = total_s / args.steps
     tokens = world * N * T * args.steps
+
+    # ---- end to end: q, k, v, g, beta from pinned host memory, the call, y back.
+    keys = ["q", "k", "v", "g", "beta"]
+    h_in = {key: torch.from_numpy(np.ascontiguousarray(x[key])).pin_memory() for key in keys}
+    h_y = torch.empty(N, T, H, S).pin_memory()
+    h2d = sum(h_in[key].numel() for key in keys) * 4
+    d2h = h_y.numel() * 4
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        state.copy_(state0)
+        flush()
+        e2e_ev[i][0].record(stream)
+        for key in keys:
+            d[key].copy_(h_in[key], non_blocking=True)
+        launch()
+        h_y.copy_(y, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
     flops = 7.0 * N * T * H * S * S
     props = torch.cuda.get_device_properties(0)
     clk = clocks.summary()
@@ -470,7 +491,8 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                      "traffic": ncu_traffic("recurrence_scan_kernel", args.workload),
                      "peak_source": "FP32 FMA pipes: SMs x 128 lanes x 2 flop x median SM clock"},
         "cpu_baseline": cpu,
-        "e2e": None,
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
         "clocks": clk,
     }
@@ -523,6 +545,55 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     gdn.gdn_device_error()
     total_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, dist, "cuda")
     per_s = total_s / args.steps
+    tokens = world * N * T * args.steps
+
+    # ---- the dominant kernel alone: the recurrence scan over the same intermediates
+    # (made once by the stand-alone step entry points), timed on the same stream.
+    C = (2 * Hk + H) * S
+    conv_out = torch.empty(N, T, C, device="cuda")
+    q = torch.empty(N, T, Hk, S, device="cuda")
+    k = torch.empty_like(q)
+    v = torch.empty(N, T, H, S, device="cuda")
+    g = torch.empty(N, T, H, device="cuda")
+    beta = torch.empty_like(g)
+    y = torch.empty_like(out)
+    reset()
+    gdn.gdn_conv1d_silu_seq(d["qkv"], st["conv_w"], conv, conv_out, N, T, C, cfg.conv_kernel)
+    gdn.gdn_qkv_split_norm(conv_out, q, k, v, N * T, Hk, H, S, cfg.eps)
+    gdn.gdn_decay_gate(d["alpha"], st["dt"], st["a"], g, H, N * T)
+    gdn.gdn_beta_sigmoid(d["b"], beta, N * T * H)
+    scan_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    for i in range(args.steps):
+        state.copy_(state0)
+        flush()
+        scan_ev[i][0].record(stream)
+        gdn.gdn_recurrence_scan(state, q, k, v, g, beta, y, N, T, Hk, H, S, cfg.scale)
+        scan_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    scan_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in scan_ev) / 1e3, dist,
+                        "cuda") / args.steps
+
+    # ---- end to end: qkv, alpha, b, z from pinned host memory, the call, out back.
+    keys = ["qkv", "alpha", "b", "z"]
+    h_in = {key: d[key].cpu().pin_memory() for key in keys}
+    h_out = torch.empty(N, T, H, S).pin_memory()
+    h2d = sum(h_in[key].numel() for key in keys) * 4
+    d2h = h_out.numel() * 4
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        reset()
+        flush()
+        e2e_ev[i][0].record(stream)
+        for key in keys:
+            d[key].copy_(h_in[key], non_blocking=True)
+        launch()
+        h_out.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
+
     flops = 7.0 * N * T * H * S * S
     props = torch.cuda.get_device_properties(0)
     clk = clocks.summary()
@@ -530,19 +601,32 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     fp32_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
     if rank != 0:
         return 0
+    cpu = None
+    if world == 1:
+        v_cpu, done, dt = cpu_sample_block(cfg, [int(seqs[0])], 10 ** 6, args.cpu_budget)
+        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"1 of {N} sequences, {done} consecutive tokens through the block "
+                         f"({dt:.1f} s; per-token work is the same in every sequence), plain C "
+                         "float build, 1 thread"}
     line = {
-        "metric": METRIC, "value": world * N * T * args.steps / total_s, "unit": "tokens/s",
+        "metric": METRIC, "value": tokens / total_s, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded PCG64; N(0,1) qkv/z, g~U(-0.5,-0.001))",
         "config": {"workload": args.workload, "n_seqs": N, "n_tokens": T, "n_k_heads": Hk,
                    "n_v_heads": H, "state_size": S, "conv_kernel": cfg.conv_kernel,
                    "kernel": "gdn_block_prefill (6 launches: conv scan, split norm, gate, beta, "
-                             "scan, gated norm)", "l2": L2_NOTE},
-        "roofline": {"bound": "alu", "achieved": flops / per_s / 1e12, "peak": fp32_peak,
-                     "unit": "TFLOP/s", "frac": flops / per_s / 1e12 / fp32_peak, "traffic": None,
-                     "peak_source": "FP32 FMA pipes (the recurrence scan dominates)"},
-        "cpu_baseline": None, "e2e": None, "gpu_launches": 6 * args.steps, "clocks": clk,
+                             "scan, gated norm)", "l2": L2_NOTE,
+                   "scan_ms": 1e3 * scan_s},
+        "roofline": {"bound": "alu", "kernel": "recurrence_scan_kernel",
+                     "achieved": flops / scan_s / 1e12, "peak": fp32_peak, "unit": "TFLOP/s",
+                     "frac": flops / scan_s / 1e12 / fp32_peak,
+                     "traffic": ncu_traffic("recurrence_scan_kernel", "prefill_scan_4x4096"),
+                     "peak_source": "FP32 FMA pipes: SMs x 128 lanes x 2 flop x median SM clock"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 6 * args.steps, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
     return 0

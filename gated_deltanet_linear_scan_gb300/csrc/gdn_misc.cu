@@ -36,11 +36,18 @@ __global__ void __launch_bounds__(kThreads) sigmoid_kernel(const float *__restri
 }
 
 // Causal depthwise conv1d + SiLU over n_tokens positions, fm_kernel_ssm.m "Causal
-// depthwise conv1d + SiLU" and its scan form. One thread per (sequence, channel);
-// the K-1 taps of history live in registers for the whole scan and are written
-// back once. The accumulation is the current tap first, then the history
-// oldest-first; a single-token call is the n_tokens == 1 case of the same code, so
-// a scan and n single-token calls agree bit for bit.
+// depthwise conv1d + SiLU" and its scan form. The history holds RAW inputs, so the
+// window of position p is just inputs p-K+1 .. p (the old conv_state standing in
+// for p < 0): positions are independent, and the scan runs in blocks of
+// kConvTokens positions, one thread per (sequence, channel, block), each carrying
+// its K-1 taps in registers across its block. The block of position 0 alone reads
+// the old conv_state and writes the new one (the last K-1 raw inputs), so the
+// in-place update cannot race. The accumulation is the current tap first, then the
+// history oldest-first; every position is computed with the same operations as a
+// single-token call, so a scan and n single-token calls agree bit for bit.
+constexpr int kConvTokens = 64;
+static_assert(kConvTokens >= 8, "a block's history must reach back no further than position 0");
+
 template <int K, bool SNAP>
 __global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
     const float *__restrict__ qkv, const float *__restrict__ w, float *conv_state,
@@ -49,9 +56,12 @@ __global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
     constexpr int TAPS = K - 1;
     const int n = blockIdx.y;
     const int c = blockIdx.x * kThreads + threadIdx.x;
+    const int t0 = blockIdx.z * kConvTokens;
+    const int t1 = min(n_tokens, t0 + kConvTokens);
     const int slot = slots ? slots[n] : n;
     if (slot < 0 || slot >= pool) {
-        if (err_count && blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(err_count, 1);
+        if (err_count && blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+            atomicAdd(err_count, 1);
         return;
     }
     if (c >= conv_dim) return;
@@ -59,12 +69,20 @@ __global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
 #pragma unroll
     for (int t = 0; t < K; ++t) wc[t] = w[static_cast<size_t>(c) * K + t];
     float *hs = conv_state + (static_cast<size_t>(slot) * conv_dim + c) * TAPS;
-    float hist[TAPS];
-#pragma unroll
-    for (int t = 0; t < TAPS; ++t) hist[t] = hs[t];
     const float *x_ptr = qkv + static_cast<size_t>(n) * n_tokens * conv_dim + c;
     float *o_ptr = out + static_cast<size_t>(n) * n_tokens * conv_dim + c;
-    for (int p = 0; p < n_tokens; ++p) {
+    // inputs at positions t0-K+1 .. t0-1 (the old state for negative positions)
+    float old[TAPS], hist[TAPS];
+    if (t0 == 0) {
+#pragma unroll
+        for (int t = 0; t < TAPS; ++t) old[t] = hs[t];
+    }
+#pragma unroll
+    for (int t = 0; t < TAPS; ++t) {
+        const int pos = t0 - TAPS + t;
+        hist[t] = pos >= 0 ? x_ptr[static_cast<size_t>(pos) * conv_dim] : old[t];  // t0 == 0
+    }
+    for (int p = t0; p < t1; ++p) {
         const float x = x_ptr[static_cast<size_t>(p) * conv_dim];
         float pre = __fmul_rn(x, wc[K - 1]);
 #pragma unroll
@@ -79,8 +97,15 @@ __global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
             for (int t = 0; t < TAPS; ++t) sn[t] = hist[t];
         }
     }
+    if (t0 == 0) {  // the new state: the last K-1 inputs of (old state, this call's inputs)
+        for (int p = max(0, n_tokens - TAPS); p < n_tokens; ++p) {
 #pragma unroll
-    for (int t = 0; t < TAPS; ++t) hs[t] = hist[t];
+            for (int t = 0; t + 1 < TAPS; ++t) old[t] = old[t + 1];
+            old[TAPS - 1] = x_ptr[static_cast<size_t>(p) * conv_dim];
+        }
+#pragma unroll
+        for (int t = 0; t < TAPS; ++t) hs[t] = old[t];
+    }
 }
 
 // q/k split + L2-norm (ssm_gated_delta.cu, fc_ssm_qknorm_gqa_nx, without the GQA
@@ -154,7 +179,8 @@ template <int K>
 gdn_status launch_conv(const float *qkv, const float *w, float *conv_state, float *out,
                        int n_seqs, int n_tokens, int conv_dim, const int32_t *slots, int pool,
                        int32_t *err_count, float *snaps, cudaStream_t s) {
-    const dim3 grid((conv_dim + kThreads - 1) / kThreads, n_seqs);
+    const dim3 grid((conv_dim + kThreads - 1) / kThreads, n_seqs,
+                    (n_tokens + kConvTokens - 1) / kConvTokens);
     if (snaps)
         conv1d_silu_kernel<K, true><<<grid, kThreads, 0, s>>>(qkv, w, conv_state, out, n_tokens,
                                                               conv_dim, slots, pool, err_count, snaps);
@@ -173,7 +199,8 @@ gdn_status conv_common(const float *qkv, const float *w, float *conv_state, floa
     if (conv_kernel < 2 || conv_kernel > 8) return GDN_ERR_SHAPE;
     GDN_TRY(check_pool(n_seqs, slots, pool));
     if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
-    if (n_seqs > 65535) return GDN_ERR_UNSUPPORTED;
+    if (n_seqs > 65535 || (n_tokens + kConvTokens - 1) / kConvTokens > 65535)
+        return GDN_ERR_UNSUPPORTED;
     const cudaStream_t s = as_cuda(stream);
     switch (conv_kernel) {
         case 2: return launch_conv<2>(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, slots, pool, err_count, snaps, s);

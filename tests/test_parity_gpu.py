@@ -80,7 +80,8 @@ def test_decay_gate_and_beta(lib):
 
 
 @pytest.mark.parametrize("K", [2, 3, 4, 5, 8])
-@pytest.mark.parametrize("C,T", [(256, 1), (256, 21), (8192, 3)])
+# T = 65 and 150 cross the scan's 64-position blocks, with a ragged last block
+@pytest.mark.parametrize("C,T", [(256, 1), (256, 21), (8192, 3), (256, 65), (512, 150)])
 def test_conv1d_silu(lib, K, C, T):
     r = np.random.default_rng(101 + K)
     N, P = 3, 5
@@ -341,9 +342,10 @@ def test_recurrence_scan_snapshots(lib, S, T):
     assert torch.equal(y_r, y_full[:, M:]) and torch.equal(st_r, st_full)
 
 
-def test_conv1d_silu_seq_snapshots(lib):
+@pytest.mark.parametrize("T", [9, 130])
+def test_conv1d_silu_seq_snapshots(lib, T):
     r = np.random.default_rng(105)
-    N, T, C, K = 2, 9, 256, 4
+    N, C, K = 2, 256, 4
     qkv = r.normal(0, 1, (N, T, C)).astype(np.float32)
     w = r.normal(0, 0.5, (C, K)).astype(np.float32)
     cs0 = r.normal(0, 1, (N, C, K - 1)).astype(np.float32)
