@@ -42,6 +42,7 @@ gdn_status launch_gated_norm(const float *y, const float *w, const float *z, flo
 // Per-translation-unit watchdog flags (a bounded wait that gave up sets a bit).
 unsigned read_and_clear_watchdog_recurrence(cudaStream_t s);
 unsigned read_and_clear_watchdog_block(cudaStream_t s);
+unsigned read_and_clear_watchdog_chunked(cudaStream_t s);
 
 }  // namespace gdn
 

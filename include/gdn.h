@@ -168,6 +168,34 @@ gdn_status gdn_recurrence_scan_snapshots(float *state, const float *q, const flo
                                          float scale, const int32_t *slots, int pool,
                                          int32_t *err_count, gdn_stream_t stream);
 
+/* The multi-token scan in chunks of 32 positions with the state-dependent
+ * contractions on the tensor cores (tcgen05, TF32 operands split hi + lo so that
+ * products keep fp32 accuracy, fp32 accumulation), for long prefill.
+ * fm_kernel_ssm.m (the softplus note and the sequential-scan section) refers to
+ * a chunked prefill path built on cumulative sums of g within each chunk and
+ * keeps the sequential scan as its permanent reference; the chunked algebra
+ * itself (an exact regrouping of the recurrence, the WY/UT form) is not given on
+ * the pages.
+ * Arguments, layouts and slot semantics as gdn_recurrence_scan, plus
+ * workspace: device memory of at least
+ *   gdn_recurrence_scan_chunked_workspace_size(n_seqs, n_tokens, H, S)
+ * bytes (per sequence, v-head and chunk of 32 positions: 106,624 bytes of
+ * tensor-core operands), 16-byte aligned, owned by the caller; its contents are
+ * ignored on entry and meaningless on return. NULL is GDN_ERR_NULL, too small is
+ * GDN_ERR_SHAPE.
+ * Only state_size 128 has this form (else GDN_ERR_UNSUPPORTED). Results agree
+ * with the sequential scan to within rounding (the same 2e-3-of-RMS bound after
+ * 4096 positions), not bit for bit. */
+size_t gdn_recurrence_scan_chunked_workspace_size(int n_seqs, int n_tokens, int n_v_heads,
+                                                  int state_size);
+gdn_status gdn_recurrence_scan_chunked(float *state, const float *q, const float *k,
+                                       const float *v, const float *g, const float *beta,
+                                       float *y, int n_seqs, int n_tokens, int n_k_heads,
+                                       int n_v_heads, int state_size, float scale,
+                                       const int32_t *slots, int pool, int32_t *err_count,
+                                       void *workspace, size_t workspace_bytes,
+                                       gdn_stream_t stream);
+
 /* The conv scan, also writing the conv history after every position (ssm_gated_delta.cu,
  * fc_ssm_conv1d_silu_seq's `snaps`): snaps [n_seqs][n_tokens][conv_dim][K-1], the
  * conv_state layout of one slot per position. NULL is an error. Otherwise as

@@ -1,6 +1,7 @@
 // Unit test of the tcgen05 building blocks in gdn_tc.cuh: one CTA computes
-// D[128 x 64] = A[128 x 32] * B[64 x 32]^T on the tensor cores with tf32 inputs
-// (one pass) or the hi/lo split (three passes), accumulator in tensor memory.
+// D[128 x N] = A[128 x 32] * B[N x 32]^T on the tensor cores with tf32 inputs
+// (one pass) or the hi/lo split (three passes), accumulator in tensor memory,
+// with A in shared memory (N = 64) or in tensor memory (N = 32 or 128).
 // Built by tests/test_tc_primitives.py into its own shared library.
 #include <cstdint>
 
@@ -82,6 +83,88 @@ __global__ void __launch_bounds__(128) tc_gemm_kernel(const float *__restrict__ 
     if (warp == 0) gdn::tc::tmem_dealloc(taddr, 64);
 }
 
+// A in tensor memory: thread t (lanes of warp t/32) writes row t of A, hi part to
+// columns [0, 32), lo part to [32, 64); D occupies columns [64, 64 + NN).
+template <int NN>
+__global__ void __launch_bounds__(128) tc_gemm_ts_kernel(const float *__restrict__ A,
+                                                         const float *__restrict__ B,
+                                                         float *__restrict__ D, int split,
+                                                         int *status) {
+    constexpr uint32_t kCols = NN + 64 <= 128 ? 128 : 256;
+    constexpr uint32_t kSbo = (K / 4) * 128;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char *b_hi = smem, *b_lo = smem + NN * K * 4;
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t s_taddr;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    for (int i = tid; i < NN * K; i += 128) {
+        const int r = i / K, k = i % K;
+        float hi, lo;
+        gdn::tc::split_tf32(B[i], hi, lo);
+        const uint32_t off = gdn::tc::kmajor_offset(r, k, LBO, kSbo);
+        *reinterpret_cast<float *>(b_hi + off) = hi;
+        *reinterpret_cast<float *>(b_lo + off) = lo;
+    }
+    gdn::fence_proxy_async_smem();
+    if (tid == 0) {
+        gdn::mbar_init(&bar, 1);
+        gdn::fence_mbar_init();
+    }
+    if (warp == 0) {
+        gdn::tc::tmem_alloc(&s_taddr, kCols);
+        gdn::tc::tmem_relinquish();
+    }
+    gdn::tc::fence_before_sync();
+    __syncthreads();
+    gdn::tc::fence_after_sync();
+    const uint32_t taddr = s_taddr;
+    const uint32_t tw = taddr + (static_cast<uint32_t>(32 * warp) << 16);
+    {
+        uint32_t hi[32], lo[32];
+        for (int k = 0; k < K; ++k) {
+            float h, l;
+            gdn::tc::split_tf32(A[tid * K + k], h, l);
+            hi[k] = __float_as_uint(h);
+            lo[k] = __float_as_uint(l);
+        }
+        gdn::tc::tmem_st32(tw, hi);
+        gdn::tc::tmem_st32(tw + 32, lo);
+        gdn::tc::tmem_st_wait();
+    }
+    gdn::tc::fence_before_sync();
+    __syncthreads();
+    gdn::tc::fence_after_sync();
+
+    if (tid == 0) {
+        const uint32_t idesc = gdn::tc::idesc_tf32(M, NN);
+        const uint32_t acol[3] = {0, 0, 32};
+        const unsigned char *bs[3] = {b_hi, b_lo, b_hi};
+        const int passes = split ? 3 : 1;
+        for (int p = 0; p < passes; ++p)
+            for (int ks = 0; ks < K / 8; ++ks) {
+                const uint64_t bd = gdn::tc::smem_desc(bs[p] + ks * 2 * LBO, LBO, kSbo);
+                gdn::tc::mma_tf32_ts(taddr + 64, taddr + acol[p] + ks * 8, bd, idesc,
+                                     p > 0 || ks > 0);
+            }
+        gdn::tc::mma_commit(&bar);
+    }
+    const bool done = gdn::mbar_wait(&bar, 0);
+    if (!done && lane == 0) atomicOr(status, 1);
+    gdn::tc::fence_after_sync();
+    if (done) {
+        for (int cb = 0; cb < NN / 32; ++cb) {
+            uint32_t v[32];
+            gdn::tc::tmem_ld32_nowait(tw + 64 + cb * 32, v);
+            gdn::tc::tmem_ld_wait();
+            for (int i = 0; i < 32; ++i) D[(32 * warp + lane) * NN + cb * 32 + i] = __uint_as_float(v[i]);
+        }
+    }
+    gdn::tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) gdn::tc::tmem_dealloc(taddr, kCols);
+}
+
 }  // namespace
 
 extern "C" int tc_gemm_test(const float *A, const float *B, float *D, int split, int *status,
@@ -89,5 +172,21 @@ extern "C" int tc_gemm_test(const float *A, const float *B, float *D, int split,
     const int smem = (M + N) * K * 4 * 2;
     cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     tc_gemm_kernel<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(A, B, D, split, status);
+    return static_cast<int>(cudaGetLastError());
+}
+
+extern "C" int tc_gemm_ts_test(const float *A, const float *B, float *D, int n, int split,
+                               int *status, void *stream) {
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int smem = n * K * 4 * 2;
+    if (n == 32) {
+        cudaFuncSetAttribute(tc_gemm_ts_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        tc_gemm_ts_kernel<32><<<1, 128, smem, st>>>(A, B, D, split, status);
+    } else if (n == 128) {
+        cudaFuncSetAttribute(tc_gemm_ts_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        tc_gemm_ts_kernel<128><<<1, 128, smem, st>>>(A, B, D, split, status);
+    } else {
+        return -1;
+    }
     return static_cast<int>(cudaGetLastError());
 }

@@ -1,0 +1,146 @@
+"""GPU parity of the chunked tensor-core scan (gdn_recurrence_scan_chunked).
+
+The chunked form regroups the recurrence exactly, so it is held to the oracle's
+long-scan bound: max |gpu - ref| <= 2e-3 * RMS(ref) for y and for the final
+state, per tensor (ref = the fp64 oracle). Cases cover one position, a chunk
+minus one, exactly one chunk, one more, several chunks with a ragged tail, GQA
+ratios 1, 2 and 4, slot routing with a skipped sequence, and the 4 x 4096 prefill
+workload at full size.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from gated_deltanet_linear_scan_gb300 import inputs as I  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.detach().cpu().numpy()
+
+
+def f64(x):
+    return np.array(x, dtype=np.float64)
+
+
+def assert_rms(gpu, ref, name, rel=2e-3):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(gpu)), f"{name}: non-finite values"
+    rms = np.sqrt(np.mean(ref * ref))
+    err = np.max(np.abs(gpu - ref))
+    assert err <= rel * rms, f"{name}: max err {err:.3e} > {rel} * RMS {rms:.3e}"
+    return err / rms
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib(cuda_lib):
+    yield cuda_lib
+    cuda_lib.gdn_device_error()  # raises if a bounded wait gave up during the module
+
+
+def case(Hk, H, N, T, seed, pool=None):
+    cfg = I.get_config(0, n_k_heads=Hk, n_v_heads=H, state_size=128, n_seqs=N, n_tokens=T,
+                       pool=pool, cid=300 + seed)
+    return cfg, I.recurrence_batch(cfg), I.state_pool(cfg)
+
+
+def run_chunked(lib, cfg, x, st, slots=None, pool=None, err=None):
+    N, T, H, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.state_size
+    y = torch.zeros(N, T, H, S, device="cuda")
+    nbytes = lib.gdn_recurrence_scan_chunked_workspace_size(N, T, H, S)
+    ws = torch.empty(max(nbytes, 16) // 4, device="cuda")
+    lib.gdn_recurrence_scan_chunked(st, dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["g"]),
+                                    dev(x["beta"]), y, N, T, cfg.n_k_heads, H, S, cfg.scale, ws,
+                                    slots=slots, pool=pool, err_count=err)
+    return y
+
+
+@pytest.mark.parametrize("Hk,H,N,T", [(2, 4, 2, 1), (2, 4, 2, 31), (1, 2, 1, 32), (2, 4, 1, 33),
+                                      (2, 4, 2, 100), (4, 4, 1, 64), (2, 8, 2, 200)])
+def test_chunked_scan_vs_oracle(lib, Hk, H, N, T):
+    cfg, x, st0 = case(Hk, H, N, T, seed=T + H)
+    st = dev(st0)
+    y = run_chunked(lib, cfg, x, st)
+    st_ref = f64(st0)
+    y_ref, _ = oracle.recurrence(st_ref, x["q"], x["k"], x["v"], x["g"], x["beta"], cfg.scale)
+    assert_rms(host(y), y_ref, "y")
+    assert_rms(host(st), st_ref, "final state")
+    # each (sequence, v-head) unit on its own scale, too
+    yh = host(y)
+    for n in range(N):
+        for vh in range(H):
+            assert_rms(yh[n, :, vh], y_ref[n, :, vh], f"y ({n},{vh})")
+
+
+def test_chunked_scan_matches_sequential_scan(lib):
+    """Against the library's sequential scan (itself bit-identical to decode steps)."""
+    cfg, x, st0 = case(2, 4, 2, 160, seed=5)
+    N, T, H, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.state_size
+    st_c, st_s = dev(st0), dev(st0)
+    y_c = run_chunked(lib, cfg, x, st_c)
+    y_s = torch.zeros(N, T, H, S, device="cuda")
+    lib.gdn_recurrence_scan(st_s, dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["g"]),
+                            dev(x["beta"]), y_s, N, T, cfg.n_k_heads, H, S, cfg.scale)
+    assert_rms(host(y_c), host(y_s), "y vs sequential")
+    assert_rms(host(st_c), host(st_s), "state vs sequential")
+
+
+def test_chunked_scan_slots(lib):
+    cfg, x, _ = case(2, 4, 3, 70, seed=9, pool=5)
+    pool0 = I.state_pool(cfg)
+    slots = np.array([4, -1, 1], dtype=np.int32)
+    st = dev(pool0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = run_chunked(lib, cfg, x, st, slots=dev(slots), pool=5, err=err)
+    assert host(err)[0] == 1
+    st_ref = f64(pool0)
+    y_ref, skipped = oracle.recurrence(st_ref, x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                       cfg.scale, slots=slots, pool=5)
+    assert skipped == 1
+    got = host(st)
+    for s in (0, 2, 3):
+        np.testing.assert_array_equal(got[s], pool0[s])  # untouched slots keep their bits
+    for s in (1, 4):
+        assert_rms(got[s], st_ref[s], f"state slot {s}")
+    yh = host(y)
+    assert np.all(yh[1] == 0.0)  # nothing written for the skipped sequence
+    assert_rms(yh[[0, 2]], y_ref[[0, 2]], "y")
+
+
+@pytest.mark.slow
+def test_chunked_scan_prefill_4x4096(lib):
+    """The prefill workload at full size (N=4, T=4096, Hk=16, H=32, S=128): every
+    output against the sequential GPU scan, sampled units against the oracle."""
+    cfg = I.get_config(2)
+    N, T, H, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.state_size
+    x = I.recurrence_batch(cfg)
+    st0 = I.state_pool(cfg)
+    st_c, st_s = dev(st0), dev(st0)
+    y_c = run_chunked(lib, cfg, x, st_c)
+    y_s = torch.zeros(N, T, H, S, device="cuda")
+    lib.gdn_recurrence_scan(st_s, dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["g"]),
+                            dev(x["beta"]), y_s, N, T, cfg.n_k_heads, H, S, cfg.scale)
+    yh, sth = host(y_c), host(st_c)
+    assert_rms(yh, host(y_s), "y vs sequential")
+    assert_rms(sth, host(st_s), "state vs sequential")
+    for n, vh in ((0, 0), (1, 17), (3, 31), (2, 8)):
+        kh = vh % cfg.n_k_heads
+        unit = {key: x[key][n:n + 1] for key in x}
+        unit["q"] = unit["q"][:, :, kh:kh + 1]
+        unit["k"] = unit["k"][:, :, kh:kh + 1]
+        unit["v"] = unit["v"][:, :, vh:vh + 1]
+        unit["g"] = unit["g"][:, :, vh:vh + 1]
+        unit["beta"] = unit["beta"][:, :, vh:vh + 1]
+        s_ref = f64(st0[n:n + 1, vh:vh + 1])
+        y_ref, _ = oracle.recurrence(s_ref, scale=cfg.scale, **unit)
+        assert_rms(yh[n, :, vh], y_ref[0, :, 0], f"y ({n},{vh})")
+        assert_rms(sth[n, vh], s_ref[0, 0], f"final state ({n},{vh})")

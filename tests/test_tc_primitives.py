@@ -1,8 +1,9 @@
 """GPU unit test of the tcgen05 building blocks (gdn_tc.cuh) on a single tile.
 
-D[128 x 64] = A[128 x 32] B[64 x 32]^T on the tensor cores: one tf32 pass must
+D[128 x N] = A[128 x 32] B[N x 32]^T on the tensor cores: one tf32 pass must
 equal the product of tf32-rounded inputs (up to accumulation order), and the
-three-pass hi/lo split must match the fp64 product to fp32 accuracy.
+three-pass hi/lo split must match the fp64 product to fp32 accuracy; A comes
+from shared memory (N = 64) or from tensor memory (N = 32, 128).
 """
 import ctypes
 import os
@@ -28,6 +29,8 @@ def tclib(tmp_path_factory):
     lib = ctypes.CDLL(out)
     lib.tc_gemm_test.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_void_p]
     lib.tc_gemm_test.restype = ctypes.c_int
+    lib.tc_gemm_ts_test.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p] * 2
+    lib.tc_gemm_ts_test.restype = ctypes.c_int
     return lib
 
 
@@ -68,3 +71,30 @@ def test_three_pass_split_tf32(tclib):
     np.testing.assert_allclose(D, want, rtol=0, atol=2e-5)
     single = run(tclib, A, B, 0)
     assert np.abs(single - want).max() > 10 * np.abs(D - want).max()
+
+
+def run_ts(tclib, A, B, split):
+    n = B.shape[0]
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dD = torch.full((128, n), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = tclib.tc_gemm_ts_test(dA.data_ptr(), dB.data_ptr(), dD.data_ptr(), n, split,
+                               st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0, "the MMA completion wait gave up"
+    return dD.cpu().numpy()
+
+
+@pytest.mark.parametrize("n", [32, 128])
+def test_a_from_tensor_memory(tclib, n):
+    r = np.random.default_rng(3 + n)
+    A = r.normal(0, 1, (128, 32)).astype(np.float32)
+    B = r.normal(0, 1, (n, 32)).astype(np.float32)
+    want = A.astype(np.float64) @ B.astype(np.float64).T
+    D1 = run_ts(tclib, A, B, 0)
+    np.testing.assert_allclose(D1, tf32_round(A).astype(np.float64)
+                               @ tf32_round(B).astype(np.float64).T, rtol=0, atol=1e-4)
+    D3 = run_ts(tclib, A, B, 1)
+    np.testing.assert_allclose(D3, want, rtol=0, atol=2e-5)
