@@ -22,7 +22,7 @@ __all__ = [
     "gdn_block_decode", "gdn_recurrence_decode_2pass", "gdn_recurrence_scan_snapshots",
     "gdn_conv1d_silu_seq_snapshots", "gdn_block_prefill_workspace_size", "gdn_block_prefill",
     "gdn_block_prefill_noalloc", "PREFILL_NOALLOC_SCRATCH_BYTES",
-    "gdn_recurrence_scan_chunked_workspace_size", "gdn_recurrence_scan_chunked",
+    "gdn_recurrence_scan_chunked",
 ]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
@@ -61,9 +61,7 @@ _SIGS = {
                                        ctypes.c_size_t, _P], _I),
     "gdn_block_prefill_noalloc": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P,
                                                _P], _I),
-    "gdn_recurrence_scan_chunked_workspace_size": ([_I, _I, _I, _I], ctypes.c_size_t),
-    "gdn_recurrence_scan_chunked": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P,
-                                                ctypes.c_size_t, _P], _I),
+    "gdn_recurrence_scan_chunked": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
 }
 
 # Size of the fixed device scratch of gdn_block_prefill_noalloc (include/gdn.h).
@@ -213,25 +211,14 @@ def gdn_recurrence_scan(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads,
         scale, _slots(slots), pool, _errc(err_count), _stream(stream)))
 
 
-def gdn_recurrence_scan_chunked_workspace_size(n_seqs, n_tokens, n_v_heads, state_size):
-    return library().gdn_recurrence_scan_chunked_workspace_size(n_seqs, n_tokens, n_v_heads,
-                                                               state_size)
-
-
 def gdn_recurrence_scan_chunked(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads,
-                                n_v_heads, state_size, scale, workspace, slots=None, pool=None,
+                                n_v_heads, state_size, scale, slots=None, pool=None,
                                 err_count=None, stream=None):
-    """`workspace`: a CUDA tensor of at least
-    gdn_recurrence_scan_chunked_workspace_size() bytes."""
     pool = _pool(pool, n_seqs, slots)
-    import torch
-    if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
-        raise ValueError("workspace must be a contiguous CUDA tensor")
     _check("gdn_recurrence_scan_chunked", library().gdn_recurrence_scan_chunked(
         _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
         _ptr(beta, "beta"), _ptr(y, "y"), n_seqs, n_tokens, n_k_heads, n_v_heads, state_size,
-        scale, _slots(slots), pool, _errc(err_count), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        scale, _slots(slots), pool, _errc(err_count), _stream(stream)))
 
 
 def gdn_gated_norm(y, w, z, out, rows, head_dim, eps, stream=None):

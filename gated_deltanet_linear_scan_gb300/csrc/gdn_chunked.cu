@@ -8,8 +8,8 @@
 // chunked algebra out. The form used here is derived from the recurrence itself
 // (the WY/UT representation of a product of generalised Householder steps). Per
 // (sequence, v-head) and chunk of positions t = 0..31 with log-decays g_t, write
-// gam_t = g_0 + .. + g_t,
-// Gam_t = exp(gam_t), S the state at the chunk start as a [dk][dv] matrix, and
+// gam_t = g_0 + .. + g_t, Gam_t = exp(gam_t), S the state at the chunk start as a
+// [dk][dv] matrix, and
 //   A[t][s] = beta_t exp(gam_t - gam_s) (k_t . k_s)        (s < t, else 0)
 //   (I + A) W  = diag(beta Gam) K,   (I + A) Ut = diag(beta) V   (forward substitution)
 //   U  = Ut - W S                                            (the per-position delta)
@@ -18,32 +18,25 @@
 // This is the recurrence of the sequential scan regrouped exactly (no truncation
 // or approximation); only the rounding differs.
 //
-// Two kernels:
-//  1. chunk_prep_kernel (one CTA per (sequence, v-head, chunk), all in parallel,
-//     fp32 on the CUDA cores): gam, the Gram products, the forward substitution,
-//     and a record holding the tensor-core operands of the chunk, laid out as the
-//     shared-memory image the second kernel copies in with one bulk copy:
-//        W          [32 c][128 dk]         single tf32 pass operand
-//        wK^T  hi/lo [128 dk][32 c]        exp(gam_31 - gam_c) k_c, split for 3 passes
-//        QM    hi/lo [32 t][128 + 32]      (Gam_t q_t | exp(gam_t - gam_s)(q_t . k_s), s<=t)
-//        Ut          [32 c][128 dv]        fp32, read by the CUDA cores
-//        Gam_31
-//  2. chunk_scan_kernel (one CTA per (sequence, v-head), sequential over chunks):
-//     the state lives in tensor memory as S^T (lane = dv, column = dk) for the
-//     whole scan; per chunk, four warps split it into tf32 hi/lo parts (also in
-//     tensor memory, the A operand of the MMAs), one thread issues
-//        D_u = S^T W^T                 (U^T = Ut^T - D_u, one tf32 pass)
-//        D_y = S^T (Gam Q)^T + U^T M^T (three passes)
-//        S^T <- Gam_31 S^T + U^T (wK)  (three passes, accumulated in place)
-//     and the four warps turn D_u into U and D_y into y.
+// One kernel, one CTA per (sequence, v-head), sequential over chunks, one CTA per
+// SM. The state lives in tensor memory as S^T (lane = dv, column = dk) for the
+// whole scan. Warp roles, linked only by mbarriers:
+//   producer (1 warp)  bulk-copies the k, q, v rows of each chunk into a 2-deep ring;
+//   state (8 warps)    split S into tf32 hi/lo parts in tensor memory (the A
+//                      operand), form U^T = Ut^T - D_u and its split, write y, and in
+//                      between, on the CUDA cores in fp32, the next chunk's Gram stage
+//                      (gam and the Gram products A and M);
+//   prep (8 warps)     per chunk, in fp32: the forward substitution and the
+//                      tensor-core operands in shared memory (each written as soon as
+//                      the previous chunk's MMAs have finished reading it);
+//   MMA (1 thread)     D_u|D_y = S^T [W | Gam Q]^T, D_y += the rest of the S part,
+//                      S^T = Gam_31 S^T + U^T (w K), D_y += U^T M^T.
 //
 // Precision: a single TF32 pass (10-bit mantissa) in any product that feeds the
 // state or y misses a 2e-3-of-RMS error bound after 4096 positions; the split
 // x = hi + lo with hi*hi + hi*lo + lo*hi ("3xTF32") restores fp32-level products.
 // Only W S tolerates one pass: its error enters U, which the delta rule corrects
 // at the next write.
-#include <mutex>
-
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 #include "gdn_tc.cuh"
@@ -51,253 +44,202 @@
 namespace gdn {
 namespace {
 
+__device__ unsigned g_watchdog_chunked;
+constexpr unsigned WD_MMA = 8u;  // a hand-off between the roles of the chunked scan
+
 constexpr int kC = 32;    // positions per chunk
 constexpr int kS = 128;   // state size (dk = dv) of the tensor-core form
-constexpr uint32_t kLbo = 128;  // K-major core matrices: next 4 elements of K
+constexpr uint32_t kLbo = 128;                 // K-major core matrices: next 4 elements of K
+constexpr uint32_t kSbo128 = (kS / 4) * 128;   // next 8 rows, K = 128 operands
+constexpr uint32_t kSbo32 = (kC / 4) * 128;    // next 8 rows, K = 32 operands
 
-// Record / shared-memory stage layout (bytes).
-constexpr uint32_t kSboW = (kS / 4) * 128;        // W: 32 rows x K = 128
-constexpr uint32_t kSboK = (kC / 4) * 128;        // wK^T: 128 rows x K = 32
-constexpr uint32_t kQmK = kS + kC;                // QM: K = 160
-constexpr uint32_t kSboQ = (kQmK / 4) * 128;      // QM: 32 rows x K = 160
-constexpr uint32_t kOffW = 0;
-constexpr uint32_t kOffKhi = kOffW + kC * kS * 4;
-constexpr uint32_t kOffKlo = kOffKhi + kS * kC * 4;
-constexpr uint32_t kOffQhi = kOffKlo + kS * kC * 4;
-constexpr uint32_t kOffQlo = kOffQhi + kC * kQmK * 4;
-constexpr uint32_t kOffUt = kOffQlo + kC * kQmK * 4;
-constexpr uint32_t kOffScal = kOffUt + kC * kS * 4;
-constexpr uint32_t kRecord = kOffScal + 128;       // 106,624 bytes, a multiple of 128
-static_assert(kRecord % 128 == 0, "records stay 128-byte aligned");
+// ---- shared memory (bytes)
+// tensor-core operands, K-major core-matrix images (see gdn_tc.cuh)
+constexpr uint32_t kOffWQ = 0;         // 64 rows x K=128: rows 0..31 W, rows 32..63 hi(Gam q)
+constexpr uint32_t kOffQlo = 32768;    // 32 rows x K=128: lo(Gam q)
+constexpr uint32_t kOffMhi = 49152;    // 32 rows (t) x K=32 (s): hi(M)
+constexpr uint32_t kOffMlo = 53248;    //                          lo(M)
+constexpr uint32_t kOffKhi = 57344;    // 128 rows (dk) x K=32 (c): hi(w_c k_c)
+constexpr uint32_t kOffKlo = 73728;    //                          lo(w_c k_c)
+constexpr uint32_t kOffUt = 90112;     // Ut, plain [c][dv] fp32
+// raw rows of k, q, v: 2 buffers x 3 arrays x 32 rows of 528 bytes (row r on bank 4r)
+constexpr uint32_t kRawRow = 528;
+constexpr int kRawRowF = kRawRow / 4;  // 132 floats
+constexpr uint32_t kRawArr = kC * kRawRow;
+constexpr uint32_t kRawBuf = 3 * kRawArr;
+constexpr uint32_t kOffRaw = 106496;
+constexpr int kAtRow = kC + 4;                         // A^T rows: 36 floats, float4 aligned
+constexpr uint32_t kAtBytes = kC * kAtRow * 4, kMBytes = kC * kC * 4;
+constexpr uint32_t kOffA = kOffRaw + 2 * kRawBuf;      // 2 x A^T [32][36] (At[s][t] = A[t][s])
+constexpr uint32_t kOffM = kOffA + 2 * kAtBytes;       // 2 x M [32][32] (until emitted)
+constexpr uint32_t kOffBars = kOffM + 2 * kMBytes;
 
-
-__device__ unsigned g_watchdog_chunked;
-
-// ============================================================================ chunk prep
-constexpr int kPrepThreads = 256;
-constexpr int kRowPad = kS + 4;  // 132 floats: row r starts on bank 4r, float4 aligned
-
-struct PrepSmem {
-    float k[kC][kRowPad];   // k_t (k-head kh), zero past the end of the sequence
-    float q[kC][kRowPad];
-    float w[kC][kRowPad];   // W, from the forward substitution
-    float v[kC][kS];        // v_t, overwritten in place by Ut
-    float a[kC][kC + 1];    // A (strictly lower)
-    float m[kC][kC];        // exp(gam_t - gam_s)(q_t . k_s), s <= t
-    float gam[kC], Gam[kC], wdec[kC], beta[kC];
-};
-
-// One CTA per (chunk, v-head, sequence). Chunk positions past n_tokens are padded
-// with k = q = v = 0, g = 0, beta = 0: an identity step that writes nothing.
-__global__ void __launch_bounds__(kPrepThreads) chunk_prep_kernel(
-    const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
-    const float *__restrict__ g, const float *__restrict__ beta, unsigned char *__restrict__ ws,
-    int n_tokens, int n_k_heads, int n_v_heads, const int32_t *__restrict__ slots, int pool) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    PrepSmem &sm = *reinterpret_cast<PrepSmem *>(smem_raw);
-    const int ci = blockIdx.x, vh = blockIdx.y, n = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int slot = slots ? slots[n] : n;
-    if (slot < 0 || slot >= pool) return;  // counted by the scan kernel
-    const int H = n_v_heads, Hk = n_k_heads, kh = vh % Hk;
-    const int n_chunks = gridDim.x;
-    const int t0 = ci * kC, valid = min(kC, n_tokens - t0);
-
-    // ---- inputs: 32 rows of k, q (k-head space) and v, as float4
-    for (int idx = tid; idx < kC * kS / 4; idx += kPrepThreads) {
-        const int t = idx / (kS / 4), c4 = (idx % (kS / 4)) * 4;
-        float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), qq = kk, vv = kk;
-        if (t < valid) {
-            const size_t row = static_cast<size_t>(n) * n_tokens + t0 + t;
-            kk = *reinterpret_cast<const float4 *>(k + (row * Hk + kh) * kS + c4);
-            qq = *reinterpret_cast<const float4 *>(q + (row * Hk + kh) * kS + c4);
-            vv = *reinterpret_cast<const float4 *>(v + (row * H + vh) * kS + c4);
-        }
-        *reinterpret_cast<float4 *>(&sm.k[t][c4]) = kk;
-        *reinterpret_cast<float4 *>(&sm.q[t][c4]) = qq;
-        *reinterpret_cast<float4 *>(&sm.v[t][c4]) = vv;
-    }
-    // ---- cumulative log-decay within the chunk (warp 0, lane = position)
-    if (warp == 0) {
-        float gt = 0.f, bt = 0.f;
-        if (lane < valid) {
-            const size_t gi = (static_cast<size_t>(n) * n_tokens + t0 + lane) * H + vh;
-            gt = g[gi];
-            bt = beta[gi];
-        }
-        float c = gt;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(FULL_MASK, c, off);
-            if (lane >= off) c += o;
-        }
-        const float last = __shfl_sync(FULL_MASK, c, 31);
-        sm.gam[lane] = c;
-        sm.Gam[lane] = expf(c);
-        sm.wdec[lane] = expf(last - c);
-        sm.beta[lane] = bt;
-    }
-    __syncthreads();
-
-    // ---- Gram products: thread -> row t = tid / 8, columns s = tid % 8 + 8 j
-    {
-        const int t = tid >> 3, s0 = tid & 7;
-        float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int i = 0; i < kS; i += 4) {
-            const float4 kt = *reinterpret_cast<const float4 *>(&sm.k[t][i]);
-            const float4 qt = *reinterpret_cast<const float4 *>(&sm.q[t][i]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 ks = *reinterpret_cast<const float4 *>(&sm.k[s0 + 8 * j][i]);
-                kk[j] = fmaf(kt.x, ks.x, kk[j]);
-                kk[j] = fmaf(kt.y, ks.y, kk[j]);
-                kk[j] = fmaf(kt.z, ks.z, kk[j]);
-                kk[j] = fmaf(kt.w, ks.w, kk[j]);
-                qk[j] = fmaf(qt.x, ks.x, qk[j]);
-                qk[j] = fmaf(qt.y, ks.y, qk[j]);
-                qk[j] = fmaf(qt.z, ks.z, qk[j]);
-                qk[j] = fmaf(qt.w, ks.w, qk[j]);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int s = s0 + 8 * j;
-            const float e = s <= t ? expf(sm.gam[t] - sm.gam[s]) : 0.f;
-            sm.a[t][s] = s < t ? sm.beta[t] * (e * kk[j]) : 0.f;
-            sm.m[t][s] = e * qk[j];
-        }
-    }
-    __syncthreads();
-
-    // ---- forward substitution, one column per thread: W (threads 0..127) and Ut
-    // (threads 128..255). Row t = base_t - sum_{s<t} A[t][s] row_s.
-    {
-        const int col = tid & (kS - 1);
-        const bool is_w = tid < kS;
-        float x[kC];
-#pragma unroll
-        for (int t = 0; t < kC; ++t) {
-            float acc = is_w ? sm.beta[t] * sm.Gam[t] * sm.k[t][col] : sm.beta[t] * sm.v[t][col];
-#pragma unroll
-            for (int s = 0; s < t; ++s) acc = fmaf(-sm.a[t][s], x[s], acc);
-            x[t] = acc;
-        }
-#pragma unroll
-        for (int t = 0; t < kC; ++t) {
-            if (is_w) sm.w[t][col] = x[t];
-            else sm.v[t][col] = x[t];
-        }
-    }
-    __syncthreads();
-
-    // ---- the record, written as 16-byte pieces in image order (coalesced)
-    unsigned char *rec = ws + ((static_cast<size_t>(n) * H + vh) * n_chunks + ci) * kRecord;
-    auto split4 = [](float4 x, float4 &hi, float4 &lo) {
-        tc::split_tf32(x.x, hi.x, lo.x);
-        tc::split_tf32(x.y, hi.y, lo.y);
-        tc::split_tf32(x.z, hi.z, lo.z);
-        tc::split_tf32(x.w, hi.w, lo.w);
-    };
-    // W: rows c, K = dk (one tf32 pass; the tensor core reads the fp32 bits as tf32)
-    for (int idx = tid; idx < kC * kS / 4; idx += kPrepThreads) {
-        const uint32_t o = idx * 16u;
-        const int c = (o / kSboW) * 8 + (o % 128) / 16, k0 = ((o % kSboW) / 128) * 4;
-        *reinterpret_cast<float4 *>(rec + kOffW + o) = *reinterpret_cast<const float4 *>(&sm.w[c][k0]);
-    }
-    // wK^T: rows dk, K = c
-    for (int idx = tid; idx < kS * kC / 4; idx += kPrepThreads) {
-        const uint32_t o = idx * 16u;
-        const int d = (o / kSboK) * 8 + (o % 128) / 16, c0 = ((o % kSboK) / 128) * 4;
-        const float4 x = make_float4(sm.wdec[c0] * sm.k[c0][d], sm.wdec[c0 + 1] * sm.k[c0 + 1][d],
-                                     sm.wdec[c0 + 2] * sm.k[c0 + 2][d],
-                                     sm.wdec[c0 + 3] * sm.k[c0 + 3][d]);
-        float4 hi, lo;
-        split4(x, hi, lo);
-        *reinterpret_cast<float4 *>(rec + kOffKhi + o) = hi;
-        *reinterpret_cast<float4 *>(rec + kOffKlo + o) = lo;
-    }
-    // QM: rows t, K = (dk | s)
-    for (int idx = tid; idx < kC * kQmK / 4; idx += kPrepThreads) {
-        const uint32_t o = idx * 16u;
-        const int t = (o / kSboQ) * 8 + (o % 128) / 16, k0 = ((o % kSboQ) / 128) * 4;
-        float4 x;
-        if (k0 < kS) {
-            x = *reinterpret_cast<const float4 *>(&sm.q[t][k0]);
-            const float G = sm.Gam[t];
-            x.x *= G; x.y *= G; x.z *= G; x.w *= G;
-        } else {
-            x = *reinterpret_cast<const float4 *>(&sm.m[t][k0 - kS]);
-        }
-        float4 hi, lo;
-        split4(x, hi, lo);
-        *reinterpret_cast<float4 *>(rec + kOffQhi + o) = hi;
-        *reinterpret_cast<float4 *>(rec + kOffQlo + o) = lo;
-    }
-    // Ut: plain [c][dv]
-    for (int idx = tid; idx < kC * kS / 4; idx += kPrepThreads) {
-        const int c = idx / (kS / 4), d4 = (idx % (kS / 4)) * 4;
-        *reinterpret_cast<float4 *>(rec + kOffUt + idx * 16) = *reinterpret_cast<const float4 *>(&sm.v[c][d4]);
-    }
-    if (tid == 0) *reinterpret_cast<float *>(rec + kOffScal) = sm.Gam[kC - 1];
-}
-
-
-// ============================================================================ chunk scan
-constexpr int kScanTcThreads = 192;  // warp 0 producer, warp 1 MMA issuer, warps 2..5 state
-constexpr unsigned WD_MMA = 8u;      // a hand-off between the MMA issuer and the state warps
-constexpr uint32_t kTmemCols = 512;
-// Tensor-memory columns (lane = dv): the state S^T, its tf32 hi/lo split (A operand
-// of the S products), U^T hi/lo (A operand of the U products), D_u and D_y.
-constexpr uint32_t kColSacc = 0, kColShi = 128, kColSlo = 256, kColUhi = 384, kColUlo = 416,
-                   kColDu = 448, kColDy = 480;
-static_assert(kColDy + kC == kTmemCols, "tensor-memory plan fills the allocation");
-
-struct ScanBars {
-    uint64_t full[2], empty[2];  // stage landed / stage free
-    uint64_t s_ready, a_done, u_ready, b_done, y_done, fin;
+struct Bars {
+    uint64_t raw_full[2], raw_empty[2], gram_ready[2];
+    uint64_t img_ready, s_ready, u_ready;
+    uint64_t a_done, b_done, y_done, fin;
     uint32_t taddr;
     int abort;
 };
-constexpr size_t kScanSmem = 2 * static_cast<size_t>(kRecord) + sizeof(ScanBars);
+constexpr size_t kSmemBytes = kOffBars + sizeof(Bars);
+static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
+static_assert(kOffRaw == kOffUt + kC * kS * 4, "image layout");
+static_assert(kOffBars % 8 == 0, "mbarrier alignment");
+
+// ---- warps
+constexpr int kProducerWarp = 0, kMmaWarp = 1;
+constexpr int kStateWarp0 = 2, kStateWarps = 8;
+constexpr int kPrepWarp0 = kStateWarp0 + kStateWarps, kPrepWarps = 8;
+constexpr int kThreads = 32 * (kPrepWarp0 + kPrepWarps);  // 576
+constexpr int kPrepThreads = 32 * kPrepWarps;
+constexpr int kStateThreads = 32 * kStateWarps;
+// Named barriers: one per multi-warp role. In each role one leader thread polls the
+// mbarriers and the other warps sleep in the named barrier, which leaves the issue
+// slots to the warps doing arithmetic.
+constexpr int kPrepBarrier = 1, kStateBarrier = 2;
+
+// ---- tensor memory (columns; lane = dv)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColSacc = 0, kColShi = 128, kColSlo = 256, kColUhi = 384, kColUlo = 416,
+                   kColDu = 448, kColDy = 480;  // D_u and D_y adjacent: one N = 64 MMA fills both
+static_assert(kColDy + kC == kTmemCols, "tensor-memory plan fills the allocation");
+
 
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
-// One CTA per (sequence, v-head); grid = n_seqs * n_v_heads. One CTA per SM (its
-// shared memory and all 512 tensor-memory columns).
-__global__ void __launch_bounds__(kScanTcThreads, 1) chunk_scan_kernel(
-    float *__restrict__ state, const unsigned char *__restrict__ ws, float *__restrict__ y,
-    int n_tokens, int n_v_heads, float scale, const int32_t *__restrict__ slots, int pool,
-    int32_t *err_count) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    ScanBars &bars = *reinterpret_cast<ScanBars *>(smem_raw + 2 * kRecord);
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+// Named barrier over `count` threads that also ORs `pred` over them: every thread
+// gets the same answer, so a role whose warps must stay in step can leave its
+// loop together.
+__device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+
+// Cumulative log-decay of a chunk from g_lane (lane = position, 0 past the end of
+// the sequence): returns gam_lane and sets `last` = gam_31. Every warp that needs
+// these runs this same code on the same inputs, so all get the same bits.
+__device__ __forceinline__ float chunk_gam_from(float c, int lane, float &last) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(FULL_MASK, c, off);
+        if (lane >= off) c += o;
+    }
+    last = __shfl_sync(FULL_MASK, c, 31);
+    return c;
+}
+
+__device__ __forceinline__ void split4(float4 x, float4 &hi, float4 &lo) {
+    tc::split_tf32(x.x, hi.x, lo.x);
+    tc::split_tf32(x.y, hi.y, lo.y);
+    tc::split_tf32(x.z, hi.z, lo.z);
+    tc::split_tf32(x.w, hi.w, lo.w);
+}
+
+// Partial Gram products of row t against columns s0 + 8 j, j < JN, over all of dk:
+// kk[j] = k_t . k_s, qk[j] = q_t . k_s. JN is a compile-time count so every load
+// of a step is issued before its FMAs.
+template <int JN>
+__device__ __forceinline__ void gram_row(const float *rk, const float *rq, int t, int s0,
+                                         float (&kk)[4], float (&qk)[4]) {
+#pragma unroll 2
+    for (int i = 0; i < kS; i += 4) {
+        const float4 kt = ld4(rk + t * kRawRowF + i), qt = ld4(rq + t * kRawRowF + i);
+        float4 ks[JN];
+#pragma unroll
+        for (int j = 0; j < JN; ++j) ks[j] = ld4(rk + (s0 + 8 * j) * kRawRowF + i);
+#pragma unroll
+        for (int j = 0; j < JN; ++j) {
+            kk[j] = fmaf(kt.x, ks[j].x, kk[j]);
+            kk[j] = fmaf(kt.y, ks[j].y, kk[j]);
+            kk[j] = fmaf(kt.z, ks[j].z, kk[j]);
+            kk[j] = fmaf(kt.w, ks[j].w, kk[j]);
+            qk[j] = fmaf(qt.x, ks[j].x, qk[j]);
+            qk[j] = fmaf(qt.y, ks[j].y, qk[j]);
+            qk[j] = fmaf(qt.z, ks[j].z, qk[j]);
+            qk[j] = fmaf(qt.w, ks[j].w, qk[j]);
+        }
+    }
+}
+
+// The Gram stage of a chunk, by the 256 threads of one role (warp gw = 0..7):
+//   At[s][t] = beta_t exp(gam_t - gam_s) (k_t . k_s)   (s < t, else 0)
+//   M[t][s]  = exp(gam_t - gam_s) (q_t . k_s)          (s <= t, else 0)
+// gam and bet hold the chunk's gam_lane and beta_lane. Row t = 4 rb + lane / 8 against
+// columns s = lane % 8 + 8 j (lower triangle only); warps gw and gw + 4 share an SM
+// sub-partition, so a short row block is paired with a long one (0+7, 2+5, 1+6, 3+4).
+__device__ __forceinline__ void chunk_gram(const float *rk, const float *rq, float *At, float *Msc,
+                                           float gam, float bet, int gw, int lane) {
+    const int pb = gw & 3, rb0 = ((pb & 1) << 1) | (pb >> 1);
+    const int rb = gw < 4 ? rb0 : 7 - rb0;
+    const int t = 4 * rb + (lane >> 3), s0 = lane & 7;
+    const int jmax = (4 * rb + 3) >> 3;  // last block j with 8 j <= the warp's max t
+    float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
+    switch (jmax) {  // warp-uniform
+        case 0: gram_row<1>(rk, rq, t, s0, kk, qk); break;
+        case 1: gram_row<2>(rk, rq, t, s0, kk, qk); break;
+        case 2: gram_row<3>(rk, rq, t, s0, kk, qk); break;
+        default: gram_row<4>(rk, rq, t, s0, kk, qk); break;
+    }
+    const float gam_t = __shfl_sync(FULL_MASK, gam, t);
+    const float bet_t = __shfl_sync(FULL_MASK, bet, t);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int s = s0 + 8 * j;
+        const float gam_s = __shfl_sync(FULL_MASK, gam, s);
+        const float e = s <= t ? expf(gam_t - gam_s) : 0.f;
+        At[s * kAtRow + t] = s < t ? bet_t * (e * kk[j]) : 0.f;
+        Msc[t * kC + s] = e * qk[j];
+    }
+}
+
+// One CTA per (sequence, v-head); grid = n_seqs * n_v_heads.
+__global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
+    float *__restrict__ state, const float *__restrict__ q, const float *__restrict__ k,
+    const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
+    float *__restrict__ y, int n_tokens, int n_k_heads, int n_v_heads, float scale,
+    const int32_t *__restrict__ slots, int pool, int32_t *err_count) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBars);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int H = n_v_heads;
-    const int vh = blockIdx.x % H, n = blockIdx.x / H;
+    const int H = n_v_heads, Hk = n_k_heads;
+    const int vh = blockIdx.x % H, n = blockIdx.x / H, kh = vh % Hk;
     const int slot = slots ? slots[n] : n;
     if (slot < 0 || slot >= pool) {  // uniform over the CTA, before any barrier
         if (vh == 0 && tid == 0 && err_count) atomicAdd(err_count, 1);
         return;
     }
     const int n_chunks = (n_tokens + kC - 1) / kC;
-    const unsigned char *rec0 = ws + (static_cast<size_t>(n) * H + vh) * n_chunks * kRecord;
-    auto stage = [&](int st) { return smem_raw + st * kRecord; };
+    const size_t row0 = static_cast<size_t>(n) * n_tokens;  // (n, t = 0) in [N][T] order
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars.full[i], 1);
-            mbar_init(&bars.empty[i], 1 + 4);  // the MMA commit + one arrival per state warp
+            mbar_init(&bars.raw_full[i], 1);
+            mbar_init(&bars.raw_empty[i], 1);
+            mbar_init(&bars.gram_ready[i], 1);
         }
-        mbar_init(&bars.s_ready, 4);
+        mbar_init(&bars.img_ready, 1);  // arrived by the leader of each role after its
+        mbar_init(&bars.s_ready, 1);    // named barrier
+        mbar_init(&bars.u_ready, 1);
         mbar_init(&bars.a_done, 1);
-        mbar_init(&bars.u_ready, 4);
         mbar_init(&bars.b_done, 1);
         mbar_init(&bars.y_done, 1);
         mbar_init(&bars.fin, 1);
         bars.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc(&bars.taddr, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -309,193 +251,394 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) chunk_scan_kernel(
 
     // A wait that gives up raises the watchdog flag and sets `abort`; every role then
     // leaves its loop and all threads meet at the final barrier.
+    // Polls sleep between tries (at most 128 ns): the pollers share SM sub-partitions
+    // with the prep warps, whose issue slots bound the whole scan.
     auto wait1 = [&](uint64_t *bar, int parity, unsigned bit) {
         if (*abort_flag) return false;
-        if (mbar_wait(bar, parity & 1)) return true;
+        if (mbar_wait_sleep(bar, parity & 1, 128)) return true;
         atomicOr(&g_watchdog_chunked, bit);
         *abort_flag = 1;
         return false;
     };
+    // One lane polls, the rest of the warp waits at the shuffle: warp-uniform result.
+    auto waitw = [&](uint64_t *bar, int parity, unsigned bit) {
+        int ok = 0;
+        if (lane == 0) ok = wait1(bar, parity, bit);
+        return __shfl_sync(FULL_MASK, ok, 0) != 0;
+    };
+    // The same for a multi-warp role: its leader thread polls, the role's other
+    // threads sleep in the role's named barrier, and all get the same answer.
+    auto group_wait = [&](bool leader, int barrier_id, int threads, uint64_t *bar, int parity,
+                          unsigned bit) {
+        bool failed = false;
+        if (leader) failed = !wait1(bar, parity, bit);
+        return !named_barrier_or(barrier_id, threads, failed || *abort_flag);
+    };
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int issued = 0;  // copies issued; chunk ci went to stage ci & 1
-            for (int ci = 0; ci < n_chunks; ++ci) {
-                const int st = ci & 1, use = ci >> 1;
-                if (use > 0 && !wait1(&bars.empty[st], use - 1, WD_STAGE_FREE)) break;
-                mbar_arrive_expect_tx(&bars.full[st], kRecord);
-                bulk_g2s(stage(st), rec0 + static_cast<size_t>(ci) * kRecord, kRecord,
-                         &bars.full[st]);
-                issued = ci + 1;
+        int issued = 0;
+        for (int ci = 0; ci < n_chunks; ++ci) {
+            const int b = ci & 1, use = ci >> 1;
+            if (use > 0 && !waitw(&bars.raw_empty[b], use - 1, WD_STAGE_FREE)) break;
+            const int t0 = ci * kC, valid = min(kC, n_tokens - t0);
+            unsigned char *raw = smem + kOffRaw + b * kRawBuf;
+            if (lane == 0) mbar_arrive_expect_tx(&bars.raw_full[b], 3u * valid * kS * 4);
+            __syncwarp();
+            if (lane < valid) {
+                const size_t row = row0 + t0 + lane;
+                bulk_g2s(raw + lane * kRawRow, k + (row * Hk + kh) * kS, kS * 4, &bars.raw_full[b]);
+                bulk_g2s(raw + kRawArr + lane * kRawRow, q + (row * Hk + kh) * kS, kS * 4,
+                         &bars.raw_full[b]);
+                bulk_g2s(raw + 2 * kRawArr + lane * kRawRow, v + (row * H + vh) * kS, kS * 4,
+                         &bars.raw_full[b]);
             }
-            // never leave with a copy still landing in shared memory: wait for the last
-            // copy into each stage
-            for (int ci = max(0, issued - 2); ci < issued; ++ci)
-                mbar_wait(&bars.full[ci & 1], (ci >> 1) & 1);
+            issued = ci + 1;
         }
-    } else if (warp == 1) {
+        // never leave with a copy still landing: wait for the last fill of each buffer
+        for (int ci = max(0, issued - 2); ci < issued; ++ci)
+            mbar_wait_sleep(&bars.raw_full[ci & 1], (ci >> 1) & 1, 128);
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t id32 = tc::idesc_tf32(128, kC), id128 = tc::idesc_tf32(128, kS);
-            const uint32_t a_s[3] = {kColShi, kColShi, kColSlo}, a_u[3] = {kColUhi, kColUhi, kColUlo};
-            const uint32_t b_q[3] = {kOffQhi, kOffQlo, kOffQhi}, b_k[3] = {kOffKhi, kOffKlo, kOffKhi};
+            const uint32_t id64 = tc::idesc_tf32(128, 2 * kC), id32 = tc::idesc_tf32(128, kC),
+                           id128 = tc::idesc_tf32(128, kS);
+            auto desc = [&](uint32_t off, uint32_t sbo) { return tc::smem_desc(smem + off, kLbo, sbo); };
             for (int ci = 0; ci < n_chunks; ++ci) {
-                const int st = ci & 1, use = ci >> 1;
-                if (!wait1(&bars.full[st], use, WD_STAGE_COPY)) break;
+                if (!wait1(&bars.img_ready, ci, WD_MMA)) break;
                 if (!wait1(&bars.s_ready, ci, WD_MMA)) break;
                 tc::fence_after_sync();
-                const unsigned char *sb = stage(st);
-                // D_u = S^T W^T: U^T before the subtraction (one pass)
+                // [D_u | D_y] = hi(S)^T [W | hi(Gam Q)]^T: all of W S (one pass) and the
+                // first pass of the S part of y
                 for (int ks = 0; ks < kS / 8; ++ks)
                     tc::mma_tf32_ts(tmem + kColDu, tmem + kColShi + 8 * ks,
-                                    tc::smem_desc(sb + kOffW + ks * 2 * kLbo, kLbo, kSboW), id32,
-                                    ks > 0);
+                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id64, ks > 0);
                 tc::mma_commit(&bars.a_done);
-                // D_y = S^T (Gam Q)^T (three passes; the U part follows below)
-                for (int p = 0; p < 3; ++p)
-                    for (int ks = 0; ks < kS / 8; ++ks)
-                        tc::mma_tf32_ts(tmem + kColDy, tmem + a_s[p] + 8 * ks,
-                                        tc::smem_desc(sb + b_q[p] + ks * 2 * kLbo, kLbo, kSboQ),
-                                        id32, p > 0 || ks > 0);
+                // D_y += hi(S)^T lo(Gam Q)^T + lo(S)^T hi(Gam Q)^T
+                for (int ks = 0; ks < kS / 8; ++ks)
+                    tc::mma_tf32_ts(tmem + kColDy, tmem + kColShi + 8 * ks,
+                                    desc(kOffQlo + ks * 2 * kLbo, kSbo128), id32, true);
+                for (int ks = 0; ks < kS / 8; ++ks)
+                    tc::mma_tf32_ts(tmem + kColDy, tmem + kColSlo + 8 * ks,
+                                    desc(kOffWQ + 4 * kSbo128 + ks * 2 * kLbo, kSbo128), id32,
+                                    true);
                 if (!wait1(&bars.u_ready, ci, WD_MMA)) break;
                 tc::fence_after_sync();
-                // S^T += U^T (w K): the state update, accumulated in place
-                for (int p = 0; p < 3; ++p)
+                // S^T += U^T (w K): hi hi + hi lo + lo hi, accumulated in place
+                for (int p = 0; p < 3; ++p) {
+                    const uint32_t a = p == 2 ? kColUlo : kColUhi, bo = p == 1 ? kOffKlo : kOffKhi;
                     for (int ks = 0; ks < kC / 8; ++ks)
-                        tc::mma_tf32_ts(tmem + kColSacc, tmem + a_u[p] + 8 * ks,
-                                        tc::smem_desc(sb + b_k[p] + ks * 2 * kLbo, kLbo, kSboK),
-                                        id128, true);
+                        tc::mma_tf32_ts(tmem + kColSacc, tmem + a + 8 * ks,
+                                        desc(bo + ks * 2 * kLbo, kSbo32), id128, true);
+                }
                 tc::mma_commit(&bars.b_done);
                 // D_y += U^T M^T
-                for (int p = 0; p < 3; ++p)
+                for (int p = 0; p < 3; ++p) {
+                    const uint32_t a = p == 2 ? kColUlo : kColUhi, bo = p == 1 ? kOffMlo : kOffMhi;
                     for (int ks = 0; ks < kC / 8; ++ks)
-                        tc::mma_tf32_ts(
-                            tmem + kColDy, tmem + a_u[p] + 8 * ks,
-                            tc::smem_desc(sb + b_q[p] + (kS / 8 + ks) * 2 * kLbo, kLbo, kSboQ),
-                            id32, true);
+                        tc::mma_tf32_ts(tmem + kColDy, tmem + a + 8 * ks,
+                                        desc(bo + ks * 2 * kLbo, kSbo32), id32, true);
+                }
                 tc::mma_commit(&bars.y_done);
-                tc::mma_commit(&bars.empty[st]);
             }
             tc::mma_commit(&bars.fin);  // tensor memory stays allocated until all MMAs end
-            mbar_wait(&bars.fin, 0);
+            mbar_wait_sleep(&bars.fin, 0, 128);
         }
-    } else {
+    } else if (warp < kPrepWarp0) {
         // ------------------------------------------------------------ state warps
-        const int quarter = warp & 3;  // the tensor-memory lanes this warp may access
+        // Warp w may access tensor-memory lanes 32 (w % 4) ..; two warps share each
+        // quarter of the lanes and split the columns: S columns c0 .. c0 + 63, U and
+        // D_y columns (positions) u0 .. u0 + 15.
+        const int quarter = warp & 3, half = (warp - kStateWarp0) >> 2;
         const int dv = quarter * 32 + lane;
+        const int c0 = half * 64, u0 = half * 16;
         const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         float *srow = state + ((static_cast<size_t>(slot) * H + vh) * kS + dv) * kS;
-        auto waitw = [&](uint64_t *bar, int parity, unsigned bit) {
-            return __all_sync(FULL_MASK, wait1(bar, parity, bit)) != 0;
+        const float *ut = reinterpret_cast<const float *>(smem + kOffUt);
+        const bool leader = warp == kStateWarp0 && lane == 0;
+        auto st_wait = [&](uint64_t *bar, int parity, unsigned bit = WD_MMA) {
+            return group_wait(leader, kStateBarrier, kStateThreads, bar, parity, bit);
         };
-#pragma unroll 1
-        for (int blk = 0; blk < kS / 32; ++blk) {
-            uint32_t r[32];
+        // Signal the MMA issuer once every state warp's tensor-memory stores are done.
+        auto st_signal = [&](uint64_t *bar) {
+            tc::fence_before_sync();
+            named_barrier_sync(kStateBarrier, kStateThreads);
+            if (leader) mbar_arrive(bar);
+        };
+
+        // y of chunk cj from D_y; false if the wait gave up
+        auto store_y = [&](int cj) {
+            if (!st_wait(&bars.y_done, cj)) return false;
+            tc::fence_after_sync();
+            uint32_t dy[16];
+            tc::tmem_ld16_nowait(trow + kColDy + u0, dy);
+            tc::tmem_ld_wait();
+            const int t0 = cj * kC, valid = min(kC, n_tokens - t0);
+            float *yp = y + ((row0 + t0) * H + vh) * kS + dv;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(srow + 32 * blk + e);
+            for (int e = 0; e < 16; ++e)
+                if (u0 + e < valid) yp[static_cast<size_t>(u0 + e) * H * kS] = scale * u2f(dy[e]);
+            return true;
+        };
+
+        // The Gram stage of chunk cj (its decay inputs gj, bj, lane = position), in the
+        // time these warps would otherwise wait for the prep warps: pad the rows past
+        // the end of the sequence with zeros (an identity step), then fill buffer cj & 1
+        // of A^T and M.
+        const int sw = warp - kStateWarp0, st_tid = 32 * sw + lane;
+        auto gram_chunk = [&](int cj, float gj, float bj) {
+            const int b = cj & 1, valid = min(kC, n_tokens - cj * kC);
+            if (!st_wait(&bars.raw_full[b], cj >> 1, WD_STAGE_COPY)) return false;
+            float *rk = reinterpret_cast<float *>(smem + kOffRaw + b * kRawBuf);
+            if (valid < kC) {
+                const int pad = (kC - valid) * kS;
+                for (int i = st_tid; i < 3 * pad; i += kStateThreads) {
+                    const int arr = i / pad, rem = i % pad;
+                    rk[arr * kC * kRawRowF + (valid + rem / kS) * kRawRowF + rem % kS] = 0.f;
+                }
+                named_barrier_sync(kStateBarrier, kStateThreads);
+            }
+            float last;
+            const float gam = chunk_gam_from(gj, lane, last);
+            chunk_gram(rk, rk + kC * kRawRowF, reinterpret_cast<float *>(smem + kOffA + b * kAtBytes),
+                       reinterpret_cast<float *>(smem + kOffM + b * kMBytes), gam, bj, sw, lane);
+            st_signal(&bars.gram_ready[b]);
+            return true;
+        };
+
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+            uint32_t r[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 x = ld4(srow + c0 + 16 * blk + e);
                 r[e] = f2u(x.x); r[e + 1] = f2u(x.y); r[e + 2] = f2u(x.z); r[e + 3] = f2u(x.w);
             }
-            tc::tmem_st32(trow + kColSacc + 32 * blk, r);
+            tc::tmem_st16(trow + kColSacc + c0 + 16 * blk, r);
         }
         tc::tmem_st_wait();
-        bool ok = true;
-        for (int ci = 0; ci < n_chunks; ++ci) {
-            const int st = ci & 1, use = ci >> 1;
-            const unsigned char *sb = stage(st);
+        float g_cur = 0.f, b_cur = 0.f;  // decay inputs of chunk ci, lane = position
+        if (lane < min(kC, n_tokens)) {
+            g_cur = g[(row0 + lane) * H + vh];
+            b_cur = beta[(row0 + lane) * H + vh];
+        }
+        bool ok = gram_chunk(0, g_cur, b_cur);
+        for (int ci = 0; ci < n_chunks && ok; ++ci) {
+            float last;
+            (void)chunk_gam_from(g_cur, lane, last);
+            const float gn = expf(last);
+            float g_nx = 0.f, b_nx = 0.f;  // the next chunk's, for its Gram stage below
+            if ((ci + 1) * kC + lane < n_tokens) {
+                g_nx = g[(row0 + (ci + 1) * kC + lane) * H + vh];
+                b_nx = beta[(row0 + (ci + 1) * kC + lane) * H + vh];
+            }
             if (ci > 0) {
-                if (!(ok = waitw(&bars.b_done, ci - 1, WD_MMA))) break;
+                if (!(ok = st_wait(&bars.b_done, ci - 1))) break;
                 tc::fence_after_sync();
             }
-            if (!(ok = waitw(&bars.full[st], use, WD_STAGE_COPY))) break;
-            const float gn = *reinterpret_cast<const float *>(sb + kOffScal);
-            // S -> (hi, lo) for the tensor cores; the accumulator becomes Gam_31 S
+            // S -> (hi, lo), the A operand of the S products; the accumulator becomes
+            // Gam_31 S, ready for this chunk's update
 #pragma unroll 1
-            for (int blk = 0; blk < kS / 32; ++blk) {
-                uint32_t r[32], hi[32], lo[32];
-                tc::tmem_ld32_nowait(trow + kColSacc + 32 * blk, r);
+            for (int blk = 0; blk < 4; ++blk) {
+                const uint32_t col = c0 + 16 * blk;
+                uint32_t r[16], hi[16], lo[16];
+                tc::tmem_ld16_nowait(trow + kColSacc + col, r);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float x = __uint_as_float(r[e]);
+                for (int e = 0; e < 16; ++e) {
+                    const float x = u2f(r[e]);
                     float h, l;
                     tc::split_tf32(x, h, l);
                     hi[e] = f2u(h);
                     lo[e] = f2u(l);
                     r[e] = f2u(gn * x);
                 }
-                tc::tmem_st32(trow + kColShi + 32 * blk, hi);
-                tc::tmem_st32(trow + kColSlo + 32 * blk, lo);
-                tc::tmem_st32(trow + kColSacc + 32 * blk, r);
+                tc::tmem_st16(trow + kColShi + col, hi);
+                tc::tmem_st16(trow + kColSlo + col, lo);
+                tc::tmem_st16(trow + kColSacc + col, r);
             }
             tc::tmem_st_wait();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.s_ready);
+            // the previous chunk's y leaves D_y before this chunk's MMAs overwrite it
+            if (ci > 0 && !(ok = store_y(ci - 1))) break;
+            st_signal(&bars.s_ready);
+            // the next chunk's Gram stage, while the prep warps finish this chunk
+            if (ci + 1 < n_chunks && !(ok = gram_chunk(ci + 1, g_nx, b_nx))) break;
+            g_cur = g_nx;
+            b_cur = b_nx;
 
-            // U^T = Ut^T - D_u
-            if (!(ok = waitw(&bars.a_done, ci, WD_MMA))) break;
+            // U^T = Ut^T - D_u, split (a_done comes after img_ready, so it also says Ut
+            // is in place; the leader checks both)
+            if (!(ok = st_wait(&bars.img_ready, ci))) break;
+            if (!(ok = st_wait(&bars.a_done, ci))) break;
             tc::fence_after_sync();
             {
-                uint32_t du[32], hi[32], lo[32];
-                tc::tmem_ld32_nowait(trow + kColDu, du);
+                uint32_t du[16], hi[16], lo[16];
+                tc::tmem_ld16_nowait(trow + kColDu + u0, du);
                 tc::tmem_ld_wait();
-                const float *ut = reinterpret_cast<const float *>(sb + kOffUt);
 #pragma unroll
-                for (int c = 0; c < kC; ++c) {
-                    const float u = ut[c * kS + dv] - __uint_as_float(du[c]);
+                for (int e = 0; e < 16; ++e) {
+                    const float u = ut[(u0 + e) * kS + dv] - u2f(du[e]);
                     float h, l;
                     tc::split_tf32(u, h, l);
-                    hi[c] = f2u(h);
-                    lo[c] = f2u(l);
+                    hi[e] = f2u(h);
+                    lo[e] = f2u(l);
                 }
-                tc::tmem_st32(trow + kColUhi, hi);
-                tc::tmem_st32(trow + kColUlo, lo);
+                tc::tmem_st16(trow + kColUhi + u0, hi);
+                tc::tmem_st16(trow + kColUlo + u0, lo);
                 tc::tmem_st_wait();
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars.u_ready);
-                mbar_arrive(&bars.empty[st]);  // done reading Ut and Gam_31 of this stage
-            }
-
-            // y_t = scale D_y[dv][t]
-            if (!(ok = waitw(&bars.y_done, ci, WD_MMA))) break;
-            tc::fence_after_sync();
-            {
-                uint32_t dy[32];
-                tc::tmem_ld32_nowait(trow + kColDy, dy);
-                tc::tmem_ld_wait();
-                const int t0 = ci * kC, valid = min(kC, n_tokens - t0);
-                float *yp = y + ((static_cast<size_t>(n) * n_tokens + t0) * H + vh) * kS + dv;
-#pragma unroll
-                for (int t = 0; t < kC; ++t)
-                    if (t < valid) yp[static_cast<size_t>(t) * H * kS] = scale * __uint_as_float(dy[t]);
-            }
+            st_signal(&bars.u_ready);
         }
-        if (ok && (ok = waitw(&bars.b_done, n_chunks - 1, WD_MMA))) {
+        if (ok && n_chunks > 0) ok = store_y(n_chunks - 1);
+        if (ok && n_chunks > 0 && (ok = st_wait(&bars.b_done, n_chunks - 1))) {
             tc::fence_after_sync();
 #pragma unroll 1
-            for (int blk = 0; blk < kS / 32; ++blk) {
-                uint32_t r[32];
-                tc::tmem_ld32_nowait(trow + kColSacc + 32 * blk, r);
+            for (int blk = 0; blk < 4; ++blk) {
+                uint32_t r[16];
+                tc::tmem_ld16_nowait(trow + kColSacc + c0 + 16 * blk, r);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4 *>(srow + 32 * blk + e) =
-                        make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                                    __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+                for (int e = 0; e < 16; e += 4)
+                    *reinterpret_cast<float4 *>(srow + c0 + 16 * blk + e) =
+                        make_float4(u2f(r[e]), u2f(r[e + 1]), u2f(r[e + 2]), u2f(r[e + 3]));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ prep warps
+        // All eight warps take every decision together (named_barrier_or), so none is
+        // ever left waiting at a named barrier that another has abandoned.
+        const int pt = tid - 32 * kPrepWarp0;  // 0..255
+        float *utw = reinterpret_cast<float *>(smem + kOffUt);
+        // true: leave the loop (a wait gave up somewhere)
+        auto prep_wait = [&](uint64_t *bar, int parity, unsigned bit) {
+            return !group_wait(pt == 0, kPrepBarrier, kPrepThreads, bar, parity, bit);
+        };
+        auto prep_sync = [&]() {
+            return named_barrier_or(kPrepBarrier, kPrepThreads, *abort_flag != 0);
+        };
+        float g_next = 0.f, b_next = 0.f;  // decay inputs of the next chunk, lane = position
+        if (lane < min(kC, n_tokens)) {
+            g_next = g[(row0 + lane) * H + vh];
+            b_next = beta[(row0 + lane) * H + vh];
+        }
+        for (int ci = 0; ci < n_chunks; ++ci) {
+            const int b = ci & 1, use = ci >> 1;
+            const int t0 = ci * kC;
+            float *rk = reinterpret_cast<float *>(smem + kOffRaw + b * kRawBuf);
+            float *rq = rk + kC * kRawRowF, *rv = rq + kC * kRawRowF;
+            const float *At = reinterpret_cast<const float *>(smem + kOffA + b * kAtBytes);
+            const float *Msc = reinterpret_cast<const float *>(smem + kOffM + b * kMBytes);
+            // per-position decay quantities, lane = position (each warp its own copy)
+            float last;
+            const float gam = chunk_gam_from(g_next, lane, last);
+            const float Gam = expf(gam), wdec = expf(last - gam);
+            const float bet = b_next;
+            g_next = b_next = 0.f;
+            if (t0 + kC + lane < n_tokens) {
+                g_next = g[(row0 + t0 + kC + lane) * H + vh];
+                b_next = beta[(row0 + t0 + kC + lane) * H + vh];
+            }
+            // the state warps have padded the raw rows and written A^T and M of this chunk
+            if (prep_wait(&bars.gram_ready[b], use, WD_MMA)) break;
+
+            // ---- forward substitution, one column per thread: W (warps 0..3), Ut (4..7).
+            // Row t is base_t - sum_{s<t} A[t][s] x_s, accumulated in order of s; done
+            // column-wise (x_s is final once the rows above are, and then updates every
+            // row below it), so the dependent chain is 32 steps long, not 496. Ut goes
+            // straight to its buffer and W to the dead raw v rows, so first wait until
+            // the previous chunk is done with Ut (its U is formed, which also means its
+            // W S product is done) and until every thread has read its base.
+            if (ci > 0 ? prep_wait(&bars.u_ready, ci - 1, WD_MMA) : prep_sync()) break;
+            const int col = pt & (kS - 1);
+            const bool is_w = pt < kS;
+            float x[kC];
+#pragma unroll
+            for (int t = 0; t < kC; ++t) {
+                const float bt = __shfl_sync(FULL_MASK, bet, t);
+                const float Gt = __shfl_sync(FULL_MASK, Gam, t);
+                x[t] = is_w ? bt * Gt * rk[t * kRawRowF + col] : bt * rv[t * kRawRowF + col];
+            }
+            named_barrier_sync(kPrepBarrier, kPrepThreads);
+#pragma unroll
+            for (int s2 = 0; s2 < kC - 1; ++s2) {
+#pragma unroll
+                for (int m = (s2 + 1) / 4; m < kC / 4; ++m) {
+                    const float4 a = ld4(At + s2 * kAtRow + 4 * m);
+                    if (4 * m + 0 > s2) x[4 * m + 0] = fmaf(-a.x, x[s2], x[4 * m + 0]);
+                    if (4 * m + 1 > s2) x[4 * m + 1] = fmaf(-a.y, x[s2], x[4 * m + 1]);
+                    if (4 * m + 2 > s2) x[4 * m + 2] = fmaf(-a.z, x[s2], x[4 * m + 2]);
+                    if (4 * m + 3 > s2) x[4 * m + 3] = fmaf(-a.w, x[s2], x[4 * m + 3]);
+                }
+            }
+            {
+                float *outp = is_w ? rv : utw;
+                const int ostride = is_w ? kRawRowF : kS;
+#pragma unroll
+                for (int t = 0; t < kC; ++t) outp[t * ostride + col] = x[t];
+            }
+            named_barrier_sync(kPrepBarrier, kPrepThreads);
+            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {  // W image
+                const uint32_t o = idx * 16u;
+                const int c = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
+                *reinterpret_cast<float4 *>(smem + kOffWQ + o) = ld4(rv + c * kRawRowF + k0);
+            }
+
+            // ---- w_c k_c, split, once the previous chunk's state update is done
+            if (ci > 0 ? prep_wait(&bars.b_done, ci - 1, WD_MMA) : prep_sync()) break;
+            for (int idx = pt; idx < kS * kC / 4; idx += kPrepThreads) {
+                const uint32_t o = idx * 16u;
+                const int d = (o / kSbo32) * 8 + (o % 128) / 16, cc = ((o % kSbo32) / 128) * 4;
+                float4 xv;
+                xv.x = __shfl_sync(FULL_MASK, wdec, cc) * rk[cc * kRawRowF + d];
+                xv.y = __shfl_sync(FULL_MASK, wdec, cc + 1) * rk[(cc + 1) * kRawRowF + d];
+                xv.z = __shfl_sync(FULL_MASK, wdec, cc + 2) * rk[(cc + 2) * kRawRowF + d];
+                xv.w = __shfl_sync(FULL_MASK, wdec, cc + 3) * rk[(cc + 3) * kRawRowF + d];
+                float4 hi, lo;
+                split4(xv, hi, lo);
+                *reinterpret_cast<float4 *>(smem + kOffKhi + o) = hi;
+                *reinterpret_cast<float4 *>(smem + kOffKlo + o) = lo;
+            }
+
+            // ---- Gam_t q_t and M, split, once the previous chunk's y products are done
+            if (ci > 0 ? prep_wait(&bars.y_done, ci - 1, WD_MMA) : prep_sync()) break;
+            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {
+                const uint32_t o = idx * 16u;
+                const int t = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
+                const float Gt = __shfl_sync(FULL_MASK, Gam, t);
+                float4 xv = ld4(rq + t * kRawRowF + k0);
+                xv.x *= Gt; xv.y *= Gt; xv.z *= Gt; xv.w *= Gt;
+                float4 hi, lo;
+                split4(xv, hi, lo);
+                *reinterpret_cast<float4 *>(smem + kOffWQ + 4 * kSbo128 + o) = hi;  // rows 32..63
+                *reinterpret_cast<float4 *>(smem + kOffQlo + o) = lo;
+            }
+            for (int idx = pt; idx < kC * kC / 4; idx += kPrepThreads) {
+                const uint32_t o = idx * 16u;
+                const int t = (o / kSbo32) * 8 + (o % 128) / 16, s0 = ((o % kSbo32) / 128) * 4;
+                float4 hi, lo;
+                split4(ld4(Msc + t * kC + s0), hi, lo);
+                *reinterpret_cast<float4 *>(smem + kOffMhi + o) = hi;
+                *reinterpret_cast<float4 *>(smem + kOffMlo + o) = lo;
+            }
+            // the operands are read by the tensor cores (async proxy) and Ut by the
+            // state warps
+            fence_proxy_async_smem();
+            named_barrier_sync(kPrepBarrier, kPrepThreads);
+            if (pt == 0) {
+                mbar_arrive(&bars.img_ready);
+                mbar_arrive(&bars.raw_empty[b]);  // done with this chunk's raw rows
             }
         }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
+}  // namespace gdn
+
+namespace gdn {
 
 unsigned read_and_clear_watchdog_chunked(cudaStream_t s) {
     unsigned flags = 0;
@@ -510,55 +653,28 @@ unsigned read_and_clear_watchdog_chunked(cudaStream_t s) {
 
 using namespace gdn;
 
-extern "C" {
-
-size_t gdn_recurrence_scan_chunked_workspace_size(int n_seqs, int n_tokens, int n_v_heads,
-                                                  int state_size) {
-    if (n_seqs < 0 || n_tokens < 0 || n_v_heads < 1 || state_size != kS) return 0;
-    const size_t n_chunks = (static_cast<size_t>(n_tokens) + kC - 1) / kC;
-    return static_cast<size_t>(n_seqs) * n_v_heads * n_chunks * kRecord;
-}
-
-gdn_status gdn_recurrence_scan_chunked(float *state, const float *q, const float *k,
-                                       const float *v, const float *g, const float *beta,
-                                       float *y, int n_seqs, int n_tokens, int n_k_heads,
-                                       int n_v_heads, int state_size, float scale,
-                                       const int32_t *slots, int pool, int32_t *err_count,
-                                       void *workspace, size_t workspace_bytes,
-                                       gdn_stream_t stream) {
+extern "C" gdn_status gdn_recurrence_scan_chunked(float *state, const float *q, const float *k,
+                                                  const float *v, const float *g,
+                                                  const float *beta, float *y, int n_seqs,
+                                                  int n_tokens, int n_k_heads, int n_v_heads,
+                                                  int state_size, float scale,
+                                                  const int32_t *slots, int pool,
+                                                  int32_t *err_count, gdn_stream_t stream) {
     if (!state || !q || !k || !v || !g || !beta || !y) return GDN_ERR_NULL;
     if (n_seqs < 0 || n_tokens < 0) return GDN_ERR_SHAPE;
     GDN_TRY(check_heads(n_k_heads, n_v_heads, state_size));
     if (state_size != kS) return GDN_ERR_UNSUPPORTED;
     GDN_TRY(check_pool(n_seqs, slots, pool));
-    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y))
-        return GDN_ERR_ALIGN;
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_ERR_ALIGN;
     if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
-    if (n_seqs > 65535 || n_v_heads > 65535 ||
-        static_cast<long long>(n_seqs) * n_v_heads > 0x7fffffffLL)
-        return GDN_ERR_UNSUPPORTED;
-    const size_t need = gdn_recurrence_scan_chunked_workspace_size(n_seqs, n_tokens, n_v_heads,
-                                                                   state_size);
-    if (!workspace) return GDN_ERR_NULL;
-    if (workspace_bytes < need) return GDN_ERR_SHAPE;
-    if (!aligned16(workspace)) return GDN_ERR_ALIGN;
-    const cudaStream_t s = as_cuda(stream);
-    const int n_chunks = (n_tokens + kC - 1) / kC;
-    static bool attrs = [] {
-        cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(PrepSmem)));
-        cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kScanSmem));
+    if (static_cast<long long>(n_seqs) * n_v_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    static const bool attr_set = [] {
+        cudaFuncSetAttribute(chunked_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
         return true;
     }();
-    (void)attrs;
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
-    chunk_prep_kernel<<<dim3(n_chunks, n_v_heads, n_seqs), kPrepThreads, sizeof(PrepSmem), s>>>(
-        q, k, v, g, beta, ws, n_tokens, n_k_heads, n_v_heads, slots, pool);
-    GDN_TRY(launch_status());
-    chunk_scan_kernel<<<n_seqs * n_v_heads, kScanTcThreads, kScanSmem, s>>>(
-        state, ws, y, n_tokens, n_v_heads, scale, slots, pool, err_count);
+    (void)attr_set;
+    chunked_scan_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, as_cuda(stream)>>>(
+        state, q, k, v, g, beta, y, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count);
     return launch_status();
 }
-
-}  // extern "C"

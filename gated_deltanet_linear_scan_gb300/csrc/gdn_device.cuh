@@ -76,6 +76,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return true;
 }
 
+// The same bounded wait for a thread that shares its SM sub-partition with warps
+// doing arithmetic: between polls it sleeps (backing off from 32 ns to max_sleep_ns),
+// so it takes next to no issue slots; the cost is up to max_sleep_ns of extra latency.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                unsigned max_sleep_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    unsigned ns = 32;
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+        __nanosleep(ns);
+        ns = ns < max_sleep_ns ? 2 * ns : max_sleep_ns;
+    }
+    return true;
+}
+
 // 1-D bulk copy global -> shared (TMA engine), completion counted on `bar` in bytes.
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

@@ -176,24 +176,17 @@ gdn_status gdn_recurrence_scan_snapshots(float *state, const float *q, const flo
  * keeps the sequential scan as its permanent reference; the chunked algebra
  * itself (an exact regrouping of the recurrence, the WY/UT form) is not given on
  * the pages.
- * Arguments, layouts and slot semantics as gdn_recurrence_scan, plus
- * workspace: device memory of at least
- *   gdn_recurrence_scan_chunked_workspace_size(n_seqs, n_tokens, H, S)
- * bytes (per sequence, v-head and chunk of 32 positions: 106,624 bytes of
- * tensor-core operands), 16-byte aligned, owned by the caller; its contents are
- * ignored on entry and meaningless on return. NULL is GDN_ERR_NULL, too small is
- * GDN_ERR_SHAPE.
+ * Arguments, layouts, ownership and slot semantics exactly as gdn_recurrence_scan
+ * (a drop-in replacement); it needs no workspace and allocates nothing. y needs
+ * no particular alignment; state, q, k and v are 16-byte aligned (GDN_ERR_ALIGN).
  * Only state_size 128 has this form (else GDN_ERR_UNSUPPORTED). Results agree
- * with the sequential scan to within rounding (the same 2e-3-of-RMS bound after
- * 4096 positions), not bit for bit. */
-size_t gdn_recurrence_scan_chunked_workspace_size(int n_seqs, int n_tokens, int n_v_heads,
-                                                  int state_size);
+ * with the sequential scan to within rounding (the 2e-3-of-RMS bound of a
+ * 4096-position scan), not bit for bit. */
 gdn_status gdn_recurrence_scan_chunked(float *state, const float *q, const float *k,
                                        const float *v, const float *g, const float *beta,
                                        float *y, int n_seqs, int n_tokens, int n_k_heads,
                                        int n_v_heads, int state_size, float scale,
                                        const int32_t *slots, int pool, int32_t *err_count,
-                                       void *workspace, size_t workspace_bytes,
                                        gdn_stream_t stream);
 
 /* The conv scan, also writing the conv history after every position (ssm_gated_delta.cu,

@@ -166,36 +166,23 @@ def test_prefill_validation(lib):
 
 
 def test_chunked_scan_validation(lib):
-    ws = lib.gdn_recurrence_scan_chunked_workspace_size
-    ws.restype = ctypes.c_size_t
-    ws.argtypes = [ctypes.c_int] * 4
-    # one 106,624-byte record per (sequence, v-head, chunk of 32 positions)
-    assert ws(2, 65, 4, 128) == 2 * 4 * 3 * 106624
-    assert ws(2, 64, 4, 128) == 2 * 4 * 2 * 106624
-    assert ws(2, 64, 4, 64) == 0 and ws(-1, 64, 4, 128) == 0
     f = lib.gdn_recurrence_scan_chunked
     f.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p,
                                                                 ctypes.c_int, ctypes.c_void_p,
-                                                                ctypes.c_void_p, ctypes.c_size_t,
                                                                 ctypes.c_void_p]
-    need = ws(2, 40, 4, 128)
 
-    def call(state=P, q=P, s=128, hk=2, hv=4, n_tokens=40, workspace=P, nbytes=need, pool=2,
-             slots=None, y=P):
-        return f(state, q, P, P, P, P, y, 2, n_tokens, hk, hv, s, 0.1, slots, pool, None,
-                 workspace, nbytes, None)
+    def call(state=P, q=P, s=128, hk=2, hv=4, n_tokens=40, pool=2, y=P):
+        return f(state, q, P, P, P, P, y, 2, n_tokens, hk, hv, s, 0.1, None, pool, None, None)
     assert call(state=None) == NULL
     assert call(y=None) == NULL
-    assert call(workspace=None) == NULL
-    assert call(nbytes=need - 16) == SHAPE
-    assert call(workspace=MIS) == ALIGN
     assert call(q=MIS) == ALIGN
+    assert call(state=MIS) == ALIGN
     assert call(s=64) == UNSUP            # valid for the method; the tensor-core form is S = 128
     assert call(s=96) == UNSUP
     assert call(s=100) == SHAPE
     assert call(hk=3) == SHAPE
     assert call(pool=1) == SHAPE          # more sequences than slots, no slot map
-    assert call(n_tokens=0, workspace=None) == OK
+    assert call(n_tokens=0) == OK
 
 
 def test_block_validation(lib):

@@ -56,10 +56,8 @@ def case(Hk, H, N, T, seed, pool=None):
 def run_chunked(lib, cfg, x, st, slots=None, pool=None, err=None):
     N, T, H, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.state_size
     y = torch.zeros(N, T, H, S, device="cuda")
-    nbytes = lib.gdn_recurrence_scan_chunked_workspace_size(N, T, H, S)
-    ws = torch.empty(max(nbytes, 16) // 4, device="cuda")
     lib.gdn_recurrence_scan_chunked(st, dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["g"]),
-                                    dev(x["beta"]), y, N, T, cfg.n_k_heads, H, S, cfg.scale, ws,
+                                    dev(x["beta"]), y, N, T, cfg.n_k_heads, H, S, cfg.scale,
                                     slots=slots, pool=pool, err_count=err)
     return y
 
