@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload batched_decode_64|single_seq_decode_1000|
                                 serving_pool_256_of_512|prefill_scan_4x4096|
-                                prefill_block_4x4096]
+                                prefill_chunked_4x4096|prefill_block_4x4096]
 
 Default workload: batched decode, 64 independent sequences, one token each per
 step (Hk=16, H=32, S=128, conv 4), through the fused gdn_block_decode kernel.
@@ -39,7 +39,20 @@ from gated_deltanet_linear_scan_gb300 import inputs as I  # noqa: E402
 
 METRIC = "GDN decode tokens/s and state HBM GB/s (fraction of GB300 peak), 1 GPU"
 WORKLOADS = {"batched_decode_64": 3, "single_seq_decode_1000": 1,
-             "serving_pool_256_of_512": 4, "prefill_scan_4x4096": 2, "prefill_block_4x4096": 2}
+             "serving_pool_256_of_512": 4, "prefill_scan_4x4096": 2,
+             "prefill_chunked_4x4096": 2, "prefill_block_4x4096": 2}
+# TF32 tensor-core rate relative to bf16 (nominal dense figures, 1.1 / 2.25 PFLOP/s)
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def chunked_tensor_flops(n_seqs, n_tokens, n_v_heads):
+    """Tensor-core flops of one chunked-scan launch (S = 128, chunks of 32): per
+    (sequence, v-head, chunk) S^T [W | Gam Q]^T (N = 64, first pass), two more passes
+    each of W S and of the S part of y (N = 32), the state update (3 passes, N = 128,
+    K = 32) and the U part of y (3 passes, N = 32, K = 32)."""
+    per = 2 * 128 * 64 * 128 + 4 * (2 * 128 * 32 * 128) + 3 * (2 * 128 * 128 * 32) + \
+        3 * (2 * 128 * 32 * 32)
+    return per * n_seqs * n_v_heads * ((n_tokens + 31) // 32)
 FLUSH_BYTES = 256 << 20
 L2_NOTE = "flushed before every timed step (256 MiB write, then 256 MiB read: cold, clean L2)"
 FALLBACK_HBM_GBS = 6800.0
@@ -68,6 +81,9 @@ KERNEL_SOURCES = {
                             "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh"],
     "recurrence_scan_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_recurrence.cu",
                                "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh"],
+    "chunked_scan_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_chunked.cu",
+                            "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh",
+                            "gated_deltanet_linear_scan_gb300/csrc/gdn_tc.cuh"],
 }
 
 
@@ -225,7 +241,7 @@ def cpu_sample_scan(cfg, tokens, budget_s):
 def run_reference(args, cfg, rank, world):
     if rank != 0:
         return 0
-    if args.workload == "prefill_scan_4x4096":
+    if args.workload in ("prefill_scan_4x4096", "prefill_chunked_4x4096"):
         tokens = 256
         vals = []
         t_all = time.perf_counter()
@@ -419,9 +435,11 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     state = state0.clone()
     y = torch.empty(N, T, H, S, device="cuda")
 
+    chunked = args.workload == "prefill_chunked_4x4096"
+    scan_fn = gdn.gdn_recurrence_scan_chunked if chunked else gdn.gdn_recurrence_scan
+
     def launch():
-        gdn.gdn_recurrence_scan(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y, N, T, Hk, H,
-                                S, cfg.scale)
+        scan_fn(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y, N, T, Hk, H, S, cfg.scale)
 
     for _ in range(args.warmup):
         state.copy_(state0)
@@ -470,6 +488,20 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
     fp32_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
     achieved = flops / per / 1e12
+    if chunked:
+        tf = chunked_tensor_flops(N, T, H)
+        tf32_peak = pk["bf16_tflops"] * TF32_PER_BF16 if "bf16_tflops" in pk else 1900.0 * TF32_PER_BF16
+        roofline = {"bound": "tensor", "achieved": tf / per / 1e12, "peak": tf32_peak,
+                    "unit": "TFLOP/s", "frac": tf / per / 1e12 / tf32_peak,
+                    "traffic": ncu_traffic("chunked_scan_kernel", args.workload),
+                    "flops_per_launch": tf,
+                    "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
+                                   f"{TF32_PER_BF16:.3f}"}
+    else:
+        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp32_peak,
+                    "traffic": ncu_traffic("recurrence_scan_kernel", args.workload),
+                    "peak_source": "FP32 FMA pipes: SMs x 128 lanes x 2 flop x median SM clock"}
     if rank != 0:
         return 0
     cpu = None
@@ -484,12 +516,12 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded PCG64; unit q/k, g~U(-0.5,-0.001))",
         "config": {"workload": args.workload, "n_seqs": N, "n_tokens": T, "n_k_heads": Hk,
-                   "n_v_heads": H, "state_size": S, "kernel": "gdn_recurrence_scan",
-                   "l2": L2_NOTE},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp32_peak,
-                     "traffic": ncu_traffic("recurrence_scan_kernel", args.workload),
-                     "peak_source": "FP32 FMA pipes: SMs x 128 lanes x 2 flop x median SM clock"},
+                   "n_v_heads": H, "state_size": S,
+                   "kernel": "gdn_recurrence_scan_chunked" if chunked else "gdn_recurrence_scan",
+                   "l2": L2_NOTE,
+                   "method_fp32_tflops": achieved,
+                   "method_fp32_frac_of_fp32_pipe_peak": achieved / fp32_peak},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -517,9 +549,9 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     ws = torch.empty(gdn.gdn_block_prefill_workspace_size(N, T, Hk, H, S) // 4 + 64, device="cuda")
 
     def launch():
-        gdn.gdn_block_prefill(d["qkv"], st["conv_w"], conv, d["alpha"], d["b"], st["dt"], st["a"],
-                              d["z"], st["norm_w"], state, out, N, T, Hk, H, S, cfg.conv_kernel,
-                              cfg.scale, cfg.eps, cfg.eps, ws)
+        gdn.gdn_block_prefill_chunked(d["qkv"], st["conv_w"], conv, d["alpha"], d["b"], st["dt"],
+                                      st["a"], d["z"], st["norm_w"], state, out, N, T, Hk, H, S,
+                                      cfg.conv_kernel, cfg.scale, cfg.eps, cfg.eps, ws)
 
     def reset():
         state.copy_(state0)
@@ -568,7 +600,7 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         state.copy_(state0)
         flush()
         scan_ev[i][0].record(stream)
-        gdn.gdn_recurrence_scan(state, q, k, v, g, beta, y, N, T, Hk, H, S, cfg.scale)
+        gdn.gdn_recurrence_scan_chunked(state, q, k, v, g, beta, y, N, T, Hk, H, S, cfg.scale)
         scan_ev[i][1].record(stream)
     torch.cuda.synchronize()
     scan_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in scan_ev) / 1e3, dist,
@@ -595,6 +627,8 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
 
     flops = 7.0 * N * T * H * S * S
+    tf = chunked_tensor_flops(N, T, H)
+    tf32_peak = pk.get("bf16_tflops", 1900.0) * TF32_PER_BF16
     props = torch.cuda.get_device_properties(0)
     clk = clocks.summary()
     mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
@@ -615,14 +649,18 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         "data": "synthetic (seeded PCG64; N(0,1) qkv/z, g~U(-0.5,-0.001))",
         "config": {"workload": args.workload, "n_seqs": N, "n_tokens": T, "n_k_heads": Hk,
                    "n_v_heads": H, "state_size": S, "conv_kernel": cfg.conv_kernel,
-                   "kernel": "gdn_block_prefill (6 launches: conv scan, split norm, gate, beta, "
-                             "scan, gated norm)", "l2": L2_NOTE,
-                   "scan_ms": 1e3 * scan_s},
-        "roofline": {"bound": "alu", "kernel": "recurrence_scan_kernel",
-                     "achieved": flops / scan_s / 1e12, "peak": fp32_peak, "unit": "TFLOP/s",
-                     "frac": flops / scan_s / 1e12 / fp32_peak,
-                     "traffic": ncu_traffic("recurrence_scan_kernel", "prefill_scan_4x4096"),
-                     "peak_source": "FP32 FMA pipes: SMs x 128 lanes x 2 flop x median SM clock"},
+                   "kernel": "gdn_block_prefill_chunked (6 launches: conv scan, split norm, "
+                             "gate, beta, chunked tensor-core scan, gated norm)", "l2": L2_NOTE,
+                   "scan_ms": 1e3 * scan_s,
+                   "method_fp32_tflops_of_scan": flops / scan_s / 1e12,
+                   "fp32_pipe_peak_tflops": fp32_peak},
+        "roofline": {"bound": "tensor", "kernel": "chunked_scan_kernel",
+                     "achieved": tf / scan_s / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
+                     "frac": tf / scan_s / 1e12 / tf32_peak,
+                     "traffic": ncu_traffic("chunked_scan_kernel", "prefill_chunked_4x4096"),
+                     "flops_per_launch": tf,
+                     "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
+                                    f"{TF32_PER_BF16:.3f}"},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -22,7 +22,7 @@ __all__ = [
     "gdn_block_decode", "gdn_recurrence_decode_2pass", "gdn_recurrence_scan_snapshots",
     "gdn_conv1d_silu_seq_snapshots", "gdn_block_prefill_workspace_size", "gdn_block_prefill",
     "gdn_block_prefill_noalloc", "PREFILL_NOALLOC_SCRATCH_BYTES",
-    "gdn_recurrence_scan_chunked",
+    "gdn_recurrence_scan_chunked", "gdn_block_prefill_chunked",
 ]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
@@ -62,6 +62,8 @@ _SIGS = {
     "gdn_block_prefill_noalloc": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P,
                                                _P], _I),
     "gdn_recurrence_scan_chunked": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
+    "gdn_block_prefill_chunked": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P, _P,
+                                               ctypes.c_size_t, _P], _I),
 }
 
 # Size of the fixed device scratch of gdn_block_prefill_noalloc (include/gdn.h).
@@ -276,19 +278,31 @@ def gdn_block_prefill_workspace_size(n_seqs, n_tokens, n_k_heads, n_v_heads, sta
 
 def gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
                       n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
-                      norm_eps, workspace, slots=None, pool=None, err_count=None, stream=None):
+                      norm_eps, workspace, slots=None, pool=None, err_count=None, stream=None,
+                      _name="gdn_block_prefill"):
     """`workspace`: a CUDA tensor of at least gdn_block_prefill_workspace_size() bytes."""
     pool = _pool(pool, n_seqs, slots)
     import torch
     if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
-    _check("gdn_block_prefill", library().gdn_block_prefill(
+    _check(_name, getattr(library(), _name)(
         _ptr(qkv, "qkv"), _ptr(conv_w, "conv_w"), _ptr(conv_state, "conv_state"),
         _ptr(alpha, "alpha"), _ptr(b, "b"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(z, "z"),
         _ptr(norm_w, "norm_w"), _ptr(state, "state"), _ptr(out, "out"), n_seqs, n_tokens,
         n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps, norm_eps, _slots(slots),
         pool, _errc(err_count), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def gdn_block_prefill_chunked(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,
+                              n_seqs, n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel,
+                              scale, l2_eps, norm_eps, workspace, slots=None, pool=None,
+                              err_count=None, stream=None):
+    """gdn_block_prefill with the chunked tensor-core scan (state_size 128)."""
+    gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                      n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                      norm_eps, workspace, slots=slots, pool=pool, err_count=err_count,
+                      stream=stream, _name="gdn_block_prefill_chunked")
 
 
 def gdn_block_prefill_noalloc(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,

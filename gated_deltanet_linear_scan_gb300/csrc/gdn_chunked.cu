@@ -32,11 +32,10 @@
 //   MMA (1 thread)     D_u|D_y = S^T [W | Gam Q]^T, D_y += the rest of the S part,
 //                      S^T = Gam_31 S^T + U^T (w K), D_y += U^T M^T.
 //
-// Precision: a single TF32 pass (10-bit mantissa) in any product that feeds the
+// Precision: a single TF32 pass (10-bit mantissa) in the products that feed the
 // state or y misses a 2e-3-of-RMS error bound after 4096 positions; the split
-// x = hi + lo with hi*hi + hi*lo + lo*hi ("3xTF32") restores fp32-level products.
-// Only W S tolerates one pass: its error enters U, which the delta rule corrects
-// at the next write.
+// x = hi + lo with hi*hi + hi*lo + lo*hi ("3xTF32") restores fp32-level products,
+// and every product here uses it.
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 #include "gdn_tc.cuh"
@@ -55,19 +54,22 @@ constexpr uint32_t kSbo32 = (kC / 4) * 128;    // next 8 rows, K = 32 operands
 
 // ---- shared memory (bytes)
 // tensor-core operands, K-major core-matrix images (see gdn_tc.cuh)
-constexpr uint32_t kOffWQ = 0;         // 64 rows x K=128: rows 0..31 W, rows 32..63 hi(Gam q)
+constexpr uint32_t kOffWQ = 0;         // 64 rows x K=128: rows 0..31 hi(W), rows 32..63 hi(Gam q)
 constexpr uint32_t kOffQlo = 32768;    // 32 rows x K=128: lo(Gam q)
-constexpr uint32_t kOffMhi = 49152;    // 32 rows (t) x K=32 (s): hi(M)
-constexpr uint32_t kOffMlo = 53248;    //                          lo(M)
-constexpr uint32_t kOffKhi = 57344;    // 128 rows (dk) x K=32 (c): hi(w_c k_c)
-constexpr uint32_t kOffKlo = 73728;    //                          lo(w_c k_c)
-constexpr uint32_t kOffUt = 90112;     // Ut, plain [c][dv] fp32
-// raw rows of k, q, v: 2 buffers x 3 arrays x 32 rows of 528 bytes (row r on bank 4r)
+constexpr uint32_t kOffWlo = 49152;    // 32 rows x K=128: lo(W)
+constexpr uint32_t kOffMhi = 65536;    // 32 rows (t) x K=32 (s): hi(M)
+constexpr uint32_t kOffMlo = 69632;    //                          lo(M)
+constexpr uint32_t kOffKhi = 73728;    // 128 rows (dk) x K=32 (c): hi(w_c k_c)
+constexpr uint32_t kOffKlo = 90112;    //                          lo(w_c k_c)
+constexpr uint32_t kOffUt = 106496;    // Ut, plain [c][dv] fp32
+// rows of 528 bytes (132 floats): row r starts on bank 4r, float4 aligned
 constexpr uint32_t kRawRow = 528;
-constexpr int kRawRowF = kRawRow / 4;  // 132 floats
+constexpr int kRawRowF = kRawRow / 4;
 constexpr uint32_t kRawArr = kC * kRawRow;
-constexpr uint32_t kRawBuf = 3 * kRawArr;
-constexpr uint32_t kOffRaw = 106496;
+constexpr uint32_t kOffWs = 122880;    // W [32][132] fp32, from the substitution
+// raw rows of k and q: 2 buffers x 2 arrays x 32 rows (v is read from global memory)
+constexpr uint32_t kRawBuf = 2 * kRawArr;
+constexpr uint32_t kOffRaw = kOffWs + kRawArr;
 constexpr int kAtRow = kC + 4;                         // A^T rows: 36 floats, float4 aligned
 constexpr uint32_t kAtBytes = kC * kAtRow * 4, kMBytes = kC * kC * 4;
 constexpr uint32_t kOffA = kOffRaw + 2 * kRawBuf;      // 2 x A^T [32][36] (At[s][t] = A[t][s])
@@ -83,7 +85,7 @@ struct Bars {
 };
 constexpr size_t kSmemBytes = kOffBars + sizeof(Bars);
 static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
-static_assert(kOffRaw == kOffUt + kC * kS * 4, "image layout");
+static_assert(kOffWs == kOffUt + kC * kS * 4, "image layout");
 static_assert(kOffBars % 8 == 0, "mbarrier alignment");
 
 // ---- warps
@@ -283,14 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             if (use > 0 && !waitw(&bars.raw_empty[b], use - 1, WD_STAGE_FREE)) break;
             const int t0 = ci * kC, valid = min(kC, n_tokens - t0);
             unsigned char *raw = smem + kOffRaw + b * kRawBuf;
-            if (lane == 0) mbar_arrive_expect_tx(&bars.raw_full[b], 3u * valid * kS * 4);
+            if (lane == 0) mbar_arrive_expect_tx(&bars.raw_full[b], 2u * valid * kS * 4);
             __syncwarp();
             if (lane < valid) {
                 const size_t row = row0 + t0 + lane;
                 bulk_g2s(raw + lane * kRawRow, k + (row * Hk + kh) * kS, kS * 4, &bars.raw_full[b]);
                 bulk_g2s(raw + kRawArr + lane * kRawRow, q + (row * Hk + kh) * kS, kS * 4,
-                         &bars.raw_full[b]);
-                bulk_g2s(raw + 2 * kRawArr + lane * kRawRow, v + (row * H + vh) * kS, kS * 4,
                          &bars.raw_full[b]);
             }
             issued = ci + 1;
@@ -308,11 +308,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
                 if (!wait1(&bars.img_ready, ci, WD_MMA)) break;
                 if (!wait1(&bars.s_ready, ci, WD_MMA)) break;
                 tc::fence_after_sync();
-                // [D_u | D_y] = hi(S)^T [W | hi(Gam Q)]^T: all of W S (one pass) and the
-                // first pass of the S part of y
+                // [D_u | D_y] = hi(S)^T [hi(W) | hi(Gam Q)]^T: the first pass of W S and
+                // of the S part of y together (N = 64), then the other two of W S
                 for (int ks = 0; ks < kS / 8; ++ks)
                     tc::mma_tf32_ts(tmem + kColDu, tmem + kColShi + 8 * ks,
                                     desc(kOffWQ + ks * 2 * kLbo, kSbo128), id64, ks > 0);
+                for (int ks = 0; ks < kS / 8; ++ks)
+                    tc::mma_tf32_ts(tmem + kColDu, tmem + kColShi + 8 * ks,
+                                    desc(kOffWlo + ks * 2 * kLbo, kSbo128), id32, true);
+                for (int ks = 0; ks < kS / 8; ++ks)
+                    tc::mma_tf32_ts(tmem + kColDu, tmem + kColSlo + 8 * ks,
+                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id32, true);
                 tc::mma_commit(&bars.a_done);
                 // D_y += hi(S)^T lo(Gam Q)^T + lo(S)^T hi(Gam Q)^T
                 for (int ks = 0; ks < kS / 8; ++ks)
@@ -392,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             float *rk = reinterpret_cast<float *>(smem + kOffRaw + b * kRawBuf);
             if (valid < kC) {
                 const int pad = (kC - valid) * kS;
-                for (int i = st_tid; i < 3 * pad; i += kStateThreads) {
+                for (int i = st_tid; i < 2 * pad; i += kStateThreads) {
                     const int arr = i / pad, rem = i % pad;
                     rk[arr * kC * kRawRowF + (valid + rem / kS) * kRawRowF + rem % kS] = 0.f;
                 }
@@ -525,7 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             const int b = ci & 1, use = ci >> 1;
             const int t0 = ci * kC;
             float *rk = reinterpret_cast<float *>(smem + kOffRaw + b * kRawBuf);
-            float *rq = rk + kC * kRawRowF, *rv = rq + kC * kRawRowF;
+            float *rq = rk + kC * kRawRowF;
+            float *ws = reinterpret_cast<float *>(smem + kOffWs);
             const float *At = reinterpret_cast<const float *>(smem + kOffA + b * kAtBytes);
             const float *Msc = reinterpret_cast<const float *>(smem + kOffM + b * kMBytes);
             // per-position decay quantities, lane = position (each warp its own copy)
@@ -540,25 +547,34 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             }
             // the state warps have padded the raw rows and written A^T and M of this chunk
             if (prep_wait(&bars.gram_ready[b], use, WD_MMA)) break;
+            // the Ut columns start from beta_t v_t: fetch v (zero past the end)
+            const int col = pt & (kS - 1);
+            const bool is_w = pt < kS;
+            float x[kC];
+            if (!is_w) {
+                const float *vp = v + ((row0 + t0) * H + vh) * kS + col;
+                const size_t vstride = static_cast<size_t>(H) * kS;
+                const int valid = min(kC, n_tokens - t0);
+#pragma unroll
+                for (int t = 0; t < kC; ++t) {
+                    x[t] = t < valid ? *vp : 0.f;
+                    vp += vstride;
+                }
+            }
 
             // ---- forward substitution, one column per thread: W (warps 0..3), Ut (4..7).
             // Row t is base_t - sum_{s<t} A[t][s] x_s, accumulated in order of s; done
             // column-wise (x_s is final once the rows above are, and then updates every
             // row below it), so the dependent chain is 32 steps long, not 496. Ut goes
-            // straight to its buffer and W to the dead raw v rows, so first wait until
-            // the previous chunk is done with Ut (its U is formed, which also means its
-            // W S product is done) and until every thread has read its base.
+            // straight to its buffer, so first wait until the previous chunk is done with
+            // it (its U is formed, which also means its W S product is done).
             if (ci > 0 ? prep_wait(&bars.u_ready, ci - 1, WD_MMA) : prep_sync()) break;
-            const int col = pt & (kS - 1);
-            const bool is_w = pt < kS;
-            float x[kC];
 #pragma unroll
             for (int t = 0; t < kC; ++t) {
                 const float bt = __shfl_sync(FULL_MASK, bet, t);
                 const float Gt = __shfl_sync(FULL_MASK, Gam, t);
-                x[t] = is_w ? bt * Gt * rk[t * kRawRowF + col] : bt * rv[t * kRawRowF + col];
+                x[t] = is_w ? bt * Gt * rk[t * kRawRowF + col] : bt * x[t];
             }
-            named_barrier_sync(kPrepBarrier, kPrepThreads);
 #pragma unroll
             for (int s2 = 0; s2 < kC - 1; ++s2) {
 #pragma unroll
@@ -571,16 +587,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
                 }
             }
             {
-                float *outp = is_w ? rv : utw;
+                float *outp = is_w ? ws : utw;
                 const int ostride = is_w ? kRawRowF : kS;
 #pragma unroll
                 for (int t = 0; t < kC; ++t) outp[t * ostride + col] = x[t];
             }
             named_barrier_sync(kPrepBarrier, kPrepThreads);
-            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {  // W image
+            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {  // W, split
                 const uint32_t o = idx * 16u;
                 const int c = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
-                *reinterpret_cast<float4 *>(smem + kOffWQ + o) = ld4(rv + c * kRawRowF + k0);
+                float4 hi, lo;
+                split4(ld4(ws + c * kRawRowF + k0), hi, lo);
+                *reinterpret_cast<float4 *>(smem + kOffWQ + o) = hi;  // rows 0..31
+                *reinterpret_cast<float4 *>(smem + kOffWlo + o) = lo;
             }
 
             // ---- w_c k_c, split, once the previous chunk's state update is done

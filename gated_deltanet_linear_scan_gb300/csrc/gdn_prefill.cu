@@ -45,19 +45,26 @@ size_t gdn_block_prefill_workspace_size(int n_seqs, int n_tokens, int n_k_heads,
            sizeof(float);
 }
 
-gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_state,
-                             const float *alpha, const float *b, const float *dt, const float *a,
-                             const float *z, const float *norm_w, float *state, float *out,
-                             int n_seqs, int n_tokens, int n_k_heads, int n_v_heads,
-                             int state_size, int conv_kernel, float scale, float l2_eps,
-                             float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
-                             void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The prefill block with either scan: the sequential one (bit for bit the fused
+// decode step, position after position) or the chunked tensor-core one.
+gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state,
+                        const float *alpha, const float *b, const float *dt, const float *a,
+                        const float *z, const float *norm_w, float *state, float *out,
+                        int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int state_size,
+                        int conv_kernel, float scale, float l2_eps, float norm_eps,
+                        const int32_t *slots, int pool, int32_t *err_count, void *workspace,
+                        size_t workspace_bytes, gdn_stream_t stream, bool chunked) {
     if (!qkv || !conv_w || !conv_state || !alpha || !b || !dt || !a || !z || !norm_w || !state ||
         !out)
         return GDN_ERR_NULL;
     if (n_seqs < 0 || n_tokens < 0) return GDN_ERR_SHAPE;
     if (conv_kernel < 2 || conv_kernel > 8) return GDN_ERR_SHAPE;
     GDN_TRY(check_heads(n_k_heads, n_v_heads, state_size));
+    if (chunked && state_size != 128) return GDN_ERR_UNSUPPORTED;
     GDN_TRY(check_pool(n_seqs, slots, pool));
     if (!aligned16(qkv) || !aligned16(conv_w) || !aligned16(conv_state) || !aligned16(state) ||
         !aligned16(z) || !aligned16(out) || !aligned16(norm_w))
@@ -83,10 +90,45 @@ gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_
                                stream));
     GDN_TRY(gdn_decay_gate(alpha, dt, a, g, H, static_cast<int>(rows), stream));
     GDN_TRY(gdn_beta_sigmoid(b, beta, static_cast<int>(rows * H), stream));
-    GDN_TRY(gdn_recurrence_scan(state, q, k, v, g, beta, out, n_seqs, n_tokens, Hk, H, S, scale,
-                                slots, pool, nullptr, stream));
+    if (chunked) {
+        GDN_TRY(gdn_recurrence_scan_chunked(state, q, k, v, g, beta, out, n_seqs, n_tokens, Hk, H,
+                                            S, scale, slots, pool, nullptr, stream));
+    } else {
+        GDN_TRY(gdn_recurrence_scan(state, q, k, v, g, beta, out, n_seqs, n_tokens, Hk, H, S,
+                                    scale, slots, pool, nullptr, stream));
+    }
     return launch_gated_norm(out, norm_w, z, out, rows * H, S, norm_eps,
                              static_cast<long long>(n_tokens) * H, slots, pool, as_cuda(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_state,
+                             const float *alpha, const float *b, const float *dt, const float *a,
+                             const float *z, const float *norm_w, float *state, float *out,
+                             int n_seqs, int n_tokens, int n_k_heads, int n_v_heads,
+                             int state_size, int conv_kernel, float scale, float l2_eps,
+                             float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
+                             void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                        n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                        norm_eps, slots, pool, err_count, workspace, workspace_bytes, stream, false);
+}
+
+gdn_status gdn_block_prefill_chunked(const float *qkv, const float *conv_w, float *conv_state,
+                                     const float *alpha, const float *b, const float *dt,
+                                     const float *a, const float *z, const float *norm_w,
+                                     float *state, float *out, int n_seqs, int n_tokens,
+                                     int n_k_heads, int n_v_heads, int state_size,
+                                     int conv_kernel, float scale, float l2_eps, float norm_eps,
+                                     const int32_t *slots, int pool, int32_t *err_count,
+                                     void *workspace, size_t workspace_bytes,
+                                     gdn_stream_t stream) {
+    return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                        n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                        norm_eps, slots, pool, err_count, workspace, workspace_bytes, stream, true);
 }
 
 }  // extern "C"

@@ -246,6 +246,21 @@ gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_
                              float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
                              void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/* gdn_block_prefill with the chunked tensor-core scan (gdn_recurrence_scan_chunked)
+ * in place of the sequential one: the production path for long prefill. Same
+ * arguments, layouts, workspace and error behaviour; state_size must be 128 (else
+ * GDN_ERR_UNSUPPORTED). Results agree with gdn_block_prefill to within rounding
+ * (the 2e-3-of-RMS long-scan bound), not bit for bit. */
+gdn_status gdn_block_prefill_chunked(const float *qkv, const float *conv_w, float *conv_state,
+                                     const float *alpha, const float *b, const float *dt,
+                                     const float *a, const float *z, const float *norm_w,
+                                     float *state, float *out, int n_seqs, int n_tokens,
+                                     int n_k_heads, int n_v_heads, int state_size,
+                                     int conv_kernel, float scale, float l2_eps, float norm_eps,
+                                     const int32_t *slots, int pool, int32_t *err_count,
+                                     void *workspace, size_t workspace_bytes,
+                                     gdn_stream_t stream);
+
 /* Bytes of the fixed device scratch gdn_block_prefill_noalloc works in. */
 #define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -185,6 +185,24 @@ def test_chunked_scan_validation(lib):
     assert call(n_tokens=0) == OK
 
 
+def test_prefill_chunked_validation(lib):
+    f = lib.gdn_block_prefill_chunked
+    f.argtypes = [ctypes.c_void_p] * 11 + [ctypes.c_int] * 6 + [ctypes.c_float] * 3 + [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+        ctypes.c_void_p]
+    ws = lib.gdn_block_prefill_workspace_size
+    ws.restype = ctypes.c_size_t
+
+    def call(s=128, workspace=P, n_tokens=16):
+        need = ws(2, n_tokens, 2, 4, s)
+        return f(P, P, P, P, P, P, P, P, P, P, P, 2, n_tokens, 2, 4, s, 4, 0.1, 1e-6, 1e-6,
+                 None, 2, None, workspace, need, None)
+    assert call(s=64) == UNSUP   # the tensor-core scan is built for S = 128
+    assert call(workspace=None) == NULL
+    assert call(workspace=MIS) == ALIGN
+    assert call(n_tokens=0, workspace=None) == OK
+
+
 def test_block_validation(lib):
     assert block(lib, qkv=None) == NULL
     assert block(lib, out=None) == NULL

@@ -5,7 +5,8 @@ long-scan bound: max |gpu - ref| <= 2e-3 * RMS(ref) for y and for the final
 state, per tensor (ref = the fp64 oracle). Cases cover one position, a chunk
 minus one, exactly one chunk, one more, several chunks with a ragged tail, GQA
 ratios 1, 2 and 4, slot routing with a skipped sequence, and the 4 x 4096 prefill
-workload at full size.
+workload at full size; then the prefill block built on it (gdn_block_prefill_chunked)
+against the oracle's block steps and against the sequential-scan prefill block.
 """
 import numpy as np
 import pytest
@@ -142,3 +143,90 @@ def test_chunked_scan_prefill_4x4096(lib):
         y_ref, _ = oracle.recurrence(s_ref, scale=cfg.scale, **unit)
         assert_rms(yh[n, :, vh], y_ref[0, :, 0], f"y ({n},{vh})")
         assert_rms(sth[n, vh], s_ref[0, 0], f"final state ({n},{vh})")
+
+
+# ------------------------------------------------------------------ prefill block
+
+def run_block_prefill(lib, cfg, T, steps, state, conv, chunked, slots=None, pool=None,
+                      err=None):
+    N, H, S = len(steps[0]["qkv"]), cfg.n_v_heads, cfg.state_size
+    st = I.block_static(cfg)
+    stack = {key: np.stack([a[key] for a in steps], axis=1) for key in ("qkv", "alpha", "b", "z")}
+    out = torch.zeros(N, T, H, S, device="cuda")
+    ws = torch.empty(lib.gdn_block_prefill_workspace_size(N, T, cfg.n_k_heads, H, S) // 4,
+                     device="cuda")
+    fn = lib.gdn_block_prefill_chunked if chunked else lib.gdn_block_prefill
+    fn(dev(stack["qkv"]), dev(st["conv_w"]), conv, dev(stack["alpha"]), dev(stack["b"]),
+       dev(st["dt"]), dev(st["a"]), dev(stack["z"]), dev(st["norm_w"]), state, out, N, T,
+       cfg.n_k_heads, H, S, cfg.conv_kernel, cfg.scale, cfg.eps, cfg.eps, ws, slots=slots,
+       pool=pool, err_count=err)
+    return out
+
+
+def oracle_block_chain(cfg, steps, st0, cs0, seqs):
+    stat = I.block_static(cfg)
+    ref_st, ref_cs = f64(st0[seqs]), f64(cs0[seqs])
+    outs = []
+    for a in steps:
+        r, _ = oracle.block_decode(a["qkv"][seqs], stat["conv_w"], ref_cs, a["alpha"][seqs],
+                                   a["b"][seqs], stat["dt"], stat["a"], a["z"][seqs],
+                                   stat["norm_w"], ref_st, cfg.n_k_heads, cfg.scale, cfg.eps,
+                                   cfg.eps)
+        outs.append(r)
+    return np.stack(outs, axis=1), ref_st, ref_cs
+
+
+@pytest.mark.parametrize("Hk,H,N,T", [(2, 4, 2, 45), (16, 32, 2, 70)])
+def test_block_prefill_chunked(lib, Hk, H, N, T):
+    cfg = I.get_config(0, n_k_heads=Hk, n_v_heads=H, state_size=128, n_seqs=N, cid=900 + T)
+    steps = [I.block_step(cfg, t) for t in range(T)]
+    st0, cs0 = I.state_pool(cfg), I.conv_state_pool(cfg)
+    state, conv = dev(st0), dev(cs0)
+    out = run_block_prefill(lib, cfg, T, steps, state, conv, chunked=True)
+    ref, ref_st, ref_cs = oracle_block_chain(cfg, steps, st0, cs0, list(range(N)))
+    assert_rms(host(out), ref, "out")
+    assert_rms(host(state), ref_st, "state")
+    assert_rms(host(conv), ref_cs, "conv_state")
+    # against the sequential-scan prefill block
+    state2, conv2 = dev(st0), dev(cs0)
+    out2 = run_block_prefill(lib, cfg, T, steps, state2, conv2, chunked=False)
+    assert_rms(host(out), host(out2), "out vs sequential prefill")
+    assert torch.equal(conv, conv2)  # the conv scan is shared: bit for bit
+
+
+def test_block_prefill_chunked_invalid_slot(lib):
+    cfg = I.get_config(0, n_k_heads=2, n_v_heads=4, state_size=128, n_seqs=3, pool=4, cid=950)
+    T = 40
+    steps = [I.block_step(cfg, t) for t in range(T)]
+    st0, cs0 = I.state_pool(cfg), I.conv_state_pool(cfg)
+    state, conv = dev(st0), dev(cs0)
+    slots = np.array([3, 6, 0], dtype=np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_block_prefill(lib, cfg, T, steps, state, conv, chunked=True, slots=dev(slots),
+                            pool=4, err=err)
+    assert host(err)[0] == 1
+    assert np.all(host(out)[1] == 0.0)
+    for sl in (1, 2):
+        np.testing.assert_array_equal(host(state)[sl], st0[sl])
+        np.testing.assert_array_equal(host(conv)[sl], cs0[sl])
+
+
+@pytest.mark.slow
+def test_block_prefill_chunked_4_sequences_512_tokens(lib):
+    """Full-width heads (Hk=16, H=32, S=128), 4 sequences x 512 tokens; one sampled
+    sequence against the oracle, all of them against the sequential-scan block."""
+    cfg = I.get_config(2)
+    T = 512
+    steps = [I.block_step(cfg, t) for t in range(T)]
+    st0, cs0 = I.state_pool(cfg), I.conv_state_pool(cfg)
+    state, conv = dev(st0), dev(cs0)
+    out = run_block_prefill(lib, cfg, T, steps, state, conv, chunked=True)
+    got = host(out)
+    n = 1
+    ref, ref_st, _ = oracle_block_chain(cfg, steps, st0, cs0, [n])
+    assert_rms(got[n], ref[0], "out")
+    assert_rms(host(state)[n], ref_st[0], "state")
+    state2, conv2 = dev(st0), dev(cs0)
+    out2 = run_block_prefill(lib, cfg, T, steps, state2, conv2, chunked=False)
+    assert_rms(got, host(out2), "out vs sequential prefill")
+    assert_rms(host(state), host(state2), "state vs sequential prefill")
