@@ -115,6 +115,16 @@ __global__ void __launch_bounds__(kThreads) block_decode_kernel(const BlockParam
         }
     }
 
+    // The gate input z and the norm weight of this CTA's rows (rb <= 128 < kThreads: at
+    // most one each per thread), fetched now so their latency hides behind the state.
+    static_assert(kThreads >= 128, "one output row per thread");
+    const size_t ob = (static_cast<size_t>(n) * H + vh) * S + row0;
+    float z_pre = 0.0f, w_pre = 0.0f;
+    if (valid && tid < rb) {
+        z_pre = p.z[ob + tid];
+        w_pre = p.norm_w[row0 + tid];
+    }
+
     // 2a. conv1d+SiLU of kh's q and k channels (old history read here).
     float nh[kQKPerThread][kTaps];
     const float *xrow = p.qkv + static_cast<size_t>(n) * conv_dim;
@@ -244,10 +254,8 @@ __global__ void __launch_bounds__(kThreads) block_decode_kernel(const BlockParam
     }
     if (ok) {
         const float inv_rms = 1.0f / sqrtf(ss_total / static_cast<float>(S) + p.norm_eps);
-        const size_t ob = (static_cast<size_t>(n) * H + vh) * S + row0;
-        for (int c = tid; c < rb; c += kThreads) {
-            const float zv = p.z[ob + c];
-            p.out[ob + c] = ybuf[c] * inv_rms * p.norm_w[row0 + c] * silu(zv);
+        if (tid < rb) {
+            p.out[ob + tid] = ybuf[tid] * inv_rms * w_pre * silu(z_pre);
         }
     }
     // Roll kh's q/k history, now that no CTA of the group will read it again.
