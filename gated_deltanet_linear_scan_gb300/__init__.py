@@ -276,16 +276,14 @@ def gdn_block_prefill_workspace_size(n_seqs, n_tokens, n_k_heads, n_v_heads, sta
                                                       state_size)
 
 
-def gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
-                      n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
-                      norm_eps, workspace, slots=None, pool=None, err_count=None, stream=None,
-                      _name="gdn_block_prefill"):
-    """`workspace`: a CUDA tensor of at least gdn_block_prefill_workspace_size() bytes."""
+def _block_prefill(name, qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                   n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                   norm_eps, workspace, slots, pool, err_count, stream):
     pool = _pool(pool, n_seqs, slots)
     import torch
     if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
-    _check(_name, getattr(library(), _name)(
+    _check(name, getattr(library(), name)(
         _ptr(qkv, "qkv"), _ptr(conv_w, "conv_w"), _ptr(conv_state, "conv_state"),
         _ptr(alpha, "alpha"), _ptr(b, "b"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(z, "z"),
         _ptr(norm_w, "norm_w"), _ptr(state, "state"), _ptr(out, "out"), n_seqs, n_tokens,
@@ -294,15 +292,24 @@ def gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state
         _stream(stream)))
 
 
+def gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                      n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                      norm_eps, workspace, slots=None, pool=None, err_count=None, stream=None):
+    """`workspace`: a CUDA tensor of at least gdn_block_prefill_workspace_size() bytes."""
+    _block_prefill("gdn_block_prefill", qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w,
+                   state, out, n_seqs, n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel,
+                   scale, l2_eps, norm_eps, workspace, slots, pool, err_count, stream)
+
+
 def gdn_block_prefill_chunked(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,
                               n_seqs, n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel,
                               scale, l2_eps, norm_eps, workspace, slots=None, pool=None,
                               err_count=None, stream=None):
     """gdn_block_prefill with the chunked tensor-core scan (state_size 128)."""
-    gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
-                      n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
-                      norm_eps, workspace, slots=slots, pool=pool, err_count=err_count,
-                      stream=stream, _name="gdn_block_prefill_chunked")
+    _block_prefill("gdn_block_prefill_chunked", qkv, conv_w, conv_state, alpha, b, dt, a, z,
+                   norm_w, state, out, n_seqs, n_tokens, n_k_heads, n_v_heads, state_size,
+                   conv_kernel, scale, l2_eps, norm_eps, workspace, slots, pool, err_count,
+                   stream)
 
 
 def gdn_block_prefill_noalloc(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,
