@@ -82,19 +82,29 @@ __global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
         const int pos = t0 - TAPS + t;
         hist[t] = pos >= 0 ? x_ptr[static_cast<size_t>(pos) * conv_dim] : old[t];  // t0 == 0
     }
-    for (int p = t0; p < t1; ++p) {
-        const float x = x_ptr[static_cast<size_t>(p) * conv_dim];
-        float pre = __fmul_rn(x, wc[K - 1]);
+    constexpr int B = 16;  // inputs loaded ahead of their use: memory-level parallelism
+    for (int pb = t0; pb < t1; pb += B) {
+        float xs[B];
 #pragma unroll
-        for (int t = 0; t < TAPS; ++t) pre = __fmaf_rn(hist[t], wc[t], pre);
-        o_ptr[static_cast<size_t>(p) * conv_dim] = silu(pre);
+        for (int j = 0; j < B; ++j)
+            xs[j] = pb + j < t1 ? x_ptr[static_cast<size_t>(pb + j) * conv_dim] : 0.0f;
 #pragma unroll
-        for (int t = 0; t + 1 < TAPS; ++t) hist[t] = hist[t + 1];
-        hist[TAPS - 1] = x;
-        if constexpr (SNAP) {  // the history after token p: snaps[n][p][C][K-1]
-            float *sn = snaps + ((static_cast<size_t>(n) * n_tokens + p) * conv_dim + c) * TAPS;
+        for (int j = 0; j < B; ++j) {
+            const int p = pb + j;
+            if (p >= t1) break;
+            const float x = xs[j];
+            float pre = __fmul_rn(x, wc[K - 1]);
 #pragma unroll
-            for (int t = 0; t < TAPS; ++t) sn[t] = hist[t];
+            for (int t = 0; t < TAPS; ++t) pre = __fmaf_rn(hist[t], wc[t], pre);
+            o_ptr[static_cast<size_t>(p) * conv_dim] = silu(pre);
+#pragma unroll
+            for (int t = 0; t + 1 < TAPS; ++t) hist[t] = hist[t + 1];
+            hist[TAPS - 1] = x;
+            if constexpr (SNAP) {  // the history after token p: snaps[n][p][C][K-1]
+                float *sn = snaps + ((static_cast<size_t>(n) * n_tokens + p) * conv_dim + c) * TAPS;
+#pragma unroll
+                for (int t = 0; t < TAPS; ++t) sn[t] = hist[t];
+            }
         }
     }
     if (t0 == 0) {  // the new state: the last K-1 inputs of (old state, this call's inputs)

@@ -1,8 +1,9 @@
 // gdn_prefill.cu -- the block over n_tokens positions per sequence (prefill): the
-// conv scan, the q/k split + L2-norm, the decay gate, beta, the sequential scan of
-// the recurrence and the gated RMSNorm, chained on one stream. Intermediates live
-// in a workspace the caller provides (the library allocates nothing); the scan
-// writes y straight into `out`, which the gated norm then rewrites in place.
+// conv scan fused with the q/k split + L2-norm, the decay gate, beta, the scan of
+// the recurrence (sequential or chunked) and the gated RMSNorm, chained on one
+// stream. Intermediates (q, k, v, g, beta) live in a workspace the caller provides
+// (the library allocates nothing); the scan writes y straight into `out`, which the
+// gated norm then rewrites in place.
 //
 // Follows the batched (prefill) variants of ssm_gated_delta.cu: decay gate, conv
 // scan, q/k norm with the v passthrough, then the recurrence scan, per position.
@@ -17,12 +18,10 @@ constexpr size_t kAlignFloats = 64;  // 256-byte sub-buffers
 size_t round_up(size_t n) { return (n + kAlignFloats - 1) / kAlignFloats * kAlignFloats; }
 
 struct PrefillLayout {
-    size_t conv_out, q, k, v, g, beta, total_floats;
+    size_t q, k, v, g, beta, total_floats;
     PrefillLayout(long long n, long long t, int hk, int h, int s) {
         const size_t rows = static_cast<size_t>(n) * static_cast<size_t>(t);
-        const size_t conv_dim = static_cast<size_t>(2 * hk + h) * s;
-        conv_out = 0;
-        q = conv_out + round_up(rows * conv_dim);
+        q = 0;
         k = q + round_up(rows * hk * s);
         v = k + round_up(rows * hk * s);
         g = v + round_up(rows * h * s);
@@ -30,6 +29,131 @@ struct PrefillLayout {
         total_floats = beta + round_up(rows * h);
     }
 };
+
+// The conv scan and the q/k split + L2-norm in one pass: one CTA per (head slice of
+// S channels, block of positions, sequence), one thread per channel. The conv is
+// the conv scan's arithmetic (current tap, then the history oldest-first; the
+// block at position 0 alone reads and rewrites conv_state). A v slice is written
+// straight out; a q or k slice goes through a shared-memory tile so that one warp
+// per position normalises the head vector with the split-norm kernel's operations
+// (lane L holds elements [E L, E L + E), one butterfly). Results are the two
+// separate kernels' bit for bit, without their [n][t][C] intermediate in HBM.
+template <int E>
+constexpr int conv_norm_positions() { return E >= 8 ? 32 : 64; }
+
+template <int E, int K>
+__global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
+    const float *__restrict__ qkv, const float *__restrict__ w, float *conv_state,
+    float *__restrict__ q, float *__restrict__ k, float *__restrict__ v, int n_tokens,
+    int n_k_heads, int n_v_heads, float eps, const int32_t *__restrict__ slots, int pool,
+    int32_t *err_count) {
+    constexpr int S = 32 * E, TAPS = K - 1, P = conv_norm_positions<E>(), ROW = S + 4;
+    __shared__ __align__(16) float tile[P * ROW];
+    const int sl = blockIdx.x, n = blockIdx.z, c = threadIdx.x;
+    const int t0 = blockIdx.y * P, t1 = min(n_tokens, t0 + P);
+    const int slot = slots ? slots[n] : n;
+    if (slot < 0 || slot >= pool) {  // uniform over the CTA
+        if (err_count && sl == 0 && blockIdx.y == 0 && c == 0) atomicAdd(err_count, 1);
+        return;
+    }
+    const int Hk = n_k_heads, H = n_v_heads;
+    const size_t conv_dim = static_cast<size_t>(2 * Hk + H) * S;
+    const size_t ch = static_cast<size_t>(sl) * S + c;
+    float wc[K];
+#pragma unroll
+    for (int t = 0; t < K; ++t) wc[t] = w[ch * K + t];
+    float *hs = conv_state + (static_cast<size_t>(slot) * conv_dim + ch) * TAPS;
+    const float *x_ptr = qkv + static_cast<size_t>(n) * n_tokens * conv_dim + ch;
+    float old[TAPS], hist[TAPS];
+    if (t0 == 0) {
+#pragma unroll
+        for (int t = 0; t < TAPS; ++t) old[t] = hs[t];
+    }
+#pragma unroll
+    for (int t = 0; t < TAPS; ++t) {
+        const int pos = t0 - TAPS + t;
+        hist[t] = pos >= 0 ? x_ptr[static_cast<size_t>(pos) * conv_dim] : old[t];  // t0 == 0
+    }
+    const bool is_qk = sl < 2 * Hk;
+    float *v_out = is_qk ? nullptr
+                         : v + (static_cast<size_t>(n) * n_tokens * H + (sl - 2 * Hk)) * S + c;
+    constexpr int B = 16;  // inputs loaded ahead of their use: memory-level parallelism
+    for (int pb = t0; pb < t1; pb += B) {
+        float xs[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+            xs[j] = pb + j < t1 ? x_ptr[static_cast<size_t>(pb + j) * conv_dim] : 0.0f;
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int p = pb + j;
+            if (p >= t1) break;
+            const float x = xs[j];
+            float pre = __fmul_rn(x, wc[K - 1]);
+#pragma unroll
+            for (int t = 0; t < TAPS; ++t) pre = __fmaf_rn(hist[t], wc[t], pre);
+            const float o = silu(pre);
+            if (is_qk) tile[(p - t0) * ROW + c] = o;
+            else v_out[static_cast<size_t>(p) * H * S] = o;
+#pragma unroll
+            for (int t = 0; t + 1 < TAPS; ++t) hist[t] = hist[t + 1];
+            hist[TAPS - 1] = x;
+        }
+    }
+    if (t0 == 0) {  // the new state: the last K-1 inputs of (old state, this call's inputs)
+        for (int p = max(0, n_tokens - TAPS); p < n_tokens; ++p) {
+#pragma unroll
+            for (int t = 0; t + 1 < TAPS; ++t) old[t] = old[t + 1];
+            old[TAPS - 1] = x_ptr[static_cast<size_t>(p) * conv_dim];
+        }
+#pragma unroll
+        for (int t = 0; t < TAPS; ++t) hs[t] = old[t];
+    }
+    if (!is_qk) return;  // uniform over the CTA
+    __syncthreads();
+    const int warp = c >> 5, lane = c & 31;
+    float *dst0 = (sl < Hk ? q : k) +
+                  (static_cast<size_t>(n) * n_tokens * Hk + (sl % Hk)) * S + lane * E;
+    for (int r = warp; r < t1 - t0; r += S / 32) {
+        float xv[E];
+        load_vec<E>(xv, tile + r * ROW + lane * E);
+        float ss = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) ss = __fmaf_rn(xv[e], xv[e], ss);
+        ss = warp_allsum(ss);
+        const float inv = 1.0f / fmaxf(sqrtf(ss), eps);
+#pragma unroll
+        for (int e = 0; e < E; ++e) xv[e] *= inv;
+        store_vec<E>(dst0 + static_cast<size_t>(t0 + r) * Hk * S, xv);
+    }
+}
+
+template <int E, int K>
+gdn_status launch_conv_split_norm_k(const float *qkv, const float *w, float *conv_state, float *q,
+                                    float *k, float *v, int n_seqs, int n_tokens, int Hk, int H,
+                                    float eps, const int32_t *slots, int pool, int32_t *err_count,
+                                    cudaStream_t s) {
+    constexpr int P = conv_norm_positions<E>();
+    const dim3 grid(2 * Hk + H, (n_tokens + P - 1) / P, n_seqs);
+    conv_split_norm_kernel<E, K><<<grid, 32 * E, 0, s>>>(qkv, w, conv_state, q, k, v, n_tokens,
+                                                         Hk, H, eps, slots, pool, err_count);
+    return launch_status();
+}
+
+template <int E>
+gdn_status launch_conv_split_norm(int conv_kernel, const float *qkv, const float *w,
+                                  float *conv_state, float *q, float *k, float *v, int n_seqs,
+                                  int n_tokens, int Hk, int H, float eps, const int32_t *slots,
+                                  int pool, int32_t *err_count, cudaStream_t s) {
+    switch (conv_kernel) {
+        case 2: return launch_conv_split_norm_k<E, 2>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
+        case 3: return launch_conv_split_norm_k<E, 3>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
+        case 4: return launch_conv_split_norm_k<E, 4>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
+        case 5: return launch_conv_split_norm_k<E, 5>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
+        case 6: return launch_conv_split_norm_k<E, 6>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
+        case 7: return launch_conv_split_norm_k<E, 7>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
+        default: return launch_conv_split_norm_k<E, 8>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
+    }
+}
 
 }  // namespace
 }  // namespace gdn
@@ -77,17 +201,20 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
     const long long rows = static_cast<long long>(n_seqs) * n_tokens;
     if (rows * n_v_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     const int S = state_size, H = n_v_heads, Hk = n_k_heads;
-    const int conv_dim = (2 * Hk + H) * S;
     float *ws = static_cast<float *>(workspace);
-    float *conv_out = ws + L.conv_out, *q = ws + L.q, *k = ws + L.k, *v = ws + L.v;
+    float *q = ws + L.q, *k = ws + L.k, *v = ws + L.v;
     float *g = ws + L.g, *beta = ws + L.beta;
+    if ((n_tokens + 31) / 32 > 65535 || n_seqs > 65535) return GDN_ERR_UNSUPPORTED;
 
-    // A skipped sequence is counted once, by the conv scan; nothing of it is written
+    // A skipped sequence is counted once, by the conv pass; nothing of it is written
     // to conv_state, state or out.
-    GDN_TRY(gdn_conv1d_silu_seq(qkv, conv_w, conv_state, conv_out, n_seqs, n_tokens, conv_dim,
-                                conv_kernel, slots, pool, err_count, stream));
-    GDN_TRY(gdn_qkv_split_norm(conv_out, q, k, v, static_cast<int>(rows), Hk, H, S, l2_eps,
-                               stream));
+    const cudaStream_t cs = as_cuda(stream);
+    switch (S) {
+        case 32: GDN_TRY(launch_conv_split_norm<1>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
+        case 64: GDN_TRY(launch_conv_split_norm<2>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
+        case 128: GDN_TRY(launch_conv_split_norm<4>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
+        default: GDN_TRY(launch_conv_split_norm<8>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
+    }
     GDN_TRY(gdn_decay_gate(alpha, dt, a, g, H, static_cast<int>(rows), stream));
     GDN_TRY(gdn_beta_sigmoid(b, beta, static_cast<int>(rows * H), stream));
     if (chunked) {

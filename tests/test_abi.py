@@ -144,9 +144,9 @@ def test_prefill_validation(lib):
     ws = lib.gdn_block_prefill_workspace_size
     ws.restype = ctypes.c_size_t
     need = ws(2, 16, 2, 4, 32)
-    # conv_out + q + k + v + g + beta, each rounded up to 64 floats
-    C = (2 * 2 + 4) * 32
-    parts = [2 * 16 * C, 2 * 16 * 2 * 32, 2 * 16 * 2 * 32, 2 * 16 * 4 * 32, 2 * 16 * 4, 2 * 16 * 4]
+    # q + k + v + g + beta, each rounded up to 64 floats (the conv pass feeds the
+    # split-norm on chip, so no [n][t][C] intermediate)
+    parts = [2 * 16 * 2 * 32, 2 * 16 * 2 * 32, 2 * 16 * 4 * 32, 2 * 16 * 4, 2 * 16 * 4]
     assert need == 4 * sum((p + 63) // 64 * 64 for p in parts)
     assert ws(-1, 16, 2, 4, 32) == 0
     f = lib.gdn_block_prefill
