@@ -39,7 +39,7 @@ struct PrefillLayout {
 // (lane L holds elements [E L, E L + E), one butterfly). Results are the two
 // separate kernels' bit for bit, without their [n][t][C] intermediate in HBM.
 template <int E>
-constexpr int conv_norm_positions() { return E >= 8 ? 16 : 32; }
+__host__ __device__ constexpr int conv_norm_positions() { return E >= 8 ? 16 : 32; }
 
 template <int E, int K>
 __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
