@@ -23,6 +23,7 @@ __all__ = [
     "gdn_conv1d_silu_seq_snapshots", "gdn_block_prefill_workspace_size", "gdn_block_prefill",
     "gdn_block_prefill_noalloc", "PREFILL_NOALLOC_SCRATCH_BYTES",
     "gdn_recurrence_scan_chunked", "gdn_block_prefill_chunked",
+    "gdn_recurrence_scan_chunked_ws_size", "gdn_recurrence_scan_chunked_ws",
 ]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
@@ -62,6 +63,9 @@ _SIGS = {
     "gdn_block_prefill_noalloc": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P,
                                                _P], _I),
     "gdn_recurrence_scan_chunked": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
+    "gdn_recurrence_scan_chunked_ws_size": ([_I, _I, _I, _I], ctypes.c_size_t),
+    "gdn_recurrence_scan_chunked_ws": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P,
+                                                   ctypes.c_size_t, _P], _I),
     "gdn_block_prefill_chunked": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P, _P,
                                                ctypes.c_size_t, _P], _I),
 }
@@ -130,6 +134,21 @@ def _slots(slots):
 def _errc(err_count):
     import torch
     return _ptr(err_count, "err_count", torch.int32, optional=True)
+
+
+def _ws_check(workspace):
+    import torch
+    if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+
+
+def _ws_ptr(workspace):
+    _ws_check(workspace)
+    return workspace.data_ptr()
+
+
+def _ws_bytes(workspace):
+    return workspace.numel() * workspace.element_size()
 
 
 def _pool(pool, n_seqs, slots):
@@ -223,6 +242,23 @@ def gdn_recurrence_scan_chunked(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_
         scale, _slots(slots), pool, _errc(err_count), _stream(stream)))
 
 
+def gdn_recurrence_scan_chunked_ws_size(n_seqs, n_tokens, n_v_heads, state_size):
+    return library().gdn_recurrence_scan_chunked_ws_size(n_seqs, n_tokens, n_v_heads, state_size)
+
+
+def gdn_recurrence_scan_chunked_ws(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads,
+                                   n_v_heads, state_size, scale, workspace, slots=None, pool=None,
+                                   err_count=None, stream=None):
+    """The two-phase chunked scan; `workspace` is a CUDA tensor (any dtype, contiguous)
+    whose byte size sets how many chunks each wave prepares."""
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_recurrence_scan_chunked_ws", library().gdn_recurrence_scan_chunked_ws(
+        _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
+        _ptr(beta, "beta"), _ptr(y, "y"), n_seqs, n_tokens, n_k_heads, n_v_heads, state_size,
+        scale, _slots(slots), pool, _errc(err_count), _ws_ptr(workspace),
+        _ws_bytes(workspace), _stream(stream)))
+
+
 def gdn_gated_norm(y, w, z, out, rows, head_dim, eps, stream=None):
     _check("gdn_gated_norm", library().gdn_gated_norm(
         _ptr(y, "y"), _ptr(w, "w"), _ptr(z, "z"), _ptr(out, "out"), rows, head_dim, eps,
@@ -280,9 +316,7 @@ def _block_prefill(name, qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, st
                    n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
                    norm_eps, workspace, slots, pool, err_count, stream):
     pool = _pool(pool, n_seqs, slots)
-    import torch
-    if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
-        raise ValueError("workspace must be a contiguous CUDA tensor")
+    _ws_check(workspace)
     _check(name, getattr(library(), name)(
         _ptr(qkv, "qkv"), _ptr(conv_w, "conv_w"), _ptr(conv_state, "conv_state"),
         _ptr(alpha, "alpha"), _ptr(b, "b"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(z, "z"),

@@ -29,13 +29,15 @@
 //   prep (8 warps)     per chunk, in fp32: the forward substitution and the
 //                      tensor-core operands in shared memory (each written as soon as
 //                      the previous chunk's MMAs have finished reading it);
-//   MMA (1 thread)     D_u|D_y = S^T [W | Gam Q]^T, D_y += the rest of the S part,
-//                      S^T = Gam_31 S^T + U^T (w K), D_y += U^T M^T.
+//   MMA (1 thread)     the S products D_u = S^T W^T and D_y = S^T (Gam Q)^T in two
+//                      passes (gdn_chunk_common.cuh), then S^T = Gam_31 S^T + U^T (w K)
+//                      and D_y += U^T M^T.
 //
 // Precision: a single TF32 pass (10-bit mantissa) in the products that feed the
 // state or y misses a 2e-3-of-RMS error bound after 4096 positions; the split
 // x = hi + lo with hi*hi + hi*lo + lo*hi ("3xTF32") restores fp32-level products,
 // and every product here uses it.
+#include "gdn_chunk_common.cuh"
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 #include "gdn_tc.cuh"
@@ -43,29 +45,14 @@
 namespace gdn {
 namespace {
 
+using namespace chunk;
+
 __device__ unsigned g_watchdog_chunked;
 constexpr unsigned WD_MMA = 8u;  // a hand-off between the roles of the chunked scan
 
-constexpr int kC = 32;    // positions per chunk
-constexpr int kS = 128;   // state size (dk = dv) of the tensor-core form
-constexpr uint32_t kLbo = 128;                 // K-major core matrices: next 4 elements of K
-constexpr uint32_t kSbo128 = (kS / 4) * 128;   // next 8 rows, K = 128 operands
-constexpr uint32_t kSbo32 = (kC / 4) * 128;    // next 8 rows, K = 32 operands
-
 // ---- shared memory (bytes)
-// tensor-core operands, K-major core-matrix images (see gdn_tc.cuh)
-constexpr uint32_t kOffWQ = 0;         // 64 rows x K=128: rows 0..31 hi(W), rows 32..63 hi(Gam q)
-constexpr uint32_t kOffQlo = 32768;    // 32 rows x K=128: lo(Gam q)
-constexpr uint32_t kOffWlo = 49152;    // 32 rows x K=128: lo(W)
-constexpr uint32_t kOffMhi = 65536;    // 32 rows (t) x K=32 (s): hi(M)
-constexpr uint32_t kOffMlo = 69632;    //                          lo(M)
-constexpr uint32_t kOffKhi = 73728;    // 128 rows (dk) x K=32 (c): hi(w_c k_c)
-constexpr uint32_t kOffKlo = 90112;    //                          lo(w_c k_c)
-constexpr uint32_t kOffUt = 106496;    // Ut, plain [c][dv] fp32
-// rows of 528 bytes (132 floats): row r starts on bank 4r, float4 aligned
-constexpr uint32_t kRawRow = 528;
-constexpr int kRawRowF = kRawRow / 4;
-constexpr uint32_t kRawArr = kC * kRawRow;
+// tensor-core operand images at kOffWQ .. kImgBytes (gdn_chunk_common.cuh), then
+constexpr uint32_t kOffUt = kImgBytes;  // Ut, plain [c][dv] fp32
 constexpr uint32_t kOffWs = 122880;    // W [32][132] fp32, from the substitution
 // raw rows of k and q: 2 buffers x 2 arrays x 32 rows (v is read from global memory)
 constexpr uint32_t kRawBuf = 2 * kRawArr;
@@ -79,7 +66,7 @@ constexpr uint32_t kOffBars = kOffM + 2 * kMBytes;
 struct Bars {
     uint64_t raw_full[2], raw_empty[2], gram_ready[2];
     uint64_t img_ready, s_ready, u_ready;
-    uint64_t a_done, b_done, y_done, fin;
+    uint64_t a_done, b_done, fin;
     uint32_t taddr;
     int abort;
 };
@@ -100,100 +87,16 @@ constexpr int kStateThreads = 32 * kStateWarps;
 // slots to the warps doing arithmetic.
 constexpr int kPrepBarrier = 1, kStateBarrier = 2;
 
-// ---- tensor memory (columns; lane = dv)
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColSacc = 0, kColShi = 128, kColSlo = 256, kColUhi = 384, kColUlo = 416,
-                   kColDu = 448, kColDy = 480;  // D_u and D_y adjacent: one N = 64 MMA fills both
-static_assert(kColDy + kC == kTmemCols, "tensor-memory plan fills the allocation");
-
-
-__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-
-__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
-
-// Named barrier over `count` threads that also ORs `pred` over them: every thread
-// gets the same answer, so a role whose warps must stay in step can leave its
-// loop together.
-__device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
-
-// Cumulative log-decay of a chunk from g_lane (lane = position, 0 past the end of
-// the sequence): returns gam_lane and sets `last` = gam_31. Every warp that needs
-// these runs this same code on the same inputs, so all get the same bits.
-__device__ __forceinline__ float chunk_gam_from(float c, int lane, float &last) {
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(FULL_MASK, c, off);
-        if (lane >= off) c += o;
-    }
-    last = __shfl_sync(FULL_MASK, c, 31);
-    return c;
-}
-
-__device__ __forceinline__ void split4(float4 x, float4 &hi, float4 &lo) {
-    tc::split_tf32(x.x, hi.x, lo.x);
-    tc::split_tf32(x.y, hi.y, lo.y);
-    tc::split_tf32(x.z, hi.z, lo.z);
-    tc::split_tf32(x.w, hi.w, lo.w);
-}
-
-// Partial Gram products of row t against columns s0 + 8 j, j < JN, over all of dk:
-// kk[j] = k_t . k_s, qk[j] = q_t . k_s. JN is a compile-time count so every load
-// of a step is issued before its FMAs.
-template <int JN>
-__device__ __forceinline__ void gram_row(const float *rk, const float *rq, int t, int s0,
-                                         float (&kk)[4], float (&qk)[4]) {
-#pragma unroll 2
-    for (int i = 0; i < kS; i += 4) {
-        const float4 kt = ld4(rk + t * kRawRowF + i), qt = ld4(rq + t * kRawRowF + i);
-        float4 ks[JN];
-#pragma unroll
-        for (int j = 0; j < JN; ++j) ks[j] = ld4(rk + (s0 + 8 * j) * kRawRowF + i);
-#pragma unroll
-        for (int j = 0; j < JN; ++j) {
-            kk[j] = fmaf(kt.x, ks[j].x, kk[j]);
-            kk[j] = fmaf(kt.y, ks[j].y, kk[j]);
-            kk[j] = fmaf(kt.z, ks[j].z, kk[j]);
-            kk[j] = fmaf(kt.w, ks[j].w, kk[j]);
-            qk[j] = fmaf(qt.x, ks[j].x, qk[j]);
-            qk[j] = fmaf(qt.y, ks[j].y, qk[j]);
-            qk[j] = fmaf(qt.z, ks[j].z, qk[j]);
-            qk[j] = fmaf(qt.w, ks[j].w, qk[j]);
-        }
-    }
-}
-
-// The Gram stage of a chunk, by the 256 threads of one role (warp gw = 0..7):
+// The Gram stage of a chunk, by the 256 threads of one role (warp gw = 0..7), on the
+// thread mapping of gram_products:
 //   At[s][t] = beta_t exp(gam_t - gam_s) (k_t . k_s)   (s < t, else 0)
 //   M[t][s]  = exp(gam_t - gam_s) (q_t . k_s)          (s <= t, else 0)
-// gam and bet hold the chunk's gam_lane and beta_lane. Row t = 4 rb + lane / 8 against
-// columns s = lane % 8 + 8 j (lower triangle only); warps gw and gw + 4 share an SM
-// sub-partition, so a short row block is paired with a long one (0+7, 2+5, 1+6, 3+4).
+// gam and bet hold the chunk's gam_lane and beta_lane.
 __device__ __forceinline__ void chunk_gram(const float *rk, const float *rq, float *At, float *Msc,
                                            float gam, float bet, int gw, int lane) {
-    const int pb = gw & 3, rb0 = ((pb & 1) << 1) | (pb >> 1);
-    const int rb = gw < 4 ? rb0 : 7 - rb0;
-    const int t = 4 * rb + (lane >> 3), s0 = lane & 7;
-    const int jmax = (4 * rb + 3) >> 3;  // last block j with 8 j <= the warp's max t
-    float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
-    switch (jmax) {  // warp-uniform
-        case 0: gram_row<1>(rk, rq, t, s0, kk, qk); break;
-        case 1: gram_row<2>(rk, rq, t, s0, kk, qk); break;
-        case 2: gram_row<3>(rk, rq, t, s0, kk, qk); break;
-        default: gram_row<4>(rk, rq, t, s0, kk, qk); break;
-    }
+    int t, s0;
+    float kk[4], qk[4];
+    gram_products(rk, rq, gw, lane, t, s0, kk, qk);
     const float gam_t = __shfl_sync(FULL_MASK, gam, t);
     const float bet_t = __shfl_sync(FULL_MASK, bet, t);
 #pragma unroll
@@ -236,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
         mbar_init(&bars.u_ready, 1);
         mbar_init(&bars.a_done, 1);
         mbar_init(&bars.b_done, 1);
-        mbar_init(&bars.y_done, 1);
         mbar_init(&bars.fin, 1);
         bars.abort = 0;
         fence_mbar_init();
@@ -301,51 +203,32 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t id64 = tc::idesc_tf32(128, 2 * kC), id32 = tc::idesc_tf32(128, kC),
-                           id128 = tc::idesc_tf32(128, kS);
+            const uint32_t id64 = tc::idesc_tf32(128, 2 * kC), id128 = tc::idesc_tf32(128, kS),
+                           id160 = tc::idesc_tf32(128, kS + kC);
             auto desc = [&](uint32_t off, uint32_t sbo) { return tc::smem_desc(smem + off, kLbo, sbo); };
             for (int ci = 0; ci < n_chunks; ++ci) {
                 if (!wait1(&bars.img_ready, ci, WD_MMA)) break;
                 if (!wait1(&bars.s_ready, ci, WD_MMA)) break;
                 tc::fence_after_sync();
-                // [D_u | D_y] = hi(S)^T [hi(W) | hi(Gam Q)]^T: the first pass of W S and
-                // of the S part of y together (N = 64), then the other two of W S
+                // the S products: hi(S) against all 128 image rows (N = 128), then lo(S)
+                // against hi(Gam q) and hi(W) (N = 64) into the first two blocks of D
                 for (int ks = 0; ks < kS / 8; ++ks)
-                    tc::mma_tf32_ts(tmem + kColDu, tmem + kColShi + 8 * ks,
-                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id64, ks > 0);
+                    tc::mma_tf32_ts(tmem + kColD, tmem + kColShi + 8 * ks,
+                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id128, ks > 0);
                 for (int ks = 0; ks < kS / 8; ++ks)
-                    tc::mma_tf32_ts(tmem + kColDu, tmem + kColShi + 8 * ks,
-                                    desc(kOffWlo + ks * 2 * kLbo, kSbo128), id32, true);
-                for (int ks = 0; ks < kS / 8; ++ks)
-                    tc::mma_tf32_ts(tmem + kColDu, tmem + kColSlo + 8 * ks,
-                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id32, true);
+                    tc::mma_tf32_ts(tmem + kColD, tmem + kColSlo + 8 * ks,
+                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id64, true);
                 tc::mma_commit(&bars.a_done);
-                // D_y += hi(S)^T lo(Gam Q)^T + lo(S)^T hi(Gam Q)^T
-                for (int ks = 0; ks < kS / 8; ++ks)
-                    tc::mma_tf32_ts(tmem + kColDy, tmem + kColShi + 8 * ks,
-                                    desc(kOffQlo + ks * 2 * kLbo, kSbo128), id32, true);
-                for (int ks = 0; ks < kS / 8; ++ks)
-                    tc::mma_tf32_ts(tmem + kColDy, tmem + kColSlo + 8 * ks,
-                                    desc(kOffWQ + 4 * kSbo128 + ks * 2 * kLbo, kSbo128), id32,
-                                    true);
                 if (!wait1(&bars.u_ready, ci, WD_MMA)) break;
                 tc::fence_after_sync();
-                // S^T += U^T (w K): hi hi + hi lo + lo hi, accumulated in place
+                // [S^T | D_y] += U^T [w K | M]^T: hi hi + hi lo + lo hi
                 for (int p = 0; p < 3; ++p) {
                     const uint32_t a = p == 2 ? kColUlo : kColUhi, bo = p == 1 ? kOffKlo : kOffKhi;
                     for (int ks = 0; ks < kC / 8; ++ks)
                         tc::mma_tf32_ts(tmem + kColSacc, tmem + a + 8 * ks,
-                                        desc(bo + ks * 2 * kLbo, kSbo32), id128, true);
+                                        desc(bo + ks * 2 * kLbo, kSbo32), id160, true);
                 }
                 tc::mma_commit(&bars.b_done);
-                // D_y += U^T M^T
-                for (int p = 0; p < 3; ++p) {
-                    const uint32_t a = p == 2 ? kColUlo : kColUhi, bo = p == 1 ? kOffMlo : kOffMhi;
-                    for (int ks = 0; ks < kC / 8; ++ks)
-                        tc::mma_tf32_ts(tmem + kColDy, tmem + a + 8 * ks,
-                                        desc(bo + ks * 2 * kLbo, kSbo32), id32, true);
-                }
-                tc::mma_commit(&bars.y_done);
             }
             tc::mma_commit(&bars.fin);  // tensor memory stays allocated until all MMAs end
             mbar_wait_sleep(&bars.fin, 0, 128);
@@ -373,18 +256,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
         };
 
         // y of chunk cj from D_y; false if the wait gave up
-        auto store_y = [&](int cj) {
-            if (!st_wait(&bars.y_done, cj)) return false;
-            tc::fence_after_sync();
-            uint32_t dy[16];
-            tc::tmem_ld16_nowait(trow + kColDy + u0, dy);
+        // y of chunk cj: read from D_y once its b_done has been waited for (before the
+        // next chunk's MMAs overwrite it), then written out (after those MMAs are under
+        // way)
+        auto read_y = [&](float (&yv)[16]) {
+            uint32_t dy[16], dy2[16];
+            tc::tmem_ld16_nowait(trow + kColDyA + u0, dy);
+            tc::tmem_ld16_nowait(trow + kColDyB + u0, dy2);
             tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) yv[e] = scale * (u2f(dy[e]) + u2f(dy2[e]));
+        };
+        auto write_y = [&](int cj, const float (&yv)[16]) {
             const int t0 = cj * kC, valid = min(kC, n_tokens - t0);
             float *yp = y + ((row0 + t0) * H + vh) * kS + dv;
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-                if (u0 + e < valid) yp[static_cast<size_t>(u0 + e) * H * kS] = scale * u2f(dy[e]);
-            return true;
+                if (u0 + e < valid) yp[static_cast<size_t>(u0 + e) * H * kS] = yv[e];
         };
 
         // The Gram stage of chunk cj (its decay inputs gj, bj, lane = position), in the
@@ -454,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
                 for (int e = 0; e < 16; ++e) {
                     const float x = u2f(r[e]);
                     float h, l;
-                    tc::split_tf32(x, h, l);
+                    split_hl(x, h, l);
                     hi[e] = f2u(h);
                     lo[e] = f2u(l);
                     r[e] = f2u(gn * x);
@@ -465,8 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             }
             tc::tmem_st_wait();
             // the previous chunk's y leaves D_y before this chunk's MMAs overwrite it
-            if (ci > 0 && !(ok = store_y(ci - 1))) break;
+            float yv[16];
+            if (ci > 0) read_y(yv);
             st_signal(&bars.s_ready);
+            if (ci > 0) write_y(ci - 1, yv);
             // the next chunk's Gram stage, while the prep warps finish this chunk
             if (ci + 1 < n_chunks && !(ok = gram_chunk(ci + 1, g_nx, b_nx))) break;
             g_cur = g_nx;
@@ -478,14 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             if (!(ok = st_wait(&bars.a_done, ci))) break;
             tc::fence_after_sync();
             {
-                uint32_t du[16], hi[16], lo[16];
-                tc::tmem_ld16_nowait(trow + kColDu + u0, du);
+                uint32_t du[16], du2[16], hi[16], lo[16];
+                tc::tmem_ld16_nowait(trow + kColDuA + u0, du);
+                tc::tmem_ld16_nowait(trow + kColDuB + u0, du2);
                 tc::tmem_ld_wait();
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float u = ut[(u0 + e) * kS + dv] - u2f(du[e]);
+                    const float u = ut[(u0 + e) * kS + dv] - (u2f(du[e]) + u2f(du2[e]));
                     float h, l;
-                    tc::split_tf32(u, h, l);
+                    split_hl(u, h, l);
                     hi[e] = f2u(h);
                     lo[e] = f2u(l);
                 }
@@ -495,9 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             }
             st_signal(&bars.u_ready);
         }
-        if (ok && n_chunks > 0) ok = store_y(n_chunks - 1);
         if (ok && n_chunks > 0 && (ok = st_wait(&bars.b_done, n_chunks - 1))) {
             tc::fence_after_sync();
+            float yv[16];
+            read_y(yv);
+            write_y(n_chunks - 1, yv);
 #pragma unroll 1
             for (int blk = 0; blk < 4; ++blk) {
                 uint32_t r[16];
@@ -598,11 +491,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
                 const int c = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
                 float4 hi, lo;
                 split4(ld4(ws + c * kRawRowF + k0), hi, lo);
-                *reinterpret_cast<float4 *>(smem + kOffWQ + o) = hi;  // rows 0..31
+                *reinterpret_cast<float4 *>(smem + kOffWhi + o) = hi;
                 *reinterpret_cast<float4 *>(smem + kOffWlo + o) = lo;
             }
 
-            // ---- w_c k_c, split, once the previous chunk's state update is done
+            // Gam_t q_t, split (the S products that read it finished before U was formed)
+            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {
+                const uint32_t o = idx * 16u;
+                const int t = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
+                const float Gt = __shfl_sync(FULL_MASK, Gam, t);
+                float4 xv = ld4(rq + t * kRawRowF + k0);
+                xv.x *= Gt; xv.y *= Gt; xv.z *= Gt; xv.w *= Gt;
+                float4 hi, lo;
+                split4(xv, hi, lo);
+                *reinterpret_cast<float4 *>(smem + kOffQhi + o) = hi;
+                *reinterpret_cast<float4 *>(smem + kOffQlo + o) = lo;
+            }
+            // ---- w_c k_c and M, split, once the previous chunk's state update is done
             if (ci > 0 ? prep_wait(&bars.b_done, ci - 1, WD_MMA) : prep_sync()) break;
             for (int idx = pt; idx < kS * kC / 4; idx += kPrepThreads) {
                 const uint32_t o = idx * 16u;
@@ -618,19 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
                 *reinterpret_cast<float4 *>(smem + kOffKlo + o) = lo;
             }
 
-            // ---- Gam_t q_t and M, split, once the previous chunk's y products are done
-            if (ci > 0 ? prep_wait(&bars.y_done, ci - 1, WD_MMA) : prep_sync()) break;
-            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {
-                const uint32_t o = idx * 16u;
-                const int t = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
-                const float Gt = __shfl_sync(FULL_MASK, Gam, t);
-                float4 xv = ld4(rq + t * kRawRowF + k0);
-                xv.x *= Gt; xv.y *= Gt; xv.z *= Gt; xv.w *= Gt;
-                float4 hi, lo;
-                split4(xv, hi, lo);
-                *reinterpret_cast<float4 *>(smem + kOffWQ + 4 * kSbo128 + o) = hi;  // rows 32..63
-                *reinterpret_cast<float4 *>(smem + kOffQlo + o) = lo;
-            }
+            // M, split (read by the same MMAs as w K)
             for (int idx = pt; idx < kC * kC / 4; idx += kPrepThreads) {
                 const uint32_t o = idx * 16u;
                 const int t = (o / kSbo32) * 8 + (o % 128) / 16, s0 = ((o % kSbo32) / 128) * 4;

@@ -1,0 +1,617 @@
+// gdn_chunked_ws.cu -- the chunked scan in two phases, with a caller workspace.
+//
+// The algebra is the one of gdn_chunked.cu (the WY/UT regrouping of the delta-rule
+// recurrence in chunks of 32 positions; fm_kernel_ssm.m, sequential-scan section,
+// names the chunked prefill path and keeps the sequential scan as its reference).
+// There, one CTA per (sequence, v-head) does everything for its chunks one after
+// the other, and the per-chunk CUDA-core work that does not depend on the state
+// (the Gram products and the forward substitution) sets the pace. Here that work
+// moves into its own fully parallel kernel:
+//
+//   chunk_prepare_kernel   one CTA per (chunk, sequence, k-head): the Gram products
+//                          of the chunk's k and q rows (shared by the k-head's GQA
+//                          v-heads), then per v-head the decay prefix, A and M, and
+//                          the forward substitutions (I + A) W = diag(beta Gam) K,
+//                          (I + A) Ut = diag(beta) V; W, Ut and M go to the workspace.
+//   chunk_state_kernel     one CTA per (sequence, v-head), sequential over chunks:
+//                          only the state-dependent part, U = Ut - W S, y and the
+//                          state update, on the tensor cores (3xTF32), with W, Ut and M
+//                          read back from the workspace.
+//
+// Both kernels run the arithmetic of gdn_chunked.cu in the same order, so the two
+// forms give the same bits. A workspace that holds fewer chunks than the sequence
+// has is used in waves (prepare a wave of chunks, advance the state over it, ...);
+// the state goes through its fp32 home between waves, which changes no bits either.
+#include "gdn_chunk_common.cuh"
+#include "gdn_device.cuh"
+#include "gdn_internal.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace chunk;
+
+__device__ unsigned g_watchdog_chunked_ws;
+constexpr unsigned WD_MMA = 8u;  // a hand-off between the roles of the state kernel
+
+// Workspace block of one (chunk, sequence, v-head), fp32: W [32][128] (rows = positions,
+// columns = dk), Ut [32][128] (columns = dv), M [32][32]; chunk-major over a wave.
+constexpr int kBlkW = 0, kBlkUt = kC * kS, kBlkM = 2 * kC * kS;
+constexpr int kBlkFloats = 2 * kC * kS + kC * kC;
+constexpr size_t kBlkBytes = static_cast<size_t>(kBlkFloats) * sizeof(float);
+
+__device__ __forceinline__ size_t blk_index(int cw, int n, int vh, int n_seqs, int H) {
+    return (static_cast<size_t>(cw) * n_seqs + n) * H + vh;
+}
+
+// ============================================================================ phase 1
+constexpr int kPThreads = 256;
+constexpr int kAtRow = kC + 4;  // A^T rows: 36 floats, float4 aligned
+constexpr uint32_t kAtBytes = kC * kAtRow * 4;
+constexpr uint32_t kPOffK = 0, kPOffQ = kRawArr, kPOffAt = 2 * kRawArr;
+constexpr size_t kPSmemBytes = 2 * kRawArr + 2 * kAtBytes;  // 43,008 B
+
+// grid = n_wave_chunks * n_seqs * n_k_heads; CTA (cw, n, kh) prepares chunk c_begin + cw of
+// sequence n for the v-heads rr * Hk + kh.
+__global__ void __launch_bounds__(kPThreads, 4) chunk_prepare_kernel(
+    const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
+    const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ ws,
+    int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int c_begin, int n_wave_chunks) {
+    __shared__ __align__(16) unsigned char smem[kPSmemBytes];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = n_v_heads, Hk = n_k_heads;
+    const int cw = blockIdx.x % n_wave_chunks;
+    const int rest = blockIdx.x / n_wave_chunks;
+    const int kh = rest % Hk, n = rest / Hk;
+    const int t0 = (c_begin + cw) * kC, valid = min(kC, n_tokens - t0);
+    const size_t row0 = static_cast<size_t>(n) * n_tokens + t0;  // (n, t0) in [N][T] order
+    float *rk = reinterpret_cast<float *>(smem + kPOffK);
+    float *rq = reinterpret_cast<float *>(smem + kPOffQ);
+
+    // k and q rows of the chunk, zero past the end of the sequence
+    for (int i = tid; i < 2 * kC * (kS / 4); i += kPThreads) {
+        const int arr = i / (kC * kS / 4), rem = i % (kC * kS / 4);
+        const int t = rem / (kS / 4), c4 = rem % (kS / 4);
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < valid) x = ld4((arr ? q : k) + ((row0 + t) * Hk + kh) * kS + 4 * c4);
+        *reinterpret_cast<float4 *>((arr ? rq : rk) + t * kRawRowF + 4 * c4) = x;
+    }
+    __syncthreads();
+    int t, s0;
+    float kk[4], qk[4];
+    gram_products(rk, rq, warp, lane, t, s0, kk, qk);
+
+    const int ratio = H / Hk;
+    const int col = tid & (kS - 1);
+    const bool is_w = tid < kS;
+    for (int rr = 0; rr < ratio; ++rr) {
+        const int vh = rr * Hk + kh;
+        float *blk = ws + blk_index(cw, n, vh, n_seqs, H) * kBlkFloats;
+        float *At = reinterpret_cast<float *>(smem + kPOffAt + (rr & 1) * kAtBytes);
+        float gl = 0.f, bl = 0.f;  // lane = position
+        if (lane < valid) {
+            gl = g[(row0 + lane) * H + vh];
+            bl = beta[(row0 + lane) * H + vh];
+        }
+        // v of the Ut columns, fetched now so the loads overlap the A stage
+        float x[kC];
+        if (!is_w) {
+            const float *vp = v + (row0 * H + vh) * kS + col;
+            const size_t vstride = static_cast<size_t>(H) * kS;
+#pragma unroll
+            for (int p = 0; p < kC; ++p) {
+                x[p] = p < valid ? *vp : 0.f;
+                vp += vstride;
+            }
+        }
+        float last;
+        const float gam = chunk_gam_from(gl, lane, last);
+        const float Gam = expf(gam);
+        {
+            // A^T[s][t] = beta_t exp(gam_t - gam_s) (k_t . k_s) (s < t); M[t][s] likewise
+            // with q_t (s <= t); the same expressions as the one-kernel form
+            const float gam_t = __shfl_sync(FULL_MASK, gam, t);
+            const float bet_t = __shfl_sync(FULL_MASK, bl, t);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int s = s0 + 8 * j;
+                const float gam_s = __shfl_sync(FULL_MASK, gam, s);
+                const float e = s <= t ? expf(gam_t - gam_s) : 0.f;
+                At[s * kAtRow + t] = s < t ? bet_t * (e * kk[j]) : 0.f;
+                blk[kBlkM + t * kC + s] = e * qk[j];
+            }
+        }
+        __syncthreads();  // A^T of this v-head is complete (the other buffer is free)
+
+        // forward substitution, one column per thread: W (threads 0..127), Ut (128..255),
+        // column-wise (x_s is final once the rows above are, then updates every row below)
+#pragma unroll
+        for (int p = 0; p < kC; ++p) {
+            const float bt = __shfl_sync(FULL_MASK, bl, p);
+            const float Gt = __shfl_sync(FULL_MASK, Gam, p);
+            x[p] = is_w ? bt * Gt * rk[p * kRawRowF + col] : bt * x[p];
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < kC - 1; ++s2) {
+#pragma unroll
+            for (int m = (s2 + 1) / 4; m < kC / 4; ++m) {
+                const float4 a = ld4(At + s2 * kAtRow + 4 * m);
+                if (4 * m + 0 > s2) x[4 * m + 0] = fmaf(-a.x, x[s2], x[4 * m + 0]);
+                if (4 * m + 1 > s2) x[4 * m + 1] = fmaf(-a.y, x[s2], x[4 * m + 1]);
+                if (4 * m + 2 > s2) x[4 * m + 2] = fmaf(-a.z, x[s2], x[4 * m + 2]);
+                if (4 * m + 3 > s2) x[4 * m + 3] = fmaf(-a.w, x[s2], x[4 * m + 3]);
+            }
+        }
+        float *outp = blk + (is_w ? kBlkW : kBlkUt) + col;
+#pragma unroll
+        for (int p = 0; p < kC; ++p) outp[p * kS] = x[p];
+    }
+}
+
+// ============================================================================ phase 2
+// shared memory (bytes): the operand images, then the raw k and q rows of 2 chunks
+// The w K | M image (both parts) is double-buffered: the prep warps build chunk ci's
+// while the state update of chunk ci - 1 still reads the other buffer.
+constexpr uint32_t kKMBytes = kImgBytes - kOffKhi;  // 40 KB: one w K | M image, hi and lo
+constexpr uint32_t kOffKM1 = kImgBytes;             // second buffer (offset kKMBytes on)
+constexpr uint32_t kRawBuf = 2 * kRawArr;
+constexpr uint32_t kOffRaw = kOffKM1 + kKMBytes;
+constexpr uint32_t kOffBars = kOffRaw + 2 * kRawBuf;
+static_assert(kOffKM1 == kOffKhi + kKMBytes, "second w K | M buffer follows the first");
+
+struct Bars {
+    uint64_t raw_full[2], raw_empty[2], km_free[2];
+    uint64_t img_ready, s_ready, u_ready;
+    uint64_t a_done, b_done, fin;
+    uint32_t taddr;
+    int abort;
+};
+constexpr size_t kSmemBytes = kOffBars + sizeof(Bars);
+static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
+static_assert(kOffBars % 8 == 0, "mbarrier alignment");
+
+constexpr int kProducerWarp = 0, kMmaWarp = 1;
+constexpr int kStateWarp0 = 2, kStateWarps = 8;
+constexpr int kPrepWarp0 = kStateWarp0 + kStateWarps, kPrepWarps = 8;
+constexpr int kThreads = 32 * (kPrepWarp0 + kPrepWarps);  // 576
+constexpr int kPrepThreads = 32 * kPrepWarps;
+constexpr int kStateThreads = 32 * kStateWarps;
+constexpr int kPrepBarrier = 1, kStateBarrier = 2;
+
+// One CTA per (sequence, v-head); grid = n_seqs * n_v_heads. Advances the state over
+// chunks c_begin .. c_begin + n_wave_chunks - 1, whose workspace blocks are prepared.
+// Roles as in the one-kernel form: producer (k, q rows), MMA issuer, state warps (the
+// split of S, U = Ut - D_u, y, no Gram stage), prep warps (operand images only).
+__global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
+    float *__restrict__ state, const float *__restrict__ q, const float *__restrict__ k,
+    const float *__restrict__ g, const float *__restrict__ ws, float *__restrict__ y,
+    int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int c_begin, int n_wave_chunks,
+    float scale, const int32_t *__restrict__ slots, int pool, int32_t *err_count) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBars);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = n_v_heads, Hk = n_k_heads;
+    const int vh = blockIdx.x % H, n = blockIdx.x / H, kh = vh % Hk;
+    const int slot = slots ? slots[n] : n;
+    if (slot < 0 || slot >= pool) {  // uniform over the CTA, before any barrier
+        if (vh == 0 && tid == 0 && err_count) atomicAdd(err_count, 1);
+        return;
+    }
+    const int nw = n_wave_chunks;
+    const size_t row0 = static_cast<size_t>(n) * n_tokens;  // (n, t = 0) in [N][T] order
+    auto chunk_t0 = [&](int ci) { return (c_begin + ci) * kC; };
+    auto blk_of = [&](int ci) { return ws + blk_index(ci, n, vh, n_seqs, H) * kBlkFloats; };
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.raw_full[i], 1);
+            mbar_init(&bars.raw_empty[i], 1);
+            mbar_init(&bars.km_free[i], 1);
+        }
+        mbar_init(&bars.img_ready, 1);
+        mbar_init(&bars.s_ready, 1);
+        mbar_init(&bars.u_ready, 1);
+        mbar_init(&bars.a_done, 1);
+        mbar_init(&bars.b_done, 1);
+        mbar_init(&bars.fin, 1);
+        bars.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tc::tmem_alloc(&bars.taddr, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = bars.taddr;
+    volatile int *abort_flag = &bars.abort;
+
+    // Bounded waits, as in the one-kernel form: a wait that gives up raises the
+    // watchdog flag and sets `abort`; every role leaves its loop and all threads meet
+    // at the final barrier.
+    auto wait1 = [&](uint64_t *bar, int parity, unsigned bit) {
+        if (*abort_flag) return false;
+        if (mbar_wait_sleep(bar, parity & 1, 128)) return true;
+        atomicOr(&g_watchdog_chunked_ws, bit);
+        *abort_flag = 1;
+        return false;
+    };
+    auto waitw = [&](uint64_t *bar, int parity, unsigned bit) {
+        int ok = 0;
+        if (lane == 0) ok = wait1(bar, parity, bit);
+        return __shfl_sync(FULL_MASK, ok, 0) != 0;
+    };
+    auto group_wait = [&](bool leader, int barrier_id, int threads, uint64_t *bar, int parity,
+                          unsigned bit) {
+        bool failed = false;
+        if (leader) failed = !wait1(bar, parity, bit);
+        return !named_barrier_or(barrier_id, threads, failed || *abort_flag);
+    };
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        int issued = 0;
+        for (int ci = 0; ci < nw; ++ci) {
+            const int b = ci & 1, use = ci >> 1;
+            if (use > 0 && !waitw(&bars.raw_empty[b], use - 1, WD_STAGE_FREE)) break;
+            const int t0 = chunk_t0(ci), valid = min(kC, n_tokens - t0);
+            unsigned char *raw = smem + kOffRaw + b * kRawBuf;
+            if (lane == 0) mbar_arrive_expect_tx(&bars.raw_full[b], 2u * valid * kS * 4);
+            __syncwarp();
+            if (lane < valid) {
+                const size_t row = row0 + t0 + lane;
+                bulk_g2s(raw + lane * kRawRow, k + (row * Hk + kh) * kS, kS * 4, &bars.raw_full[b]);
+                bulk_g2s(raw + kRawArr + lane * kRawRow, q + (row * Hk + kh) * kS, kS * 4,
+                         &bars.raw_full[b]);
+            }
+            issued = ci + 1;
+        }
+        for (int ci = max(0, issued - 2); ci < issued; ++ci)
+            mbar_wait_sleep(&bars.raw_full[ci & 1], (ci >> 1) & 1, 128);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id64 = tc::idesc_tf32(128, 2 * kC), id128 = tc::idesc_tf32(128, kS),
+                           id160 = tc::idesc_tf32(128, kS + kC);
+            auto desc = [&](uint32_t off, uint32_t sbo) { return tc::smem_desc(smem + off, kLbo, sbo); };
+            for (int ci = 0; ci < nw; ++ci) {
+                if (!wait1(&bars.img_ready, ci, WD_MMA)) break;
+                if (!wait1(&bars.s_ready, ci, WD_MMA)) break;
+                tc::fence_after_sync();
+                // the S products: hi(S) against all 128 image rows (N = 128), then lo(S)
+                // against hi(Gam q) and hi(W) (N = 64) into the first two blocks of D
+                for (int ks = 0; ks < kS / 8; ++ks)
+                    tc::mma_tf32_ts(tmem + kColD, tmem + kColShi + 8 * ks,
+                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id128, ks > 0);
+                for (int ks = 0; ks < kS / 8; ++ks)
+                    tc::mma_tf32_ts(tmem + kColD, tmem + kColSlo + 8 * ks,
+                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id64, true);
+                tc::mma_commit(&bars.a_done);
+                if (!wait1(&bars.u_ready, ci, WD_MMA)) break;
+                tc::fence_after_sync();
+                // [S^T | D_y] += U^T [w K | M]^T: hi hi + hi lo + lo hi, from buffer ci & 1
+                const uint32_t km = (ci & 1) * kKMBytes;
+                for (int p = 0; p < 3; ++p) {
+                    const uint32_t a = p == 2 ? kColUlo : kColUhi,
+                                   bo = (p == 1 ? kOffKlo : kOffKhi) + km;
+                    for (int ks = 0; ks < kC / 8; ++ks)
+                        tc::mma_tf32_ts(tmem + kColSacc, tmem + a + 8 * ks,
+                                        desc(bo + ks * 2 * kLbo, kSbo32), id160, true);
+                }
+                tc::mma_commit(&bars.b_done);
+                tc::mma_commit(&bars.km_free[ci & 1]);
+            }
+            tc::mma_commit(&bars.fin);  // tensor memory stays allocated until all MMAs end
+            mbar_wait_sleep(&bars.fin, 0, 128);
+        }
+    } else if (warp < kPrepWarp0) {
+        // ------------------------------------------------------------ state warps
+        const int quarter = warp & 3, half = (warp - kStateWarp0) >> 2;
+        const int dv = quarter * 32 + lane;
+        const int c0 = half * 64, u0 = half * 16;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        float *srow = state + ((static_cast<size_t>(slot) * H + vh) * kS + dv) * kS;
+        const bool leader = warp == kStateWarp0 && lane == 0;
+        auto st_wait = [&](uint64_t *bar, int parity, unsigned bit = WD_MMA) {
+            return group_wait(leader, kStateBarrier, kStateThreads, bar, parity, bit);
+        };
+        auto st_signal = [&](uint64_t *bar) {
+            tc::fence_before_sync();
+            named_barrier_sync(kStateBarrier, kStateThreads);
+            if (leader) mbar_arrive(bar);
+        };
+        // y of chunk cj: read from D_y once its b_done has been waited for (before the
+        // next chunk's MMAs overwrite it), then written out (after those MMAs are under
+        // way)
+        auto read_y = [&](float (&yv)[16]) {
+            uint32_t dy[16], dy2[16];
+            tc::tmem_ld16_nowait(trow + kColDyA + u0, dy);
+            tc::tmem_ld16_nowait(trow + kColDyB + u0, dy2);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) yv[e] = scale * (u2f(dy[e]) + u2f(dy2[e]));
+        };
+        auto write_y = [&](int cj, const float (&yv)[16]) {
+            const int t0 = chunk_t0(cj), valid = min(kC, n_tokens - t0);
+            float *yp = y + ((row0 + t0) * H + vh) * kS + dv;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (u0 + e < valid) yp[static_cast<size_t>(u0 + e) * H * kS] = yv[e];
+        };
+
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+            uint32_t r[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 x = ld4(srow + c0 + 16 * blk + e);
+                r[e] = f2u(x.x); r[e + 1] = f2u(x.y); r[e + 2] = f2u(x.z); r[e + 3] = f2u(x.w);
+            }
+            tc::tmem_st16(trow + kColSacc + c0 + 16 * blk, r);
+        }
+        tc::tmem_st_wait();
+        float g_cur = 0.f;  // log-decays of chunk ci, lane = position
+        if (chunk_t0(0) + lane < n_tokens) g_cur = g[(row0 + chunk_t0(0) + lane) * H + vh];
+        bool ok = true;
+        for (int ci = 0; ci < nw && ok; ++ci) {
+            // this chunk's Ut (dv = this thread's lane of tensor memory, positions u0..)
+            float utv[16];
+            {
+                const float *up = blk_of(ci) + kBlkUt + u0 * kS + dv;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) utv[e] = up[e * kS];
+            }
+            float last;
+            (void)chunk_gam_from(g_cur, lane, last);
+            const float gn = expf(last);
+            float g_nx = 0.f;
+            if (ci + 1 < nw && chunk_t0(ci + 1) + lane < n_tokens)
+                g_nx = g[(row0 + chunk_t0(ci + 1) + lane) * H + vh];
+            if (ci > 0) {
+                if (!(ok = st_wait(&bars.b_done, ci - 1))) break;
+                tc::fence_after_sync();
+            }
+            // S -> (hi, lo), the A operand of the S products; the accumulator becomes
+            // Gam_31 S, ready for this chunk's update
+#pragma unroll 1
+            for (int blk = 0; blk < 4; ++blk) {
+                const uint32_t col = c0 + 16 * blk;
+                uint32_t r[16], hi[16], lo[16];
+                tc::tmem_ld16_nowait(trow + kColSacc + col, r);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float x = u2f(r[e]);
+                    float h, l;
+                    split_hl(x, h, l);
+                    hi[e] = f2u(h);
+                    lo[e] = f2u(l);
+                    r[e] = f2u(gn * x);
+                }
+                tc::tmem_st16(trow + kColShi + col, hi);
+                tc::tmem_st16(trow + kColSlo + col, lo);
+                tc::tmem_st16(trow + kColSacc + col, r);
+            }
+            tc::tmem_st_wait();
+            float yv[16];
+            if (ci > 0) read_y(yv);
+            st_signal(&bars.s_ready);
+            if (ci > 0) write_y(ci - 1, yv);
+            g_cur = g_nx;
+
+            // U^T = Ut^T - D_u, split
+            if (!(ok = st_wait(&bars.a_done, ci))) break;
+            tc::fence_after_sync();
+            {
+                uint32_t du[16], du2[16], hi[16], lo[16];
+                tc::tmem_ld16_nowait(trow + kColDuA + u0, du);
+                tc::tmem_ld16_nowait(trow + kColDuB + u0, du2);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float u = utv[e] - (u2f(du[e]) + u2f(du2[e]));
+                    float h, l;
+                    split_hl(u, h, l);
+                    hi[e] = f2u(h);
+                    lo[e] = f2u(l);
+                }
+                tc::tmem_st16(trow + kColUhi + u0, hi);
+                tc::tmem_st16(trow + kColUlo + u0, lo);
+                tc::tmem_st_wait();
+            }
+            st_signal(&bars.u_ready);
+        }
+        if (ok && nw > 0 && (ok = st_wait(&bars.b_done, nw - 1))) {
+            tc::fence_after_sync();
+            float yv[16];
+            read_y(yv);
+            write_y(nw - 1, yv);
+#pragma unroll 1
+            for (int blk = 0; blk < 4; ++blk) {
+                uint32_t r[16];
+                tc::tmem_ld16_nowait(trow + kColSacc + c0 + 16 * blk, r);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; e += 4)
+                    *reinterpret_cast<float4 *>(srow + c0 + 16 * blk + e) =
+                        make_float4(u2f(r[e]), u2f(r[e + 1]), u2f(r[e + 2]), u2f(r[e + 3]));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ prep warps
+        const int pt = tid - 32 * kPrepWarp0;  // 0..255
+        auto prep_wait = [&](uint64_t *bar, int parity, unsigned bit) {
+            return !group_wait(pt == 0, kPrepBarrier, kPrepThreads, bar, parity, bit);
+        };
+        auto prep_sync = [&]() {
+            return named_barrier_or(kPrepBarrier, kPrepThreads, *abort_flag != 0);
+        };
+        float g_next = 0.f;
+        if (chunk_t0(0) + lane < n_tokens) g_next = g[(row0 + chunk_t0(0) + lane) * H + vh];
+        for (int ci = 0; ci < nw; ++ci) {
+            const int b = ci & 1, use = ci >> 1;
+            const int t0 = chunk_t0(ci), valid = min(kC, n_tokens - t0);
+            const float *rk = reinterpret_cast<const float *>(smem + kOffRaw + b * kRawBuf);
+            const float *rq = rk + kC * kRawRowF;
+            const float *blk = blk_of(ci);
+            float last;
+            const float gam = chunk_gam_from(g_next, lane, last);
+            const float Gam = expf(gam), wdec = expf(last - gam);
+            g_next = 0.f;
+            if (ci + 1 < nw && chunk_t0(ci + 1) + lane < n_tokens)
+                g_next = g[(row0 + chunk_t0(ci + 1) + lane) * H + vh];
+            // this chunk's W and M, in the order the images take them
+            float4 wv[kC * kS / 4 / kPrepThreads], mv;
+#pragma unroll
+            for (int i = 0; i < kC * kS / 4 / kPrepThreads; ++i) {
+                const uint32_t o = (pt + i * kPrepThreads) * 16u;
+                const int c = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
+                wv[i] = ld4(blk + kBlkW + c * kS + k0);
+            }
+            {
+                const uint32_t o = pt * 16u;
+                const int t = (o / kSbo32) * 8 + (o % 128) / 16, s0 = ((o % kSbo32) / 128) * 4;
+                mv = ld4(blk + kBlkM + t * kC + s0);
+            }
+            static_assert(kC * kC / 4 == kPrepThreads, "one float4 of M per prep thread");
+
+            // the chunk's k and q rows (rows past the end of the sequence count as zero)
+            if (prep_wait(&bars.raw_full[b], use, WD_STAGE_COPY)) break;
+            // w_c k_c and M, split, into buffer ci & 1 once the state update of chunk
+            // ci - 2 has finished reading it
+            if (use > 0 ? prep_wait(&bars.km_free[b], use - 1, WD_MMA) : prep_sync()) break;
+            unsigned char *kmb = smem + b * kKMBytes;
+            for (int idx = pt; idx < kS * kC / 4; idx += kPrepThreads) {
+                const uint32_t o = idx * 16u;
+                const int d = (o / kSbo32) * 8 + (o % 128) / 16, cc = ((o % kSbo32) / 128) * 4;
+                float4 xv;
+                xv.x = __shfl_sync(FULL_MASK, wdec, cc) * (cc < valid ? rk[cc * kRawRowF + d] : 0.f);
+                xv.y = __shfl_sync(FULL_MASK, wdec, cc + 1) *
+                       (cc + 1 < valid ? rk[(cc + 1) * kRawRowF + d] : 0.f);
+                xv.z = __shfl_sync(FULL_MASK, wdec, cc + 2) *
+                       (cc + 2 < valid ? rk[(cc + 2) * kRawRowF + d] : 0.f);
+                xv.w = __shfl_sync(FULL_MASK, wdec, cc + 3) *
+                       (cc + 3 < valid ? rk[(cc + 3) * kRawRowF + d] : 0.f);
+                float4 hi, lo;
+                split4(xv, hi, lo);
+                *reinterpret_cast<float4 *>(kmb + kOffKhi + o) = hi;
+                *reinterpret_cast<float4 *>(kmb + kOffKlo + o) = lo;
+            }
+            {
+                float4 hi, lo;
+                split4(mv, hi, lo);
+                *reinterpret_cast<float4 *>(kmb + kOffMhi + pt * 16u) = hi;
+                *reinterpret_cast<float4 *>(kmb + kOffMlo + pt * 16u) = lo;
+            }
+            // W and Gam_t q_t, split, once the previous chunk's U is formed (its S
+            // products are done)
+            if (ci > 0 ? prep_wait(&bars.u_ready, ci - 1, WD_MMA) : prep_sync()) break;
+#pragma unroll
+            for (int i = 0; i < kC * kS / 4 / kPrepThreads; ++i) {
+                const uint32_t o = (pt + i * kPrepThreads) * 16u;
+                float4 hi, lo;
+                split4(wv[i], hi, lo);
+                *reinterpret_cast<float4 *>(smem + kOffWhi + o) = hi;
+                *reinterpret_cast<float4 *>(smem + kOffWlo + o) = lo;
+            }
+            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {
+                const uint32_t o = idx * 16u;
+                const int t = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
+                const float Gt = __shfl_sync(FULL_MASK, Gam, t);
+                float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < valid) xv = ld4(rq + t * kRawRowF + k0);
+                xv.x *= Gt; xv.y *= Gt; xv.z *= Gt; xv.w *= Gt;
+                float4 hi, lo;
+                split4(xv, hi, lo);
+                *reinterpret_cast<float4 *>(smem + kOffQhi + o) = hi;
+                *reinterpret_cast<float4 *>(smem + kOffQlo + o) = lo;
+            }
+            fence_proxy_async_smem();
+            named_barrier_sync(kPrepBarrier, kPrepThreads);
+            if (pt == 0) {
+                mbar_arrive(&bars.img_ready);
+                mbar_arrive(&bars.raw_empty[b]);  // done with this chunk's raw rows
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+size_t bytes_per_chunk(int n_seqs, int n_v_heads) {
+    return static_cast<size_t>(n_seqs) * static_cast<size_t>(n_v_heads) * kBlkBytes;
+}
+
+}  // namespace
+
+unsigned read_and_clear_watchdog_chunked_ws(cudaStream_t s) {
+    unsigned flags = 0;
+    const unsigned zero = 0;
+    cudaMemcpyFromSymbolAsync(&flags, g_watchdog_chunked_ws, sizeof(flags), 0,
+                              cudaMemcpyDeviceToHost, s);
+    cudaMemcpyToSymbolAsync(g_watchdog_chunked_ws, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+    cudaStreamSynchronize(s);
+    return flags;
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" size_t gdn_recurrence_scan_chunked_ws_size(int n_seqs, int n_tokens, int n_v_heads,
+                                                      int state_size) {
+    if (n_seqs < 1 || n_tokens < 1 || n_v_heads < 1 || state_size != chunk::kS) return 0;
+    const size_t n_chunks = (static_cast<size_t>(n_tokens) + chunk::kC - 1) / chunk::kC;
+    return n_chunks * bytes_per_chunk(n_seqs, n_v_heads);
+}
+
+extern "C" gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *q, const float *k,
+                                                     const float *v, const float *g,
+                                                     const float *beta, float *y, int n_seqs,
+                                                     int n_tokens, int n_k_heads, int n_v_heads,
+                                                     int state_size, float scale,
+                                                     const int32_t *slots, int pool,
+                                                     int32_t *err_count, void *workspace,
+                                                     size_t workspace_bytes, gdn_stream_t stream) {
+    if (!state || !q || !k || !v || !g || !beta || !y) return GDN_ERR_NULL;
+    if (n_seqs < 0 || n_tokens < 0) return GDN_ERR_SHAPE;
+    GDN_TRY(check_heads(n_k_heads, n_v_heads, state_size));
+    if (state_size != chunk::kS) return GDN_ERR_UNSUPPORTED;
+    GDN_TRY(check_pool(n_seqs, slots, pool));
+    if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
+    if (!workspace) return GDN_ERR_NULL;
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(workspace))
+        return GDN_ERR_ALIGN;
+    const int n_chunks = (n_tokens + chunk::kC - 1) / chunk::kC;
+    const size_t per_chunk = bytes_per_chunk(n_seqs, n_v_heads);
+    const size_t fit = workspace_bytes / per_chunk;
+    if (fit < 1) return GDN_ERR_SHAPE;
+    const int wave = fit < static_cast<size_t>(n_chunks) ? static_cast<int>(fit) : n_chunks;
+    if (static_cast<long long>(n_seqs) * n_v_heads > 0x7fffffffLL ||
+        static_cast<long long>(wave) * n_seqs * n_k_heads > 0x7fffffffLL)
+        return GDN_ERR_UNSUPPORTED;
+    static const bool attr_set = [] {
+        cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+        return true;
+    }();
+    (void)attr_set;
+    const cudaStream_t s = as_cuda(stream);
+    float *ws = static_cast<float *>(workspace);
+    for (int cb = 0; cb < n_chunks; cb += wave) {
+        const int nwc = n_chunks - cb < wave ? n_chunks - cb : wave;
+        chunk_prepare_kernel<<<nwc * n_seqs * n_k_heads, kPThreads, 0, s>>>(
+            q, k, v, g, beta, ws, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nwc);
+        GDN_TRY(launch_status());
+        // slot errors are counted once, in the first wave
+        chunk_state_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, s>>>(
+            state, q, k, g, ws, y, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nwc, scale, slots,
+            pool, cb == 0 ? err_count : nullptr);
+        GDN_TRY(launch_status());
+    }
+    return GDN_OK;
+}

@@ -43,6 +43,7 @@ gdn_status launch_gated_norm(const float *y, const float *w, const float *z, flo
 unsigned read_and_clear_watchdog_recurrence(cudaStream_t s);
 unsigned read_and_clear_watchdog_block(cudaStream_t s);
 unsigned read_and_clear_watchdog_chunked(cudaStream_t s);
+unsigned read_and_clear_watchdog_chunked_ws(cudaStream_t s);
 
 }  // namespace gdn
 

@@ -264,7 +264,7 @@ gdn_status gdn_device_error(gdn_stream_t stream) {
     const cudaStream_t s = as_cuda(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_LAUNCH;
     unsigned flags = read_and_clear_watchdog_recurrence(s) | read_and_clear_watchdog_block(s) |
-                     read_and_clear_watchdog_chunked(s);
+                     read_and_clear_watchdog_chunked(s) | read_and_clear_watchdog_chunked_ws(s);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_LAUNCH;
     return flags ? GDN_ERR_DEVICE : GDN_OK;
 }

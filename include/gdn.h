@@ -189,6 +189,35 @@ gdn_status gdn_recurrence_scan_chunked(float *state, const float *q, const float
                                        const int32_t *slots, int pool, int32_t *err_count,
                                        gdn_stream_t stream);
 
+/* Bytes of workspace for gdn_recurrence_scan_chunked_ws to prepare every chunk of
+ * the call at once: ceil(n_tokens / 32) * n_seqs * n_v_heads * 36 KiB (W, Ut and M of
+ * each chunk, fp32). 0 for invalid sizes or a state_size other than 128. */
+size_t gdn_recurrence_scan_chunked_ws_size(int n_seqs, int n_tokens, int n_v_heads,
+                                           int state_size);
+
+/* The chunked scan of gdn_recurrence_scan_chunked in two phases: a fully parallel
+ * kernel over (chunk, sequence, k-head) forms each chunk's state-independent
+ * quantities (Gram products, the forward substitutions of the WY/UT form) in the
+ * workspace, then one CTA per (sequence, v-head) advances the state over the
+ * chunks on the tensor cores. Same sources on the pages as
+ * gdn_recurrence_scan_chunked, and the same bits: both run the same arithmetic in
+ * the same order.
+ * Arguments, layouts, ownership and slot semantics as gdn_recurrence_scan_chunked,
+ * plus workspace: device memory owned by the caller, 16-byte aligned
+ * (GDN_ERR_ALIGN), contents on entry irrelevant and garbage afterwards; NULL is
+ * GDN_ERR_NULL. A workspace of gdn_recurrence_scan_chunked_ws_size() bytes takes
+ * two launches; a smaller one is used in waves of as many chunks as it holds
+ * (two launches per wave, same results); less than one chunk's worth
+ * (n_seqs * n_v_heads * 36 KiB) is GDN_ERR_SHAPE. Calls that share a workspace
+ * must not overlap. */
+gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *q, const float *k,
+                                          const float *v, const float *g, const float *beta,
+                                          float *y, int n_seqs, int n_tokens, int n_k_heads,
+                                          int n_v_heads, int state_size, float scale,
+                                          const int32_t *slots, int pool, int32_t *err_count,
+                                          void *workspace, size_t workspace_bytes,
+                                          gdn_stream_t stream);
+
 /* The conv scan, also writing the conv history after every position (ssm_gated_delta.cu,
  * fc_ssm_conv1d_silu_seq's `snaps`): snaps [n_seqs][n_tokens][conv_dim][K-1], the
  * conv_state layout of one slot per position. NULL is an error. Otherwise as

@@ -185,6 +185,38 @@ def test_chunked_scan_validation(lib):
     assert call(n_tokens=0) == OK
 
 
+def test_chunked_ws_validation(lib):
+    f = lib.gdn_recurrence_scan_chunked_ws
+    f.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_size_t, ctypes.c_void_p]
+    size = lib.gdn_recurrence_scan_chunked_ws_size
+    size.argtypes = [ctypes.c_int] * 4
+    size.restype = ctypes.c_size_t
+    blk = 36 * 1024  # W, Ut and M of one chunk of one (sequence, v-head), fp32
+    assert size(2, 40, 4, 128) == 2 * 2 * 4 * blk
+    assert size(3, 32, 8, 128) == 1 * 3 * 8 * blk
+    assert size(1, 4096, 32, 128) == 128 * 32 * blk
+    assert size(2, 40, 4, 64) == 0 and size(0, 40, 4, 128) == 0 and size(2, 0, 4, 128) == 0
+
+    def call(state=P, q=P, s=128, hk=2, hv=4, n_tokens=40, pool=2, y=P, workspace=P,
+             nbytes=None):
+        nbytes = size(2, n_tokens, hv, 128) if nbytes is None else nbytes
+        return f(state, q, P, P, P, P, y, 2, n_tokens, hk, hv, s, 0.1, None, pool, None,
+                 workspace, nbytes, None)
+    assert call(state=None) == NULL
+    assert call(y=None) == NULL
+    assert call(workspace=None) == NULL
+    assert call(q=MIS) == ALIGN
+    assert call(workspace=MIS) == ALIGN
+    assert call(s=64) == UNSUP
+    assert call(s=100) == SHAPE
+    assert call(hk=3) == SHAPE
+    assert call(pool=1) == SHAPE
+    assert call(nbytes=2 * 4 * blk - 16) == SHAPE  # less than one chunk of every unit
+    assert call(n_tokens=0, workspace=None) == OK
+
+
 def test_prefill_chunked_validation(lib):
     f = lib.gdn_block_prefill_chunked
     f.argtypes = [ctypes.c_void_p] * 11 + [ctypes.c_int] * 6 + [ctypes.c_float] * 3 + [
