@@ -46,13 +46,23 @@ TF32_PER_BF16 = 1.1 / 2.25
 
 
 def chunked_tensor_flops(n_seqs, n_tokens, n_v_heads):
-    """Tensor-core flops of one chunked-scan launch (S = 128, chunks of 32): per
-    (sequence, v-head, chunk) S^T [W | Gam Q]^T (N = 64, first pass), two more passes
-    each of W S and of the S part of y (N = 32), the state update (3 passes, N = 128,
-    K = 32) and the U part of y (3 passes, N = 32, K = 32)."""
-    per = 2 * 128 * 64 * 128 + 4 * (2 * 128 * 32 * 128) + 3 * (2 * 128 * 128 * 32) + \
-        3 * (2 * 128 * 32 * 32)
+    """Tensor-core flops the chunked scan issues (S = 128, chunks of 32): per
+    (sequence, v-head, chunk) the S products hi(S) [hi W | hi Gam q | lo W | lo Gam q]
+    (N = 128, K = 128) and lo(S) [hi W | hi Gam q] (N = 64), then the state update with
+    the U part of y, U^T [w K | M]^T in 3 passes (N = 160, K = 32)."""
+    per = 2 * 128 * 128 * 128 + 2 * 128 * 64 * 128 + 3 * (2 * 128 * 160 * 32)
     return per * n_seqs * n_v_heads * ((n_tokens + 31) // 32)
+
+
+def chunk_prepare_flops(n_seqs, n_tokens, n_k_heads, n_v_heads):
+    """FP32 flops of the chunk-preparation phase (S = 128, chunks of 32): per (sequence,
+    k-head, chunk) the Gram products k_t.k_s (s < t) and q_t.k_s (s <= t) over dk; per
+    v-head the right-hand sides, A and M, and the two forward substitutions (W and Ut,
+    128 columns each, 496 multiply-adds per column)."""
+    gram = (496 + 528) * 128 * 2
+    per_vhead = 2 * 128 * 496 * 2 + 32 * 128 * 3 + (496 + 528) * 3
+    n_chunks = (n_tokens + 31) // 32
+    return n_seqs * n_k_heads * n_chunks * (gram + (n_v_heads // n_k_heads) * per_vhead)
 FLUSH_BYTES = 256 << 20
 L2_NOTE = "flushed before every timed step (256 MiB write, then 256 MiB read: cold, clean L2)"
 FALLBACK_HBM_GBS = 6800.0
@@ -82,9 +92,37 @@ KERNEL_SOURCES = {
     "recurrence_scan_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_recurrence.cu",
                                "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh"],
     "chunked_scan_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_chunked.cu",
+                            "gated_deltanet_linear_scan_gb300/csrc/gdn_chunk_common.cuh",
                             "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh",
                             "gated_deltanet_linear_scan_gb300/csrc/gdn_tc.cuh"],
+    "chunk_state_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_chunked_ws.cu",
+                           "gated_deltanet_linear_scan_gb300/csrc/gdn_chunk_common.cuh",
+                           "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh",
+                           "gated_deltanet_linear_scan_gb300/csrc/gdn_tc.cuh"],
 }
+
+
+def time_chunked_phases(gdn, torch, stream, state, state0, x, y, dims, scale, ws, steps, flush):
+    """Per-step seconds of the two phases of the chunked scan (gdn_chunked_prepare,
+    gdn_chunked_advance over all chunks), each timed with CUDA events on `stream`, L2
+    flushed before every step."""
+    N, T, Hk, H, S = dims
+    nc = (T + 31) // 32
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        state.copy_(state0)
+        flush()
+        ev[i][0].record(stream)
+        gdn.gdn_chunked_prepare(x["q"], x["k"], x["v"], x["g"], x["beta"], ws, N, T, Hk, H, S,
+                                0, nc)
+        ev[i][1].record(stream)
+        gdn.gdn_chunked_advance(state, x["q"], x["k"], x["g"], ws, y, N, T, Hk, H, S, scale, 0,
+                                nc)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    prep = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3 / steps
+    adv = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3 / steps
+    return prep, adv
 
 
 def ncu_traffic(kernel, workload):
@@ -463,10 +501,17 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     y = torch.empty(N, T, H, S, device="cuda")
 
     chunked = args.workload == "prefill_chunked_4x4096"
-    scan_fn = gdn.gdn_recurrence_scan_chunked if chunked else gdn.gdn_recurrence_scan
+    ws = None
+    if chunked:
+        ws = torch.empty(gdn.gdn_recurrence_scan_chunked_ws_size(N, T, H, S) // 4, device="cuda")
 
     def launch():
-        scan_fn(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y, N, T, Hk, H, S, cfg.scale)
+        if chunked:
+            gdn.gdn_recurrence_scan_chunked_ws(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y,
+                                               N, T, Hk, H, S, cfg.scale, ws)
+        else:
+            gdn.gdn_recurrence_scan(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y, N, T,
+                                    Hk, H, S, cfg.scale)
 
     for _ in range(args.warmup):
         state.copy_(state0)
@@ -515,15 +560,38 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
     fp32_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
     achieved = flops / per / 1e12
+    extra = {}
     if chunked:
+        # the two phases timed apart (the dominant, tensor-core one for the roofline), and
+        # the one-kernel form on the same inputs for comparison
+        prep_s, adv_s = time_chunked_phases(gdn, torch, stream, state, state0, d, y,
+                                            (N, T, Hk, H, S), cfg.scale, ws, args.steps, flush)
+        one_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+        for i in range(args.steps):
+            state.copy_(state0)
+            flush()
+            one_ev[i][0].record(stream)
+            gdn.gdn_recurrence_scan_chunked(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y,
+                                            N, T, Hk, H, S, cfg.scale)
+            one_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        one_s = sum(e0.elapsed_time(e1) for e0, e1 in one_ev) / 1e3 / args.steps
         tf = chunked_tensor_flops(N, T, H)
+        pf = chunk_prepare_flops(N, T, Hk, H)
         tf32_peak = pk["bf16_tflops"] * TF32_PER_BF16 if "bf16_tflops" in pk else 1900.0 * TF32_PER_BF16
-        roofline = {"bound": "tensor", "achieved": tf / per / 1e12, "peak": tf32_peak,
-                    "unit": "TFLOP/s", "frac": tf / per / 1e12 / tf32_peak,
-                    "traffic": ncu_traffic("chunked_scan_kernel", args.workload),
+        roofline = {"bound": "tensor", "kernel": "chunk_state_kernel (gdn_chunked_advance)",
+                    "achieved": tf / adv_s / 1e12, "peak": tf32_peak,
+                    "unit": "TFLOP/s", "frac": tf / adv_s / 1e12 / tf32_peak,
+                    "traffic": ncu_traffic("chunk_state_kernel", args.workload),
                     "flops_per_launch": tf,
                     "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
                                    f"{TF32_PER_BF16:.3f}"}
+        extra = {"advance_ms": 1e3 * adv_s, "prepare_ms": 1e3 * prep_s,
+                 "prepare_fp32_tflops": pf / prep_s / 1e12,
+                 "prepare_frac_of_fp32_pipes": pf / prep_s / 1e12 / fp32_peak,
+                 "one_kernel_form_ms": 1e3 * one_s,
+                 "workspace_bytes": ws.numel() * 4}
     else:
         roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
                     "frac": achieved / fp32_peak,
@@ -544,15 +612,16 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         "data": "synthetic (seeded PCG64; unit q/k, g~U(-0.5,-0.001))",
         "config": {"workload": args.workload, "n_seqs": N, "n_tokens": T, "n_k_heads": Hk,
                    "n_v_heads": H, "state_size": S,
-                   "kernel": "gdn_recurrence_scan_chunked" if chunked else "gdn_recurrence_scan",
+                   "kernel": ("gdn_recurrence_scan_chunked_ws (2 launches: chunk preparation, "
+                              "tensor-core state advance)") if chunked else "gdn_recurrence_scan",
                    "l2": L2_NOTE,
                    "method_fp32_tflops": achieved,
-                   "method_fp32_frac_of_fp32_pipe_peak": achieved / fp32_peak},
+                   "method_fp32_frac_of_fp32_pipe_peak": achieved / fp32_peak, **extra},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": (2 if chunked else 1) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -573,7 +642,8 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     conv0 = dev(I.conv_state_pool(cfg, which=seqs))
     state, conv = state0.clone(), conv0.clone()
     out = torch.empty(N, T, H, S, device="cuda")
-    ws = torch.empty(gdn.gdn_block_prefill_workspace_size(N, T, Hk, H, S) // 4 + 64, device="cuda")
+    ws = torch.empty(gdn.gdn_block_prefill_chunked_workspace_size(N, T, Hk, H, S) // 4 + 64,
+                     device="cuda")
 
     def launch():
         gdn.gdn_block_prefill_chunked(d["qkv"], st["conv_w"], conv, d["alpha"], d["b"], st["dt"],
@@ -606,8 +676,9 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     per_s = total_s / args.steps
     tokens = world * N * T * args.steps
 
-    # ---- the dominant kernel alone: the recurrence scan over the same intermediates
-    # (made once by the stand-alone step entry points), timed on the same stream.
+    # ---- the dominant kernel alone: the tensor-core state advance of the chunked scan
+    # over the same intermediates (made once by the stand-alone step entry points),
+    # timed on the same stream.
     C = (2 * Hk + H) * S
     conv_out = torch.empty(N, T, C, device="cuda")
     q = torch.empty(N, T, Hk, S, device="cuda")
@@ -621,17 +692,13 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     gdn.gdn_qkv_split_norm(conv_out, q, k, v, N * T, Hk, H, S, cfg.eps)
     gdn.gdn_decay_gate(d["alpha"], st["dt"], st["a"], g, H, N * T)
     gdn.gdn_beta_sigmoid(d["b"], beta, N * T * H)
-    scan_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    for i in range(args.steps):
-        state.copy_(state0)
-        flush()
-        scan_ev[i][0].record(stream)
-        gdn.gdn_recurrence_scan_chunked(state, q, k, v, g, beta, y, N, T, Hk, H, S, cfg.scale)
-        scan_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    scan_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in scan_ev) / 1e3, dist,
-                        "cuda") / args.steps
+    scan_ws = torch.empty(gdn.gdn_recurrence_scan_chunked_ws_size(N, T, H, S) // 4,
+                          device="cuda")
+    prep_s, adv_s = time_chunked_phases(gdn, torch, stream, state, state0,
+                                        {"q": q, "k": k, "v": v, "g": g, "beta": beta}, y,
+                                        (N, T, Hk, H, S), cfg.scale, scan_ws, args.steps, flush)
+    adv_s = reduce_max(adv_s, dist, "cuda")
+    del scan_ws
 
     # ---- end to end: qkv, alpha, b, z from pinned host memory, the call, out back.
     keys = ["qkv", "alpha", "b", "z"]
@@ -676,15 +743,17 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         "data": "synthetic (seeded PCG64; N(0,1) qkv/z, g~U(-0.5,-0.001))",
         "config": {"workload": args.workload, "n_seqs": N, "n_tokens": T, "n_k_heads": Hk,
                    "n_v_heads": H, "state_size": S, "conv_kernel": cfg.conv_kernel,
-                   "kernel": "gdn_block_prefill_chunked (6 launches: conv scan, split norm, "
-                             "gate, beta, chunked tensor-core scan, gated norm)", "l2": L2_NOTE,
-                   "scan_ms": 1e3 * scan_s,
-                   "method_fp32_tflops_of_scan": flops / scan_s / 1e12,
+                   "kernel": "gdn_block_prefill_chunked (6 launches: conv scan with the q/k "
+                             "split-norm, gate, beta, chunk preparation, tensor-core state "
+                             "advance, gated norm)", "l2": L2_NOTE,
+                   "workspace_bytes": ws.numel() * 4,
+                   "scan_prepare_ms": 1e3 * prep_s, "scan_advance_ms": 1e3 * adv_s,
+                   "method_fp32_tflops_of_scan": flops / (prep_s + adv_s) / 1e12,
                    "fp32_pipe_peak_tflops": fp32_peak},
-        "roofline": {"bound": "tensor", "kernel": "chunked_scan_kernel",
-                     "achieved": tf / scan_s / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
-                     "frac": tf / scan_s / 1e12 / tf32_peak,
-                     "traffic": ncu_traffic("chunked_scan_kernel", "prefill_chunked_4x4096"),
+        "roofline": {"bound": "tensor", "kernel": "chunk_state_kernel (gdn_chunked_advance)",
+                     "achieved": tf / adv_s / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
+                     "frac": tf / adv_s / 1e12 / tf32_peak,
+                     "traffic": ncu_traffic("chunk_state_kernel", "prefill_chunked_4x4096"),
                      "flops_per_launch": tf,
                      "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
                                     f"{TF32_PER_BF16:.3f}"},

@@ -24,6 +24,7 @@ __all__ = [
     "gdn_block_prefill_noalloc", "PREFILL_NOALLOC_SCRATCH_BYTES",
     "gdn_recurrence_scan_chunked", "gdn_block_prefill_chunked",
     "gdn_recurrence_scan_chunked_ws_size", "gdn_recurrence_scan_chunked_ws",
+    "gdn_chunked_prepare", "gdn_chunked_advance", "gdn_block_prefill_chunked_workspace_size",
 ]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
@@ -66,6 +67,10 @@ _SIGS = {
     "gdn_recurrence_scan_chunked_ws_size": ([_I, _I, _I, _I], ctypes.c_size_t),
     "gdn_recurrence_scan_chunked_ws": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P,
                                                    ctypes.c_size_t, _P], _I),
+    "gdn_chunked_prepare": ([_P] * 5 + [_P, ctypes.c_size_t] + [_I] * 7 + [_P], _I),
+    "gdn_chunked_advance": ([_P] * 5 + [ctypes.c_size_t, _P] + [_I] * 5 + [_F, _I, _I, _P, _I,
+                                                                          _P, _P], _I),
+    "gdn_block_prefill_chunked_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
     "gdn_block_prefill_chunked": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P, _P,
                                                ctypes.c_size_t, _P], _I),
 }
@@ -259,6 +264,26 @@ def gdn_recurrence_scan_chunked_ws(state, q, k, v, g, beta, y, n_seqs, n_tokens,
         _ws_bytes(workspace), _stream(stream)))
 
 
+def gdn_chunked_prepare(q, k, v, g, beta, workspace, n_seqs, n_tokens, n_k_heads, n_v_heads,
+                        state_size, chunk_begin, n_chunks, stream=None):
+    """Phase 1 of the two-phase chunked scan over chunks chunk_begin .. + n_chunks - 1."""
+    _check("gdn_chunked_prepare", library().gdn_chunked_prepare(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"), _ptr(beta, "beta"),
+        _ws_ptr(workspace), _ws_bytes(workspace), n_seqs, n_tokens, n_k_heads, n_v_heads,
+        state_size, chunk_begin, n_chunks, _stream(stream)))
+
+
+def gdn_chunked_advance(state, q, k, g, workspace, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
+                        state_size, scale, chunk_begin, n_chunks, slots=None, pool=None,
+                        err_count=None, stream=None):
+    """Phase 2: advance the state over the prepared chunks, writing their y."""
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_chunked_advance", library().gdn_chunked_advance(
+        _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(g, "g"), _ws_ptr(workspace),
+        _ws_bytes(workspace), _ptr(y, "y"), n_seqs, n_tokens, n_k_heads, n_v_heads, state_size,
+        scale, chunk_begin, n_chunks, _slots(slots), pool, _errc(err_count), _stream(stream)))
+
+
 def gdn_gated_norm(y, w, z, out, rows, head_dim, eps, stream=None):
     _check("gdn_gated_norm", library().gdn_gated_norm(
         _ptr(y, "y"), _ptr(w, "w"), _ptr(z, "z"), _ptr(out, "out"), rows, head_dim, eps,
@@ -310,6 +335,11 @@ def gdn_conv1d_silu_seq_snapshots(qkv, w, conv_state, out, snaps, n_seqs, n_toke
 def gdn_block_prefill_workspace_size(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size):
     return library().gdn_block_prefill_workspace_size(n_seqs, n_tokens, n_k_heads, n_v_heads,
                                                       state_size)
+
+
+def gdn_block_prefill_chunked_workspace_size(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size):
+    return library().gdn_block_prefill_chunked_workspace_size(n_seqs, n_tokens, n_k_heads,
+                                                              n_v_heads, state_size)
 
 
 def _block_prefill(name, qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,

@@ -545,6 +545,54 @@ size_t bytes_per_chunk(int n_seqs, int n_v_heads) {
     return static_cast<size_t>(n_seqs) * static_cast<size_t>(n_v_heads) * kBlkBytes;
 }
 
+// Checks shared by the entry points; n_seqs > 0 and n_tokens > 0 on GDN_OK.
+gdn_status check_common(int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int state_size) {
+    if (n_seqs < 0 || n_tokens < 0) return GDN_ERR_SHAPE;
+    GDN_TRY(check_heads(n_k_heads, n_v_heads, state_size));
+    if (state_size != kS) return GDN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(n_seqs) * n_v_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+// A chunk range [cb, cb + nc) of the call and a workspace that holds it.
+gdn_status check_range(int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int cb, int nc,
+                       const void *workspace, size_t workspace_bytes) {
+    const int n_chunks = (n_tokens + kC - 1) / kC;
+    if (cb < 0 || nc < 0 || cb > n_chunks || nc > n_chunks - cb) return GDN_ERR_SHAPE;
+    if (nc == 0) return GDN_OK;
+    if (!workspace) return GDN_ERR_NULL;
+    if (!aligned16(workspace)) return GDN_ERR_ALIGN;
+    if (workspace_bytes / bytes_per_chunk(n_seqs, n_v_heads) < static_cast<size_t>(nc))
+        return GDN_ERR_SHAPE;
+    if (static_cast<long long>(nc) * n_seqs * n_k_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+gdn_status launch_prepare(const float *q, const float *k, const float *v, const float *g,
+                          const float *beta, float *ws, int n_seqs, int n_tokens, int n_k_heads,
+                          int n_v_heads, int cb, int nc, cudaStream_t s) {
+    chunk_prepare_kernel<<<nc * n_seqs * n_k_heads, kPThreads, 0, s>>>(
+        q, k, v, g, beta, ws, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nc);
+    return launch_status();
+}
+
+gdn_status launch_advance(float *state, const float *q, const float *k, const float *g,
+                          const float *ws, float *y, int n_seqs, int n_tokens, int n_k_heads,
+                          int n_v_heads, float scale, int cb, int nc, const int32_t *slots,
+                          int pool, int32_t *err_count, cudaStream_t s) {
+    static const bool attr_set = [] {
+        cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+        return true;
+    }();
+    (void)attr_set;
+    // slot errors are counted once, with the first chunk
+    chunk_state_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, s>>>(
+        state, q, k, g, ws, y, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nc, scale, slots, pool,
+        cb == 0 ? err_count : nullptr);
+    return launch_status();
+}
+
 }  // namespace
 
 unsigned read_and_clear_watchdog_chunked_ws(cudaStream_t s) {
@@ -560,12 +608,49 @@ unsigned read_and_clear_watchdog_chunked_ws(cudaStream_t s) {
 }  // namespace gdn
 
 using namespace gdn;
+using namespace gdn::chunk;
 
 extern "C" size_t gdn_recurrence_scan_chunked_ws_size(int n_seqs, int n_tokens, int n_v_heads,
                                                       int state_size) {
-    if (n_seqs < 1 || n_tokens < 1 || n_v_heads < 1 || state_size != chunk::kS) return 0;
-    const size_t n_chunks = (static_cast<size_t>(n_tokens) + chunk::kC - 1) / chunk::kC;
+    if (n_seqs < 1 || n_tokens < 1 || n_v_heads < 1 || state_size != kS) return 0;
+    const size_t n_chunks = (static_cast<size_t>(n_tokens) + kC - 1) / kC;
     return n_chunks * bytes_per_chunk(n_seqs, n_v_heads);
+}
+
+extern "C" gdn_status gdn_chunked_prepare(const float *q, const float *k, const float *v,
+                                          const float *g, const float *beta, void *workspace,
+                                          size_t workspace_bytes, int n_seqs, int n_tokens,
+                                          int n_k_heads, int n_v_heads, int state_size,
+                                          int chunk_begin, int n_chunks, gdn_stream_t stream) {
+    if (!q || !k || !v || !g || !beta) return GDN_ERR_NULL;
+    GDN_TRY(check_common(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size));
+    if (n_seqs == 0 || n_tokens == 0) return n_chunks == 0 && chunk_begin == 0 ? GDN_OK : GDN_ERR_SHAPE;
+    GDN_TRY(check_range(n_seqs, n_tokens, n_k_heads, n_v_heads, chunk_begin, n_chunks, workspace,
+                        workspace_bytes));
+    if (n_chunks == 0) return GDN_OK;
+    if (!aligned16(q) || !aligned16(k)) return GDN_ERR_ALIGN;
+    return launch_prepare(q, k, v, g, beta, static_cast<float *>(workspace), n_seqs, n_tokens,
+                          n_k_heads, n_v_heads, chunk_begin, n_chunks, as_cuda(stream));
+}
+
+extern "C" gdn_status gdn_chunked_advance(float *state, const float *q, const float *k,
+                                          const float *g, const void *workspace,
+                                          size_t workspace_bytes, float *y, int n_seqs,
+                                          int n_tokens, int n_k_heads, int n_v_heads,
+                                          int state_size, float scale, int chunk_begin,
+                                          int n_chunks, const int32_t *slots, int pool,
+                                          int32_t *err_count, gdn_stream_t stream) {
+    if (!state || !q || !k || !g || !y) return GDN_ERR_NULL;
+    GDN_TRY(check_common(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size));
+    GDN_TRY(check_pool(n_seqs, slots, pool));
+    if (n_seqs == 0 || n_tokens == 0) return n_chunks == 0 && chunk_begin == 0 ? GDN_OK : GDN_ERR_SHAPE;
+    GDN_TRY(check_range(n_seqs, n_tokens, n_k_heads, n_v_heads, chunk_begin, n_chunks, workspace,
+                        workspace_bytes));
+    if (n_chunks == 0) return GDN_OK;
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k)) return GDN_ERR_ALIGN;
+    return launch_advance(state, q, k, g, static_cast<const float *>(workspace), y, n_seqs,
+                          n_tokens, n_k_heads, n_v_heads, scale, chunk_begin, n_chunks, slots,
+                          pool, err_count, as_cuda(stream));
 }
 
 extern "C" gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *q, const float *k,
@@ -577,41 +662,26 @@ extern "C" gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *
                                                      int32_t *err_count, void *workspace,
                                                      size_t workspace_bytes, gdn_stream_t stream) {
     if (!state || !q || !k || !v || !g || !beta || !y) return GDN_ERR_NULL;
-    if (n_seqs < 0 || n_tokens < 0) return GDN_ERR_SHAPE;
-    GDN_TRY(check_heads(n_k_heads, n_v_heads, state_size));
-    if (state_size != chunk::kS) return GDN_ERR_UNSUPPORTED;
+    GDN_TRY(check_common(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size));
     GDN_TRY(check_pool(n_seqs, slots, pool));
     if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
     if (!workspace) return GDN_ERR_NULL;
     if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
         !aligned16(workspace))
         return GDN_ERR_ALIGN;
-    const int n_chunks = (n_tokens + chunk::kC - 1) / chunk::kC;
-    const size_t per_chunk = bytes_per_chunk(n_seqs, n_v_heads);
-    const size_t fit = workspace_bytes / per_chunk;
+    const int n_chunks = (n_tokens + kC - 1) / kC;
+    const size_t fit = workspace_bytes / bytes_per_chunk(n_seqs, n_v_heads);
     if (fit < 1) return GDN_ERR_SHAPE;
     const int wave = fit < static_cast<size_t>(n_chunks) ? static_cast<int>(fit) : n_chunks;
-    if (static_cast<long long>(n_seqs) * n_v_heads > 0x7fffffffLL ||
-        static_cast<long long>(wave) * n_seqs * n_k_heads > 0x7fffffffLL)
-        return GDN_ERR_UNSUPPORTED;
-    static const bool attr_set = [] {
-        cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-        return true;
-    }();
-    (void)attr_set;
+    if (static_cast<long long>(wave) * n_seqs * n_k_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     const cudaStream_t s = as_cuda(stream);
     float *ws = static_cast<float *>(workspace);
     for (int cb = 0; cb < n_chunks; cb += wave) {
-        const int nwc = n_chunks - cb < wave ? n_chunks - cb : wave;
-        chunk_prepare_kernel<<<nwc * n_seqs * n_k_heads, kPThreads, 0, s>>>(
-            q, k, v, g, beta, ws, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nwc);
-        GDN_TRY(launch_status());
-        // slot errors are counted once, in the first wave
-        chunk_state_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, s>>>(
-            state, q, k, g, ws, y, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nwc, scale, slots,
-            pool, cb == 0 ? err_count : nullptr);
-        GDN_TRY(launch_status());
+        const int nc = n_chunks - cb < wave ? n_chunks - cb : wave;
+        GDN_TRY(launch_prepare(q, k, v, g, beta, ws, n_seqs, n_tokens, n_k_heads, n_v_heads, cb,
+                               nc, s));
+        GDN_TRY(launch_advance(state, q, k, g, ws, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
+                               scale, cb, nc, slots, pool, err_count, s));
     }
     return GDN_OK;
 }

@@ -169,6 +169,15 @@ size_t gdn_block_prefill_workspace_size(int n_seqs, int n_tokens, int n_k_heads,
            sizeof(float);
 }
 
+size_t gdn_block_prefill_chunked_workspace_size(int n_seqs, int n_tokens, int n_k_heads,
+                                                int n_v_heads, int state_size) {
+    const size_t base =
+        gdn_block_prefill_workspace_size(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size);
+    if (base == 0 || state_size != 128) return base;
+    return (base + 15) / 16 * 16 +
+           gdn_recurrence_scan_chunked_ws_size(n_seqs, n_tokens, n_v_heads, state_size);
+}
+
 }  // extern "C"
 
 namespace {
@@ -218,8 +227,18 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
     GDN_TRY(gdn_decay_gate(alpha, dt, a, g, H, static_cast<int>(rows), stream));
     GDN_TRY(gdn_beta_sigmoid(b, beta, static_cast<int>(rows * H), stream));
     if (chunked) {
-        GDN_TRY(gdn_recurrence_scan_chunked(state, q, k, v, g, beta, out, n_seqs, n_tokens, Hk, H,
-                                            S, scale, slots, pool, nullptr, stream));
+        // the two-phase form in the bytes past the intermediates, if they hold one chunk
+        const size_t base = (L.total_floats * sizeof(float) + 15) / 16 * 16;
+        const size_t one_chunk = gdn_recurrence_scan_chunked_ws_size(n_seqs, 1, H, S);
+        if (workspace_bytes >= base + one_chunk) {
+            GDN_TRY(gdn_recurrence_scan_chunked_ws(state, q, k, v, g, beta, out, n_seqs, n_tokens,
+                                                   Hk, H, S, scale, slots, pool, nullptr,
+                                                   static_cast<char *>(workspace) + base,
+                                                   workspace_bytes - base, stream));
+        } else {
+            GDN_TRY(gdn_recurrence_scan_chunked(state, q, k, v, g, beta, out, n_seqs, n_tokens,
+                                                Hk, H, S, scale, slots, pool, nullptr, stream));
+        }
     } else {
         GDN_TRY(gdn_recurrence_scan(state, q, k, v, g, beta, out, n_seqs, n_tokens, Hk, H, S,
                                     scale, slots, pool, nullptr, stream));

@@ -218,6 +218,33 @@ gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *q, const fl
                                           void *workspace, size_t workspace_bytes,
                                           gdn_stream_t stream);
 
+/* The two phases of gdn_recurrence_scan_chunked_ws as separate calls, for callers
+ * that schedule them themselves (e.g. prepare the next wave of chunks on another
+ * stream while the state advances over this one). A chunk range is chunk_begin ..
+ * chunk_begin + n_chunks - 1 of the ceil(n_tokens / 32) chunks of every sequence
+ * (outside it: GDN_ERR_SHAPE); the workspace holds the range's blocks, n_chunks *
+ * n_seqs * n_v_heads * 36 KiB (less: GDN_ERR_SHAPE), 16-byte aligned, the block of
+ * chunk chunk_begin + c of (sequence n, v-head vh) at byte offset
+ * ((c * n_seqs + n) * n_v_heads + vh) * 36 KiB: W [32][128], Ut [32][128], M [32][32].
+ * gdn_chunked_prepare reads q, k, v, g, beta and writes the blocks.
+ * gdn_chunked_advance reads the blocks, q, k and g, advances the state over the
+ * range and writes y of its positions; it counts skipped sequences (slot semantics
+ * as gdn_recurrence_scan) only when chunk_begin == 0, so a sweep over the chunks in
+ * order counts each once. Running prepare then advance over consecutive ranges
+ * from chunk 0 to the last gives the bits of gdn_recurrence_scan_chunked. Other
+ * arguments as gdn_recurrence_scan_chunked_ws. */
+gdn_status gdn_chunked_prepare(const float *q, const float *k, const float *v, const float *g,
+                               const float *beta, void *workspace, size_t workspace_bytes,
+                               int n_seqs, int n_tokens, int n_k_heads, int n_v_heads,
+                               int state_size, int chunk_begin, int n_chunks,
+                               gdn_stream_t stream);
+gdn_status gdn_chunked_advance(float *state, const float *q, const float *k, const float *g,
+                               const void *workspace, size_t workspace_bytes, float *y,
+                               int n_seqs, int n_tokens, int n_k_heads, int n_v_heads,
+                               int state_size, float scale, int chunk_begin, int n_chunks,
+                               const int32_t *slots, int pool, int32_t *err_count,
+                               gdn_stream_t stream);
+
 /* The conv scan, also writing the conv history after every position (ssm_gated_delta.cu,
  * fc_ssm_conv1d_silu_seq's `snaps`): snaps [n_seqs][n_tokens][conv_dim][K-1], the
  * conv_state layout of one slot per position. NULL is an error. Otherwise as
@@ -275,11 +302,19 @@ gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_
                              float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
                              void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
-/* gdn_block_prefill with the chunked tensor-core scan (gdn_recurrence_scan_chunked)
- * in place of the sequential one: the production path for long prefill. Same
- * arguments, layouts, workspace and error behaviour; state_size must be 128 (else
- * GDN_ERR_UNSUPPORTED). Results agree with gdn_block_prefill to within rounding
- * (the 2e-3-of-RMS long-scan bound), not bit for bit. */
+/* gdn_block_prefill with the chunked tensor-core scan in place of the sequential
+ * one: the production path for long prefill. Same arguments, layouts, workspace and
+ * error behaviour; state_size must be 128 (else GDN_ERR_UNSUPPORTED). Results agree
+ * with gdn_block_prefill to within rounding (the 2e-3-of-RMS long-scan bound), not
+ * bit for bit. With the minimum workspace the scan is gdn_recurrence_scan_chunked;
+ * workspace bytes beyond gdn_block_prefill_workspace_size() rounded up to 16 serve
+ * gdn_recurrence_scan_chunked_ws (in waves if they hold fewer chunks than the call
+ * has; used once they hold one chunk of every sequence and v-head), which gives the
+ * same bits faster. gdn_block_prefill_chunked_workspace_size() is the size with room
+ * for every chunk at once. */
+size_t gdn_block_prefill_chunked_workspace_size(int n_seqs, int n_tokens, int n_k_heads,
+                                                int n_v_heads, int state_size);
+
 gdn_status gdn_block_prefill_chunked(const float *qkv, const float *conv_w, float *conv_state,
                                      const float *alpha, const float *b, const float *dt,
                                      const float *a, const float *z, const float *norm_w,

@@ -217,6 +217,50 @@ def test_chunked_ws_validation(lib):
     assert call(n_tokens=0, workspace=None) == OK
 
 
+def test_chunked_phase_validation(lib):
+    prep = lib.gdn_chunked_prepare
+    prep.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_size_t] + [ctypes.c_int] * 7 + [
+        ctypes.c_void_p]
+    adv = lib.gdn_chunked_advance
+    adv.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p] + [
+        ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    blk = 36 * 1024 * 2 * 4  # one chunk of 2 sequences x 4 v-heads
+
+    def p(cb=0, nc=2, nbytes=2 * blk, ws=P, q=P, s=128, n_tokens=40):
+        return prep(q, P, P, P, P, ws, nbytes, 2, n_tokens, 2, 4, s, cb, nc, None)
+
+    def a(cb=0, nc=2, nbytes=2 * blk, ws=P, state=P, pool=2, n_tokens=40):
+        return adv(state, P, P, P, ws, nbytes, P, 2, n_tokens, 2, 4, 128, 0.1, cb, nc, None,
+                   pool, None, None)
+    for f in (p, a):
+        assert f(ws=None) == NULL
+        assert f(ws=MIS) == ALIGN
+        assert f(nbytes=2 * blk - 4) == SHAPE   # the range does not fit
+        assert f(cb=1, nc=2) == SHAPE           # 40 positions are 2 chunks
+        assert f(cb=-1, nc=1) == SHAPE
+        assert f(cb=2, nc=0, ws=None) == OK     # an empty range at the end
+        assert f(n_tokens=0, nc=0, ws=None) == OK
+    assert p(q=None) == NULL
+    assert p(q=MIS) == ALIGN
+    assert p(s=64) == UNSUP
+    assert a(state=None) == NULL
+    assert a(pool=1) == SHAPE
+
+
+def test_prefill_chunked_workspace_size(lib):
+    base = lib.gdn_block_prefill_workspace_size
+    base.restype = ctypes.c_size_t
+    full = lib.gdn_block_prefill_chunked_workspace_size
+    full.restype = ctypes.c_size_t
+    scan = lib.gdn_recurrence_scan_chunked_ws_size
+    scan.restype = ctypes.c_size_t
+    for args in ((2, 40, 2, 4), (4, 4096, 16, 32), (1, 7, 1, 3)):
+        b = base(*args, 128)
+        assert full(*args, 128) == (b + 15) // 16 * 16 + scan(args[0], args[1], args[3], 128)
+        assert full(*args, 64) == base(*args, 64)  # no tensor-core form: nothing extra
+
+
 def test_prefill_chunked_validation(lib):
     f = lib.gdn_block_prefill_chunked
     f.argtypes = [ctypes.c_void_p] * 11 + [ctypes.c_int] * 6 + [ctypes.c_float] * 3 + [

@@ -148,13 +148,15 @@ def test_chunked_scan_prefill_4x4096(lib):
 # ------------------------------------------------------------------ prefill block
 
 def run_block_prefill(lib, cfg, T, steps, state, conv, chunked, slots=None, pool=None,
-                      err=None):
+                      err=None, ws_bytes=None):
+    """ws_bytes: the workspace size (None = the minimum, gdn_block_prefill_workspace_size)."""
     N, H, S = len(steps[0]["qkv"]), cfg.n_v_heads, cfg.state_size
     st = I.block_static(cfg)
     stack = {key: np.stack([a[key] for a in steps], axis=1) for key in ("qkv", "alpha", "b", "z")}
     out = torch.zeros(N, T, H, S, device="cuda")
-    ws = torch.empty(lib.gdn_block_prefill_workspace_size(N, T, cfg.n_k_heads, H, S) // 4,
-                     device="cuda")
+    if ws_bytes is None:
+        ws_bytes = lib.gdn_block_prefill_workspace_size(N, T, cfg.n_k_heads, H, S)
+    ws = torch.full(((ws_bytes + 3) // 4,), float("nan"), device="cuda")
     fn = lib.gdn_block_prefill_chunked if chunked else lib.gdn_block_prefill
     fn(dev(stack["qkv"]), dev(st["conv_w"]), conv, dev(stack["alpha"]), dev(stack["b"]),
        dev(st["dt"]), dev(st["a"]), dev(stack["z"]), dev(st["norm_w"]), state, out, N, T,
@@ -192,6 +194,28 @@ def test_block_prefill_chunked(lib, Hk, H, N, T):
     out2 = run_block_prefill(lib, cfg, T, steps, state2, conv2, chunked=False)
     assert_rms(host(out), host(out2), "out vs sequential prefill")
     assert torch.equal(conv, conv2)  # the conv scan is shared: bit for bit
+
+
+def test_block_prefill_chunked_two_phase_workspace(lib):
+    """A workspace with room for the two-phase scan (all chunks, or 3 at a time) gives
+    the bits of the minimum workspace (the one-kernel scan)."""
+    cfg = I.get_config(0, n_k_heads=2, n_v_heads=4, state_size=128, n_seqs=2, cid=960)
+    T = 150
+    steps = [I.block_step(cfg, t) for t in range(T)]
+    st0, cs0 = I.state_pool(cfg), I.conv_state_pool(cfg)
+    N, H, S = 2, cfg.n_v_heads, cfg.state_size
+    base = lib.gdn_block_prefill_workspace_size(N, T, cfg.n_k_heads, H, S)
+    full = lib.gdn_block_prefill_chunked_workspace_size(N, T, cfg.n_k_heads, H, S)
+    assert full > base
+    results = []
+    for nbytes in (base, full, (base + 15) // 16 * 16 + 3 * N * H * 36 * 1024):
+        state, conv = dev(st0), dev(cs0)
+        out = run_block_prefill(lib, cfg, T, steps, state, conv, chunked=True, ws_bytes=nbytes)
+        results.append((out, state, conv))
+    for out, state, conv in results[1:]:
+        assert torch.equal(out, results[0][0])
+        assert torch.equal(state, results[0][1])
+        assert torch.equal(conv, results[0][2])
 
 
 def test_block_prefill_chunked_invalid_slot(lib):

@@ -155,3 +155,29 @@ def test_ws_prefill_4x4096(lib):
         y_ref, _ = oracle.recurrence(s_ref, scale=cfg.scale, **unit)
         assert_rms(yh[n, :, vh], y_ref[0, :, 0], f"y ({n},{vh})")
         assert_rms(sth[n, vh], s_ref[0, 0], f"final state ({n},{vh})")
+
+
+def test_phases_equal_one_call(lib):
+    """gdn_chunked_prepare / gdn_chunked_advance over consecutive ranges of 2 chunks,
+    with slot routing and a skipped sequence: the bits of the one-kernel form, the
+    skipped sequence counted once."""
+    cfg, x, _ = case(2, 4, 3, 230, seed=57, pool=6)
+    N, T, H, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.state_size
+    pool0 = I.state_pool(cfg)
+    slots = dev(np.array([5, -1, 2], dtype=np.int32))
+    st_p, st_f = dev(pool0), dev(pool0)
+    y_f = run(lib, cfg, x, st_f, "fused", slots=slots, pool=6)
+    d = {key: dev(x[key]) for key in ("q", "k", "v", "g", "beta")}
+    y_p = torch.zeros(N, T, H, S, device="cuda")
+    ws = torch.full((2 * N * H * BLK // 4,), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n_chunks = (T + 31) // 32
+    for cb in range(0, n_chunks, 2):
+        nc = min(2, n_chunks - cb)
+        lib.gdn_chunked_prepare(d["q"], d["k"], d["v"], d["g"], d["beta"], ws, N, T,
+                                cfg.n_k_heads, H, S, cb, nc)
+        lib.gdn_chunked_advance(st_p, d["q"], d["k"], d["g"], ws, y_p, N, T, cfg.n_k_heads, H,
+                                S, cfg.scale, cb, nc, slots=slots, pool=6, err_count=err)
+    assert host(err)[0] == 1
+    assert torch.equal(st_p, st_f)
+    assert torch.equal(y_p, y_f)
