@@ -49,16 +49,22 @@ __device__ __forceinline__ size_t blk_index(int cw, int n, int vh, int n_seqs, i
 constexpr int kPThreads = 256;
 constexpr int kAtRow = kC + 4;  // A^T rows: 36 floats, float4 aligned
 constexpr uint32_t kAtBytes = kC * kAtRow * 4;
-constexpr uint32_t kPOffK = 0, kPOffQ = kRawArr, kPOffAt = 2 * kRawArr;
-constexpr size_t kPSmemBytes = 2 * kRawArr + 2 * kAtBytes;  // 43,008 B
+constexpr uint32_t kVBytes = kC * kS * 4;  // the v rows of one v-head, unpadded
+// shared memory: k and q rows (padded), the v rows of two v-heads, A^T, 3 mbarriers
+constexpr uint32_t kPOffK = 0, kPOffQ = kRawArr, kPOffV = 2 * kRawArr;
+constexpr uint32_t kPOffAt = kPOffV + 2 * kVBytes, kPOffBar = kPOffAt + kAtBytes;
+constexpr size_t kPSmemBytes = kPOffBar + 3 * sizeof(uint64_t);  // 71,296 B: 3 CTAs per SM
+static_assert(kPOffBar % 8 == 0, "mbarrier alignment");
 
 // grid = n_wave_chunks * n_seqs * n_k_heads; CTA (cw, n, kh) prepares chunk c_begin + cw of
-// sequence n for the v-heads rr * Hk + kh.
-__global__ void __launch_bounds__(kPThreads, 4) chunk_prepare_kernel(
+// sequence n for the v-heads rr * Hk + kh. Warp 0 bulk-copies the chunk's k and q rows
+// and the v rows of the first two v-heads at the start (the v rows of v-head rr + 2
+// into the buffer of rr once rr is done), so a CTA waits on memory about once.
+__global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
     const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
     const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ ws,
     int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int c_begin, int n_wave_chunks) {
-    __shared__ __align__(16) unsigned char smem[kPSmemBytes];
+    extern __shared__ __align__(16) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = n_v_heads, Hk = n_k_heads;
     const int cw = blockIdx.x % n_wave_chunks;
@@ -66,44 +72,62 @@ __global__ void __launch_bounds__(kPThreads, 4) chunk_prepare_kernel(
     const int kh = rest % Hk, n = rest / Hk;
     const int t0 = (c_begin + cw) * kC, valid = min(kC, n_tokens - t0);
     const size_t row0 = static_cast<size_t>(n) * n_tokens + t0;  // (n, t0) in [N][T] order
+    const int ratio = H / Hk;
     float *rk = reinterpret_cast<float *>(smem + kPOffK);
     float *rq = reinterpret_cast<float *>(smem + kPOffQ);
+    float *At = reinterpret_cast<float *>(smem + kPOffAt);
+    uint64_t *bar_kq = reinterpret_cast<uint64_t *>(smem + kPOffBar);
+    uint64_t *bar_v = bar_kq + 1;  // [2]
 
-    // k and q rows of the chunk, zero past the end of the sequence
-    for (int i = tid; i < 2 * kC * (kS / 4); i += kPThreads) {
-        const int arr = i / (kC * kS / 4), rem = i % (kC * kS / 4);
-        const int t = rem / (kS / 4), c4 = rem % (kS / 4);
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < valid) x = ld4((arr ? q : k) + ((row0 + t) * Hk + kh) * kS + 4 * c4);
-        *reinterpret_cast<float4 *>((arr ? rq : rk) + t * kRawRowF + 4 * c4) = x;
+    // v rows of v-head rr into buffer rr & 1 (warp 0)
+    auto issue_v = [&](int rr) {
+        uint64_t *bar = bar_v + (rr & 1);
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(valid) * kS * 4);
+        __syncwarp();
+        if (lane < valid) {
+            const int vh = rr * Hk + kh;
+            bulk_g2s(smem + kPOffV + (rr & 1) * kVBytes + lane * kS * 4,
+                     v + ((row0 + lane) * H + vh) * kS, kS * 4, bar);
+        }
+    };
+    if (tid == 0) {
+        mbar_init(bar_kq, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_v + 1, 1);
+        fence_mbar_init();
     }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(bar_kq, 2u * valid * kS * 4);
+        __syncwarp();
+        if (lane < valid) {
+            const size_t row = (row0 + lane) * Hk + kh;
+            bulk_g2s(rk + lane * kRawRowF, k + row * kS, kS * 4, bar_kq);
+            bulk_g2s(rq + lane * kRawRowF, q + row * kS, kS * 4, bar_kq);
+        }
+        issue_v(0);
+        if (ratio > 1) issue_v(1);
+    }
+    // rows past the end of the sequence are zero (not copied)
+    for (int i = tid; i < 2 * (kC - valid) * kS; i += kPThreads) {
+        const int arr = i / ((kC - valid) * kS), rem = i % ((kC - valid) * kS);
+        (arr ? rq : rk)[(valid + rem / kS) * kRawRowF + rem % kS] = 0.f;
+    }
+    bool ok = mbar_wait(bar_kq, 0);
     __syncthreads();
     int t, s0;
     float kk[4], qk[4];
     gram_products(rk, rq, warp, lane, t, s0, kk, qk);
 
-    const int ratio = H / Hk;
     const int col = tid & (kS - 1);
     const bool is_w = tid < kS;
     for (int rr = 0; rr < ratio; ++rr) {
         const int vh = rr * Hk + kh;
         float *blk = ws + blk_index(cw, n, vh, n_seqs, H) * kBlkFloats;
-        float *At = reinterpret_cast<float *>(smem + kPOffAt + (rr & 1) * kAtBytes);
         float gl = 0.f, bl = 0.f;  // lane = position
         if (lane < valid) {
             gl = g[(row0 + lane) * H + vh];
             bl = beta[(row0 + lane) * H + vh];
-        }
-        // v of the Ut columns, fetched now so the loads overlap the A stage
-        float x[kC];
-        if (!is_w) {
-            const float *vp = v + (row0 * H + vh) * kS + col;
-            const size_t vstride = static_cast<size_t>(H) * kS;
-#pragma unroll
-            for (int p = 0; p < kC; ++p) {
-                x[p] = p < valid ? *vp : 0.f;
-                vp += vstride;
-            }
         }
         float last;
         const float gam = chunk_gam_from(gl, lane, last);
@@ -122,15 +146,25 @@ __global__ void __launch_bounds__(kPThreads, 4) chunk_prepare_kernel(
                 blk[kBlkM + t * kC + s] = e * qk[j];
             }
         }
-        __syncthreads();  // A^T of this v-head is complete (the other buffer is free)
+        __syncthreads();  // A^T of this v-head is complete
 
         // forward substitution, one column per thread: W (threads 0..127), Ut (128..255),
         // column-wise (x_s is final once the rows above are, then updates every row below)
+        float x[kC];
+        if (is_w) {
+#pragma unroll
+            for (int p = 0; p < kC; ++p) x[p] = rk[p * kRawRowF + col];
+        } else {
+            ok = mbar_wait(bar_v + (rr & 1), (rr >> 1) & 1) && ok;
+            const float *rv = reinterpret_cast<const float *>(smem + kPOffV + (rr & 1) * kVBytes);
+#pragma unroll
+            for (int p = 0; p < kC; ++p) x[p] = p < valid ? rv[p * kS + col] : 0.f;
+        }
 #pragma unroll
         for (int p = 0; p < kC; ++p) {
             const float bt = __shfl_sync(FULL_MASK, bl, p);
             const float Gt = __shfl_sync(FULL_MASK, Gam, p);
-            x[p] = is_w ? bt * Gt * rk[p * kRawRowF + col] : bt * x[p];
+            x[p] = is_w ? bt * Gt * x[p] : bt * x[p];
         }
 #pragma unroll
         for (int s2 = 0; s2 < kC - 1; ++s2) {
@@ -146,6 +180,15 @@ __global__ void __launch_bounds__(kPThreads, 4) chunk_prepare_kernel(
         float *outp = blk + (is_w ? kBlkW : kBlkUt) + col;
 #pragma unroll
         for (int p = 0; p < kC; ++p) outp[p * kS] = x[p];
+        __syncthreads();  // done with A^T and with this v-head's v rows
+        if (warp == 0 && rr + 2 < ratio) issue_v(rr + 2);
+    }
+    if (!ok) {
+        // a copy wait gave up: flag it, and never leave with a copy still landing
+        atomicOr(&g_watchdog_chunked_ws, WD_STAGE_COPY);
+        mbar_wait(bar_kq, 0);
+        for (int j = 0; j < 2 && j < ratio; ++j)
+            mbar_wait(bar_v + j, ((ratio - 1 - j) / 2) & 1);  // last use of buffer j
     }
 }
 
@@ -571,7 +614,13 @@ gdn_status check_range(int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, i
 gdn_status launch_prepare(const float *q, const float *k, const float *v, const float *g,
                           const float *beta, float *ws, int n_seqs, int n_tokens, int n_k_heads,
                           int n_v_heads, int cb, int nc, cudaStream_t s) {
-    chunk_prepare_kernel<<<nc * n_seqs * n_k_heads, kPThreads, 0, s>>>(
+    static const bool attr_set = [] {
+        cudaFuncSetAttribute(chunk_prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPSmemBytes));
+        return true;
+    }();
+    (void)attr_set;
+    chunk_prepare_kernel<<<nc * n_seqs * n_k_heads, kPThreads, kPSmemBytes, s>>>(
         q, k, v, g, beta, ws, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nc);
     return launch_status();
 }
@@ -628,7 +677,7 @@ extern "C" gdn_status gdn_chunked_prepare(const float *q, const float *k, const 
     GDN_TRY(check_range(n_seqs, n_tokens, n_k_heads, n_v_heads, chunk_begin, n_chunks, workspace,
                         workspace_bytes));
     if (n_chunks == 0) return GDN_OK;
-    if (!aligned16(q) || !aligned16(k)) return GDN_ERR_ALIGN;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_ERR_ALIGN;
     return launch_prepare(q, k, v, g, beta, static_cast<float *>(workspace), n_seqs, n_tokens,
                           n_k_heads, n_v_heads, chunk_begin, n_chunks, as_cuda(stream));
 }
