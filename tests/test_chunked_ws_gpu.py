@@ -1,11 +1,12 @@
-"""GPU parity of the two-phase chunked scan (gdn_recurrence_scan_chunked_ws).
+"""GPU parity of the two-phase chunked scan (gdn_recurrence_scan_chunked_ws and its
+phases, gdn_chunked_prepare / gdn_chunked_advance).
 
 It runs the arithmetic of the one-kernel chunked scan in the same order, so its y and
 final state must equal that form's bit for bit, whatever the workspace size (one
 wave, or waves of 1 and 3 chunks with the state passing through its fp32 home in
-between). It is also held directly to the oracle's long-scan bound (max |gpu - ref|
-<= 2e-3 * RMS(ref) per tensor), including at the full 4 x 4096 prefill size on
-sampled units.
+between) and however the phases are called. It is also held directly to the oracle's
+long-scan bound (max |gpu - ref| <= 2e-3 * RMS(ref) per tensor), including at the full
+4 x 4096 prefill size on sampled units.
 """
 import numpy as np
 import pytest
@@ -67,8 +68,10 @@ def run(lib, cfg, x, st, form, ws_chunks=None, slots=None, pool=None, err=None):
     return y
 
 
+# GQA ratios 1, 2, 3, 4 and 5 (odd ratios reuse the two v-row buffers of the chunk
+# preparation unevenly), single positions, ragged and exact chunk ends
 CASES = [(2, 4, 2, 1), (2, 4, 2, 31), (1, 2, 1, 32), (2, 4, 1, 33), (2, 4, 2, 100),
-         (4, 4, 1, 64), (2, 8, 2, 200), (1, 1, 3, 97)]
+         (4, 4, 1, 64), (2, 8, 2, 200), (1, 1, 3, 97), (1, 3, 2, 70), (2, 10, 1, 45)]
 
 
 @pytest.mark.parametrize("Hk,H,N,T", CASES)
