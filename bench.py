@@ -391,6 +391,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     gdn.gdn_device_error()
     kernel_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     total_s = reduce_max(sum(kernel_ms) / 1e3, dist, "cuda")
+    step_us = sorted(1e3 * t for t in kernel_ms)
     tokens = world * N * args.steps
     value = tokens / total_s
     per_launch_s = total_s / args.steps
@@ -471,6 +472,10 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "l2": L2_NOTE,
                    "state_gbs": state_b / per_launch_s / 1e9,
                    "state_frac_of_peak": state_b / per_launch_s / 1e9 / pk["hbm_gbs"],
+                   "step_us": {"mean": statistics.fmean(step_us), "min": step_us[0],
+                               "median": statistics.median(step_us),
+                               "p90": step_us[int(0.9 * (len(step_us) - 1))],
+                               "max": step_us[-1]},
                    "wall_s_timed_loop": t_wall,
                    **({"graph_chain": chain} if chain else {})},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
