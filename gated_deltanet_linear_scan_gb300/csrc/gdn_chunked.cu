@@ -580,12 +580,10 @@ extern "C" gdn_status gdn_recurrence_scan_chunked(float *state, const float *q, 
     if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_ERR_ALIGN;
     if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
     if (static_cast<long long>(n_seqs) * n_v_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-    static const bool attr_set = [] {
-        cudaFuncSetAttribute(chunked_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-        return true;
-    }();
-    (void)attr_set;
+    // per launch: the attribute belongs to the current device
+    if (cudaFuncSetAttribute(chunked_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
     chunked_scan_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, as_cuda(stream)>>>(
         state, q, k, v, g, beta, y, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count);
     return launch_status();

@@ -614,12 +614,10 @@ gdn_status check_range(int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, i
 gdn_status launch_prepare(const float *q, const float *k, const float *v, const float *g,
                           const float *beta, float *ws, int n_seqs, int n_tokens, int n_k_heads,
                           int n_v_heads, int cb, int nc, cudaStream_t s) {
-    static const bool attr_set = [] {
-        cudaFuncSetAttribute(chunk_prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kPSmemBytes));
-        return true;
-    }();
-    (void)attr_set;
+    // per launch: the attribute belongs to the current device
+    if (cudaFuncSetAttribute(chunk_prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPSmemBytes)) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
     chunk_prepare_kernel<<<nc * n_seqs * n_k_heads, kPThreads, kPSmemBytes, s>>>(
         q, k, v, g, beta, ws, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nc);
     return launch_status();
@@ -629,12 +627,10 @@ gdn_status launch_advance(float *state, const float *q, const float *k, const fl
                           const float *ws, float *y, int n_seqs, int n_tokens, int n_k_heads,
                           int n_v_heads, float scale, int cb, int nc, const int32_t *slots,
                           int pool, int32_t *err_count, cudaStream_t s) {
-    static const bool attr_set = [] {
-        cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-        return true;
-    }();
-    (void)attr_set;
+    // per launch: the attribute belongs to the current device
+    if (cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
     // slot errors are counted once, with the first chunk
     chunk_state_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, s>>>(
         state, q, k, g, ws, y, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nc, scale, slots, pool,
