@@ -398,6 +398,35 @@ def run_ours(args, cfg, rank, world, local_rank):
     state_b, alg_b = algorithmic_bytes_block(cfg, N)
     achieved = alg_b / per_launch_s / 1e9
 
+    # ---- the recurrence alone (gdn_recurrence_decode on precomputed q^, k^, v, g, beta),
+    # on the same state and slots, timed the same way; reported beside the fused block.
+    xr = I.recurrence_batch(cfg, seqs=seqs, n_tokens=n_distinct)
+    r_steps = [{key: dev(xr[key][:, t]) for key in xr} for t in range(n_distinct)]
+    y_rec = torch.empty(N, H, S, device="cuda")
+
+    def launch_rec(a):
+        gdn.gdn_recurrence_decode(state, a["q"], a["k"], a["v"], a["g"], a["beta"], y_rec, N,
+                                  cfg.n_k_heads, H, S, cfg.scale, slots=d_slots, pool=pool)
+
+    for w in range(args.warmup):
+        flush()
+        launch_rec(r_steps[w % n_distinct])
+    rec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush()
+        rec_ev[i][0].record(stream)
+        launch_rec(r_steps[i % n_distinct])
+        rec_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    rec_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in rec_ev) / 1e3, dist,
+                       "cuda") / args.steps
+    rec_bytes = state_b + N * (2 * cfg.n_k_heads * S + 2 * H * S + 2 * H) * 4
+    recurrence_only = {"kernel": "gdn_recurrence_decode", "us_per_step": 1e6 * rec_s,
+                       "state_gbs": state_b / rec_s / 1e9,
+                       "hbm_gbs": rec_bytes / rec_s / 1e9,
+                       "hbm_frac_of_peak": rec_bytes / rec_s / 1e9 / pk["hbm_gbs"]}
+
     # ---- end to end: pinned host inputs -> device, the C-ABI call, output -> host.
     # A step's inputs (qkv, alpha, b, z) are packed in one pinned host buffer and
     # cross in one copy; the output comes back in one copy.
@@ -477,6 +506,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                                "p90": step_us[int(0.9 * (len(step_us) - 1))],
                                "max": step_us[-1]},
                    "wall_s_timed_loop": t_wall,
+                   "recurrence_only": recurrence_only,
                    **({"graph_chain": chain} if chain else {})},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"],
