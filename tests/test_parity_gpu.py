@@ -439,14 +439,14 @@ def test_block_decode_tiny_chain(lib):
 
 
 @pytest.mark.parametrize("Hk,H,S,N", [(1, 1, 64, 2), (2, 8, 128, 3), (4, 4, 256, 2),
-                                      (1, 2, 32, 5)])
+                                      (1, 2, 32, 5), (2, 16, 128, 2)])  # GQA up to 8
 def test_block_decode_shapes(lib, Hk, H, S, N):
     cfg = I.get_config(0, n_k_heads=Hk, n_v_heads=H, state_size=S, n_seqs=N, cid=300 + S + H)
     check_block_chain(lib, cfg, list(range(N)), steps=3)
 
 
 @pytest.mark.parametrize("Hk,H,S,N", [(16, 32, 128, 20), (8, 16, 64, 40), (16, 16, 128, 20),
-                                      (4, 16, 128, 80)])
+                                      (4, 16, 128, 80), (2, 16, 128, 160)])  # GQA up to 8
 def test_block_decode_persistent_shapes(lib, Hk, H, S, N):
     """At least two (sequence, k-head) groups per SM: the persistent form runs."""
     cfg = I.get_config(0, n_k_heads=Hk, n_v_heads=H, state_size=S, n_seqs=N, cid=500 + S + H + N)
