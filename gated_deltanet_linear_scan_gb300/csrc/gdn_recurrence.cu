@@ -112,19 +112,26 @@ __global__ void __launch_bounds__(kWarps * 32) recurrence_decode_kernel(
 // (L^2, L^1) are shuffles inside the group: every sum, hence every state bit and
 // output, is the decode kernels'. A scan over T tokens still equals T decode calls
 // bit for bit.
-constexpr int kScanWarps = 4;       // consumer warps per CTA
 constexpr int kScanRowsPerWarp = 8; // 8 groups of 4 lanes
-constexpr int kScanRows = kScanWarps * kScanRowsPerWarp;  // 32 state rows per CTA
 constexpr int kScanTok = 16;        // tokens per staged chunk
 constexpr int kScanDepth = 2;       // chunks in flight
 
+// CTA shape and shared memory of the scan for S = 32 E. A CTA has 8 consumer warps
+// (64 rows) wherever a head has that many rows, else 4, plus the producer warp: at
+// S = 128, 2 CTAs per SM at 96 registers, each staging k and q once for 64 rows (a
+// third less time than 4-warp CTAs at 4 per SM, same bits).
 template <int E>
 struct ScanSmem {
     static constexpr int S = 32 * E;
+    static constexpr int kWarps = S >= 64 ? 8 : 4;           // consumer warps
+    static constexpr int kRows = kWarps * kScanRowsPerWarp;  // state rows per CTA
+    static constexpr int kThreads = (kWarps + 1) * 32;
+    static constexpr int kMinBlocks = E >= 8 ? 1 : (E == 1 ? 4 : 2);
     static constexpr int kFloats = kScanTok * S;             // per array per stage
-    static constexpr int vFloats = kScanTok * kScanRows;
+    static constexpr int vFloats = kScanTok * kRows;
     static constexpr size_t stage_bytes = (2 * kFloats + vFloats) * sizeof(float);
     static constexpr size_t bytes = kScanDepth * stage_bytes + 2 * kScanDepth * sizeof(uint64_t);
+    static_assert(S % kRows == 0, "a head is a whole number of CTA row blocks");
 };
 
 // The 8 chunks of lane g of a row: chunk m starts at cell 4E*m + E*g.
@@ -163,21 +170,22 @@ __device__ __forceinline__ float group_dot(const float (&r)[8][E], const float *
     return acc;
 }
 
-// Grid: one CTA per (sequence, v-head, block of 32 rows); 4 consumer warps hold 8
-// rows each in registers for all tokens, plus one producer warp that stages the
+// Grid: one CTA per (sequence, v-head, block of 64 rows, or 32 at S = 32); 8 (or 4)
+// consumer warps hold 8 rows each in registers for all tokens, plus one producer warp that stages the
 // per-token k, q (S floats each) and this block's 32 v values through a 2-deep ring
 // of shared-memory chunks with bulk copies, each chunk tracked by a "full" and an
 // "empty" mbarrier. g and beta (one float per token and head) are read by the lanes
 // a chunk ahead and broadcast with shuffles. The state reaches HBM once per call.
 template <int E, bool SNAP>
-__global__ void __launch_bounds__((kScanWarps + 1) * 32, (E >= 8 ? 2 : 4)) recurrence_scan_kernel(
+__global__ void __launch_bounds__(ScanSmem<E>::kThreads, ScanSmem<E>::kMinBlocks) recurrence_scan_kernel(
     float *state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
     float *__restrict__ y, int n_tokens, int n_k_heads, int n_v_heads, float scale,
     const int32_t *__restrict__ slots, int pool, int32_t *err_count, float *__restrict__ snaps) {
     constexpr int S = 32 * E, TC = kScanTok;
-    constexpr int kBlocksPerHead = S / kScanRows;
     using L = ScanSmem<E>;
+    constexpr int kScanWarps = L::kWarps, kScanRows = L::kRows;
+    constexpr int kBlocksPerHead = S / kScanRows;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + kScanDepth * L::stage_bytes);
     uint64_t *empty = full + kScanDepth;
@@ -244,7 +252,7 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, (E >= 8 ? 2 : 4)) recur
 
     // ---- consumer warps: lane = 4 * (row of the warp) + g
     const int rho = lane >> 2, gq = lane & 3;
-    const int rl = warp * kScanRowsPerWarp + rho;  // row within the CTA's 32
+    const int rl = warp * kScanRowsPerWarp + rho;  // row within the CTA's block
     const int j = part * kScanRows + rl;         // state row (v index)
     float *grow = state + ((static_cast<size_t>(slot) * n_v_heads + vh) * S + j) * S;
     float row[8][E];
@@ -283,6 +291,10 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, (E >= 8 ? 2 : 4)) recur
         const float *qs = ks + L::kFloats;
         const float *vs = qs + L::kFloats;
         const int tc = min(TC, n_tokens - c * TC);
+        // unrolled by 3: a warp issues in order, and this lets it start the next tokens'
+        // products while a token's readout is still in its shuffles (deeper unrolling
+        // spills at this register budget)
+#pragma unroll 3
         for (int t = 0; t < tc; ++t) {
             // the row step of the decode kernels, in the group layout
             const float decay = __shfl_sync(FULL_MASK, dec_cur, t);
@@ -351,9 +363,9 @@ gdn_status launch_scan(float *state, const float *q, const float *k, const float
     constexpr int S = 32 * E;
     const size_t smem = ScanSmem<E>::bytes;
     GDN_TRY(set_smem(recurrence_scan_kernel<E, SNAP>, smem));
-    const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / kScanRows);
+    const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / ScanSmem<E>::kRows);
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-    recurrence_scan_kernel<E, SNAP><<<static_cast<unsigned>(blocks), (kScanWarps + 1) * 32, smem, s>>>(
+    recurrence_scan_kernel<E, SNAP><<<static_cast<unsigned>(blocks), ScanSmem<E>::kThreads, smem, s>>>(
         state, q, k, v, g, beta, y, n_tokens, n_k_heads, n_v_heads, scale, slots, pool,
         err_count, snaps);
     return launch_status();
