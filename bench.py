@@ -3,7 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload batched_decode_64|single_seq_decode_1000|
                                 serving_pool_256_of_512|prefill_scan_4x4096|
-                                prefill_chunked_4x4096|prefill_block_4x4096]
+                                prefill_chunked_4x4096|prefill_block_4x4096|
+                                spec_verify_64x4]
 
 Default workload: batched decode, 64 independent sequences, one token each per
 step (Hk=16, H=32, S=128, conv 4), through the fused gdn_block_decode kernel.
@@ -40,7 +41,12 @@ from gated_deltanet_linear_scan_gb300 import inputs as I  # noqa: E402
 METRIC = "GDN decode tokens/s and state HBM GB/s (fraction of GB300 peak), 1 GPU"
 WORKLOADS = {"batched_decode_64": 3, "single_seq_decode_1000": 1,
              "serving_pool_256_of_512": 4, "prefill_scan_4x4096": 2,
-             "prefill_chunked_4x4096": 2, "prefill_block_4x4096": 2}
+             "prefill_chunked_4x4096": 2, "prefill_block_4x4096": 2,
+             "spec_verify_64x4": 3}
+# Workloads that take a configuration with fields replaced: speculative-decoding
+# verification scores 4 draft tokens of each of the 64 batched-decode sequences.
+OVERRIDES = {"spec_verify_64x4": {"n_tokens": 4}}
+SPEC_TOKENS = 4
 # TF32 tensor-core rate relative to bf16 (nominal dense figures, 1.1 / 2.25 PFLOP/s)
 TF32_PER_BF16 = 1.1 / 2.25
 
@@ -269,9 +275,11 @@ def cpu_sample_scan(cfg, tokens, budget_s):
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
-    units = cfg.n_seqs * cfg.n_v_heads
-    # tokens of the full workload per second = tokens per unit-second / units
-    return reps * tokens / dt / units, reps, dt
+    # A token of the workload is one position of one sequence, which the oracle
+    # advances through all n_v_heads units of that sequence: one core runs the
+    # workload at (unit tokens per second) / n_v_heads tokens per second, for any
+    # number of sequences.
+    return reps * tokens / dt / cfg.n_v_heads, reps, dt
 
 
 # ------------------------------------------------------------------ reference arm
@@ -279,7 +287,20 @@ def cpu_sample_scan(cfg, tokens, budget_s):
 def run_reference(args, cfg, rank, world):
     if rank != 0:
         return 0
-    if args.workload in ("prefill_scan_4x4096", "prefill_chunked_4x4096"):
+    if args.workload == "spec_verify_64x4":
+        vals = []
+        for _ in range(args.warmup):
+            cpu_sample_scan(cfg, SPEC_TOKENS, 0.0)
+        for _ in range(args.steps):
+            v, _, _ = cpu_sample_scan(cfg, SPEC_TOKENS, 0.2)
+            vals.append(v)
+        value = statistics.mean(vals)
+        sample = (f"one (sequence, v-head) unit's {SPEC_TOKENS} tokens, repeated for 0.2 s per "
+                  f"step, scaled to the {cfg.n_v_heads} v-heads of a token (the oracle's scan; "
+                  "it keeps no snapshots)")
+        ms = 1e3 * cfg.n_seqs * SPEC_TOKENS / value
+        unit = "tokens/s"
+    elif args.workload in ("prefill_scan_4x4096", "prefill_chunked_4x4096"):
         tokens = 256
         vals = []
         t_all = time.perf_counter()
@@ -290,7 +311,7 @@ def run_reference(args, cfg, rank, world):
             vals.append(v)
         value = statistics.mean(vals)
         sample = (f"one (sequence, v-head) unit of the 4x4096 scan, {tokens} tokens per step, "
-                  "scaled to the 128 units")
+                  f"scaled to the {cfg.n_v_heads} v-heads of a token")
         ms = 1e3 * cfg.n_seqs * cfg.n_tokens / value
         unit = "tokens/s"
     else:
@@ -342,6 +363,8 @@ def run_ours(args, cfg, rank, world, local_rank):
 
     if args.workload == "prefill_block_4x4096":
         return run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
+    if args.workload == "spec_verify_64x4":
+        return run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
     if cfg.cid == 2:
         return run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
 
@@ -426,6 +449,25 @@ def run_ours(args, cfg, rank, world, local_rank):
                        "state_gbs": state_b / rec_s / 1e9,
                        "hbm_gbs": rec_bytes / rec_s / 1e9,
                        "hbm_frac_of_peak": rec_bytes / rec_s / 1e9 / pk["hbm_gbs"]}
+
+    # ---- the same with the factorised readout (gdn_recurrence_decode_2pass)
+    tp_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush()
+        a = r_steps[i % n_distinct]
+        tp_ev[i][0].record(stream)
+        gdn.gdn_recurrence_decode_2pass(state, a["q"], a["k"], a["v"], a["g"], a["beta"], y_rec,
+                                        N, cfg.n_k_heads, H, S, cfg.scale, slots=d_slots,
+                                        pool=pool)
+        tp_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    tp_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in tp_ev) / 1e3, dist,
+                      "cuda") / args.steps
+    recurrence_only["two_pass"] = {"kernel": "gdn_recurrence_decode_2pass",
+                                   "us_per_step": 1e6 * tp_s,
+                                   "hbm_gbs": rec_bytes / tp_s / 1e9,
+                                   "hbm_frac_of_peak": rec_bytes / tp_s / 1e9 / pk["hbm_gbs"]}
 
     # ---- end to end: pinned host inputs -> device, the C-ABI call, output -> host.
     # A step's inputs (qkv, alpha, b, z) are packed in one pinned host buffer and
@@ -639,7 +681,7 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         v_cpu, reps, dt = cpu_sample_scan(cfg, 256, args.cpu_budget)
         cpu = {"value": v_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"one (sequence, v-head) unit, 256 tokens x {reps} reps ({dt:.1f} s), "
-                         "scaled to the 128 units; plain C float build, 1 thread"}
+                         f"scaled to the {H} v-heads of a token; plain C float build, 1 thread"}
     line = {
         "metric": METRIC, "value": tokens / total_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per,
@@ -657,6 +699,110 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": (2 if chunked else 1) * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
+    """Speculative-decoding verification: the delta-rule scan over 4 draft tokens of each
+    of 64 sequences, keeping the state after every token (gdn_recurrence_scan_snapshots),
+    so the caller can roll back to the last accepted token. HBM-bound: the state is read
+    and written once and written again as a snapshot after every token."""
+    import torch
+    import gated_deltanet_linear_scan_gb300 as gdn
+    stream = torch.cuda.current_stream()
+    N, T, H, Hk, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.n_k_heads, cfg.state_size
+    seqs = rank_work(cfg, rank)["seqs"]
+    x = I.recurrence_batch(cfg, seqs=seqs)
+    d = {k: dev(v) for k, v in x.items()}
+    state0 = dev(I.state_pool(cfg, which=seqs))
+    state = state0.clone()
+    y = torch.empty(N, T, H, S, device="cuda")
+    snaps = torch.empty(N, T, H, S, S, device="cuda")
+
+    def launch():
+        gdn.gdn_recurrence_scan_snapshots(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y,
+                                          snaps, N, T, Hk, H, S, cfg.scale)
+
+    for _ in range(args.warmup):
+        state.copy_(state0)
+        flush()
+        launch()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        for i in range(args.steps):
+            state.copy_(state0)
+            flush()
+            ev[i][0].record(stream)
+            launch()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    gdn.gdn_device_error()
+    total_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, dist, "cuda")
+    per = total_s / args.steps
+    tokens = world * N * T * args.steps
+    # algorithmic bytes of one launch: the state read and written once, a snapshot per
+    # token, and the per-token activations (q, k per k-head; v, y per v-head; g, beta)
+    state_bytes = N * H * (2 + T) * S * S * 4
+    alg_bytes = state_bytes + N * T * (2 * Hk * S + 2 * H * S + 2 * H) * 4
+    achieved = alg_bytes / per / 1e9
+
+    # ---- end to end: q, k, v, g, beta from pinned host memory, the call, y back (the
+    # snapshots stay on the device, where a rollback reads them)
+    keys = ["q", "k", "v", "g", "beta"]
+    h_in = {key: torch.from_numpy(np.ascontiguousarray(x[key])).pin_memory() for key in keys}
+    h_y = torch.empty(N, T, H, S).pin_memory()
+    h2d = sum(h_in[key].numel() for key in keys) * 4
+    d2h = h_y.numel() * 4
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        state.copy_(state0)
+        flush()
+        e2e_ev[i][0].record(stream)
+        for key in keys:
+            d[key].copy_(h_in[key], non_blocking=True)
+        launch()
+        h_y.copy_(y, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
+    clk = clocks.summary()
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1:
+        v_cpu, reps, dt = cpu_sample_scan(cfg, T, args.cpu_budget)
+        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"one (sequence, v-head) unit's {T} tokens x {reps} reps ({dt:.1f} s), "
+                         f"scaled to the {H} v-heads of a token; the oracle's scan keeps no "
+                         "snapshots; plain C float build, 1 thread"}
+    line = {
+        "metric": METRIC, "value": tokens / total_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded PCG64; unit q/k, g~U(-2,-0.01))",
+        "config": {"workload": args.workload, "n_seqs": N, "n_tokens": T, "n_k_heads": Hk,
+                   "n_v_heads": H, "state_size": S,
+                   "kernel": "gdn_recurrence_scan_snapshots (state after every token)",
+                   "l2": L2_NOTE, "snapshot_bytes": snaps.numel() * 4,
+                   "algorithmic_bytes_per_step": alg_bytes,
+                   "state_gbs": state_bytes / per / 1e9},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": ncu_traffic("recurrence_scan_kernel", args.workload),
+                     "kernel": "recurrence_scan_kernel<4, true>",
+                     "peak_source": f"hbm_gbs ({pk_kind})"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -816,7 +962,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = I.get_config(WORKLOADS[args.workload])
+    cfg = I.get_config(WORKLOADS[args.workload], **OVERRIDES.get(args.workload, {}))
     if args.impl == "reference":
         return run_reference(args, cfg, rank, world)
     if world > 1:
