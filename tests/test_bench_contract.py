@@ -35,6 +35,19 @@ def test_reference_arm_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
 
 
+def test_reference_arm_speculative_verify():
+    """The speculative-verification workload's reference arm: the oracle's scan over the
+    same 4 tokens, scaled to a token's v-heads."""
+    res = run_bench("--impl", "reference", "--workload", "spec_verify_64x4", "--steps", "1",
+                    "--warmup", "3")
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["config"]["workload"] == "spec_verify_64x4"
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"]
+
+
 def test_gpu_arm_fails_loudly_without_a_gpu():
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
