@@ -342,6 +342,37 @@ def test_recurrence_scan_snapshots(lib, S, T):
     assert torch.equal(y_r, y_full[:, M:]) and torch.equal(st_r, st_full)
 
 
+@pytest.mark.slow
+def test_recurrence_scan_snapshots_speculative_verify_size(lib):
+    """The speculative-verification workload at full size (64 sequences x 4 draft tokens,
+    Hk=16, H=32, S=128, the launch the bench times): the last snapshot is the final state
+    bit for bit, and sampled (sequence, v-head) units match the oracle token by token in
+    y and in every snapshot."""
+    cfg = I.get_config(3, n_tokens=4)
+    N, T, Hk, H, S = cfg.n_seqs, cfg.n_tokens, cfg.n_k_heads, cfg.n_v_heads, cfg.state_size
+    x = I.recurrence_batch(cfg)
+    st0 = I.state_pool(cfg)
+    st = dev(st0)
+    y = torch.zeros(N, T, H, S, device="cuda")
+    snaps = torch.zeros(N, T, H, S, S, device="cuda")
+    lib.gdn_recurrence_scan_snapshots(st, dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["g"]),
+                                      dev(x["beta"]), y, snaps, N, T, Hk, H, S, cfg.scale)
+    assert torch.equal(snaps[:, T - 1], st)
+    for n, vh in ((0, 0), (17, 5), (40, 22), (63, 31)):
+        kh = vh % Hk
+        unit = {"q": x["q"][n:n + 1, :, kh:kh + 1], "k": x["k"][n:n + 1, :, kh:kh + 1],
+                "v": x["v"][n:n + 1, :, vh:vh + 1], "g": x["g"][n:n + 1, :, vh:vh + 1],
+                "beta": x["beta"][n:n + 1, :, vh:vh + 1]}
+        got_y = host(y[n, :, vh])
+        got_s = host(snaps[n, :, vh])
+        for t in range(T):
+            s_ref = f64(st0[n:n + 1, vh:vh + 1])
+            y_ref, _ = oracle.recurrence(s_ref, scale=cfg.scale,
+                                         **{k_: v_[:, :t + 1] for k_, v_ in unit.items()})
+            assert_step(got_y[t], y_ref[0, t, 0], f"y ({n},{vh}) token {t}")
+            assert_step(got_s[t], s_ref[0, 0], f"snapshot ({n},{vh}) token {t}")
+
+
 @pytest.mark.parametrize("T", [9, 130])
 def test_conv1d_silu_seq_snapshots(lib, T):
     r = np.random.default_rng(105)
