@@ -753,6 +753,24 @@ def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     alg_bytes = state_bytes + N * T * (2 * Hk * S + 2 * H * S + 2 * H) * 4
     achieved = alg_bytes / per / 1e9
 
+    # ---- the rollback that follows a verification (gdn_snapshot_restore), timed the same
+    # way: every sequence back to a seeded accepted count in [1, T]
+    acc = torch.from_numpy(np.random.default_rng(cfg.seed).integers(1, T + 1, N)
+                           .astype(np.int32)).cuda()
+    rs_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush()
+        rs_ev[i][0].record(stream)
+        gdn.gdn_snapshot_restore(state, snaps, acc, N, T, H, S)
+        rs_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    gdn.gdn_device_error()
+    rs_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in rs_ev) / 1e3, dist, "cuda") / args.steps
+    rs_bytes = 2 * N * H * S * S * 4
+    restore = {"kernel": "gdn_snapshot_restore", "us_per_call": 1e6 * rs_s,
+               "hbm_gbs": rs_bytes / rs_s / 1e9, "hbm_frac_of_peak": rs_bytes / rs_s / 1e9 / pk["hbm_gbs"]}
+
     # ---- end to end: q, k, v, g, beta from pinned host memory, the call, y back (the
     # snapshots stay on the device, where a rollback reads them)
     keys = ["q", "k", "v", "g", "beta"]
@@ -793,7 +811,7 @@ def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                    "kernel": "gdn_recurrence_scan_snapshots (state after every token)",
                    "l2": L2_NOTE, "snapshot_bytes": snaps.numel() * 4,
                    "algorithmic_bytes_per_step": alg_bytes,
-                   "state_gbs": state_bytes / per / 1e9},
+                   "state_gbs": state_bytes / per / 1e9, "restore": restore},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                      "traffic": ncu_traffic("recurrence_scan_kernel", args.workload),

@@ -20,7 +20,8 @@ __all__ = [
     "gdn_decay_gate", "gdn_beta_sigmoid", "gdn_conv1d_silu", "gdn_conv1d_silu_seq",
     "gdn_qkv_split_norm", "gdn_recurrence_decode", "gdn_recurrence_scan", "gdn_gated_norm",
     "gdn_block_decode", "gdn_recurrence_decode_2pass", "gdn_recurrence_scan_snapshots",
-    "gdn_conv1d_silu_seq_snapshots", "gdn_block_prefill_workspace_size", "gdn_block_prefill",
+    "gdn_conv1d_silu_seq_snapshots", "gdn_snapshot_restore",
+    "gdn_block_prefill_workspace_size", "gdn_block_prefill",
     "gdn_block_prefill_noalloc", "PREFILL_NOALLOC_SCRATCH_BYTES",
     "gdn_recurrence_scan_chunked", "gdn_block_prefill_chunked",
     "gdn_recurrence_scan_chunked_ws_size", "gdn_recurrence_scan_chunked_ws",
@@ -58,6 +59,7 @@ _SIGS = {
     "gdn_recurrence_decode_2pass": ([_P] * 7 + [_I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
     "gdn_recurrence_scan_snapshots": ([_P] * 8 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
     "gdn_conv1d_silu_seq_snapshots": ([_P] * 5 + [_I, _I, _I, _I, _P, _I, _P, _P], _I),
+    "gdn_snapshot_restore": ([_P] * 5 + [_I] * 6 + [_P, _I, _P, _P], _I),
     "gdn_block_prefill_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
     "gdn_block_prefill": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P, _P,
                                        ctypes.c_size_t, _P], _I),
@@ -329,6 +331,21 @@ def gdn_conv1d_silu_seq_snapshots(qkv, w, conv_state, out, snaps, n_seqs, n_toke
     _check("gdn_conv1d_silu_seq_snapshots", library().gdn_conv1d_silu_seq_snapshots(
         _ptr(qkv, "qkv"), _ptr(w, "w"), _ptr(conv_state, "conv_state"), _ptr(out, "out"),
         _ptr(snaps, "snaps"), n_seqs, n_tokens, conv_dim, conv_kernel, _slots(slots), pool,
+        _errc(err_count), _stream(stream)))
+
+
+def gdn_snapshot_restore(state, snaps, accepted, n_seqs, n_tokens, n_v_heads, state_size,
+                         conv_state=None, conv_snaps=None, conv_dim=0, conv_kernel=0,
+                         slots=None, pool=None, err_count=None, stream=None):
+    """Roll each sequence back to the snapshot after its accepted[n]-th position (int32
+    CUDA tensor of n_seqs counts in [1, n_tokens]); the conv history too when conv_state
+    and conv_snaps are given."""
+    import torch
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_snapshot_restore", library().gdn_snapshot_restore(
+        _ptr(state, "state"), _ptr(snaps, "snaps"), _ptr(conv_state, "conv_state", optional=True),
+        _ptr(conv_snaps, "conv_snaps", optional=True), _ptr(accepted, "accepted", torch.int32),
+        n_seqs, n_tokens, n_v_heads, state_size, conv_dim, conv_kernel, _slots(slots), pool,
         _errc(err_count), _stream(stream)))
 
 

@@ -223,6 +223,53 @@ gdn_status conv_common(const float *qkv, const float *w, float *conv_state, floa
     }
 }
 
+
+// ---------------------------------------------------------------- snapshot restore
+// Rollback after a speculative verification: sequence n (grid row n) copies the
+// snapshot taken after its accepted[n]-th position into its state slot and, if given,
+// its conv slot. The first `state_parts` CTAs of a row copy the state (16-byte
+// vectors, kRestoreVec4 per CTA), the rest the conv history (single floats, whose
+// count need not be a multiple of 4). A row whose accepted count or slot is out of
+// range copies nothing and is counted once.
+constexpr int kRestoreVec4 = kThreads * 8;   // float4 per CTA of the state copy (32 KiB)
+constexpr int kRestoreConv = kThreads * 16;  // floats per CTA of the conv copy
+
+__global__ void __launch_bounds__(kThreads) snapshot_restore_kernel(
+    float *state, const float *__restrict__ snaps, float *conv_state,
+    const float *__restrict__ conv_snaps, const int32_t *__restrict__ accepted, int n_tokens,
+    size_t state_floats, size_t conv_floats, int state_parts, const int32_t *__restrict__ slots,
+    int pool, int32_t *err_count) {
+    const int n = blockIdx.y, part = blockIdx.x;
+    const int slot = slots ? slots[n] : n;
+    const int m = accepted[n];
+    if (slot < 0 || slot >= pool || m < 1 || m > n_tokens) {  // uniform over the row
+        if (err_count && part == 0 && threadIdx.x == 0) atomicAdd(err_count, 1);
+        return;
+    }
+    const size_t snap = static_cast<size_t>(n) * n_tokens + (m - 1);  // snapshot index
+    if (part < state_parts) {
+        // all 8 loads of a thread in flight before its stores
+        const float4 *src = reinterpret_cast<const float4 *>(snaps + snap * state_floats);
+        float4 *dst = reinterpret_cast<float4 *>(state + static_cast<size_t>(slot) * state_floats);
+        const size_t n4 = state_floats / 4, i0 = static_cast<size_t>(part) * kRestoreVec4 + threadIdx.x;
+        float4 v[kRestoreVec4 / kThreads];
+#pragma unroll
+        for (int j = 0; j < kRestoreVec4 / kThreads; ++j)
+            if (i0 + j * kThreads < n4) v[j] = src[i0 + j * kThreads];
+#pragma unroll
+        for (int j = 0; j < kRestoreVec4 / kThreads; ++j)
+            if (i0 + j * kThreads < n4) dst[i0 + j * kThreads] = v[j];
+    } else {
+        const float *src = conv_snaps + snap * conv_floats;
+        float *dst = conv_state + static_cast<size_t>(slot) * conv_floats;
+        const size_t end = min(conv_floats, static_cast<size_t>(part - state_parts + 1) * kRestoreConv);
+#pragma unroll 4
+        for (size_t i = static_cast<size_t>(part - state_parts) * kRestoreConv + threadIdx.x; i < end;
+             i += kThreads)
+            dst[i] = src[i];
+    }
+}
+
 }  // namespace
 
 gdn_status launch_gated_norm(const float *y, const float *w, const float *z, float *out,
@@ -310,6 +357,34 @@ gdn_status gdn_conv1d_silu_seq_snapshots(const float *qkv, const float *w, float
     if (!snaps) return GDN_ERR_NULL;
     return conv_common(qkv, w, conv_state, out, n_seqs, n_tokens, conv_dim, conv_kernel, slots,
                        pool, err_count, snaps, stream);
+}
+
+gdn_status gdn_snapshot_restore(float *state, const float *snaps, float *conv_state,
+                                const float *conv_snaps, const int32_t *accepted, int n_seqs,
+                                int n_tokens, int n_v_heads, int state_size, int conv_dim,
+                                int conv_kernel, const int32_t *slots, int pool,
+                                int32_t *err_count, gdn_stream_t stream) {
+    if (!state || !snaps || !accepted) return GDN_ERR_NULL;
+    const bool conv = conv_state || conv_snaps;
+    if (conv && !(conv_state && conv_snaps)) return GDN_ERR_NULL;
+    if (n_seqs < 0 || n_tokens < 1 || n_v_heads < 1) return GDN_ERR_SHAPE;
+    if (state_size < 32 || state_size % 32 != 0 || state_size > 256) return GDN_ERR_SHAPE;
+    if (!supported_state_size(state_size)) return GDN_ERR_UNSUPPORTED;  // as the snapshot scan
+    if (conv && (conv_dim < 1 || conv_kernel < 2 || conv_kernel > 8)) return GDN_ERR_SHAPE;
+    GDN_TRY(check_pool(n_seqs, slots, pool));
+    if (!aligned16(state) || !aligned16(snaps)) return GDN_ERR_ALIGN;
+    if (n_seqs == 0) return GDN_OK;
+    if (n_seqs > 65535) return GDN_ERR_UNSUPPORTED;
+    const size_t state_floats = static_cast<size_t>(n_v_heads) * state_size * state_size;
+    const size_t conv_floats = conv ? static_cast<size_t>(conv_dim) * (conv_kernel - 1) : 0;
+    const long long state_parts = static_cast<long long>((state_floats / 4 + kRestoreVec4 - 1) / kRestoreVec4);
+    const long long conv_parts = static_cast<long long>((conv_floats + kRestoreConv - 1) / kRestoreConv);
+    if (state_parts + conv_parts > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    const dim3 grid(static_cast<unsigned>(state_parts + conv_parts), static_cast<unsigned>(n_seqs));
+    snapshot_restore_kernel<<<grid, kThreads, 0, as_cuda(stream)>>>(
+        state, snaps, conv_state, conv_snaps, accepted, n_tokens, state_floats, conv_floats,
+        static_cast<int>(state_parts), slots, pool, err_count);
+    return launch_status();
 }
 
 gdn_status gdn_qkv_split_norm(const float *conv_out, float *q, float *k, float *v, int rows,

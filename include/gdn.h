@@ -254,6 +254,24 @@ gdn_status gdn_conv1d_silu_seq_snapshots(const float *qkv, const float *w, float
                                          int conv_dim, int conv_kernel, const int32_t *slots,
                                          int pool, int32_t *err_count, gdn_stream_t stream);
 
+/* Speculative-decoding rollback for a batch in one launch: the restore the two
+ * snapshot scans above exist for (ssm_gated_delta.cu, fc_ssm_recurrence_seq and
+ * fc_ssm_conv1d_silu_seq: after a partial accept of M positions the state after M is
+ * snaps[M-1], one contiguous copy). For sequence n, with M = accepted[n]:
+ * state slot slots[n] (n when slots is NULL) <- snaps[n][M-1] (n_v_heads*S*S floats,
+ * the layouts of gdn_recurrence_scan_snapshots), and, when conv_state and conv_snaps
+ * are both given, its conv slot <- conv_snaps[n][M-1] (conv_dim*(K-1) floats, the
+ * layouts of gdn_conv1d_silu_seq_snapshots; both NULL skips the conv history, one NULL
+ * is GDN_ERR_NULL). accepted: device int32[n_seqs]; M must lie in [1, n_tokens] (the
+ * first verified position is always kept; M = n_tokens leaves the scans' final state).
+ * A sequence whose M or slot is out of range is left untouched and counted once in the
+ * optional err_count. state and snaps 16-byte aligned; copies only, no arithmetic. */
+gdn_status gdn_snapshot_restore(float *state, const float *snaps, float *conv_state,
+                                const float *conv_snaps, const int32_t *accepted, int n_seqs,
+                                int n_tokens, int n_v_heads, int state_size, int conv_dim,
+                                int conv_kernel, const int32_t *slots, int pool,
+                                int32_t *err_count, gdn_stream_t stream);
+
 /* Gated RMSNorm. fm_kernel_ssm.m, "Gated RMSNorm"; ssm_gated_delta.cu, Kernel 3.
  *   out[r][d] = y[r][d] / sqrt(mean_d(y[r]^2) + eps) * w[d] * silu(z[r][d])
  * y, z, out: [rows][head_dim]; w: [head_dim], the one weight shared by all heads.

@@ -100,6 +100,23 @@ def test_conv_validation(lib):
     assert fs(P, P, P, P, 1, 0, 256, 4, None, 1, None, None) == OK
 
 
+
+def test_snapshot_restore_validation(lib):
+    f = lib.gdn_snapshot_restore
+    # state, snaps, conv_state, conv_snaps, accepted, N, T, H, S, conv_dim, K, slots, pool, err
+    assert f(None, P, None, None, P, 1, 4, 4, 128, 0, 0, None, 1, None, None) == NULL
+    assert f(P, P, None, None, None, 1, 4, 4, 128, 0, 0, None, 1, None, None) == NULL
+    assert f(P, P, P, None, P, 1, 4, 4, 128, 256, 4, None, 1, None, None) == NULL  # one conv buffer
+    assert f(P, P, None, None, P, 1, 0, 4, 128, 0, 0, None, 1, None, None) == SHAPE
+    assert f(P, P, None, None, P, 1, 4, 0, 128, 0, 0, None, 1, None, None) == SHAPE
+    assert f(P, P, None, None, P, 1, 4, 4, 100, 0, 0, None, 1, None, None) == SHAPE
+    assert f(P, P, None, None, P, 1, 4, 4, 96, 0, 0, None, 1, None, None) == UNSUP
+    assert f(P, P, P, P, P, 1, 4, 4, 128, 256, 1, None, 1, None, None) == SHAPE
+    assert f(P, P, None, None, P, 2, 4, 4, 128, 0, 0, None, 1, None, None) == SHAPE  # pool < N
+    assert f(MIS, P, None, None, P, 1, 4, 4, 128, 0, 0, None, 1, None, None) == ALIGN
+    assert f(P, MIS, None, None, P, 1, 4, 4, 128, 0, 0, None, 1, None, None) == ALIGN
+    assert f(P, P, P, P, P, 0, 4, 4, 128, 256, 4, None, 1, None, None) == OK  # nothing to do
+
 def test_elementwise_validation(lib):
     assert lib.gdn_decay_gate(P, P, None, P, 4, 2, None) == NULL
     assert lib.gdn_decay_gate(P, P, P, P, 0, 2, None) == SHAPE

@@ -342,6 +342,58 @@ def test_recurrence_scan_snapshots(lib, S, T):
     assert torch.equal(y_r, y_full[:, M:]) and torch.equal(st_r, st_full)
 
 
+def test_snapshot_restore(lib):
+    """Rollback after a verification scan: restoring each sequence to the snapshots after
+    its accepted count equals scanning (and conv-scanning) only that prefix, bit for bit;
+    slots route; an out-of-range count leaves its slots as the scans left them and is
+    counted once; slots no sequence uses keep their bits."""
+    S, T, C, K = 128, 9, 256, 4
+    cfg, x, pool0 = rec_case(2, 4, S, N=4, T=T, seed=77, pool=6)
+    N, H, Hk = cfg.n_seqs, cfg.n_v_heads, cfg.n_k_heads
+    slots = np.array([5, 0, 3, 2], dtype=np.int32)
+    accepted = np.array([1, T, 4, 0], dtype=np.int32)
+    r = np.random.default_rng(78)
+    qkv = r.normal(0, 1, (N, T, C)).astype(np.float32)
+    w = r.normal(0, 0.5, (C, K)).astype(np.float32)
+    cs0 = r.normal(0, 1, (6, C, K - 1)).astype(np.float32)
+    d_slots = dev(slots)
+    st, cs = dev(pool0), dev(cs0)
+    y = torch.zeros(N, T, H, S, device="cuda")
+    snaps = torch.zeros(N, T, H, S, S, device="cuda")
+    lib.gdn_recurrence_scan_snapshots(st, dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["g"]),
+                                      dev(x["beta"]), y, snaps, N, T, Hk, H, S, cfg.scale,
+                                      slots=d_slots, pool=6)
+    out = torch.zeros(N, T, C, device="cuda")
+    csnaps = torch.zeros(N, T, C, K - 1, device="cuda")
+    lib.gdn_conv1d_silu_seq_snapshots(dev(qkv), dev(w), cs, out, csnaps, N, T, C, K,
+                                      slots=d_slots, pool=6)
+    after_st, after_cs = host(st), host(cs)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.gdn_snapshot_restore(st, snaps, dev(accepted), N, T, H, S, conv_state=cs,
+                             conv_snaps=csnaps, conv_dim=C, conv_kernel=K, slots=d_slots,
+                             pool=6, err_count=err)
+    assert host(err)[0] == 1
+    got_st, got_cs = host(st), host(cs)
+    for n in range(N):
+        sl, m = slots[n], accepted[n]
+        if not 1 <= m <= T:
+            np.testing.assert_array_equal(got_st[sl], after_st[sl])
+            np.testing.assert_array_equal(got_cs[sl], after_cs[sl])
+            continue
+        st_ref = dev(pool0[sl:sl + 1])
+        lib.gdn_recurrence_scan(st_ref, *(dev(x[k_][n:n + 1, :m]) for k_ in
+                                          ("q", "k", "v", "g", "beta")),
+                                torch.zeros(1, m, H, S, device="cuda"), 1, m, Hk, H, S, cfg.scale)
+        np.testing.assert_array_equal(got_st[sl], host(st_ref)[0], f"state of sequence {n}")
+        cs_ref = dev(cs0[sl:sl + 1])
+        lib.gdn_conv1d_silu_seq(dev(qkv[n:n + 1, :m]), dev(w), cs_ref,
+                                torch.zeros(1, m, C, device="cuda"), 1, m, C, K)
+        np.testing.assert_array_equal(got_cs[sl], host(cs_ref)[0], f"conv of sequence {n}")
+    for sl in (1, 4):  # no sequence uses these slots
+        np.testing.assert_array_equal(got_st[sl], pool0[sl])
+        np.testing.assert_array_equal(got_cs[sl], cs0[sl])
+
+
 @pytest.mark.slow
 def test_recurrence_scan_snapshots_speculative_verify_size(lib):
     """The speculative-verification workload at full size (64 sequences x 4 draft tokens,
