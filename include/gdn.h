@@ -79,8 +79,9 @@ int gdn_version(void);
  * GDN_ERR_LAUNCH if the synchronisation itself reported a CUDA error. */
 gdn_status gdn_device_error(gdn_stream_t stream);
 
-/* Decay gate. fm_kernel_ssm.m, "Decay gate: g[r][h] = a[h] * softplus(alpha[r][h] +
- * dt[h])"; ssm_gated_delta.cu, glue kernels (fc_ssm_decay_gate, _nx).
+/* Decay gate. fm_kernel_ssm.m, decay-gate section; ssm_gated_delta.cu, glue kernels
+ * (fc_ssm_decay_gate, _nx). Per row r and head h the log-decay is a[h] times the
+ * softplus of alpha[r][h] + dt[h], softplus taken as the identity above 20:
  *   g[r][h] = a[h] * softplus(alpha[r][h] + dt[h]),  softplus(v) = v > 20 ? v : log1p(exp(v))
  * alpha, g: [rows][n_heads]; dt, a: [n_heads] (a = -exp(A_log), baked by the caller).
  * g may alias alpha. rows == 0 is a no-op. */
@@ -111,8 +112,9 @@ gdn_status gdn_conv1d_silu_seq(const float *qkv, const float *w, float *conv_sta
                                gdn_stream_t stream);
 
 /* Split a conv output row [q | k | v] and L2-normalise q and k per k-head.
- * ssm_gated_delta.cu, glue kernels (fc_ssm_qknorm_gqa_nx: "x / max(sqrt(sum x^2),
- * eps)", v a plain copy). No GQA copy is made: the recurrence maps v-head vh to
+ * ssm_gated_delta.cu, glue kernels (fc_ssm_qknorm_gqa_nx): each head vector is divided
+ * by the larger of its Euclidean norm and eps; v is copied unchanged. No GQA copy is
+ * made: the recurrence maps v-head vh to
  * k-head vh % n_k_heads itself.
  * conv_out: [rows][C]; q, k: [rows][Hk][S]; v: [rows][H][S]. No aliasing. */
 gdn_status gdn_qkv_split_norm(const float *conv_out, float *q, float *k, float *v, int rows,
@@ -155,9 +157,9 @@ gdn_status gdn_recurrence_scan(float *state, const float *q, const float *k, con
                                gdn_stream_t stream);
 
 /* The scan, also writing the state after every position, for speculative
- * decoding: ssm_gated_delta.cu, fc_ssm_recurrence_seq's `snaps` ("snaps[t] = the
- * full recurrent state AFTER position t's update ... a partial accept of M
- * positions restores state-after-M with one contiguous copy of snaps[M-1]").
+ * decoding: ssm_gated_delta.cu, fc_ssm_recurrence_seq's `snaps` argument. snaps[t]
+ * holds the whole recurrent state once position t has been applied, so rolling back
+ * to the first M verified positions is a single copy of snaps[M-1].
  * snaps: [n_seqs][n_tokens][H][S][S] (the state layout of one slot per position,
  * sequence n in call order), 16-byte aligned, NULL is an error. Otherwise as
  * gdn_recurrence_scan, whose results it reproduces bit for bit. */
@@ -255,9 +257,9 @@ gdn_status gdn_conv1d_silu_seq_snapshots(const float *qkv, const float *w, float
                                          int pool, int32_t *err_count, gdn_stream_t stream);
 
 /* Speculative-decoding rollback for a batch in one launch: the restore the two
- * snapshot scans above exist for (ssm_gated_delta.cu, fc_ssm_recurrence_seq and
- * fc_ssm_conv1d_silu_seq: after a partial accept of M positions the state after M is
- * snaps[M-1], one contiguous copy). For sequence n, with M = accepted[n]:
+ * snapshot scans above exist for (ssm_gated_delta.cu, the `snaps` arguments of
+ * fc_ssm_recurrence_seq and fc_ssm_conv1d_silu_seq). Each sequence keeps its own
+ * number of verified positions. For sequence n, with M = accepted[n]:
  * state slot slots[n] (n when slots is NULL) <- snaps[n][M-1] (n_v_heads*S*S floats,
  * the layouts of gdn_recurrence_scan_snapshots), and, when conv_state and conv_snaps
  * are both given, its conv slot <- conv_snaps[n][M-1] (conv_dim*(K-1) floats, the

@@ -31,9 +31,9 @@
 
 int gdn_ref_precision(void) { return (int)(sizeof(gdn_real) / sizeof(float)); }
 
-/* Softplus with the overflow guard at 20: [fm] "softplus(v) = log(1 + exp(v)),
- * guarded at 20" and [cu] fc_ssm_decay_gate ("softplus(v) = v>20 ? v :
- * log1p(exp(v))"). Above 20 the correction log1p(exp(-v)) is below 2.1e-9. */
+/* Softplus, log(1 + e^v), taken as v itself above 20: both pages guard it there
+ * ([fm] decay-gate section, [cu] fc_ssm_decay_gate). Above 20 the dropped term
+ * log1p(exp(-v)) is below 2.1e-9. */
 gdn_real gdn_ref_softplus(gdn_real v) {
     if (v > (gdn_real)20) return v;
     return R_LOG1P(R_EXP(v));
@@ -42,7 +42,7 @@ gdn_real gdn_ref_softplus(gdn_real v) {
 /* SiLU in the divisor form both pages use: [fm] fmssm_silu, [cu] fc_ssm_silu. */
 gdn_real gdn_ref_silu(gdn_real x) { return x / ((gdn_real)1 + R_EXP(-x)); }
 
-/* Decay gate, [fm] "Decay gate: g[r][h] = a[h] * softplus(alpha[r][h] + dt[h])";
+/* Decay gate, [fm] decay-gate section: g = a * softplus(alpha + dt) per row and head;
  * dt and a are per head, broadcast over rows. a = -exp(A_log) is baked by the
  * caller ([cu] "Glue" section, fc_ssm_decay_gate). */
 void gdn_ref_decay_gate(const gdn_real *alpha, const gdn_real *dt, const gdn_real *a,
@@ -54,7 +54,7 @@ void gdn_ref_decay_gate(const gdn_real *alpha, const gdn_real *dt, const gdn_rea
         }
 }
 
-/* beta = sigmoid(b), [cu] fc_sigmoid ("x = 1/(1+exp(-x))"). */
+/* beta = sigmoid(b) = 1 / (1 + e^-b), [cu] fc_sigmoid. */
 void gdn_ref_sigmoid(const gdn_real *b, gdn_real *beta, int n) {
     for (int i = 0; i < n; i++) beta[i] = (gdn_real)1 / ((gdn_real)1 + R_EXP(-b[i]));
 }
@@ -94,8 +94,9 @@ int gdn_ref_conv1d_silu_seq(const gdn_real *qkv, const gdn_real *w, gdn_real *co
     return skipped;
 }
 
-/* L2-norm of one head vector, [cu] fc_ssm_qknorm_gqa ("x / max(sqrt(sum
- * x^2), eps)"). Applied to q and k after conv+SiLU, never to v. */
+/* L2-norm of one head vector, [cu] fc_ssm_qknorm_gqa: the vector divided by the
+ * larger of its Euclidean norm and eps. Applied to q and k after conv+SiLU, never
+ * to v. */
 void gdn_ref_l2norm(const gdn_real *x, gdn_real *out, int rows, int dim, gdn_real eps) {
     for (int r = 0; r < rows; r++) {
         const gdn_real *xr = x + (size_t)r * dim;
