@@ -226,7 +226,7 @@ def run_scan(lib, cfg, x, st, lo, hi, slots=None, pool=None, err=None):
 
 
 @pytest.mark.parametrize("Hk,H,S,T", [(2, 4, 32, 16), (2, 4, 128, 37), (1, 2, 64, 5),
-                                      (2, 4, 256, 33)])
+                                      (2, 4, 256, 33), (1, 2, 64, 50)])
 def test_recurrence_scan(lib, Hk, H, S, T):
     cfg, x, st0 = rec_case(Hk, H, S, N=2, T=T, seed=T + S)
     st = dev(st0)
@@ -313,7 +313,7 @@ def test_recurrence_decode_2pass(lib, Hk, H, S):
     assert_step(host(y_a), host(y_b), "y plain vs 2-pass")
 
 
-@pytest.mark.parametrize("S,T", [(128, 37), (32, 16)])
+@pytest.mark.parametrize("S,T", [(128, 37), (32, 16), (64, 20), (256, 7)])
 def test_recurrence_scan_snapshots(lib, S, T):
     """snaps[t] is the state after token t: equal bit for bit to t+1 decode calls,
     and restoring snaps[M-1] then scanning the rest reproduces the full scan."""
