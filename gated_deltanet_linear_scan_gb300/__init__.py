@@ -21,7 +21,7 @@ __all__ = [
     "gdn_qkv_split_norm", "gdn_recurrence_decode", "gdn_recurrence_scan", "gdn_gated_norm",
     "gdn_block_decode", "gdn_recurrence_decode_2pass", "gdn_recurrence_scan_snapshots",
     "gdn_conv1d_silu_seq_snapshots", "gdn_snapshot_restore",
-    "gdn_block_prefill_workspace_size", "gdn_block_prefill",
+    "gdn_block_prefill_workspace_size", "gdn_block_prefill", "gdn_block_prefill_snapshots",
     "gdn_block_prefill_noalloc", "PREFILL_NOALLOC_SCRATCH_BYTES",
     "gdn_recurrence_scan_chunked", "gdn_block_prefill_chunked",
     "gdn_recurrence_scan_chunked_ws_size", "gdn_recurrence_scan_chunked_ws",
@@ -65,6 +65,8 @@ _SIGS = {
                                        ctypes.c_size_t, _P], _I),
     "gdn_block_prefill_noalloc": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P,
                                                _P], _I),
+    "gdn_block_prefill_snapshots": ([_P] * 13 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P,
+                                                 _P, ctypes.c_size_t, _P], _I),
     "gdn_recurrence_scan_chunked": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P], _I),
     "gdn_recurrence_scan_chunked_ws_size": ([_I, _I, _I, _I], ctypes.c_size_t),
     "gdn_recurrence_scan_chunked_ws": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P,
@@ -380,6 +382,23 @@ def gdn_block_prefill(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state
     _block_prefill("gdn_block_prefill", qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w,
                    state, out, n_seqs, n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel,
                    scale, l2_eps, norm_eps, workspace, slots, pool, err_count, stream)
+
+
+def gdn_block_prefill_snapshots(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,
+                                snaps, conv_snaps, n_seqs, n_tokens, n_k_heads, n_v_heads,
+                                state_size, conv_kernel, scale, l2_eps, norm_eps, workspace,
+                                slots=None, pool=None, err_count=None, stream=None):
+    """gdn_block_prefill keeping the state and the conv history after every position
+    (snaps [n][t][H][S][S], conv_snaps [n][t][C][K-1]) for speculative-decoding rollback."""
+    pool = _pool(pool, n_seqs, slots)
+    _ws_check(workspace)
+    _check("gdn_block_prefill_snapshots", library().gdn_block_prefill_snapshots(
+        _ptr(qkv, "qkv"), _ptr(conv_w, "conv_w"), _ptr(conv_state, "conv_state"),
+        _ptr(alpha, "alpha"), _ptr(b, "b"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(z, "z"),
+        _ptr(norm_w, "norm_w"), _ptr(state, "state"), _ptr(out, "out"), _ptr(snaps, "snaps"),
+        _ptr(conv_snaps, "conv_snaps"), n_seqs, n_tokens, n_k_heads, n_v_heads, state_size,
+        conv_kernel, scale, l2_eps, norm_eps, _slots(slots), pool, _errc(err_count),
+        _ws_ptr(workspace), _ws_bytes(workspace), _stream(stream)))
 
 
 def gdn_block_prefill_chunked(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,

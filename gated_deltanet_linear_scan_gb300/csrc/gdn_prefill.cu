@@ -155,6 +155,29 @@ gdn_status launch_conv_split_norm(int conv_kernel, const float *qkv, const float
     }
 }
 
+
+// The conv history after every position, for speculative-decoding rollback: the K-1
+// raw inputs ending at position t, oldest first (snaps [n][t][C][K-1], the conv_state
+// layout of one slot per position), positions before the call read from the old
+// conv_state. Runs before the conv pass rolls conv_state; copies only.
+constexpr int kHistThreads = 256;
+
+__global__ void __launch_bounds__(kHistThreads) conv_history_snapshots_kernel(
+    const float *__restrict__ qkv, const float *__restrict__ conv_state,
+    float *__restrict__ snaps, int n_tokens, int conv_dim, int taps,
+    const int32_t *__restrict__ slots, int pool) {
+    const int c = blockIdx.x * kHistThreads + threadIdx.x, t = blockIdx.y, n = blockIdx.z;
+    const int slot = slots ? slots[n] : n;
+    if (c >= conv_dim || slot < 0 || slot >= pool) return;  // a skipped sequence is counted by the conv pass
+    const size_t row = static_cast<size_t>(n) * n_tokens;
+    float *dst = snaps + ((row + t) * conv_dim + c) * taps;
+    for (int j = 0; j < taps; ++j) {
+        const int pos = t - (taps - 1) + j;
+        dst[j] = pos >= 0 ? qkv[(row + pos) * conv_dim + c]
+                          : conv_state[(static_cast<size_t>(slot) * conv_dim + c) * taps + taps + pos];
+    }
+}
+
 }  // namespace
 }  // namespace gdn
 
@@ -190,10 +213,12 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
                         int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int state_size,
                         int conv_kernel, float scale, float l2_eps, float norm_eps,
                         const int32_t *slots, int pool, int32_t *err_count, void *workspace,
-                        size_t workspace_bytes, gdn_stream_t stream, bool chunked) {
+                        size_t workspace_bytes, gdn_stream_t stream, bool chunked,
+                        float *snaps = nullptr, float *conv_snaps = nullptr) {
     if (!qkv || !conv_w || !conv_state || !alpha || !b || !dt || !a || !z || !norm_w || !state ||
         !out)
         return GDN_ERR_NULL;
+    const bool snapshots = snaps != nullptr;  // the snapshot form passes both, non-NULL
     if (n_seqs < 0 || n_tokens < 0) return GDN_ERR_SHAPE;
     if (conv_kernel < 2 || conv_kernel > 8) return GDN_ERR_SHAPE;
     GDN_TRY(check_heads(n_k_heads, n_v_heads, state_size));
@@ -214,10 +239,18 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
     float *q = ws + L.q, *k = ws + L.k, *v = ws + L.v;
     float *g = ws + L.g, *beta = ws + L.beta;
     if ((n_tokens + 31) / 32 > 65535 || n_seqs > 65535) return GDN_ERR_UNSUPPORTED;
+    if (snapshots && n_tokens > 65535) return GDN_ERR_UNSUPPORTED;  // positions on grid.y
 
     // A skipped sequence is counted once, by the conv pass; nothing of it is written
     // to conv_state, state or out.
     const cudaStream_t cs = as_cuda(stream);
+    if (snapshots) {
+        const int C = (2 * Hk + H) * S;
+        const dim3 grid((C + kHistThreads - 1) / kHistThreads, n_tokens, n_seqs);
+        conv_history_snapshots_kernel<<<grid, kHistThreads, 0, cs>>>(
+            qkv, conv_state, conv_snaps, n_tokens, C, conv_kernel - 1, slots, pool);
+        GDN_TRY(launch_status());
+    }
     switch (S) {
         case 32: GDN_TRY(launch_conv_split_norm<1>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
         case 64: GDN_TRY(launch_conv_split_norm<2>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
@@ -239,6 +272,10 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
             GDN_TRY(gdn_recurrence_scan_chunked(state, q, k, v, g, beta, out, n_seqs, n_tokens,
                                                 Hk, H, S, scale, slots, pool, nullptr, stream));
         }
+    } else if (snapshots) {
+        GDN_TRY(gdn_recurrence_scan_snapshots(state, q, k, v, g, beta, out, snaps, n_seqs,
+                                              n_tokens, Hk, H, S, scale, slots, pool, nullptr,
+                                              stream));
     } else {
         GDN_TRY(gdn_recurrence_scan(state, q, k, v, g, beta, out, n_seqs, n_tokens, Hk, H, S,
                                     scale, slots, pool, nullptr, stream));
@@ -261,6 +298,24 @@ gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_
     return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
                         n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
                         norm_eps, slots, pool, err_count, workspace, workspace_bytes, stream, false);
+}
+
+gdn_status gdn_block_prefill_snapshots(const float *qkv, const float *conv_w,
+                                       float *conv_state, const float *alpha, const float *b,
+                                       const float *dt, const float *a, const float *z,
+                                       const float *norm_w, float *state, float *out,
+                                       float *snaps, float *conv_snaps, int n_seqs,
+                                       int n_tokens, int n_k_heads, int n_v_heads,
+                                       int state_size, int conv_kernel, float scale,
+                                       float l2_eps, float norm_eps, const int32_t *slots,
+                                       int pool, int32_t *err_count, void *workspace,
+                                       size_t workspace_bytes, gdn_stream_t stream) {
+    if (!snaps || !conv_snaps) return GDN_ERR_NULL;
+    if (!aligned16(snaps)) return GDN_ERR_ALIGN;
+    return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                        n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                        norm_eps, slots, pool, err_count, workspace, workspace_bytes, stream, false,
+                        snaps, conv_snaps);
 }
 
 gdn_status gdn_block_prefill_chunked(const float *qkv, const float *conv_w, float *conv_state,

@@ -322,6 +322,26 @@ gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_
                              float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
                              void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/* The prefill block over draft positions for speculative decoding: gdn_block_prefill
+ * (same arguments, workspace and results, bit for bit) that also keeps, for every
+ * position t, the recurrent state after t in snaps [n_seqs][n_tokens][H][S][S] (as
+ * gdn_recurrence_scan_snapshots) and the conv history after t in conv_snaps
+ * [n_seqs][n_tokens][C][K-1] (as gdn_conv1d_silu_seq_snapshots), C = (2 Hk + H) S.
+ * ssm_gated_delta.cu, the `snaps` arguments of fc_ssm_recurrence_seq and
+ * fc_ssm_conv1d_silu_seq. After verification, gdn_snapshot_restore rolls each
+ * sequence back to its accepted count. snaps 16-byte aligned; NULL snaps or
+ * conv_snaps is GDN_ERR_NULL; n_tokens above 65535 is GDN_ERR_UNSUPPORTED. */
+gdn_status gdn_block_prefill_snapshots(const float *qkv, const float *conv_w,
+                                       float *conv_state, const float *alpha, const float *b,
+                                       const float *dt, const float *a, const float *z,
+                                       const float *norm_w, float *state, float *out,
+                                       float *snaps, float *conv_snaps, int n_seqs,
+                                       int n_tokens, int n_k_heads, int n_v_heads,
+                                       int state_size, int conv_kernel, float scale,
+                                       float l2_eps, float norm_eps, const int32_t *slots,
+                                       int pool, int32_t *err_count, void *workspace,
+                                       size_t workspace_bytes, gdn_stream_t stream);
+
 /* gdn_block_prefill with the chunked tensor-core scan in place of the sequential
  * one: the production path for long prefill. Same arguments, layouts, workspace and
  * error behaviour; state_size must be 128 (else GDN_ERR_UNSUPPORTED). Results agree

@@ -180,6 +180,16 @@ def test_prefill_validation(lib):
     assert call(workspace=MIS) == ALIGN
     assert call(K=9) == SHAPE
     assert call(n_tokens=0, workspace=None) == OK
+    fs = lib.gdn_block_prefill_snapshots  # + snaps, conv_snaps after out
+
+    def call_s(snaps=P, conv_snaps=P, n_tokens=16, workspace=P):
+        return fs(P, P, P, P, P, P, P, P, P, P, P, snaps, conv_snaps, 2, n_tokens, 2, 4, 32, 4,
+                  0.1, 1e-6, 1e-6, None, 2, None, workspace, ws(2, n_tokens, 2, 4, 32), None)
+    assert call_s(snaps=None) == NULL
+    assert call_s(conv_snaps=None) == NULL
+    assert call_s(snaps=MIS) == ALIGN
+    assert call_s(n_tokens=70000) == UNSUP  # positions beyond a grid dimension
+    assert call_s(n_tokens=0, workspace=None) == OK
 
 
 def test_chunked_scan_validation(lib):

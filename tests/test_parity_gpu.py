@@ -701,6 +701,50 @@ def test_block_prefill(lib, Hk, H, S, N, T):
         assert_step(got[:, t], host(o), f"prefill vs decode, token {t}")
 
 
+def test_block_prefill_snapshots(lib):
+    """The prefill block keeping snapshots: out, state and conv history are gdn_block_prefill's
+    bit for bit; snaps[t] and conv_snaps[t] are the state and conv history the block leaves
+    after the first t + 1 positions (bit for bit); slots route; gdn_snapshot_restore then
+    rolls every sequence back to its own accepted count."""
+    cfg = I.get_config(0, n_k_heads=2, n_v_heads=4, state_size=128, n_seqs=3, pool=5, cid=905)
+    N, Hk, H, S, K, T = 3, 2, 4, 128, cfg.conv_kernel, 7
+    C = (2 * Hk + H) * S
+    steps = [I.block_step(cfg, t) for t in range(T)]
+    st0, cs0 = I.state_pool(cfg), I.conv_state_pool(cfg)
+    slots = dev(np.array([4, 0, 2], dtype=np.int32))
+    # without snapshots
+    state_r, conv_r = dev(st0), dev(cs0)
+    out_r, stack = run_prefill(lib, cfg, T, steps, state_r, conv_r, slots=slots, pool=5)
+    # with them
+    stat = {k_: dev(v_) for k_, v_ in I.block_static(cfg).items()}
+    state, conv = dev(st0), dev(cs0)
+    out = torch.zeros(N, T, H, S, device="cuda")
+    snaps = torch.zeros(N, T, H, S, S, device="cuda")
+    csnaps = torch.zeros(N, T, C, K - 1, device="cuda")
+    ws = torch.empty(lib.gdn_block_prefill_workspace_size(N, T, Hk, H, S) // 4, device="cuda")
+    lib.gdn_block_prefill_snapshots(dev(stack["qkv"]), stat["conv_w"], conv, dev(stack["alpha"]),
+                                    dev(stack["b"]), stat["dt"], stat["a"], dev(stack["z"]),
+                                    stat["norm_w"], state, out, snaps, csnaps, N, T, Hk, H, S, K,
+                                    cfg.scale, cfg.eps, cfg.eps, ws, slots=slots, pool=5)
+    assert torch.equal(out, out_r) and torch.equal(state, state_r) and torch.equal(conv, conv_r)
+    sl = [4, 0, 2]
+    for t in range(T):
+        st_p, cs_p = dev(st0), dev(cs0)
+        run_prefill(lib, cfg, t + 1, steps[:t + 1], st_p, cs_p, slots=slots, pool=5)
+        for n in range(N):
+            assert torch.equal(snaps[n, t], st_p[sl[n]]), f"state snapshot {t}, sequence {n}"
+            assert torch.equal(csnaps[n, t], cs_p[sl[n]]), f"conv snapshot {t}, sequence {n}"
+    accepted = np.array([2, T, 5], dtype=np.int32)
+    lib.gdn_snapshot_restore(state, snaps, dev(accepted), N, T, H, S, conv_state=conv,
+                             conv_snaps=csnaps, conv_dim=C, conv_kernel=K, slots=slots, pool=5)
+    for n in range(N):
+        assert torch.equal(state[sl[n]], snaps[n, accepted[n] - 1])
+        assert torch.equal(conv[sl[n]], csnaps[n, accepted[n] - 1])
+    for s_ in (1, 3):  # slots no sequence uses
+        np.testing.assert_array_equal(host(state)[s_], st0[s_])
+        np.testing.assert_array_equal(host(conv)[s_], cs0[s_])
+
+
 def test_block_prefill_invalid_slot(lib):
     cfg = I.get_config(0, n_seqs=3, pool=4, cid=800)
     T = 12
