@@ -267,7 +267,8 @@ gdn_status gdn_conv1d_silu_seq_snapshots(const float *qkv, const float *w, float
  * is GDN_ERR_NULL). accepted: device int32[n_seqs]; M must lie in [1, n_tokens] (the
  * first verified position is always kept; M = n_tokens leaves the scans' final state).
  * A sequence whose M or slot is out of range is left untouched and counted once in the
- * optional err_count. state and snaps 16-byte aligned; copies only, no arithmetic. */
+ * optional err_count. state_size as the snapshot scan (32, 64, 128 or 256), conv_kernel
+ * in [2, 8]. state and snaps 16-byte aligned; copies only, no arithmetic. */
 gdn_status gdn_snapshot_restore(float *state, const float *snaps, float *conv_state,
                                 const float *conv_snaps, const int32_t *accepted, int n_seqs,
                                 int n_tokens, int n_v_heads, int state_size, int conv_dim,
