@@ -115,6 +115,7 @@ def time_chunked_phases(gdn, torch, stream, state, state0, x, y, dims, scale, ws
     N, T, Hk, H, S = dims
     nc = (T + 31) // 32
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    gpu_head_start(torch)
     for i in range(steps):
         state.copy_(state0)
         flush()
@@ -132,17 +133,53 @@ def time_chunked_phases(gdn, torch, stream, state, state0, x, y, dims, scale, ws
 
 
 def ncu_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, if the kernel's source is unchanged since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    """DRAM bytes per launch of this kernel and workload from the machine-readable ncu
+    record (profiles/ncu_traffic.json, one entry per committed summary), if the
+    kernel's source is unchanged since the counters were taken; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
-    text = open(path).read()
-    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    m_s = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
-    if not (m_b and m_s) or m_s.group(1) != source_sha(KERNEL_SOURCES[kernel]):
+    with open(path) as f:
+        rec = json.load(f).get(f"{kernel}_{workload}")
+    if not rec or rec.get("source_sha256_16") != source_sha(KERNEL_SOURCES[kernel]):
         return None
-    return float(m_b.group(1))
+    return float(rec["dram_bytes_per_launch"])
+
+
+def gpu_head_start(torch):
+    """Give the device about a millisecond of work before the first timed step, so the
+    host enqueues the timed steps ahead of the device: no host latency lands between a
+    step's two events."""
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        sleep(4_000_000)
+
+
+def host_cpu():
+    """The host's logical CPU count and model name (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                model = line.split(":", 1)[1].strip()
+                break
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+def cpu_record(value, sample, cores=1):
+    """The cpu_baseline object: the oracle's rate with the host it ran on and its build."""
+    from oracle import build as oracle_build
+    return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample, **host_cpu(),
+            "oracle_build": "gcc " + " ".join(oracle_build.CFLAGS) + " (float build)"}
 
 
 class ClockSampler:
@@ -155,6 +192,11 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.t_mark = None
+
+    def mark(self):
+        """The timed region starts now: the summary keeps only later samples."""
+        self.t_mark = time.monotonic()
 
     def __enter__(self):
         try:
@@ -171,7 +213,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -184,7 +226,10 @@ class ClockSampler:
     def summary(self):
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        lines = [ln for t, ln in self.lines if self.t_mark is None or t >= self.t_mark]
+        if not lines and self.lines:  # a timed region shorter than one sampling period
+            lines = [self.lines[-1][1]]
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -200,6 +245,38 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def timed_steps(torch, stream, gpu, dist, warmup, steps, before, launch):
+    """`warmup` untimed steps, then exactly `steps` timed ones, each bracketed by CUDA
+    events on `stream` around launch(i) (before(i) -- the L2 flush, a state reset -- runs
+    outside the events), between a barrier and a synchronize on both sides. The clock
+    sampler starts before the warm-up, so no idle gap precedes the timed steps, and its
+    summary covers the timed steps only. Returns (per-step ms, clock summary, wall s)."""
+    with ClockSampler(gpu) as clocks:
+        for w in range(warmup):
+            before(w)
+            launch(w)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        clocks.mark()
+        t_wall = time.perf_counter()
+        gpu_head_start(torch)
+        for i in range(steps):
+            before(i)
+            ev[i][0].record(stream)
+            launch(i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev], clocks.summary(), t_wall
 
 
 # ------------------------------------------------------------------ ranks (weak scaling)
@@ -328,8 +405,7 @@ def run_reference(args, cfg, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "oracle": "plain C, float build, 1 thread"},
-        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": cpu_record(value, sample),
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -390,29 +466,10 @@ def run_ours(args, cfg, rank, world, local_rank):
                              cfg.conv_kernel, cfg.scale, cfg.eps, cfg.eps, slots=d_slots,
                              pool=pool)
 
-    for w in range(args.warmup):
-        flush()
-        launch(d_steps[w % n_distinct], out)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    t_wall = time.perf_counter()
-    with ClockSampler(local_rank) as clocks:
-        for i in range(args.steps):
-            flush()
-            ev[i][0].record(stream)
-            launch(d_steps[i % n_distinct], out)
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
+    kernel_ms, clk, t_wall = timed_steps(
+        torch, stream, local_rank, dist, args.warmup, args.steps, lambda i: flush(),
+        lambda i: launch(d_steps[i % n_distinct], out))
     gdn.gdn_device_error()
-    kernel_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     total_s = reduce_max(sum(kernel_ms) / 1e3, dist, "cuda")
     step_us = sorted(1e3 * t for t in kernel_ms)
     tokens = world * N * args.steps
@@ -436,6 +493,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         launch_rec(r_steps[w % n_distinct])
     rec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
+    gpu_head_start(torch)
     for i in range(args.steps):
         flush()
         rec_ev[i][0].record(stream)
@@ -453,6 +511,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     # ---- the same with the factorised readout (gdn_recurrence_decode_2pass)
     tp_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(args.steps)]
+    gpu_head_start(torch)
     for i in range(args.steps):
         flush()
         a = r_steps[i % n_distinct]
@@ -487,6 +546,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     d2h = h_out.numel() * 4
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
+    gpu_head_start(torch)
     for i in range(args.steps):
         flush()
         e2e_ev[i][0].record(stream)
@@ -529,9 +589,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     if world == 1:
         sample_seqs = list(range(min(4, N)))
         v_cpu, done, dt = cpu_sample_block(cfg, sample_seqs, 10 ** 6, args.cpu_budget)
-        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{len(sample_seqs)} of {N} sequences, {done} chained steps of the block "
-                         f"({dt:.1f} s), plain C float build, 1 thread"}
+        cpu = cpu_record(v_cpu, f"{len(sample_seqs)} of {N} sequences, {done} chained steps "
+                                f"of the block ({dt:.1f} s), plain C float build, 1 thread")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
@@ -559,7 +618,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clk,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -590,25 +649,14 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
             gdn.gdn_recurrence_scan(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y, N, T,
                                     Hk, H, S, cfg.scale)
 
-    for _ in range(args.warmup):
+    def before(i):
         state.copy_(state0)
         flush()
-        launch()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    with ClockSampler(torch.cuda.current_device()) as clocks:
-        for i in range(args.steps):
-            state.copy_(state0)
-            flush()
-            ev[i][0].record(stream)
-            launch()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
+
+    step_ms, clk, _ = timed_steps(torch, stream, torch.cuda.current_device(), dist,
+                                  args.warmup, args.steps, before, lambda i: launch())
     gdn.gdn_device_error()
-    total_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, dist, "cuda")
+    total_s = reduce_max(sum(step_ms) / 1e3, dist, "cuda")
     per = total_s / args.steps
     tokens = world * N * T * args.steps
 
@@ -620,6 +668,7 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     d2h = h_y.numel() * 4
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
+    gpu_head_start(torch)
     for i in range(args.steps):
         state.copy_(state0)
         flush()
@@ -633,7 +682,6 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
     flops = 7.0 * N * T * H * S * S
     props = torch.cuda.get_device_properties(0)
-    clk = clocks.summary()
     mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
     fp32_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
     achieved = flops / per / 1e12
@@ -645,6 +693,7 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                                             (N, T, Hk, H, S), cfg.scale, ws, args.steps, flush)
         one_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.steps)]
+        gpu_head_start(torch)
         for i in range(args.steps):
             state.copy_(state0)
             flush()
@@ -679,9 +728,9 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     cpu = None
     if world == 1:
         v_cpu, reps, dt = cpu_sample_scan(cfg, 256, args.cpu_budget)
-        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"one (sequence, v-head) unit, 256 tokens x {reps} reps ({dt:.1f} s), "
-                         f"scaled to the {H} v-heads of a token; plain C float build, 1 thread"}
+        cpu = cpu_record(v_cpu, f"one (sequence, v-head) unit, 256 tokens x {reps} reps "
+                                f"({dt:.1f} s), scaled to the {H} v-heads of a token; plain C "
+                                "float build, 1 thread")
     line = {
         "metric": METRIC, "value": tokens / total_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per,
@@ -726,25 +775,14 @@ def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         gdn.gdn_recurrence_scan_snapshots(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y,
                                           snaps, N, T, Hk, H, S, cfg.scale)
 
-    for _ in range(args.warmup):
+    def before(i):
         state.copy_(state0)
         flush()
-        launch()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    with ClockSampler(torch.cuda.current_device()) as clocks:
-        for i in range(args.steps):
-            state.copy_(state0)
-            flush()
-            ev[i][0].record(stream)
-            launch()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
+
+    step_ms, clk, _ = timed_steps(torch, stream, torch.cuda.current_device(), dist,
+                                  args.warmup, args.steps, before, lambda i: launch())
     gdn.gdn_device_error()
-    total_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, dist, "cuda")
+    total_s = reduce_max(sum(step_ms) / 1e3, dist, "cuda")
     per = total_s / args.steps
     tokens = world * N * T * args.steps
     # algorithmic bytes of one launch: the state read and written once, a snapshot per
@@ -759,6 +797,7 @@ def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                            .astype(np.int32)).cuda()
     rs_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(args.steps)]
+    gpu_head_start(torch)
     for i in range(args.steps):
         flush()
         rs_ev[i][0].record(stream)
@@ -780,6 +819,7 @@ def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     d2h = h_y.numel() * 4
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
+    gpu_head_start(torch)
     for i in range(args.steps):
         state.copy_(state0)
         flush()
@@ -791,16 +831,14 @@ def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
-    clk = clocks.summary()
     if rank != 0:
         return 0
     cpu = None
     if world == 1:
         v_cpu, reps, dt = cpu_sample_scan(cfg, T, args.cpu_budget)
-        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"one (sequence, v-head) unit's {T} tokens x {reps} reps ({dt:.1f} s), "
-                         f"scaled to the {H} v-heads of a token; the oracle's scan keeps no "
-                         "snapshots; plain C float build, 1 thread"}
+        cpu = cpu_record(v_cpu, f"one (sequence, v-head) unit's {T} tokens x {reps} reps "
+                                f"({dt:.1f} s), scaled to the {H} v-heads of a token; the "
+                                "oracle's scan keeps no snapshots; plain C float build, 1 thread")
     line = {
         "metric": METRIC, "value": tokens / total_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per,
@@ -853,25 +891,14 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         state.copy_(state0)
         conv.copy_(conv0)
 
-    for _ in range(args.warmup):
+    def before(i):
         reset()
         flush()
-        launch()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    with ClockSampler(torch.cuda.current_device()) as clocks:
-        for i in range(args.steps):
-            reset()
-            flush()
-            ev[i][0].record(stream)
-            launch()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
+
+    step_ms, clk, _ = timed_steps(torch, stream, torch.cuda.current_device(), dist,
+                                  args.warmup, args.steps, before, lambda i: launch())
     gdn.gdn_device_error()
-    total_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, dist, "cuda")
+    total_s = reduce_max(sum(step_ms) / 1e3, dist, "cuda")
     per_s = total_s / args.steps
     tokens = world * N * T * args.steps
 
@@ -907,6 +934,7 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     d2h = h_out.numel() * 4
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
+    gpu_head_start(torch)
     for i in range(args.steps):
         reset()
         flush()
@@ -923,7 +951,6 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     tf = chunked_tensor_flops(N, T, H)
     tf32_peak = pk.get("bf16_tflops", 1900.0) * TF32_PER_BF16
     props = torch.cuda.get_device_properties(0)
-    clk = clocks.summary()
     mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
     fp32_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
     if rank != 0:
@@ -931,10 +958,9 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     cpu = None
     if world == 1:
         v_cpu, done, dt = cpu_sample_block(cfg, [int(seqs[0])], 10 ** 6, args.cpu_budget)
-        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"1 of {N} sequences, {done} consecutive tokens through the block "
-                         f"({dt:.1f} s; per-token work is the same in every sequence), plain C "
-                         "float build, 1 thread"}
+        cpu = cpu_record(v_cpu, f"1 of {N} sequences, {done} consecutive tokens through the "
+                                f"block ({dt:.1f} s; per-token work is the same in every "
+                                "sequence), plain C float build, 1 thread")
     line = {
         "metric": METRIC, "value": tokens / total_s, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_s,
@@ -978,6 +1004,12 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        # one process per GPU: N > 1 needs a launcher that starts N ranks (torchrun)
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; run N > 1 as "
+              f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py "
+              f"--gpus {args.gpus} ...", file=sys.stderr)
+        return 2
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = I.get_config(WORKLOADS[args.workload], **OVERRIDES.get(args.workload, {}))

@@ -218,12 +218,11 @@ __global__ void __launch_bounds__(ScanSmem<E>::kThreads, ScanSmem<E>::kMinBlocks
 
     if (warp == kScanWarps) {
         // ---- producer warp: lane t copies token t of each chunk.
-        bool ok = true;
-        for (int c = 0; c < n_chunks && ok; ++c) {
+        int issued = 0;  // chunks whose copies were issued
+        for (int c = 0; c < n_chunks; ++c) {
             const int s = c % kScanDepth, use = c / kScanDepth;
             if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1)) {
                 if (lane == 0) atomicOr(&g_watchdog, WD_STAGE_FREE);
-                ok = false;
                 break;
             }
             const int tc = min(TC, n_tokens - c * TC);
@@ -241,12 +240,12 @@ __global__ void __launch_bounds__(ScanSmem<E>::kThreads, ScanSmem<E>::kMinBlocks
                 bulk_g2s(vs + lane * kScanRows, vbase + t * v_tok, kScanRows * sizeof(float),
                          full + s);
             }
+            issued = c + 1;
         }
-        // Do not leave while copies may still be landing in this CTA's shared memory.
-        if (ok && n_chunks > 0) {
-            for (int c = max(0, n_chunks - kScanDepth); c < n_chunks; ++c)
-                mbar_wait(full + c % kScanDepth, (c / kScanDepth) & 1);
-        }
+        // Do not leave while copies may still be landing in this CTA's shared memory,
+        // also when a wait above gave up (each of these waits is bounded too).
+        for (int c = max(0, issued - kScanDepth); c < issued; ++c)
+            mbar_wait(full + c % kScanDepth, (c / kScanDepth) & 1);
         return;
     }
 

@@ -76,7 +76,11 @@ int gdn_version(void);
 
 /* Synchronises `stream`, then reads and clears the device-side flag raised by
  * bounded waits that gave up. GDN_OK if none did, GDN_ERR_DEVICE otherwise, or
- * GDN_ERR_LAUNCH if the synchronisation itself reported a CUDA error. */
+ * GDN_ERR_LAUNCH if the synchronisation itself reported a CUDA error.
+ * The flag belongs to the library on the current device, not to a stream: it
+ * reports, and clears, give-ups of this library's kernels launched on any stream
+ * of the current device since the last call. Synchronise the other streams first
+ * if their kernels must be covered. */
 gdn_status gdn_device_error(gdn_stream_t stream);
 
 /* Decay gate. fm_kernel_ssm.m, decay-gate section; ssm_gated_delta.cu, glue kernels

@@ -55,3 +55,42 @@ def test_gpu_arm_fails_loudly_without_a_gpu():
     res = run_bench("--steps", "1", "--warmup", "3", timeout=300)
     assert res.returncode != 0
     assert not any(ln.lstrip().startswith("{") for ln in res.stdout.splitlines())
+
+
+def test_gpus_flag_without_a_launcher_fails_loudly():
+    """--gpus 2 in a single process (no torchrun, WORLD_SIZE unset) must not run as one
+    rank and report n_gpus 1."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                         timeout=300, cwd=ROOT, env=env)
+    assert res.returncode != 0
+    assert "WORLD_SIZE" in res.stderr
+    assert not any(ln.lstrip().startswith("{") for ln in res.stdout.splitlines())
+
+
+def test_cpu_baseline_names_the_host_and_the_oracle_build():
+    res = run_bench("--impl", "reference", "--steps", "1", "--warmup", "3")
+    assert res.returncode == 0, res.stderr[-2000:]
+    cb = json.loads(res.stdout.strip().splitlines()[-1])["cpu_baseline"]
+    assert cb["nproc"] == os.cpu_count() and cb["cores"] == 1
+    assert isinstance(cb["cpu_model"], str) and cb["cpu_model"]
+    assert "-ffp-contract=off" in cb["oracle_build"]
+
+
+def test_ncu_traffic_comes_from_the_json_record(monkeypatch):
+    """roofline.traffic is read from profiles/ncu_traffic.json, and only while the
+    kernel's source hash is the one recorded beside the counters."""
+    sys.path.insert(0, ROOT)
+    import bench
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        rec = json.load(f)
+    assert rec
+    for key, entry in rec.items():
+        assert os.path.exists(os.path.join(ROOT, "profiles", entry["summary"])), key
+        kernel = next(k for k in bench.KERNEL_SOURCES if key.startswith(k + "_"))
+        workload = key[len(kernel) + 1:]
+        monkeypatch.setattr(bench, "source_sha", lambda files, h=entry["source_sha256_16"]: h)
+        assert bench.ncu_traffic(kernel, workload) == float(entry["dram_bytes_per_launch"])
+        monkeypatch.setattr(bench, "source_sha", lambda files: "0" * 16)
+        assert bench.ncu_traffic(kernel, workload) is None

@@ -15,6 +15,7 @@ torch = pytest.importorskip("torch")
 
 import oracle  # noqa: E402
 from gated_deltanet_linear_scan_gb300 import inputs as I  # noqa: E402
+from tests.oracle_units import prefill_4x4096  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -118,7 +119,8 @@ def test_chunked_scan_slots(lib):
 @pytest.mark.slow
 def test_chunked_scan_prefill_4x4096(lib):
     """The prefill workload at full size (N=4, T=4096, Hk=16, H=32, S=128): every
-    output against the sequential GPU scan, sampled units against the oracle."""
+    output against the sequential GPU scan and every (sequence, v-head) unit against
+    the oracle, under the long-scan bound."""
     cfg = I.get_config(2)
     N, T, H, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.state_size
     x = I.recurrence_batch(cfg)
@@ -131,18 +133,11 @@ def test_chunked_scan_prefill_4x4096(lib):
     yh, sth = host(y_c), host(st_c)
     assert_rms(yh, host(y_s), "y vs sequential")
     assert_rms(sth, host(st_s), "state vs sequential")
-    for n, vh in ((0, 0), (1, 17), (3, 31), (2, 8)):
-        kh = vh % cfg.n_k_heads
-        unit = {key: x[key][n:n + 1] for key in x}
-        unit["q"] = unit["q"][:, :, kh:kh + 1]
-        unit["k"] = unit["k"][:, :, kh:kh + 1]
-        unit["v"] = unit["v"][:, :, vh:vh + 1]
-        unit["g"] = unit["g"][:, :, vh:vh + 1]
-        unit["beta"] = unit["beta"][:, :, vh:vh + 1]
-        s_ref = f64(st0[n:n + 1, vh:vh + 1])
-        y_ref, _ = oracle.recurrence(s_ref, scale=cfg.scale, **unit)
-        assert_rms(yh[n, :, vh], y_ref[0, :, 0], f"y ({n},{vh})")
-        assert_rms(sth[n, vh], s_ref[0, 0], f"final state ({n},{vh})")
+    _, _, _, refs = prefill_4x4096()
+    assert len(refs) == N * H
+    for (n, vh), (y_ref, s_ref) in refs.items():  # every unit against the oracle
+        assert_rms(yh[n, :, vh], y_ref, f"y ({n},{vh})")
+        assert_rms(sth[n, vh], s_ref, f"final state ({n},{vh})")
 
 
 # ------------------------------------------------------------------ prefill block

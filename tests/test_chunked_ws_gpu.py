@@ -15,6 +15,7 @@ torch = pytest.importorskip("torch")
 
 import oracle  # noqa: E402
 from gated_deltanet_linear_scan_gb300 import inputs as I  # noqa: E402
+from tests.oracle_units import prefill_4x4096  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -131,7 +132,7 @@ def test_ws_slots_counted_once(lib):
 @pytest.mark.slow
 def test_ws_prefill_4x4096(lib):
     """The prefill workload at full size: bit for bit the one-kernel form, in one wave
-    and in waves of 16 chunks; sampled units against the oracle."""
+    and in waves of 16 chunks; every (sequence, v-head) unit against the oracle."""
     cfg = I.get_config(2)
     N, T, H, S = cfg.n_seqs, cfg.n_tokens, cfg.n_v_heads, cfg.state_size
     x = I.recurrence_batch(cfg)
@@ -146,18 +147,11 @@ def test_ws_prefill_4x4096(lib):
     assert torch.equal(st_v, st_w)
     del y_f, y_v
     yh, sth = host(y_w), host(st_w)
-    for n, vh in ((0, 3), (2, 30)):
-        kh = vh % cfg.n_k_heads
-        unit = {key: x[key][n:n + 1] for key in x}
-        unit["q"] = unit["q"][:, :, kh:kh + 1]
-        unit["k"] = unit["k"][:, :, kh:kh + 1]
-        unit["v"] = unit["v"][:, :, vh:vh + 1]
-        unit["g"] = unit["g"][:, :, vh:vh + 1]
-        unit["beta"] = unit["beta"][:, :, vh:vh + 1]
-        s_ref = np.array(st0[n:n + 1, vh:vh + 1], dtype=np.float64)
-        y_ref, _ = oracle.recurrence(s_ref, scale=cfg.scale, **unit)
-        assert_rms(yh[n, :, vh], y_ref[0, :, 0], f"y ({n},{vh})")
-        assert_rms(sth[n, vh], s_ref[0, 0], f"final state ({n},{vh})")
+    _, _, _, refs = prefill_4x4096()
+    assert len(refs) == N * H
+    for (n, vh), (y_ref, s_ref) in refs.items():  # every unit against the oracle
+        assert_rms(yh[n, :, vh], y_ref, f"y ({n},{vh})")
+        assert_rms(sth[n, vh], s_ref, f"final state ({n},{vh})")
 
 
 def test_phases_equal_one_call(lib):

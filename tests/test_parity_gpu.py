@@ -14,6 +14,7 @@ import pytest
 
 import oracle
 from gated_deltanet_linear_scan_gb300 import inputs as I
+from tests.oracle_units import prefill_4x4096
 
 torch = pytest.importorskip("torch")
 
@@ -269,28 +270,18 @@ def test_recurrence_scan_slots(lib):
 
 @pytest.mark.slow
 def test_recurrence_scan_prefill_4x4096(lib):
-    """The long-scan workload at full size (N=4, T=4096, H=32, Hk=16, S=128),
-    checked on sampled (sequence, v-head) units against the oracle."""
-    cfg = I.get_config(2)
-    x = I.recurrence_batch(cfg)
-    st0 = I.state_pool(cfg)
+    """The long-scan workload at full size (N=4, T=4096, H=32, Hk=16, S=128), in the
+    launch the bench times: every (sequence, v-head) unit against the oracle, y and the
+    final state under the long-scan bound, the first token under the one-step bound."""
+    cfg, x, st0, refs = prefill_4x4096()
     st = dev(st0)
     y = run_scan(lib, cfg, x, st, 0, cfg.n_tokens)
     yh, sth = host(y), host(st)
-    assert np.all(np.isfinite(yh)) and np.all(np.isfinite(sth))
-    for n, vh in ((0, 0), (1, 17), (3, 31), (2, 8)):
-        kh = vh % cfg.n_k_heads
-        unit = {key: x[key][n:n + 1] for key in x}
-        unit["q"] = unit["q"][:, :, kh:kh + 1]
-        unit["k"] = unit["k"][:, :, kh:kh + 1]
-        unit["v"] = unit["v"][:, :, vh:vh + 1]
-        unit["g"] = unit["g"][:, :, vh:vh + 1]
-        unit["beta"] = unit["beta"][:, :, vh:vh + 1]
-        s_ref = f64(st0[n:n + 1, vh:vh + 1])
-        y_ref, _ = oracle.recurrence(s_ref, scale=cfg.scale, **unit)
-        assert_step(yh[n, :1, vh], y_ref[0, :1, 0], f"y token 0 ({n},{vh})")
-        assert_rms(yh[n, :, vh], y_ref[0, :, 0], f"y ({n},{vh})")
-        assert_rms(sth[n, vh], s_ref[0, 0], f"final state ({n},{vh})")
+    assert len(refs) == cfg.n_seqs * cfg.n_v_heads
+    for (n, vh), (y_ref, s_ref) in refs.items():
+        assert_step(yh[n, :1, vh], y_ref[:1], f"y token 0 ({n},{vh})")
+        assert_rms(yh[n, :, vh], y_ref, f"y ({n},{vh})")
+        assert_rms(sth[n, vh], s_ref, f"final state ({n},{vh})")
 
 
 @pytest.mark.parametrize("Hk,H,S", [(2, 4, 32), (16, 32, 128), (4, 16, 256), (1, 2, 64)])
@@ -497,15 +488,20 @@ class BlockRun:
 
 
 def check_block_chain(lib, cfg, sample, steps):
+    """Chained fused-block steps: after the first step out, state and conv_state of the
+    sampled sequences meet the one-step elementwise bound, after the last the long-chain
+    RMS bound."""
     run = BlockRun(lib, cfg, sample)
+    ids = [run.slot_of(n) for n in sample]
     for step in range(steps):
         out, ref = run.step(step)
         if step == 0:
             assert_step(out[sample], ref, "out, first step")
+            assert_step(host(run.state[ids]), run.ref_state, "state, first step")
+            assert_step(host(run.conv[ids]), run.ref_conv, "conv_state, first step")
     assert_rms(out[sample], ref, f"out after {steps} steps")
-    ids = [run.slot_of(n) for n in sample]
-    assert_rms(host(run.state)[ids], run.ref_state, f"state after {steps} steps")
-    assert_rms(host(run.conv)[ids], run.ref_conv, f"conv_state after {steps} steps")
+    assert_rms(host(run.state[ids]), run.ref_state, f"state after {steps} steps")
+    assert_rms(host(run.conv[ids]), run.ref_conv, f"conv_state after {steps} steps")
     assert host(run.err)[0] == 0
     return run
 
