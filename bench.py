@@ -42,7 +42,10 @@ METRIC = "GDN decode tokens/s and state HBM GB/s (fraction of GB300 peak), 1 GPU
 WORKLOADS = {"batched_decode_64": 3, "single_seq_decode_1000": 1,
              "serving_pool_256_of_512": 4, "prefill_scan_4x4096": 2,
              "prefill_chunked_4x4096": 2, "prefill_block_4x4096": 2,
-             "spec_verify_64x4": 3}
+             "spec_verify_64x4": 3, "prefill_varlen_16k": 2}
+# Ragged prefill: a seeded mix of lengths (log-uniform in [1, 4096]) adding up to the
+# 4 x 4096 workload's 16384 tokens, through the chunked prefill block in one call.
+VARLEN_TOKENS = 16384
 # Workloads that take a configuration with fields replaced: speculative-decoding
 # verification scores 4 draft tokens of each of the 64 batched-decode sequences.
 OVERRIDES = {"spec_verify_64x4": {"n_tokens": 4}}
@@ -58,6 +61,14 @@ def chunked_tensor_flops(n_seqs, n_tokens, n_v_heads):
     the U part of y, U^T [w K | M]^T in 3 passes (N = 160, K = 32)."""
     per = 2 * 128 * 128 * 128 + 2 * 128 * 64 * 128 + 3 * (2 * 128 * 160 * 32)
     return per * n_seqs * n_v_heads * ((n_tokens + 31) // 32)
+
+
+def chunked_method_flops(n_chunks_total, n_v_heads):
+    """The chunked scan's own contraction flops, without the 3xTF32 passes: per (sequence,
+    v-head, chunk) the S products S^T [Gam q | W] (M = 128, N = 64, K = 128) and the state
+    update with the U part of y, U^T [w K | M]^T (M = 128, N = 160, K = 32)."""
+    per = 2 * 128 * 64 * 128 + 2 * 128 * 160 * 32
+    return per * n_chunks_total * n_v_heads
 
 
 def chunk_prepare_flops(n_seqs, n_tokens, n_k_heads, n_v_heads):
@@ -441,6 +452,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         return run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
     if args.workload == "spec_verify_64x4":
         return run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
+    if args.workload == "prefill_varlen_16k":
+        return run_ours_varlen(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
     if cfg.cid == 2:
         return run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist)
 
@@ -706,14 +719,18 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         tf = chunked_tensor_flops(N, T, H)
         pf = chunk_prepare_flops(N, T, Hk, H)
         tf32_peak = pk["bf16_tflops"] * TF32_PER_BF16 if "bf16_tflops" in pk else 1900.0 * TF32_PER_BF16
+        mf = chunked_method_flops(N * ((T + 31) // 32), H)
         roofline = {"bound": "tensor", "kernel": "chunk_state_kernel (gdn_chunked_advance)",
-                    "achieved": tf / adv_s / 1e12, "peak": tf32_peak,
-                    "unit": "TFLOP/s", "frac": tf / adv_s / 1e12 / tf32_peak,
+                    "achieved": mf / adv_s / 1e12, "peak": tf32_peak,
+                    "unit": "TFLOP/s", "frac": mf / adv_s / 1e12 / tf32_peak,
                     "traffic": ncu_traffic("chunk_state_kernel", args.workload),
-                    "flops_per_launch": tf,
+                    "flops_per_launch": mf,
+                    "flops_note": "the method's own contraction flops (each product once); "
+                                  "the kernel issues 3 TF32 passes per product (3xTF32)",
                     "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
                                    f"{TF32_PER_BF16:.3f}"}
         extra = {"advance_ms": 1e3 * adv_s, "prepare_ms": 1e3 * prep_s,
+                 "advance_tensor_issued_tflops": tf / adv_s / 1e12,
                  "prepare_fp32_tflops": pf / prep_s / 1e12,
                  "prepare_frac_of_fp32_pipes": pf / prep_s / 1e12 / fp32_peak,
                  "one_kernel_form_ms": 1e3 * one_s,
@@ -948,7 +965,7 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
 
     flops = 7.0 * N * T * H * S * S
-    tf = chunked_tensor_flops(N, T, H)
+    mf = chunked_method_flops(N * ((T + 31) // 32), H)
     tf32_peak = pk.get("bf16_tflops", 1900.0) * TF32_PER_BF16
     props = torch.cuda.get_device_properties(0)
     mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
@@ -976,10 +993,135 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                    "method_fp32_tflops_of_scan": flops / (prep_s + adv_s) / 1e12,
                    "fp32_pipe_peak_tflops": fp32_peak},
         "roofline": {"bound": "tensor", "kernel": "chunk_state_kernel (gdn_chunked_advance)",
-                     "achieved": tf / adv_s / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
-                     "frac": tf / adv_s / 1e12 / tf32_peak,
+                     "achieved": mf / adv_s / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
+                     "frac": mf / adv_s / 1e12 / tf32_peak,
                      "traffic": ncu_traffic("chunk_state_kernel", "prefill_chunked_4x4096"),
-                     "flops_per_launch": tf,
+                     "flops_per_launch": mf,
+                     "flops_note": "the method's own contraction flops (each product once); "
+                                   "the kernel issues 3 TF32 passes per product (3xTF32)",
+                     "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
+                                    f"{TF32_PER_BF16:.3f}"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 6 * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_varlen(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
+    """A ragged prefill batch: sequences of mixed lengths (seeded, log-uniform in [1, 4096],
+    16384 tokens in all) packed token-major through gdn_block_prefill_chunked_varlen in one
+    call per step (conv + q/k split-norm, gate, beta, the two-phase chunked scan, gated
+    norm). The state and conv history of every sequence start fresh each step."""
+    import torch
+    import gated_deltanet_linear_scan_gb300 as gdn
+    stream = torch.cuda.current_stream()
+    H, Hk, S, K = cfg.n_v_heads, cfg.n_k_heads, cfg.state_size, cfg.conv_kernel
+    lengths = I.ragged_lengths(cfg, VARLEN_TOKENS)
+    N, total, maxt = len(lengths), sum(lengths), max(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    vcfg = I.get_config(2, n_seqs=N)
+    first = rank * N  # this rank's sequences: their own seeded streams
+    per = [I.prefill_seq(vcfg, first + n, n_tokens=L) for n, L in enumerate(lengths)]
+    d = {key: dev(np.concatenate([p_[key] for p_ in per])) for key in per[0]}
+    d_cu = dev(cu)
+    st = {k_: dev(v_) for k_, v_ in I.block_static(vcfg).items()}
+    state0 = dev(I.state_pool(vcfg, which=range(first, first + N)))
+    conv0 = dev(I.conv_state_pool(vcfg, which=range(first, first + N)))
+    state, conv = state0.clone(), conv0.clone()
+    out = torch.empty(total, H, S, device="cuda")
+    ws = torch.empty(gdn.gdn_block_prefill_chunked_varlen_workspace_size(N, total, Hk, H, S) // 4
+                     + 64, device="cuda")
+
+    def launch():
+        gdn.gdn_block_prefill_chunked_varlen(d["qkv"], st["conv_w"], conv, d["alpha"], d["b"],
+                                             st["dt"], st["a"], d["z"], st["norm_w"], state, out,
+                                             d_cu, N, total, maxt, Hk, H, S, K, cfg.scale,
+                                             cfg.eps, cfg.eps, ws)
+
+    def before(i):
+        state.copy_(state0)
+        conv.copy_(conv0)
+        flush()
+
+    step_ms, clk, _ = timed_steps(torch, stream, torch.cuda.current_device(), dist,
+                                  args.warmup, args.steps, before, lambda i: launch())
+    gdn.gdn_device_error()
+    total_s = reduce_max(sum(step_ms) / 1e3, dist, "cuda")
+    per_s = total_s / args.steps
+    tokens = world * total * args.steps
+
+    # ---- the chunked scan alone (both phases, the dominant part of the step) over the
+    # same lengths, on the recurrence inputs of the scan workloads (unit q, k): method
+    # flops per time
+    rx = [I.recurrence_seq(vcfg, first + n, n_tokens=L) for n, L in enumerate(lengths)]
+    rd = {key: dev(np.concatenate([p_[key] for p_ in rx])) for key in rx[0]}
+    q, k, v, g, beta = rd["q"], rd["k"], rd["v"], rd["g"], rd["beta"]
+    y = torch.empty_like(out)
+    scan_ws = torch.empty(gdn.gdn_recurrence_scan_chunked_varlen_ws_size(N, total, H, S) // 4,
+                          device="cuda")
+    scan_ms, _, _ = timed_steps(
+        torch, stream, torch.cuda.current_device(), dist, 3, args.steps, lambda i: before(i),
+        lambda i: gdn.gdn_recurrence_scan_chunked_varlen(state, q, k, v, g, beta, y, d_cu, N,
+                                                         total, maxt, Hk, H, S, cfg.scale,
+                                                         workspace=scan_ws))
+    scan_s = reduce_max(sum(scan_ms) / 1e3, dist, "cuda") / args.steps
+    del scan_ws
+    n_chunks = sum((L + 31) // 32 for L in lengths)
+    mflops = chunked_method_flops(n_chunks, H)
+    tf32_peak = pk.get("bf16_tflops", 1900.0) * TF32_PER_BF16
+
+    # ---- end to end: qkv, alpha, b, z and cu_seqlens from pinned host memory, the call,
+    # out back
+    keys = ["qkv", "alpha", "b", "z"]
+    h_in = {key: d[key].cpu().pin_memory() for key in keys}
+    h_cu = torch.from_numpy(cu).pin_memory()
+    h_out = torch.empty(total, H, S).pin_memory()
+    h2d = sum(h_in[key].numel() for key in keys) * 4 + h_cu.numel() * 4
+    d2h = h_out.numel() * 4
+
+    def e2e_launch(i):
+        for key in keys:
+            d[key].copy_(h_in[key], non_blocking=True)
+        d_cu.copy_(h_cu, non_blocking=True)
+        launch()
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_ms, _, _ = timed_steps(torch, stream, torch.cuda.current_device(), dist, 3, args.steps,
+                               before, e2e_launch)
+    e2e_s = reduce_max(sum(e2e_ms) / 1e3, dist, "cuda")
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1:
+        v_cpu, done, dt = cpu_sample_block(vcfg, [0], 10 ** 6, args.cpu_budget)
+        cpu = cpu_record(v_cpu, f"1 sequence, {done} consecutive tokens through the block "
+                                f"({dt:.1f} s; per-token work does not depend on the length), "
+                                "plain C float build, 1 thread")
+    line = {
+        "metric": METRIC, "value": tokens / total_s, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_s,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded PCG64; N(0,1) qkv/z, g~U(-0.5,-0.001); lengths "
+                "log-uniform in [1, 4096])",
+        "config": {"workload": args.workload, "n_seqs": N, "total_tokens": total,
+                   "max_tokens": maxt, "lengths": lengths, "n_k_heads": Hk, "n_v_heads": H,
+                   "state_size": S, "conv_kernel": K,
+                   "kernel": "gdn_block_prefill_chunked_varlen (6 launches: conv scan with the "
+                             "q/k split-norm, gate, beta, chunk preparation, tensor-core state "
+                             "advance, gated norm)", "l2": L2_NOTE,
+                   "workspace_bytes": ws.numel() * 4, "scan_ms": 1e3 * scan_s,
+                   "chunks": n_chunks},
+        "roofline": {"bound": "tensor",
+                     "kernel": "chunk_prepare_kernel + chunk_state_kernel "
+                               "(gdn_recurrence_scan_chunked_varlen, timed together)",
+                     "achieved": mflops / scan_s / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
+                     "frac": mflops / scan_s / 1e12 / tf32_peak, "traffic": None,
+                     "flops_per_launch": mflops,
+                     "flops_note": "the method's own contraction flops (each product once); "
+                                   "the kernels issue 3 TF32 passes per product (3xTF32)",
                      "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
                                     f"{TF32_PER_BF16:.3f}"},
         "cpu_baseline": cpu,

@@ -26,6 +26,11 @@ __all__ = [
     "gdn_recurrence_scan_chunked", "gdn_block_prefill_chunked",
     "gdn_recurrence_scan_chunked_ws_size", "gdn_recurrence_scan_chunked_ws",
     "gdn_chunked_prepare", "gdn_chunked_advance", "gdn_block_prefill_chunked_workspace_size",
+    "gdn_recurrence_scan_varlen", "gdn_recurrence_scan_chunked_varlen_ws_size",
+    "gdn_recurrence_scan_chunked_varlen", "gdn_block_prefill_varlen_workspace_size",
+    "gdn_block_prefill_chunked_varlen_workspace_size", "gdn_block_prefill_varlen",
+    "gdn_block_prefill_chunked_varlen", "gdn_block_prefill_snapshots_varlen",
+    "gdn_snapshot_restore_varlen",
 ]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
@@ -77,6 +82,19 @@ _SIGS = {
     "gdn_block_prefill_chunked_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
     "gdn_block_prefill_chunked": ([_P] * 11 + [_I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _P, _P,
                                                ctypes.c_size_t, _P], _I),
+    "gdn_recurrence_scan_varlen": ([_P] * 8 + [_I] * 6 + [_F, _P, _I, _P, _P], _I),
+    "gdn_recurrence_scan_chunked_varlen_ws_size": ([_I, _I, _I, _I], ctypes.c_size_t),
+    "gdn_recurrence_scan_chunked_varlen": ([_P] * 8 + [_I] * 6 + [_F, _P, _I, _P, _P,
+                                                                ctypes.c_size_t, _P], _I),
+    "gdn_block_prefill_varlen_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
+    "gdn_block_prefill_chunked_varlen_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
+    "gdn_block_prefill_varlen": ([_P] * 12 + [_I] * 7 + [_F, _F, _F, _P, _I, _P, _P,
+                                                       ctypes.c_size_t, _P], _I),
+    "gdn_block_prefill_chunked_varlen": ([_P] * 12 + [_I] * 7 + [_F, _F, _F, _P, _I, _P, _P,
+                                                               ctypes.c_size_t, _P], _I),
+    "gdn_block_prefill_snapshots_varlen": ([_P] * 14 + [_I] * 7 + [_F, _F, _F, _P, _I, _P, _P,
+                                                                 ctypes.c_size_t, _P], _I),
+    "gdn_snapshot_restore_varlen": ([_P] * 6 + [_I] * 7 + [_P, _I, _P, _P], _I),
 }
 
 # Size of the fixed device scratch of gdn_block_prefill_noalloc (include/gdn.h).
@@ -425,3 +443,125 @@ def gdn_block_prefill_noalloc(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_
         _ptr(norm_w, "norm_w"), _ptr(state, "state"), _ptr(out, "out"), n_seqs, n_tokens,
         n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps, norm_eps, _slots(slots),
         pool, _errc(err_count), _stream(stream)))
+
+
+# ------------------------------------------------------------------ ragged batches
+# Sequences of different lengths packed token-major ([total_tokens][...] arrays);
+# `cu_seqlens` is an int32 CUDA tensor of n_seqs + 1 offsets (sequence n owns positions
+# cu_seqlens[n] .. cu_seqlens[n+1] - 1), `max_tokens` an upper bound on one length.
+
+def _cu(cu_seqlens):
+    import torch
+    return _ptr(cu_seqlens, "cu_seqlens", torch.int32)
+
+
+def gdn_recurrence_scan_varlen(state, q, k, v, g, beta, y, cu_seqlens, n_seqs, total_tokens,
+                               max_tokens, n_k_heads, n_v_heads, state_size, scale, slots=None,
+                               pool=None, err_count=None, stream=None):
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_recurrence_scan_varlen", library().gdn_recurrence_scan_varlen(
+        _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
+        _ptr(beta, "beta"), _ptr(y, "y"), _cu(cu_seqlens), n_seqs, total_tokens, max_tokens,
+        n_k_heads, n_v_heads, state_size, scale, _slots(slots), pool, _errc(err_count),
+        _stream(stream)))
+
+
+def gdn_recurrence_scan_chunked_varlen_ws_size(n_seqs, total_tokens, n_v_heads, state_size):
+    return library().gdn_recurrence_scan_chunked_varlen_ws_size(n_seqs, total_tokens, n_v_heads,
+                                                                state_size)
+
+
+def gdn_recurrence_scan_chunked_varlen(state, q, k, v, g, beta, y, cu_seqlens, n_seqs,
+                                       total_tokens, max_tokens, n_k_heads, n_v_heads,
+                                       state_size, scale, workspace=None, slots=None, pool=None,
+                                       err_count=None, stream=None):
+    """`workspace` None: the one-kernel form; a CUDA tensor of at least
+    gdn_recurrence_scan_chunked_varlen_ws_size() bytes: the two-phase form."""
+    pool = _pool(pool, n_seqs, slots)
+    ws, nbytes = (None, 0) if workspace is None else (_ws_ptr(workspace), _ws_bytes(workspace))
+    _check("gdn_recurrence_scan_chunked_varlen", library().gdn_recurrence_scan_chunked_varlen(
+        _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
+        _ptr(beta, "beta"), _ptr(y, "y"), _cu(cu_seqlens), n_seqs, total_tokens, max_tokens,
+        n_k_heads, n_v_heads, state_size, scale, _slots(slots), pool, _errc(err_count), ws,
+        nbytes, _stream(stream)))
+
+
+def gdn_block_prefill_varlen_workspace_size(n_seqs, total_tokens, n_k_heads, n_v_heads,
+                                            state_size):
+    return library().gdn_block_prefill_varlen_workspace_size(n_seqs, total_tokens, n_k_heads,
+                                                             n_v_heads, state_size)
+
+
+def gdn_block_prefill_chunked_varlen_workspace_size(n_seqs, total_tokens, n_k_heads, n_v_heads,
+                                                    state_size):
+    return library().gdn_block_prefill_chunked_varlen_workspace_size(
+        n_seqs, total_tokens, n_k_heads, n_v_heads, state_size)
+
+
+def _block_prefill_varlen(name, qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,
+                          extra, cu_seqlens, n_seqs, total_tokens, max_tokens, n_k_heads,
+                          n_v_heads, state_size, conv_kernel, scale, l2_eps, norm_eps, workspace,
+                          slots, pool, err_count, stream):
+    pool = _pool(pool, n_seqs, slots)
+    _ws_check(workspace)
+    _check(name, getattr(library(), name)(
+        _ptr(qkv, "qkv"), _ptr(conv_w, "conv_w"), _ptr(conv_state, "conv_state"),
+        _ptr(alpha, "alpha"), _ptr(b, "b"), _ptr(dt, "dt"), _ptr(a, "a"), _ptr(z, "z"),
+        _ptr(norm_w, "norm_w"), _ptr(state, "state"), _ptr(out, "out"), *extra,
+        _cu(cu_seqlens), n_seqs, total_tokens, max_tokens, n_k_heads, n_v_heads, state_size,
+        conv_kernel, scale, l2_eps, norm_eps, _slots(slots), pool, _errc(err_count),
+        _ws_ptr(workspace), _ws_bytes(workspace), _stream(stream)))
+
+
+def gdn_block_prefill_varlen(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out,
+                             cu_seqlens, n_seqs, total_tokens, max_tokens, n_k_heads, n_v_heads,
+                             state_size, conv_kernel, scale, l2_eps, norm_eps, workspace,
+                             slots=None, pool=None, err_count=None, stream=None):
+    """gdn_block_prefill over a ragged batch; `workspace` of at least
+    gdn_block_prefill_varlen_workspace_size() bytes."""
+    _block_prefill_varlen("gdn_block_prefill_varlen", qkv, conv_w, conv_state, alpha, b, dt, a,
+                          z, norm_w, state, out, (), cu_seqlens, n_seqs, total_tokens,
+                          max_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale,
+                          l2_eps, norm_eps, workspace, slots, pool, err_count, stream)
+
+
+def gdn_block_prefill_chunked_varlen(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state,
+                                     out, cu_seqlens, n_seqs, total_tokens, max_tokens,
+                                     n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                                     norm_eps, workspace, slots=None, pool=None, err_count=None,
+                                     stream=None):
+    """gdn_block_prefill_chunked over a ragged batch (state_size 128)."""
+    _block_prefill_varlen("gdn_block_prefill_chunked_varlen", qkv, conv_w, conv_state, alpha, b,
+                          dt, a, z, norm_w, state, out, (), cu_seqlens, n_seqs, total_tokens,
+                          max_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale,
+                          l2_eps, norm_eps, workspace, slots, pool, err_count, stream)
+
+
+def gdn_block_prefill_snapshots_varlen(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state,
+                                       out, snaps, conv_snaps, cu_seqlens, n_seqs, total_tokens,
+                                       max_tokens, n_k_heads, n_v_heads, state_size, conv_kernel,
+                                       scale, l2_eps, norm_eps, workspace, slots=None, pool=None,
+                                       err_count=None, stream=None):
+    """gdn_block_prefill_snapshots over a ragged batch: snaps [total][H][S][S], conv_snaps
+    [total][C][K-1], packed as the positions are."""
+    _block_prefill_varlen("gdn_block_prefill_snapshots_varlen", qkv, conv_w, conv_state, alpha,
+                          b, dt, a, z, norm_w, state, out,
+                          (_ptr(snaps, "snaps"), _ptr(conv_snaps, "conv_snaps")), cu_seqlens,
+                          n_seqs, total_tokens, max_tokens, n_k_heads, n_v_heads, state_size,
+                          conv_kernel, scale, l2_eps, norm_eps, workspace, slots, pool,
+                          err_count, stream)
+
+
+def gdn_snapshot_restore_varlen(state, snaps, accepted, cu_seqlens, n_seqs, total_tokens,
+                                max_tokens, n_v_heads, state_size, conv_state=None,
+                                conv_snaps=None, conv_dim=0, conv_kernel=0, slots=None,
+                                pool=None, err_count=None, stream=None):
+    """Roll each sequence of a ragged batch back to the snapshot after its accepted[n]-th
+    position (snapshots packed as the positions are)."""
+    import torch
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_snapshot_restore_varlen", library().gdn_snapshot_restore_varlen(
+        _ptr(state, "state"), _ptr(snaps, "snaps"), _ptr(conv_state, "conv_state", optional=True),
+        _ptr(conv_snaps, "conv_snaps", optional=True), _ptr(accepted, "accepted", torch.int32),
+        _cu(cu_seqlens), n_seqs, total_tokens, max_tokens, n_v_heads, state_size, conv_dim,
+        conv_kernel, _slots(slots), pool, _errc(err_count), _stream(stream)))

@@ -113,7 +113,7 @@ __device__ __forceinline__ void chunk_gram(const float *rk, const float *rq, flo
 __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
     float *__restrict__ state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
-    float *__restrict__ y, int n_tokens, int n_k_heads, int n_v_heads, float scale,
+    float *__restrict__ y, const SeqMap seqs, int n_k_heads, int n_v_heads, float scale,
     const int32_t *__restrict__ slots, int pool, int32_t *err_count) {
     extern __shared__ __align__(16) unsigned char smem[];
     Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBars);
@@ -121,12 +121,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
     const int H = n_v_heads, Hk = n_k_heads;
     const int vh = blockIdx.x % H, n = blockIdx.x / H, kh = vh % Hk;
     const int slot = slots ? slots[n] : n;
-    if (slot < 0 || slot >= pool) {  // uniform over the CTA, before any barrier
+    size_t row0;   // (n, t = 0) in the token-major arrays
+    int n_tokens;  // positions of sequence n
+    if (slot < 0 || slot >= pool || !seqs.range(n, row0, n_tokens)) {
+        // uniform over the CTA, before any barrier
         if (vh == 0 && tid == 0 && err_count) atomicAdd(err_count, 1);
         return;
     }
+    if (n_tokens == 0) return;  // nothing to scan: the state keeps its bits
     const int n_chunks = (n_tokens + kC - 1) / kC;
-    const size_t row0 = static_cast<size_t>(n) * n_tokens;  // (n, t = 0) in [N][T] order
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -565,6 +568,25 @@ unsigned read_and_clear_watchdog_chunked(cudaStream_t s) {
 
 using namespace gdn;
 
+namespace gdn {
+
+gdn_status launch_chunked_one_kernel(float *state, const float *q, const float *k,
+                                     const float *v, const float *g, const float *beta, float *y,
+                                     int n_seqs, SeqMap seqs, int n_k_heads, int n_v_heads,
+                                     float scale, const int32_t *slots, int pool,
+                                     int32_t *err_count, cudaStream_t s) {
+    if (static_cast<long long>(n_seqs) * n_v_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    // per launch: the attribute belongs to the current device
+    if (cudaFuncSetAttribute(chunked_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    chunked_scan_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, s>>>(
+        state, q, k, v, g, beta, y, seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count);
+    return launch_status();
+}
+
+}  // namespace gdn
+
 extern "C" gdn_status gdn_recurrence_scan_chunked(float *state, const float *q, const float *k,
                                                   const float *v, const float *g,
                                                   const float *beta, float *y, int n_seqs,
@@ -579,12 +601,7 @@ extern "C" gdn_status gdn_recurrence_scan_chunked(float *state, const float *q, 
     GDN_TRY(check_pool(n_seqs, slots, pool));
     if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_ERR_ALIGN;
     if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
-    if (static_cast<long long>(n_seqs) * n_v_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-    // per launch: the attribute belongs to the current device
-    if (cudaFuncSetAttribute(chunked_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
-        return GDN_ERR_LAUNCH;
-    chunked_scan_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, as_cuda(stream)>>>(
-        state, q, k, v, g, beta, y, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count);
-    return launch_status();
+    return launch_chunked_one_kernel(state, q, k, v, g, beta, y, n_seqs,
+                                     uniform_seqs(n_seqs, n_tokens), n_k_heads, n_v_heads, scale,
+                                     slots, pool, err_count, as_cuda(stream));
 }

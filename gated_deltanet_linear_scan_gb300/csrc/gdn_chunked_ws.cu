@@ -45,6 +45,19 @@ __device__ __forceinline__ size_t blk_index(int cw, int n, int vh, int n_seqs, i
     return (static_cast<size_t>(cw) * n_seqs + n) * H + vh;
 }
 
+// A ragged batch is prepared in one wave, its blocks indexed by chunk slot: chunk c of
+// sequence n takes slot cu[n] / 32 + n + c. The slots of consecutive sequences never
+// collide (floor((a + L) / 32) + 1 >= floor(a / 32) + ceil(L / 32)) and stay below
+// total / 32 + n_seqs, so the workspace needs (total / 32 + n_seqs) slots of blocks
+// whatever the lengths are, and a slot maps back to its sequence by binary search.
+__device__ __forceinline__ long long chunk_slot_base(const int32_t *cu, int n) {
+    return static_cast<long long>(cu[n]) / kC + n;
+}
+
+__host__ __device__ __forceinline__ long long ragged_chunk_slots(long long total, int n_seqs) {
+    return total / kC + n_seqs;
+}
+
 // ============================================================================ phase 1
 constexpr int kPThreads = 256;
 constexpr int kAtRow = kC + 4;  // A^T rows: 36 floats, float4 aligned
@@ -63,15 +76,41 @@ static_assert(kPOffBar % 8 == 0, "mbarrier alignment");
 __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
     const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
     const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ ws,
-    int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int c_begin, int n_wave_chunks) {
+    int n_seqs, const SeqMap seqs, int n_k_heads, int n_v_heads, int c_begin, int n_wave_chunks) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = n_v_heads, Hk = n_k_heads;
-    const int cw = blockIdx.x % n_wave_chunks;
-    const int rest = blockIdx.x / n_wave_chunks;
-    const int kh = rest % Hk, n = rest / Hk;
-    const int t0 = (c_begin + cw) * kC, valid = min(kC, n_tokens - t0);
-    const size_t row0 = static_cast<size_t>(n) * n_tokens + t0;  // (n, t0) in [N][T] order
+    int kh, n, chunk;
+    size_t seq0, blk_row;  // first position of sequence n; workspace block row of the chunk
+    int n_tokens;
+    if (seqs.cu == nullptr) {  // uniform batch: grid (wave chunk, k-head, sequence)
+        const int cw = blockIdx.x % n_wave_chunks, rest = blockIdx.x / n_wave_chunks;
+        kh = rest % Hk;
+        n = rest / Hk;
+        seqs.range(n, seq0, n_tokens);
+        chunk = c_begin + cw;
+        blk_row = static_cast<size_t>(cw) * n_seqs + n;
+    } else {  // ragged batch: grid (chunk slot, k-head); slots no chunk owns return
+        const int cs = blockIdx.x % n_wave_chunks;
+        kh = blockIdx.x / n_wave_chunks;
+        int lo = 0, hi = n_seqs - 1;
+        n = -1;
+        while (lo <= hi) {
+            const int mid = (lo + hi) >> 1;
+            if (chunk_slot_base(seqs.cu, mid) <= cs) {
+                n = mid;
+                lo = mid + 1;
+            } else {
+                hi = mid - 1;
+            }
+        }
+        if (n < 0 || !seqs.range(n, seq0, n_tokens)) return;  // uniform over the CTA
+        chunk = static_cast<int>(cs - chunk_slot_base(seqs.cu, n));
+        if (chunk * kC >= n_tokens) return;
+        blk_row = static_cast<size_t>(cs);
+    }
+    const int t0 = chunk * kC, valid = min(kC, n_tokens - t0);
+    const size_t row0 = seq0 + t0;  // (n, t0) in the token-major arrays
     const int ratio = H / Hk;
     float *rk = reinterpret_cast<float *>(smem + kPOffK);
     float *rq = reinterpret_cast<float *>(smem + kPOffQ);
@@ -123,7 +162,7 @@ __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
     const bool is_w = tid < kS;
     for (int rr = 0; rr < ratio; ++rr) {
         const int vh = rr * Hk + kh;
-        float *blk = ws + blk_index(cw, n, vh, n_seqs, H) * kBlkFloats;
+        float *blk = ws + (blk_row * H + vh) * kBlkFloats;
         float gl = 0.f, bl = 0.f;  // lane = position
         if (lane < valid) {
             gl = g[(row0 + lane) * H + vh];
@@ -229,7 +268,7 @@ constexpr int kPrepBarrier = 1, kStateBarrier = 2;
 __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
     float *__restrict__ state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ g, const float *__restrict__ ws, float *__restrict__ y,
-    int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int c_begin, int n_wave_chunks,
+    int n_seqs, const SeqMap seqs, int n_k_heads, int n_v_heads, int c_begin, int n_wave_chunks,
     float scale, const int32_t *__restrict__ slots, int pool, int32_t *err_count) {
     extern __shared__ __align__(16) unsigned char smem[];
     Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBars);
@@ -237,14 +276,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
     const int H = n_v_heads, Hk = n_k_heads;
     const int vh = blockIdx.x % H, n = blockIdx.x / H, kh = vh % Hk;
     const int slot = slots ? slots[n] : n;
-    if (slot < 0 || slot >= pool) {  // uniform over the CTA, before any barrier
+    size_t row0;   // (n, t = 0) in the token-major arrays
+    int n_tokens;  // positions of sequence n
+    if (slot < 0 || slot >= pool || !seqs.range(n, row0, n_tokens)) {
+        // uniform over the CTA, before any barrier
         if (vh == 0 && tid == 0 && err_count) atomicAdd(err_count, 1);
         return;
     }
-    const int nw = n_wave_chunks;
-    const size_t row0 = static_cast<size_t>(n) * n_tokens;  // (n, t = 0) in [N][T] order
+    // uniform batch: this wave's chunks, block rows ci * n_seqs + n; ragged batch: all of
+    // the sequence's chunks in one wave, block rows from its first chunk slot on
+    const int nw = seqs.cu ? (n_tokens + kC - 1) / kC : n_wave_chunks;
+    if (nw == 0) return;  // an empty sequence: the state keeps its bits
+    const size_t blk_row0 = seqs.cu ? static_cast<size_t>(chunk_slot_base(seqs.cu, n)) : n;
+    const size_t blk_step = seqs.cu ? 1 : static_cast<size_t>(n_seqs);
     auto chunk_t0 = [&](int ci) { return (c_begin + ci) * kC; };
-    auto blk_of = [&](int ci) { return ws + blk_index(ci, n, vh, n_seqs, H) * kBlkFloats; };
+    auto blk_of = [&](int ci) {
+        return ws + ((blk_row0 + ci * blk_step) * H + vh) * kBlkFloats;
+    };
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -611,20 +659,25 @@ gdn_status check_range(int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, i
     return GDN_OK;
 }
 
+// Uniform batch: chunks cb .. cb + nc - 1 of every sequence. Ragged batch (seqs.cu set,
+// cb = 0): every chunk slot, nc = ragged_chunk_slots().
 gdn_status launch_prepare(const float *q, const float *k, const float *v, const float *g,
-                          const float *beta, float *ws, int n_seqs, int n_tokens, int n_k_heads,
+                          const float *beta, float *ws, int n_seqs, SeqMap seqs, int n_k_heads,
                           int n_v_heads, int cb, int nc, cudaStream_t s) {
     // per launch: the attribute belongs to the current device
     if (cudaFuncSetAttribute(chunk_prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kPSmemBytes)) != cudaSuccess)
         return GDN_ERR_LAUNCH;
-    chunk_prepare_kernel<<<nc * n_seqs * n_k_heads, kPThreads, kPSmemBytes, s>>>(
-        q, k, v, g, beta, ws, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nc);
+    const long long blocks =
+        static_cast<long long>(nc) * (seqs.cu ? 1 : n_seqs) * n_k_heads;
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    chunk_prepare_kernel<<<static_cast<unsigned>(blocks), kPThreads, kPSmemBytes, s>>>(
+        q, k, v, g, beta, ws, n_seqs, seqs, n_k_heads, n_v_heads, cb, nc);
     return launch_status();
 }
 
 gdn_status launch_advance(float *state, const float *q, const float *k, const float *g,
-                          const float *ws, float *y, int n_seqs, int n_tokens, int n_k_heads,
+                          const float *ws, float *y, int n_seqs, SeqMap seqs, int n_k_heads,
                           int n_v_heads, float scale, int cb, int nc, const int32_t *slots,
                           int pool, int32_t *err_count, cudaStream_t s) {
     // per launch: the attribute belongs to the current device
@@ -633,7 +686,7 @@ gdn_status launch_advance(float *state, const float *q, const float *k, const fl
         return GDN_ERR_LAUNCH;
     // slot errors are counted once, with the first chunk
     chunk_state_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, s>>>(
-        state, q, k, g, ws, y, n_seqs, n_tokens, n_k_heads, n_v_heads, cb, nc, scale, slots, pool,
+        state, q, k, g, ws, y, n_seqs, seqs, n_k_heads, n_v_heads, cb, nc, scale, slots, pool,
         cb == 0 ? err_count : nullptr);
     return launch_status();
 }
@@ -648,6 +701,37 @@ unsigned read_and_clear_watchdog_chunked_ws(cudaStream_t s) {
     cudaMemcpyToSymbolAsync(g_watchdog_chunked_ws, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
     cudaStreamSynchronize(s);
     return flags;
+}
+
+size_t ragged_chunked_ws_size(int n_seqs, long long total, int n_v_heads) {
+    if (n_seqs < 1 || n_v_heads < 1 || total < 0) return 0;
+    return static_cast<size_t>(ragged_chunk_slots(total, n_seqs)) * n_v_heads * kBlkBytes;
+}
+
+size_t chunked_seqs_ws_size(int n_seqs, SeqMap seqs, int n_v_heads) {
+    if (n_seqs < 1 || n_v_heads < 1) return 0;
+    if (seqs.cu == nullptr)
+        return static_cast<size_t>((seqs.n_tokens + kC - 1) / kC) * bytes_per_chunk(n_seqs, n_v_heads);
+    return ragged_chunked_ws_size(n_seqs, seqs.total, n_v_heads);
+}
+
+gdn_status launch_chunked_seqs(float *state, const float *q, const float *k, const float *v,
+                               const float *g, const float *beta, float *y, int n_seqs,
+                               SeqMap seqs, int n_k_heads, int n_v_heads, float scale,
+                               const int32_t *slots, int pool, int32_t *err_count,
+                               void *workspace, size_t workspace_bytes, cudaStream_t s) {
+    const size_t need = chunked_seqs_ws_size(n_seqs, seqs, n_v_heads);
+    if (workspace == nullptr || need == 0 || workspace_bytes < need || !aligned16(workspace))
+        return launch_chunked_one_kernel(state, q, k, v, g, beta, y, n_seqs, seqs, n_k_heads,
+                                         n_v_heads, scale, slots, pool, err_count, s);
+    const long long slots_or_chunks =
+        seqs.cu ? ragged_chunk_slots(seqs.total, n_seqs) : (seqs.n_tokens + kC - 1) / kC;
+    if (slots_or_chunks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    float *ws = static_cast<float *>(workspace);
+    const int nc = static_cast<int>(slots_or_chunks);
+    GDN_TRY(launch_prepare(q, k, v, g, beta, ws, n_seqs, seqs, n_k_heads, n_v_heads, 0, nc, s));
+    return launch_advance(state, q, k, g, ws, y, n_seqs, seqs, n_k_heads, n_v_heads, scale, 0, nc,
+                          slots, pool, err_count, s);
 }
 
 }  // namespace gdn
@@ -674,8 +758,9 @@ extern "C" gdn_status gdn_chunked_prepare(const float *q, const float *k, const 
                         workspace_bytes));
     if (n_chunks == 0) return GDN_OK;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_ERR_ALIGN;
-    return launch_prepare(q, k, v, g, beta, static_cast<float *>(workspace), n_seqs, n_tokens,
-                          n_k_heads, n_v_heads, chunk_begin, n_chunks, as_cuda(stream));
+    return launch_prepare(q, k, v, g, beta, static_cast<float *>(workspace), n_seqs,
+                          uniform_seqs(n_seqs, n_tokens), n_k_heads, n_v_heads, chunk_begin,
+                          n_chunks, as_cuda(stream));
 }
 
 extern "C" gdn_status gdn_chunked_advance(float *state, const float *q, const float *k,
@@ -694,8 +779,8 @@ extern "C" gdn_status gdn_chunked_advance(float *state, const float *q, const fl
     if (n_chunks == 0) return GDN_OK;
     if (!aligned16(state) || !aligned16(q) || !aligned16(k)) return GDN_ERR_ALIGN;
     return launch_advance(state, q, k, g, static_cast<const float *>(workspace), y, n_seqs,
-                          n_tokens, n_k_heads, n_v_heads, scale, chunk_begin, n_chunks, slots,
-                          pool, err_count, as_cuda(stream));
+                          uniform_seqs(n_seqs, n_tokens), n_k_heads, n_v_heads, scale,
+                          chunk_begin, n_chunks, slots, pool, err_count, as_cuda(stream));
 }
 
 extern "C" gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *q, const float *k,
@@ -723,10 +808,36 @@ extern "C" gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *
     float *ws = static_cast<float *>(workspace);
     for (int cb = 0; cb < n_chunks; cb += wave) {
         const int nc = n_chunks - cb < wave ? n_chunks - cb : wave;
-        GDN_TRY(launch_prepare(q, k, v, g, beta, ws, n_seqs, n_tokens, n_k_heads, n_v_heads, cb,
-                               nc, s));
-        GDN_TRY(launch_advance(state, q, k, g, ws, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
-                               scale, cb, nc, slots, pool, err_count, s));
+        const SeqMap seqs = uniform_seqs(n_seqs, n_tokens);
+        GDN_TRY(launch_prepare(q, k, v, g, beta, ws, n_seqs, seqs, n_k_heads, n_v_heads, cb, nc,
+                               s));
+        GDN_TRY(launch_advance(state, q, k, g, ws, y, n_seqs, seqs, n_k_heads, n_v_heads, scale,
+                               cb, nc, slots, pool, err_count, s));
     }
     return GDN_OK;
+}
+
+extern "C" size_t gdn_recurrence_scan_chunked_varlen_ws_size(int n_seqs, int total_tokens,
+                                                             int n_v_heads, int state_size) {
+    if (state_size != kS) return 0;
+    return ragged_chunked_ws_size(n_seqs, total_tokens, n_v_heads);
+}
+
+extern "C" gdn_status gdn_recurrence_scan_chunked_varlen(
+    float *state, const float *q, const float *k, const float *v, const float *g,
+    const float *beta, float *y, const int32_t *cu_seqlens, int n_seqs, int total_tokens,
+    int max_tokens, int n_k_heads, int n_v_heads, int state_size, float scale,
+    const int32_t *slots, int pool, int32_t *err_count, void *workspace, size_t workspace_bytes,
+    gdn_stream_t stream) {
+    if (!state || !q || !k || !v || !g || !beta || !y) return GDN_ERR_NULL;
+    GDN_TRY(check_varlen(cu_seqlens, n_seqs, total_tokens, max_tokens));
+    GDN_TRY(check_common(n_seqs, max_tokens, n_k_heads, n_v_heads, state_size));
+    GDN_TRY(check_pool(n_seqs, slots, pool));
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_ERR_ALIGN;
+    if (workspace && !aligned16(workspace)) return GDN_ERR_ALIGN;
+    if (n_seqs == 0 || total_tokens == 0 || max_tokens == 0) return GDN_OK;
+    return launch_chunked_seqs(state, q, k, v, g, beta, y, n_seqs,
+                               SeqMap{cu_seqlens, max_tokens, total_tokens}, n_k_heads, n_v_heads,
+                               scale, slots, pool, err_count, workspace,
+                               workspace ? workspace_bytes : 0, as_cuda(stream));
 }

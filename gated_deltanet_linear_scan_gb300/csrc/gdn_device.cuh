@@ -65,15 +65,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete, for at most WAIT_LIMIT_NS.
-// Returns false if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Waits for phase `parity` of `bar` to complete, for at most limit_ns. Returns false
+// if it gave up.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+
+// The bounded wait of every kernel here: at most WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, WAIT_LIMIT_NS);
+}
+
+// Self-test of the bounded-wait path (one thread): arms an mbarrier for `bytes` that no
+// copy will bring when `arm` is set (a plain arrival completes the phase otherwise),
+// waits at most limit_ns, and on giving up raises `bit` in `flag` and leaves `out`
+// alone, as a kernel's guarded work is skipped; a completed wait writes 1 to out[0].
+// Nothing follows the wait that could block, so the thread always returns.
+__device__ __forceinline__ void bounded_wait_probe(bool arm, uint64_t limit_ns, unsigned *flag,
+                                                   unsigned bit, float *out) {
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (arm) mbar_arrive_expect_tx(&bar, 16);
+    else mbar_arrive(&bar);
+    if (mbar_wait_for(&bar, 0, limit_ns)) {
+        out[0] = 1.0f;
+    } else {
+        atomicOr(flag, bit);
+    }
 }
 
 // The same bounded wait for a thread that shares its SM sub-partition with warps

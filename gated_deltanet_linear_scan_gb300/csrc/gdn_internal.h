@@ -10,6 +10,52 @@ namespace gdn {
 
 inline cudaStream_t as_cuda(gdn_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Where each sequence's positions lie in the token-major arrays of a call.
+// Uniform batch (cu == NULL): every sequence has n_tokens positions, sequence n's
+// starting at n * n_tokens. Ragged batch: sequence n owns the packed positions
+// cu[n] .. cu[n+1] - 1 of `total`, and n_tokens bounds the length of any one
+// sequence (it sizes the grids). A ragged range that is not valid (negative, reversed,
+// past `total` or longer than n_tokens) makes its sequence be skipped, as an
+// out-of-range slot does.
+struct SeqMap {
+    const int32_t *cu;
+    int n_tokens;
+    long long total;
+
+    __device__ __forceinline__ bool range(int n, size_t &t0, int &len) const {
+        if (cu == nullptr) {
+            t0 = static_cast<size_t>(n) * n_tokens;
+            len = n_tokens;
+            return true;
+        }
+        const int a = cu[n], b = cu[n + 1];
+        if (a < 0 || b < a || b > total || b - a > n_tokens) return false;
+        t0 = static_cast<size_t>(a);
+        len = b - a;
+        return true;
+    }
+};
+
+inline SeqMap uniform_seqs(int n_seqs, int n_tokens) {
+    return SeqMap{nullptr, n_tokens, static_cast<long long>(n_seqs) * n_tokens};
+}
+
+// The last sequence n in [0, n_seqs) with cu[n] <= pos (binary search; -1 if none).
+// With a valid ragged batch that is the sequence owning position pos, if any.
+__device__ __forceinline__ int seq_of_position(const int32_t *cu, int n_seqs, long long pos) {
+    int lo = 0, hi = n_seqs - 1, found = -1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        if (cu[mid] <= pos) {
+            found = mid;
+            lo = mid + 1;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    return found;
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline bool supported_state_size(int s) { return s == 32 || s == 64 || s == 128 || s == 256; }
@@ -33,11 +79,39 @@ inline gdn_status check_heads(int n_k_heads, int n_v_heads, int state_size) {
     return GDN_OK;
 }
 
-// Gated RMSNorm over `rows` rows of head_dim; with `slots` non-NULL the rows of
-// sequence r / rows_per_seq are skipped when its slot is outside [0, pool).
-gdn_status launch_gated_norm(const float *y, const float *w, const float *z, float *out,
-                             long long rows, int head_dim, float eps, long long rows_per_seq,
-                             const int32_t *slots, int pool, cudaStream_t s);
+// Gated RMSNorm over `rows` rows of head_dim, row r being head r % heads of position
+// r / heads of the positions `seqs` maps. With `slots` non-NULL, or a ragged batch, the
+// rows of a skipped sequence (slot outside [0, pool), range not valid) and of positions
+// no sequence owns are left untouched.
+gdn_status launch_gated_norm_seqs(const float *y, const float *w, const float *z, float *out,
+                                  long long rows, int head_dim, float eps, int heads, int n_seqs,
+                                  SeqMap seqs, const int32_t *slots, int pool, cudaStream_t s);
+
+// Checks of a ragged batch's host arguments (cu_seqlens itself is device memory).
+gdn_status check_varlen(const int32_t *cu_seqlens, int n_seqs, int total_tokens, int max_tokens);
+
+// The sequential scan (snaps non-NULL: its snapshot form) over the positions `seqs` maps.
+gdn_status launch_scan_seqs(float *state, const float *q, const float *k, const float *v,
+                            const float *g, const float *beta, float *y, int n_seqs, SeqMap seqs,
+                            int n_k_heads, int n_v_heads, int state_size, float scale,
+                            const int32_t *slots, int pool, int32_t *err_count, float *snaps,
+                            cudaStream_t s);
+
+// The chunked scan over the positions `seqs` maps: the two-phase form in `workspace`
+// if it holds every chunk of the call (chunked_seqs_ws_size bytes), else the
+// one-kernel form.
+size_t chunked_seqs_ws_size(int n_seqs, SeqMap seqs, int n_v_heads);
+size_t ragged_chunked_ws_size(int n_seqs, long long total, int n_v_heads);
+gdn_status launch_chunked_seqs(float *state, const float *q, const float *k, const float *v,
+                               const float *g, const float *beta, float *y, int n_seqs,
+                               SeqMap seqs, int n_k_heads, int n_v_heads, float scale,
+                               const int32_t *slots, int pool, int32_t *err_count,
+                               void *workspace, size_t workspace_bytes, cudaStream_t s);
+gdn_status launch_chunked_one_kernel(float *state, const float *q, const float *k,
+                                     const float *v, const float *g, const float *beta, float *y,
+                                     int n_seqs, SeqMap seqs, int n_k_heads, int n_v_heads,
+                                     float scale, const int32_t *slots, int pool,
+                                     int32_t *err_count, cudaStream_t s);
 
 // Per-translation-unit watchdog flags (a bounded wait that gave up sets a bit).
 unsigned read_and_clear_watchdog_recurrence(cudaStream_t s);

@@ -152,22 +152,36 @@ __global__ void __launch_bounds__(kThreads) qkv_split_norm_kernel(
 
 // Gated RMSNorm, fm_kernel_ssm.m "Gated RMSNorm" and ssm_gated_delta.cu Kernel 3:
 // one warp per head row, one shuffle reduction, weight shared across heads.
-// With `slots` non-NULL, row r belongs to sequence r / rows_per_seq, and the rows
-// of a sequence whose slot is outside [0, pool) are left untouched.
+// Row r is head r % heads of position r / heads. With `slots` or a ragged batch, the
+// rows of a sequence whose slot is outside [0, pool) or whose range is not valid,
+// and (ragged) rows of positions no sequence owns, are left untouched.
 template <int E>
 __global__ void __launch_bounds__(kThreads) gated_norm_kernel(const float *y,
                                                                const float *__restrict__ w,
                                                                const float *__restrict__ z,
                                                                float *out, long long rows,
-                                                               float eps, long long rows_per_seq,
+                                                               float eps, int heads, int n_seqs,
+                                                               const SeqMap seqs,
                                                                const int32_t *__restrict__ slots,
                                                                int pool) {
     constexpr int D = 32 * E;
     const long long row = blockIdx.x * static_cast<long long>(kThreads / 32) + (threadIdx.x >> 5);
     if (row >= rows) return;
-    if (slots) {
-        const int slot = slots[row / rows_per_seq];
-        if (slot < 0 || slot >= pool) return;
+    if (slots || seqs.cu) {
+        const long long pos = row / heads;
+        int n;
+        if (seqs.cu) {
+            n = seq_of_position(seqs.cu, n_seqs, pos);
+            size_t t0;
+            int len;
+            if (n < 0 || !seqs.range(n, t0, len) || pos >= static_cast<long long>(t0) + len) return;
+        } else {
+            n = static_cast<int>(pos / seqs.n_tokens);
+        }
+        if (slots) {
+            const int slot = slots[n];
+            if (slot < 0 || slot >= pool) return;
+        }
     }
     const int lane = threadIdx.x & 31;
     float yv[E], zv[E], wv[E];
@@ -236,17 +250,20 @@ constexpr int kRestoreConv = kThreads * 16;  // floats per CTA of the conv copy
 
 __global__ void __launch_bounds__(kThreads) snapshot_restore_kernel(
     float *state, const float *__restrict__ snaps, float *conv_state,
-    const float *__restrict__ conv_snaps, const int32_t *__restrict__ accepted, int n_tokens,
+    const float *__restrict__ conv_snaps, const int32_t *__restrict__ accepted, const SeqMap seqs,
     size_t state_floats, size_t conv_floats, int state_parts, const int32_t *__restrict__ slots,
     int pool, int32_t *err_count) {
     const int n = blockIdx.y, part = blockIdx.x;
     const int slot = slots ? slots[n] : n;
     const int m = accepted[n];
-    if (slot < 0 || slot >= pool || m < 1 || m > n_tokens) {  // uniform over the row
+    size_t t0;  // the snapshot after position t of sequence n is snapshot t0 + t
+    int len;
+    if (slot < 0 || slot >= pool || !seqs.range(n, t0, len) || m < 1 || m > len) {
+        // uniform over the row
         if (err_count && part == 0 && threadIdx.x == 0) atomicAdd(err_count, 1);
         return;
     }
-    const size_t snap = static_cast<size_t>(n) * n_tokens + (m - 1);  // snapshot index
+    const size_t snap = t0 + (m - 1);  // snapshot index
     if (part < state_parts) {
         // all 8 loads of a thread in flight before its stores
         const float4 *src = reinterpret_cast<const float4 *>(snaps + snap * state_floats);
@@ -272,16 +289,16 @@ __global__ void __launch_bounds__(kThreads) snapshot_restore_kernel(
 
 }  // namespace
 
-gdn_status launch_gated_norm(const float *y, const float *w, const float *z, float *out,
-                             long long rows, int head_dim, float eps, long long rows_per_seq,
-                             const int32_t *slots, int pool, cudaStream_t s) {
+gdn_status launch_gated_norm_seqs(const float *y, const float *w, const float *z, float *out,
+                                  long long rows, int head_dim, float eps, int heads, int n_seqs,
+                                  SeqMap seqs, const int32_t *slots, int pool, cudaStream_t s) {
     if (rows == 0) return GDN_OK;
     const unsigned blocks = static_cast<unsigned>((rows + kThreads / 32 - 1) / (kThreads / 32));
     switch (head_dim) {
-        case 32: gated_norm_kernel<1><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, rows_per_seq, slots, pool); break;
-        case 64: gated_norm_kernel<2><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, rows_per_seq, slots, pool); break;
-        case 128: gated_norm_kernel<4><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, rows_per_seq, slots, pool); break;
-        default: gated_norm_kernel<8><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, rows_per_seq, slots, pool); break;
+        case 32: gated_norm_kernel<1><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, heads, n_seqs, seqs, slots, pool); break;
+        case 64: gated_norm_kernel<2><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, heads, n_seqs, seqs, slots, pool); break;
+        case 128: gated_norm_kernel<4><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, heads, n_seqs, seqs, slots, pool); break;
+        default: gated_norm_kernel<8><<<blocks, kThreads, 0, s>>>(y, w, z, out, rows, eps, heads, n_seqs, seqs, slots, pool); break;
     }
     return launch_status();
 }
@@ -359,15 +376,20 @@ gdn_status gdn_conv1d_silu_seq_snapshots(const float *qkv, const float *w, float
                        pool, err_count, snaps, stream);
 }
 
-gdn_status gdn_snapshot_restore(float *state, const float *snaps, float *conv_state,
-                                const float *conv_snaps, const int32_t *accepted, int n_seqs,
-                                int n_tokens, int n_v_heads, int state_size, int conv_dim,
-                                int conv_kernel, const int32_t *slots, int pool,
-                                int32_t *err_count, gdn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+gdn_status restore_impl(float *state, const float *snaps, float *conv_state,
+                        const float *conv_snaps, const int32_t *accepted, int n_seqs, SeqMap seqs,
+                        int n_v_heads, int state_size, int conv_dim, int conv_kernel,
+                        const int32_t *slots, int pool, int32_t *err_count, gdn_stream_t stream) {
     if (!state || !snaps || !accepted) return GDN_ERR_NULL;
     const bool conv = conv_state || conv_snaps;
     if (conv && !(conv_state && conv_snaps)) return GDN_ERR_NULL;
-    if (n_seqs < 0 || n_tokens < 1 || n_v_heads < 1) return GDN_ERR_SHAPE;
+    if (n_seqs < 0 || n_v_heads < 1) return GDN_ERR_SHAPE;
+    if (seqs.cu == nullptr ? seqs.n_tokens < 1 : (seqs.n_tokens < 0 || seqs.total < 0))
+        return GDN_ERR_SHAPE;
     if (state_size < 32 || state_size % 32 != 0 || state_size > 256) return GDN_ERR_SHAPE;
     if (!supported_state_size(state_size)) return GDN_ERR_UNSUPPORTED;  // as the snapshot scan
     if (conv && (conv_dim < 1 || conv_kernel < 2 || conv_kernel > 8)) return GDN_ERR_SHAPE;
@@ -382,9 +404,35 @@ gdn_status gdn_snapshot_restore(float *state, const float *snaps, float *conv_st
     if (state_parts + conv_parts > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     const dim3 grid(static_cast<unsigned>(state_parts + conv_parts), static_cast<unsigned>(n_seqs));
     snapshot_restore_kernel<<<grid, kThreads, 0, as_cuda(stream)>>>(
-        state, snaps, conv_state, conv_snaps, accepted, n_tokens, state_floats, conv_floats,
+        state, snaps, conv_state, conv_snaps, accepted, seqs, state_floats, conv_floats,
         static_cast<int>(state_parts), slots, pool, err_count);
     return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_snapshot_restore(float *state, const float *snaps, float *conv_state,
+                                const float *conv_snaps, const int32_t *accepted, int n_seqs,
+                                int n_tokens, int n_v_heads, int state_size, int conv_dim,
+                                int conv_kernel, const int32_t *slots, int pool,
+                                int32_t *err_count, gdn_stream_t stream) {
+    return restore_impl(state, snaps, conv_state, conv_snaps, accepted, n_seqs,
+                        uniform_seqs(n_seqs, n_tokens), n_v_heads, state_size, conv_dim,
+                        conv_kernel, slots, pool, err_count, stream);
+}
+
+gdn_status gdn_snapshot_restore_varlen(float *state, const float *snaps, float *conv_state,
+                                       const float *conv_snaps, const int32_t *accepted,
+                                       const int32_t *cu_seqlens, int n_seqs, int total_tokens,
+                                       int max_tokens, int n_v_heads, int state_size,
+                                       int conv_dim, int conv_kernel, const int32_t *slots,
+                                       int pool, int32_t *err_count, gdn_stream_t stream) {
+    GDN_TRY(check_varlen(cu_seqlens, n_seqs, total_tokens, max_tokens));
+    return restore_impl(state, snaps, conv_state, conv_snaps, accepted, n_seqs,
+                        SeqMap{cu_seqlens, max_tokens, total_tokens}, n_v_heads, state_size,
+                        conv_dim, conv_kernel, slots, pool, err_count, stream);
 }
 
 gdn_status gdn_qkv_split_norm(const float *conv_out, float *q, float *k, float *v, int rows,
@@ -413,7 +461,8 @@ gdn_status gdn_gated_norm(const float *y, const float *w, const float *z, float 
         return (head_dim % 32 == 0 && head_dim <= 256) ? GDN_ERR_UNSUPPORTED : GDN_ERR_SHAPE;
     }
     if (!aligned16(y) || !aligned16(w) || !aligned16(z) || !aligned16(out)) return GDN_ERR_ALIGN;
-    return launch_gated_norm(y, w, z, out, rows, head_dim, eps, 1, nullptr, 0, as_cuda(stream));
+    return launch_gated_norm_seqs(y, w, z, out, rows, head_dim, eps, 1, rows,
+                                  uniform_seqs(rows, 1), nullptr, 0, as_cuda(stream));
 }
 
 }  // extern "C"

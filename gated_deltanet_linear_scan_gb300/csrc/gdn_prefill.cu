@@ -17,10 +17,12 @@ constexpr size_t kAlignFloats = 64;  // 256-byte sub-buffers
 
 size_t round_up(size_t n) { return (n + kAlignFloats - 1) / kAlignFloats * kAlignFloats; }
 
+// Intermediates of a call over `rows` positions in all (n_seqs * n_tokens for a uniform
+// batch, the packed total for a ragged one).
 struct PrefillLayout {
     size_t q, k, v, g, beta, total_floats;
-    PrefillLayout(long long n, long long t, int hk, int h, int s) {
-        const size_t rows = static_cast<size_t>(n) * static_cast<size_t>(t);
+    PrefillLayout(long long rows_ll, int hk, int h, int s) {
+        const size_t rows = static_cast<size_t>(rows_ll);
         q = 0;
         k = q + round_up(rows * hk * s);
         v = k + round_up(rows * hk * s);
@@ -44,18 +46,21 @@ __host__ __device__ constexpr int conv_norm_positions() { return E >= 8 ? 16 : 3
 template <int E, int K>
 __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
     const float *__restrict__ qkv, const float *__restrict__ w, float *conv_state,
-    float *__restrict__ q, float *__restrict__ k, float *__restrict__ v, int n_tokens,
+    float *__restrict__ q, float *__restrict__ k, float *__restrict__ v, const SeqMap seqs,
     int n_k_heads, int n_v_heads, float eps, const int32_t *__restrict__ slots, int pool,
     int32_t *err_count) {
     constexpr int S = 32 * E, TAPS = K - 1, P = conv_norm_positions<E>(), ROW = S + 4;
     __shared__ __align__(16) float tile[P * ROW];
     const int sl = blockIdx.x, n = blockIdx.z, c = threadIdx.x;
-    const int t0 = blockIdx.y * P, t1 = min(n_tokens, t0 + P);
     const int slot = slots ? slots[n] : n;
-    if (slot < 0 || slot >= pool) {  // uniform over the CTA
+    size_t seq0;   // first position of sequence n in the token-major arrays
+    int n_tokens;  // its length
+    if (slot < 0 || slot >= pool || !seqs.range(n, seq0, n_tokens)) {  // uniform over the CTA
         if (err_count && sl == 0 && blockIdx.y == 0 && c == 0) atomicAdd(err_count, 1);
         return;
     }
+    const int t0 = blockIdx.y * P, t1 = min(n_tokens, t0 + P);
+    if (t0 >= n_tokens) return;  // past the end of a shorter sequence: uniform over the CTA
     const int Hk = n_k_heads, H = n_v_heads;
     const size_t conv_dim = static_cast<size_t>(2 * Hk + H) * S;
     const size_t ch = static_cast<size_t>(sl) * S + c;
@@ -63,7 +68,7 @@ __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
 #pragma unroll
     for (int t = 0; t < K; ++t) wc[t] = w[ch * K + t];
     float *hs = conv_state + (static_cast<size_t>(slot) * conv_dim + ch) * TAPS;
-    const float *x_ptr = qkv + static_cast<size_t>(n) * n_tokens * conv_dim + ch;
+    const float *x_ptr = qkv + seq0 * conv_dim + ch;
     float old[TAPS], hist[TAPS];
     if (t0 == 0) {
 #pragma unroll
@@ -75,8 +80,7 @@ __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
         hist[t] = pos >= 0 ? x_ptr[static_cast<size_t>(pos) * conv_dim] : old[t];  // t0 == 0
     }
     const bool is_qk = sl < 2 * Hk;
-    float *v_out = is_qk ? nullptr
-                         : v + (static_cast<size_t>(n) * n_tokens * H + (sl - 2 * Hk)) * S + c;
+    float *v_out = is_qk ? nullptr : v + (seq0 * H + (sl - 2 * Hk)) * S + c;
     constexpr int B = 16;  // inputs loaded ahead of their use: memory-level parallelism
     for (int pb = t0; pb < t1; pb += B) {
         float xs[B];
@@ -111,8 +115,7 @@ __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
     if (!is_qk) return;  // uniform over the CTA
     __syncthreads();
     const int warp = c >> 5, lane = c & 31;
-    float *dst0 = (sl < Hk ? q : k) +
-                  (static_cast<size_t>(n) * n_tokens * Hk + (sl % Hk)) * S + lane * E;
+    float *dst0 = (sl < Hk ? q : k) + (seq0 * Hk + (sl % Hk)) * S + lane * E;
     for (int r = warp; r < t1 - t0; r += S / 32) {
         float xv[E];
         load_vec<E>(xv, tile + r * ROW + lane * E);
@@ -129,12 +132,12 @@ __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
 
 template <int E, int K>
 gdn_status launch_conv_split_norm_k(const float *qkv, const float *w, float *conv_state, float *q,
-                                    float *k, float *v, int n_seqs, int n_tokens, int Hk, int H,
+                                    float *k, float *v, int n_seqs, SeqMap seqs, int Hk, int H,
                                     float eps, const int32_t *slots, int pool, int32_t *err_count,
                                     cudaStream_t s) {
     constexpr int P = conv_norm_positions<E>();
-    const dim3 grid(2 * Hk + H, (n_tokens + P - 1) / P, n_seqs);
-    conv_split_norm_kernel<E, K><<<grid, 32 * E, 0, s>>>(qkv, w, conv_state, q, k, v, n_tokens,
+    const dim3 grid(2 * Hk + H, (seqs.n_tokens + P - 1) / P, n_seqs);
+    conv_split_norm_kernel<E, K><<<grid, 32 * E, 0, s>>>(qkv, w, conv_state, q, k, v, seqs,
                                                          Hk, H, eps, slots, pool, err_count);
     return launch_status();
 }
@@ -142,16 +145,16 @@ gdn_status launch_conv_split_norm_k(const float *qkv, const float *w, float *con
 template <int E>
 gdn_status launch_conv_split_norm(int conv_kernel, const float *qkv, const float *w,
                                   float *conv_state, float *q, float *k, float *v, int n_seqs,
-                                  int n_tokens, int Hk, int H, float eps, const int32_t *slots,
+                                  SeqMap seqs, int Hk, int H, float eps, const int32_t *slots,
                                   int pool, int32_t *err_count, cudaStream_t s) {
     switch (conv_kernel) {
-        case 2: return launch_conv_split_norm_k<E, 2>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
-        case 3: return launch_conv_split_norm_k<E, 3>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
-        case 4: return launch_conv_split_norm_k<E, 4>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
-        case 5: return launch_conv_split_norm_k<E, 5>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
-        case 6: return launch_conv_split_norm_k<E, 6>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
-        case 7: return launch_conv_split_norm_k<E, 7>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
-        default: return launch_conv_split_norm_k<E, 8>(qkv, w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, eps, slots, pool, err_count, s);
+        case 2: return launch_conv_split_norm_k<E, 2>(qkv, w, conv_state, q, k, v, n_seqs, seqs, Hk, H, eps, slots, pool, err_count, s);
+        case 3: return launch_conv_split_norm_k<E, 3>(qkv, w, conv_state, q, k, v, n_seqs, seqs, Hk, H, eps, slots, pool, err_count, s);
+        case 4: return launch_conv_split_norm_k<E, 4>(qkv, w, conv_state, q, k, v, n_seqs, seqs, Hk, H, eps, slots, pool, err_count, s);
+        case 5: return launch_conv_split_norm_k<E, 5>(qkv, w, conv_state, q, k, v, n_seqs, seqs, Hk, H, eps, slots, pool, err_count, s);
+        case 6: return launch_conv_split_norm_k<E, 6>(qkv, w, conv_state, q, k, v, n_seqs, seqs, Hk, H, eps, slots, pool, err_count, s);
+        case 7: return launch_conv_split_norm_k<E, 7>(qkv, w, conv_state, q, k, v, n_seqs, seqs, Hk, H, eps, slots, pool, err_count, s);
+        default: return launch_conv_split_norm_k<E, 8>(qkv, w, conv_state, q, k, v, n_seqs, seqs, Hk, H, eps, slots, pool, err_count, s);
     }
 }
 
@@ -164,12 +167,15 @@ constexpr int kHistThreads = 256;
 
 __global__ void __launch_bounds__(kHistThreads) conv_history_snapshots_kernel(
     const float *__restrict__ qkv, const float *__restrict__ conv_state,
-    float *__restrict__ snaps, int n_tokens, int conv_dim, int taps,
+    float *__restrict__ snaps, const SeqMap seqs, int conv_dim, int taps,
     const int32_t *__restrict__ slots, int pool) {
     const int c = blockIdx.x * kHistThreads + threadIdx.x, t = blockIdx.y, n = blockIdx.z;
     const int slot = slots ? slots[n] : n;
-    if (c >= conv_dim || slot < 0 || slot >= pool) return;  // a skipped sequence is counted by the conv pass
-    const size_t row = static_cast<size_t>(n) * n_tokens;
+    size_t row;  // first position of sequence n
+    int n_tokens;
+    // a skipped sequence is counted by the conv pass
+    if (c >= conv_dim || slot < 0 || slot >= pool || !seqs.range(n, row, n_tokens)) return;
+    if (t >= n_tokens) return;
     float *dst = snaps + ((row + t) * conv_dim + c) * taps;
     for (int j = 0; j < taps; ++j) {
         const int pos = t - (taps - 1) + j;
@@ -188,8 +194,8 @@ extern "C" {
 size_t gdn_block_prefill_workspace_size(int n_seqs, int n_tokens, int n_k_heads, int n_v_heads,
                                         int state_size) {
     if (n_seqs < 0 || n_tokens < 0 || n_k_heads < 1 || n_v_heads < 1 || state_size < 1) return 0;
-    return PrefillLayout(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size).total_floats *
-           sizeof(float);
+    return PrefillLayout(static_cast<long long>(n_seqs) * n_tokens, n_k_heads, n_v_heads,
+                         state_size).total_floats * sizeof(float);
 }
 
 size_t gdn_block_prefill_chunked_workspace_size(int n_seqs, int n_tokens, int n_k_heads,
@@ -206,11 +212,13 @@ size_t gdn_block_prefill_chunked_workspace_size(int n_seqs, int n_tokens, int n_
 namespace {
 
 // The prefill block with either scan: the sequential one (bit for bit the fused
-// decode step, position after position) or the chunked tensor-core one.
+// decode step, position after position) or the chunked tensor-core one, over a
+// uniform batch (seqs.cu NULL: n_seqs x seqs.n_tokens positions) or a ragged one
+// (seqs.total packed positions; seqs.n_tokens bounds one sequence's length).
 gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state,
                         const float *alpha, const float *b, const float *dt, const float *a,
                         const float *z, const float *norm_w, float *state, float *out,
-                        int n_seqs, int n_tokens, int n_k_heads, int n_v_heads, int state_size,
+                        int n_seqs, SeqMap seqs, int n_k_heads, int n_v_heads, int state_size,
                         int conv_kernel, float scale, float l2_eps, float norm_eps,
                         const int32_t *slots, int pool, int32_t *err_count, void *workspace,
                         size_t workspace_bytes, gdn_stream_t stream, bool chunked,
@@ -219,7 +227,8 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
         !out)
         return GDN_ERR_NULL;
     const bool snapshots = snaps != nullptr;  // the snapshot form passes both, non-NULL
-    if (n_seqs < 0 || n_tokens < 0) return GDN_ERR_SHAPE;
+    const int n_tokens = seqs.n_tokens;       // positions of a sequence (ragged: at most)
+    if (n_seqs < 0 || n_tokens < 0 || seqs.total < 0) return GDN_ERR_SHAPE;
     if (conv_kernel < 2 || conv_kernel > 8) return GDN_ERR_SHAPE;
     GDN_TRY(check_heads(n_k_heads, n_v_heads, state_size));
     if (chunked && state_size != 128) return GDN_ERR_UNSUPPORTED;
@@ -227,12 +236,12 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
     if (!aligned16(qkv) || !aligned16(conv_w) || !aligned16(conv_state) || !aligned16(state) ||
         !aligned16(z) || !aligned16(out) || !aligned16(norm_w))
         return GDN_ERR_ALIGN;
-    if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
-    const PrefillLayout L(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size);
+    if (n_seqs == 0 || n_tokens == 0 || seqs.total == 0) return GDN_OK;
+    const long long rows = seqs.total;  // positions in all
+    const PrefillLayout L(rows, n_k_heads, n_v_heads, state_size);
     if (!workspace) return GDN_ERR_NULL;
     if (workspace_bytes < L.total_floats * sizeof(float)) return GDN_ERR_SHAPE;
     if (!aligned16(workspace)) return GDN_ERR_ALIGN;
-    const long long rows = static_cast<long long>(n_seqs) * n_tokens;
     if (rows * n_v_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     const int S = state_size, H = n_v_heads, Hk = n_k_heads;
     float *ws = static_cast<float *>(workspace);
@@ -248,18 +257,18 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
         const int C = (2 * Hk + H) * S;
         const dim3 grid((C + kHistThreads - 1) / kHistThreads, n_tokens, n_seqs);
         conv_history_snapshots_kernel<<<grid, kHistThreads, 0, cs>>>(
-            qkv, conv_state, conv_snaps, n_tokens, C, conv_kernel - 1, slots, pool);
+            qkv, conv_state, conv_snaps, seqs, C, conv_kernel - 1, slots, pool);
         GDN_TRY(launch_status());
     }
     switch (S) {
-        case 32: GDN_TRY(launch_conv_split_norm<1>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
-        case 64: GDN_TRY(launch_conv_split_norm<2>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
-        case 128: GDN_TRY(launch_conv_split_norm<4>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
-        default: GDN_TRY(launch_conv_split_norm<8>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, n_tokens, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
+        case 32: GDN_TRY(launch_conv_split_norm<1>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, seqs, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
+        case 64: GDN_TRY(launch_conv_split_norm<2>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, seqs, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
+        case 128: GDN_TRY(launch_conv_split_norm<4>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, seqs, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
+        default: GDN_TRY(launch_conv_split_norm<8>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, seqs, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
     }
     GDN_TRY(gdn_decay_gate(alpha, dt, a, g, H, static_cast<int>(rows), stream));
     GDN_TRY(gdn_beta_sigmoid(b, beta, static_cast<int>(rows * H), stream));
-    if (chunked) {
+    if (chunked && seqs.cu == nullptr) {
         // the two-phase form in the bytes past the intermediates, if they hold one chunk
         const size_t base = (L.total_floats * sizeof(float) + 15) / 16 * 16;
         const size_t one_chunk = gdn_recurrence_scan_chunked_ws_size(n_seqs, 1, H, S);
@@ -272,16 +281,20 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
             GDN_TRY(gdn_recurrence_scan_chunked(state, q, k, v, g, beta, out, n_seqs, n_tokens,
                                                 Hk, H, S, scale, slots, pool, nullptr, stream));
         }
-    } else if (snapshots) {
-        GDN_TRY(gdn_recurrence_scan_snapshots(state, q, k, v, g, beta, out, snaps, n_seqs,
-                                              n_tokens, Hk, H, S, scale, slots, pool, nullptr,
-                                              stream));
+    } else if (chunked) {
+        // ragged: the two-phase form if the bytes past the intermediates hold every chunk
+        const size_t base = (L.total_floats * sizeof(float) + 15) / 16 * 16;
+        GDN_TRY(launch_chunked_seqs(state, q, k, v, g, beta, out, n_seqs, seqs, Hk, H, scale,
+                                    slots, pool, nullptr,
+                                    workspace_bytes > base ? static_cast<char *>(workspace) + base
+                                                           : nullptr,
+                                    workspace_bytes > base ? workspace_bytes - base : 0, cs));
     } else {
-        GDN_TRY(gdn_recurrence_scan(state, q, k, v, g, beta, out, n_seqs, n_tokens, Hk, H, S,
-                                    scale, slots, pool, nullptr, stream));
+        GDN_TRY(launch_scan_seqs(state, q, k, v, g, beta, out, n_seqs, seqs, Hk, H, S, scale,
+                                 slots, pool, nullptr, snapshots ? snaps : nullptr, cs));
     }
-    return launch_gated_norm(out, norm_w, z, out, rows * H, S, norm_eps,
-                             static_cast<long long>(n_tokens) * H, slots, pool, as_cuda(stream));
+    return launch_gated_norm_seqs(out, norm_w, z, out, rows * H, S, norm_eps, H, n_seqs, seqs,
+                                  slots, pool, cs);
 }
 
 }  // namespace
@@ -296,7 +309,8 @@ gdn_status gdn_block_prefill(const float *qkv, const float *conv_w, float *conv_
                              float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
                              void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
     return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
-                        n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                        uniform_seqs(n_seqs, n_tokens), n_k_heads, n_v_heads, state_size,
+                        conv_kernel, scale, l2_eps,
                         norm_eps, slots, pool, err_count, workspace, workspace_bytes, stream, false);
 }
 
@@ -313,7 +327,8 @@ gdn_status gdn_block_prefill_snapshots(const float *qkv, const float *conv_w,
     if (!snaps || !conv_snaps) return GDN_ERR_NULL;
     if (!aligned16(snaps)) return GDN_ERR_ALIGN;
     return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
-                        n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                        uniform_seqs(n_seqs, n_tokens), n_k_heads, n_v_heads, state_size,
+                        conv_kernel, scale, l2_eps,
                         norm_eps, slots, pool, err_count, workspace, workspace_bytes, stream, false,
                         snaps, conv_snaps);
 }
@@ -328,8 +343,85 @@ gdn_status gdn_block_prefill_chunked(const float *qkv, const float *conv_w, floa
                                      void *workspace, size_t workspace_bytes,
                                      gdn_stream_t stream) {
     return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
-                        n_tokens, n_k_heads, n_v_heads, state_size, conv_kernel, scale, l2_eps,
+                        uniform_seqs(n_seqs, n_tokens), n_k_heads, n_v_heads, state_size,
+                        conv_kernel, scale, l2_eps,
                         norm_eps, slots, pool, err_count, workspace, workspace_bytes, stream, true);
+}
+
+}  // extern "C"
+
+// ============================================================================ ragged batches
+// The prefill block over sequences of different lengths packed token-major: sequence
+// n owns positions cu_seqlens[n] .. cu_seqlens[n+1] - 1 of every [total][...] array.
+// Each kernel finds its sequence's range through the same SeqMap as the uniform
+// calls, so a sequence gets the bits it would get in a call of its own.
+extern "C" {
+
+size_t gdn_block_prefill_varlen_workspace_size(int n_seqs, int total_tokens, int n_k_heads,
+                                               int n_v_heads, int state_size) {
+    if (n_seqs < 0 || total_tokens < 0 || n_k_heads < 1 || n_v_heads < 1 || state_size < 1)
+        return 0;
+    return PrefillLayout(total_tokens, n_k_heads, n_v_heads, state_size).total_floats *
+           sizeof(float);
+}
+
+size_t gdn_block_prefill_chunked_varlen_workspace_size(int n_seqs, int total_tokens,
+                                                       int n_k_heads, int n_v_heads,
+                                                       int state_size) {
+    const size_t base = gdn_block_prefill_varlen_workspace_size(n_seqs, total_tokens, n_k_heads,
+                                                                n_v_heads, state_size);
+    if (base == 0 || state_size != 128 || n_seqs < 1) return base;
+    return (base + 15) / 16 * 16 + ragged_chunked_ws_size(n_seqs, total_tokens, n_v_heads);
+}
+
+gdn_status gdn_block_prefill_varlen(const float *qkv, const float *conv_w, float *conv_state,
+                                    const float *alpha, const float *b, const float *dt,
+                                    const float *a, const float *z, const float *norm_w,
+                                    float *state, float *out, const int32_t *cu_seqlens,
+                                    int n_seqs, int total_tokens, int max_tokens, int n_k_heads,
+                                    int n_v_heads, int state_size, int conv_kernel, float scale,
+                                    float l2_eps, float norm_eps, const int32_t *slots, int pool,
+                                    int32_t *err_count, void *workspace, size_t workspace_bytes,
+                                    gdn_stream_t stream) {
+    GDN_TRY(check_varlen(cu_seqlens, n_seqs, total_tokens, max_tokens));
+    return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                        SeqMap{cu_seqlens, max_tokens, total_tokens}, n_k_heads, n_v_heads,
+                        state_size, conv_kernel, scale, l2_eps, norm_eps, slots, pool, err_count,
+                        workspace, workspace_bytes, stream, false);
+}
+
+gdn_status gdn_block_prefill_chunked_varlen(const float *qkv, const float *conv_w,
+                                            float *conv_state, const float *alpha,
+                                            const float *b, const float *dt, const float *a,
+                                            const float *z, const float *norm_w, float *state,
+                                            float *out, const int32_t *cu_seqlens, int n_seqs,
+                                            int total_tokens, int max_tokens, int n_k_heads,
+                                            int n_v_heads, int state_size, int conv_kernel,
+                                            float scale, float l2_eps, float norm_eps,
+                                            const int32_t *slots, int pool, int32_t *err_count,
+                                            void *workspace, size_t workspace_bytes,
+                                            gdn_stream_t stream) {
+    GDN_TRY(check_varlen(cu_seqlens, n_seqs, total_tokens, max_tokens));
+    return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                        SeqMap{cu_seqlens, max_tokens, total_tokens}, n_k_heads, n_v_heads,
+                        state_size, conv_kernel, scale, l2_eps, norm_eps, slots, pool, err_count,
+                        workspace, workspace_bytes, stream, true);
+}
+
+gdn_status gdn_block_prefill_snapshots_varlen(
+    const float *qkv, const float *conv_w, float *conv_state, const float *alpha, const float *b,
+    const float *dt, const float *a, const float *z, const float *norm_w, float *state, float *out,
+    float *snaps, float *conv_snaps, const int32_t *cu_seqlens, int n_seqs, int total_tokens,
+    int max_tokens, int n_k_heads, int n_v_heads, int state_size, int conv_kernel, float scale,
+    float l2_eps, float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
+    void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    GDN_TRY(check_varlen(cu_seqlens, n_seqs, total_tokens, max_tokens));
+    if (!snaps || !conv_snaps) return GDN_ERR_NULL;
+    if (!aligned16(snaps)) return GDN_ERR_ALIGN;
+    return prefill_impl(qkv, conv_w, conv_state, alpha, b, dt, a, z, norm_w, state, out, n_seqs,
+                        SeqMap{cu_seqlens, max_tokens, total_tokens}, n_k_heads, n_v_heads,
+                        state_size, conv_kernel, scale, l2_eps, norm_eps, slots, pool, err_count,
+                        workspace, workspace_bytes, stream, false, snaps, conv_snaps);
 }
 
 }  // extern "C"
@@ -379,9 +471,8 @@ extern "C" gdn_status gdn_block_prefill_noalloc(
     gdn_stream_t stream) {
     if (n_seqs < 0 || n_tokens < 0 || n_k_heads < 1 || n_v_heads < 1 || state_size < 1)
         return GDN_ERR_SHAPE;
-    const size_t need =
-        PrefillLayout(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size).total_floats *
-        sizeof(float);
+    const size_t need = PrefillLayout(static_cast<long long>(n_seqs) * n_tokens, n_k_heads,
+                                      n_v_heads, state_size).total_floats * sizeof(float);
     if (need > kNoAllocScratchBytes) return GDN_ERR_UNSUPPORTED;  // beyond the fixed scratch
     void *scratch = nullptr;
     GDN_TRY(scratch_on_current_device(&scratch));

@@ -180,7 +180,7 @@ template <int E, bool SNAP>
 __global__ void __launch_bounds__(ScanSmem<E>::kThreads, ScanSmem<E>::kMinBlocks) recurrence_scan_kernel(
     float *state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
-    float *__restrict__ y, int n_tokens, int n_k_heads, int n_v_heads, float scale,
+    float *__restrict__ y, const SeqMap seqs, int n_k_heads, int n_v_heads, float scale,
     const int32_t *__restrict__ slots, int pool, int32_t *err_count, float *__restrict__ snaps) {
     constexpr int S = 32 * E, TC = kScanTok;
     using L = ScanSmem<E>;
@@ -196,10 +196,13 @@ __global__ void __launch_bounds__(ScanSmem<E>::kThreads, ScanSmem<E>::kMinBlocks
     const int n = blockIdx.x / (kBlocksPerHead * n_v_heads);
     const int kh = vh % n_k_heads;
     const int slot = slots ? slots[n] : n;
-    if (slot < 0 || slot >= pool) {
+    size_t tok0;   // first position of sequence n in the token-major arrays
+    int n_tokens;  // its length
+    if (slot < 0 || slot >= pool || !seqs.range(n, tok0, n_tokens)) {
         if (err_count && vh == 0 && part == 0 && threadIdx.x == 0) atomicAdd(err_count, 1);
         return;
     }
+    if (n_tokens == 0) return;  // uniform over the CTA: nothing to scan
     if (threadIdx.x == 0) {
         for (int s = 0; s < kScanDepth; ++s) {
             mbar_init(full + s, 1);
@@ -211,10 +214,9 @@ __global__ void __launch_bounds__(ScanSmem<E>::kThreads, ScanSmem<E>::kMinBlocks
     const int n_chunks = (n_tokens + TC - 1) / TC;
     const size_t kq_tok = static_cast<size_t>(n_k_heads) * S;   // q/k stride per token
     const size_t v_tok = static_cast<size_t>(n_v_heads) * S;    // v/y stride per token
-    const float *kbase = k + (static_cast<size_t>(n) * n_tokens * n_k_heads + kh) * S;
-    const float *qbase = q + (static_cast<size_t>(n) * n_tokens * n_k_heads + kh) * S;
-    const float *vbase = v + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S +
-                         part * kScanRows;
+    const float *kbase = k + (tok0 * n_k_heads + kh) * S;
+    const float *qbase = q + (tok0 * n_k_heads + kh) * S;
+    const float *vbase = v + (tok0 * n_v_heads + vh) * S + part * kScanRows;
 
     if (warp == kScanWarps) {
         // ---- producer warp: lane t copies token t of each chunk.
@@ -256,12 +258,12 @@ __global__ void __launch_bounds__(ScanSmem<E>::kThreads, ScanSmem<E>::kMinBlocks
     float *grow = state + ((static_cast<size_t>(slot) * n_v_heads + vh) * S + j) * S;
     float row[8][E];
     load_group<E>(row, grow, gq);
-    const size_t gb_base = static_cast<size_t>(n) * n_tokens * n_v_heads + vh;
-    float *yrow = y + (static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S + j;
-    // snapshot of token t: snaps[n][t][H][S][S], the state layout of one slot
+    const size_t gb_base = tok0 * n_v_heads + vh;
+    float *yrow = y + (tok0 * n_v_heads + vh) * S + j;
+    // snapshot after position t of sequence n: at packed position tok0 + t of snaps
+    // ([N][T][H][S][S] for a uniform batch), the state layout of one slot
     const size_t snap_tok = static_cast<size_t>(n_v_heads) * S * S;
-    float *srow = SNAP ? snaps + ((static_cast<size_t>(n) * n_tokens * n_v_heads + vh) * S + j) * S
-                       : nullptr;
+    float *srow = SNAP ? snaps + ((tok0 * n_v_heads + vh) * S + j) * S : nullptr;
 
     // g and beta of token (chunk*TC + lane), one chunk ahead.
     auto fetch_gb = [&](int c, float &dec, float &bt) {
@@ -356,7 +358,7 @@ gdn_status launch_decode(float *state, const float *q, const float *k, const flo
 
 template <int E, bool SNAP>
 gdn_status launch_scan(float *state, const float *q, const float *k, const float *v,
-                       const float *g, const float *beta, float *y, int n_seqs, int n_tokens,
+                       const float *g, const float *beta, float *y, int n_seqs, SeqMap seqs,
                        int n_k_heads, int n_v_heads, float scale, const int32_t *slots, int pool,
                        int32_t *err_count, float *snaps, cudaStream_t s) {
     constexpr int S = 32 * E;
@@ -365,7 +367,7 @@ gdn_status launch_scan(float *state, const float *q, const float *k, const float
     const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / ScanSmem<E>::kRows);
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     recurrence_scan_kernel<E, SNAP><<<static_cast<unsigned>(blocks), ScanSmem<E>::kThreads, smem, s>>>(
-        state, q, k, v, g, beta, y, n_tokens, n_k_heads, n_v_heads, scale, slots, pool,
+        state, q, k, v, g, beta, y, seqs, n_k_heads, n_v_heads, scale, slots, pool,
         err_count, snaps);
     return launch_status();
 }
@@ -413,6 +415,20 @@ gdn_status decode_entry(float *state, const float *q, const float *k, const floa
 }
 
 template <bool SNAP>
+gdn_status scan_launch(float *state, const float *q, const float *k, const float *v,
+                       const float *g, const float *beta, float *y, int n_seqs, SeqMap seqs,
+                       int n_k_heads, int n_v_heads, int state_size, float scale,
+                       const int32_t *slots, int pool, int32_t *err_count, float *snaps,
+                       cudaStream_t s) {
+    switch (state_size) {
+        case 32: return launch_scan<1, SNAP>(state, q, k, v, g, beta, y, n_seqs, seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
+        case 64: return launch_scan<2, SNAP>(state, q, k, v, g, beta, y, n_seqs, seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
+        case 128: return launch_scan<4, SNAP>(state, q, k, v, g, beta, y, n_seqs, seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
+        default: return launch_scan<8, SNAP>(state, q, k, v, g, beta, y, n_seqs, seqs, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
+    }
+}
+
+template <bool SNAP>
 gdn_status scan_entry(float *state, const float *q, const float *k, const float *v,
                       const float *g, const float *beta, float *y, int n_seqs, int n_tokens,
                       int n_k_heads, int n_v_heads, int state_size, float scale,
@@ -423,13 +439,9 @@ gdn_status scan_entry(float *state, const float *q, const float *k, const float 
     if (SNAP && snaps == nullptr) return GDN_ERR_NULL;
     if (SNAP && !aligned16(snaps)) return GDN_ERR_ALIGN;
     if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
-    const cudaStream_t s = as_cuda(stream);
-    switch (state_size) {
-        case 32: return launch_scan<1, SNAP>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
-        case 64: return launch_scan<2, SNAP>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
-        case 128: return launch_scan<4, SNAP>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
-        default: return launch_scan<8, SNAP>(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads, scale, slots, pool, err_count, snaps, s);
-    }
+    return scan_launch<SNAP>(state, q, k, v, g, beta, y, n_seqs, uniform_seqs(n_seqs, n_tokens),
+                             n_k_heads, n_v_heads, state_size, scale, slots, pool, err_count,
+                             snaps, as_cuda(stream));
 }
 
 }  // namespace
@@ -477,3 +489,43 @@ gdn_status gdn_recurrence_scan_snapshots(float *state, const float *q, const flo
 }
 
 }  // extern "C"
+
+// ============================================================================ ragged batches
+namespace gdn {
+
+gdn_status launch_scan_seqs(float *state, const float *q, const float *k, const float *v,
+                            const float *g, const float *beta, float *y, int n_seqs, SeqMap seqs,
+                            int n_k_heads, int n_v_heads, int state_size, float scale,
+                            const int32_t *slots, int pool, int32_t *err_count, float *snaps,
+                            cudaStream_t s) {
+    if (snaps)
+        return scan_launch<true>(state, q, k, v, g, beta, y, n_seqs, seqs, n_k_heads, n_v_heads,
+                                 state_size, scale, slots, pool, err_count, snaps, s);
+    return scan_launch<false>(state, q, k, v, g, beta, y, n_seqs, seqs, n_k_heads, n_v_heads,
+                              state_size, scale, slots, pool, err_count, nullptr, s);
+}
+
+gdn_status check_varlen(const int32_t *cu_seqlens, int n_seqs, int total_tokens, int max_tokens) {
+    if (!cu_seqlens) return GDN_ERR_NULL;
+    if (n_seqs < 0 || total_tokens < 0 || max_tokens < 0) return GDN_ERR_SHAPE;
+    return GDN_OK;
+}
+
+}  // namespace gdn
+
+extern "C" gdn_status gdn_recurrence_scan_varlen(float *state, const float *q, const float *k,
+                                                 const float *v, const float *g,
+                                                 const float *beta, float *y,
+                                                 const int32_t *cu_seqlens, int n_seqs,
+                                                 int total_tokens, int max_tokens,
+                                                 int n_k_heads, int n_v_heads, int state_size,
+                                                 float scale, const int32_t *slots, int pool,
+                                                 int32_t *err_count, gdn_stream_t stream) {
+    GDN_TRY(check_varlen(cu_seqlens, n_seqs, total_tokens, max_tokens));
+    GDN_TRY(check_recurrence_args(state, q, k, v, g, beta, y, n_seqs, max_tokens, n_k_heads,
+                                  n_v_heads, state_size, slots, pool));
+    if (n_seqs == 0 || total_tokens == 0 || max_tokens == 0) return GDN_OK;
+    return launch_scan_seqs(state, q, k, v, g, beta, y, n_seqs,
+                            SeqMap{cu_seqlens, max_tokens, total_tokens}, n_k_heads, n_v_heads,
+                            state_size, scale, slots, pool, err_count, nullptr, as_cuda(stream));
+}

@@ -85,7 +85,7 @@ def get_config(which, **overrides):
 
 _TAGS = {"state": 1, "conv_state": 2, "conv_w": 3, "norm_w": 4, "gate_params": 5, "slots": 6,
          "qkv": 11, "gate": 12, "b": 13, "z": 14, "q": 21, "k": 22, "v": 23, "g": 24, "beta": 25,
-         "pqkv": 31, "pgate": 32, "pb": 33, "pz": 34}
+         "pqkv": 31, "pgate": 32, "pb": 33, "pz": 34, "lengths": 41}
 
 
 def _rng(cfg, tag, idx=0, step=0):
@@ -188,6 +188,20 @@ def prefill_seq(cfg, n, n_tokens=None):
     alpha = (np.log(np.expm1(g / a.astype(np.float64))) - dt).astype(np.float32)
     return {"qkv": _normal(_rng(cfg, "pqkv", n), (T, C)), "alpha": alpha,
             "b": _normal(_rng(cfg, "pb", n), (T, H)), "z": _normal(_rng(cfg, "pz", n), (T, H, S))}
+
+
+def ragged_lengths(cfg, total_tokens, lo=1, hi=4096):
+    """Sequence lengths of a ragged prefill batch: log-uniform in [lo, hi] (seeded), drawn
+    until they add up to total_tokens (the last one trimmed to fit), so short prompts
+    and long ones share a call as they do in a serving prefill batch."""
+    rng = _rng(cfg, "lengths")
+    lengths, left = [], int(total_tokens)
+    while left > 0:
+        L = int(np.exp(rng.uniform(np.log(lo), np.log(hi + 1))))
+        L = min(max(L, lo), hi, left)
+        lengths.append(L)
+        left -= L
+    return lengths
 
 
 def block_static(cfg):

@@ -370,6 +370,122 @@ gdn_status gdn_block_prefill_chunked(const float *qkv, const float *conv_w, floa
                                      void *workspace, size_t workspace_bytes,
                                      gdn_stream_t stream);
 
+/* ---------------------------------------------------------------- ragged batches
+ * A prefill batch of sequences of different lengths, packed token-major: every
+ * [N][T][...] array of the uniform calls becomes [total_tokens][...], and sequence n
+ * owns positions cu_seqlens[n] .. cu_seqlens[n+1] - 1 of it. ssm_gated_delta.cu,
+ * "BATCHED (prefill) variants", runs one sequence of n positions per launch; these
+ * calls run a whole batch of mixed lengths in the launches of one uniform call, and
+ * each sequence gets the bits a call of its own would give it (same kernels, same
+ * order of operations).
+ * - cu_seqlens: DEVICE int32[n_seqs + 1], owned by the caller. It stays on the device
+ *   (the host never reads it), so its entries are checked by the kernels: a sequence
+ *   whose range is not valid (cu_seqlens[n] < 0, cu_seqlens[n+1] < cu_seqlens[n],
+ *   cu_seqlens[n+1] > total_tokens, or a length above max_tokens) is skipped as an
+ *   out-of-range slot is -- its state, conv_state and out rows are not written -- and
+ *   counted once in err_count. Ranges of different sequences must not overlap
+ *   (overlapping ranges race: undefined results, but every access stays inside the
+ *   arrays). Rows of out, and snapshots, at positions no sequence owns are not
+ *   written. A sequence of length 0 is a no-op.
+ * - total_tokens: rows of the packed arrays; max_tokens: an upper bound on any one
+ *   sequence's length (it sizes the grids; host int).
+ * - Snapshots (the _snapshots form) are packed the same way: the state after position
+ *   t of sequence n is snaps[cu_seqlens[n] + t], [total_tokens][H][S][S]; the conv
+ *   history likewise, [total_tokens][C][K-1].
+ * - Everything else (slots, pool, err_count, layouts of state and conv_state, scale,
+ *   eps, alignment, workspace ownership, no allocation) as for the uniform calls. */
+
+/* The sequential scan over a ragged batch: q, k [total][Hk][S]; v, y [total][H][S];
+ * g, beta [total][H]. Otherwise as gdn_recurrence_scan. */
+gdn_status gdn_recurrence_scan_varlen(float *state, const float *q, const float *k,
+                                      const float *v, const float *g, const float *beta,
+                                      float *y, const int32_t *cu_seqlens, int n_seqs,
+                                      int total_tokens, int max_tokens, int n_k_heads,
+                                      int n_v_heads, int state_size, float scale,
+                                      const int32_t *slots, int pool, int32_t *err_count,
+                                      gdn_stream_t stream);
+
+/* Bytes of workspace for gdn_recurrence_scan_chunked_varlen to take its two-phase form:
+ * (total_tokens / 32 + n_seqs) * n_v_heads * 36 KiB -- chunk c of sequence n takes the
+ * block row cu_seqlens[n] / 32 + n + c, whatever the lengths. 0 for invalid sizes or a
+ * state_size other than 128. */
+size_t gdn_recurrence_scan_chunked_varlen_ws_size(int n_seqs, int total_tokens, int n_v_heads,
+                                                  int state_size);
+
+/* The chunked tensor-core scan (state_size 128) over a ragged batch; layouts as
+ * gdn_recurrence_scan_varlen. With a workspace of at least
+ * gdn_recurrence_scan_chunked_varlen_ws_size() bytes (16-byte aligned, contents
+ * irrelevant, garbage afterwards) it runs the two-phase form of
+ * gdn_recurrence_scan_chunked_ws in one wave; with a smaller one or NULL, the one-kernel
+ * form of gdn_recurrence_scan_chunked. Both give the same bits. */
+gdn_status gdn_recurrence_scan_chunked_varlen(float *state, const float *q, const float *k,
+                                              const float *v, const float *g, const float *beta,
+                                              float *y, const int32_t *cu_seqlens, int n_seqs,
+                                              int total_tokens, int max_tokens, int n_k_heads,
+                                              int n_v_heads, int state_size, float scale,
+                                              const int32_t *slots, int pool,
+                                              int32_t *err_count, void *workspace,
+                                              size_t workspace_bytes, gdn_stream_t stream);
+
+/* Workspace of the ragged prefill blocks: gdn_block_prefill_varlen and _snapshots_varlen
+ * need gdn_block_prefill_varlen_workspace_size() bytes (the intermediates of
+ * total_tokens positions); gdn_block_prefill_chunked_varlen takes its two-phase chunked
+ * scan when given gdn_block_prefill_chunked_varlen_workspace_size() bytes, else (at
+ * least the former) the one-kernel form, with the same bits. */
+size_t gdn_block_prefill_varlen_workspace_size(int n_seqs, int total_tokens, int n_k_heads,
+                                               int n_v_heads, int state_size);
+size_t gdn_block_prefill_chunked_varlen_workspace_size(int n_seqs, int total_tokens,
+                                                       int n_k_heads, int n_v_heads,
+                                                       int state_size);
+
+/* gdn_block_prefill over a ragged batch: qkv [total][C]; alpha, b [total][H]; z, out
+ * [total][H][S]; any K in [2, 8]. Each sequence's out, state and conv_state are the
+ * bits of gdn_block_prefill on that sequence alone. */
+gdn_status gdn_block_prefill_varlen(const float *qkv, const float *conv_w, float *conv_state,
+                                    const float *alpha, const float *b, const float *dt,
+                                    const float *a, const float *z, const float *norm_w,
+                                    float *state, float *out, const int32_t *cu_seqlens,
+                                    int n_seqs, int total_tokens, int max_tokens, int n_k_heads,
+                                    int n_v_heads, int state_size, int conv_kernel, float scale,
+                                    float l2_eps, float norm_eps, const int32_t *slots, int pool,
+                                    int32_t *err_count, void *workspace, size_t workspace_bytes,
+                                    gdn_stream_t stream);
+
+/* gdn_block_prefill_chunked over a ragged batch (state_size 128); each sequence gets the
+ * bits of gdn_block_prefill_chunked on that sequence alone. */
+gdn_status gdn_block_prefill_chunked_varlen(const float *qkv, const float *conv_w,
+                                            float *conv_state, const float *alpha,
+                                            const float *b, const float *dt, const float *a,
+                                            const float *z, const float *norm_w, float *state,
+                                            float *out, const int32_t *cu_seqlens, int n_seqs,
+                                            int total_tokens, int max_tokens, int n_k_heads,
+                                            int n_v_heads, int state_size, int conv_kernel,
+                                            float scale, float l2_eps, float norm_eps,
+                                            const int32_t *slots, int pool, int32_t *err_count,
+                                            void *workspace, size_t workspace_bytes,
+                                            gdn_stream_t stream);
+
+/* gdn_block_prefill_snapshots over a ragged batch: snaps [total][H][S][S], conv_snaps
+ * [total][C][K-1] packed as the positions are; max_tokens above 65535 is
+ * GDN_ERR_UNSUPPORTED. gdn_snapshot_restore_varlen rolls each sequence back. */
+gdn_status gdn_block_prefill_snapshots_varlen(
+    const float *qkv, const float *conv_w, float *conv_state, const float *alpha, const float *b,
+    const float *dt, const float *a, const float *z, const float *norm_w, float *state, float *out,
+    float *snaps, float *conv_snaps, const int32_t *cu_seqlens, int n_seqs, int total_tokens,
+    int max_tokens, int n_k_heads, int n_v_heads, int state_size, int conv_kernel, float scale,
+    float l2_eps, float norm_eps, const int32_t *slots, int pool, int32_t *err_count,
+    void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/* gdn_snapshot_restore for snapshots of a ragged batch: sequence n with M = accepted[n]
+ * in [1, its length] gets snaps[cu_seqlens[n] + M - 1] (and conv_snaps likewise). A
+ * sequence whose M, slot or range is not valid is left untouched and counted once. */
+gdn_status gdn_snapshot_restore_varlen(float *state, const float *snaps, float *conv_state,
+                                       const float *conv_snaps, const int32_t *accepted,
+                                       const int32_t *cu_seqlens, int n_seqs, int total_tokens,
+                                       int max_tokens, int n_v_heads, int state_size,
+                                       int conv_dim, int conv_kernel, const int32_t *slots,
+                                       int pool, int32_t *err_count, gdn_stream_t stream);
+
 /* Bytes of the fixed device scratch gdn_block_prefill_noalloc works in. */
 #define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -325,3 +325,79 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(4)
     with pytest.raises(ValueError):
         gdn.gdn_beta_sigmoid(x, x, 4, stream=0)
+
+
+def declared_signatures():
+    """{name: [parameter type strings]} of every function include/gdn.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"#define[^\n]*", "", text)
+    sigs = {}
+    for m in re.finditer(r"\b(gdn_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).replace("\n", " ").split(",")]
+        sigs[m.group(1)] = [] if params == ["void"] else params
+    return sigs
+
+
+def _ctype_of(param):
+    """The ctypes type a header parameter declaration maps to."""
+    decl = " ".join(param.split())
+    if "*" in decl or decl.startswith("gdn_stream_t"):
+        return ctypes.c_void_p
+    if decl.startswith("size_t"):
+        return ctypes.c_size_t
+    if decl.startswith("float"):
+        return ctypes.c_float
+    if decl.startswith(("int", "gdn_status")):
+        return ctypes.c_int
+    raise AssertionError(f"unmapped parameter type: {param}")
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every ctypes signature of the binding has the header's parameter count and types:
+    a miscounted argument list would pass garbage through the C ABI."""
+    sigs = declared_signatures()
+    assert set(sigs) == set(declared_functions())
+    for name, params in sigs.items():
+        assert name in gdn._SIGS, f"binding has no signature for {name}"
+        argtypes = gdn._SIGS[name][0]
+        assert len(argtypes) == len(params), f"{name}: {len(argtypes)} != {len(params)} params"
+        for i, (got, param) in enumerate(zip(argtypes, params)):
+            assert got is _ctype_of(param), f"{name} argument {i} ({param}): {got}"
+
+
+def test_varlen_validation(lib):
+    """Ragged-batch calls: NULL cu_seqlens, negative sizes, and the documented no-ops are
+    decided on the host, before anything is enqueued."""
+    f = lib.gdn_recurrence_scan_varlen
+    # state q k v g beta y cu | n_seqs total max Hk H S | scale slots pool err stream
+    assert f(P, P, P, P, P, P, P, None, 2, 10, 8, 2, 4, 32, 0.1, None, 2, None, None) == NULL
+    assert f(P, P, P, P, P, P, P, P, -1, 10, 8, 2, 4, 32, 0.1, None, 2, None, None) == SHAPE
+    assert f(P, P, P, P, P, P, P, P, 2, -1, 8, 2, 4, 32, 0.1, None, 2, None, None) == SHAPE
+    assert f(P, P, P, P, P, P, P, P, 2, 10, -1, 2, 4, 32, 0.1, None, 2, None, None) == SHAPE
+    assert f(P, P, P, P, P, P, P, P, 2, 10, 8, 3, 4, 32, 0.1, None, 2, None, None) == SHAPE
+    assert f(MIS, P, P, P, P, P, P, P, 2, 10, 8, 2, 4, 32, 0.1, None, 2, None, None) == ALIGN
+    assert f(P, P, P, P, P, P, P, P, 0, 0, 0, 2, 4, 32, 0.1, None, 1, None, None) == OK
+    assert f(P, P, P, P, P, P, P, P, 2, 0, 8, 2, 4, 32, 0.1, None, 2, None, None) == OK
+    c = lib.gdn_recurrence_scan_chunked_varlen
+    assert c(P, P, P, P, P, P, P, P, 2, 10, 8, 2, 4, 64, 0.1, None, 2, None, None, 0,
+             None) == UNSUP
+    assert c(P, P, P, P, P, P, P, P, 2, 10, 8, 2, 4, 128, 0.1, None, 2, None, MIS, 1 << 20,
+             None) == ALIGN
+    assert lib.gdn_recurrence_scan_chunked_varlen_ws_size(3, 100, 4, 128) == (100 // 32 + 3) * 4 * 36864
+    assert lib.gdn_recurrence_scan_chunked_varlen_ws_size(3, 100, 4, 64) == 0
+    b = lib.gdn_block_prefill_varlen
+    args = [P] * 11
+    tail = [2, 4, 32, 4, 0.1, 1e-6, 1e-6, None, 2, None]
+    assert b(*args, None, 2, 10, 8, *tail, P, 1 << 30, None) == NULL
+    assert b(*args, P, 2, 10, 8, *tail, P, 16, None) == SHAPE  # workspace too small
+    assert b(*args, P, 2, 0, 8, *tail, None, 0, None) == OK    # nothing to do
+    need = lib.gdn_block_prefill_varlen_workspace_size(2, 10, 2, 4, 32)
+    assert need == lib.gdn_block_prefill_workspace_size(1, 10, 2, 4, 32) > 0
+    assert (lib.gdn_block_prefill_chunked_varlen_workspace_size(2, 100, 2, 4, 128)
+            >= lib.gdn_block_prefill_varlen_workspace_size(2, 100, 2, 4, 128)
+            + lib.gdn_recurrence_scan_chunked_varlen_ws_size(2, 100, 4, 128))
+    r = lib.gdn_snapshot_restore_varlen
+    # state snaps conv_state conv_snaps accepted cu | n total max H S C K | slots pool err stream
+    assert r(P, P, None, None, P, None, 2, 10, 8, 4, 32, 0, 0, None, 2, None, None) == NULL
+    assert r(P, P, None, None, P, P, 2, -1, 8, 4, 32, 0, 0, None, 2, None, None) == SHAPE
+    assert r(P, P, P, None, P, P, 2, 10, 8, 4, 32, 8, 4, None, 2, None, None) == NULL
