@@ -30,7 +30,7 @@ __all__ = [
     "gdn_recurrence_scan_chunked_varlen", "gdn_block_prefill_varlen_workspace_size",
     "gdn_block_prefill_chunked_varlen_workspace_size", "gdn_block_prefill_varlen",
     "gdn_block_prefill_chunked_varlen", "gdn_block_prefill_snapshots_varlen",
-    "gdn_snapshot_restore_varlen",
+    "gdn_snapshot_restore_varlen", "gdn_selftest_bounded_wait",
 ]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_UNSUPPORTED",
@@ -52,6 +52,7 @@ _SIGS = {
     "gdn_status_str": ([_I], ctypes.c_char_p),
     "gdn_version": ([], _I),
     "gdn_device_error": ([_P], _I),
+    "gdn_selftest_bounded_wait": ([ctypes.c_uint, ctypes.c_uint, _P, _P], _I),
     "gdn_decay_gate": ([_P, _P, _P, _P, _I, _I, _P], _I),
     "gdn_beta_sigmoid": ([_P, _P, _I, _P], _I),
     "gdn_conv1d_silu": ([_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P], _I),
@@ -204,6 +205,14 @@ def gdn_version():
 def gdn_device_error(stream=None):
     """Synchronise the stream; raise GdnError if a kernel's bounded wait gave up."""
     _check("gdn_device_error", library().gdn_device_error(_stream(stream)))
+
+
+def gdn_selftest_bounded_wait(arm_mask, limit_us, out, stream=None):
+    """Enqueue the bounded-wait self-test: probe i (bit i of arm_mask) waits at most
+    limit_us for a copy that never comes and raises the device flag; `out` is a CUDA
+    float32 tensor of 4 elements (unarmed probes write 1.0 there)."""
+    _check("gdn_selftest_bounded_wait", library().gdn_selftest_bounded_wait(
+        int(arm_mask), int(limit_us), _ptr(out, "out"), _stream(stream)))
 
 
 def gdn_decay_gate(alpha, dt, a, g, n_heads, rows, stream=None):

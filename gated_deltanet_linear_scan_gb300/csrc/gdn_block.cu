@@ -687,6 +687,16 @@ gdn_status launch_block(BlockParams p, int n_seqs, cudaStream_t s) {
 
 }  // namespace
 
+// The bounded-wait self-test on this unit's watchdog flag (gdn_selftest_bounded_wait).
+__global__ void wait_probe_kernel_block(int arm, unsigned long long limit_ns, float *out) {
+    bounded_wait_probe(arm != 0, limit_ns, &g_watchdog, WD_STAGE_COPY, out);
+}
+
+gdn_status launch_wait_probe_block(bool arm, uint64_t limit_ns, float *out, cudaStream_t s) {
+    wait_probe_kernel_block<<<1, 1, 0, s>>>(arm ? 1 : 0, limit_ns, out);
+    return launch_status();
+}
+
 unsigned read_and_clear_watchdog_block(cudaStream_t s) {
     unsigned flags = 0;
     const unsigned zero = 0;

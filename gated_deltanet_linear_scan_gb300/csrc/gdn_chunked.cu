@@ -555,6 +555,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
 
 namespace gdn {
 
+// The bounded-wait self-test on this unit's watchdog flag (gdn_selftest_bounded_wait).
+__global__ void wait_probe_kernel_chunked(int arm, unsigned long long limit_ns, float *out) {
+    bounded_wait_probe(arm != 0, limit_ns, &g_watchdog_chunked, WD_STAGE_COPY, out);
+}
+
+gdn_status launch_wait_probe_chunked(bool arm, uint64_t limit_ns, float *out, cudaStream_t s) {
+    wait_probe_kernel_chunked<<<1, 1, 0, s>>>(arm ? 1 : 0, limit_ns, out);
+    return launch_status();
+}
+
 unsigned read_and_clear_watchdog_chunked(cudaStream_t s) {
     unsigned flags = 0;
     const unsigned zero = 0;

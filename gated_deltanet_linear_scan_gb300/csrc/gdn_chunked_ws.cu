@@ -693,6 +693,16 @@ gdn_status launch_advance(float *state, const float *q, const float *k, const fl
 
 }  // namespace
 
+// The bounded-wait self-test on this unit's watchdog flag (gdn_selftest_bounded_wait).
+__global__ void wait_probe_kernel_chunked_ws(int arm, unsigned long long limit_ns, float *out) {
+    bounded_wait_probe(arm != 0, limit_ns, &g_watchdog_chunked_ws, WD_STAGE_COPY, out);
+}
+
+gdn_status launch_wait_probe_chunked_ws(bool arm, uint64_t limit_ns, float *out, cudaStream_t s) {
+    wait_probe_kernel_chunked_ws<<<1, 1, 0, s>>>(arm ? 1 : 0, limit_ns, out);
+    return launch_status();
+}
+
 unsigned read_and_clear_watchdog_chunked_ws(cudaStream_t s) {
     unsigned flags = 0;
     const unsigned zero = 0;

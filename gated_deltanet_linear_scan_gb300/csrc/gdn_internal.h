@@ -113,6 +113,12 @@ gdn_status launch_chunked_one_kernel(float *state, const float *q, const float *
                                      float scale, const int32_t *slots, int pool,
                                      int32_t *err_count, cudaStream_t s);
 
+// Bounded-wait self-test kernels, one per translation unit with a watchdog flag.
+gdn_status launch_wait_probe_recurrence(bool arm, uint64_t limit_ns, float *out, cudaStream_t s);
+gdn_status launch_wait_probe_block(bool arm, uint64_t limit_ns, float *out, cudaStream_t s);
+gdn_status launch_wait_probe_chunked(bool arm, uint64_t limit_ns, float *out, cudaStream_t s);
+gdn_status launch_wait_probe_chunked_ws(bool arm, uint64_t limit_ns, float *out, cudaStream_t s);
+
 // Per-translation-unit watchdog flags (a bounded wait that gave up sets a bit).
 unsigned read_and_clear_watchdog_recurrence(cudaStream_t s);
 unsigned read_and_clear_watchdog_block(cudaStream_t s);

@@ -333,6 +333,18 @@ gdn_status gdn_device_error(gdn_stream_t stream) {
     return flags ? GDN_ERR_DEVICE : GDN_OK;
 }
 
+gdn_status gdn_selftest_bounded_wait(unsigned arm_mask, unsigned limit_us, float *out,
+                                     gdn_stream_t stream) {
+    if (!out) return GDN_ERR_NULL;
+    if (arm_mask > 15u || limit_us < 1 || limit_us > 2000000u) return GDN_ERR_SHAPE;
+    const cudaStream_t s = as_cuda(stream);
+    const uint64_t ns = 1000ull * limit_us;
+    GDN_TRY(launch_wait_probe_recurrence(arm_mask & 1u, ns, out + 0, s));
+    GDN_TRY(launch_wait_probe_block(arm_mask & 2u, ns, out + 1, s));
+    GDN_TRY(launch_wait_probe_chunked(arm_mask & 4u, ns, out + 2, s));
+    return launch_wait_probe_chunked_ws(arm_mask & 8u, ns, out + 3, s);
+}
+
 gdn_status gdn_decay_gate(const float *alpha, const float *dt, const float *a, float *g,
                           int n_heads, int rows, gdn_stream_t stream) {
     if (!alpha || !dt || !a || !g) return GDN_ERR_NULL;

@@ -83,6 +83,20 @@ int gdn_version(void);
  * if their kernels must be covered. */
 gdn_status gdn_device_error(gdn_stream_t stream);
 
+/* Self-test of the failure path above, for a caller's health check or a test suite.
+ * Enqueues four one-thread kernels, one on each watchdog flag gdn_device_error() reads;
+ * probe i (bit i of arm_mask set) waits, bounded by limit_us microseconds, for bytes
+ * that no copy will bring -- the wait runs out, the probe raises its flag and skips its
+ * guarded write, as a kernel whose copy never lands does. A probe whose bit is clear
+ * waits for a phase that completes at once and writes 1.0f to out[i]. So after the
+ * call gdn_device_error() returns GDN_ERR_DEVICE if arm_mask != 0 (then GDN_OK on the
+ * next call), out[i] keeps its contents for armed probes, and the context stays usable.
+ * Nothing faults, traps or waits without bound. The pages have no counterpart: their
+ * launchers return silently and their kernels have no bounded waits.
+ * out: device float[4]; arm_mask in [0, 15]; limit_us in [1, 2000000]. */
+gdn_status gdn_selftest_bounded_wait(unsigned arm_mask, unsigned limit_us, float *out,
+                                     gdn_stream_t stream);
+
 /* Decay gate. fm_kernel_ssm.m, decay-gate section; ssm_gated_delta.cu, glue kernels
  * (fc_ssm_decay_gate, _nx). Per row r and head h the log-decay is a[h] times the
  * softplus of alpha[r][h] + dt[h], softplus taken as the identity above 20:

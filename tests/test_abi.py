@@ -347,6 +347,8 @@ def _ctype_of(param):
         return ctypes.c_size_t
     if decl.startswith("float"):
         return ctypes.c_float
+    if decl.startswith("unsigned"):
+        return ctypes.c_uint
     if decl.startswith(("int", "gdn_status")):
         return ctypes.c_int
     raise AssertionError(f"unmapped parameter type: {param}")
@@ -401,3 +403,11 @@ def test_varlen_validation(lib):
     assert r(P, P, None, None, P, None, 2, 10, 8, 4, 32, 0, 0, None, 2, None, None) == NULL
     assert r(P, P, None, None, P, P, 2, -1, 8, 4, 32, 0, 0, None, 2, None, None) == SHAPE
     assert r(P, P, P, None, P, P, 2, 10, 8, 4, 32, 8, 4, None, 2, None, None) == NULL
+
+
+def test_selftest_validation(lib):
+    f = lib.gdn_selftest_bounded_wait
+    assert f(1, 1000, None, None) == NULL
+    assert f(16, 1000, P, None) == SHAPE
+    assert f(1, 0, P, None) == SHAPE
+    assert f(1, 2000001, P, None) == SHAPE
