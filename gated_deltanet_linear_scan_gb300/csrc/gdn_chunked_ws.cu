@@ -274,7 +274,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
     Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBars);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = n_v_heads, Hk = n_k_heads;
-    const int vh = blockIdx.x % H, n = blockIdx.x / H, kh = vh % Hk;
+    const int vh = blockIdx.x % H, kh = vh % Hk;
+    int n = blockIdx.x / H;
+    if (seqs.cu && n_seqs <= kLongestFirstMaxSeqs) {
+        // a small ragged batch: the longest sequences' CTAs first, so the longest chain
+        // of chunks starts at once instead of wherever its index puts it
+        __shared__ int pick;
+        n = seq_by_length_rank(seqs, n_seqs, n, &pick);
+    }
     const int slot = slots ? slots[n] : n;
     size_t row0;   // (n, t = 0) in the token-major arrays
     int n_tokens;  // positions of sequence n

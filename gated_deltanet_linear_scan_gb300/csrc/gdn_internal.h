@@ -40,6 +40,55 @@ inline SeqMap uniform_seqs(int n_seqs, int n_tokens) {
     return SeqMap{nullptr, n_tokens, static_cast<long long>(n_seqs) * n_tokens};
 }
 
+// The same search by a whole warp (every lane returns the answer): each round the lanes
+// probe 32 evenly spaced entries of the remaining range, so a batch of up to 32
+// sequences takes one coalesced load, 1024 two.
+__device__ __forceinline__ int warp_seq_of_position(const int32_t *cu, int n_seqs, long long pos) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = n_seqs;  // the answer is the last n in [lo, hi) with cu[n] <= pos, or lo - 1
+    while (hi - lo > 32) {
+        const int step = (hi - lo + 31) / 32;
+        const int idx = lo + lane * step;
+        const unsigned hit = __ballot_sync(0xffffffffu, idx < hi && cu[idx] <= pos);
+        if (hit == 0) return lo - 1;
+        const int last = 31 - __clz(hit);
+        lo += last * step;
+        hi = min(hi, lo + step);
+    }
+    const int idx = lo + lane;
+    const unsigned hit = __ballot_sync(0xffffffffu, idx < hi && cu[idx] <= pos);
+    return hit == 0 ? lo - 1 : lo + 31 - __clz(hit);
+}
+
+// Longest-first order of a ragged batch for CTA scheduling: the sequence whose valid
+// length is the rank-th largest (ties by index; invalid ranges count as length 0), found
+// by the whole CTA (every thread returns it; uses one int of shared memory and two
+// __syncthreads). O(n_seqs^2 / threads) work, so callers use it for small batches only.
+__device__ __forceinline__ int seq_by_length_rank(const SeqMap &seqs, int n_seqs, int rank,
+                                                  int *shared_slot) {
+    auto len_of = [&](int m) {
+        size_t t0;
+        int len;
+        return seqs.range(m, t0, len) ? len : 0;
+    };
+    if (threadIdx.x == 0) *shared_slot = rank;  // stays if no thread matches (cannot happen)
+    __syncthreads();
+    for (int m = threadIdx.x; m < n_seqs; m += blockDim.x) {
+        const int lm = len_of(m);
+        int above = 0;
+        for (int j = 0; j < n_seqs; ++j) {
+            const int lj = len_of(j);
+            above += (lj > lm) || (lj == lm && j < m);
+        }
+        if (above == rank) *shared_slot = m;
+    }
+    __syncthreads();
+    return *shared_slot;
+}
+
+// Ragged batches up to this many sequences run their per-sequence CTAs longest first.
+constexpr int kLongestFirstMaxSeqs = 256;
+
 // The last sequence n in [0, n_seqs) with cu[n] <= pos (binary search; -1 if none).
 // With a valid ragged batch that is the sequence owning position pos, if any.
 __device__ __forceinline__ int seq_of_position(const int32_t *cu, int n_seqs, long long pos) {

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) gated_norm_kernel(const float *y,
         const long long pos = row / heads;
         int n;
         if (seqs.cu) {
-            n = seq_of_position(seqs.cu, n_seqs, pos);
+            n = warp_seq_of_position(seqs.cu, n_seqs, pos);  // row (and pos) is per warp
             size_t t0;
             int len;
             if (n < 0 || !seqs.range(n, t0, len) || pos >= static_cast<long long>(t0) + len) return;

@@ -43,23 +43,59 @@ struct PrefillLayout {
 template <int E>
 __host__ __device__ constexpr int conv_norm_positions() { return E >= 8 ? 16 : 32; }
 
-template <int E, int K>
+// Grid, uniform batch: (slice, block of P positions, sequence). Ragged batch: (slice,
+// block slot); block b of sequence n takes slot cu[n] / P + n + b (the chunk-slot scheme
+// of the chunked scan: slots of consecutive sequences never collide and number at most
+// total / P + n_seqs), so no CTA is launched for positions past a sequence's end.
+template <int E, int K, bool RAGGED>
 __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
     const float *__restrict__ qkv, const float *__restrict__ w, float *conv_state,
     float *__restrict__ q, float *__restrict__ k, float *__restrict__ v, const SeqMap seqs,
-    int n_k_heads, int n_v_heads, float eps, const int32_t *__restrict__ slots, int pool,
-    int32_t *err_count) {
+    int n_seqs, int n_k_heads, int n_v_heads, float eps, const int32_t *__restrict__ slots,
+    int pool, int32_t *err_count) {
     constexpr int S = 32 * E, TAPS = K - 1, P = conv_norm_positions<E>(), ROW = S + 4;
     __shared__ __align__(16) float tile[P * ROW];
-    const int sl = blockIdx.x, n = blockIdx.z, c = threadIdx.x;
-    const int slot = slots ? slots[n] : n;
+    const int sl = blockIdx.x, c = threadIdx.x;
+    int n, t0;
     size_t seq0;   // first position of sequence n in the token-major arrays
     int n_tokens;  // its length
-    if (slot < 0 || slot >= pool || !seqs.range(n, seq0, n_tokens)) {  // uniform over the CTA
-        if (err_count && sl == 0 && blockIdx.y == 0 && c == 0) atomicAdd(err_count, 1);
-        return;
+    if (!RAGGED) {
+        n = blockIdx.z;
+        t0 = blockIdx.y * P;
+        seqs.range(n, seq0, n_tokens);
+        const int slot_n = slots ? slots[n] : n;
+        if (slot_n < 0 || slot_n >= pool) {  // uniform over the CTA
+            if (err_count && sl == 0 && blockIdx.y == 0 && c == 0) atomicAdd(err_count, 1);
+            return;
+        }
+    } else {
+        if (err_count && sl == 0 && blockIdx.y == 0) {  // count each skipped sequence once
+            for (int m = c; m < n_seqs; m += blockDim.x) {
+                const int slot_m = slots ? slots[m] : m;
+                size_t a;
+                int len;
+                if (slot_m < 0 || slot_m >= pool || !seqs.range(m, a, len)) atomicAdd(err_count, 1);
+            }
+        }
+        const long long cs = blockIdx.y;
+        int lo = 0, hi = n_seqs - 1;
+        n = -1;
+        while (lo <= hi) {  // the last sequence whose first block slot is <= cs
+            const int mid = (lo + hi) >> 1;
+            if (static_cast<long long>(seqs.cu[mid]) / P + mid <= cs) {
+                n = mid;
+                lo = mid + 1;
+            } else {
+                hi = mid - 1;
+            }
+        }
+        if (n < 0 || !seqs.range(n, seq0, n_tokens)) return;  // uniform over the CTA
+        const int slot_n = slots ? slots[n] : n;
+        if (slot_n < 0 || slot_n >= pool) return;
+        t0 = static_cast<int>(cs - (static_cast<long long>(seqs.cu[n]) / P + n)) * P;
     }
-    const int t0 = blockIdx.y * P, t1 = min(n_tokens, t0 + P);
+    const int slot = slots ? slots[n] : n;
+    const int t1 = min(n_tokens, t0 + P);
     if (t0 >= n_tokens) return;  // past the end of a shorter sequence: uniform over the CTA
     const int Hk = n_k_heads, H = n_v_heads;
     const size_t conv_dim = static_cast<size_t>(2 * Hk + H) * S;
@@ -136,9 +172,17 @@ gdn_status launch_conv_split_norm_k(const float *qkv, const float *w, float *con
                                     float eps, const int32_t *slots, int pool, int32_t *err_count,
                                     cudaStream_t s) {
     constexpr int P = conv_norm_positions<E>();
-    const dim3 grid(2 * Hk + H, (seqs.n_tokens + P - 1) / P, n_seqs);
-    conv_split_norm_kernel<E, K><<<grid, 32 * E, 0, s>>>(qkv, w, conv_state, q, k, v, seqs,
-                                                         Hk, H, eps, slots, pool, err_count);
+    if (seqs.cu == nullptr) {
+        const dim3 grid(2 * Hk + H, (seqs.n_tokens + P - 1) / P, n_seqs);
+        conv_split_norm_kernel<E, K, false><<<grid, 32 * E, 0, s>>>(
+            qkv, w, conv_state, q, k, v, seqs, n_seqs, Hk, H, eps, slots, pool, err_count);
+    } else {
+        const long long block_slots = seqs.total / P + n_seqs;
+        if (block_slots > 65535) return GDN_ERR_UNSUPPORTED;
+        const dim3 grid(2 * Hk + H, static_cast<unsigned>(block_slots), 1);
+        conv_split_norm_kernel<E, K, true><<<grid, 32 * E, 0, s>>>(
+            qkv, w, conv_state, q, k, v, seqs, n_seqs, Hk, H, eps, slots, pool, err_count);
+    }
     return launch_status();
 }
 

@@ -176,12 +176,16 @@ __device__ __forceinline__ float group_dot(const float (&r)[8][E], const float *
 // of shared-memory chunks with bulk copies, each chunk tracked by a "full" and an
 // "empty" mbarrier. g and beta (one float per token and head) are read by the lanes
 // a chunk ahead and broadcast with shuffles. The state reaches HBM once per call.
-template <int E, bool SNAP>
+// RAGGED selects the ragged-batch form; the uniform one reads the sequence length and
+// offset straight from the kernel parameters, which keeps them out of the registers the
+// token loop needs.
+template <int E, bool SNAP, bool RAGGED>
 __global__ void __launch_bounds__(ScanSmem<E>::kThreads, ScanSmem<E>::kMinBlocks) recurrence_scan_kernel(
     float *state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
-    float *__restrict__ y, const SeqMap seqs, int n_k_heads, int n_v_heads, float scale,
-    const int32_t *__restrict__ slots, int pool, int32_t *err_count, float *__restrict__ snaps) {
+    float *__restrict__ y, const SeqMap seqs, int n_seqs_ragged, int n_k_heads, int n_v_heads,
+    float scale, const int32_t *__restrict__ slots, int pool, int32_t *err_count,
+    float *__restrict__ snaps) {
     constexpr int S = 32 * E, TC = kScanTok;
     using L = ScanSmem<E>;
     constexpr int kScanWarps = L::kWarps, kScanRows = L::kRows;
@@ -193,12 +197,21 @@ __global__ void __launch_bounds__(ScanSmem<E>::kThreads, ScanSmem<E>::kMinBlocks
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int part = blockIdx.x % kBlocksPerHead;
     const int vh = (blockIdx.x / kBlocksPerHead) % n_v_heads;
-    const int n = blockIdx.x / (kBlocksPerHead * n_v_heads);
+    int n = blockIdx.x / (kBlocksPerHead * n_v_heads);
+    if (RAGGED && n_seqs_ragged <= kLongestFirstMaxSeqs) {
+        // a small ragged batch: the longest sequences' CTAs first
+        __shared__ int pick;
+        n = seq_by_length_rank(seqs, n_seqs_ragged, n, &pick);
+    }
     const int kh = vh % n_k_heads;
     const int slot = slots ? slots[n] : n;
     size_t tok0;   // first position of sequence n in the token-major arrays
     int n_tokens;  // its length
-    if (slot < 0 || slot >= pool || !seqs.range(n, tok0, n_tokens)) {
+    if (!RAGGED) {
+        n_tokens = seqs.n_tokens;
+        tok0 = static_cast<size_t>(n) * seqs.n_tokens;
+    }
+    if (slot < 0 || slot >= pool || (RAGGED && !seqs.range(n, tok0, n_tokens))) {
         if (err_count && vh == 0 && part == 0 && threadIdx.x == 0) atomicAdd(err_count, 1);
         return;
     }
@@ -356,20 +369,33 @@ gdn_status launch_decode(float *state, const float *q, const float *k, const flo
     return launch_status();
 }
 
+template <int E, bool SNAP, bool RAGGED>
+gdn_status launch_scan_form(float *state, const float *q, const float *k, const float *v,
+                            const float *g, const float *beta, float *y, int n_seqs, SeqMap seqs,
+                            int n_k_heads, int n_v_heads, float scale, const int32_t *slots,
+                            int pool, int32_t *err_count, float *snaps, cudaStream_t s) {
+    constexpr int S = 32 * E;
+    const size_t smem = ScanSmem<E>::bytes;
+    GDN_TRY(set_smem(recurrence_scan_kernel<E, SNAP, RAGGED>, smem));
+    const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / ScanSmem<E>::kRows);
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    recurrence_scan_kernel<E, SNAP, RAGGED><<<static_cast<unsigned>(blocks), ScanSmem<E>::kThreads, smem, s>>>(
+        state, q, k, v, g, beta, y, seqs, n_seqs, n_k_heads, n_v_heads, scale, slots, pool,
+        err_count, snaps);
+    return launch_status();
+}
+
 template <int E, bool SNAP>
 gdn_status launch_scan(float *state, const float *q, const float *k, const float *v,
                        const float *g, const float *beta, float *y, int n_seqs, SeqMap seqs,
                        int n_k_heads, int n_v_heads, float scale, const int32_t *slots, int pool,
                        int32_t *err_count, float *snaps, cudaStream_t s) {
-    constexpr int S = 32 * E;
-    const size_t smem = ScanSmem<E>::bytes;
-    GDN_TRY(set_smem(recurrence_scan_kernel<E, SNAP>, smem));
-    const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / ScanSmem<E>::kRows);
-    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-    recurrence_scan_kernel<E, SNAP><<<static_cast<unsigned>(blocks), ScanSmem<E>::kThreads, smem, s>>>(
-        state, q, k, v, g, beta, y, seqs, n_k_heads, n_v_heads, scale, slots, pool,
-        err_count, snaps);
-    return launch_status();
+    if (seqs.cu)
+        return launch_scan_form<E, SNAP, true>(state, q, k, v, g, beta, y, n_seqs, seqs,
+                                               n_k_heads, n_v_heads, scale, slots, pool,
+                                               err_count, snaps, s);
+    return launch_scan_form<E, SNAP, false>(state, q, k, v, g, beta, y, n_seqs, seqs, n_k_heads,
+                                            n_v_heads, scale, slots, pool, err_count, snaps, s);
 }
 
 gdn_status check_recurrence_args(const float *state, const float *q, const float *k,

@@ -85,3 +85,43 @@ def test_chunked_scan_in_a_graph(lib, form):
     torch.cuda.synchronize()
     assert torch.equal(state_g, state_e)
     assert torch.equal(y_g, y_e)
+
+
+@pytest.mark.parametrize("chunked", [False, True])
+def test_ragged_prefill_in_a_graph(lib, chunked):
+    """A ragged prefill call (cu_seqlens on the device, read only by the kernels) captured
+    once and replayed gives the eager call's bits."""
+    cfg = I.get_config(2, n_seqs=4, n_k_heads=2, n_v_heads=4, cid=820 + chunked)
+    Hk, H, S, K = cfg.n_k_heads, cfg.n_v_heads, cfg.state_size, cfg.conv_kernel
+    lengths = [40, 1, 65, 9]
+    cu = dev(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32))
+    total = sum(lengths)
+    per = [I.prefill_seq(cfg, n, n_tokens=L) for n, L in enumerate(lengths)]
+    x = {key: dev(np.concatenate([p[key] for p in per])) for key in per[0]}
+    st = {k: dev(v) for k, v in I.block_static(cfg).items()}
+    state0, conv0 = I.state_pool(cfg), I.conv_state_pool(cfg)
+    size = (lib.gdn_block_prefill_chunked_varlen_workspace_size if chunked
+            else lib.gdn_block_prefill_varlen_workspace_size)
+    ws = torch.empty(size(4, total, Hk, H, S) // 4 + 64, device="cuda")
+    fn = lib.gdn_block_prefill_chunked_varlen if chunked else lib.gdn_block_prefill_varlen
+
+    def run(state, conv, out):
+        fn(x["qkv"], st["conv_w"], conv, x["alpha"], x["b"], st["dt"], st["a"], x["z"],
+           st["norm_w"], state, out, cu, 4, total, max(lengths), Hk, H, S, K, cfg.scale, cfg.eps,
+           cfg.eps, ws)
+
+    state_e, conv_e = dev(state0), dev(conv0)
+    out_e = torch.empty(total, H, S, device="cuda")
+    run(state_e, conv_e, out_e)
+    state_g, conv_g = dev(state0), dev(conv0)
+    out_g = torch.empty(total, H, S, device="cuda")
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(state_g, conv_g, out_g)
+    state_g.copy_(dev(state0))
+    conv_g.copy_(dev(conv0))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g, out_e)
+    assert torch.equal(state_g, state_e) and torch.equal(conv_g, conv_e)
