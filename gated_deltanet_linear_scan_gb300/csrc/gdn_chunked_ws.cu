@@ -36,14 +36,11 @@ __device__ unsigned g_watchdog_chunked_ws;
 constexpr unsigned WD_MMA = 8u;  // a hand-off between the roles of the state kernel
 
 // Workspace block of one (chunk, sequence, v-head), fp32: W [32][128] (rows = positions,
-// columns = dk), Ut [32][128] (columns = dv), M [32][32]; chunk-major over a wave.
+// columns = dk), Ut [32][128] (columns = dv), M [32][32]; chunk-major over a wave: block
+// ((c * n_seqs + n) * H + vh) for wave chunk c of a uniform batch.
 constexpr int kBlkW = 0, kBlkUt = kC * kS, kBlkM = 2 * kC * kS;
 constexpr int kBlkFloats = 2 * kC * kS + kC * kC;
 constexpr size_t kBlkBytes = static_cast<size_t>(kBlkFloats) * sizeof(float);
-
-__device__ __forceinline__ size_t blk_index(int cw, int n, int vh, int n_seqs, int H) {
-    return (static_cast<size_t>(cw) * n_seqs + n) * H + vh;
-}
 
 // A ragged batch is prepared in one wave, its blocks indexed by chunk slot: chunk c of
 // sequence n takes slot cu[n] / 32 + n + c. The slots of consecutive sequences never

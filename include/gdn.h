@@ -308,7 +308,9 @@ gdn_status gdn_gated_norm(const float *y, const float *w, const float *z, float 
  * qkv: [n_seqs][C] raw; conv_w: [C][4]; conv_state: [pool][C][3] in place;
  * alpha, b: [n_seqs][H] raw gate and beta logits; dt, a: [H]; z: [n_seqs][H][S];
  * norm_w: [S]; state: [pool][H][S][S] in place; out: [n_seqs][H][S].
- * conv_kernel must be 4; n_v_heads / n_k_heads <= 8. All pointers 16-byte aligned. */
+ * conv_kernel must be 4; n_v_heads / n_k_heads <= 8 (<= 4 at state_size 256, whose head
+ * tile is split over two CTAs of a cluster of at most 8); otherwise GDN_ERR_UNSUPPORTED.
+ * All pointers 16-byte aligned. */
 gdn_status gdn_block_decode(const float *qkv, const float *conv_w, float *conv_state,
                             const float *alpha, const float *b, const float *dt, const float *a,
                             const float *z, const float *norm_w, float *state, float *out,
