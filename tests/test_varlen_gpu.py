@@ -310,3 +310,45 @@ def test_recurrence_scans_varlen_against_own_calls(lib):
                                              **{key: v[None] for key, v in per[n].items()})
                 assert_rms(host(y[cu[n]:cu[n + 1]]), y_ref[0], f"S={S}: y vs oracle")
                 assert_rms(host(st[n]), ref_s[0], f"S={S}: state vs oracle")
+
+
+@pytest.mark.parametrize("form", ["sequential", "chunked"])
+def test_block_prefill_varlen_many_sequences(lib, form):
+    """300 short sequences (more than the batches scheduled longest-first): every sequence
+    gets the bits of a call of its own (checked on a sample), and sampled ones match the
+    oracle."""
+    cfg = I.get_config(2, n_seqs=300, n_k_heads=1, n_v_heads=2, cid=953)
+    lengths = [int(x) for x in np.random.default_rng(954).integers(0, 40, 300)]
+    rg = Ragged(cfg, lengths)
+    out, state, conv = run_varlen(lib, rg, form)
+    sample = [0, 1, 77, 150, 299] + [n for n in range(300) if lengths[n] in (0, 1, 32, 33)][:6]
+    for n in sample:
+        a, L = rg.cu[n], rg.lengths[n]
+        if L == 0:
+            assert np.array_equal(host(state[n]), rg.st0[n])
+            continue
+        o1, s1, c1 = run_alone(lib, rg, n, form)
+        assert torch.equal(out[a:a + L], o1), f"seq {n}: out differs from its own call"
+        assert torch.equal(state[n], s1) and torch.equal(conv[n], c1), f"seq {n}: states"
+    refs = oracle_all(rg, [n for n in (1, 150, 299) if lengths[n] > 0])
+    check_against_oracle(rg, refs, out, state, conv)
+
+
+def test_block_prefill_varlen_unowned_positions(lib):
+    """Offsets need not start at 0 nor end at total_tokens: rows of out at positions no
+    sequence owns keep their contents, and the sequences get their own calls' bits."""
+    cfg = I.get_config(2, n_seqs=2, n_k_heads=2, n_v_heads=4, cid=955)
+    rg = Ragged(cfg, [7, 40])
+    cu = np.array([3, 10, 50], np.int32)
+    packed = {key: np.concatenate([np.zeros((3,) + v.shape[1:], v.dtype), v,
+                                   np.zeros((5,) + v.shape[1:], v.dtype)])
+              for key, v in rg.packed.items()}
+    rg.packed, rg.total = packed, 55
+    for form in ("sequential", "chunked"):
+        out, state, conv = run_varlen(lib, rg, form, out_fill=3.0, cu=cu, max_tokens=40)
+        o = host(out)
+        assert np.all(o[:3] == 3.0) and np.all(o[50:] == 3.0), f"{form}: unowned rows written"
+        for n in range(2):
+            o1, s1, c1 = run_alone(lib, rg, n, form)
+            assert torch.equal(out[cu[n]:cu[n + 1]], o1), f"{form} seq {n}: out"
+            assert torch.equal(state[n], s1) and torch.equal(conv[n], c1), f"{form} seq {n}"
