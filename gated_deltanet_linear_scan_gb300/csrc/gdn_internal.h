@@ -40,9 +40,10 @@ inline SeqMap uniform_seqs(int n_seqs, int n_tokens) {
     return SeqMap{nullptr, n_tokens, static_cast<long long>(n_seqs) * n_tokens};
 }
 
-// The same search by a whole warp (every lane returns the answer): each round the lanes
-// probe 32 evenly spaced entries of the remaining range, so a batch of up to 32
-// sequences takes one coalesced load, 1024 two.
+// The last sequence n in [0, n_seqs) with cu[n] <= pos, or -1 if none -- with a valid
+// ragged batch, the sequence owning position pos if any -- found by a whole warp (every
+// lane returns it): each round the lanes probe 32 evenly spaced entries of the remaining
+// range, so a batch of up to 32 sequences takes one coalesced load, 1024 two.
 __device__ __forceinline__ int warp_seq_of_position(const int32_t *cu, int n_seqs, long long pos) {
     const int lane = threadIdx.x & 31;
     int lo = 0, hi = n_seqs;  // the answer is the last n in [lo, hi) with cu[n] <= pos, or lo - 1
@@ -88,22 +89,6 @@ __device__ __forceinline__ int seq_by_length_rank(const SeqMap &seqs, int n_seqs
 
 // Ragged batches up to this many sequences run their per-sequence CTAs longest first.
 constexpr int kLongestFirstMaxSeqs = 256;
-
-// The last sequence n in [0, n_seqs) with cu[n] <= pos (binary search; -1 if none).
-// With a valid ragged batch that is the sequence owning position pos, if any.
-__device__ __forceinline__ int seq_of_position(const int32_t *cu, int n_seqs, long long pos) {
-    int lo = 0, hi = n_seqs - 1, found = -1;
-    while (lo <= hi) {
-        const int mid = (lo + hi) >> 1;
-        if (cu[mid] <= pos) {
-            found = mid;
-            lo = mid + 1;
-        } else {
-            hi = mid - 1;
-        }
-    }
-    return found;
-}
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
