@@ -42,7 +42,7 @@ inline SeqMap uniform_seqs(int n_seqs, int n_tokens) {
 
 // The last sequence n in [0, n_seqs) with cu[n] <= pos, or -1 if none -- with a valid
 // ragged batch, the sequence owning position pos if any -- found by a whole warp (every
-// lane returns it): each round the lanes probe 32 evenly spaced entries of the remaining
+// lane returns it): each pass the lanes probe 32 evenly spaced entries of the remaining
 // range, so a batch of up to 32 sequences takes one coalesced load, 1024 two.
 __device__ __forceinline__ int warp_seq_of_position(const int32_t *cu, int n_seqs, long long pos) {
     const int lane = threadIdx.x & 31;
