@@ -105,17 +105,21 @@ def source_sha(files):
 
 KERNEL_SOURCES = {
     "block_decode_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_block.cu",
-                            "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh"],
+                            "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh",
+                            "gated_deltanet_linear_scan_gb300/csrc/gdn_internal.h"],
     "recurrence_scan_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_recurrence.cu",
-                               "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh"],
+                               "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh",
+                               "gated_deltanet_linear_scan_gb300/csrc/gdn_internal.h"],
     "chunked_scan_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_chunked.cu",
                             "gated_deltanet_linear_scan_gb300/csrc/gdn_chunk_common.cuh",
                             "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh",
-                            "gated_deltanet_linear_scan_gb300/csrc/gdn_tc.cuh"],
+                            "gated_deltanet_linear_scan_gb300/csrc/gdn_tc.cuh",
+                            "gated_deltanet_linear_scan_gb300/csrc/gdn_internal.h"],
     "chunk_state_kernel": ["gated_deltanet_linear_scan_gb300/csrc/gdn_chunked_ws.cu",
                            "gated_deltanet_linear_scan_gb300/csrc/gdn_chunk_common.cuh",
                            "gated_deltanet_linear_scan_gb300/csrc/gdn_device.cuh",
-                           "gated_deltanet_linear_scan_gb300/csrc/gdn_tc.cuh"],
+                           "gated_deltanet_linear_scan_gb300/csrc/gdn_tc.cuh",
+                           "gated_deltanet_linear_scan_gb300/csrc/gdn_internal.h"],
 }
 
 
