@@ -94,3 +94,23 @@ def test_ncu_traffic_comes_from_the_json_record(monkeypatch):
         assert bench.ncu_traffic(kernel, workload) == float(entry["dram_bytes_per_launch"])
         monkeypatch.setattr(bench, "source_sha", lambda files: "0" * 16)
         assert bench.ncu_traffic(kernel, workload) is None
+
+
+def test_reference_arm_under_a_launcher_prints_one_line():
+    """Launched as two ranks (torchrun, as for N > 1), rank 0 alone runs the oracle and
+    prints the line; the other rank exits 0 without work."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    res = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                          "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                          "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                          "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
+                          "--cpu-budget", "0.5"], capture_output=True, text=True, timeout=600,
+                         cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.lstrip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
