@@ -90,17 +90,7 @@ __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
     } else {  // ragged batch: grid (chunk slot, k-head); slots no chunk owns return
         const int cs = blockIdx.x % n_wave_chunks;
         kh = blockIdx.x / n_wave_chunks;
-        int lo = 0, hi = n_seqs - 1;
-        n = -1;
-        while (lo <= hi) {
-            const int mid = (lo + hi) >> 1;
-            if (chunk_slot_base(seqs.cu, mid) <= cs) {
-                n = mid;
-                lo = mid + 1;
-            } else {
-                hi = mid - 1;
-            }
-        }
+        n = warp_seq_of_slot(seqs.cu, n_seqs, kC, cs);  // each warp finds it; the same n
         if (n < 0 || !seqs.range(n, seq0, n_tokens)) return;  // uniform over the CTA
         chunk = static_cast<int>(cs - chunk_slot_base(seqs.cu, n));
         if (chunk * kC >= n_tokens) return;

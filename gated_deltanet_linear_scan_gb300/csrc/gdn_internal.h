@@ -40,25 +40,43 @@ inline SeqMap uniform_seqs(int n_seqs, int n_tokens) {
     return SeqMap{nullptr, n_tokens, static_cast<long long>(n_seqs) * n_tokens};
 }
 
-// The last sequence n in [0, n_seqs) with cu[n] <= pos, or -1 if none -- with a valid
-// ragged batch, the sequence owning position pos if any -- found by a whole warp (every
-// lane returns it): each pass the lanes probe 32 evenly spaced entries of the remaining
-// range, so a batch of up to 32 sequences takes one coalesced load, 1024 two.
-__device__ __forceinline__ int warp_seq_of_position(const int32_t *cu, int n_seqs, long long pos) {
+// The last index n in [0, count) with key(n) <= target, or -1 if none, for a key that is
+// non-decreasing in n (with any other key the answer is still some index in [-1, count),
+// which callers validate). Found by a whole warp, every lane returning it: each pass the
+// lanes probe 32 evenly spaced keys of the remaining range, so up to 32 keys take one
+// round of loads, 1024 two.
+template <typename Key>
+__device__ __forceinline__ int warp_last_le(int count, long long target, Key key) {
     const int lane = threadIdx.x & 31;
-    int lo = 0, hi = n_seqs;  // the answer is the last n in [lo, hi) with cu[n] <= pos, or lo - 1
+    int lo = 0, hi = count;  // the answer is the last n in [lo, hi) with key(n) <= target, or lo - 1
     while (hi - lo > 32) {
         const int step = (hi - lo + 31) / 32;
         const int idx = lo + lane * step;
-        const unsigned hit = __ballot_sync(0xffffffffu, idx < hi && cu[idx] <= pos);
+        const unsigned hit = __ballot_sync(0xffffffffu, idx < hi && key(idx) <= target);
         if (hit == 0) return lo - 1;
         const int last = 31 - __clz(hit);
         lo += last * step;
         hi = min(hi, lo + step);
     }
     const int idx = lo + lane;
-    const unsigned hit = __ballot_sync(0xffffffffu, idx < hi && cu[idx] <= pos);
+    const unsigned hit = __ballot_sync(0xffffffffu, idx < hi && key(idx) <= target);
     return hit == 0 ? lo - 1 : lo + 31 - __clz(hit);
+}
+
+// The sequence of a ragged batch that owns packed position pos (with valid offsets), or
+// -1: the last n with cu[n] <= pos. Called by a whole warp.
+__device__ __forceinline__ int warp_seq_of_position(const int32_t *cu, int n_seqs, long long pos) {
+    return warp_last_le(n_seqs, pos, [&](int n) { return static_cast<long long>(cu[n]); });
+}
+
+// The sequence whose block slots contain `slot`, when block b of sequence n takes slot
+// cu[n] / per_block + n + b (the slots of consecutive sequences never collide): the last n
+// with cu[n] / per_block + n <= slot, or -1. Called by a whole warp.
+__device__ __forceinline__ int warp_seq_of_slot(const int32_t *cu, int n_seqs, int per_block,
+                                                long long slot) {
+    return warp_last_le(n_seqs, slot, [&](int n) {
+        return static_cast<long long>(cu[n]) / per_block + n;
+    });
 }
 
 // Longest-first order of a ragged batch for CTA scheduling: the sequence whose valid

@@ -167,6 +167,12 @@ __global__ void __launch_bounds__(kThreads) gated_norm_kernel(const float *y,
     constexpr int D = 32 * E;
     const long long row = blockIdx.x * static_cast<long long>(kThreads / 32) + (threadIdx.x >> 5);
     if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    // the row's operands first: their latency overlaps the lookup of its sequence
+    float yv[E], zv[E], wv[E];
+    load_vec<E>(yv, y + row * D + lane * E);
+    load_vec<E>(zv, z + row * D + lane * E);
+    load_vec<E>(wv, w + lane * E);
     if (slots || seqs.cu) {
         const long long pos = row / heads;
         int n;
@@ -183,11 +189,6 @@ __global__ void __launch_bounds__(kThreads) gated_norm_kernel(const float *y,
             if (slot < 0 || slot >= pool) return;
         }
     }
-    const int lane = threadIdx.x & 31;
-    float yv[E], zv[E], wv[E];
-    load_vec<E>(yv, y + row * D + lane * E);
-    load_vec<E>(zv, z + row * D + lane * E);
-    load_vec<E>(wv, w + lane * E);
     float ss = 0.0f;
 #pragma unroll
     for (int e = 0; e < E; ++e) ss = __fmaf_rn(yv[e], yv[e], ss);

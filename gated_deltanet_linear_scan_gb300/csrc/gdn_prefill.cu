@@ -78,17 +78,7 @@ __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
             }
         }
         const long long cs = blockIdx.y;
-        int lo = 0, hi = n_seqs - 1;
-        n = -1;
-        while (lo <= hi) {  // the last sequence whose first block slot is <= cs
-            const int mid = (lo + hi) >> 1;
-            if (static_cast<long long>(seqs.cu[mid]) / P + mid <= cs) {
-                n = mid;
-                lo = mid + 1;
-            } else {
-                hi = mid - 1;
-            }
-        }
+        n = warp_seq_of_slot(seqs.cu, n_seqs, P, cs);  // each warp finds it; the same n
         if (n < 0 || !seqs.range(n, seq0, n_tokens)) return;  // uniform over the CTA
         const int slot_n = slots ? slots[n] : n;
         if (slot_n < 0 || slot_n >= pool) return;
