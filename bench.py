@@ -351,6 +351,20 @@ def cpu_sample_block(cfg, seqs, max_steps, budget_s):
     return len(seqs) * done / dt, done, dt
 
 
+def cpu_sample_block_all_cores(cfg, budget_s):
+    """The oracle's block on every host core at once: one thread per core, each stepping
+    its own sequence (the oracle is C called through ctypes, which releases the GIL; the
+    oracle itself is unchanged). Returns (tokens/s over all threads, threads, seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+    threads = max(1, min(os.cpu_count() or 1, cfg.n_seqs))
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        t0 = time.perf_counter()
+        runs = list(ex.map(lambda n: cpu_sample_block(cfg, [n], 10 ** 6, budget_s),
+                           range(threads)))
+        dt = time.perf_counter() - t0
+    return sum(r[0] for r in runs), threads, dt
+
+
 def cpu_sample_scan(cfg, tokens, budget_s):
     """Time the oracle scan on one (sequence, v-head) unit for `tokens` tokens and
     scale to all units: returns tokens/s of the whole workload on one core."""
@@ -608,6 +622,10 @@ def run_ours(args, cfg, rank, world, local_rank):
         v_cpu, done, dt = cpu_sample_block(cfg, sample_seqs, 10 ** 6, args.cpu_budget)
         cpu = cpu_record(v_cpu, f"{len(sample_seqs)} of {N} sequences, {done} chained steps "
                                 f"of the block ({dt:.1f} s), plain C float build, 1 thread")
+        v_all, threads, dt_all = cpu_sample_block_all_cores(cfg, min(3.0, args.cpu_budget))
+        cpu["all_cores"] = {"value": v_all, "unit": "tokens/s", "cores": threads,
+                            "sample": f"{threads} sequences, one thread each, stepping for "
+                                      f"{dt_all:.1f} s (the same oracle)"}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
