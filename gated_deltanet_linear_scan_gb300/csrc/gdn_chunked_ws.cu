@@ -46,7 +46,8 @@ constexpr size_t kBlkBytes = static_cast<size_t>(kBlkFloats) * sizeof(float);
 // sequence n takes slot cu[n] / 32 + n + c. The slots of consecutive sequences never
 // collide (floor((a + L) / 32) + 1 >= floor(a / 32) + ceil(L / 32)) and stay below
 // total / 32 + n_seqs, so the workspace needs (total / 32 + n_seqs) slots of blocks
-// whatever the lengths are, and a slot maps back to its sequence by binary search.
+// whatever the lengths are, and a slot maps back to its sequence by a search over the
+// sequences' first slots.
 __device__ __forceinline__ long long chunk_slot_base(const int32_t *cu, int n) {
     return static_cast<long long>(cu[n]) / kC + n;
 }

@@ -42,6 +42,8 @@ struct PrefillLayout {
 // separate kernels' bit for bit, without their [n][t][C] intermediate in HBM.
 template <int E>
 __host__ __device__ constexpr int conv_norm_positions() { return E >= 8 ? 16 : 32; }
+static_assert(conv_norm_positions<8>() == 16 && conv_norm_positions<4>() == 32,
+              "the ragged grid check in prefill_impl assumes these block sizes");
 
 // Grid, uniform batch: (slice, block of P positions, sequence). Ragged batch: (slice,
 // block slot); block b of sequence n takes slot cu[n] / P + n + b (the chunk-slot scheme
@@ -283,6 +285,11 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
     float *g = ws + L.g, *beta = ws + L.beta;
     if ((n_tokens + 31) / 32 > 65535 || n_seqs > 65535) return GDN_ERR_UNSUPPORTED;
     if (snapshots && n_tokens > 65535) return GDN_ERR_UNSUPPORTED;  // positions on grid.y
+    if (seqs.cu) {  // the ragged grids, checked before anything is enqueued
+        const long long per_block = S >= 256 ? 16 : 32;  // conv_norm_positions
+        if (rows / per_block + n_seqs > 65535) return GDN_ERR_UNSUPPORTED;
+        if (chunked && (rows / 32 + n_seqs) * n_k_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    }
 
     // A skipped sequence is counted once, by the conv pass; nothing of it is written
     // to conv_state, state or out.
