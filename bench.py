@@ -1140,7 +1140,9 @@ def run_ours_varlen(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                      "kernel": "chunk_prepare_kernel + chunk_state_kernel "
                                "(gdn_recurrence_scan_chunked_varlen, timed together)",
                      "achieved": mflops / scan_s / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
-                     "frac": mflops / scan_s / 1e12 / tf32_peak, "traffic": None,
+                     "frac": mflops / scan_s / 1e12 / tf32_peak,
+                     "traffic": ncu_traffic("chunk_state_kernel", args.workload),
+                     "traffic_note": "both kernels of the ragged chunked scan, per call",
                      "flops_per_launch": mflops,
                      "flops_note": "the method's own contraction flops (each product once); "
                                    "the kernels issue 3 TF32 passes per product (3xTF32)",
