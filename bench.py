@@ -50,21 +50,19 @@ VARLEN_TOKENS = 16384
 # verification scores 4 draft tokens of each of the 64 batched-decode sequences.
 OVERRIDES = {"spec_verify_64x4": {"n_tokens": 4}}
 SPEC_TOKENS = 4
-# TF32 tensor-core rate relative to bf16 (nominal dense figures, 1.1 / 2.25 PFLOP/s)
-TF32_PER_BF16 = 1.1 / 2.25
 
 
 def chunked_tensor_flops(n_seqs, n_tokens, n_v_heads):
-    """Tensor-core flops the chunked scan issues (S = 128, chunks of 32): per
-    (sequence, v-head, chunk) the S products hi(S) [hi W | hi Gam q | lo W | lo Gam q]
-    (N = 128, K = 128) and lo(S) [hi W | hi Gam q] (N = 64), then the state update with
-    the U part of y, U^T [w K | M]^T in 3 passes (N = 160, K = 32)."""
+    """Tensor-core flops the chunked scan issues (S = 128, chunks of 32, bf16 operand
+    parts): per (sequence, v-head, chunk) the S products hi(S) [hi W | hi Gam q | lo W |
+    lo Gam q] (N = 128, K = 128) and lo(S) [hi W | hi Gam q] (N = 64), then the state
+    update with the U part of y, U^T [w K | M]^T in 3 passes (N = 160, K = 32)."""
     per = 2 * 128 * 128 * 128 + 2 * 128 * 64 * 128 + 3 * (2 * 128 * 160 * 32)
     return per * n_seqs * n_v_heads * ((n_tokens + 31) // 32)
 
 
 def chunked_method_flops(n_chunks_total, n_v_heads):
-    """The chunked scan's own contraction flops, without the 3xTF32 passes: per (sequence,
+    """The chunked scan's own contraction flops, without the 3xBF16 passes: per (sequence,
     v-head, chunk) the S products S^T [Gam q | W] (M = 128, N = 64, K = 128) and the state
     update with the U part of y, U^T [w K | M]^T (M = 128, N = 160, K = 32)."""
     per = 2 * 128 * 64 * 128 + 2 * 128 * 160 * 32
@@ -740,17 +738,16 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         one_s = sum(e0.elapsed_time(e1) for e0, e1 in one_ev) / 1e3 / args.steps
         tf = chunked_tensor_flops(N, T, H)
         pf = chunk_prepare_flops(N, T, Hk, H)
-        tf32_peak = pk["bf16_tflops"] * TF32_PER_BF16 if "bf16_tflops" in pk else 1900.0 * TF32_PER_BF16
+        bf16_peak = pk.get("bf16_tflops", 1900.0)
         mf = chunked_method_flops(N * ((T + 31) // 32), H)
         roofline = {"bound": "tensor", "kernel": "chunk_state_kernel (gdn_chunked_advance)",
-                    "achieved": mf / adv_s / 1e12, "peak": tf32_peak,
-                    "unit": "TFLOP/s", "frac": mf / adv_s / 1e12 / tf32_peak,
+                    "achieved": mf / adv_s / 1e12, "peak": bf16_peak,
+                    "unit": "TFLOP/s", "frac": mf / adv_s / 1e12 / bf16_peak,
                     "traffic": ncu_traffic("chunk_state_kernel", args.workload),
                     "flops_per_launch": mf,
                     "flops_note": "the method's own contraction flops (each product once); "
-                                  "the kernel issues 3 TF32 passes per product (3xTF32)",
-                    "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
-                                   f"{TF32_PER_BF16:.3f}"}
+                                  "the kernel issues 3 bf16 passes per product (3xBF16)",
+                    "peak_source": f"bf16_tflops ({pk_kind})"}
         extra = {"advance_ms": 1e3 * adv_s, "prepare_ms": 1e3 * prep_s,
                  "advance_tensor_issued_tflops": tf / adv_s / 1e12,
                  "prepare_fp32_tflops": pf / prep_s / 1e12,
@@ -988,7 +985,7 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
 
     flops = 7.0 * N * T * H * S * S
     mf = chunked_method_flops(N * ((T + 31) // 32), H)
-    tf32_peak = pk.get("bf16_tflops", 1900.0) * TF32_PER_BF16
+    bf16_peak = pk.get("bf16_tflops", 1900.0)
     props = torch.cuda.get_device_properties(0)
     mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
     fp32_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
@@ -1015,14 +1012,13 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                    "method_fp32_tflops_of_scan": flops / (prep_s + adv_s) / 1e12,
                    "fp32_pipe_peak_tflops": fp32_peak},
         "roofline": {"bound": "tensor", "kernel": "chunk_state_kernel (gdn_chunked_advance)",
-                     "achieved": mf / adv_s / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
-                     "frac": mf / adv_s / 1e12 / tf32_peak,
+                     "achieved": mf / adv_s / 1e12, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": mf / adv_s / 1e12 / bf16_peak,
                      "traffic": ncu_traffic("chunk_state_kernel", "prefill_chunked_4x4096"),
                      "flops_per_launch": mf,
                      "flops_note": "the method's own contraction flops (each product once); "
-                                   "the kernel issues 3 TF32 passes per product (3xTF32)",
-                     "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
-                                    f"{TF32_PER_BF16:.3f}"},
+                                   "the kernel issues 3 bf16 passes per product (3xBF16)",
+                     "peak_source": f"bf16_tflops ({pk_kind})"},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -1093,7 +1089,7 @@ def run_ours_varlen(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     del scan_ws
     n_chunks = sum((L + 31) // 32 for L in lengths)
     mflops = chunked_method_flops(n_chunks, H)
-    tf32_peak = pk.get("bf16_tflops", 1900.0) * TF32_PER_BF16
+    bf16_peak = pk.get("bf16_tflops", 1900.0)
 
     # ---- end to end: qkv, alpha, b, z and cu_seqlens from pinned host memory, the call,
     # out back
@@ -1139,15 +1135,14 @@ def run_ours_varlen(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         "roofline": {"bound": "tensor",
                      "kernel": "chunk_prepare_kernel + chunk_state_kernel "
                                "(gdn_recurrence_scan_chunked_varlen, timed together)",
-                     "achieved": mflops / scan_s / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
-                     "frac": mflops / scan_s / 1e12 / tf32_peak,
+                     "achieved": mflops / scan_s / 1e12, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": mflops / scan_s / 1e12 / bf16_peak,
                      "traffic": ncu_traffic("chunk_state_kernel", args.workload),
                      "traffic_note": "both kernels of the ragged chunked scan, per call",
                      "flops_per_launch": mflops,
                      "flops_note": "the method's own contraction flops (each product once); "
-                                   "the kernels issue 3 TF32 passes per product (3xTF32)",
-                     "peak_source": f"bf16_tflops ({pk_kind}) x nominal TF32/bf16 ratio "
-                                    f"{TF32_PER_BF16:.3f}"},
+                                   "the kernels issue 3 bf16 passes per product (3xBF16)",
+                     "peak_source": f"bf16_tflops ({pk_kind})"},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

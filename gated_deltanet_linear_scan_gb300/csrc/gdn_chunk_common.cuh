@@ -1,7 +1,8 @@
 // gdn_chunk_common.cuh -- pieces shared by the two chunked forms of the scan (the
 // one-kernel form of gdn_chunked.cu and the two-phase form of gdn_chunked_ws.cu):
-// chunk geometry, the tensor-core operand images in shared memory, the
-// tensor-memory plan, the per-chunk decay prefix and the Gram products. Both forms
+// chunk geometry, the bf16 tensor-core operand images in shared memory and their
+// hi / lo split, the tensor-memory plan, the per-chunk decay prefix and the Gram
+// products. Both forms
 // run the same code for these, so they produce the same bits.
 #pragma once
 
@@ -15,24 +16,25 @@ namespace chunk {
 
 constexpr int kC = 32;    // positions per chunk
 constexpr int kS = 128;   // state size (dk = dv) of the tensor-core form
-constexpr uint32_t kLbo = 128;                 // K-major core matrices: next 4 elements of K
-constexpr uint32_t kSbo128 = (kS / 4) * 128;   // next 8 rows, K = 128 operands
-constexpr uint32_t kSbo32 = (kC / 4) * 128;    // next 8 rows, K = 32 operands
+constexpr uint32_t kLbo = 128;                 // K-major core matrices: next 8 bf16 of K
+constexpr uint32_t kSbo128 = (kS / 8) * 128;   // next 8 rows, K = 128 operands
+constexpr uint32_t kSbo32 = (kC / 8) * 128;    // next 8 rows, K = 32 operands
 
-// ---- tensor-core operands in shared memory: K-major core-matrix images (gdn_tc.cuh)
-// One 128-row image over K = 128 (dk): rows 0..31 hi(Gam q), 32..63 hi(W), 64..95 lo(W),
-// 96..127 lo(Gam q); one 160-row image over K = 32 (positions) per part: rows 0..127
-// w_c k_c (by dk), rows 128..159 M (by t), hi part then lo part.
+// ---- tensor-core operands in shared memory: bf16 K-major core-matrix images
+// (gdn_tc.cuh, 16-bit layout). One 128-row image over K = 128 (dk): rows 0..31
+// hi(Gam q), 32..63 hi(W), 64..95 lo(W), 96..127 lo(Gam q); one 160-row image over
+// K = 32 (positions) per part: rows 0..127 w_c k_c (by dk), rows 128..159 M (by t),
+// hi part then lo part.
 constexpr uint32_t kOffWQ = 0;         // the 128-row image
 constexpr uint32_t kOffQhi = 0;        //   rows 0..31:   hi(Gam q)
-constexpr uint32_t kOffWhi = 16384;    //   rows 32..63:  hi(W)
-constexpr uint32_t kOffWlo = 32768;    //   rows 64..95:  lo(W)
-constexpr uint32_t kOffQlo = 49152;    //   rows 96..127: lo(Gam q)
-constexpr uint32_t kOffKhi = 65536;    // hi part: rows 0..127 hi(w_c k_c)
-constexpr uint32_t kOffMhi = 81920;    //          rows 128..159 hi(M)
-constexpr uint32_t kOffKlo = 86016;    // lo part: rows 0..127 lo(w_c k_c)
-constexpr uint32_t kOffMlo = 102400;   //          rows 128..159 lo(M)
-constexpr uint32_t kImgBytes = 106496;
+constexpr uint32_t kOffWhi = 8192;     //   rows 32..63:  hi(W)
+constexpr uint32_t kOffWlo = 16384;    //   rows 64..95:  lo(W)
+constexpr uint32_t kOffQlo = 24576;    //   rows 96..127: lo(Gam q)
+constexpr uint32_t kOffKhi = 32768;    // hi part: rows 0..127 hi(w_c k_c)
+constexpr uint32_t kOffMhi = 40960;    //          rows 128..159 hi(M)
+constexpr uint32_t kOffKlo = 43008;    // lo part: rows 0..127 lo(w_c k_c)
+constexpr uint32_t kOffMlo = 51200;    //          rows 128..159 lo(M)
+constexpr uint32_t kImgBytes = 53248;
 
 // Raw rows of k and q in shared memory: 528 bytes (132 floats), so row r starts on
 // bank 4r and stays float4 aligned.
@@ -41,25 +43,33 @@ constexpr int kRawRowF = kRawRow / 4;
 constexpr uint32_t kRawArr = kC * kRawRow;
 
 // ---- tensor memory (columns; lane = dv)
-// A tcgen05 TF32 MMA (M = 128, K = 8) costs the tensor pipe about the same for any
+// A tcgen05 bf16 MMA (M = 128, K = 16) costs the tensor pipe about the same for any
 // N up to 160, so a chunk takes three groups of MMAs:
 //   the S products: hi(S) against the 128-row image (N = 128), then lo(S) against its
 //     first 64 rows (N = 64), into the four 32-column blocks of D:
 //     D_y = D[kColDyA] + D[kColDyB],   D_u = D[kColDuA] + D[kColDuB];
-//   once U is formed (its split takes over the two D_u blocks: lo(U) kColDuA, hi(U)
-//     kColDuB), the state update and the rest of y in one N = 160 group against the
-//     160-row image: [S^T | D[kColDyA]] += U^T [w K | M]^T, which needs the accumulator
-//     S^T and the D_y block kColDyA side by side.
+//   once U is formed (its split into hi(U) at kColUhi and lo(U) at kColUlo), the
+//     state update and the rest of y in one N = 160 group against the 160-row image:
+//     [S^T | D[kColDyA]] += U^T [w K | M]^T, which needs the accumulator S^T and the
+//     D_y block kColDyA side by side.
+// hi(S), lo(S) and the parts of U are bf16 pairs, two to a column (gdn_tc.cuh); S^T and
+// D are fp32. The parts of U have columns of their own: the two warps that share a
+// lane quarter read D_u and write U over different position ranges, and a packed U
+// laid over D_u would put one warp's writes on columns the other still reads.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColShi = 0, kColSlo = 128, kColSacc = 256, kColD = 384;
+constexpr uint32_t kColShi = 0, kColSlo = 64, kColUhi = 128, kColUlo = 160;
+constexpr uint32_t kColSacc = 256, kColD = 384;
 constexpr uint32_t kColDyA = kColD, kColDuA = kColD + 32, kColDuB = kColD + 64,
                    kColDyB = kColD + 96;
-constexpr uint32_t kColUlo = kColDuA, kColUhi = kColDuB;
 static_assert(kColD + 4 * kC == kTmemCols, "tensor-memory plan fills the allocation");
 static_assert(kColSacc + kS == kColDyA, "S^T and the first D_y block are adjacent");
+static_assert(kColShi + kS / 2 <= kColSlo && kColSlo + kS / 2 <= kColUhi &&
+                  kColUhi + kC / 2 <= kColUlo && kColUlo + kC / 2 <= kColSacc,
+              "the packed parts of S and U fit below the accumulator");
 static_assert(kOffQhi == kOffWQ && kOffWhi == kOffWQ + 4 * kSbo128 &&
                   kOffWlo == kOffWQ + 8 * kSbo128 && kOffQlo == kOffWQ + 12 * kSbo128,
               "the four 32-row operand images form one 128-row image");
+static_assert(kOffKhi == kOffQlo + 4 * kSbo128, "the 160-row images follow the 128-row one");
 static_assert(kOffMhi == kOffKhi + 16 * kSbo32 && kOffMlo == kOffKlo + 16 * kSbo32 &&
                   kOffKlo == kOffMhi + 4 * kSbo32 && kOffMlo + 4 * kSbo32 == kImgBytes,
               "w K and M form one 160-row image per part");
@@ -98,22 +108,61 @@ __device__ __forceinline__ float chunk_gam_from(float c, int lane, float &last) 
     return c;
 }
 
-// The split x = hi + lo of the 3xTF32 products: hi keeps the sign, the exponent and
-// the 10 leading mantissa bits of x (the rest cleared), lo = x - hi exactly. The
-// tensor core reads a 32-bit operand at tf32 precision (the low 13 mantissa bits
-// ignored), so it sees lo' with |lo - lo'| < 2^-10 |lo| < 2^-20 |x|, and
-// hi*hi + hi*lo' + lo'*hi stays within a few units of 2^-20 of the exact product:
-// fp32-level accuracy from one integer and one float operation, no conversions.
-__device__ __forceinline__ void split_hl(float x, float &hi, float &lo) {
-    hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-    lo = __fsub_rn(x, hi);
+// One 16-byte unit of an image (8 consecutive K elements of one row) at byte `o` of
+// an image whose row groups are `sbo` bytes apart: its row r and first element k0.
+__device__ __forceinline__ void image_unit(uint32_t o, uint32_t sbo, int &r, int &k0) {
+    r = static_cast<int>((o / sbo) * 8 + (o % 128) / 16);
+    k0 = static_cast<int>(((o % sbo) / 128) * 8);
 }
 
-__device__ __forceinline__ void split4(float4 x, float4 &hi, float4 &lo) {
-    split_hl(x.x, hi.x, lo.x);
-    split_hl(x.y, hi.y, lo.y);
-    split_hl(x.z, hi.z, lo.z);
-    split_hl(x.w, hi.w, lo.w);
+// Unit u (0 .. 511) of a w K image part (rows d = dk, K = positions), by the units a
+// warp takes: 32 consecutive rows d at one position block cc (8 positions), so that
+// the warp's reads of the raw k rows, k[cc + j][d], fall on 32 different banks.
+__device__ __forceinline__ void wk_unit(int u, int &d, int &cc) {
+    cc = 8 * (u / kS);
+    d = u % kS;
+}
+
+// x[0..7] split into bf16 hi and lo parts (tc::split_bf16x2, pairs in K order) and
+// stored as one 16-byte unit of each part.
+__device__ __forceinline__ void split8_store(const float (&x)[8], unsigned char *hi_dst,
+                                             unsigned char *lo_dst) {
+    uint4 h, l;
+    tc::split_bf16x2(x[0], x[1], h.x, l.x);
+    tc::split_bf16x2(x[2], x[3], h.y, l.y);
+    tc::split_bf16x2(x[4], x[5], h.z, l.z);
+    tc::split_bf16x2(x[6], x[7], h.w, l.w);
+    *reinterpret_cast<uint4 *>(hi_dst) = h;
+    *reinterpret_cast<uint4 *>(lo_dst) = l;
+}
+
+// 16 fp32 values of a tensor-memory row split into 8 packed hi and 8 packed lo words.
+__device__ __forceinline__ void split16_packed(const float (&x)[16], uint32_t (&hi)[8],
+                                               uint32_t (&lo)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tc::split_bf16x2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+}
+
+// The state split of a chunk, for columns c0 .. c0 + 63 of the tensor-memory lane at
+// trow (one thread's row of S^T): S -> packed (hi, lo), the A operand of the S
+// products, and the accumulator scaled to Gam_31 S, ready for the chunk's update; four
+// passes of 16 columns. Completes its stores (tcgen05.wait::st) before returning.
+__device__ __forceinline__ void split_state_row(uint32_t trow, int c0, float gn) {
+#pragma unroll 1
+    for (int h = 0; h < 4; ++h) {
+        const uint32_t col = c0 + 16 * h;
+        uint32_t r[16], hi[8], lo[8];
+        tc::tmem_ld16_nowait(trow + kColSacc + col, r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tc::split_bf16x2(u2f(r[2 * e]), u2f(r[2 * e + 1]), hi[e], lo[e]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) r[e] = f2u(gn * u2f(r[e]));
+        tc::tmem_st8(trow + kColShi + col / 2, hi);
+        tc::tmem_st8(trow + kColSlo + col / 2, lo);
+        tc::tmem_st16(trow + kColSacc + col, r);
+    }
+    tc::tmem_st_wait();
 }
 
 // Partial Gram products of row t against columns s0 + 8 j, j < JN, over all of dk:

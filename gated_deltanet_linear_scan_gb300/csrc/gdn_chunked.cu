@@ -1,6 +1,6 @@
 // gdn_chunked.cu -- the multi-token scan of the delta-rule recurrence in chunks of
 // 32 positions, with the state-dependent contractions on the 5th-generation tensor
-// cores (tcgen05, TF32 inputs, fp32 accumulation in tensor memory).
+// cores (tcgen05, bf16 hi / lo operand parts, fp32 accumulation in tensor memory).
 //
 // fm_kernel_ssm.m (its softplus note and the sequential-scan section) speaks of a
 // chunked prefill path that takes cumulative sums of g along each chunk, with the
@@ -22,7 +22,7 @@
 // SM. The state lives in tensor memory as S^T (lane = dv, column = dk) for the
 // whole scan. Warp roles, linked only by mbarriers:
 //   producer (1 warp)  bulk-copies the k, q, v rows of each chunk into a 2-deep ring;
-//   state (8 warps)    split S into tf32 hi/lo parts in tensor memory (the A
+//   state (8 warps)    split S into bf16 hi/lo parts in tensor memory (the A
 //                      operand), form U^T = Ut^T - D_u and its split, write y, and in
 //                      between, on the CUDA cores in fp32, the next chunk's Gram stage
 //                      (gam and the Gram products A and M);
@@ -33,10 +33,13 @@
 //                      passes (gdn_chunk_common.cuh), then S^T = Gam_31 S^T + U^T (w K)
 //                      and D_y += U^T M^T.
 //
-// Precision: a single TF32 pass (10-bit mantissa) in the products that feed the
-// state or y misses a 2e-3-of-RMS error bound after 4096 positions; the split
-// x = hi + lo with hi*hi + hi*lo + lo*hi ("3xTF32") restores fp32-level products,
-// and every product here uses it.
+// Precision: one pass of bf16 (8 significant bits) or of tf32 (11) in the products
+// that feed the state or y misses a 2e-3-of-RMS error bound over long scans. Every
+// product here takes the split x = hi + lo into two bf16 parts (hi = bf16(x),
+// lo = bf16(x - hi)) and sums hi*hi + hi*lo + lo*hi ("3xBF16"): products within about
+// 3 * 2^-16 relative, which keeps a 4096-position scan near 1e-4 of the output's RMS.
+// A bf16 MMA (K = 16) takes the tensor pipe about as long as a tf32 one (K = 8), so
+// the three bf16 passes cost half of what three tf32 passes would.
 #include "gdn_chunk_common.cuh"
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
@@ -52,8 +55,8 @@ constexpr unsigned WD_MMA = 8u;  // a hand-off between the roles of the chunked 
 
 // ---- shared memory (bytes)
 // tensor-core operand images at kOffWQ .. kImgBytes (gdn_chunk_common.cuh), then
-constexpr uint32_t kOffUt = kImgBytes;  // Ut, plain [c][dv] fp32
-constexpr uint32_t kOffWs = 122880;    // W [32][132] fp32, from the substitution
+constexpr uint32_t kOffUt = kImgBytes;                  // Ut, plain [c][dv] fp32
+constexpr uint32_t kOffWs = kOffUt + kC * kS * 4;       // W [32][132] fp32, from the substitution
 // raw rows of k and q: 2 buffers x 2 arrays x 32 rows (v is read from global memory)
 constexpr uint32_t kRawBuf = 2 * kRawArr;
 constexpr uint32_t kOffRaw = kOffWs + kRawArr;
@@ -72,7 +75,7 @@ struct Bars {
 };
 constexpr size_t kSmemBytes = kOffBars + sizeof(Bars);
 static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
-static_assert(kOffWs == kOffUt + kC * kS * 4, "image layout");
+static_assert(kOffWs % 16 == 0 && kOffRaw % 16 == 0, "bulk-copy and float4 alignment");
 static_assert(kOffBars % 8 == 0, "mbarrier alignment");
 
 // ---- warps
@@ -86,6 +89,8 @@ constexpr int kStateThreads = 32 * kStateWarps;
 // mbarriers and the other warps sleep in the named barrier, which leaves the issue
 // slots to the warps doing arithmetic.
 constexpr int kPrepBarrier = 1, kStateBarrier = 2;
+// 16-byte image units (8 bf16) of an operand image part
+constexpr int kUnits128x32 = kC * kS / 8, kUnitsM = kC * kC / 8;
 
 // The Gram stage of a chunk, by the 256 threads of one role (warp gw = 0..7), on the
 // thread mapping of gram_products:
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars.raw_full[i], 1);
+            mbar_init(&bars.raw_full[i], 32);  // one arrival per producer lane
             mbar_init(&bars.raw_empty[i], 1);
             mbar_init(&bars.gram_ready[i], 1);
         }
@@ -190,14 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             if (use > 0 && !waitw(&bars.raw_empty[b], use - 1, WD_STAGE_FREE)) break;
             const int t0 = ci * kC, valid = min(kC, n_tokens - t0);
             unsigned char *raw = smem + kOffRaw + b * kRawBuf;
-            if (lane == 0) mbar_arrive_expect_tx(&bars.raw_full[b], 2u * valid * kS * 4);
-            __syncwarp();
-            if (lane < valid) {
-                const size_t row = row0 + t0 + lane;
-                bulk_g2s(raw + lane * kRawRow, k + (row * Hk + kh) * kS, kS * 4, &bars.raw_full[b]);
-                bulk_g2s(raw + kRawArr + lane * kRawRow, q + (row * Hk + kh) * kS, kS * 4,
-                         &bars.raw_full[b]);
+            // row r of k and of q: lane l moves bytes 16 l .. 16 l + 15 (one 512-byte row a
+            // warp instruction); each lane then arrives on raw_full once its copies land
+            for (int r = 0; r < valid; ++r) {
+                const size_t row = ((row0 + t0 + r) * Hk + kh) * kS + 4 * lane;
+                cp_async16(raw + r * kRawRow + 16 * lane, k + row);
+                cp_async16(raw + kRawArr + r * kRawRow + 16 * lane, q + row);
             }
+            cp_async_arrive_noinc(&bars.raw_full[b]);
             issued = ci + 1;
         }
         // never leave with a copy still landing: wait for the last fill of each buffer
@@ -206,30 +211,37 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t id64 = tc::idesc_tf32(128, 2 * kC), id128 = tc::idesc_tf32(128, kS),
-                           id160 = tc::idesc_tf32(128, kS + kC);
+            const uint32_t id64 = tc::idesc_bf16(128, 2 * kC), id128 = tc::idesc_bf16(128, kS),
+                           id160 = tc::idesc_bf16(128, kS + kC);
             auto desc = [&](uint32_t off, uint32_t sbo) { return tc::smem_desc(smem + off, kLbo, sbo); };
+            // K step ks starts 2 core matrices (256 bytes) further: + 16 in the
+            // descriptor's address field (no carry: shared memory stays below 256 KiB)
+            const uint64_t d_wq = desc(kOffWQ, kSbo128);
+            constexpr uint64_t kStep = (2 * kLbo) >> 4;
+            const uint64_t d_hi = desc(kOffKhi, kSbo32), d_lo = desc(kOffKlo, kSbo32);
             for (int ci = 0; ci < n_chunks; ++ci) {
                 if (!wait1(&bars.img_ready, ci, WD_MMA)) break;
                 if (!wait1(&bars.s_ready, ci, WD_MMA)) break;
                 tc::fence_after_sync();
-                // the S products: hi(S) against all 128 image rows (N = 128), then lo(S)
-                // against hi(Gam q) and hi(W) (N = 64) into the first two blocks of D
-                for (int ks = 0; ks < kS / 8; ++ks)
-                    tc::mma_tf32_ts(tmem + kColD, tmem + kColShi + 8 * ks,
-                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id128, ks > 0);
-                for (int ks = 0; ks < kS / 8; ++ks)
-                    tc::mma_tf32_ts(tmem + kColD, tmem + kColSlo + 8 * ks,
-                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id64, true);
+                // the S products, K = 16 a step (8 packed columns of S): hi(S) against all
+                // 128 image rows (N = 128), then lo(S) against hi(Gam q) and hi(W) (N = 64)
+                // into the first two blocks of D
+                for (int ks = 0; ks < kS / 16; ++ks)
+                    tc::mma_bf16_ts(tmem + kColD, tmem + kColShi + 8 * ks, d_wq + kStep * ks,
+                                    id128, ks > 0);
+                for (int ks = 0; ks < kS / 16; ++ks)
+                    tc::mma_bf16_ts(tmem + kColD, tmem + kColSlo + 8 * ks, d_wq + kStep * ks,
+                                    id64, true);
                 tc::mma_commit(&bars.a_done);
                 if (!wait1(&bars.u_ready, ci, WD_MMA)) break;
                 tc::fence_after_sync();
                 // [S^T | D_y] += U^T [w K | M]^T: hi hi + hi lo + lo hi
                 for (int p = 0; p < 3; ++p) {
-                    const uint32_t a = p == 2 ? kColUlo : kColUhi, bo = p == 1 ? kOffKlo : kOffKhi;
-                    for (int ks = 0; ks < kC / 8; ++ks)
-                        tc::mma_tf32_ts(tmem + kColSacc, tmem + a + 8 * ks,
-                                        desc(bo + ks * 2 * kLbo, kSbo32), id160, true);
+                    const uint32_t a = p == 2 ? kColUlo : kColUhi;
+                    const uint64_t bd = p == 1 ? d_lo : d_hi;
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        tc::mma_bf16_ts(tmem + kColSacc, tmem + a + 8 * ks, bd + kStep * ks, id160,
+                                        true);
                 }
                 tc::mma_commit(&bars.b_done);
             }
@@ -335,26 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             }
             // S -> (hi, lo), the A operand of the S products; the accumulator becomes
             // Gam_31 S, ready for this chunk's update
-#pragma unroll 1
-            for (int blk = 0; blk < 4; ++blk) {
-                const uint32_t col = c0 + 16 * blk;
-                uint32_t r[16], hi[16], lo[16];
-                tc::tmem_ld16_nowait(trow + kColSacc + col, r);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float x = u2f(r[e]);
-                    float h, l;
-                    split_hl(x, h, l);
-                    hi[e] = f2u(h);
-                    lo[e] = f2u(l);
-                    r[e] = f2u(gn * x);
-                }
-                tc::tmem_st16(trow + kColShi + col, hi);
-                tc::tmem_st16(trow + kColSlo + col, lo);
-                tc::tmem_st16(trow + kColSacc + col, r);
-            }
-            tc::tmem_st_wait();
+            split_state_row(trow, c0, gn);
             // the previous chunk's y leaves D_y before this chunk's MMAs overwrite it
             float yv[16];
             if (ci > 0) read_y(yv);
@@ -371,20 +364,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             if (!(ok = st_wait(&bars.a_done, ci))) break;
             tc::fence_after_sync();
             {
-                uint32_t du[16], du2[16], hi[16], lo[16];
+                uint32_t du[16], du2[16], hi[8], lo[8];
+                float u[16];
                 tc::tmem_ld16_nowait(trow + kColDuA + u0, du);
                 tc::tmem_ld16_nowait(trow + kColDuB + u0, du2);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float u = ut[(u0 + e) * kS + dv] - (u2f(du[e]) + u2f(du2[e]));
-                    float h, l;
-                    split_hl(u, h, l);
-                    hi[e] = f2u(h);
-                    lo[e] = f2u(l);
-                }
-                tc::tmem_st16(trow + kColUhi + u0, hi);
-                tc::tmem_st16(trow + kColUlo + u0, lo);
+                for (int e = 0; e < 16; ++e) u[e] = ut[(u0 + e) * kS + dv] - (u2f(du[e]) + u2f(du2[e]));
+                split16_packed(u, hi, lo);
+                // positions u0.. of this warp, two to a column
+                tc::tmem_st8(trow + kColUhi + u0 / 2, hi);
+                tc::tmem_st8(trow + kColUlo + u0 / 2, lo);
                 tc::tmem_st_wait();
             }
             st_signal(&bars.u_ready);
@@ -489,51 +479,47 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
                 for (int t = 0; t < kC; ++t) outp[t * ostride + col] = x[t];
             }
             named_barrier_sync(kPrepBarrier, kPrepThreads);
-            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {  // W, split
+            // the images take 16-byte units of 8 bf16: 8 fp32 values a unit
+            for (int idx = pt; idx < kUnits128x32; idx += kPrepThreads) {  // W, split
                 const uint32_t o = idx * 16u;
-                const int c = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
-                float4 hi, lo;
-                split4(ld4(ws + c * kRawRowF + k0), hi, lo);
-                *reinterpret_cast<float4 *>(smem + kOffWhi + o) = hi;
-                *reinterpret_cast<float4 *>(smem + kOffWlo + o) = lo;
+                int c, k0;
+                image_unit(o, kSbo128, c, k0);
+                const float4 a = ld4(ws + c * kRawRowF + k0), b4 = ld4(ws + c * kRawRowF + k0 + 4);
+                const float x[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+                split8_store(x, smem + kOffWhi + o, smem + kOffWlo + o);
             }
-
             // Gam_t q_t, split (the S products that read it finished before U was formed)
-            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {
+            for (int idx = pt; idx < kUnits128x32; idx += kPrepThreads) {
                 const uint32_t o = idx * 16u;
-                const int t = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
+                int t, k0;
+                image_unit(o, kSbo128, t, k0);
                 const float Gt = __shfl_sync(FULL_MASK, Gam, t);
-                float4 xv = ld4(rq + t * kRawRowF + k0);
-                xv.x *= Gt; xv.y *= Gt; xv.z *= Gt; xv.w *= Gt;
-                float4 hi, lo;
-                split4(xv, hi, lo);
-                *reinterpret_cast<float4 *>(smem + kOffQhi + o) = hi;
-                *reinterpret_cast<float4 *>(smem + kOffQlo + o) = lo;
+                const float4 a = ld4(rq + t * kRawRowF + k0), b4 = ld4(rq + t * kRawRowF + k0 + 4);
+                float x[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] *= Gt;
+                split8_store(x, smem + kOffQhi + o, smem + kOffQlo + o);
             }
             // ---- w_c k_c and M, split, once the previous chunk's state update is done
             if (ci > 0 ? prep_wait(&bars.b_done, ci - 1, WD_MMA) : prep_sync()) break;
-            for (int idx = pt; idx < kS * kC / 4; idx += kPrepThreads) {
-                const uint32_t o = idx * 16u;
-                const int d = (o / kSbo32) * 8 + (o % 128) / 16, cc = ((o % kSbo32) / 128) * 4;
-                float4 xv;
-                xv.x = __shfl_sync(FULL_MASK, wdec, cc) * rk[cc * kRawRowF + d];
-                xv.y = __shfl_sync(FULL_MASK, wdec, cc + 1) * rk[(cc + 1) * kRawRowF + d];
-                xv.z = __shfl_sync(FULL_MASK, wdec, cc + 2) * rk[(cc + 2) * kRawRowF + d];
-                xv.w = __shfl_sync(FULL_MASK, wdec, cc + 3) * rk[(cc + 3) * kRawRowF + d];
-                float4 hi, lo;
-                split4(xv, hi, lo);
-                *reinterpret_cast<float4 *>(smem + kOffKhi + o) = hi;
-                *reinterpret_cast<float4 *>(smem + kOffKlo + o) = lo;
+            for (int u = pt; u < kUnits128x32; u += kPrepThreads) {
+                int d, cc;
+                wk_unit(u, d, cc);
+                const uint32_t o = tc::kmajor_offset16(d, cc, kLbo, kSbo32);
+                float x[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    x[j] = __shfl_sync(FULL_MASK, wdec, cc + j) * rk[(cc + j) * kRawRowF + d];
+                split8_store(x, smem + kOffKhi + o, smem + kOffKlo + o);
             }
-
             // M, split (read by the same MMAs as w K)
-            for (int idx = pt; idx < kC * kC / 4; idx += kPrepThreads) {
+            for (int idx = pt; idx < kUnitsM; idx += kPrepThreads) {
                 const uint32_t o = idx * 16u;
-                const int t = (o / kSbo32) * 8 + (o % 128) / 16, s0 = ((o % kSbo32) / 128) * 4;
-                float4 hi, lo;
-                split4(ld4(Msc + t * kC + s0), hi, lo);
-                *reinterpret_cast<float4 *>(smem + kOffMhi + o) = hi;
-                *reinterpret_cast<float4 *>(smem + kOffMlo + o) = lo;
+                int t, s0;
+                image_unit(o, kSbo32, t, s0);
+                const float4 a = ld4(Msc + t * kC + s0), b4 = ld4(Msc + t * kC + s0 + 4);
+                const float x[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+                split8_store(x, smem + kOffMhi + o, smem + kOffMlo + o);
             }
             // the operands are read by the tensor cores (async proxy) and Ut by the
             // state warps

@@ -15,7 +15,7 @@
 //                          (I + A) Ut = diag(beta) V; W, Ut and M go to the workspace.
 //   chunk_state_kernel     one CTA per (sequence, v-head), sequential over chunks:
 //                          only the state-dependent part, U = Ut - W S, y and the
-//                          state update, on the tensor cores (3xTF32), with W, Ut and M
+//                          state update, on the tensor cores (3xBF16), with W, Ut and M
 //                          read back from the workspace.
 //
 // Both kernels run the arithmetic of gdn_chunked.cu in the same order, so the two
@@ -220,19 +220,27 @@ __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
 }
 
 // ============================================================================ phase 2
-// shared memory (bytes): the operand images, then the raw k and q rows of 2 chunks
-// The w K | M image (both parts) is double-buffered: the prep warps build chunk ci's
-// while the state update of chunk ci - 1 still reads the other buffer.
-constexpr uint32_t kKMBytes = kImgBytes - kOffKhi;  // 40 KB: one w K | M image, hi and lo
-constexpr uint32_t kOffKM1 = kImgBytes;             // second buffer (offset kKMBytes on)
-constexpr uint32_t kRawBuf = 2 * kRawArr;
-constexpr uint32_t kOffRaw = kOffKM1 + kKMBytes;
+// shared memory (bytes): the operand images of two chunks, then a ring of two chunk
+// stages (the raw k and q rows, and the W and M rows from the workspace, each row padded
+// so that a float4 column walk over 8 rows covers all banks). Both images are double-buffered, so the prep warps build chunk ci + 1's
+// (buffer (ci + 1) & 1) while the tensor cores still read chunk ci's: image buffer 0 is
+// the layout of gdn_chunk_common.cuh at 0 (128-row image, then w K | M); buffer 1 is the
+// w K | M image at kOffKM1 and the 128-row image at kOffWQ1.
+constexpr uint32_t kKMBytes = kImgBytes - kOffKhi;  // 20 KB: one w K | M image, hi and lo
+constexpr uint32_t kWQBytes = kOffKhi;              // 32 KB: one 128-row image, hi and lo
+constexpr uint32_t kOffKM1 = kImgBytes;             // second w K | M buffer
+constexpr uint32_t kOffWQ1 = kOffKM1 + kKMBytes;    // second 128-row image
+constexpr int kMRowF = kC + 4;                      // M rows in a stage: 36 floats
+constexpr uint32_t kStW = 2 * kRawArr, kStM = 3 * kRawArr;  // within a stage
+constexpr uint32_t kRawBuf = kStM + kC * kMRowF * 4;        // one stage: 55,296 bytes
+constexpr uint32_t kOffRaw = kOffWQ1 + kWQBytes;
 constexpr uint32_t kOffBars = kOffRaw + 2 * kRawBuf;
 static_assert(kOffKM1 == kOffKhi + kKMBytes, "second w K | M buffer follows the first");
+static_assert(kOffWQ1 % 1024 == 0 && kOffRaw % 16 == 0, "buffer alignment");
 
 struct Bars {
-    uint64_t raw_full[2], raw_empty[2], km_free[2];
-    uint64_t img_ready, s_ready, u_ready;
+    uint64_t raw_full[2], raw_empty[2];
+    uint64_t img_ready[2], buf_free[2], s_ready, u_ready;
     uint64_t a_done, b_done, fin;
     uint32_t taddr;
     int abort;
@@ -248,6 +256,9 @@ constexpr int kThreads = 32 * (kPrepWarp0 + kPrepWarps);  // 576
 constexpr int kPrepThreads = 32 * kPrepWarps;
 constexpr int kStateThreads = 32 * kStateWarps;
 constexpr int kPrepBarrier = 1, kStateBarrier = 2;
+// 16-byte image units (8 bf16) of W and of M a prep thread converts per chunk
+constexpr int kWUnits = kC * kS / 8 / kPrepThreads, kMUnits = kC * kC / 8;
+static_assert(kWUnits * kPrepThreads * 8 == kC * kS && kMUnits <= kPrepThreads, "unit split");
 
 // One CTA per (sequence, v-head); grid = n_seqs * n_v_heads. Advances the state over
 // chunks c_begin .. c_begin + n_wave_chunks - 1, whose workspace blocks are prepared.
@@ -291,11 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars.raw_full[i], 1);
+            mbar_init(&bars.raw_full[i], 32);  // one arrival per producer lane
             mbar_init(&bars.raw_empty[i], 1);
-            mbar_init(&bars.km_free[i], 1);
         }
-        mbar_init(&bars.img_ready, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.img_ready[i], 1);  // chunk ci's images are in buffer ci & 1
+            mbar_init(&bars.buf_free[i], 1);   // the MMAs of chunk ci are done with it
+        }
         mbar_init(&bars.s_ready, 1);
         mbar_init(&bars.u_ready, 1);
         mbar_init(&bars.a_done, 1);
@@ -344,14 +357,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             if (use > 0 && !waitw(&bars.raw_empty[b], use - 1, WD_STAGE_FREE)) break;
             const int t0 = chunk_t0(ci), valid = min(kC, n_tokens - t0);
             unsigned char *raw = smem + kOffRaw + b * kRawBuf;
-            if (lane == 0) mbar_arrive_expect_tx(&bars.raw_full[b], 2u * valid * kS * 4);
-            __syncwarp();
-            if (lane < valid) {
-                const size_t row = row0 + t0 + lane;
-                bulk_g2s(raw + lane * kRawRow, k + (row * Hk + kh) * kS, kS * 4, &bars.raw_full[b]);
-                bulk_g2s(raw + kRawArr + lane * kRawRow, q + (row * Hk + kh) * kS, kS * 4,
-                         &bars.raw_full[b]);
+            // row r of k and of q: lane l moves bytes 16 l .. 16 l + 15 (one 512-byte row a
+            // warp instruction); then the chunk's W rows and M rows from its workspace
+            // block (all 32 of each are written there); each lane then arrives on raw_full
+            // once its copies land
+            for (int r = 0; r < valid; ++r) {
+                const size_t row = ((row0 + t0 + r) * Hk + kh) * kS + 4 * lane;
+                cp_async16(raw + r * kRawRow + 16 * lane, k + row);
+                cp_async16(raw + kRawArr + r * kRawRow + 16 * lane, q + row);
             }
+            const float *blk = blk_of(ci);
+            for (int r = 0; r < kC; ++r)
+                cp_async16(raw + kStW + r * kRawRow + 16 * lane, blk + kBlkW + r * kS + 4 * lane);
+            for (int i = 0; i < kC / 4; ++i) {  // 4 rows of M (128 bytes each) a warp instruction
+                const int r = 4 * i + (lane >> 3), c4 = 4 * (lane & 7);
+                cp_async16(raw + kStM + (r * kMRowF + c4) * 4, blk + kBlkM + r * kC + c4);
+            }
+            cp_async_arrive_noinc(&bars.raw_full[b]);
             issued = ci + 1;
         }
         for (int ci = max(0, issued - 2); ci < issued; ++ci)
@@ -359,35 +381,42 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t id64 = tc::idesc_tf32(128, 2 * kC), id128 = tc::idesc_tf32(128, kS),
-                           id160 = tc::idesc_tf32(128, kS + kC);
+            const uint32_t id64 = tc::idesc_bf16(128, 2 * kC), id128 = tc::idesc_bf16(128, kS),
+                           id160 = tc::idesc_bf16(128, kS + kC);
             auto desc = [&](uint32_t off, uint32_t sbo) { return tc::smem_desc(smem + off, kLbo, sbo); };
+            // K step ks starts 2 core matrices (256 bytes) further: + 16 in the
+            // descriptor's address field (no carry: shared memory stays below 256 KiB)
+            const uint64_t d_wq0 = desc(kOffWQ, kSbo128), d_wq1 = desc(kOffWQ1, kSbo128);
+            constexpr uint64_t kStep = (2 * kLbo) >> 4;
             for (int ci = 0; ci < nw; ++ci) {
-                if (!wait1(&bars.img_ready, ci, WD_MMA)) break;
+                if (!wait1(&bars.img_ready[ci & 1], ci >> 1, WD_MMA)) break;
+                const uint64_t d_wq = ci & 1 ? d_wq1 : d_wq0;
                 if (!wait1(&bars.s_ready, ci, WD_MMA)) break;
                 tc::fence_after_sync();
-                // the S products: hi(S) against all 128 image rows (N = 128), then lo(S)
-                // against hi(Gam q) and hi(W) (N = 64) into the first two blocks of D
-                for (int ks = 0; ks < kS / 8; ++ks)
-                    tc::mma_tf32_ts(tmem + kColD, tmem + kColShi + 8 * ks,
-                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id128, ks > 0);
-                for (int ks = 0; ks < kS / 8; ++ks)
-                    tc::mma_tf32_ts(tmem + kColD, tmem + kColSlo + 8 * ks,
-                                    desc(kOffWQ + ks * 2 * kLbo, kSbo128), id64, true);
+                // the S products, K = 16 a step (8 packed columns of S): hi(S) against all
+                // 128 image rows (N = 128), then lo(S) against hi(Gam q) and hi(W) (N = 64)
+                // into the first two blocks of D
+                for (int ks = 0; ks < kS / 16; ++ks)
+                    tc::mma_bf16_ts(tmem + kColD, tmem + kColShi + 8 * ks, d_wq + kStep * ks,
+                                    id128, ks > 0);
+                for (int ks = 0; ks < kS / 16; ++ks)
+                    tc::mma_bf16_ts(tmem + kColD, tmem + kColSlo + 8 * ks, d_wq + kStep * ks,
+                                    id64, true);
                 tc::mma_commit(&bars.a_done);
                 if (!wait1(&bars.u_ready, ci, WD_MMA)) break;
                 tc::fence_after_sync();
                 // [S^T | D_y] += U^T [w K | M]^T: hi hi + hi lo + lo hi, from buffer ci & 1
                 const uint32_t km = (ci & 1) * kKMBytes;
+                const uint64_t d_hi = desc(kOffKhi + km, kSbo32), d_lo = desc(kOffKlo + km, kSbo32);
                 for (int p = 0; p < 3; ++p) {
-                    const uint32_t a = p == 2 ? kColUlo : kColUhi,
-                                   bo = (p == 1 ? kOffKlo : kOffKhi) + km;
-                    for (int ks = 0; ks < kC / 8; ++ks)
-                        tc::mma_tf32_ts(tmem + kColSacc, tmem + a + 8 * ks,
-                                        desc(bo + ks * 2 * kLbo, kSbo32), id160, true);
+                    const uint32_t a = p == 2 ? kColUlo : kColUhi;
+                    const uint64_t bd = p == 1 ? d_lo : d_hi;
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        tc::mma_bf16_ts(tmem + kColSacc, tmem + a + 8 * ks, bd + kStep * ks, id160,
+                                        true);
                 }
                 tc::mma_commit(&bars.b_done);
-                tc::mma_commit(&bars.km_free[ci & 1]);
+                tc::mma_commit(&bars.buf_free[ci & 1]);
             }
             tc::mma_commit(&bars.fin);  // tensor memory stays allocated until all MMAs end
             mbar_wait_sleep(&bars.fin, 0, 128);
@@ -461,26 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             }
             // S -> (hi, lo), the A operand of the S products; the accumulator becomes
             // Gam_31 S, ready for this chunk's update
-#pragma unroll 1
-            for (int blk = 0; blk < 4; ++blk) {
-                const uint32_t col = c0 + 16 * blk;
-                uint32_t r[16], hi[16], lo[16];
-                tc::tmem_ld16_nowait(trow + kColSacc + col, r);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float x = u2f(r[e]);
-                    float h, l;
-                    split_hl(x, h, l);
-                    hi[e] = f2u(h);
-                    lo[e] = f2u(l);
-                    r[e] = f2u(gn * x);
-                }
-                tc::tmem_st16(trow + kColShi + col, hi);
-                tc::tmem_st16(trow + kColSlo + col, lo);
-                tc::tmem_st16(trow + kColSacc + col, r);
-            }
-            tc::tmem_st_wait();
+            split_state_row(trow, c0, gn);
             float yv[16];
             if (ci > 0) read_y(yv);
             st_signal(&bars.s_ready);
@@ -491,20 +501,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             if (!(ok = st_wait(&bars.a_done, ci))) break;
             tc::fence_after_sync();
             {
-                uint32_t du[16], du2[16], hi[16], lo[16];
+                uint32_t du[16], du2[16], hi[8], lo[8];
+                float u[16];
                 tc::tmem_ld16_nowait(trow + kColDuA + u0, du);
                 tc::tmem_ld16_nowait(trow + kColDuB + u0, du2);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float u = utv[e] - (u2f(du[e]) + u2f(du2[e]));
-                    float h, l;
-                    split_hl(u, h, l);
-                    hi[e] = f2u(h);
-                    lo[e] = f2u(l);
-                }
-                tc::tmem_st16(trow + kColUhi + u0, hi);
-                tc::tmem_st16(trow + kColUlo + u0, lo);
+                for (int e = 0; e < 16; ++e) u[e] = utv[e] - (u2f(du[e]) + u2f(du2[e]));
+                split16_packed(u, hi, lo);
+                // positions u0.. of this warp, two to a column
+                tc::tmem_st8(trow + kColUhi + u0 / 2, hi);
+                tc::tmem_st8(trow + kColUlo + u0 / 2, lo);
                 tc::tmem_st_wait();
             }
             st_signal(&bars.u_ready);
@@ -528,97 +535,94 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
     } else {
         // ------------------------------------------------------------ prep warps
         const int pt = tid - 32 * kPrepWarp0;  // 0..255
-        auto prep_wait = [&](uint64_t *bar, int parity, unsigned bit) {
-            return !group_wait(pt == 0, kPrepBarrier, kPrepThreads, bar, parity, bit);
-        };
-        auto prep_sync = [&]() {
-            return named_barrier_or(kPrepBarrier, kPrepThreads, *abort_flag != 0);
-        };
         float g_next = 0.f;
         if (chunk_t0(0) + lane < n_tokens) g_next = g[(row0 + chunk_t0(0) + lane) * H + vh];
+        // true: leave the loop. The leader waits for the chunk's k and q rows and, from
+        // the third chunk on, for image buffer cj & 1 to be free (the MMAs of chunk
+        // cj - 2 are done with it).
+        auto prep_wait_chunk = [&](int cj) {
+            bool failed = false;
+            if (pt == 0)
+                failed = !wait1(&bars.raw_full[cj & 1], cj >> 1, WD_STAGE_COPY) ||
+                         (cj > 1 && !wait1(&bars.buf_free[cj & 1], (cj >> 1) - 1, WD_MMA)) ||
+                         (cj > 0 && !wait1(&bars.a_done, cj - 1, WD_MMA));
+            return named_barrier_or(kPrepBarrier, kPrepThreads, failed || *abort_flag);
+        };
         for (int ci = 0; ci < nw; ++ci) {
-            const int b = ci & 1, use = ci >> 1;
+            const int b = ci & 1;
             const int t0 = chunk_t0(ci), valid = min(kC, n_tokens - t0);
             const float *rk = reinterpret_cast<const float *>(smem + kOffRaw + b * kRawBuf);
             const float *rq = rk + kC * kRawRowF;
-            const float *blk = blk_of(ci);
+            const float *sw = reinterpret_cast<const float *>(smem + kOffRaw + b * kRawBuf + kStW);
+            const float *sm = reinterpret_cast<const float *>(smem + kOffRaw + b * kRawBuf + kStM);
             float last;
             const float gam = chunk_gam_from(g_next, lane, last);
             const float Gam = expf(gam), wdec = expf(last - gam);
             g_next = 0.f;
             if (ci + 1 < nw && chunk_t0(ci + 1) + lane < n_tokens)
                 g_next = g[(row0 + chunk_t0(ci + 1) + lane) * H + vh];
-            // this chunk's W and M, in the order the images take them
-            float4 wv[kC * kS / 4 / kPrepThreads], mv;
+            // 8 fp32 values from p, one 16-byte image unit (8 bf16) of a part
+            auto ld8 = [](const float *p, float (&x)[8]) {
+                const float4 a = ld4(p), b4 = ld4(p + 4);
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                x[4] = b4.x; x[5] = b4.y; x[6] = b4.z; x[7] = b4.w;
+            };
+            if (prep_wait_chunk(ci)) break;
+            // W and Gam_t q_t, split (rows past the end of the sequence count as zero), into
+            // image buffer ci & 1
+            unsigned char *wq = smem + (b ? kOffWQ1 : kOffWQ);
 #pragma unroll
-            for (int i = 0; i < kC * kS / 4 / kPrepThreads; ++i) {
-                const uint32_t o = (pt + i * kPrepThreads) * 16u;
-                const int c = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
-                wv[i] = ld4(blk + kBlkW + c * kS + k0);
+            for (int j = 0; j < kWUnits; ++j) {
+                const uint32_t o = (pt + j * kPrepThreads) * 16u;
+                int c, k0;
+                float x[8];
+                image_unit(o, kSbo128, c, k0);
+                ld8(sw + c * kRawRowF + k0, x);
+                split8_store(x, wq + kOffWhi + o, wq + kOffWlo + o);
             }
-            {
-                const uint32_t o = pt * 16u;
-                const int t = (o / kSbo32) * 8 + (o % 128) / 16, s0 = ((o % kSbo32) / 128) * 4;
-                mv = ld4(blk + kBlkM + t * kC + s0);
-            }
-            static_assert(kC * kC / 4 == kPrepThreads, "one float4 of M per prep thread");
-
-            // the chunk's k and q rows (rows past the end of the sequence count as zero)
-            if (prep_wait(&bars.raw_full[b], use, WD_STAGE_COPY)) break;
-            // w_c k_c and M, split, into buffer ci & 1 once the state update of chunk
-            // ci - 2 has finished reading it
-            if (use > 0 ? prep_wait(&bars.km_free[b], use - 1, WD_MMA) : prep_sync()) break;
-            unsigned char *kmb = smem + b * kKMBytes;
-            for (int idx = pt; idx < kS * kC / 4; idx += kPrepThreads) {
+            for (int idx = pt; idx < kC * kS / 8; idx += kPrepThreads) {
                 const uint32_t o = idx * 16u;
-                const int d = (o / kSbo32) * 8 + (o % 128) / 16, cc = ((o % kSbo32) / 128) * 4;
-                float4 xv;
-                xv.x = __shfl_sync(FULL_MASK, wdec, cc) * (cc < valid ? rk[cc * kRawRowF + d] : 0.f);
-                xv.y = __shfl_sync(FULL_MASK, wdec, cc + 1) *
-                       (cc + 1 < valid ? rk[(cc + 1) * kRawRowF + d] : 0.f);
-                xv.z = __shfl_sync(FULL_MASK, wdec, cc + 2) *
-                       (cc + 2 < valid ? rk[(cc + 2) * kRawRowF + d] : 0.f);
-                xv.w = __shfl_sync(FULL_MASK, wdec, cc + 3) *
-                       (cc + 3 < valid ? rk[(cc + 3) * kRawRowF + d] : 0.f);
-                float4 hi, lo;
-                split4(xv, hi, lo);
-                *reinterpret_cast<float4 *>(kmb + kOffKhi + o) = hi;
-                *reinterpret_cast<float4 *>(kmb + kOffKlo + o) = lo;
-            }
-            {
-                float4 hi, lo;
-                split4(mv, hi, lo);
-                *reinterpret_cast<float4 *>(kmb + kOffMhi + pt * 16u) = hi;
-                *reinterpret_cast<float4 *>(kmb + kOffMlo + pt * 16u) = lo;
-            }
-            // W and Gam_t q_t, split, once the previous chunk's U is formed (its S
-            // products are done)
-            if (ci > 0 ? prep_wait(&bars.u_ready, ci - 1, WD_MMA) : prep_sync()) break;
-#pragma unroll
-            for (int i = 0; i < kC * kS / 4 / kPrepThreads; ++i) {
-                const uint32_t o = (pt + i * kPrepThreads) * 16u;
-                float4 hi, lo;
-                split4(wv[i], hi, lo);
-                *reinterpret_cast<float4 *>(smem + kOffWhi + o) = hi;
-                *reinterpret_cast<float4 *>(smem + kOffWlo + o) = lo;
-            }
-            for (int idx = pt; idx < kC * kS / 4; idx += kPrepThreads) {
-                const uint32_t o = idx * 16u;
-                const int t = (o / kSbo128) * 8 + (o % 128) / 16, k0 = ((o % kSbo128) / 128) * 4;
+                int t, k0;
+                image_unit(o, kSbo128, t, k0);
                 const float Gt = __shfl_sync(FULL_MASK, Gam, t);
-                float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t < valid) xv = ld4(rq + t * kRawRowF + k0);
-                xv.x *= Gt; xv.y *= Gt; xv.z *= Gt; xv.w *= Gt;
-                float4 hi, lo;
-                split4(xv, hi, lo);
-                *reinterpret_cast<float4 *>(smem + kOffQhi + o) = hi;
-                *reinterpret_cast<float4 *>(smem + kOffQlo + o) = lo;
+                float x[8];
+                if (t < valid) {
+                    const float4 a = ld4(rq + t * kRawRowF + k0), b4 = ld4(rq + t * kRawRowF + k0 + 4);
+                    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                    x[4] = b4.x; x[5] = b4.y; x[6] = b4.z; x[7] = b4.w;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[j] = 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] *= Gt;
+                split8_store(x, wq + kOffQhi + o, wq + kOffQlo + o);
+            }
+            // w_c k_c and M, split, into buffer ci & 1
+            unsigned char *kmb = smem + b * kKMBytes;
+            for (int u = pt; u < kS * kC / 8; u += kPrepThreads) {
+                int d, cc;
+                wk_unit(u, d, cc);
+                const uint32_t o = tc::kmajor_offset16(d, cc, kLbo, kSbo32);
+                float x[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    x[j] = __shfl_sync(FULL_MASK, wdec, cc + j) *
+                           (cc + j < valid ? rk[(cc + j) * kRawRowF + d] : 0.f);
+                split8_store(x, kmb + kOffKhi + o, kmb + kOffKlo + o);
+            }
+            if (pt < kMUnits) {
+                int t, s0;
+                float x[8];
+                image_unit(pt * 16u, kSbo32, t, s0);
+                ld8(sm + t * kMRowF + s0, x);
+                split8_store(x, kmb + kOffMhi + pt * 16u, kmb + kOffMlo + pt * 16u);
             }
             fence_proxy_async_smem();
             named_barrier_sync(kPrepBarrier, kPrepThreads);
             if (pt == 0) {
-                mbar_arrive(&bars.img_ready);
-                mbar_arrive(&bars.raw_empty[b]);  // done with this chunk's raw rows
+                mbar_arrive(&bars.img_ready[b]);
+                mbar_arrive(&bars.raw_empty[b]);  // done with this chunk's stage
             }
         }
     }

@@ -126,6 +126,21 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared by one thread (the non-bulk form: a warp
+// moves 512 contiguous bytes with one instruction, where a bulk copy per lane costs
+// the issuing thread tens of cycles per copy). Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp_async16 this thread issued before has landed. The
+// arrival is not counted in advance (.noinc): `bar`'s expected count includes it.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory accesses before later
 // async-proxy (bulk copy) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -1,13 +1,14 @@
 // gdn_tc.cuh -- 5th-generation tensor core (tcgen05) building blocks for sm_103a:
-// tensor-memory allocation, shared-memory matrix descriptors, the TF32 MMA issued
-// by one thread with its accumulator in tensor memory, completion through an
-// mbarrier, and tensor memory -> register loads.
+// tensor-memory allocation, shared-memory matrix descriptors, the TF32 and BF16
+// MMAs issued by one thread with their accumulator in tensor memory, completion
+// through an mbarrier, and tensor memory <-> register moves.
 //
 // Operand layout used throughout: K-major, no swizzle. A tile of R rows by K
-// 32-bit elements is stored as 8-row x 16-byte core matrices; element (r, k) sits
-// at byte  (r / 8) * sbo + (k / 4) * lbo + (r % 8) * 16 + (k % 4) * 4,
-// so a core matrix is 128 contiguous bytes, lbo steps to the next 4 elements of K
-// and sbo to the next 8 rows.
+// elements is stored as 8-row x 16-byte core matrices: for 32-bit elements,
+// element (r, k) sits at byte  (r / 8) * sbo + (k / 4) * lbo + (r % 8) * 16 + (k % 4) * 4;
+// for 16-bit elements at  (r / 8) * sbo + (k / 8) * lbo + (r % 8) * 16 + (k % 8) * 2.
+// A core matrix is 128 contiguous bytes, lbo steps to the next 16 bytes of K and
+// sbo to the next 8 rows.
 #pragma once
 
 #include <cstdint>
@@ -21,6 +22,12 @@ namespace tc {
 __host__ __device__ __forceinline__ uint32_t kmajor_offset(int r, int k, uint32_t lbo, uint32_t sbo) {
     return static_cast<uint32_t>(r >> 3) * sbo + static_cast<uint32_t>(k >> 2) * lbo +
            static_cast<uint32_t>(r & 7) * 16u + static_cast<uint32_t>(k & 3) * 4u;
+}
+
+// The same for 16-bit elements.
+__host__ __device__ __forceinline__ uint32_t kmajor_offset16(int r, int k, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint32_t>(r >> 3) * sbo + static_cast<uint32_t>(k >> 3) * lbo +
+           static_cast<uint32_t>(r & 7) * 16u + static_cast<uint32_t>(k & 7) * 2u;
 }
 
 // Shared-memory matrix descriptor: start address, leading (K) and stride (row
@@ -38,6 +45,13 @@ __device__ __forceinline__ uint64_t smem_desc(const void *start, uint32_t lbo, u
 // B, both K-major, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
     return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Instruction descriptor of a dense kind::f16 MMA with bf16 A and B: f32
+// accumulator, both operands K-major, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 
@@ -89,6 +103,31 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
+// D[M x N] (+)= A[M x K=16] * B[N x K=16]^T, bf16 inputs, f32 accumulate, A and B
+// in shared memory.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
+// The same with A read from tensor memory: A[M x 16] occupies lanes 0..M-1 and 8
+// consecutive 32-bit columns starting at a_tmem, two elements to a column (row m in
+// lane m; elements 2c and 2c + 1 in column c, 2c in the low half).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
         : "memory");
 }
@@ -172,6 +211,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+        "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -187,6 +234,26 @@ __device__ __forceinline__ float to_tf32(float x) {
 __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
     hi = to_tf32(x);
     lo = to_tf32(x - hi);
+}
+
+// Two fp32 values rounded to bf16 (nearest, ties to even) and packed in one 32-bit
+// word: `even` in the low half, `odd` in the high half (the order of K in an
+// operand word).
+__device__ __forceinline__ uint32_t pack_bf16x2(float even, float odd) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(odd), "f"(even));
+    return r;
+}
+
+// The split x = hi + lo of the 3xBF16 products, for a pair of values: hi = bf16(x)
+// and lo = bf16(x - hi), each pair packed as pack_bf16x2 packs it. hi is x rounded
+// to 8 significant bits, so x - hi (at most 2^-8 |x|) is exact in fp32, and hi + lo
+// is within 2^-16 |x| of x; hi*hi + hi*lo + lo*hi is then within about 3 * 2^-16 of
+// the exact product (against 2^-8 for one bf16 pass).
+__device__ __forceinline__ void split_bf16x2(float even, float odd, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf16x2(even, odd);
+    const float he = __uint_as_float(hi << 16), ho = __uint_as_float(hi & 0xFFFF0000u);
+    lo = pack_bf16x2(__fsub_rn(even, he), __fsub_rn(odd, ho));
 }
 
 }  // namespace tc

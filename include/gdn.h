@@ -189,8 +189,9 @@ gdn_status gdn_recurrence_scan_snapshots(float *state, const float *q, const flo
                                          int32_t *err_count, gdn_stream_t stream);
 
 /* The multi-token scan in chunks of 32 positions with the state-dependent
- * contractions on the tensor cores (tcgen05, TF32 operands split hi + lo so that
- * products keep fp32 accuracy, fp32 accumulation), for long prefill.
+ * contractions on the tensor cores (tcgen05: every fp32 operand split into bf16
+ * parts hi + lo and each product summed as hi*hi + hi*lo + lo*hi, within about
+ * 3 * 2^-16 of the exact product; fp32 accumulation), for long prefill.
  * fm_kernel_ssm.m (the softplus note and the sequential-scan section) refers to
  * a chunked prefill path built on cumulative sums of g within each chunk and
  * keeps the sequential scan as its permanent reference; the chunked algebra
