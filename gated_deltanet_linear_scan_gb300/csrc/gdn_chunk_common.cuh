@@ -143,13 +143,14 @@ __device__ __forceinline__ void split16_packed(const float (&x)[16], uint32_t (&
     for (int e = 0; e < 8; ++e) tc::split_bf16x2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
 }
 
-// The state split of a chunk, for columns c0 .. c0 + 63 of the tensor-memory lane at
-// trow (one thread's row of S^T): S -> packed (hi, lo), the A operand of the S
-// products, and the accumulator scaled to Gam_31 S, ready for the chunk's update; four
+// The state split of a chunk, for columns c0 .. c0 + NCOL - 1 of the tensor-memory lane
+// at trow (one thread's row of S^T): S -> packed (hi, lo), the A operand of the S
+// products, and the accumulator scaled to Gam_31 S, ready for the chunk's update; in
 // passes of 16 columns. Completes its stores (tcgen05.wait::st) before returning.
-__device__ __forceinline__ void split_state_row(uint32_t trow, int c0, float gn) {
+template <int NCOL>
+__device__ __forceinline__ void split_state_cols(uint32_t trow, int c0, float gn) {
 #pragma unroll 1
-    for (int h = 0; h < 4; ++h) {
+    for (int h = 0; h < NCOL / 16; ++h) {
         const uint32_t col = c0 + 16 * h;
         uint32_t r[16], hi[8], lo[8];
         tc::tmem_ld16_nowait(trow + kColSacc + col, r);
@@ -163,6 +164,10 @@ __device__ __forceinline__ void split_state_row(uint32_t trow, int c0, float gn)
         tc::tmem_st16(trow + kColSacc + col, r);
     }
     tc::tmem_st_wait();
+}
+
+__device__ __forceinline__ void split_state_row(uint32_t trow, int c0, float gn) {
+    split_state_cols<64>(trow, c0, gn);
 }
 
 // Partial Gram products of row t against columns s0 + 8 j, j < JN, over all of dk:

@@ -106,32 +106,31 @@ __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
     uint64_t *bar_kq = reinterpret_cast<uint64_t *>(smem + kPOffBar);
     uint64_t *bar_v = bar_kq + 1;  // [2]
 
-    // v rows of v-head rr into buffer rr & 1 (warp 0)
+    // v rows of v-head rr into buffer rr & 1 (warp 0): row r's 512 bytes in one warp
+    // instruction (16 bytes a lane), then each lane arrives once its copies land
     auto issue_v = [&](int rr) {
-        uint64_t *bar = bar_v + (rr & 1);
-        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(valid) * kS * 4);
-        __syncwarp();
-        if (lane < valid) {
-            const int vh = rr * Hk + kh;
-            bulk_g2s(smem + kPOffV + (rr & 1) * kVBytes + lane * kS * 4,
-                     v + ((row0 + lane) * H + vh) * kS, kS * 4, bar);
-        }
+        const int vh = rr * Hk + kh;
+#pragma unroll 1
+        for (int r = 0; r < valid; ++r)
+            cp_async16(smem + kPOffV + (rr & 1) * kVBytes + r * kS * 4 + 16 * lane,
+                       v + ((row0 + r) * H + vh) * kS + 4 * lane);
+        cp_async_arrive_noinc(bar_v + (rr & 1));
     };
     if (tid == 0) {
-        mbar_init(bar_kq, 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_v + 1, 1);
+        mbar_init(bar_kq, 32);  // one arrival per lane of warp 0
+        mbar_init(bar_v, 32);
+        mbar_init(bar_v + 1, 32);
         fence_mbar_init();
     }
     __syncthreads();
     if (warp == 0) {
-        if (lane == 0) mbar_arrive_expect_tx(bar_kq, 2u * valid * kS * 4);
-        __syncwarp();
-        if (lane < valid) {
-            const size_t row = (row0 + lane) * Hk + kh;
-            bulk_g2s(rk + lane * kRawRowF, k + row * kS, kS * 4, bar_kq);
-            bulk_g2s(rq + lane * kRawRowF, q + row * kS, kS * 4, bar_kq);
+#pragma unroll 1
+        for (int r = 0; r < valid; ++r) {
+            const size_t row = ((row0 + r) * Hk + kh) * kS + 4 * lane;
+            cp_async16(rk + r * kRawRowF + 4 * lane, k + row);
+            cp_async16(rq + r * kRawRowF + 4 * lane, q + row);
         }
+        cp_async_arrive_noinc(bar_kq);
         issue_v(0);
         if (ratio > 1) issue_v(1);
     }
@@ -490,7 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             }
             // S -> (hi, lo), the A operand of the S products; the accumulator becomes
             // Gam_31 S, ready for this chunk's update
-            split_state_row(trow, c0, gn);
+            // the first chunk's split is the state warps' alone; later ones are shared
+            // with the prep warps, which take columns c0 + 32 .. c0 + 63
+            split_state_cols<64>(trow, c0, gn);
             float yv[16];
             if (ci > 0) read_y(yv);
             st_signal(&bars.s_ready);
@@ -544,8 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             bool failed = false;
             if (pt == 0)
                 failed = !wait1(&bars.raw_full[cj & 1], cj >> 1, WD_STAGE_COPY) ||
-                         (cj > 1 && !wait1(&bars.buf_free[cj & 1], (cj >> 1) - 1, WD_MMA)) ||
-                         (cj > 0 && !wait1(&bars.a_done, cj - 1, WD_MMA));
+                         (cj > 1 && !wait1(&bars.buf_free[cj & 1], (cj >> 1) - 1, WD_MMA));
             return named_barrier_or(kPrepBarrier, kPrepThreads, failed || *abort_flag);
         };
         for (int ci = 0; ci < nw; ++ci) {
@@ -580,8 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
                 ld8(sw + c * kRawRowF + k0, x);
                 split8_store(x, wq + kOffWhi + o, wq + kOffWlo + o);
             }
-            for (int idx = pt; idx < kC * kS / 8; idx += kPrepThreads) {
-                const uint32_t o = idx * 16u;
+#pragma unroll
+            for (int j = 0; j < kWUnits; ++j) {
+                const uint32_t o = (pt + j * kPrepThreads) * 16u;
                 int t, k0;
                 image_unit(o, kSbo128, t, k0);
                 const float Gt = __shfl_sync(FULL_MASK, Gam, t);
@@ -600,9 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             }
             // w_c k_c and M, split, into buffer ci & 1
             unsigned char *kmb = smem + b * kKMBytes;
-            for (int u = pt; u < kS * kC / 8; u += kPrepThreads) {
+#pragma unroll
+            for (int j = 0; j < kWUnits; ++j) {
                 int d, cc;
-                wk_unit(u, d, cc);
+                wk_unit(pt + j * kPrepThreads, d, cc);
                 const uint32_t o = tc::kmajor_offset16(d, cc, kLbo, kSbo32);
                 float x[8];
 #pragma unroll
@@ -624,6 +626,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
                 mbar_arrive(&bars.img_ready[b]);
                 mbar_arrive(&bars.raw_empty[b]);  // done with this chunk's stage
             }
+            // this chunk's state split, columns c0 + 32 .. c0 + 63 of this warp's lane
+            // quarter, once the previous chunk's state update is done (the first chunk's
+            // split is the state warps' alone)
+
         }
     }
     tc::fence_before_sync();
