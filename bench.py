@@ -292,6 +292,92 @@ def timed_steps(torch, stream, gpu, dist, warmup, steps, before, launch):
     return [e0.elapsed_time(e1) for e0, e1 in ev], clocks.summary(), t_wall
 
 
+PIPELINE_NOTE = ("pipelined: step i + 1's inputs cross to the device on one copy stream and "
+                 "step i - 1's result back on another while step i computes (inputs and "
+                 "outputs double-buffered); every step's copies are inside the timed region; "
+                 "no L2 flush (the step's working set exceeds L2)")
+
+
+def pipelined_e2e(torch, dist, steps, h2d, compute, d2h, warmup=2, graph=False):
+    """End-to-end steps as a server runs them: h2d(i, b) copies step i's inputs from pinned
+    host memory into device buffer set b = i % 2 on a copy stream, compute(i, b) runs the
+    step on the current stream once they have landed, d2h(i, b) copies its result back on
+    a second copy stream. A buffer set is refilled only after the step that used it has
+    finished computing and its result has been copied out. Returns the seconds from the
+    first input copy to the last result copy of the `steps` timed steps (max over ranks),
+    after `warmup` untimed ones. With graph=True the same `steps` steps (the copies and the
+    library calls, in their stream order) are captured once in a CUDA graph and the graph
+    is replayed, once untimed and once timed: the device time without the host's per-call
+    overhead."""
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def enqueue(n, cur):
+        # streams switched with set_stream (a stream context costs the host several times
+        # more, and at decode rates the host's enqueue cost is what a step is waiting for)
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_done = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        for i in range(n):
+            b = i % 2
+            if i >= 2:
+                s_in.wait_event(ev_done[i - 2])  # step i - 2 no longer reads buffer b
+            torch.cuda.set_stream(s_in)
+            h2d(i, b)
+            torch.cuda.set_stream(cur)
+            ev_in[i].record(s_in)
+            cur.wait_event(ev_in[i])
+            if i >= 2:
+                cur.wait_event(ev_out[i - 2])  # step i - 2's result has left buffer b
+            compute(i, b)
+            ev_done[i].record(cur)
+            s_out.wait_event(ev_done[i])
+            torch.cuda.set_stream(s_out)
+            d2h(i, b)
+            torch.cuda.set_stream(cur)
+            ev_out[i].record(s_out)
+
+    cur = torch.cuda.current_stream()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            cap = torch.cuda.current_stream()
+            s_in.wait_stream(cap)
+            s_out.wait_stream(cap)
+            enqueue(steps, cap)
+            cap.wait_stream(s_in)
+            cap.wait_stream(s_out)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        start.record(cur)
+        g.replay()
+        end.record(cur)
+        torch.cuda.synchronize()
+        return reduce_max(start.elapsed_time(end) / 1e3, dist, "cuda")
+
+    def run(n, timed):
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        with torch.cuda.stream(s_in):
+            if timed:
+                gpu_head_start(torch)
+            start.record(s_in)
+        enqueue(n, cur)
+        with torch.cuda.stream(s_out):
+            end.record(s_out)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / 1e3
+
+    run(warmup, False)
+    return reduce_max(run(steps, True), dist, "cuda")
+
+
 # ------------------------------------------------------------------ ranks (weak scaling)
 
 def rank_work(cfg, rank):
@@ -573,18 +659,41 @@ def run_ours(args, cfg, rank, world, local_rank):
     h_out = torch.empty(N, H, S).pin_memory()
     h2d = sum(sizes) * 4
     d2h = h_out.numel() * 4
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    gpu_head_start(torch)
-    for i in range(args.steps):
-        flush()
-        e2e_ev[i][0].record(stream)
-        d_packed.copy_(h_packed[i % n_distinct], non_blocking=True)
-        launch(views, out)
-        h_out.copy_(out, non_blocking=True)
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
+    e2e_note, e2e_graph_s = None, None
+    if cfg.cid == 1:
+        # one sequence: its 2 MiB state fits in L2, so every step is flushed and its copies
+        # and launch run one after the other
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+        gpu_head_start(torch)
+        for i in range(args.steps):
+            flush()
+            e2e_ev[i][0].record(stream)
+            d_packed.copy_(h_packed[i % n_distinct], non_blocking=True)
+            launch(views, out)
+            h_out.copy_(out, non_blocking=True)
+            e2e_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
+        e2e_note = ("serial: each step's input copy, launch and result copy in turn on one "
+                    "stream, L2 flushed before every step")
+    else:
+        packed = [d_packed, torch.empty_like(d_packed)]
+        views2 = [views, {}]
+        off = 0
+        for key, sz in zip(keys, sizes):
+            views2[1][key] = packed[1][off:off + sz].view(d_steps[0][key].shape)
+            off += sz
+        outs = [out, torch.empty_like(out)]
+        h_outs = [h_out, torch.empty(N, H, S).pin_memory()]
+        e2e_fns = (lambda i, b: packed[b].copy_(h_packed[i % n_distinct], non_blocking=True),
+                   lambda i, b: launch(views2[b], outs[b]),
+                   lambda i, b: h_outs[b].copy_(outs[b], non_blocking=True))
+        e2e_s = pipelined_e2e(torch, dist, args.steps, *e2e_fns)
+        e2e_note = PIPELINE_NOTE
+        # the same pipelined steps captured once in a CUDA graph and replayed (how a server
+        # runs decode steps without the host's per-call cost, ~60 us of Python a step here)
+        e2e_graph_s = pipelined_e2e(torch, dist, args.steps, *e2e_fns, graph=True)
 
     # ---- one sequence: the serving form of the chain, a CUDA graph of 1000 consecutive
     # decode steps replayed as one unit (state and conv history carried, L2 warm: the
@@ -649,7 +758,11 @@ def run_ours(args, cfg, rank, world, local_rank):
                      "peak_source": f"hbm_gbs ({pk_kind})"},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "timing": e2e_note,
+                "graph_replay": None if e2e_graph_s is None else {
+                    "value": tokens / e2e_graph_s, "unit": "tokens/s",
+                    "timing": "the same pipelined steps captured once in a CUDA graph and "
+                              "replayed (first input copy to last result copy)"}},
         "gpu_launches": args.steps,
         "clocks": clk,
     }
@@ -674,13 +787,15 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     if chunked:
         ws = torch.empty(gdn.gdn_recurrence_scan_chunked_ws_size(N, T, H, S) // 4, device="cuda")
 
-    def launch():
+    def launch(dd=None, yy=None):
+        dd = d if dd is None else dd
+        yy = y if yy is None else yy
         if chunked:
-            gdn.gdn_recurrence_scan_chunked_ws(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y,
-                                               N, T, Hk, H, S, cfg.scale, ws)
+            gdn.gdn_recurrence_scan_chunked_ws(state, dd["q"], dd["k"], dd["v"], dd["g"],
+                                               dd["beta"], yy, N, T, Hk, H, S, cfg.scale, ws)
         else:
-            gdn.gdn_recurrence_scan(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y, N, T,
-                                    Hk, H, S, cfg.scale)
+            gdn.gdn_recurrence_scan(state, dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], yy,
+                                    N, T, Hk, H, S, cfg.scale)
 
     def before(i):
         state.copy_(state0)
@@ -693,26 +808,26 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     per = total_s / args.steps
     tokens = world * N * T * args.steps
 
-    # ---- end to end: q, k, v, g, beta from pinned host memory, the call, y back.
+    # ---- end to end: q, k, v, g, beta from pinned host memory, the call (the state reset
+    # first), y back; pipelined over double buffers
     keys = ["q", "k", "v", "g", "beta"]
     h_in = {key: torch.from_numpy(np.ascontiguousarray(x[key])).pin_memory() for key in keys}
-    h_y = torch.empty(N, T, H, S).pin_memory()
+    h_y = [torch.empty(N, T, H, S).pin_memory() for _ in range(2)]
     h2d = sum(h_in[key].numel() for key in keys) * 4
-    d2h = h_y.numel() * 4
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    gpu_head_start(torch)
-    for i in range(args.steps):
-        state.copy_(state0)
-        flush()
-        e2e_ev[i][0].record(stream)
+    d2h = h_y[0].numel() * 4
+    d_in = [{key: d[key] for key in keys}, {key: torch.empty_like(d[key]) for key in keys}]
+    ys = [y, torch.empty_like(y)]
+
+    def e2e_in(i, b):
         for key in keys:
-            d[key].copy_(h_in[key], non_blocking=True)
-        launch()
-        h_y.copy_(y, non_blocking=True)
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
+            d_in[b][key].copy_(h_in[key], non_blocking=True)
+
+    def e2e_step(i, b):
+        state.copy_(state0)
+        launch(d_in[b], ys[b])
+
+    e2e_s = pipelined_e2e(torch, dist, args.steps, e2e_in, e2e_step,
+                          lambda i, b: h_y[b].copy_(ys[b], non_blocking=True))
     flops = 7.0 * N * T * H * S * S
     props = torch.cuda.get_device_properties(0)
     mhz = clk["sm_mhz"] or pk.get("sm_max_mhz", 2070.0)
@@ -782,7 +897,7 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "timing": PIPELINE_NOTE},
         "gpu_launches": (2 if chunked else 1) * args.steps,
         "clocks": clk,
     }
@@ -807,9 +922,11 @@ def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     y = torch.empty(N, T, H, S, device="cuda")
     snaps = torch.empty(N, T, H, S, S, device="cuda")
 
-    def launch():
-        gdn.gdn_recurrence_scan_snapshots(state, d["q"], d["k"], d["v"], d["g"], d["beta"], y,
-                                          snaps, N, T, Hk, H, S, cfg.scale)
+    def launch(dd=None, yy=None):
+        dd = d if dd is None else dd
+        yy = y if yy is None else yy
+        gdn.gdn_recurrence_scan_snapshots(state, dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"],
+                                          yy, snaps, N, T, Hk, H, S, cfg.scale)
 
     def before(i):
         state.copy_(state0)
@@ -846,27 +963,27 @@ def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     restore = {"kernel": "gdn_snapshot_restore", "us_per_call": 1e6 * rs_s,
                "hbm_gbs": rs_bytes / rs_s / 1e9, "hbm_frac_of_peak": rs_bytes / rs_s / 1e9 / pk["hbm_gbs"]}
 
-    # ---- end to end: q, k, v, g, beta from pinned host memory, the call, y back (the
-    # snapshots stay on the device, where a rollback reads them)
+    # ---- end to end: q, k, v, g, beta from pinned host memory, the call (the state reset
+    # first), y back (the snapshots stay on the device, where a rollback reads them);
+    # pipelined over double buffers
     keys = ["q", "k", "v", "g", "beta"]
     h_in = {key: torch.from_numpy(np.ascontiguousarray(x[key])).pin_memory() for key in keys}
-    h_y = torch.empty(N, T, H, S).pin_memory()
+    h_y = [torch.empty(N, T, H, S).pin_memory() for _ in range(2)]
     h2d = sum(h_in[key].numel() for key in keys) * 4
-    d2h = h_y.numel() * 4
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    gpu_head_start(torch)
-    for i in range(args.steps):
-        state.copy_(state0)
-        flush()
-        e2e_ev[i][0].record(stream)
+    d2h = h_y[0].numel() * 4
+    d_in = [{key: d[key] for key in keys}, {key: torch.empty_like(d[key]) for key in keys}]
+    ys = [y, torch.empty_like(y)]
+
+    def e2e_in(i, b):
         for key in keys:
-            d[key].copy_(h_in[key], non_blocking=True)
-        launch()
-        h_y.copy_(y, non_blocking=True)
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
+            d_in[b][key].copy_(h_in[key], non_blocking=True)
+
+    def e2e_step(i, b):
+        state.copy_(state0)
+        launch(d_in[b], ys[b])
+
+    e2e_s = pipelined_e2e(torch, dist, args.steps, e2e_in, e2e_step,
+                          lambda i, b: h_y[b].copy_(ys[b], non_blocking=True))
     if rank != 0:
         return 0
     cpu = None
@@ -893,7 +1010,7 @@ def run_ours_spec(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                      "peak_source": f"hbm_gbs ({pk_kind})"},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "timing": PIPELINE_NOTE},
         "gpu_launches": args.steps,
         "clocks": clk,
     }
@@ -918,10 +1035,12 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     ws = torch.empty(gdn.gdn_block_prefill_chunked_workspace_size(N, T, Hk, H, S) // 4 + 64,
                      device="cuda")
 
-    def launch():
-        gdn.gdn_block_prefill_chunked(d["qkv"], st["conv_w"], conv, d["alpha"], d["b"], st["dt"],
-                                      st["a"], d["z"], st["norm_w"], state, out, N, T, Hk, H, S,
-                                      cfg.conv_kernel, cfg.scale, cfg.eps, cfg.eps, ws)
+    def launch(dd=None, oo=None):
+        dd = d if dd is None else dd
+        oo = out if oo is None else oo
+        gdn.gdn_block_prefill_chunked(dd["qkv"], st["conv_w"], conv, dd["alpha"], dd["b"],
+                                      st["dt"], st["a"], dd["z"], st["norm_w"], state, oo, N, T,
+                                      Hk, H, S, cfg.conv_kernel, cfg.scale, cfg.eps, cfg.eps, ws)
 
     def reset():
         state.copy_(state0)
@@ -962,26 +1081,26 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     adv_s = reduce_max(adv_s, dist, "cuda")
     del scan_ws
 
-    # ---- end to end: qkv, alpha, b, z from pinned host memory, the call, out back.
+    # ---- end to end: qkv, alpha, b, z from pinned host memory, the call (state and conv
+    # history reset first), out back; pipelined over double buffers
     keys = ["qkv", "alpha", "b", "z"]
     h_in = {key: d[key].cpu().pin_memory() for key in keys}
-    h_out = torch.empty(N, T, H, S).pin_memory()
+    h_out = [torch.empty(N, T, H, S).pin_memory() for _ in range(2)]
     h2d = sum(h_in[key].numel() for key in keys) * 4
-    d2h = h_out.numel() * 4
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    gpu_head_start(torch)
-    for i in range(args.steps):
-        reset()
-        flush()
-        e2e_ev[i][0].record(stream)
+    d2h = h_out[0].numel() * 4
+    d_in = [{key: d[key] for key in keys}, {key: torch.empty_like(d[key]) for key in keys}]
+    outs = [out, torch.empty_like(out)]
+
+    def e2e_in(i, b):
         for key in keys:
-            d[key].copy_(h_in[key], non_blocking=True)
-        launch()
-        h_out.copy_(out, non_blocking=True)
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev) / 1e3, dist, "cuda")
+            d_in[b][key].copy_(h_in[key], non_blocking=True)
+
+    def e2e_step(i, b):
+        reset()
+        launch(d_in[b], outs[b])
+
+    e2e_s = pipelined_e2e(torch, dist, args.steps, e2e_in, e2e_step,
+                          lambda i, b: h_out[b].copy_(outs[b], non_blocking=True))
 
     flops = 7.0 * N * T * H * S * S
     mf = chunked_method_flops(N * ((T + 31) // 32), H)
@@ -1021,7 +1140,7 @@ def run_ours_prefill(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                      "peak_source": f"bf16_tflops ({pk_kind})"},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "timing": PIPELINE_NOTE},
         "gpu_launches": 6 * args.steps, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -1053,11 +1172,14 @@ def run_ours_varlen(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     ws = torch.empty(gdn.gdn_block_prefill_chunked_varlen_workspace_size(N, total, Hk, H, S) // 4
                      + 64, device="cuda")
 
-    def launch():
-        gdn.gdn_block_prefill_chunked_varlen(d["qkv"], st["conv_w"], conv, d["alpha"], d["b"],
-                                             st["dt"], st["a"], d["z"], st["norm_w"], state, out,
-                                             d_cu, N, total, maxt, Hk, H, S, K, cfg.scale,
-                                             cfg.eps, cfg.eps, ws)
+    def launch(dd=None, oo=None, cu_d=None):
+        dd = d if dd is None else dd
+        oo = out if oo is None else oo
+        cu_d = d_cu if cu_d is None else cu_d
+        gdn.gdn_block_prefill_chunked_varlen(dd["qkv"], st["conv_w"], conv, dd["alpha"],
+                                             dd["b"], st["dt"], st["a"], dd["z"], st["norm_w"],
+                                             state, oo, cu_d, N, total, maxt, Hk, H, S, K,
+                                             cfg.scale, cfg.eps, cfg.eps, ws)
 
     def before(i):
         state.copy_(state0)
@@ -1091,25 +1213,30 @@ def run_ours_varlen(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
     mflops = chunked_method_flops(n_chunks, H)
     bf16_peak = pk.get("bf16_tflops", 1900.0)
 
-    # ---- end to end: qkv, alpha, b, z and cu_seqlens from pinned host memory, the call,
-    # out back
+    # ---- end to end: qkv, alpha, b, z and cu_seqlens from pinned host memory, the call
+    # (state and conv history reset first), out back; pipelined over double buffers
     keys = ["qkv", "alpha", "b", "z"]
     h_in = {key: d[key].cpu().pin_memory() for key in keys}
     h_cu = torch.from_numpy(cu).pin_memory()
-    h_out = torch.empty(total, H, S).pin_memory()
+    h_out = [torch.empty(total, H, S).pin_memory() for _ in range(2)]
     h2d = sum(h_in[key].numel() for key in keys) * 4 + h_cu.numel() * 4
-    d2h = h_out.numel() * 4
+    d2h = h_out[0].numel() * 4
+    d_in = [{key: d[key] for key in keys}, {key: torch.empty_like(d[key]) for key in keys}]
+    cus = [d_cu, torch.empty_like(d_cu)]
+    outs = [out, torch.empty_like(out)]
 
-    def e2e_launch(i):
+    def e2e_in(i, b):
         for key in keys:
-            d[key].copy_(h_in[key], non_blocking=True)
-        d_cu.copy_(h_cu, non_blocking=True)
-        launch()
-        h_out.copy_(out, non_blocking=True)
+            d_in[b][key].copy_(h_in[key], non_blocking=True)
+        cus[b].copy_(h_cu, non_blocking=True)
 
-    e2e_ms, _, _ = timed_steps(torch, stream, torch.cuda.current_device(), dist, 3, args.steps,
-                               before, e2e_launch)
-    e2e_s = reduce_max(sum(e2e_ms) / 1e3, dist, "cuda")
+    def e2e_step(i, b):
+        state.copy_(state0)
+        conv.copy_(conv0)
+        launch(d_in[b], outs[b], cus[b])
+
+    e2e_s = pipelined_e2e(torch, dist, args.steps, e2e_in, e2e_step,
+                          lambda i, b: h_out[b].copy_(outs[b], non_blocking=True))
     if rank != 0:
         return 0
     cpu = None
@@ -1145,7 +1272,7 @@ def run_ours_varlen(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                      "peak_source": f"bf16_tflops ({pk_kind})"},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "timing": PIPELINE_NOTE},
         "gpu_launches": 6 * args.steps, "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -129,10 +129,28 @@ def library():
 
 # ------------------------------------------------------------------ marshalling helpers
 
+_TORCH = None
+
+
+def _torch():
+    """torch, imported on first use (the package itself imports without it)."""
+    global _TORCH
+    if _TORCH is None:
+        import torch
+        _TORCH = torch
+    return _TORCH
+
+
 def _stream(stream):
+    """The stream argument of a call: the caller's, else torch's current stream (read
+    through the raw-stream accessor when this torch has it: a tenth of the cost of building
+    a Stream object, which matters at decode-step rates)."""
     if stream is not None:
         return int(stream)
-    import torch
+    torch = _torch()
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch.cuda.current_device())
     return torch.cuda.current_stream().cuda_stream
 
 
@@ -141,7 +159,7 @@ def _ptr(t, name, dtype=None, optional=False):
         if optional:
             return None
         raise ValueError(f"{name} is required")
-    import torch
+    torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch tensor")
     if not t.is_cuda:
@@ -155,17 +173,15 @@ def _ptr(t, name, dtype=None, optional=False):
 
 
 def _slots(slots):
-    import torch
-    return _ptr(slots, "slots", torch.int32, optional=True)
+    return None if slots is None else _ptr(slots, "slots", _torch().int32)
 
 
 def _errc(err_count):
-    import torch
-    return _ptr(err_count, "err_count", torch.int32, optional=True)
+    return None if err_count is None else _ptr(err_count, "err_count", _torch().int32)
 
 
 def _ws_check(workspace):
-    import torch
+    torch = _torch()
     if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
 
