@@ -64,7 +64,8 @@ constexpr int kAtRow = kC + 4;                         // A^T rows: 36 floats, f
 constexpr uint32_t kAtBytes = kC * kAtRow * 4, kMBytes = kC * kC * 4;
 constexpr uint32_t kOffA = kOffRaw + 2 * kRawBuf;      // 2 x A^T [32][36] (At[s][t] = A[t][s])
 constexpr uint32_t kOffM = kOffA + 2 * kAtBytes;       // 2 x M [32][32] (until emitted)
-constexpr uint32_t kOffBars = kOffM + 2 * kMBytes;
+constexpr uint32_t kOffScale = kOffM + 2 * kMBytes;  // beta Gam[32], beta[32] of a chunk
+constexpr uint32_t kOffBars = kOffScale + 2 * kC * 4;
 
 struct Bars {
     uint64_t raw_full[2], raw_empty[2], gram_ready[2];
@@ -454,12 +455,31 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_scan_kernel(
             // row below it), so the dependent chain is 32 steps long, not 496. Ut goes
             // straight to its buffer, so first wait until the previous chunk is done with
             // it (its U is formed, which also means its W S product is done).
+            // the per-position scale factors, written by one warp before the wait below
+            // (whose barrier publishes them; the previous chunk's readers are long done)
+            float *sc = reinterpret_cast<float *>(smem + kOffScale);
+            if (pt < 32) {
+                sc[lane] = bet * Gam;
+                sc[kC + lane] = bet;
+            }
             if (ci > 0 ? prep_wait(&bars.u_ready, ci - 1, WD_MMA) : prep_sync()) break;
+            {
+                const float *scp = sc + (is_w ? 0 : kC);  // warp-uniform choice
 #pragma unroll
-            for (int t = 0; t < kC; ++t) {
-                const float bt = __shfl_sync(FULL_MASK, bet, t);
-                const float Gt = __shfl_sync(FULL_MASK, Gam, t);
-                x[t] = is_w ? bt * Gt * rk[t * kRawRowF + col] : bt * x[t];
+                for (int t = 0; t < kC; t += 4) {
+                    const float4 f = ld4(scp + t);
+                    if (is_w) {
+                        x[t] = f.x * rk[t * kRawRowF + col];
+                        x[t + 1] = f.y * rk[(t + 1) * kRawRowF + col];
+                        x[t + 2] = f.z * rk[(t + 2) * kRawRowF + col];
+                        x[t + 3] = f.w * rk[(t + 3) * kRawRowF + col];
+                    } else {
+                        x[t] = f.x * x[t];
+                        x[t + 1] = f.y * x[t + 1];
+                        x[t + 2] = f.z * x[t + 2];
+                        x[t + 3] = f.w * x[t + 3];
+                    }
+                }
             }
 #pragma unroll
             for (int s2 = 0; s2 < kC - 1; ++s2) {

@@ -64,7 +64,8 @@ constexpr uint32_t kVBytes = kC * kS * 4;  // the v rows of one v-head, unpadded
 // shared memory: k and q rows (padded), the v rows of two v-heads, A^T, 3 mbarriers
 constexpr uint32_t kPOffK = 0, kPOffQ = kRawArr, kPOffV = 2 * kRawArr;
 constexpr uint32_t kPOffAt = kPOffV + 2 * kVBytes, kPOffBar = kPOffAt + kAtBytes;
-constexpr size_t kPSmemBytes = kPOffBar + 3 * sizeof(uint64_t);  // 71,296 B: 3 CTAs per SM
+constexpr uint32_t kPOffScale = kPOffBar + 4 * sizeof(uint64_t);  // beta Gam[32], beta[32]
+constexpr size_t kPSmemBytes = kPOffScale + 2 * kC * sizeof(float);
 static_assert(kPOffBar % 8 == 0, "mbarrier alignment");
 
 // grid = n_wave_chunks * n_seqs * n_k_heads; CTA (cw, n, kh) prepares chunk c_begin + cw of
@@ -172,7 +173,13 @@ __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
                 blk[kBlkM + t * kC + s] = e * qk[j];
             }
         }
-        __syncthreads();  // A^T of this v-head is complete
+        // the substitution's per-position scale factors, one warp writing them
+        float *sc = reinterpret_cast<float *>(smem + kPOffScale);
+        if (warp == 0) {
+            sc[lane] = bl * Gam;
+            sc[kC + lane] = bl;
+        }
+        __syncthreads();  // A^T of this v-head is complete, and the scale factors
 
         // forward substitution, one column per thread: W (threads 0..127), Ut (128..255),
         // column-wise (x_s is final once the rows above are, then updates every row below)
@@ -186,11 +193,16 @@ __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
 #pragma unroll
             for (int p = 0; p < kC; ++p) x[p] = p < valid ? rv[p * kS + col] : 0.f;
         }
+        {
+            const float *scp = sc + (is_w ? 0 : kC);  // warp-uniform choice
 #pragma unroll
-        for (int p = 0; p < kC; ++p) {
-            const float bt = __shfl_sync(FULL_MASK, bl, p);
-            const float Gt = __shfl_sync(FULL_MASK, Gam, p);
-            x[p] = is_w ? bt * Gt * x[p] : bt * x[p];
+            for (int p = 0; p < kC; p += 4) {
+                const float4 f = ld4(scp + p);
+                x[p] = f.x * x[p];
+                x[p + 1] = f.y * x[p + 1];
+                x[p + 2] = f.z * x[p + 2];
+                x[p + 3] = f.w * x[p + 3];
+            }
         }
 #pragma unroll
         for (int s2 = 0; s2 < kC - 1; ++s2) {
@@ -233,7 +245,8 @@ constexpr int kMRowF = kC + 4;                      // M rows in a stage: 36 flo
 constexpr uint32_t kStW = 2 * kRawArr, kStM = 3 * kRawArr;  // within a stage
 constexpr uint32_t kRawBuf = kStM + kC * kMRowF * 4;        // one stage: 55,296 bytes
 constexpr uint32_t kOffRaw = kOffWQ1 + kWQBytes;
-constexpr uint32_t kOffBars = kOffRaw + 2 * kRawBuf;
+constexpr uint32_t kOffPTab = kOffRaw + 2 * kRawBuf;  // Gam[32], w_c[32] of the prep's chunk
+constexpr uint32_t kOffBars = kOffPTab + 2 * kC * 4;
 static_assert(kOffKM1 == kOffKhi + kKMBytes, "second w K | M buffer follows the first");
 static_assert(kOffWQ1 % 1024 == 0 && kOffRaw % 16 == 0, "buffer alignment");
 
@@ -555,18 +568,26 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             const float *rq = rk + kC * kRawRowF;
             const float *sw = reinterpret_cast<const float *>(smem + kOffRaw + b * kRawBuf + kStW);
             const float *sm = reinterpret_cast<const float *>(smem + kOffRaw + b * kRawBuf + kStM);
-            float last;
-            const float gam = chunk_gam_from(g_next, lane, last);
-            const float Gam = expf(gam), wdec = expf(last - gam);
-            g_next = 0.f;
-            if (ci + 1 < nw && chunk_t0(ci + 1) + lane < n_tokens)
-                g_next = g[(row0 + chunk_t0(ci + 1) + lane) * H + vh];
             // 8 fp32 values from p, one 16-byte image unit (8 bf16) of a part
             auto ld8 = [](const float *p, float (&x)[8]) {
                 const float4 a = ld4(p), b4 = ld4(p + 4);
                 x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
                 x[4] = b4.x; x[5] = b4.y; x[6] = b4.z; x[7] = b4.w;
             };
+            // the chunk's Gam_t and w_t for the image units: the first prep warp forms them
+            // (lane = position) and writes them before the wait below, whose barrier
+            // publishes them (the previous chunk's readers are past the barrier that ended
+            // their iteration)
+            float *tab = reinterpret_cast<float *>(smem + kOffPTab);
+            if (pt < 32) {
+                float last;
+                const float gam = chunk_gam_from(g_next, lane, last);
+                tab[lane] = expf(gam);
+                tab[kC + lane] = expf(last - gam);
+                g_next = 0.f;
+                if (ci + 1 < nw && chunk_t0(ci + 1) + lane < n_tokens)
+                    g_next = g[(row0 + chunk_t0(ci + 1) + lane) * H + vh];
+            }
             if (prep_wait_chunk(ci)) break;
             // W and Gam_t q_t, split (rows past the end of the sequence count as zero), into
             // image buffer ci & 1
@@ -585,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
                 const uint32_t o = (pt + j * kPrepThreads) * 16u;
                 int t, k0;
                 image_unit(o, kSbo128, t, k0);
-                const float Gt = __shfl_sync(FULL_MASK, Gam, t);
+                const float Gt = tab[t];
                 float x[8];
                 if (t < valid) {
                     const float4 a = ld4(rq + t * kRawRowF + k0), b4 = ld4(rq + t * kRawRowF + k0 + 4);
@@ -606,11 +627,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
                 int d, cc;
                 wk_unit(pt + j * kPrepThreads, d, cc);
                 const uint32_t o = tc::kmajor_offset16(d, cc, kLbo, kSbo32);
-                float x[8];
+                float x[8], wd[8];
+                ld8(tab + kC + cc, wd);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    x[j] = __shfl_sync(FULL_MASK, wdec, cc + j) *
-                           (cc + j < valid ? rk[(cc + j) * kRawRowF + d] : 0.f);
+                    x[j] = wd[j] * (cc + j < valid ? rk[(cc + j) * kRawRowF + d] : 0.f);
                 split8_store(x, kmb + kOffKhi + o, kmb + kOffKlo + o);
             }
             if (pt < kMUnits) {
