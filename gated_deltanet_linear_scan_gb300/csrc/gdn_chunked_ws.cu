@@ -69,9 +69,9 @@ constexpr size_t kPSmemBytes = kPOffScale + 2 * kC * sizeof(float);
 static_assert(kPOffBar % 8 == 0, "mbarrier alignment");
 
 // grid = n_wave_chunks * n_seqs * n_k_heads; CTA (cw, n, kh) prepares chunk c_begin + cw of
-// sequence n for the v-heads rr * Hk + kh. Warp 0 bulk-copies the chunk's k and q rows
-// and the v rows of the first two v-heads at the start (the v rows of v-head rr + 2
-// into the buffer of rr once rr is done), so a CTA waits on memory about once.
+// sequence n for the v-heads rr * Hk + kh. Warp 0 moves the chunk's k and q rows and the
+// v rows of the first two v-heads by 16-byte cp.async at the start (the v rows of v-head
+// rr + 2 into the buffer of rr once rr is done), so a CTA waits on memory about once.
 __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
     const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
     const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ ws,
