@@ -25,6 +25,7 @@ __all__ = [
     "gdn_block_prefill_noalloc", "PREFILL_NOALLOC_SCRATCH_BYTES",
     "gdn_recurrence_scan_chunked", "gdn_block_prefill_chunked",
     "gdn_recurrence_scan_chunked_ws_size", "gdn_recurrence_scan_chunked_ws",
+    "gdn_chunked_snapshot_count", "gdn_recurrence_scan_chunked_snapshots",
     "gdn_chunked_prepare", "gdn_chunked_advance", "gdn_block_prefill_chunked_workspace_size",
     "gdn_recurrence_scan_varlen", "gdn_recurrence_scan_chunked_varlen_ws_size",
     "gdn_recurrence_scan_chunked_varlen", "gdn_block_prefill_varlen_workspace_size",
@@ -77,6 +78,9 @@ _SIGS = {
     "gdn_recurrence_scan_chunked_ws_size": ([_I, _I, _I, _I], ctypes.c_size_t),
     "gdn_recurrence_scan_chunked_ws": ([_P] * 7 + [_I, _I, _I, _I, _I, _F, _P, _I, _P, _P,
                                                    ctypes.c_size_t, _P], _I),
+    "gdn_chunked_snapshot_count": ([_I, _I], _I),
+    "gdn_recurrence_scan_chunked_snapshots": ([_P] * 8 + [_I] * 6 + [_F, _P, _I, _P, _P,
+                                                                  ctypes.c_size_t, _P], _I),
     "gdn_chunked_prepare": ([_P] * 5 + [_P, ctypes.c_size_t] + [_I] * 7 + [_P], _I),
     "gdn_chunked_advance": ([_P] * 5 + [ctypes.c_size_t, _P] + [_I] * 5 + [_F, _I, _I, _P, _I,
                                                                           _P, _P], _I),
@@ -309,6 +313,26 @@ def gdn_recurrence_scan_chunked_ws(state, q, k, v, g, beta, y, n_seqs, n_tokens,
         _ptr(beta, "beta"), _ptr(y, "y"), n_seqs, n_tokens, n_k_heads, n_v_heads, state_size,
         scale, _slots(slots), pool, _errc(err_count), _ws_ptr(workspace),
         _ws_bytes(workspace), _stream(stream)))
+
+
+def gdn_chunked_snapshot_count(n_tokens, snap_every):
+    return library().gdn_chunked_snapshot_count(n_tokens, snap_every)
+
+
+def gdn_recurrence_scan_chunked_snapshots(state, q, k, v, g, beta, y, snaps, snap_every, n_seqs,
+                                          n_tokens, n_k_heads, n_v_heads, state_size, scale,
+                                          workspace, slots=None, pool=None, err_count=None,
+                                          stream=None):
+    """The two-phase chunked scan, also writing the state every 32 * snap_every positions
+    into snaps [n_seqs][n_snaps][H][S][S]; snaps may be None when n_snaps is 0."""
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_recurrence_scan_chunked_snapshots",
+           library().gdn_recurrence_scan_chunked_snapshots(
+               _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
+               _ptr(beta, "beta"), _ptr(y, "y"), _ptr(snaps, "snaps", optional=True),
+               snap_every, n_seqs, n_tokens, n_k_heads, n_v_heads, state_size, scale,
+               _slots(slots), pool, _errc(err_count), _ws_ptr(workspace), _ws_bytes(workspace),
+               _stream(stream)))
 
 
 def gdn_chunked_prepare(q, k, v, g, beta, workspace, n_seqs, n_tokens, n_k_heads, n_v_heads,

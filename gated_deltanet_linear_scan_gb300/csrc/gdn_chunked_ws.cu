@@ -272,15 +272,75 @@ constexpr int kPrepBarrier = 1, kStateBarrier = 2;
 constexpr int kWUnits = kC * kS / 8 / kPrepThreads, kMUnits = kC * kC / 8;
 static_assert(kWUnits * kPrepThreads * 8 == kC * kS && kMUnits <= kPrepThreads, "unit split");
 
+// 8 words r[o ..] to p, one 256-bit store; p 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(float *p, const uint32_t (&r)[16], int o) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "r"(r[o]), "r"(r[o + 1]), "r"(r[o + 2]), "r"(r[o + 3]),
+                    "r"(r[o + 4]), "r"(r[o + 5]), "r"(r[o + 6]), "r"(r[o + 7])
+                 : "memory");
+}
+
+// Columns c0 .. c0 + 63 of the state accumulator's lane at trow (one thread's row of S^T,
+// fp32) to dst[c0 ..], 16-byte aligned, in passes of 16 columns. A warp's lanes hold 32
+// rows 512 bytes apart, so each store instruction touches 32 lines: 256-bit stores
+// (where dst is 32-byte aligned) halve the instructions and requests of 128-bit ones.
+__device__ __forceinline__ void copy_state_row(uint32_t trow, int c0, float *dst) {
+    const bool wide = (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t r[16];
+        tc::tmem_ld16_nowait(trow + kColSacc + c0 + 16 * blk, r);
+        tc::tmem_ld_wait();
+        float *d = dst + c0 + 16 * blk;
+        if (wide) {
+            st_global_v8(d, r, 0);
+            st_global_v8(d + 8, r, 8);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4 *>(d + e) =
+                    make_float4(u2f(r[e]), u2f(r[e + 1]), u2f(r[e + 2]), u2f(r[e + 3]));
+        }
+    }
+}
+
+// State snapshots of a uniform batch: every `every` chunks, the state after the chunk
+// that ends there. Snapshot j of sequence n is the state after position
+// (j + 1) * every * kC - 1, at p + (n * count + j) * H * kS * kS, laid out as one state
+// slot. p == nullptr: none.
+struct SnapOut {
+    float *p;
+    int every, count;
+
+    // the first chunk, from chunk cb on, that a snapshot precedes (a positive multiple
+    // of every)
+    __device__ __forceinline__ int first(int cb) const {
+        const int m = (cb + every - 1) / every;
+        return (m > 1 ? m : 1) * every;
+    }
+    // the row dv of v-head vh of the snapshot that precedes chunk cg (a positive multiple
+    // of every), or nullptr past the last one
+    __device__ __forceinline__ float *row(int cg, int n, int vh, int H, int dv) const {
+        const int j = cg / every - 1;
+        if (j >= count) return nullptr;
+        return p + ((static_cast<size_t>(n) * count + j) * H + vh) * (kS * kS) +
+               static_cast<size_t>(dv) * kS;
+    }
+};
+
 // One CTA per (sequence, v-head); grid = n_seqs * n_v_heads. Advances the state over
 // chunks c_begin .. c_begin + n_wave_chunks - 1, whose workspace blocks are prepared.
+// kSnap (uniform batches, snap.p set): it also writes the snapshots that fall in them;
+// a separate instantiation, so that the plain form keeps its registers.
 // Roles as in the one-kernel form: producer (k, q rows), MMA issuer, state warps (the
 // split of S, U = Ut - D_u, y, no Gram stage), prep warps (operand images only).
+template <bool kSnap>
 __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
     float *__restrict__ state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ g, const float *__restrict__ ws, float *__restrict__ y,
     int n_seqs, const SeqMap seqs, int n_k_heads, int n_v_heads, int c_begin, int n_wave_chunks,
-    float scale, const int32_t *__restrict__ slots, int pool, int32_t *err_count) {
+    float scale, const int32_t *__restrict__ slots, int pool, int32_t *err_count,
+    const SnapOut snap) {
     extern __shared__ __align__(16) unsigned char smem[];
     Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBars);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -482,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
         float g_cur = 0.f;  // log-decays of chunk ci, lane = position
         if (chunk_t0(0) + lane < n_tokens) g_cur = g[(row0 + chunk_t0(0) + lane) * H + vh];
         bool ok = true;
+        int snap_cg = kSnap ? snap.first(c_begin) : 0;  // the next chunk a snapshot precedes
         for (int ci = 0; ci < nw && ok; ++ci) {
             // this chunk's Ut (dv = this thread's lane of tensor memory, positions u0..)
             float utv[16];
@@ -500,10 +561,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
                 if (!(ok = st_wait(&bars.b_done, ci - 1))) break;
                 tc::fence_after_sync();
             }
+            // S here is the state after the previous chunk: a snapshot when that chunk
+            // ends a snapshot interval
+            if (kSnap && c_begin + ci == snap_cg) {
+                if (float *row = snap.row(snap_cg, n, vh, H, dv)) copy_state_row(trow, c0, row);
+                snap_cg += snap.every;
+            }
             // S -> (hi, lo), the A operand of the S products; the accumulator becomes
             // Gam_31 S, ready for this chunk's update
-            // the first chunk's split is the state warps' alone; later ones are shared
-            // with the prep warps, which take columns c0 + 32 .. c0 + 63
             split_state_cols<64>(trow, c0, gn);
             float yv[16];
             if (ci > 0) read_y(yv);
@@ -535,15 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             float yv[16];
             read_y(yv);
             write_y(nw - 1, yv);
-#pragma unroll 1
-            for (int blk = 0; blk < 4; ++blk) {
-                uint32_t r[16];
-                tc::tmem_ld16_nowait(trow + kColSacc + c0 + 16 * blk, r);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; e += 4)
-                    *reinterpret_cast<float4 *>(srow + c0 + 16 * blk + e) =
-                        make_float4(u2f(r[e]), u2f(r[e + 1]), u2f(r[e + 2]), u2f(r[e + 3]));
+            copy_state_row(trow, c0, srow);
+            // the final state is the last snapshot too when the sequence ends on one
+            if (kSnap && c_begin + nw == snap_cg && snap_cg * kC == n_tokens) {
+                if (float *row = snap.row(snap_cg, n, vh, H, dv)) copy_state_row(trow, c0, row);
             }
         }
     } else {
@@ -705,15 +765,17 @@ gdn_status launch_prepare(const float *q, const float *k, const float *v, const 
 gdn_status launch_advance(float *state, const float *q, const float *k, const float *g,
                           const float *ws, float *y, int n_seqs, SeqMap seqs, int n_k_heads,
                           int n_v_heads, float scale, int cb, int nc, const int32_t *slots,
-                          int pool, int32_t *err_count, cudaStream_t s) {
+                          int pool, int32_t *err_count, cudaStream_t s,
+                          SnapOut snap = SnapOut{nullptr, 1, 0}) {
     // per launch: the attribute belongs to the current device
-    if (cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto *kernel = snap.p ? chunk_state_kernel<true> : chunk_state_kernel<false>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess)
         return GDN_ERR_LAUNCH;
     // slot errors are counted once, with the first chunk
-    chunk_state_kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, s>>>(
+    kernel<<<n_seqs * n_v_heads, kThreads, kSmemBytes, s>>>(
         state, q, k, g, ws, y, n_seqs, seqs, n_k_heads, n_v_heads, cb, nc, scale, slots, pool,
-        cb == 0 ? err_count : nullptr);
+        cb == 0 ? err_count : nullptr, snap);
     return launch_status();
 }
 
@@ -819,6 +881,35 @@ extern "C" gdn_status gdn_chunked_advance(float *state, const float *q, const fl
                           chunk_begin, n_chunks, slots, pool, err_count, as_cuda(stream));
 }
 
+namespace {
+
+// A uniform batch in waves of as many chunks as the workspace holds; the arguments are
+// checked by the caller, n_seqs and n_tokens are positive.
+gdn_status scan_uniform_waves(float *state, const float *q, const float *k, const float *v,
+                              const float *g, const float *beta, float *y, int n_seqs,
+                              int n_tokens, int n_k_heads, int n_v_heads, float scale,
+                              const int32_t *slots, int pool, int32_t *err_count,
+                              void *workspace, size_t workspace_bytes, SnapOut snap,
+                              cudaStream_t s) {
+    const int n_chunks = (n_tokens + kC - 1) / kC;
+    const size_t fit = workspace_bytes / bytes_per_chunk(n_seqs, n_v_heads);
+    if (fit < 1) return GDN_ERR_SHAPE;
+    const int wave = fit < static_cast<size_t>(n_chunks) ? static_cast<int>(fit) : n_chunks;
+    if (static_cast<long long>(wave) * n_seqs * n_k_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    float *ws = static_cast<float *>(workspace);
+    for (int cb = 0; cb < n_chunks; cb += wave) {
+        const int nc = n_chunks - cb < wave ? n_chunks - cb : wave;
+        const SeqMap seqs = uniform_seqs(n_seqs, n_tokens);
+        GDN_TRY(launch_prepare(q, k, v, g, beta, ws, n_seqs, seqs, n_k_heads, n_v_heads, cb, nc,
+                               s));
+        GDN_TRY(launch_advance(state, q, k, g, ws, y, n_seqs, seqs, n_k_heads, n_v_heads, scale,
+                               cb, nc, slots, pool, err_count, s, snap));
+    }
+    return GDN_OK;
+}
+
+}  // namespace
+
 extern "C" gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *q, const float *k,
                                                      const float *v, const float *g,
                                                      const float *beta, float *y, int n_seqs,
@@ -835,22 +926,36 @@ extern "C" gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *
     if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
         !aligned16(workspace))
         return GDN_ERR_ALIGN;
-    const int n_chunks = (n_tokens + kC - 1) / kC;
-    const size_t fit = workspace_bytes / bytes_per_chunk(n_seqs, n_v_heads);
-    if (fit < 1) return GDN_ERR_SHAPE;
-    const int wave = fit < static_cast<size_t>(n_chunks) ? static_cast<int>(fit) : n_chunks;
-    if (static_cast<long long>(wave) * n_seqs * n_k_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-    const cudaStream_t s = as_cuda(stream);
-    float *ws = static_cast<float *>(workspace);
-    for (int cb = 0; cb < n_chunks; cb += wave) {
-        const int nc = n_chunks - cb < wave ? n_chunks - cb : wave;
-        const SeqMap seqs = uniform_seqs(n_seqs, n_tokens);
-        GDN_TRY(launch_prepare(q, k, v, g, beta, ws, n_seqs, seqs, n_k_heads, n_v_heads, cb, nc,
-                               s));
-        GDN_TRY(launch_advance(state, q, k, g, ws, y, n_seqs, seqs, n_k_heads, n_v_heads, scale,
-                               cb, nc, slots, pool, err_count, s));
-    }
-    return GDN_OK;
+    return scan_uniform_waves(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
+                              scale, slots, pool, err_count, workspace, workspace_bytes,
+                              SnapOut{nullptr, 1, 0}, as_cuda(stream));
+}
+
+extern "C" int gdn_chunked_snapshot_count(int n_tokens, int snap_every) {
+    if (n_tokens < 0 || snap_every < 1) return -1;
+    return static_cast<int>(n_tokens / (static_cast<long long>(kC) * snap_every));
+}
+
+extern "C" gdn_status gdn_recurrence_scan_chunked_snapshots(
+    float *state, const float *q, const float *k, const float *v, const float *g,
+    const float *beta, float *y, float *snaps, int snap_every, int n_seqs, int n_tokens,
+    int n_k_heads, int n_v_heads, int state_size, float scale, const int32_t *slots, int pool,
+    int32_t *err_count, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    if (!state || !q || !k || !v || !g || !beta || !y) return GDN_ERR_NULL;
+    GDN_TRY(check_common(n_seqs, n_tokens, n_k_heads, n_v_heads, state_size));
+    GDN_TRY(check_pool(n_seqs, slots, pool));
+    if (snap_every < 1) return GDN_ERR_SHAPE;
+    if (n_seqs == 0 || n_tokens == 0) return GDN_OK;
+    const int n_snaps = gdn_chunked_snapshot_count(n_tokens, snap_every);
+    if (n_snaps > 0 && !snaps) return GDN_ERR_NULL;
+    if (!workspace) return GDN_ERR_NULL;
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(workspace) || (n_snaps > 0 && !aligned16(snaps)))
+        return GDN_ERR_ALIGN;
+    return scan_uniform_waves(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
+                              scale, slots, pool, err_count, workspace, workspace_bytes,
+                              SnapOut{n_snaps > 0 ? snaps : nullptr, snap_every, n_snaps},
+                              as_cuda(stream));
 }
 
 extern "C" size_t gdn_recurrence_scan_chunked_varlen_ws_size(int n_seqs, int total_tokens,

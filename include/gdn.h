@@ -239,6 +239,31 @@ gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *q, const fl
                                           void *workspace, size_t workspace_bytes,
                                           gdn_stream_t stream);
 
+/* Snapshots the chunked scan writes for n_tokens positions at interval snap_every
+ * (in chunks of 32 positions): floor(n_tokens / (32 * snap_every)); -1 for a
+ * negative n_tokens or a snap_every below 1. */
+int gdn_chunked_snapshot_count(int n_tokens, int snap_every);
+
+/* gdn_recurrence_scan_chunked_ws, also writing the state at every 32 * snap_every
+ * positions, for prefix caching of long prompts: a subsample of what
+ * gdn_recurrence_scan_snapshots writes (ssm_gated_delta.cu, fc_ssm_recurrence_seq's
+ * `snaps` argument: the whole recurrent state after a position's update).
+ * Snapshot j of sequence n is the state once position (j + 1) * 32 * snap_every - 1
+ * has been applied, j < gdn_chunked_snapshot_count(n_tokens, snap_every); a call
+ * whose n_tokens is a multiple of 32 * snap_every ends on one, equal to the final
+ * state. snaps: [n_seqs][n_snaps][H][S][S] (each snapshot laid out as one state
+ * slot, sequence n in call order, not by slot), device memory owned by the caller,
+ * written, 16-byte aligned (GDN_ERR_ALIGN); NULL when n_snaps > 0 is GDN_ERR_NULL.
+ * snap_every below 1 is GDN_ERR_SHAPE. Other arguments, errors, workspace and waves
+ * as gdn_recurrence_scan_chunked_ws, whose y and state it reproduces bit for bit;
+ * the snapshots are the same fp32 values the scan carries (a continuation from
+ * snapshot j gives the bits of the full call's later chunks). */
+gdn_status gdn_recurrence_scan_chunked_snapshots(
+    float *state, const float *q, const float *k, const float *v, const float *g,
+    const float *beta, float *y, float *snaps, int snap_every, int n_seqs, int n_tokens,
+    int n_k_heads, int n_v_heads, int state_size, float scale, const int32_t *slots, int pool,
+    int32_t *err_count, void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
 /* The two phases of gdn_recurrence_scan_chunked_ws as separate calls, for callers
  * that schedule them themselves (e.g. prepare the next wave of chunks on another
  * stream while the state advances over this one). A chunk range is chunk_begin ..

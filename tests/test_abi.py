@@ -244,6 +244,41 @@ def test_chunked_ws_validation(lib):
     assert call(n_tokens=0, workspace=None) == OK
 
 
+def test_chunked_snapshot_validation(lib):
+    count = lib.gdn_chunked_snapshot_count
+    count.argtypes = [ctypes.c_int] * 2
+    count.restype = ctypes.c_int
+    assert count(64, 1) == 2 and count(63, 1) == 1 and count(31, 1) == 0
+    assert count(4096, 16) == 8 and count(4095, 16) == 7 and count(0, 3) == 0
+    assert count(2**31 - 1, 2**30) == 0  # no overflow in 32 * snap_every
+    assert count(10, 0) == -1 and count(-1, 1) == -1
+    f = lib.gdn_recurrence_scan_chunked_snapshots
+    f.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 6 + [
+        ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_size_t, ctypes.c_void_p]
+    blk = 36 * 1024
+
+    def call(snaps=P, every=1, n_tokens=64, q=P, workspace=P, nbytes=None, s=128, pool=2,
+             state=P):
+        nbytes = 2 * 2 * 4 * blk if nbytes is None else nbytes
+        return f(state, q, P, P, P, P, P, snaps, every, 2, n_tokens, 2, 4, s, 0.1, None, pool,
+                 None, workspace, nbytes, None)
+    assert call(every=0) == SHAPE
+    assert call(every=-3) == SHAPE
+    assert call(snaps=None) == NULL              # two snapshots to write
+    assert call(snaps=MIS) == ALIGN
+    assert call(state=None) == NULL
+    assert call(workspace=None) == NULL
+    assert call(s=64) == UNSUP
+    assert call(pool=1) == SHAPE
+    # no snapshot falls in 40 positions at an interval of 2 chunks: snaps may be NULL
+    # or unaligned, the call gets as far as the workspace check
+    assert call(snaps=None, every=2, n_tokens=40, q=MIS) == ALIGN
+    assert call(snaps=MIS, every=2, n_tokens=40, nbytes=16) == SHAPE
+    assert call(n_tokens=0, snaps=None, workspace=None) == OK
+    assert call(n_tokens=0, every=0) == SHAPE  # the interval is checked even when empty
+
+
 def test_chunked_phase_validation(lib):
     prep = lib.gdn_chunked_prepare
     prep.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_size_t] + [ctypes.c_int] * 7 + [
