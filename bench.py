@@ -851,6 +851,26 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
             one_ev[i][1].record(stream)
         torch.cuda.synchronize()
         one_s = sum(e0.elapsed_time(e1) for e0, e1 in one_ev) / 1e3 / args.steps
+        # the snapshot form (prefix caching): the state every 16 chunks (512 positions)
+        every = 16
+        n_snaps = gdn.gdn_chunked_snapshot_count(T, every)
+        snaps = torch.empty(N, n_snaps, H, S, S, device="cuda")
+        snap_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+        gpu_head_start(torch)
+        for i in range(args.steps):
+            state.copy_(state0)
+            flush()
+            snap_ev[i][0].record(stream)
+            gdn.gdn_recurrence_scan_chunked_snapshots(state, d["q"], d["k"], d["v"], d["g"],
+                                                      d["beta"], y, snaps, every, N, T, Hk, H, S,
+                                                      cfg.scale, ws)
+            snap_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        gdn.gdn_device_error()
+        snap_s = sum(e0.elapsed_time(e1) for e0, e1 in snap_ev) / 1e3 / args.steps
+        snap_bytes = snaps.numel() * 4
+        del snaps
         tf = chunked_tensor_flops(N, T, H)
         pf = chunk_prepare_flops(N, T, Hk, H)
         bf16_peak = pk.get("bf16_tflops", 1900.0)
@@ -868,6 +888,10 @@ def run_ours_scan(args, cfg, rank, world, dev, flush, pk, pk_kind, dist):
                  "prepare_fp32_tflops": pf / prep_s / 1e12,
                  "prepare_frac_of_fp32_pipes": pf / prep_s / 1e12 / fp32_peak,
                  "one_kernel_form_ms": 1e3 * one_s,
+                 "snapshot_form": {"call": "gdn_recurrence_scan_chunked_snapshots",
+                                   "snap_every_chunks": every, "snapshots_per_seq": n_snaps,
+                                   "snapshot_bytes": snap_bytes, "ms": 1e3 * snap_s,
+                                   "over_plain_ms": 1e3 * (snap_s - per)},
                  "workspace_bytes": ws.numel() * 4}
     else:
         roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",

@@ -28,7 +28,8 @@ __all__ = [
     "gdn_chunked_snapshot_count", "gdn_recurrence_scan_chunked_snapshots",
     "gdn_chunked_prepare", "gdn_chunked_advance", "gdn_block_prefill_chunked_workspace_size",
     "gdn_recurrence_scan_varlen", "gdn_recurrence_scan_chunked_varlen_ws_size",
-    "gdn_recurrence_scan_chunked_varlen", "gdn_block_prefill_varlen_workspace_size",
+    "gdn_recurrence_scan_chunked_varlen", "gdn_recurrence_scan_chunked_snapshots_varlen",
+    "gdn_block_prefill_varlen_workspace_size",
     "gdn_block_prefill_chunked_varlen_workspace_size", "gdn_block_prefill_varlen",
     "gdn_block_prefill_chunked_varlen", "gdn_block_prefill_snapshots_varlen",
     "gdn_snapshot_restore_varlen", "gdn_selftest_bounded_wait",
@@ -89,6 +90,9 @@ _SIGS = {
                                                ctypes.c_size_t, _P], _I),
     "gdn_recurrence_scan_varlen": ([_P] * 8 + [_I] * 6 + [_F, _P, _I, _P, _P], _I),
     "gdn_recurrence_scan_chunked_varlen_ws_size": ([_I, _I, _I, _I], ctypes.c_size_t),
+    "gdn_recurrence_scan_chunked_snapshots_varlen": ([_P] * 9 + [_I, _I, _P] + [_I] * 6 +
+                                                     [_F, _P, _I, _P, _P, ctypes.c_size_t, _P],
+                                                     _I),
     "gdn_recurrence_scan_chunked_varlen": ([_P] * 8 + [_I] * 6 + [_F, _P, _I, _P, _P,
                                                                 ctypes.c_size_t, _P], _I),
     "gdn_block_prefill_varlen_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
@@ -533,6 +537,25 @@ def gdn_recurrence_scan_chunked_varlen(state, q, k, v, g, beta, y, cu_seqlens, n
         _ptr(beta, "beta"), _ptr(y, "y"), _cu(cu_seqlens), n_seqs, total_tokens, max_tokens,
         n_k_heads, n_v_heads, state_size, scale, _slots(slots), pool, _errc(err_count), ws,
         nbytes, _stream(stream)))
+
+
+def gdn_recurrence_scan_chunked_snapshots_varlen(state, q, k, v, g, beta, y, snaps, snap_base,
+                                                 snap_pool, snap_every, cu_seqlens, n_seqs,
+                                                 total_tokens, max_tokens, n_k_heads, n_v_heads,
+                                                 state_size, scale, workspace, slots=None,
+                                                 pool=None, err_count=None, stream=None):
+    """The ragged chunked scan keeping snapshots: sequence n's snapshot j in slot
+    snap_base[n] + j of `snaps` ([snap_pool][H][S][S]); snaps and snap_base may be None
+    when no sequence can reach a snapshot."""
+    pool = _pool(pool, n_seqs, slots)
+    _check("gdn_recurrence_scan_chunked_snapshots_varlen",
+           library().gdn_recurrence_scan_chunked_snapshots_varlen(
+               _ptr(state, "state"), _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g"),
+               _ptr(beta, "beta"), _ptr(y, "y"), _ptr(snaps, "snaps", optional=True),
+               _ptr(snap_base, "snap_base", _torch().int32, optional=True), snap_pool,
+               snap_every, _cu(cu_seqlens), n_seqs, total_tokens, max_tokens, n_k_heads,
+               n_v_heads, state_size, scale, _slots(slots), pool, _errc(err_count),
+               _ws_ptr(workspace), _ws_bytes(workspace), _stream(stream)))
 
 
 def gdn_block_prefill_varlen_workspace_size(n_seqs, total_tokens, n_k_heads, n_v_heads,

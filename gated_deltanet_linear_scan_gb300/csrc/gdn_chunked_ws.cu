@@ -304,13 +304,18 @@ __device__ __forceinline__ void copy_state_row(uint32_t trow, int c0, float *dst
     }
 }
 
-// State snapshots of a uniform batch: every `every` chunks, the state after the chunk
-// that ends there. Snapshot j of sequence n is the state after position
-// (j + 1) * every * kC - 1, at p + (n * count + j) * H * kS * kS, laid out as one state
-// slot. p == nullptr: none.
+// State snapshots: every `every` chunks, the state after the chunk that ends there.
+// Snapshot j of a sequence is the state after its position (j + 1) * every * kC - 1,
+// laid out as one state slot (H * kS * kS floats) of p. Uniform batch (base == nullptr):
+// `count` a sequence, sequence n's at slots n * count + j. Ragged batch: sequence n's
+// floor(len / (every * kC)) snapshots at slots base[n] + j of a pool of `pool` slots; a
+// negative base, or a range past the pool, writes none of them (and is counted).
+// p == nullptr: none.
 struct SnapOut {
     float *p;
     int every, count;
+    const int32_t *base;
+    int pool;
 
     // the first chunk, from chunk cb on, that a snapshot precedes (a positive multiple
     // of every)
@@ -318,20 +323,33 @@ struct SnapOut {
         const int m = (cb + every - 1) / every;
         return (m > 1 ? m : 1) * every;
     }
-    // the row dv of v-head vh of the snapshot that precedes chunk cg (a positive multiple
-    // of every), or nullptr past the last one
-    __device__ __forceinline__ float *row(int cg, int n, int vh, int H, int dv) const {
-        const int j = cg / every - 1;
-        if (j >= count) return nullptr;
-        return p + ((static_cast<size_t>(n) * count + j) * H + vh) * (kS * kS) +
-               static_cast<size_t>(dv) * kS;
+    // Row dv of v-head vh in snapshot slot 0 of sequence n (of n_tok positions), and the
+    // number of its snapshots to write; false for a ragged range that does not fit.
+    __device__ __forceinline__ bool place(int n, int n_tok, int vh, int H, int dv, float *&row0,
+                                          int &n_snap) const {
+        long long slot0;
+        if (base == nullptr) {
+            slot0 = static_cast<long long>(n) * count;
+            n_snap = count;
+        } else {
+            slot0 = base[n];
+            n_snap = n_tok / (every * kC);
+            if (n_snap == 0 || slot0 < 0 || slot0 + n_snap > pool) {
+                const bool fits = n_snap == 0;
+                n_snap = 0;
+                row0 = nullptr;
+                return fits;
+            }
+        }
+        row0 = p + (static_cast<size_t>(slot0) * H + vh) * (kS * kS) + static_cast<size_t>(dv) * kS;
+        return true;
     }
 };
 
 // One CTA per (sequence, v-head); grid = n_seqs * n_v_heads. Advances the state over
 // chunks c_begin .. c_begin + n_wave_chunks - 1, whose workspace blocks are prepared.
-// kSnap (uniform batches, snap.p set): it also writes the snapshots that fall in them;
-// a separate instantiation, so that the plain form keeps its registers.
+// kSnap (snap.p set): it also writes the snapshots that fall in them; a separate
+// instantiation, so that the plain form keeps its registers.
 // Roles as in the one-kernel form: producer (k, q rows), MMA issuer, state warps (the
 // split of S, U = Ut - D_u, y, no Gram stage), prep warps (operand images only).
 template <bool kSnap>
@@ -361,6 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
         if (vh == 0 && tid == 0 && err_count) atomicAdd(err_count, 1);
         return;
     }
+    float *snap_row0 = nullptr;  // this thread's row of the sequence's snapshot slot 0
+    int snap_n = 0;              // snapshots of the sequence to write
+    // (tid & 127 is a state thread's row dv: quarter * 32 + lane)
+    if (kSnap && !snap.place(n, n_tokens, vh, H, tid & 127, snap_row0, snap_n) && vh == 0 &&
+        tid == 0 && err_count)
+        atomicAdd(err_count, 1);  // the scan runs; its snapshots are not written
     // uniform batch: this wave's chunks, block rows ci * n_seqs + n; ragged batch: all of
     // the sequence's chunks in one wave, block rows from its first chunk slot on
     const int nw = seqs.cu ? (n_tokens + kC - 1) / kC : n_wave_chunks;
@@ -543,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
         if (chunk_t0(0) + lane < n_tokens) g_cur = g[(row0 + chunk_t0(0) + lane) * H + vh];
         bool ok = true;
         int snap_cg = kSnap ? snap.first(c_begin) : 0;  // the next chunk a snapshot precedes
+        const size_t snap_stride = static_cast<size_t>(H) * kS * kS;
         for (int ci = 0; ci < nw && ok; ++ci) {
             // this chunk's Ut (dv = this thread's lane of tensor memory, positions u0..)
             float utv[16];
@@ -564,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             // S here is the state after the previous chunk: a snapshot when that chunk
             // ends a snapshot interval
             if (kSnap && c_begin + ci == snap_cg) {
-                if (float *row = snap.row(snap_cg, n, vh, H, dv)) copy_state_row(trow, c0, row);
+                const int j = snap_cg / snap.every - 1;
+                if (j < snap_n) copy_state_row(trow, c0, snap_row0 + j * snap_stride);
                 snap_cg += snap.every;
             }
             // S -> (hi, lo), the A operand of the S products; the accumulator becomes
@@ -603,7 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(
             copy_state_row(trow, c0, srow);
             // the final state is the last snapshot too when the sequence ends on one
             if (kSnap && c_begin + nw == snap_cg && snap_cg * kC == n_tokens) {
-                if (float *row = snap.row(snap_cg, n, vh, H, dv)) copy_state_row(trow, c0, row);
+                const int j = snap_cg / snap.every - 1;
+                if (j < snap_n) copy_state_row(trow, c0, snap_row0 + j * snap_stride);
             }
         }
     } else {
@@ -766,7 +793,7 @@ gdn_status launch_advance(float *state, const float *q, const float *k, const fl
                           const float *ws, float *y, int n_seqs, SeqMap seqs, int n_k_heads,
                           int n_v_heads, float scale, int cb, int nc, const int32_t *slots,
                           int pool, int32_t *err_count, cudaStream_t s,
-                          SnapOut snap = SnapOut{nullptr, 1, 0}) {
+                          SnapOut snap = SnapOut{nullptr, 1, 0, nullptr, 0}) {
     // per launch: the attribute belongs to the current device
     auto *kernel = snap.p ? chunk_state_kernel<true> : chunk_state_kernel<false>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -811,6 +838,20 @@ size_t chunked_seqs_ws_size(int n_seqs, SeqMap seqs, int n_v_heads) {
     if (seqs.cu == nullptr)
         return static_cast<size_t>((seqs.n_tokens + kC - 1) / kC) * bytes_per_chunk(n_seqs, n_v_heads);
     return ragged_chunked_ws_size(n_seqs, seqs.total, n_v_heads);
+}
+
+// The two-phase chunked scan of a ragged batch in one wave, its workspace checked.
+static gdn_status chunked_ragged_ws(float *state, const float *q, const float *k, const float *v,
+                                    const float *g, const float *beta, float *y, int n_seqs,
+                                    SeqMap seqs, int n_k_heads, int n_v_heads, float scale,
+                                    const int32_t *slots, int pool, int32_t *err_count,
+                                    float *ws, SnapOut snap, cudaStream_t s) {
+    const long long n_slots = ragged_chunk_slots(seqs.total, n_seqs);
+    if (n_slots > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    const int nc = static_cast<int>(n_slots);
+    GDN_TRY(launch_prepare(q, k, v, g, beta, ws, n_seqs, seqs, n_k_heads, n_v_heads, 0, nc, s));
+    return launch_advance(state, q, k, g, ws, y, n_seqs, seqs, n_k_heads, n_v_heads, scale, 0, nc,
+                          slots, pool, err_count, s, snap);
 }
 
 gdn_status launch_chunked_seqs(float *state, const float *q, const float *k, const float *v,
@@ -928,7 +969,7 @@ extern "C" gdn_status gdn_recurrence_scan_chunked_ws(float *state, const float *
         return GDN_ERR_ALIGN;
     return scan_uniform_waves(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
                               scale, slots, pool, err_count, workspace, workspace_bytes,
-                              SnapOut{nullptr, 1, 0}, as_cuda(stream));
+                              SnapOut{nullptr, 1, 0, nullptr, 0}, as_cuda(stream));
 }
 
 extern "C" int gdn_chunked_snapshot_count(int n_tokens, int snap_every) {
@@ -954,7 +995,7 @@ extern "C" gdn_status gdn_recurrence_scan_chunked_snapshots(
         return GDN_ERR_ALIGN;
     return scan_uniform_waves(state, q, k, v, g, beta, y, n_seqs, n_tokens, n_k_heads, n_v_heads,
                               scale, slots, pool, err_count, workspace, workspace_bytes,
-                              SnapOut{n_snaps > 0 ? snaps : nullptr, snap_every, n_snaps},
+                              SnapOut{n_snaps > 0 ? snaps : nullptr, snap_every, n_snaps, nullptr, 0},
                               as_cuda(stream));
 }
 
@@ -981,4 +1022,31 @@ extern "C" gdn_status gdn_recurrence_scan_chunked_varlen(
                                SeqMap{cu_seqlens, max_tokens, total_tokens}, n_k_heads, n_v_heads,
                                scale, slots, pool, err_count, workspace,
                                workspace ? workspace_bytes : 0, as_cuda(stream));
+}
+
+extern "C" gdn_status gdn_recurrence_scan_chunked_snapshots_varlen(
+    float *state, const float *q, const float *k, const float *v, const float *g,
+    const float *beta, float *y, float *snaps, const int32_t *snap_base, int snap_pool,
+    int snap_every, const int32_t *cu_seqlens, int n_seqs, int total_tokens, int max_tokens,
+    int n_k_heads, int n_v_heads, int state_size, float scale, const int32_t *slots, int pool,
+    int32_t *err_count, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    if (!state || !q || !k || !v || !g || !beta || !y) return GDN_ERR_NULL;
+    GDN_TRY(check_varlen(cu_seqlens, n_seqs, total_tokens, max_tokens));
+    GDN_TRY(check_common(n_seqs, max_tokens, n_k_heads, n_v_heads, state_size));
+    GDN_TRY(check_pool(n_seqs, slots, pool));
+    if (snap_every < 1 || snap_pool < 0) return GDN_ERR_SHAPE;
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_ERR_ALIGN;
+    if (n_seqs == 0 || total_tokens == 0 || max_tokens == 0) return GDN_OK;
+    // no sequence of at most max_tokens positions reaches a snapshot: the plain scan
+    const bool any = max_tokens / (static_cast<long long>(kC) * snap_every) > 0;
+    if (any && (!snaps || !snap_base)) return GDN_ERR_NULL;
+    if (!workspace) return GDN_ERR_NULL;
+    if ((any && !aligned16(snaps)) || !aligned16(workspace)) return GDN_ERR_ALIGN;
+    if (workspace_bytes < ragged_chunked_ws_size(n_seqs, total_tokens, n_v_heads))
+        return GDN_ERR_SHAPE;
+    return chunked_ragged_ws(state, q, k, v, g, beta, y, n_seqs,
+                             SeqMap{cu_seqlens, max_tokens, total_tokens}, n_k_heads, n_v_heads,
+                             scale, slots, pool, err_count, static_cast<float *>(workspace),
+                             SnapOut{any ? snaps : nullptr, snap_every, 0, snap_base, snap_pool},
+                             as_cuda(stream));
 }

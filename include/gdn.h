@@ -469,6 +469,29 @@ gdn_status gdn_recurrence_scan_chunked_varlen(float *state, const float *q, cons
                                               int32_t *err_count, void *workspace,
                                               size_t workspace_bytes, gdn_stream_t stream);
 
+/* gdn_recurrence_scan_chunked_snapshots over a ragged batch (prefix caching of a batch
+ * of prompts of different lengths): the two-phase scan of
+ * gdn_recurrence_scan_chunked_varlen, also writing each sequence's state after its
+ * positions (j + 1) * 32 * snap_every - 1, j < floor(len / (32 * snap_every)) (len its
+ * own length; a sequence that ends on an interval gets its final state as its last
+ * snapshot). The snapshots go to a caller-managed pool, as the state goes to state
+ * slots: snaps holds snap_pool slots of n_v_heads * S * S floats (the layout of one
+ * state slot), 16-byte aligned; sequence n's snapshot j goes to slot snap_base[n] + j
+ * (snap_base: int32 device array of n_seqs entries). A sequence whose range does not
+ * lie in [0, snap_pool) (a negative base included) writes none of its snapshots and is
+ * counted in err_count; its scan, state and y are still computed. snaps and snap_base
+ * may be NULL when max_tokens < 32 * snap_every (no snapshot can fall), else NULL is
+ * GDN_ERR_NULL; snap_every below 1 or a negative snap_pool is GDN_ERR_SHAPE. The
+ * workspace is required: at least gdn_recurrence_scan_chunked_varlen_ws_size() bytes
+ * (less: GDN_ERR_SHAPE; NULL: GDN_ERR_NULL). y and state are the bits of
+ * gdn_recurrence_scan_chunked_varlen; other arguments as that call. */
+gdn_status gdn_recurrence_scan_chunked_snapshots_varlen(
+    float *state, const float *q, const float *k, const float *v, const float *g,
+    const float *beta, float *y, float *snaps, const int32_t *snap_base, int snap_pool,
+    int snap_every, const int32_t *cu_seqlens, int n_seqs, int total_tokens, int max_tokens,
+    int n_k_heads, int n_v_heads, int state_size, float scale, const int32_t *slots, int pool,
+    int32_t *err_count, void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
 /* Workspace of the ragged prefill blocks: gdn_block_prefill_varlen and _snapshots_varlen
  * need gdn_block_prefill_varlen_workspace_size() bytes (the intermediates of
  * total_tokens positions); gdn_block_prefill_chunked_varlen takes its two-phase chunked

@@ -50,6 +50,25 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(gdn, name), f"binding lacks {name}"
 
 
+def declared_arity():
+    """Parameter count of every function include/gdn.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else len(params.split(","))
+    return out
+
+
+def test_binding_arity_matches_the_header():
+    """The ctypes table gives each call as many arguments as its C declaration has."""
+    arity = declared_arity()
+    assert len(arity) == len(declared_functions())
+    for name, (args, _) in gdn._SIGS.items():
+        assert name in arity, f"{name} is bound but not declared"
+        assert len(args) == arity[name], f"{name}: {len(args)} argtypes, {arity[name]} parameters"
+
+
 def test_status_strings_and_version(lib):
     for code, name in gdn.STATUS.items():
         assert lib.gdn_status_str(code).decode() == name
@@ -277,6 +296,34 @@ def test_chunked_snapshot_validation(lib):
     assert call(snaps=MIS, every=2, n_tokens=40, nbytes=16) == SHAPE
     assert call(n_tokens=0, snaps=None, workspace=None) == OK
     assert call(n_tokens=0, every=0) == SHAPE  # the interval is checked even when empty
+
+
+def test_ragged_chunked_snapshot_validation(lib):
+    f = lib.gdn_recurrence_scan_chunked_snapshots_varlen
+    size = lib.gdn_recurrence_scan_chunked_varlen_ws_size
+    size.argtypes = [ctypes.c_int] * 4
+    size.restype = ctypes.c_size_t
+
+    def call(snaps=P, base=P, snap_pool=4, every=1, max_tokens=64, total=100, cu=P, state=P,
+             q=P, workspace=P, nbytes=None, n_seqs=2):
+        nbytes = size(2, total, 4, 128) if nbytes is None else nbytes
+        return f(state, q, P, P, P, P, P, snaps, base, snap_pool, every, cu, n_seqs, total,
+                 max_tokens, 2, 4, 128, 0.1, None, 2, None, workspace, nbytes, None)
+    assert call(state=None) == NULL
+    assert call(cu=None) == NULL
+    assert call(every=0) == SHAPE
+    assert call(snap_pool=-1) == SHAPE
+    assert call(snaps=None) == NULL           # a 64-position sequence reaches a snapshot
+    assert call(base=None) == NULL
+    assert call(snaps=MIS) == ALIGN
+    assert call(q=MIS) == ALIGN
+    assert call(workspace=None) == NULL
+    assert call(workspace=MIS) == ALIGN
+    assert call(nbytes=16) == SHAPE           # less than the ragged workspace
+    # at most 63 positions and an interval of 2 chunks: no snapshot can fall, so snaps
+    # and snap_base may be NULL (the call gets as far as the workspace check)
+    assert call(snaps=None, base=None, every=2, max_tokens=63, nbytes=16) == SHAPE
+    assert call(n_seqs=0, total=0, max_tokens=0, snaps=None, base=None, workspace=None) == OK
 
 
 def test_chunked_phase_validation(lib):

@@ -263,3 +263,130 @@ def test_snapshots_prefill_4x4096(lib):
     y_c = run_plain(lib, cfg, inputs(x, t0), st_c, T=T - t0)
     assert torch.equal(y_c, y_s[:, t0:])
     assert torch.equal(st_c, st_s)
+
+
+# ------------------------------------------------------------------ ragged batches
+
+class RaggedScan:
+    """Sequences of the given lengths, each seeded on its own, packed position-major."""
+
+    def __init__(self, lengths, Hk=2, H=4, seed=0, pool=None):
+        self.lengths = list(lengths)
+        self.n = len(lengths)
+        self.cfg = I.get_config(0, n_k_heads=Hk, n_v_heads=H, state_size=128, n_seqs=self.n,
+                                n_tokens=max(lengths), pool=pool, cid=1300 + seed)
+        self.per = [I.recurrence_batch(I.get_config(0, n_k_heads=Hk, n_v_heads=H,
+                                                    state_size=128, n_seqs=1, n_tokens=L,
+                                                    cid=1400 + 31 * seed + i))
+                    for i, L in enumerate(lengths)]
+        self.packed = {key: np.concatenate([p[key][0] for p in self.per])
+                       for key in ("q", "k", "v", "g", "beta")}
+        self.cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+        self.total = int(self.cu[-1])
+        self.st0 = I.state_pool(self.cfg)
+
+    def run(self, lib, every, base, snap_pool, slots=None, pool=None, err=None, snaps=True):
+        cfg, H, S = self.cfg, self.cfg.n_v_heads, 128
+        st = dev(self.st0)
+        y = torch.zeros(self.total, H, S, device="cuda")
+        sn = (torch.full((snap_pool, H, S, S), float("nan"), device="cuda")
+              if snaps else None)
+        ws = torch.empty(lib.gdn_recurrence_scan_chunked_varlen_ws_size(
+            self.n, self.total, H, S) // 4, device="cuda")
+        d = [dev(self.packed[key]) for key in ("q", "k", "v", "g", "beta")]
+        lib.gdn_recurrence_scan_chunked_snapshots_varlen(
+            st, *d, y, sn, None if base is None else dev(np.asarray(base, np.int32)), snap_pool,
+            every, dev(self.cu), self.n, self.total, max(self.lengths), cfg.n_k_heads, H, S,
+            cfg.scale, ws, slots=slots, pool=pool, err_count=err)
+        return y, st, sn
+
+    def run_plain(self, lib, slots=None, pool=None):
+        cfg, H, S = self.cfg, self.cfg.n_v_heads, 128
+        st = dev(self.st0)
+        y = torch.zeros(self.total, H, S, device="cuda")
+        ws = torch.empty(lib.gdn_recurrence_scan_chunked_varlen_ws_size(
+            self.n, self.total, H, S) // 4, device="cuda")
+        d = [dev(self.packed[key]) for key in ("q", "k", "v", "g", "beta")]
+        lib.gdn_recurrence_scan_chunked_varlen(st, *d, y, dev(self.cu), self.n, self.total,
+                                               max(self.lengths), cfg.n_k_heads, H, S, cfg.scale,
+                                               workspace=ws, slots=slots, pool=pool)
+        return y, st
+
+    def counts(self, every):
+        return [L // (C * every) for L in self.lengths]
+
+
+LENGTHS = [1, 31, 32, 33, 100, 257, 64, 130]
+
+
+@pytest.mark.parametrize("every", [1, 2])
+def test_ragged_snapshots_equal_single_sequence_calls(lib, every):
+    """Each sequence's snapshots (at slots base[n] + j of a dense pool), y and final state:
+    the bits of a uniform snapshot call of that sequence alone, and y and state the bits
+    of the plain ragged call."""
+    rg = RaggedScan(LENGTHS, seed=every)
+    cnt = rg.counts(every)
+    base = np.concatenate([[0], np.cumsum(cnt)[:-1]]).astype(np.int32)
+    snap_pool = int(sum(cnt))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y, st, sn = rg.run(lib, every, base, snap_pool, err=err)
+    assert host(err)[0] == 0
+    y_p, st_p = rg.run_plain(lib)
+    assert torch.equal(y, y_p) and torch.equal(st, st_p)
+    H, S = rg.cfg.n_v_heads, 128
+    for n, L in enumerate(LENGTHS):
+        one = I.get_config(0, n_k_heads=2, n_v_heads=H, state_size=128, n_seqs=1, n_tokens=L,
+                           cid=1)
+        st1 = dev(rg.st0[n:n + 1])
+        y1, s1 = run_snap(lib, one, inputs(rg.per[n]), st1, every)
+        assert torch.equal(y[rg.cu[n]:rg.cu[n + 1]], y1[0]), f"y of sequence {n}"
+        assert torch.equal(st[n], st1[0]), f"state of sequence {n}"
+        if cnt[n]:
+            assert torch.equal(sn[base[n]:base[n] + cnt[n]], s1[0]), f"snapshots of sequence {n}"
+    assert not torch.isnan(sn).any()  # the dense pool is filled exactly
+
+
+def test_ragged_snapshots_vs_oracle(lib):
+    """Two sequences' snapshots against the oracle's state at the same positions."""
+    every = 1
+    rg = RaggedScan(LENGTHS, seed=5)
+    cnt = rg.counts(every)
+    base = np.concatenate([[0], np.cumsum(cnt)[:-1]]).astype(np.int32)
+    _, _, sn = rg.run(lib, every, base, int(sum(cnt)))
+    got = host(sn)
+    for n in (5, 7):  # 257 and 130 positions: 8 and 4 snapshots
+        one = I.get_config(0, n_k_heads=2, n_v_heads=4, state_size=128, n_seqs=1,
+                           n_tokens=LENGTHS[n], cid=1)
+        ref = oracle_snapshots(one, rg.per[n], rg.st0[n:n + 1], every)
+        for j in range(cnt[n]):
+            for vh in range(4):
+                assert_rms(got[base[n] + j, vh], ref[0, j, vh], f"snapshot ({n},{j},{vh})")
+
+
+def test_ragged_snapshot_placement_and_slots(lib):
+    """Snapshot ranges that leave the pool (a negative base, one past the end) are
+    skipped and counted once each, a sequence with no snapshots is never counted, state
+    slots route as usual, and y and state stay the plain call's."""
+    lengths = [100, 40, 70, 20, 64]   # 3, 1, 2, 0, 2 snapshots at an interval of 1 chunk
+    rg = RaggedScan(lengths, seed=9, pool=7)
+    slots = dev(np.array([6, 0, 3, 5, 2], dtype=np.int32))
+    base = [0, -1, 9, -5, 3]           # sequence 1 negative, 2 past the pool of 10 slots,
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")  # 3 has none (not counted)
+    y, st, sn = rg.run(lib, 1, base, 10, slots=slots, pool=7, err=err)
+    assert host(err)[0] == 2
+    y_p, st_p = rg.run_plain(lib, slots=slots, pool=7)
+    assert torch.equal(y, y_p) and torch.equal(st, st_p)
+    got = host(sn)
+    assert not np.isnan(got[0:3]).any() and not np.isnan(got[3:5]).any()
+    assert np.isnan(got[5:]).all()     # nothing else written
+    # sequence 4's second snapshot at slot 4 is its final state (64 = 2 chunks)
+    np.testing.assert_array_equal(got[4], host(st)[2])
+
+
+def test_ragged_snapshots_none_reachable(lib):
+    """No sequence reaches 32 * snap_every positions: snaps and snap_base may be NULL,
+    and the call is the plain ragged scan."""
+    rg = RaggedScan([5, 40, 63], seed=4)
+    y, st, _ = rg.run(lib, 2, None, 0, snaps=False)
+    y_p, st_p = rg.run_plain(lib)
+    assert torch.equal(y, y_p) and torch.equal(st, st_p)
