@@ -303,6 +303,7 @@ constexpr int kPThreads = (kPRowWarps + 1 + kPProWarps + kPEpiWarps) * 32;
 constexpr int kPUnitRows = kPRowWarps * kR;  // 64 state rows per ring stage
 constexpr int kPMaxStages = 8;
 constexpr int kPBufs = 3;  // depth of the per-group operand buffers and slots
+constexpr int kPEarlyUnits = 1;  // state units issued before the first group's operands
 constexpr int kPSmemBudget = 227 * 1024;
 
 struct PLayout {
@@ -440,6 +441,32 @@ __global__ void __launch_bounds__(kPThreads, 1) block_decode_persistent_kernel(c
 
         if (warp == kPProducer) {
             // -------------------------------------------------------- producer
+            bool ok = true;
+            auto issue_unit = [&](int u) {
+                const int unit = (gi - 1) * units_per_group + u;
+                const int st = unit % stages, su = unit / stages;
+                if (su > 0 && !wait(sempty + st, su - 1, WD_STAGE_FREE)) return false;
+                if (lane == 0) {
+                    const int rr = u / units_per_head, row0 = (u % units_per_head) * kPUnitRows;
+                    const float *src =
+                        p.state + ((static_cast<size_t>(slot) * H + rr * Hk + kh) * S + row0) * S;
+                    mbar_arrive_expect_tx(sfull + st, static_cast<uint32_t>(L.unit_bytes));
+                    bulk_g2s(smem_raw + L.ring + st * L.unit_bytes, src,
+                             static_cast<uint32_t>(L.unit_bytes), sfull + st);
+                    s_issued[st] = su + 1;
+                }
+                __syncwarp();
+                return true;
+            };
+            // The CTA's first group: its first state unit goes out ahead of the operand
+            // copies. At start-up that unit's arrival, not the prologue, gates the row
+            // warps; one unit (4.9 MB over the GPU) delays the operands little, a whole
+            // ring (19.5 MB) delays them more than it gains.
+            const int early = gi == 1 ? (kPEarlyUnits < units_per_group ? kPEarlyUnits
+                                                                        : units_per_group)
+                                      : 0;
+            for (int u = 0; u < early && ok; ++u) ok = issue_unit(u);
+            if (!ok) break;
             if (use > 0 && !wait(gempty + b, use - 1, WD_STAGE_FREE)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(gfull + b, static_cast<uint32_t>(L.gbuf_bytes));
@@ -466,22 +493,7 @@ __global__ void __launch_bounds__(kPThreads, 1) block_decode_persistent_kernel(c
                              S * sizeof(float), gfull + b);
                 }
             }
-            bool ok = true;
-            for (int u = 0; u < units_per_group; ++u) {
-                const int unit = (gi - 1) * units_per_group + u;
-                const int st = unit % stages, su = unit / stages;
-                if (su > 0 && !wait(sempty + st, su - 1, WD_STAGE_FREE)) { ok = false; break; }
-                if (lane == 0) {
-                    const int rr = u / units_per_head, row0 = (u % units_per_head) * kPUnitRows;
-                    const float *src =
-                        p.state + ((static_cast<size_t>(slot) * H + rr * Hk + kh) * S + row0) * S;
-                    mbar_arrive_expect_tx(sfull + st, static_cast<uint32_t>(L.unit_bytes));
-                    bulk_g2s(smem_raw + L.ring + st * L.unit_bytes, src,
-                             static_cast<uint32_t>(L.unit_bytes), sfull + st);
-                    s_issued[st] = su + 1;
-                }
-                __syncwarp();
-            }
+            for (int u = early; u < units_per_group && ok; ++u) ok = issue_unit(u);
             if (!ok) break;
         } else if (warp >= kPPro0 && warp < kPEpi0) {
             // -------------------------------------------------------- prologue
