@@ -593,6 +593,25 @@ def run_ours(args, cfg, rank, world, local_rank):
     state_b, alg_b = algorithmic_bytes_block(cfg, N)
     achieved = alg_b / per_launch_s / 1e9
 
+    # ---- the same steps back to back, nothing between them (how a server runs them):
+    # each step also writes back what the previous one left dirty in L2, and reads what
+    # it left there; one span over all the steps
+    b2b = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    torch.cuda.synchronize()
+    gpu_head_start(torch)
+    b2b[0].record(stream)
+    for i in range(args.steps):
+        launch(d_steps[i % n_distinct], out)
+    b2b[1].record(stream)
+    torch.cuda.synchronize()
+    gdn.gdn_device_error()
+    b2b_s = reduce_max(b2b[0].elapsed_time(b2b[1]) / 1e3, dist, "cuda") / args.steps
+    back_to_back = {"us_per_step": 1e6 * b2b_s, "tokens_per_s": world * N / b2b_s,
+                    "hbm_gbs": alg_b / b2b_s / 1e9,
+                    "hbm_frac_of_peak": alg_b / b2b_s / 1e9 / pk["hbm_gbs"],
+                    "timing": "the steps with no flush between them, one event pair around "
+                              "all of them"}
+
     # ---- the recurrence alone (gdn_recurrence_decode on precomputed q^, k^, v, g, beta),
     # on the same state and slots, timed the same way; reported beside the fused block.
     xr = I.recurrence_batch(cfg, seqs=seqs, n_tokens=n_distinct)
@@ -749,6 +768,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                                "p90": step_us[int(0.9 * (len(step_us) - 1))],
                                "max": step_us[-1]},
                    "wall_s_timed_loop": t_wall,
+                   "back_to_back": back_to_back,
                    "recurrence_only": recurrence_only,
                    **({"graph_chain": chain} if chain else {})},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",

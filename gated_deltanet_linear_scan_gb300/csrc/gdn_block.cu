@@ -358,7 +358,8 @@ __device__ __forceinline__ void p_conv_lane(const float *X, const float *Hh, con
 template <int E>
 __global__ void __launch_bounds__(kPThreads, 1) block_decode_persistent_kernel(const BlockParams p,
                                                                                int n_groups,
-                                                                               int stages) {
+                                                                               int stages,
+                                                                               int reverse) {
     constexpr int S = 32 * E;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int r = p.ratio;
@@ -424,7 +425,10 @@ __global__ void __launch_bounds__(kPThreads, 1) block_decode_persistent_kernel(c
     auto BET = [&](float *c) { return c + 2 * S + 2 * r * S + r; };
 
     int gi = 0;  // index of the valid group, shared by all roles
-    for (int g = blockIdx.x; g < n_groups; g += gridDim.x) {
+    // reverse: the groups in descending order, so that a launch starts on the groups the
+    // previous one (ascending) wrote last, whose new state is still in L2
+    for (int gf = blockIdx.x; gf < n_groups; gf += gridDim.x) {
+        const int g = reverse ? n_groups - 1 - gf : gf;
         const int n = g / Hk, kh = g % Hk;
         const int slot = slot_of(n);
         if (!valid_slot(slot)) {
@@ -649,7 +653,14 @@ gdn_status launch_block_persistent(BlockParams p, int n_seqs, cudaStream_t s, bo
                              static_cast<int>(smem)) != cudaSuccess)
         return GDN_ERR_LAUNCH;
     used = true;
-    block_decode_persistent_kernel<E><<<sms, kPThreads, smem, s>>>(p, static_cast<int>(groups), stages);
+    // Consecutive decode steps walk the groups in alternating directions. A step leaves
+    // the state it wrote last (tens of MB) dirty in L2; the next step, walking the other
+    // way, reads that state first, from L2, instead of evicting it unread. The results do
+    // not depend on the order (each group is independent).
+    static std::atomic<unsigned> launches{0};
+    const int reverse = static_cast<int>(launches.fetch_add(1, std::memory_order_relaxed) & 1u);
+    block_decode_persistent_kernel<E><<<sms, kPThreads, smem, s>>>(p, static_cast<int>(groups), stages,
+                                                                    reverse);
     return launch_status();
 }
 
