@@ -637,10 +637,20 @@ def run_ours(args, cfg, rank, world, local_rank):
     rec_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in rec_ev) / 1e3, dist,
                        "cuda") / args.steps
     rec_bytes = state_b + N * (2 * cfg.n_k_heads * S + 2 * H * S + 2 * H) * 4
+    rb = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    torch.cuda.synchronize()
+    gpu_head_start(torch)
+    rb[0].record(stream)
+    for i in range(args.steps):
+        launch_rec(r_steps[i % n_distinct])
+    rb[1].record(stream)
+    torch.cuda.synchronize()
+    rec_b2b_s = reduce_max(rb[0].elapsed_time(rb[1]) / 1e3, dist, "cuda") / args.steps
     recurrence_only = {"kernel": "gdn_recurrence_decode", "us_per_step": 1e6 * rec_s,
                        "state_gbs": state_b / rec_s / 1e9,
                        "hbm_gbs": rec_bytes / rec_s / 1e9,
-                       "hbm_frac_of_peak": rec_bytes / rec_s / 1e9 / pk["hbm_gbs"]}
+                       "hbm_frac_of_peak": rec_bytes / rec_s / 1e9 / pk["hbm_gbs"],
+                       "back_to_back_us_per_step": 1e6 * rec_b2b_s}
 
     # ---- the same with the factorised readout (gdn_recurrence_decode_2pass)
     tp_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

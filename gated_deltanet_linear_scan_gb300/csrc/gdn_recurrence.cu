@@ -10,6 +10,8 @@
 // the token loop. Decode and scan call the same row step, so a scan over T tokens
 // and T decode calls agree bit for bit (fm_kernel_ssm.m states the same property
 // of its scan).
+#include <atomic>
+
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 
@@ -42,17 +44,20 @@ __global__ void __launch_bounds__(kWarps * 32) recurrence_decode_kernel(
     float *state, const float *__restrict__ q, const float *__restrict__ k,
     const float *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
     float *__restrict__ y, int n_k_heads, int n_v_heads, float scale,
-    const int32_t *__restrict__ slots, int pool, int32_t *err_count) {
+    const int32_t *__restrict__ slots, int pool, int32_t *err_count, int reverse) {
     constexpr int S = 32 * E, R = kRowsPerWarp;
     constexpr int kBlocksPerHead = S / kRowsPerCta;
+    // reverse: the tiles in descending order, so that a launch starts on the tiles the
+    // previous one (ascending) wrote last, whose new state is still in L2
+    const int blk = reverse ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float *tile = reinterpret_cast<float *>(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + kRowsPerCta * S * sizeof(float));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int part = blockIdx.x % kBlocksPerHead;
-    const int vh = (blockIdx.x / kBlocksPerHead) % n_v_heads;
-    const int n = blockIdx.x / (kBlocksPerHead * n_v_heads);
+    const int part = blk % kBlocksPerHead;
+    const int vh = (blk / kBlocksPerHead) % n_v_heads;
+    const int n = blk / (kBlocksPerHead * n_v_heads);
     const int kh = vh % n_k_heads;
     const int slot = slots ? slots[n] : n;
     if (slot < 0 || slot >= pool) {
@@ -364,8 +369,13 @@ gdn_status launch_decode(float *state, const float *q, const float *k, const flo
     GDN_TRY(set_smem(recurrence_decode_kernel<E, FACTORED>, smem));
     const long long blocks = static_cast<long long>(n_seqs) * n_v_heads * (S / kRowsPerCta);
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    // Consecutive decode steps visit the tiles in alternating directions: a step leaves the
+    // state it wrote last dirty in L2 and the next one, walking the other way, reads that
+    // state first instead of evicting it unread. The results do not depend on the order.
+    static std::atomic<unsigned> launches{0};
+    const int reverse = static_cast<int>(launches.fetch_add(1, std::memory_order_relaxed) & 1u);
     recurrence_decode_kernel<E, FACTORED><<<static_cast<unsigned>(blocks), kWarps * 32, smem, s>>>(
-        state, q, k, v, g, beta, y, n_k_heads, n_v_heads, scale, slots, pool, err_count);
+        state, q, k, v, g, beta, y, n_k_heads, n_v_heads, scale, slots, pool, err_count, reverse);
     return launch_status();
 }
 
