@@ -144,7 +144,10 @@ gdn_status gdn_qkv_split_norm(const float *conv_out, float *q, float *k, float *
  * the slot variant; gated_delta_net_decode.metal, "Mathematical recurrence".
  * state: [pool][H][S][S], updated in place (16-byte aligned); q, k: [n_seqs][Hk][S]
  * (post-norm, 16-byte aligned); v, y: [n_seqs][H][S]; g, beta: [n_seqs][H].
- * scale multiplies the readout: 1/sqrt(S), or 1.0f when q is pre-scaled. */
+ * scale multiplies the readout: 1/sqrt(S), or 1.0f when q is pre-scaled.
+ * Consecutive calls visit the state tiles in alternating directions, so a step starts
+ * on the state the previous step wrote last, still in L2; the results do not depend on
+ * it (a CUDA graph records the direction of the call it captures). */
 gdn_status gdn_recurrence_decode(float *state, const float *q, const float *k, const float *v,
                                  const float *g, const float *beta, float *y, int n_seqs,
                                  int n_k_heads, int n_v_heads, int state_size, float scale,
@@ -336,7 +339,11 @@ gdn_status gdn_gated_norm(const float *y, const float *w, const float *z, float 
  * norm_w: [S]; state: [pool][H][S][S] in place; out: [n_seqs][H][S].
  * conv_kernel must be 4; n_v_heads / n_k_heads <= 8 (<= 4 at state_size 256, whose head
  * tile is split over two CTAs of a cluster of at most 8); otherwise GDN_ERR_UNSUPPORTED.
- * All pointers 16-byte aligned. */
+ * All pointers 16-byte aligned. With many sequences, consecutive calls visit the
+ * (sequence, k-head) groups in alternating directions, so a step starts on the state
+ * the previous step wrote last, still in L2; the results do not depend on it. A CUDA
+ * graph captures the direction of the call it records: capture two consecutive steps
+ * to keep the alternation when replaying. */
 gdn_status gdn_block_decode(const float *qkv, const float *conv_w, float *conv_state,
                             const float *alpha, const float *b, const float *dt, const float *a,
                             const float *z, const float *norm_w, float *state, float *out,
