@@ -140,6 +140,19 @@ __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
         const int arr = i / ((kC - valid) * kS), rem = i % ((kC - valid) * kS);
         (arr ? rq : rk)[(valid + rem / kS) * kRawRowF + rem % kS] = 0.f;
     }
+    // g and beta of the first v-head (lane = position), loaded while the copies land; each
+    // v-head's loop then loads the next one's, so no iteration waits on global memory
+    auto load_gb = [&](int rr, float &gl, float &bl) {
+        gl = 0.f;
+        bl = 0.f;
+        if (rr < ratio && lane < valid) {
+            const int vh = rr * Hk + kh;
+            gl = g[(row0 + lane) * H + vh];
+            bl = beta[(row0 + lane) * H + vh];
+        }
+    };
+    float gl_next, bl_next;
+    load_gb(0, gl_next, bl_next);
     bool ok = mbar_wait(bar_kq, 0);
     __syncthreads();
     int t, s0;
@@ -151,11 +164,8 @@ __global__ void __launch_bounds__(kPThreads, 3) chunk_prepare_kernel(
     for (int rr = 0; rr < ratio; ++rr) {
         const int vh = rr * Hk + kh;
         float *blk = ws + (blk_row * H + vh) * kBlkFloats;
-        float gl = 0.f, bl = 0.f;  // lane = position
-        if (lane < valid) {
-            gl = g[(row0 + lane) * H + vh];
-            bl = beta[(row0 + lane) * H + vh];
-        }
+        const float gl = gl_next, bl = bl_next;  // lane = position
+        load_gb(rr + 1, gl_next, bl_next);
         float last;
         const float gam = chunk_gam_from(gl, lane, last);
         const float Gam = expf(gam);
