@@ -296,9 +296,14 @@ PIPELINE_NOTE = ("pipelined: step i + 1's inputs cross to the device on one copy
                  "step i - 1's result back on another while step i computes (inputs and "
                  "outputs double-buffered); every step's copies are inside the timed region; "
                  "no L2 flush (the step's working set exceeds L2)")
+PIPELINE_NOTE_ONE = ("pipelined on one copy stream: once step i has computed, its result "
+                     "and step i + 2's inputs cross while step i + 1 computes (inputs and "
+                     "outputs double-buffered); every step's copies are inside the timed "
+                     "region; no L2 flush (the step's working set exceeds L2)")
 
 
-def pipelined_e2e(torch, dist, steps, h2d, compute, d2h, warmup=2, graph=False):
+def pipelined_e2e(torch, dist, steps, h2d, compute, d2h, warmup=2, graph=False,
+                  one_copy_stream=False):
     """End-to-end steps as a server runs them: h2d(i, b) copies step i's inputs from pinned
     host memory into device buffer set b = i % 2 on a copy stream, compute(i, b) runs the
     step on the current stream once they have landed, d2h(i, b) copies its result back on
@@ -308,10 +313,36 @@ def pipelined_e2e(torch, dist, steps, h2d, compute, d2h, warmup=2, graph=False):
     after `warmup` untimed ones. With graph=True the same `steps` steps (the copies and the
     library calls, in their stream order) are captured once in a CUDA graph and the graph
     is replayed, once untimed and once timed: the device time without the host's per-call
-    overhead."""
+    overhead. one_copy_stream: both directions on one copy stream (for steps whose copies
+    take well under a step, where the host's event and stream calls are the cost): the
+    result of step i and the inputs of step i + 2 cross once step i has computed."""
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_last = s_in if one_copy_stream else s_out  # the stream of the last result copy
+
+    def enqueue_one(n, cur):
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_done = [torch.cuda.Event() for _ in range(n)]
+        torch.cuda.set_stream(s_in)
+        for i in range(min(2, n)):
+            h2d(i, i % 2)
+            ev_in[i].record(s_in)
+        torch.cuda.set_stream(cur)
+        for i in range(n):
+            b = i % 2
+            cur.wait_event(ev_in[i])      # its inputs have landed; step i - 2's result has
+            compute(i, b)                 # left buffer b (copied before those inputs)
+            ev_done[i].record(cur)
+            s_in.wait_event(ev_done[i])
+            torch.cuda.set_stream(s_in)
+            d2h(i, b)
+            if i + 2 < n:                 # buffer b is free for step i + 2's inputs
+                h2d(i + 2, b)
+                ev_in[i + 2].record(s_in)
+            torch.cuda.set_stream(cur)
 
     def enqueue(n, cur):
+        if one_copy_stream:
+            return enqueue_one(n, cur)
         # streams switched with set_stream (a stream context costs the host several times
         # more, and at decode rates the host's enqueue cost is what a step is waiting for)
         ev_in = [torch.cuda.Event() for _ in range(n)]
@@ -369,8 +400,8 @@ def pipelined_e2e(torch, dist, steps, h2d, compute, d2h, warmup=2, graph=False):
                 gpu_head_start(torch)
             start.record(s_in)
         enqueue(n, cur)
-        with torch.cuda.stream(s_out):
-            end.record(s_out)
+        with torch.cuda.stream(s_last):
+            end.record(s_last)
         torch.cuda.synchronize()
         return start.elapsed_time(end) / 1e3
 
@@ -718,11 +749,12 @@ def run_ours(args, cfg, rank, world, local_rank):
         e2e_fns = (lambda i, b: packed[b].copy_(h_packed[i % n_distinct], non_blocking=True),
                    lambda i, b: launch(views2[b], outs[b]),
                    lambda i, b: h_outs[b].copy_(outs[b], non_blocking=True))
-        e2e_s = pipelined_e2e(torch, dist, args.steps, *e2e_fns)
-        e2e_note = PIPELINE_NOTE
+        e2e_s = pipelined_e2e(torch, dist, args.steps, *e2e_fns, one_copy_stream=True)
+        e2e_note = PIPELINE_NOTE_ONE
         # the same pipelined steps captured once in a CUDA graph and replayed (how a server
         # runs decode steps without the host's per-call cost, ~60 us of Python a step here)
-        e2e_graph_s = pipelined_e2e(torch, dist, args.steps, *e2e_fns, graph=True)
+        e2e_graph_s = pipelined_e2e(torch, dist, args.steps, *e2e_fns, graph=True,
+                                    one_copy_stream=True)
 
     # ---- one sequence: the serving form of the chain, a CUDA graph of 1000 consecutive
     # decode steps replayed as one unit (state and conv history carried, L2 warm: the
