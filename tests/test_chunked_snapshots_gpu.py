@@ -390,3 +390,50 @@ def test_ragged_snapshots_none_reachable(lib):
     y, st, _ = rg.run(lib, 2, None, 0, snaps=False)
     y_p, st_p = rg.run_plain(lib)
     assert torch.equal(y, y_p) and torch.equal(st, st_p)
+
+
+def snap_draw(i):
+    """Case i: a reproducible ragged batch, interval, slot routing and snapshot placement."""
+    r = np.random.default_rng(9100 + i)
+    Hk = int(r.choice([1, 2, 4]))
+    ratio = int(r.choice([1, 2, 3, 4]))
+    N = int(r.integers(1, 7))
+    lengths = [int(x) for x in r.integers(1, 300, N)]
+    every = int(r.integers(1, 5))
+    pool = N + int(r.integers(0, 3))
+    slots = r.permutation(pool)[:N].astype(np.int32)
+    cnt = [L // (C * every) for L in lengths]
+    # the sequences' snapshot ranges in shuffled order, with a gap of 0-2 slots before each
+    base, nxt = [0] * N, 0
+    for n in r.permutation(N):
+        nxt += int(r.integers(0, 3))
+        base[n] = nxt
+        nxt += cnt[n]
+    return dict(Hk=Hk, H=Hk * ratio, N=N, lengths=lengths, every=every, pool=pool,
+                slots=slots, base=np.array(base, np.int32), snap_pool=nxt + 1, cnt=cnt)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_ragged_snapshots_random(lib, i):
+    """Seeded ragged batches: every sequence's snapshots are the bits of a uniform call of
+    that sequence alone (from its routed slot's state), the unwritten snapshot slots keep
+    their contents, and y and the state pool are the plain ragged call's."""
+    c = snap_draw(i)
+    rg = RaggedScan(c["lengths"], Hk=c["Hk"], H=c["H"], seed=50 + i, pool=c["pool"])
+    slots = dev(c["slots"])
+    y, st, sn = rg.run(lib, c["every"], c["base"], c["snap_pool"], slots=slots, pool=c["pool"])
+    y_p, st_p = rg.run_plain(lib, slots=slots, pool=c["pool"])
+    assert torch.equal(y, y_p) and torch.equal(st, st_p)
+    written = np.zeros(c["snap_pool"], bool)
+    for n, L in enumerate(c["lengths"]):
+        if not c["cnt"][n]:
+            continue
+        one = I.get_config(0, n_k_heads=c["Hk"], n_v_heads=c["H"], state_size=128, n_seqs=1,
+                           n_tokens=L, cid=1)
+        st1 = dev(rg.st0[c["slots"][n]:c["slots"][n] + 1])
+        _, s1 = run_snap(lib, one, inputs(rg.per[n]), st1, c["every"])
+        b0 = c["base"][n]
+        assert torch.equal(sn[b0:b0 + c["cnt"][n]], s1[0]), f"case {i}: snapshots of sequence {n}"
+        written[b0:b0 + c["cnt"][n]] = True
+    got = host(sn)
+    assert np.isnan(got[~written]).all(), f"case {i}: a slot outside every range was written"
