@@ -195,6 +195,22 @@ gdn_status launch_conv_split_norm(int conv_kernel, const float *qkv, const float
 }
 
 
+// The decay gate and beta of the block's rows in one pass, thread per (row, head):
+// g = a[h] * softplus(alpha + dt[h]) (fm_kernel_ssm.m, "Decay gate"; ssm_gated_delta.cu,
+// fc_ssm_decay_gate_nx) and beta = sigmoid(b) (ssm_gated_delta.cu, fc_sigmoid), with the
+// operations of gdn_decay_gate and gdn_beta_sigmoid, so the same bits.
+constexpr int kGateThreads = 256;
+__global__ void __launch_bounds__(kGateThreads) gate_beta_kernel(
+    const float *__restrict__ alpha, const float *__restrict__ dt, const float *__restrict__ a,
+    const float *__restrict__ b, float *__restrict__ g, float *__restrict__ beta, int n_heads,
+    long long total) {
+    const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (idx >= total) return;
+    const int h = static_cast<int>(idx % n_heads);
+    g[idx] = a[h] * softplus_guarded(alpha[idx] + dt[h]);
+    beta[idx] = 1.0f / (1.0f + expf(-b[idx]));
+}
+
 // The conv history after every position, for speculative-decoding rollback: the K-1
 // raw inputs ending at position t, oldest first (snaps [n][t][C][K-1], the conv_state
 // layout of one slot per position), positions before the call read from the old
@@ -307,8 +323,12 @@ gdn_status prefill_impl(const float *qkv, const float *conv_w, float *conv_state
         case 128: GDN_TRY(launch_conv_split_norm<4>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, seqs, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
         default: GDN_TRY(launch_conv_split_norm<8>(conv_kernel, qkv, conv_w, conv_state, q, k, v, n_seqs, seqs, Hk, H, l2_eps, slots, pool, err_count, cs)); break;
     }
-    GDN_TRY(gdn_decay_gate(alpha, dt, a, g, H, static_cast<int>(rows), stream));
-    GDN_TRY(gdn_beta_sigmoid(b, beta, static_cast<int>(rows * H), stream));
+    {
+        const long long total = rows * H;
+        gate_beta_kernel<<<static_cast<unsigned>((total + kGateThreads - 1) / kGateThreads),
+                           kGateThreads, 0, cs>>>(alpha, dt, a, b, g, beta, H, total);
+        GDN_TRY(launch_status());
+    }
     if (chunked && seqs.cu == nullptr) {
         // the two-phase form in the bytes past the intermediates, if they hold one chunk
         const size_t base = (L.total_floats * sizeof(float) + 15) / 16 * 16;
