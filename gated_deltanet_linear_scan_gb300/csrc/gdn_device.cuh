@@ -181,8 +181,14 @@ __device__ __forceinline__ float ld_shared_cluster(const float *local, uint32_t 
 
 // ------------------------------------------------------------------ math
 
-// SiLU in the divisor form: x / (1 + exp(-x)).
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+// SiLU in the divisor form, x / (1 + exp(-x)), with CUDA's fast exponential and fast
+// division intrinsics: a few ulp at the magnitudes a conv output takes, against the
+// 1e-4 relative bound of one step; where exp(-x) overflows (x below about -88) the
+// quotient is a signed zero, the exact value being below 1e-36 in magnitude. Every
+// kernel calls this one function, so the fused and stand-alone paths keep the same
+// bits. (The IEEE division and expf cost three times the instructions and made the
+// prefill block's conv pass issue-bound.)
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float softplus_guarded(float v) {
     return v > 20.0f ? v : log1pf(expf(v));

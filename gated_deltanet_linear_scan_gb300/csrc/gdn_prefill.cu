@@ -32,32 +32,37 @@ struct PrefillLayout {
     }
 };
 
-// The conv scan and the q/k split + L2-norm in one pass: one CTA per (head slice of
-// S channels, block of positions, sequence), one thread per channel. The conv is
-// the conv scan's arithmetic (current tap, then the history oldest-first; the
-// block at position 0 alone reads and rewrites conv_state). A v slice is written
-// straight out; a q or k slice goes through a shared-memory tile so that one warp
-// per position normalises the head vector with the split-norm kernel's operations
-// (lane L holds elements [E L, E L + E), one butterfly). Results are the two
-// separate kernels' bit for bit, without their [n][t][C] intermediate in HBM.
+// The conv scan and the q/k split + L2-norm in one pass: one warp per (head slice of S
+// channels, block of positions, sequence), kConvNormWarps consecutive slices to a CTA.
+// Lane L holds channels [E L, E L + E) of its slice, the split-norm kernel's lane layout,
+// so a q or k head vector is normalised in registers with one butterfly, and each load
+// and store moves E consecutive channels (one 16-byte access at E = 4). The conv is the
+// conv scan's arithmetic (current tap, then the history oldest-first; the block at
+// position 0 alone reads and rewrites conv_state) and the norm the split-norm kernel's,
+// so the results are those two kernels' bit for bit, without their [n][t][C]
+// intermediate in HBM.
+constexpr int kConvNormWarps = 4;
+
 template <int E>
 __host__ __device__ constexpr int conv_norm_positions() { return E >= 8 ? 16 : 32; }
 static_assert(conv_norm_positions<8>() == 16 && conv_norm_positions<4>() == 32,
               "the ragged grid check in prefill_impl assumes these block sizes");
 
-// Grid, uniform batch: (slice, block of P positions, sequence). Ragged batch: (slice,
-// block slot); block b of sequence n takes slot cu[n] / P + n + b (the chunk-slot scheme
-// of the chunked scan: slots of consecutive sequences never collide and number at most
-// total / P + n_seqs), so no CTA is launched for positions past a sequence's end.
+// Grid, uniform batch: (group of slices, block of P positions, sequence). Ragged batch:
+// (group of slices, block slot); block b of sequence n takes slot cu[n] / P + n + b (the
+// chunk-slot scheme of the chunked scan: slots of consecutive sequences never collide
+// and number at most total / P + n_seqs), so no CTA is launched for positions past a
+// sequence's end.
 template <int E, int K, bool RAGGED>
-__global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
+__global__ void __launch_bounds__(32 * kConvNormWarps) conv_split_norm_kernel(
     const float *__restrict__ qkv, const float *__restrict__ w, float *conv_state,
     float *__restrict__ q, float *__restrict__ k, float *__restrict__ v, const SeqMap seqs,
     int n_seqs, int n_k_heads, int n_v_heads, float eps, const int32_t *__restrict__ slots,
     int pool, int32_t *err_count) {
-    constexpr int S = 32 * E, TAPS = K - 1, P = conv_norm_positions<E>(), ROW = S + 4;
-    __shared__ __align__(16) float tile[P * ROW];
-    const int sl = blockIdx.x, c = threadIdx.x;
+    constexpr int S = 32 * E, TAPS = K - 1, P = conv_norm_positions<E>();
+    constexpr int B = E >= 8 ? 4 : 8;  // positions loaded ahead of their use
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hk = n_k_heads, H = n_v_heads;
     int n, t0;
     size_t seq0;   // first position of sequence n in the token-major arrays
     int n_tokens;  // its length
@@ -67,12 +72,13 @@ __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
         seqs.range(n, seq0, n_tokens);
         const int slot_n = slots ? slots[n] : n;
         if (slot_n < 0 || slot_n >= pool) {  // uniform over the CTA
-            if (err_count && sl == 0 && blockIdx.y == 0 && c == 0) atomicAdd(err_count, 1);
+            if (err_count && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+                atomicAdd(err_count, 1);
             return;
         }
     } else {
-        if (err_count && sl == 0 && blockIdx.y == 0) {  // count each skipped sequence once
-            for (int m = c; m < n_seqs; m += blockDim.x) {
+        if (err_count && blockIdx.x == 0 && blockIdx.y == 0) {  // each skipped sequence once
+            for (int m = threadIdx.x; m < n_seqs; m += blockDim.x) {
                 const int slot_m = slots ? slots[m] : m;
                 size_t a;
                 int len;
@@ -86,75 +92,110 @@ __global__ void __launch_bounds__(32 * E) conv_split_norm_kernel(
         if (slot_n < 0 || slot_n >= pool) return;
         t0 = static_cast<int>(cs - (static_cast<long long>(seqs.cu[n]) / P + n)) * P;
     }
+    const int sl = blockIdx.x * kConvNormWarps + warp;  // this warp's head slice
+    if (sl >= 2 * Hk + H) return;  // uniform over the warp; no CTA barrier follows
     const int slot = slots ? slots[n] : n;
     const int t1 = min(n_tokens, t0 + P);
     if (t0 >= n_tokens) return;  // past the end of a shorter sequence: uniform over the CTA
-    const int Hk = n_k_heads, H = n_v_heads;
     const size_t conv_dim = static_cast<size_t>(2 * Hk + H) * S;
-    const size_t ch = static_cast<size_t>(sl) * S + c;
-    float wc[K];
+    const size_t ch0 = static_cast<size_t>(sl) * S + E * lane;  // this lane's first channel
+    float wc[K][E];
 #pragma unroll
-    for (int t = 0; t < K; ++t) wc[t] = w[ch * K + t];
-    float *hs = conv_state + (static_cast<size_t>(slot) * conv_dim + ch) * TAPS;
-    const float *x_ptr = qkv + seq0 * conv_dim + ch;
-    float old[TAPS], hist[TAPS];
-    if (t0 == 0) {
+    for (int e = 0; e < E; ++e)
 #pragma unroll
-        for (int t = 0; t < TAPS; ++t) old[t] = hs[t];
-    }
+        for (int t = 0; t < K; ++t) wc[t][e] = w[(ch0 + e) * K + t];
+    // the lane's channels' histories, channel-major: hs[e * TAPS + t]
+    float *hs = conv_state + (static_cast<size_t>(slot) * conv_dim + ch0) * TAPS;
+    const float *x_ptr = qkv + seq0 * conv_dim + ch0;
+    float hist[TAPS][E];
 #pragma unroll
     for (int t = 0; t < TAPS; ++t) {
         const int pos = t0 - TAPS + t;
-        hist[t] = pos >= 0 ? x_ptr[static_cast<size_t>(pos) * conv_dim] : old[t];  // t0 == 0
-    }
-    const bool is_qk = sl < 2 * Hk;
-    float *v_out = is_qk ? nullptr : v + (seq0 * H + (sl - 2 * Hk)) * S + c;
-    constexpr int B = 16;  // inputs loaded ahead of their use: memory-level parallelism
-    for (int pb = t0; pb < t1; pb += B) {
-        float xs[B];
+        if (pos >= 0) {
+            load_vec<E>(hist[t], x_ptr + static_cast<size_t>(pos) * conv_dim);
+        } else {  // t0 == 0: the old state
 #pragma unroll
-        for (int j = 0; j < B; ++j)
-            xs[j] = pb + j < t1 ? x_ptr[static_cast<size_t>(pb + j) * conv_dim] : 0.0f;
+            for (int e = 0; e < E; ++e) hist[t][e] = hs[e * TAPS + t];
+        }
+    }
+    const bool is_qk = sl < 2 * Hk;  // uniform over the warp
+    float *dst = is_qk ? (sl < Hk ? q : k) + (seq0 * Hk + (sl % Hk)) * S + E * lane
+                       : v + (seq0 * H + (sl - 2 * Hk)) * S + E * lane;
+    const size_t dst_step = static_cast<size_t>(is_qk ? Hk : H) * S;  // floats a position
+    // position p from its input x: the conv, SiLU, the L2-norm of a q or k head vector,
+    // the store, then x joins the history
+    auto position = [&](const float (&x)[E], int p) {
+        float o[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            float pre = __fmul_rn(x[e], wc[K - 1][e]);
+#pragma unroll
+            for (int t = 0; t < TAPS; ++t) pre = __fmaf_rn(hist[t][e], wc[t][e], pre);
+            o[e] = silu(pre);
+        }
+        if (is_qk) {
+            float ss = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) ss = __fmaf_rn(o[e], o[e], ss);
+            ss = warp_allsum(ss);
+            const float inv = 1.0f / fmaxf(sqrtf(ss), eps);
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] *= inv;
+        }
+        store_vec<E>(dst + static_cast<size_t>(p) * dst_step, o);
+#pragma unroll
+        for (int t = 0; t + 1 < TAPS; ++t)
+#pragma unroll
+            for (int e = 0; e < E; ++e) hist[t][e] = hist[t + 1][e];
+#pragma unroll
+        for (int e = 0; e < E; ++e) hist[TAPS - 1][e] = x[e];
+    };
+    // whole groups of B positions without per-position checks, so that the independent
+    // work of neighbouring positions can interleave; then the sequence's last few
+    int pb = t0;
+    for (; pb + B <= t1; pb += B) {
+        float xs[B][E];
+#pragma unroll
+        for (int j = 0; j < B; ++j) load_vec<E>(xs[j], x_ptr + static_cast<size_t>(pb + j) * conv_dim);
+#pragma unroll
+        for (int j = 0; j < B; ++j) position(xs[j], pb + j);
+    }
+    if (pb < t1) {
+        float xs[B][E];
 #pragma unroll
         for (int j = 0; j < B; ++j) {
-            const int p = pb + j;
-            if (p >= t1) break;
-            const float x = xs[j];
-            float pre = __fmul_rn(x, wc[K - 1]);
+            if (pb + j < t1) {
+                load_vec<E>(xs[j], x_ptr + static_cast<size_t>(pb + j) * conv_dim);
+            } else {
 #pragma unroll
-            for (int t = 0; t < TAPS; ++t) pre = __fmaf_rn(hist[t], wc[t], pre);
-            const float o = silu(pre);
-            if (is_qk) tile[(p - t0) * ROW + c] = o;
-            else v_out[static_cast<size_t>(p) * H * S] = o;
-#pragma unroll
-            for (int t = 0; t + 1 < TAPS; ++t) hist[t] = hist[t + 1];
-            hist[TAPS - 1] = x;
-        }
-    }
-    if (t0 == 0) {  // the new state: the last K-1 inputs of (old state, this call's inputs)
-        for (int p = max(0, n_tokens - TAPS); p < n_tokens; ++p) {
-#pragma unroll
-            for (int t = 0; t + 1 < TAPS; ++t) old[t] = old[t + 1];
-            old[TAPS - 1] = x_ptr[static_cast<size_t>(p) * conv_dim];
+                for (int e = 0; e < E; ++e) xs[j][e] = 0.0f;
+            }
         }
 #pragma unroll
-        for (int t = 0; t < TAPS; ++t) hs[t] = old[t];
+        for (int j = 0; j < B; ++j) {
+            if (pb + j >= t1) break;  // uniform over the warp
+            position(xs[j], pb + j);
+        }
     }
-    if (!is_qk) return;  // uniform over the CTA
-    __syncthreads();
-    const int warp = c >> 5, lane = c & 31;
-    float *dst0 = (sl < Hk ? q : k) + (seq0 * Hk + (sl % Hk)) * S + lane * E;
-    for (int r = warp; r < t1 - t0; r += S / 32) {
-        float xv[E];
-        load_vec<E>(xv, tile + r * ROW + lane * E);
-        float ss = 0.0f;
+    if (t0 == 0) {
+        // the new state: the last K-1 inputs of (old state, this call's inputs); entry t
+        // is input n_tokens - TAPS + t, or old entry n_tokens + t where that is negative
+        // (the old state is read before this lane rewrites it; no other thread touches it)
+        float nw[TAPS][E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) ss = __fmaf_rn(xv[e], xv[e], ss);
-        ss = warp_allsum(ss);
-        const float inv = 1.0f / fmaxf(sqrtf(ss), eps);
+        for (int t = 0; t < TAPS; ++t) {
+            const int pos = n_tokens - TAPS + t;
+            if (pos >= 0) {
+                load_vec<E>(nw[t], x_ptr + static_cast<size_t>(pos) * conv_dim);
+            } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) xv[e] *= inv;
-        store_vec<E>(dst0 + static_cast<size_t>(t0 + r) * Hk * S, xv);
+                for (int e = 0; e < E; ++e) nw[t][e] = hs[e * TAPS + pos + TAPS];
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TAPS; ++t)
+#pragma unroll
+            for (int e = 0; e < E; ++e) hs[e * TAPS + t] = nw[t][e];
     }
 }
 
@@ -164,15 +205,16 @@ gdn_status launch_conv_split_norm_k(const float *qkv, const float *w, float *con
                                     float eps, const int32_t *slots, int pool, int32_t *err_count,
                                     cudaStream_t s) {
     constexpr int P = conv_norm_positions<E>();
+    const unsigned groups = (2 * Hk + H + kConvNormWarps - 1) / kConvNormWarps;
     if (seqs.cu == nullptr) {
-        const dim3 grid(2 * Hk + H, (seqs.n_tokens + P - 1) / P, n_seqs);
-        conv_split_norm_kernel<E, K, false><<<grid, 32 * E, 0, s>>>(
+        const dim3 grid(groups, (seqs.n_tokens + P - 1) / P, n_seqs);
+        conv_split_norm_kernel<E, K, false><<<grid, 32 * kConvNormWarps, 0, s>>>(
             qkv, w, conv_state, q, k, v, seqs, n_seqs, Hk, H, eps, slots, pool, err_count);
     } else {
         const long long block_slots = seqs.total / P + n_seqs;
         if (block_slots > 65535) return GDN_ERR_UNSUPPORTED;
-        const dim3 grid(2 * Hk + H, static_cast<unsigned>(block_slots), 1);
-        conv_split_norm_kernel<E, K, true><<<grid, 32 * E, 0, s>>>(
+        const dim3 grid(groups, static_cast<unsigned>(block_slots), 1);
+        conv_split_norm_kernel<E, K, true><<<grid, 32 * kConvNormWarps, 0, s>>>(
             qkv, w, conv_state, q, k, v, seqs, n_seqs, Hk, H, eps, slots, pool, err_count);
     }
     return launch_status();

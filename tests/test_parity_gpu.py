@@ -129,6 +129,43 @@ def test_conv1d_silu_invalid_slot(lib):
     np.testing.assert_array_equal(host(cs)[[0, 2, 3]], cs0[[0, 2, 3]])
 
 
+# SiLU's argument over its whole range. It covers values near zero, values whose result
+# is x itself, and values below about -88, where exp(-x) overflows and the divisor passes
+# 2^126. The arguments go through the conv (the current tap alone with weight 1, so the
+# pre-activation is the input) and through the gated norm's gate.
+SILU_ARGS = np.array([0.0, -0.0, 1e-30, -1e-30, 1e-3, -1e-3, 0.5, -0.5, 1.0, -1.0, 5.0, -5.0,
+                      10.0, -10.0, 20.0, -20.0, 50.0, -50.0, 87.0, -87.0, 88.5, -88.5, 89.0,
+                      -89.0, 100.0, -100.0, 1000.0, -1000.0, 3e38, -3e38], dtype=np.float32)
+
+
+def test_silu_argument_range(lib):
+    C, T, K = 256, 3, 2
+    qkv = np.stack([np.resize(np.roll(SILU_ARGS, 7 * t), C) for t in range(T)])[None]
+    w = np.tile(np.array([0.0, 1.0], dtype=np.float32), (C, 1))
+    cs0 = np.zeros((1, C, K - 1), dtype=np.float32)
+    out = torch.zeros(1, T, C, device="cuda")
+    lib.gdn_conv1d_silu_seq(dev(qkv), dev(w), dev(cs0), out, 1, T, C, K)
+    ref, _ = oracle.conv1d_silu_seq(qkv, w, f64(cs0))
+    got = host(out)
+    assert_step(got, ref, "silu through the conv")
+    assert np.all(np.abs(got[qkv <= -100.0]) <= 1e-30)
+    # the fast exponential and division stay within 1e-5 relative where |x| <= 20 (the
+    # range a conv output takes): far inside the one-step bound
+    mid = np.abs(qkv) <= 20.0
+    assert np.all(np.abs(got[mid] - ref[mid]) <= 1e-5 * np.abs(ref[mid]) + 1e-37)
+
+    # the gate's arguments up to 1000 in magnitude: with z = 3e38 the gated output
+    # y w silu(z) / rms is beyond fp32's range whatever SiLU returns
+    D, rows = 128, 8
+    zargs = SILU_ARGS[np.abs(SILU_ARGS) <= 1000.0]
+    z = np.stack([np.resize(np.roll(zargs, 3 * i), D) for i in range(rows)])
+    y = np.random.default_rng(105).normal(0, 1, (rows, D)).astype(np.float32)
+    nw = np.ones(D, dtype=np.float32)
+    o = torch.empty(rows, D, device="cuda")
+    lib.gdn_gated_norm(dev(y), dev(nw), dev(z), o, rows, D, 1e-6)
+    assert_step(host(o), oracle.gated_norm(y, nw, z, 1e-6), "silu through the gated norm")
+
+
 @pytest.mark.parametrize("Hk,H,S", [(2, 4, 32), (16, 32, 128), (1, 2, 64), (2, 4, 256)])
 def test_qkv_split_norm(lib, Hk, H, S):
     r = np.random.default_rng(103)
