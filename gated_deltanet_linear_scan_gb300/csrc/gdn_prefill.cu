@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(32 * kConvNormWarps) conv_split_norm_kernel(
     int n_seqs, int n_k_heads, int n_v_heads, float eps, const int32_t *__restrict__ slots,
     int pool, int32_t *err_count) {
     constexpr int S = 32 * E, TAPS = K - 1, P = conv_norm_positions<E>();
-    constexpr int B = E >= 8 ? 4 : 8;  // positions loaded ahead of their use
+    constexpr int B = E >= 8 ? 2 : 4;  // positions a load group holds
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hk = n_k_heads, H = n_v_heads;
     int n, t0;
@@ -151,14 +151,32 @@ __global__ void __launch_bounds__(32 * kConvNormWarps) conv_split_norm_kernel(
         for (int e = 0; e < E; ++e) hist[TAPS - 1][e] = x[e];
     };
     // whole groups of B positions without per-position checks, so that the independent
-    // work of neighbouring positions can interleave; then the sequence's last few
+    // work of neighbouring positions can interleave, with the next group's loads issued
+    // before the current group's work (two register buffers in turn); then the
+    // sequence's last few positions
     int pb = t0;
-    for (; pb + B <= t1; pb += B) {
-        float xs[B][E];
+    {
+        float xa[B][E], xb[B][E];
+        auto load_group = [&](float (&xg)[B][E], int p0) {
 #pragma unroll
-        for (int j = 0; j < B; ++j) load_vec<E>(xs[j], x_ptr + static_cast<size_t>(pb + j) * conv_dim);
+            for (int j = 0; j < B; ++j) load_vec<E>(xg[j], x_ptr + static_cast<size_t>(p0 + j) * conv_dim);
+        };
+        bool have = pb + B <= t1;  // uniform over the warp, as every condition below
+        if (have) load_group(xa, pb);
+        while (have) {
+            const bool next_b = pb + 2 * B <= t1;
+            if (next_b) load_group(xb, pb + B);
 #pragma unroll
-        for (int j = 0; j < B; ++j) position(xs[j], pb + j);
+            for (int j = 0; j < B; ++j) position(xa[j], pb + j);
+            pb += B;
+            if (!next_b) break;
+            const bool next_a = pb + 2 * B <= t1;
+            if (next_a) load_group(xa, pb + B);
+#pragma unroll
+            for (int j = 0; j < B; ++j) position(xb[j], pb + j);
+            pb += B;
+            have = next_a;
+        }
     }
     if (pb < t1) {
         float xs[B][E];
