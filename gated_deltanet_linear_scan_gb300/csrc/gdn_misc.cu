@@ -39,23 +39,25 @@ __global__ void __launch_bounds__(kThreads) sigmoid_kernel(const float *__restri
 // depthwise conv1d + SiLU" and its scan form. The history holds RAW inputs, so the
 // window of position p is just inputs p-K+1 .. p (the old conv_state standing in
 // for p < 0): positions are independent, and the scan runs in blocks of
-// kConvTokens positions, one thread per (sequence, channel, block), each carrying
-// its K-1 taps in registers across its block. The block of position 0 alone reads
-// the old conv_state and writes the new one (the last K-1 raw inputs), so the
-// in-place update cannot race. The accumulation is the current tap first, then the
-// history oldest-first; every position is computed with the same operations as a
-// single-token call, so a scan and n single-token calls agree bit for bit.
+// kConvTokens positions, one thread per (sequence, V consecutive channels, block),
+// each carrying its K-1 taps in registers across its block. V = 4 where the channel
+// count and the qkv and out pointers allow 16-byte accesses, else 1. The block of
+// position 0 alone reads the old conv_state and writes the new one (the last K-1 raw
+// inputs), so the in-place update cannot race. The accumulation is the current tap
+// first, then the history oldest-first, per channel whatever V is; every position is
+// computed with the same operations as a single-token call, so a scan and n
+// single-token calls agree bit for bit.
 constexpr int kConvTokens = 64;
 static_assert(kConvTokens >= 8, "a block's history must reach back no further than position 0");
 
-template <int K, bool SNAP>
+template <int K, bool SNAP, int V>
 __global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
     const float *__restrict__ qkv, const float *__restrict__ w, float *conv_state,
     float *__restrict__ out, int n_tokens, int conv_dim, const int32_t *__restrict__ slots,
     int pool, int32_t *err_count, float *__restrict__ snaps) {
-    constexpr int TAPS = K - 1;
+    constexpr int TAPS = K - 1, B = 16 / V;  // B: positions a load group holds
     const int n = blockIdx.y;
-    const int c = blockIdx.x * kThreads + threadIdx.x;
+    const int c0 = (blockIdx.x * kThreads + threadIdx.x) * V;  // this thread's first channel
     const int t0 = blockIdx.z * kConvTokens;
     const int t1 = min(n_tokens, t0 + kConvTokens);
     const int slot = slots ? slots[n] : n;
@@ -64,57 +66,115 @@ __global__ void __launch_bounds__(kThreads) conv1d_silu_kernel(
             atomicAdd(err_count, 1);
         return;
     }
-    if (c >= conv_dim) return;
-    float wc[K];
+    if (c0 >= conv_dim) return;  // V divides conv_dim
+    float wc[K][V];
 #pragma unroll
-    for (int t = 0; t < K; ++t) wc[t] = w[static_cast<size_t>(c) * K + t];
-    float *hs = conv_state + (static_cast<size_t>(slot) * conv_dim + c) * TAPS;
-    const float *x_ptr = qkv + static_cast<size_t>(n) * n_tokens * conv_dim + c;
-    float *o_ptr = out + static_cast<size_t>(n) * n_tokens * conv_dim + c;
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+        for (int t = 0; t < K; ++t) wc[t][v] = w[static_cast<size_t>(c0 + v) * K + t];
+    // the thread's channels' histories, channel-major: hs[v * TAPS + t]
+    float *hs = conv_state + (static_cast<size_t>(slot) * conv_dim + c0) * TAPS;
+    const float *x_ptr = qkv + static_cast<size_t>(n) * n_tokens * conv_dim + c0;
+    float *o_ptr = out + static_cast<size_t>(n) * n_tokens * conv_dim + c0;
     // inputs at positions t0-K+1 .. t0-1 (the old state for negative positions)
-    float old[TAPS], hist[TAPS];
-    if (t0 == 0) {
-#pragma unroll
-        for (int t = 0; t < TAPS; ++t) old[t] = hs[t];
-    }
+    float hist[TAPS][V];
 #pragma unroll
     for (int t = 0; t < TAPS; ++t) {
         const int pos = t0 - TAPS + t;
-        hist[t] = pos >= 0 ? x_ptr[static_cast<size_t>(pos) * conv_dim] : old[t];  // t0 == 0
-    }
-    constexpr int B = 16;  // inputs loaded ahead of their use: memory-level parallelism
-    for (int pb = t0; pb < t1; pb += B) {
-        float xs[B];
+        if (pos >= 0) {
+            load_vec<V>(hist[t], x_ptr + static_cast<size_t>(pos) * conv_dim);
+        } else {  // t0 == 0
 #pragma unroll
-        for (int j = 0; j < B; ++j)
-            xs[j] = pb + j < t1 ? x_ptr[static_cast<size_t>(pb + j) * conv_dim] : 0.0f;
+            for (int v = 0; v < V; ++v) hist[t][v] = hs[v * TAPS + t];
+        }
+    }
+    auto position = [&](const float (&x)[V], int p) {
+        float o[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float pre = __fmul_rn(x[v], wc[K - 1][v]);
+#pragma unroll
+            for (int t = 0; t < TAPS; ++t) pre = __fmaf_rn(hist[t][v], wc[t][v], pre);
+            o[v] = silu(pre);
+        }
+        store_vec<V>(o_ptr + static_cast<size_t>(p) * conv_dim, o);
+#pragma unroll
+        for (int t = 0; t + 1 < TAPS; ++t)
+#pragma unroll
+            for (int v = 0; v < V; ++v) hist[t][v] = hist[t + 1][v];
+#pragma unroll
+        for (int v = 0; v < V; ++v) hist[TAPS - 1][v] = x[v];
+        if constexpr (SNAP) {  // the history after token p: snaps[n][p][C][K-1]
+            float *sn = snaps + ((static_cast<size_t>(n) * n_tokens + p) * conv_dim + c0) * TAPS;
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+#pragma unroll
+                for (int t = 0; t < TAPS; ++t) sn[v * TAPS + t] = hist[t][v];
+        }
+    };
+    // whole groups of B positions without per-position checks, the next group's loads
+    // issued before the current group's work (two register buffers in turn); then the
+    // block's last few positions
+    int pb = t0;
+    {
+        float xa[B][V], xb[B][V];
+        auto load_group = [&](float (&xg)[B][V], int p0) {
+#pragma unroll
+            for (int j = 0; j < B; ++j) load_vec<V>(xg[j], x_ptr + static_cast<size_t>(p0 + j) * conv_dim);
+        };
+        bool have = pb + B <= t1;
+        if (have) load_group(xa, pb);
+        while (have) {
+            const bool next_b = pb + 2 * B <= t1;
+            if (next_b) load_group(xb, pb + B);
+#pragma unroll
+            for (int j = 0; j < B; ++j) position(xa[j], pb + j);
+            pb += B;
+            if (!next_b) break;
+            const bool next_a = pb + 2 * B <= t1;
+            if (next_a) load_group(xa, pb + B);
+#pragma unroll
+            for (int j = 0; j < B; ++j) position(xb[j], pb + j);
+            pb += B;
+            have = next_a;
+        }
+    }
+    if (pb < t1) {
+        float xs[B][V];
 #pragma unroll
         for (int j = 0; j < B; ++j) {
-            const int p = pb + j;
-            if (p >= t1) break;
-            const float x = xs[j];
-            float pre = __fmul_rn(x, wc[K - 1]);
+            if (pb + j < t1) {
+                load_vec<V>(xs[j], x_ptr + static_cast<size_t>(pb + j) * conv_dim);
+            } else {
 #pragma unroll
-            for (int t = 0; t < TAPS; ++t) pre = __fmaf_rn(hist[t], wc[t], pre);
-            o_ptr[static_cast<size_t>(p) * conv_dim] = silu(pre);
-#pragma unroll
-            for (int t = 0; t + 1 < TAPS; ++t) hist[t] = hist[t + 1];
-            hist[TAPS - 1] = x;
-            if constexpr (SNAP) {  // the history after token p: snaps[n][p][C][K-1]
-                float *sn = snaps + ((static_cast<size_t>(n) * n_tokens + p) * conv_dim + c) * TAPS;
-#pragma unroll
-                for (int t = 0; t < TAPS; ++t) sn[t] = hist[t];
+                for (int v = 0; v < V; ++v) xs[j][v] = 0.0f;
             }
         }
-    }
-    if (t0 == 0) {  // the new state: the last K-1 inputs of (old state, this call's inputs)
-        for (int p = max(0, n_tokens - TAPS); p < n_tokens; ++p) {
 #pragma unroll
-            for (int t = 0; t + 1 < TAPS; ++t) old[t] = old[t + 1];
-            old[TAPS - 1] = x_ptr[static_cast<size_t>(p) * conv_dim];
+        for (int j = 0; j < B; ++j) {
+            if (pb + j >= t1) break;
+            position(xs[j], pb + j);
+        }
+    }
+    if (t0 == 0) {
+        // the new state: the last K-1 inputs of (old state, this call's inputs); entry t
+        // is input n_tokens - TAPS + t, or old entry n_tokens + t where that is negative
+        // (the old state is read before this thread rewrites it; no other thread touches it)
+        float nw[TAPS][V];
+#pragma unroll
+        for (int t = 0; t < TAPS; ++t) {
+            const int pos = n_tokens - TAPS + t;
+            if (pos >= 0) {
+                load_vec<V>(nw[t], x_ptr + static_cast<size_t>(pos) * conv_dim);
+            } else {
+#pragma unroll
+                for (int v = 0; v < V; ++v) nw[t][v] = hs[v * TAPS + pos + TAPS];
+            }
         }
 #pragma unroll
-        for (int t = 0; t < TAPS; ++t) hs[t] = old[t];
+        for (int t = 0; t < TAPS; ++t)
+#pragma unroll
+            for (int v = 0; v < V; ++v) hs[v * TAPS + t] = nw[t][v];
     }
 }
 
@@ -204,14 +264,26 @@ template <int K>
 gdn_status launch_conv(const float *qkv, const float *w, float *conv_state, float *out,
                        int n_seqs, int n_tokens, int conv_dim, const int32_t *slots, int pool,
                        int32_t *err_count, float *snaps, cudaStream_t s) {
-    const dim3 grid((conv_dim + kThreads - 1) / kThreads, n_seqs,
+    // four channels a thread where the channel rows allow 16-byte accesses
+    const bool wide = conv_dim % 4 == 0 && aligned16(qkv) && aligned16(out);
+    const int per = wide ? 4 : 1;
+    const dim3 grid((conv_dim / per + kThreads - 1) / kThreads, n_seqs,
                     (n_tokens + kConvTokens - 1) / kConvTokens);
-    if (snaps)
-        conv1d_silu_kernel<K, true><<<grid, kThreads, 0, s>>>(qkv, w, conv_state, out, n_tokens,
-                                                              conv_dim, slots, pool, err_count, snaps);
-    else
-        conv1d_silu_kernel<K, false><<<grid, kThreads, 0, s>>>(qkv, w, conv_state, out, n_tokens,
-                                                               conv_dim, slots, pool, err_count, nullptr);
+    if (wide) {
+        if (snaps)
+            conv1d_silu_kernel<K, true, 4><<<grid, kThreads, 0, s>>>(
+                qkv, w, conv_state, out, n_tokens, conv_dim, slots, pool, err_count, snaps);
+        else
+            conv1d_silu_kernel<K, false, 4><<<grid, kThreads, 0, s>>>(
+                qkv, w, conv_state, out, n_tokens, conv_dim, slots, pool, err_count, nullptr);
+    } else {
+        if (snaps)
+            conv1d_silu_kernel<K, true, 1><<<grid, kThreads, 0, s>>>(
+                qkv, w, conv_state, out, n_tokens, conv_dim, slots, pool, err_count, snaps);
+        else
+            conv1d_silu_kernel<K, false, 1><<<grid, kThreads, 0, s>>>(
+                qkv, w, conv_state, out, n_tokens, conv_dim, slots, pool, err_count, nullptr);
+    }
     return launch_status();
 }
 

@@ -82,7 +82,8 @@ def test_decay_gate_and_beta(lib):
 
 @pytest.mark.parametrize("K", [2, 3, 4, 5, 8])
 # T = 65 and 150 cross the scan's 64-position blocks, with a ragged last block
-@pytest.mark.parametrize("C,T", [(256, 1), (256, 21), (8192, 3), (256, 65), (512, 150)])
+# C = 250 runs the one-channel-a-thread form (a channel count not divisible by 4)
+@pytest.mark.parametrize("C,T", [(256, 1), (256, 21), (8192, 3), (256, 65), (512, 150), (250, 70)])
 def test_conv1d_silu(lib, K, C, T):
     r = np.random.default_rng(101 + K)
     N, P = 3, 5
@@ -109,6 +110,26 @@ def test_conv1d_silu(lib, K, C, T):
         lib.gdn_conv1d_silu(dev(qkv[:, t]), dev(w), cs2, o1, N, C, K, slots=dev(slots), pool=P)
         np.testing.assert_array_equal(host(o1), host(out)[:, t])
     np.testing.assert_array_equal(host(cs2), host(cs))
+
+
+def test_conv1d_silu_channel_grouping_same_bits(lib):
+    """Four channels a thread (16-byte accesses) and one channel a thread (the form for
+    rows that are not 16-byte aligned) give the same bits: the same inputs, and outputs
+    one float past a 16-byte boundary, against the aligned call."""
+    r = np.random.default_rng(106)
+    N, T, C, K = 2, 150, 512, 4
+    qkv = r.normal(0, 1, (N, T, C)).astype(np.float32)
+    w = dev(r.normal(0, 0.5, (C, K)).astype(np.float32))
+    cs0 = r.normal(0, 1, (N, C, K - 1)).astype(np.float32)
+    cs_a, out_a = dev(cs0), torch.zeros(N, T, C, device="cuda")
+    lib.gdn_conv1d_silu_seq(dev(qkv), w, cs_a, out_a, N, T, C, K)
+    qb = torch.zeros(qkv.size + 1, device="cuda")
+    qb[1:] = dev(qkv).reshape(-1)
+    ob = torch.zeros(out_a.numel() + 1, device="cuda")
+    cs_b = dev(cs0)
+    lib.gdn_conv1d_silu_seq(qb[1:].view(N, T, C), w, cs_b, ob[1:].view(N, T, C), N, T, C, K)
+    assert torch.equal(ob[1:].view(N, T, C), out_a)
+    assert torch.equal(cs_b, cs_a)
 
 
 def test_conv1d_silu_invalid_slot(lib):
